@@ -1,0 +1,355 @@
+"""Benchmark of the batched constrained logits sampler.
+
+One step = one sampler call (penalties, bias, grammar mask, temperature, top-k ->
+top-p -> min-p, exponential race, logprob) over one batch of the penalties+bias
+workload: B=192 rows, V=151936, fp32 logits, Zipf histories of 0-4096 ids, 16
+logit_bias entries per row, bitmasks on 25% of rows, mixed parameters.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Inputs are rotated over three resident copies of the
+batch (3 x 122 MB, more than twice the 129 MB L2), so no step reads a batch that the
+previous step left in L2.  Per-launch times come from CUDA events on the launching
+stream; SM clocks are sampled with nvidia-smi during the timed region.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "rows/s & HBM GB/s (% of peak), fused mask+top-k/p sample, B=192 V=151936"
+WORKLOAD = 4
+N_SETS = 3
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", type=int, default=WORKLOAD)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for p in ("constrained_logits_sampling_gb300/csrc/clsample.cu", "include/clsample.h"):
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profile(workload_name):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("kernel_source_sha") != kernel_source_hash() or d.get("workload") != workload_name:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            parts = [x.strip() for x in l.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() in ("active", "1"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(batch, sample_rows, repeats):
+    """The oracle as it stands, on the host cores, on a bounded sample of the batch."""
+    from oracle import oracle as O
+    sub = batch.rows(range(min(sample_rows, batch.B)))
+    O.sample(sub, nthreads=0, want_transformed=False)  # warm-up (page-in, thread start)
+    t0 = time.perf_counter()
+    threads = 1
+    for _ in range(repeats):
+        threads = O.sample(sub, nthreads=0, want_transformed=False)["threads"]
+    dt = time.perf_counter() - t0
+    rows = sub.B * repeats
+    return {"value": rows / dt, "unit": "rows/s", "cores": int(threads), "kind": "oracle",
+            "sample": f"{sub.B} rows of workload {batch.name} (B={batch.B}, V={batch.V}) x {repeats} repeats, "
+                      f"{dt:.2f} s wall on {threads} threads"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    from constrained_logits_sampling_gb300.workloads import make_workload
+    from oracle import oracle as O
+    O.build()
+    b = make_workload(args.workload)
+    sample_rows = 32
+    sub = b.rows(range(sample_rows))
+    for _ in range(max(args.warmup, 0)):
+        O.sample(sub, nthreads=0)
+    t0 = time.perf_counter()
+    threads = 1
+    for _ in range(args.steps):
+        threads = O.sample(sub, nthreads=0)["threads"]
+    dt = time.perf_counter() - t0
+    value = sample_rows * args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32+f64",
+        "data": "synthetic",
+        "config": {"workload": f"{b.name}: B={b.B} V={b.V} fp32 logits, penalties+bias, 25% bitmasked rows",
+                   "sample_rows_per_step": sample_rows},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": int(threads), "kind": "oracle",
+                         "sample": f"{sample_rows} rows of {b.name} per step, {args.steps} steps"},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import numpy as np
+    import torch
+
+    from constrained_logits_sampling_gb300 import build as cuda_build
+    from constrained_logits_sampling_gb300.sampler import Sampler, batch_to_device
+    from constrained_logits_sampling_gb300.workloads import make_workload
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    cuda_build.build()
+    dev = torch.device("cuda", local)
+    b = make_workload(args.workload)
+    s = Sampler(b.B, b.V)
+    sets = []
+    for i in range(N_SETS):
+        kw = batch_to_device(b, dev)
+        logits = kw.pop("logits")
+        out = {"tokens": torch.empty(b.B, dtype=torch.int32, device=dev),
+               "logprobs": torch.empty(b.B, dtype=torch.float32, device=dev)}
+        sets.append((s.make_args(logits, tokens=out["tokens"], logprobs=out["logprobs"], **kw), kw, logits, out))
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for i in range(args.warmup):
+        s.apply(sets[i % N_SETS][0], stream)
+    barrier()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    t_all0 = torch.cuda.Event(enable_timing=True)
+    t_all1 = torch.cuda.Event(enable_timing=True)
+    t_all0.record(stream)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        s.apply(sets[i % N_SETS][0], stream)
+        ends[i].record(stream)
+    t_all1.record(stream)
+    barrier()
+    # keep the GPU busy while the clock sampler catches up on a long-enough window
+    extra = 0
+    t_end = time.perf_counter() + 1.0
+    while time.perf_counter() < t_end:
+        s.apply(sets[extra % N_SETS][0], stream)
+        extra += 1
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    launch_ms = [a.elapsed_time(e) for a, e in zip(starts, ends)]
+    total_ms = t_all0.elapsed_time(t_all1)
+    mean_launch_ms = sum(launch_ms) / len(launch_ms)
+    if dist is not None:
+        t = torch.tensor([total_ms, mean_launch_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, mean_launch_ms = float(t[0]), float(t[1])
+    ms_per_step = total_ms / args.steps
+    value = b.B * world * args.steps / (total_ms / 1e3)
+
+    # ---- end to end through the public API: host inputs -> device -> sampler -> host
+    e2e = None
+    if not args.no_e2e:
+        host = {}
+        kw0 = batch_to_device(b, "cpu")
+        for k, v in kw0.items():
+            if isinstance(v, torch.Tensor):
+                host[k] = v.pin_memory()
+            else:
+                host[k] = v
+        h2d = sum(v.numel() * v.element_size() for v in host.values() if isinstance(v, torch.Tensor))
+        out_host = {"tokens": torch.empty(b.B, dtype=torch.int32).pin_memory(),
+                    "logprobs": torch.empty(b.B, dtype=torch.float32).pin_memory()}
+        d2h = sum(v.numel() * v.element_size() for v in out_host.values())
+        e2e_steps = max(10, min(args.steps, 50))
+
+        def e2e_step():
+            dkw = {k: (v.to(dev, non_blocking=True) if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
+            lg = dkw.pop("logits")
+            out = s(lg, **dkw)
+            out_host["tokens"].copy_(out["tokens"], non_blocking=True)
+            out_host["logprobs"].copy_(out["logprobs"], non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        e_ms = e0.elapsed_time(e1)
+        if dist is not None:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t[0])
+        e2e = {"value": b.B * world * e2e_steps / (e_ms / 1e3), "unit": "rows/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e2e_steps}
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    peak, peak_kind = peaks()
+    alg = b.algorithmic_bytes()
+    achieved = alg / (mean_launch_ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "rows/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": f"{b.name}: B={b.B} V={b.V} fp32 logits, Zipf(1.1) histories 0-4096 ids, "
+                        "16 logit_bias/row, bitmasks on 25% of rows, mixed T/top-k/top-p/min-p, 25% greedy",
+            "rows_per_gpu": b.B,
+            "l2": f"inputs rotated over {N_SETS} resident copies ({N_SETS * alg / 1e6:.0f} MB > 2 x L2)",
+            "parallelism": f"replicas x{world} (rows are independent)",
+        },
+        "hbm_gbs": achieved,
+        "roofline": {
+            "bound": "hbm",
+            "achieved": achieved,
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": achieved / peak,
+            "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
+            "traffic": traffic_from_profile(b.name),
+            "algorithmic_bytes_per_launch": alg,
+            "mean_launch_us": mean_launch_ms * 1e3,
+            "kernel": "sampler_kernel (one launch per step)",
+        },
+        "gpu_launches": args.steps,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(b, sample_rows=b.B, repeats=3)
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,174 @@
+/* clsample.h: C ABI of the GB300 (sm_103a) batched constrained logits sampler.
+ *
+ * One call turns a [B, V] next-token logits matrix into one token id per row, plus the
+ * drawn token's logprob.  For every row it applies, in order:
+ *
+ *   1. sanitising of non-finite logits
+ *        (SGLang source teardown (10): Sampling, Grammar and structured output,
+ *         section "_preprocess_logits");
+ *   2. frequency / presence penalties (additive), then the repetition penalty (scaling),
+ *      then sparse logit_bias (a repeated id keeps its last value)
+ *        (same page, sections "Order semantics of the penalties" and "Why logit_bias is
+ *         built from triples");
+ *   3. the int32 grammar bitmask: bit (i & 31) of word i >> 5 equal to 0 sets logit i to
+ *      -inf, before any truncation
+ *        (same page, section "Bitmask: one int32 covers 32 tokens");
+ *   4. the greedy rule: temperature < 1e-5 (GLM-5.3 inference (7): output side, section
+ *      "Sampling") or top_k in {0, 1} (SGLang page, section "Field groups");
+ *   5. temperature, then top-k -> top-p -> min-p truncation on the tempered distribution
+ *        (SGLang page, section "The maths of the three cuts": S_k, S_p, S_m);
+ *   6. an exponential race keyed by (seed, position): token = argmax_i p_i / E_i over the
+ *      kept set, E_i = -ln U_i with U_i from Philox4x32-10 (Salmon et al., SC'11) at
+ *      counter (i / 4, position, 0) and key seed, so a request's draw does not depend on
+ *      the batch it is in (SGLang page, section "Call site"; GLM-5.3 page: one random
+ *      stream per request);
+ *   7. the logprob of the drawn token under the full tempered distribution, computed as
+ *      log-softmax (SGLang page, section "Numerical consistency of logprobs").
+ *
+ * Threading and ownership.  A handle is bound to the CUDA device that was current at
+ * clsample_create and holds no device memory.  Every array in clsample_args_t is a
+ * DEVICE pointer owned by the caller; it must stay valid until the work enqueued on
+ * the stream has finished.  The logits are read-only (never written in place).  Calls
+ * on one handle from several host threads are safe; calls on different streams may
+ * overlap freely (the kernels keep no state between calls).
+ *
+ * Errors.  Every entry point validates its arguments on the host, without any device
+ * synchronisation, and returns a negative CLSAMPLE_ERR_* code on a bad argument;
+ * nothing is enqueued then.  Data errors found on the device (ids outside [0, V),
+ * decreasing CSR offsets, NaN parameters, a row with no allowed token) never trap:
+ * they go to the per-row status (OK < OVERFLOW < INVALID, ordered by severity so that
+ * a MAX reduction over rows gives one verdict; SGLang page, section
+ * "LogitsProcessorOutput"), and such a row gets token -1 and logprob -inf.
+ */
+#ifndef CLSAMPLE_H
+#define CLSAMPLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* clsample_stream_t;
+typedef struct clsample_handle clsample_t;
+
+enum {
+  CLSAMPLE_LOGITS_F32 = 0,  /* float32 logits */
+  CLSAMPLE_LOGITS_BF16 = 1  /* bfloat16 logits, widened exactly to float32 */
+};
+
+/* Per-row status codes written to row_status. */
+enum { CLSAMPLE_ROW_OK = 0, CLSAMPLE_ROW_OVERFLOW = 1, CLSAMPLE_ROW_INVALID = 2 };
+
+/* Return codes. */
+enum {
+  CLSAMPLE_SUCCESS = 0,
+  CLSAMPLE_ERR_NULL = -1,       /* a required pointer is NULL */
+  CLSAMPLE_ERR_BATCH = -2,      /* B < 0 or B > max_batch */
+  CLSAMPLE_ERR_VOCAB = -3,      /* V <= 0, V != the handle's vocab, or vocab too large */
+  CLSAMPLE_ERR_STRIDE = -4,     /* logits_row_stride < V or bitmask_row_stride < ceil(V/32) */
+  CLSAMPLE_ERR_DTYPE = -5,      /* logits_dtype is not a CLSAMPLE_LOGITS_* value */
+  CLSAMPLE_ERR_CUDA = -6,       /* a CUDA runtime call failed (launch, attribute, device) */
+  CLSAMPLE_ERR_DEVICE = -7      /* the current device is not the handle's or not sm_103 */
+};
+
+/* Arguments of one sampler call.  B rows, V vocabulary entries.
+ *
+ * logits            [B, logits_row_stride] elements of logits_dtype, row-major.
+ * temperatures      f32[B]; NULL = 1.0.  T < 1e-5 (including 0 and negatives) is greedy;
+ *                   NaN or +inf is INVALID.
+ * top_ks            i32[B]; NULL = -1.  -1 (or >= the number of allowed tokens) keeps the
+ *                   whole vocabulary; 0 and 1 are greedy; < -1 is INVALID.  Every token
+ *                   tied with the k-th largest probability is kept.
+ * top_ps            f32[B]; NULL = 1.0.  Must lie in (0, 1], else INVALID.
+ * min_ps            f32[B]; NULL = 0.0.  Must lie in [0, 1], else INVALID.
+ * rep, freq, pres   f32[B] each, NULL = 1.0 / 0.0 / 0.0.  For a token seen c > 0 times in
+ *                   the row's history: z -= freq*c; z -= pres; then z = z > 0 ? z/rep :
+ *                   z*rep.  rep must be finite and > 0, freq and pres finite.
+ * hist_offs/ids     CSR of the rows' token histories: ids hist_ids[hist_offs[r] ..
+ *                   hist_offs[r+1]), duplicates counted.  NULL offs = no penalties.
+ * bias_offs/ids/vals CSR of logit_bias entries; z += val; for a repeated id the LAST
+ *                   entry of the row wins.  NULL offs = no bias.  NaN values are INVALID.
+ * bitmask           i32[B, bitmask_row_stride] words, bit i & 31 of word i >> 5 allows
+ *                   token i; NULL = unconstrained.  A row of all -1 words is unconstrained.
+ * seeds             u64[B]; NULL = 0 for every row.  The request's random key.
+ * positions         i64[B]; NULL = `step` for every row.  The request's token position;
+ *                   rows of one request at different positions draw independently.
+ * tokens            i32[B] output (required).
+ * logprobs          f32[B] output or NULL: ln p(token) under softmax(z'/T_eff) over all
+ *                   allowed tokens (T_eff = 1 for rows with T < 1e-5).
+ * row_status        i32[B] output or NULL.
+ * dbg_transformed   f32[B, V] output or NULL: the transformed logits z' (after penalties,
+ *                   bias and mask), row-major with row stride V.
+ * dbg_kept_count    i32[B] output or NULL: size of the kept set K (1 for greedy rows).
+ * dbg_cut           f32[B] output or NULL: min over K of y = (z' - max z') * (1/T).
+ *
+ * Limits: per row, at most 1024 distinct penalised or biased ids may fall inside one
+ * vocabulary slice of ceil(V / cluster) tokens (cluster = 8 for V > 14336); a row that
+ * exceeds it gets status OVERFLOW.  Histories of up to 4096 ids never exceed it.
+ */
+typedef struct {
+  int32_t B, V;
+  int32_t logits_dtype;
+  int32_t reserved0;
+  const void* logits;
+  int64_t logits_row_stride;
+  const float* temperatures;
+  const int32_t* top_ks;
+  const float* top_ps;
+  const float* min_ps;
+  const float* rep;
+  const float* freq;
+  const float* pres;
+  const int32_t* hist_offs;
+  const int32_t* hist_ids;
+  const int32_t* bias_offs;
+  const int32_t* bias_ids;
+  const float* bias_vals;
+  const int32_t* bitmask;
+  int64_t bitmask_row_stride;
+  const uint64_t* seeds;
+  const int64_t* positions;
+  int64_t step;
+  int32_t* tokens;
+  float* logprobs;
+  int32_t* row_status;
+  float* dbg_transformed;
+  int32_t* dbg_kept_count;
+  float* dbg_cut;
+} clsample_args_t;
+
+/* Creates a handle for batches of up to max_batch rows over a vocabulary of `vocab`
+ * tokens on the current CUDA device.  Sets the kernels' shared-memory and cluster
+ * attributes; allocates no device memory.  Returns CLSAMPLE_SUCCESS and *out, or a
+ * negative code (*out = NULL). */
+int clsample_create(int32_t max_batch, int32_t vocab, clsample_t** out);
+
+/* Releases a handle (NULL is ignored).  Does not synchronise. */
+void clsample_destroy(clsample_t* handle);
+
+/* Enqueues one sampler call on `stream` (one kernel launch; nothing when B == 0).
+ * Returns after enqueueing; results are valid once the stream reaches this point. */
+int clsample_apply(clsample_t* handle, const clsample_args_t* args, clsample_stream_t stream);
+
+/* Static description of a return code. */
+const char* clsample_strerror(int code);
+
+/* Launch geometry chosen for a vocabulary size: CTAs per row (one thread-block
+ * cluster per row), tokens per CTA and dynamic shared memory per CTA.  Host-only;
+ * needs no GPU.  Returns CLSAMPLE_SUCCESS or CLSAMPLE_ERR_VOCAB. */
+int clsample_geometry(int32_t vocab, int32_t* cluster, int32_t* chunk, int32_t* smem_bytes);
+
+/* Diagnostics of the building blocks, on device arrays of length n (enqueued on
+ * `stream`): the fixed-point top-p weight floor(exp32(y) * 2^40) of each y (y <= 0),
+ * and the race uniform U of (seed, position, token).  They run the same device code
+ * as clsample_apply, so tests can compare them with an independent implementation. */
+int clsample_debug_weights(const float* y, uint64_t* weights, int32_t n, clsample_stream_t stream);
+int clsample_debug_uniforms(const uint64_t* seeds, const int64_t* positions, const int64_t* tokens,
+                            float* u, int32_t n, clsample_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CLSAMPLE_H */

@@ -179,13 +179,14 @@ static float sanitize(float v) {
 }
 
 static void write_row(const cls_oracle_args* a, int r, int status, int token, double lp, int kept,
-                      float cut, float gap) {
+                      float cut, float gap, float best) {
   a->tokens[r] = token;
   if (a->logprobs) a->logprobs[r] = lp;
   if (a->status) a->status[r] = status;
   if (a->kept_count) a->kept_count[r] = kept;
   if (a->cut) a->cut[r] = cut;
   if (a->race_gap) a->race_gap[r] = gap;
+  if (a->race_best) a->race_best[r] = best;
 }
 
 static void sample_row(const cls_oracle_args* a, int r, row_scratch* s) {
@@ -279,7 +280,7 @@ static void sample_row(const cls_oracle_args* a, int r, row_scratch* s) {
   if (a->transformed) memcpy(a->transformed + (int64_t)r * V, s->z, sizeof(float) * (size_t)V);
 
   if (status != ORACLE_OK) {
-    write_row(a, r, status, -1, -INFINITY, 0, -INFINITY, INFINITY);
+    write_row(a, r, status, -1, -INFINITY, 0, -INFINITY, INFINITY, -INFINITY);
     return;
   }
 
@@ -297,7 +298,7 @@ static void sample_row(const cls_oracle_args* a, int r, row_scratch* s) {
     }
   }
   if (n_cand == 0) {
-    write_row(a, r, ORACLE_INVALID, -1, -INFINITY, 0, -INFINITY, INFINITY);
+    write_row(a, r, ORACLE_INVALID, -1, -INFINITY, 0, -INFINITY, INFINITY, -INFINITY);
     return;
   }
 
@@ -316,7 +317,7 @@ static void sample_row(const cls_oracle_args* a, int r, row_scratch* s) {
   }
   double logS = log(S);
   if (greedy) {
-    write_row(a, r, ORACLE_OK, arg, (double)s->y[arg] - logS, 1, s->y[arg], INFINITY);
+    write_row(a, r, ORACLE_OK, arg, (double)s->y[arg] - logS, 1, s->y[arg], INFINITY, -INFINITY);
     return;
   }
 
@@ -396,7 +397,7 @@ static void sample_row(const cls_oracle_args* a, int r, row_scratch* s) {
   }
   /* 9. logprob of the drawn token under the full (pre-truncation) distribution at T */
   write_row(a, r, ORACLE_OK, tok, (double)s->y[tok] - logS, kept, cut,
-            kept > 1 ? best - second : INFINITY);
+            kept > 1 ? best - second : INFINITY, best);
 }
 
 /* ------------------------------------------------------------------ batch driver */

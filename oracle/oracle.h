@@ -48,6 +48,7 @@ typedef struct {
   int32_t* kept_count;             /* [B] or NULL */
   float* cut;                      /* [B] or NULL: smallest y in the kept set */
   float* race_gap;                 /* [B] or NULL: best - second race score (+inf if one) */
+  float* race_best;                /* [B] or NULL: best race score (-inf if none) */
   int32_t nthreads;                /* 0 = all online cores */
 } cls_oracle_args;
 

@@ -46,7 +46,7 @@ class _Args(ctypes.Structure):
         ("seeds", ctypes.c_void_p), ("positions", ctypes.c_void_p), ("step", ctypes.c_int64),
         ("tokens", ctypes.c_void_p), ("logprobs", ctypes.c_void_p), ("status", ctypes.c_void_p),
         ("transformed", ctypes.c_void_p), ("kept_count", ctypes.c_void_p), ("cut", ctypes.c_void_p),
-        ("race_gap", ctypes.c_void_p), ("nthreads", ctypes.c_int32),
+        ("race_gap", ctypes.c_void_p), ("race_best", ctypes.c_void_p), ("nthreads", ctypes.c_int32),
     ]
 
 
@@ -82,7 +82,7 @@ def _ptr(a: Optional[np.ndarray], dtype) -> Optional[int]:
 def sample(batch, nthreads: int = 0, want_transformed: bool = False) -> Dict[str, np.ndarray]:
     """Run the oracle on a ``workloads.Batch`` (or any object with the same
     fields).  Returns tokens, logprobs (float64), status, kept_count, cut,
-    race_gap, threads and optionally the transformed logits z'."""
+    race_gap, race_best, threads and optionally the transformed logits z'."""
     L = lib()
     B, V = int(batch.B), int(batch.V)
     logits = np.ascontiguousarray(batch.logits)
@@ -104,6 +104,7 @@ def sample(batch, nthreads: int = 0, want_transformed: bool = False) -> Dict[str
         "tokens": np.zeros(B, np.int32), "logprobs": np.zeros(B, np.float64),
         "status": np.zeros(B, np.int32), "kept_count": np.zeros(B, np.int32),
         "cut": np.zeros(B, np.float32), "race_gap": np.zeros(B, np.float32),
+        "race_best": np.zeros(B, np.float32),
     }
     if want_transformed:
         out["transformed"] = np.zeros((B, V), np.float32)
@@ -127,6 +128,7 @@ def sample(batch, nthreads: int = 0, want_transformed: bool = False) -> Dict[str
     a.kept_count = out["kept_count"].ctypes.data
     a.cut = out["cut"].ctypes.data
     a.race_gap = out["race_gap"].ctypes.data
+    a.race_best = out["race_best"].ctypes.data
     a.transformed = out["transformed"].ctypes.data if want_transformed else None
     a.nthreads = int(nthreads)
     out["threads"] = L.cls_oracle_sample(ctypes.byref(a))

@@ -1,0 +1,237 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the same
+seeded inputs, element by element.  See tests/parity.py for the acceptance bar."""
+import math
+
+import numpy as np
+import pytest
+
+from constrained_logits_sampling_gb300.workloads import Batch, make_workload, round_to_bf16_bits
+
+from parity import compare, run_gpu, run_oracle
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+F32 = np.float32
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from constrained_logits_sampling_gb300 import build
+    build.build()
+
+
+def small(logits, **kw):
+    z = np.ascontiguousarray(np.atleast_2d(np.asarray(logits, dtype=np.float32)))
+    b = Batch(B=z.shape[0], V=z.shape[1], logits=z, logits_bf16=False)
+    for k, v in kw.items():
+        setattr(b, k, v)
+    return b
+
+
+# ----------------------------------------------------------------------------- building blocks
+
+def test_device_weights_bitexact():
+    from constrained_logits_sampling_gb300.sampler import debug_weights
+    from oracle import oracle as O
+    ys = np.concatenate([np.linspace(-33, 0, 30001, dtype=np.float32),
+                         -np.logspace(-9, 1.6, 3001).astype(np.float32), np.array([0.0, -0.0, -np.inf], F32)])
+    g = debug_weights(torch.from_numpy(ys).cuda()).cpu().numpy().view(np.uint64)
+    o = np.array([O.weight_fx(float(y)) for y in ys], dtype=np.uint64)
+    assert np.array_equal(g, o), np.nonzero(g != o)[0][:10]
+
+
+def test_device_uniforms_bitexact():
+    from constrained_logits_sampling_gb300.sampler import debug_uniforms
+    from oracle import oracle as O
+    rng = np.random.default_rng(11)
+    n = 20000
+    seeds = rng.integers(0, 2 ** 63, size=n, dtype=np.int64)
+    pos = rng.integers(0, 2 ** 40, size=n, dtype=np.int64)
+    tok = rng.integers(0, 151936, size=n, dtype=np.int64)
+    g = debug_uniforms(torch.from_numpy(seeds).cuda(), torch.from_numpy(pos).cuda(),
+                       torch.from_numpy(tok).cuda()).cpu().numpy()
+    o = np.array([O.uniform(int(s) & (2 ** 64 - 1), int(p), int(t)) for s, p, t in zip(seeds, pos, tok)], F32)
+    assert np.array_equal(g, o)
+
+
+# ----------------------------------------------------------------------------- workloads
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("V", [5003, 40000])
+def test_parity_reduced(n, V):
+    """Reduced batches over ragged vocabularies (several slices, a ragged tail)."""
+    b = make_workload(n, B={1: 4, 2: 24, 3: 32, 4: 32, 5: 40}[n], V=V)
+    compare(b, run_gpu(b), run_oracle(b), name=f"w{n} V={V}")
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
+def test_parity_full_size(n):
+    """The five workloads at full size, in the launch configuration the benchmark times."""
+    b = make_workload(n)
+    g = run_gpu(b)
+    o = run_oracle(b)
+    stats = compare(b, g, o, name=f"workload {n}")
+    print(f"workload {n}: B={b.B} ambiguous={stats['ambiguous']} max|dlogprob|={stats['max_logprob_err']:.2e}")
+
+
+# ----------------------------------------------------------------------------- edge cases
+
+def test_empty_batch():
+    from constrained_logits_sampling_gb300.sampler import Sampler
+    s = Sampler(4, 1000)
+    out = s(torch.zeros(0, 1000, device="cuda"))
+    torch.cuda.synchronize()
+    assert out["tokens"].numel() == 0
+
+
+@pytest.mark.parametrize("V", [1, 2, 7, 8, 31, 33, 100, 2049, 16385, 100003])
+def test_tiny_and_ragged_vocab(V):
+    rng = np.random.default_rng(V)
+    B = 12
+    z = (rng.standard_normal((B, V)) * 2).astype(F32)
+    b = small(z, temperatures=rng.choice(np.array([0.0, 0.7, 1.3], F32), B),
+              top_ks=rng.choice(np.array([-1, 1, 2, 5], np.int32), B),
+              top_ps=rng.choice(np.array([0.5, 0.9, 1.0], F32), B),
+              min_ps=rng.choice(np.array([0.0, 0.1], F32), B),
+              seeds=np.arange(B, dtype=np.uint64), positions=np.arange(B, dtype=np.int64) * 3)
+    compare(b, run_gpu(b), run_oracle(b), name=f"V={V}")
+
+
+def test_non_finite_and_masked_rows():
+    V = 3000
+    rng = np.random.default_rng(5)
+    z = rng.standard_normal((8, V)).astype(F32)
+    z[0, 10] = np.nan
+    z[1, 20] = np.inf
+    z[2, :] = -np.inf
+    z[3, :] = np.nan  # every token out -> INVALID
+    z[4, 100] = np.inf
+    z[4, 200] = np.inf  # two +inf: lowest id wins
+    bm = np.full((8, (V + 31) // 32), -1, np.int32)
+    bm[5, :] = 0  # nothing allowed -> INVALID
+    bm[6, :] = 0
+    bm[6, 3] = 1 << 7  # exactly one allowed token
+    b = small(z, bitmask=bm, temperatures=np.array([1, 0, 1, 1, 0, 1, 1, 0.5], F32))
+    g, o = run_gpu(b), run_oracle(b)
+    compare(b, g, o, name="non-finite")
+    assert g["status"][3] == 2 and g["status"][5] == 2
+    assert g["tokens"][1] == 20 and g["tokens"][4] == 100 and g["tokens"][6] == 3 * 32 + 7
+
+
+def test_invalid_parameters_and_ids():
+    V = 500
+    z = np.zeros((9, V), F32)
+    b = small(z, temperatures=np.array([np.nan, np.inf, 1, 1, 1, 1, 1, 1, -3], F32),
+              top_ks=np.array([-1, -1, -5, -1, -1, -1, -1, -1, -1], np.int32),
+              top_ps=np.array([1, 1, 1, 1.5, 1, 1, 1, 1, 1], F32),
+              min_ps=np.array([0, 0, 0, 0, -0.1, 0, 0, 0, 0], F32),
+              rep=np.array([1, 1, 1, 1, 1, -1, 1, 1, 1], F32),
+              hist_offs=np.array([0, 0, 0, 0, 0, 0, 0, 1, 1, 1], np.int32), hist_ids=np.array([V], np.int32),
+              bias_offs=np.array([0, 0, 0, 0, 0, 0, 0, 0, 1, 1], np.int32), bias_ids=np.array([3], np.int32),
+              bias_vals=np.array([np.nan], F32))
+    g, o = run_gpu(b), run_oracle(b)
+    compare(b, g, o, name="invalid")
+    assert list(g["status"]) == [2, 2, 2, 2, 2, 2, 2, 2, 0]
+
+
+def test_bf16_equals_widened_fp32():
+    b16 = make_workload(5, B=16, V=7001)
+    g16 = run_gpu(b16)
+    b32 = make_workload(5, B=16, V=7001)
+    b32.logits = (b16.logits.astype(np.uint32) << 16).view(np.float32)
+    b32.logits_bf16 = False
+    g32 = run_gpu(b32)
+    for k in ("tokens", "logprobs", "status", "kept_count", "cut", "transformed"):
+        assert np.array_equal(g16[k], g32[k]), k
+
+
+def test_padded_row_stride_and_unaligned_rows():
+    from constrained_logits_sampling_gb300.sampler import Sampler, batch_to_device
+    b = make_workload(4, B=10, V=3001)
+    o = run_oracle(b)
+    s = Sampler(10, 3001)
+    kw = batch_to_device(b, s.device)
+    logits = kw.pop("logits")
+    for pad in (1, 3, 64):  # stride V+pad: rows lose 16-byte alignment for pad = 1, 3
+        big = torch.full((10, 3001 + pad), float("nan"), device="cuda")
+        big[:, :3001] = logits
+        out = s(big[:, :3001], debug=True, **kw)
+        torch.cuda.synchronize()
+        g = {k: v.cpu().numpy() for k, v in out.items()}
+        compare(b, g, o, name=f"pad {pad}")
+
+
+def test_history_overflow_is_reported():
+    """More distinct penalised ids in one slice than the per-slice table holds: the row
+    reports OVERFLOW instead of sampling from a wrong distribution."""
+    V = 151936
+    z = np.zeros((2, V), F32)
+    hist = np.arange(0, 4000, dtype=np.int32)  # 4000 distinct ids in the first slice
+    b = small(z, hist_offs=np.array([0, 4000, 4001], np.int32),
+              hist_ids=np.concatenate([hist, np.array([5], np.int32)]),
+              freq=np.full(2, 0.1, F32), temperatures=np.zeros(2, F32))
+    g = run_gpu(b, debug=False)
+    assert g["status"][0] == 1 and g["tokens"][0] == -1
+    assert g["status"][1] == 0
+
+
+# ----------------------------------------------------------------------------- laws and invariants
+
+def test_greedy_rules_on_gpu():
+    rng = np.random.default_rng(8)
+    V = 20000
+    z = rng.integers(-20, 20, size=(16, V)).astype(F32)  # exact ties everywhere
+    T = np.array([0, 1e-6, -1, 9.99e-6] * 4, F32)
+    k = np.array([-1] * 4 + [0] * 4 + [1] * 4 + [1] * 4, np.int32)
+    T[4:] = np.array([0.3, 1.0, 5.0, 0.7] * 3, F32)
+    b = small(z, temperatures=T, top_ks=k, positions=np.arange(16, dtype=np.int64))
+    g = run_gpu(b)
+    assert np.array_equal(g["tokens"], np.argmax(z, axis=1))
+
+
+def test_masked_tokens_never_emitted():
+    b = make_workload(3, B=128)
+    b.temperatures[:] = 1.5
+    b.top_ks[:] = -1
+    b.top_ps[:] = 1.0
+    b.min_ps[:] = 0.0
+    for step in range(3):
+        b.positions = b.positions + 1
+        g = run_gpu(b, debug=False)
+        bits = np.unpackbits(b.bitmask.view(np.uint8), axis=1, bitorder="little")
+        assert bits[np.arange(b.B), g["tokens"]].all()
+
+
+def test_chi_square_v8():
+    """1e5 draws at V=8 (one row per position) follow P(i) = w_i / sum_K w."""
+    from scipy import stats
+    n = 100000
+    z = np.array([1.0, 0.5, 0.0, -0.25, 2.0, -1.0, 0.75, 1.5], F32)
+    T, k, p, mp = 0.8, 6, 0.95, 0.05
+    b = small(np.repeat(z[None], n, 0), temperatures=np.full(n, T, F32), top_ks=np.full(n, k, np.int32),
+              top_ps=np.full(n, p, F32), min_ps=np.full(n, mp, F32), seeds=np.full(n, 99, np.uint64),
+              positions=np.arange(n, dtype=np.int64))
+    g = run_gpu(b, debug=True)
+    o = run_oracle(b, want_transformed=False)
+    assert np.array_equal(g["tokens"], o["tokens"])  # every draw identical to the oracle's
+    kept = g["kept_count"][0]
+    y = (z - z.max()) / T
+    order = np.argsort(-y)
+    idx = order[:kept]
+    w = np.exp(y[idx].astype(np.float64))
+    counts = np.bincount(g["tokens"], minlength=8)
+    assert counts.sum() == counts[idx].sum()
+    assert stats.chisquare(counts[idx], w / w.sum() * n).pvalue > 1e-4
+
+
+def test_batch_composition_independence_gpu():
+    b = make_workload(4, B=48, V=30011)
+    g = run_gpu(b, debug=False)
+    perm = np.random.default_rng(9).permutation(48)
+    g2 = run_gpu(b.rows(perm), debug=False)
+    assert np.array_equal(g2["tokens"], g["tokens"][perm])
+    assert np.array_equal(g2["logprobs"], g["logprobs"][perm])
+    g3 = run_gpu(b.rows([5, 5, 17]), debug=False)
+    assert list(g3["tokens"]) == [g["tokens"][5], g["tokens"][5], g["tokens"][17]]

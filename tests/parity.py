@@ -45,7 +45,8 @@ def compare(batch, g, o, name="", max_ambiguous_frac=1e-3):
         name, "kept_count", np.nonzero(g["kept_count"] != o["kept_count"])[0][:10])
     assert np.array_equal(g["cut"][ok].view(np.uint32), o["cut"][ok].view(np.uint32)), (
         name, "cut", np.nonzero(g["cut"] != o["cut"])[0][:10])
-    amb = ok & (o["race_gap"] <= RACE_REL * np.maximum(1.0, np.abs(o["race_best"])))
+    gap, best = o["race_gap"], o["race_best"]
+    amb = ok & np.isfinite(gap) & np.isfinite(best) & (gap <= RACE_REL * np.maximum(1.0, np.abs(best)))
     same = g["tokens"] == o["tokens"]
     mism = np.nonzero(~same & ~amb)[0]
     assert len(mism) == 0, (name, "token mismatch rows", mism[:10], g["tokens"][mism[:10]], o["tokens"][mism[:10]])

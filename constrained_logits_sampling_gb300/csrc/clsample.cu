@@ -1,20 +1,27 @@
 // Batched constrained logits sampler for GB300 (sm_103a).
 //
 // One thread-block cluster samples one row.  The row's V logits are split into C
-// contiguous slices ("chunks", a multiple of 32 tokens so that every CTA owns whole
-// bitmask words); CTA `rank` of the cluster keeps its slice resident in shared memory
-// for the whole call, so HBM sees every logit exactly once.  Row-wide quantities
-// (max, argmax, softmax normaliser, radix-select histograms, race winners) are
-// exchanged through distributed shared memory (DSMEM) between hardware cluster
-// barriers.  Nothing is written to global memory except the per-row outputs.
+// contiguous slices (a multiple of 32 tokens, so that every CTA owns whole bitmask
+// words).  Each CTA pulls its slice into shared memory with a single TMA bulk copy
+// issued at entry, so the whole slice is in flight while the CTA reads the row's token
+// history and logit_bias lists; HBM sees every logit exactly once and nothing but the
+// per-row outputs is written back.
 //
-// The arithmetic that decides integers (kept set, sampled id) is exact and identical on
-// any IEEE machine: y = fl32(fl32(z' - m) * fl32(1/T)); top-k compares y; top-p sums the
-// fixed-point weights floor(exp32(y) * 2^40) exactly and compares with ceil(p * W);
-// min-p compares y with fl32(ln min_p).  The race score y - ln(-ln U) is fp32.
+//   pass A    sanitise + mask + penalties/bias (the few penalised tokens live in a small
+//             hash with their final value), slice max, lowest argmax and an online sum of
+//             exp((z' - max)/T); per-thread maxima give a lower bound of the top-k cut.
+//   exchange  every CTA pushes its slice statistics into every CTA's shared memory
+//             (DSMEM) and one cluster barrier publishes them.  Greedy rows end here.
+//   pass B    the tokens that can survive truncation (y >= a provable bound) are
+//             compacted; a leader CTA gathers them (DSMEM stores + a remote mbarrier
+//             arrive) and finishes top-k -> top-p -> min-p and the exponential race alone.
+//   slow path rows without a usable bound (top-p alone, very large k, compaction
+//             overflow) run cluster-wide radix selects over the resident slices.
 //
-// Page references: "SGLang source teardown (10): Sampling, Grammar and structured
-// output" (SGLang page) and "GLM-5.3 inference (7): output side" (GLM page).
+// The arithmetic that decides integers (kept set, drawn id) is exact and identical on
+// any IEEE machine (sampler_math.cuh).  Page references: "SGLang source teardown (10):
+// Sampling, Grammar and structured output" (SGLang page) and "GLM-5.3 inference (7):
+// output side" (GLM page).
 
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
@@ -26,316 +33,205 @@
 #include <cstring>
 
 #include "clsample.h"
+#include "cluster_sync.cuh"
+#include "sampler_math.cuh"
 
 namespace cg = cooperative_groups;
 
 namespace {
 
+using namespace clsample;
+
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kHashCap = 1024;  // distinct penalised/biased ids per CTA slice
-constexpr uint32_t kEmpty = 0xFFFFFFFFu;
+constexpr int kHashCap = 1024;   // distinct penalised / biased ids per slice
+constexpr int kCandCap = 512;    // compacted candidates per slice
 constexpr int kMaxCluster = 16;
-constexpr float kGreedyEps = 1e-5f;
+constexpr uint32_t kEmpty = 0xFFFFFFFFu;
+// The slice's bulk copy is issued as this many TMA copies (all on one mbarrier).
+#ifndef CLSAMPLE_BULK_PIECES
+#define CLSAMPLE_BULK_PIECES 1
+#endif
+constexpr int kBulkPieces = CLSAMPLE_BULK_PIECES;
+// Longest slice: pass A keeps a bit per token of the slice in the histogram area.
+constexpr int kMaxChunk = 32 * 1024;
 
 enum : int { kRowOk = 0, kRowOverflow = 1, kRowInvalid = 2 };
-enum : int { kFlagInvalid = 1, kFlagOverflow = 2 };
+enum : int { kFlagInvalid = 1, kFlagOverflow = 2, kFlagTimeout = 4 };
 
 struct Geometry {
   int C;      // CTAs per row (cluster size)
   int chunk;  // tokens per CTA, multiple of 32
-  int smem;   // dynamic shared memory bytes per CTA
+  int smem;   // dynamic shared memory per CTA for this element size
+  int cap;    // compacted candidates per CTA the leader can gather
 };
 
 struct LaunchParams {
   clsample_args_t a;
   int C;
   int chunk;
-  int vec_ok;  // logits rows are 16-byte (f32) / 8-byte (bf16) aligned for vector loads
+  int cap;
+  int bulk_ok;  // every row start is 16-byte aligned: the slice can be bulk-copied
 };
 
-// ---------------------------------------------------------------- shared memory layout
-
-// Dynamic shared memory of one CTA (offsets in bytes from the base):
-//   zs      f32[chunk]          transformed logits z' of the slice (padding = -inf)
-//   modbits u32[chunk/32]       1 = token is penalised or biased (handled separately)
-//   hkey    u32[kHashCap]       hash of the slice's penalised/biased local ids
-//   hcnt    u32[kHashCap]       occurrences in the history
-//   hbias   i32[kHashCap]       index of the last logit_bias entry for the id, or -1
-//   hist_c  u32[2][256]         radix histogram, counts (double-buffered across passes)
-//   hist_w  u64[2][256]         radix histogram, fixed-point weights
-//   merged  u64[2][256]         cluster-merged counts and weights
-struct Smem {
-  float* zs;
-  uint32_t* modbits;
-  uint32_t* hkey;
-  uint32_t* hcnt;
-  int32_t* hbias;
-  uint32_t* hist_c;
-  unsigned long long* hist_w;
-  unsigned long long* merged_c;
-  unsigned long long* merged_w;
+struct Cand {
+  float y;
+  int id;
 };
 
-__host__ __device__ inline size_t smem_bytes_for(int chunk) {
-  size_t b = 0;
-  b += sizeof(float) * (size_t)chunk;
-  b += sizeof(uint32_t) * (size_t)(chunk / 32);
-  b += sizeof(uint32_t) * kHashCap * 3;
-  b = (b + 15) & ~size_t(15);
-  b += sizeof(uint32_t) * 2 * 256;
-  b += sizeof(unsigned long long) * 2 * 256;
-  b += sizeof(unsigned long long) * 2 * 256;
-  return b;
-}
+// Slice statistics pushed to every CTA after pass A.
+struct X1 {
+  float m;      // slice max of z' (-inf if no candidate)
+  int arg;      // lowest id reaching m (INT_MAX if none)
+  float s;      // sum over the slice's candidates of 2^((z' - m) * log2(e) / T)
+  int flags;    // kFlag*
+  float lk;     // max over warps of the warp's k-th largest thread max of z' (-inf: unknown)
+  float lkc;    // min over warps of the ceil(k / (16 C))-th largest thread max (-inf: unknown)
+};
 
-__device__ inline Smem carve(unsigned char* base, int chunk) {
-  Smem s;
-  size_t off = 0;
-  s.zs = reinterpret_cast<float*>(base + off);
-  off += sizeof(float) * (size_t)chunk;
-  s.modbits = reinterpret_cast<uint32_t*>(base + off);
-  off += sizeof(uint32_t) * (size_t)(chunk / 32);
-  s.hkey = reinterpret_cast<uint32_t*>(base + off);
-  off += sizeof(uint32_t) * kHashCap;
-  s.hcnt = reinterpret_cast<uint32_t*>(base + off);
-  off += sizeof(uint32_t) * kHashCap;
-  s.hbias = reinterpret_cast<int32_t*>(base + off);
-  off += sizeof(int32_t) * kHashCap;
-  off = (off + 15) & ~size_t(15);
-  s.hist_c = reinterpret_cast<uint32_t*>(base + off);
-  off += sizeof(uint32_t) * 2 * 256;
-  s.hist_w = reinterpret_cast<unsigned long long*>(base + off);
-  off += sizeof(unsigned long long) * 2 * 256;
-  s.merged_c = reinterpret_cast<unsigned long long*>(base + off);
-  off += sizeof(unsigned long long) * 256;
-  s.merged_w = reinterpret_cast<unsigned long long*>(base + off);
-  return s;
-}
-
-// Per-CTA values published to the other CTAs of the cluster.  Each exchange round has
-// its own fields, so a fast CTA never overwrites a value a slow CTA is still reading.
-struct Exchange {
-  float m;          // slice max of z' (-inf if none)
-  int arg;          // lowest global id reaching m (INT_MAX if none)
-  float S;          // sum of 2^((z' - m) * c) over the slice's candidates
-  int ncand;        // candidates (z' > -inf)
-  int flags;        // kFlagInvalid | kFlagOverflow
-  unsigned long long W;  // top-p: fixed-point mass of the slice's part of S_k
-  float race_s;     // best race score of the slice
-  int race_tok;     // its id (lowest id on ties)
-  int kept;         // kept tokens in the slice
-  float ymin;       // smallest y of a kept token in the slice
+// Slice results pushed to every CTA after pass B (and by the slow path).
+struct X2 {
+  int count;                // compacted candidates (may exceed the capacity)
+  int flags;
+  unsigned long long w;     // fixed-point weight partial (top-p mass)
+  float race_s;             // best race score of the slice
+  int race_tok;             // its id
+  int kept;                 // kept tokens of the slice
+  float ymin;               // smallest y of a kept token
+  float ytok;               // y of the slice's winner
 };
 
 struct RowParams {
   float T, p, mp, rep, freq, pres;
   int k;
   unsigned long long seed;
-  long long pos;
+  unsigned long long pos;
   int invalid;
 };
 
-// ---------------------------------------------------------------- scalar helpers
+struct RowState {
+  float m;
+  int arg;
+  float S;
+  int flags;
+  float bound;  // lower bound of the k-th largest z' (-inf if none)
+};
 
-// Non-finite logits: NaN -> -inf (never drawn), +inf -> FLT_MAX, -inf -> -FLT_MAX
-// (SGLang page, "_preprocess_logits": keep the row samplable).
-__device__ __forceinline__ float sanitize(float v) {
-  if (v != v) return -INFINITY;
-  return fminf(fmaxf(v, -FLT_MAX), FLT_MAX);
+// ---------------------------------------------------------------- shared memory layout
+
+__host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Dynamic shared memory of one CTA:
+//   raw       chunk * esize       the slice as loaded (f32 or bf16 bits); the leader
+//                                  reuses it to gather the cluster's candidates
+//   live      u32[chunk/32]       allowed by the bitmask, inside the row, not penalised
+//   hkey/hcnt/hbias/hval          hash of the slice's penalised / biased tokens: local id,
+//                                  history count, last bias entry, its value then final z'
+//   cand      Cand[kCandCap]      compacted candidates of the slice
+//   hist_c    u32[256]            local radix histogram (counts); also the sort buffer
+//   hist_w    u64[256]            local radix histogram (fixed-point weights)
+//   mrg_c     u32[2][256]         cluster-merged histograms (DSMEM atomics from every
+//   mrg_w     u64[2][256]         CTA), double-buffered across passes
+struct Smem {
+  unsigned char* raw;
+  uint32_t* live;
+  uint32_t* hkey;
+  uint32_t* hcnt;
+  int32_t* hbias;
+  float* hval;
+  Cand* cand;
+  uint32_t* hist_c;
+  unsigned long long* hist_w;
+  uint32_t* mrg_c;
+  unsigned long long* mrg_w;
+};
+
+// The top-p histogram (kWarps x 64 bins of u64) reuses cand + hist_c + hist_w, which
+// are contiguous; pass A's per-token `modbits` (kMaxChunk bits) reuses hist_c + hist_w.
+static_assert(sizeof(uint32_t) * kThreads + sizeof(unsigned long long) * 256 >= kMaxChunk / 8,
+              "pass A modbits do not fit the histogram area");
+static_assert(sizeof(Cand) * kCandCap + sizeof(uint32_t) * kThreads + sizeof(unsigned long long) * 256 >=
+                  sizeof(unsigned long long) * kWarps * 64,
+              "top-p histogram does not fit the candidate area");
+
+__host__ __device__ inline size_t smem_bytes_for(int chunk, int esize) {
+  size_t b = align_up((size_t)chunk * esize, 128);
+  b += sizeof(uint32_t) * (size_t)(chunk / 32);
+  b = align_up(b, 16);
+  b += (sizeof(uint32_t) * 3 + sizeof(float)) * kHashCap;
+  b += sizeof(Cand) * kCandCap;
+  b = align_up(b, 16);
+  b += sizeof(uint32_t) * kThreads;  // >= 256 counts; sized for the 512-entry sort
+  b += sizeof(unsigned long long) * 256;
+  b += sizeof(uint32_t) * 2 * 256;
+  b += sizeof(unsigned long long) * 2 * 256;
+  return b;
 }
 
-// An overflow of the penalty/bias arithmetic folds back like sanitising, except that
-// -inf stays -inf.
-__device__ __forceinline__ float guard(float v) {
-  if (v != v) return -INFINITY;
-  return v == INFINITY ? FLT_MAX : v;
+__device__ inline Smem carve(unsigned char* base, int chunk, int esize) {
+  Smem s;
+  size_t off = 0;
+  s.raw = base;
+  off = align_up((size_t)chunk * esize, 128);
+  s.live = reinterpret_cast<uint32_t*>(base + off);
+  off += sizeof(uint32_t) * (size_t)(chunk / 32);
+  off = align_up(off, 16);
+  s.hkey = reinterpret_cast<uint32_t*>(base + off);
+  off += sizeof(uint32_t) * kHashCap;
+  s.hcnt = reinterpret_cast<uint32_t*>(base + off);
+  off += sizeof(uint32_t) * kHashCap;
+  s.hbias = reinterpret_cast<int32_t*>(base + off);
+  off += sizeof(int32_t) * kHashCap;
+  s.hval = reinterpret_cast<float*>(base + off);
+  off += sizeof(float) * kHashCap;
+  s.cand = reinterpret_cast<Cand*>(base + off);
+  off += sizeof(Cand) * kCandCap;
+  off = align_up(off, 16);
+  s.hist_c = reinterpret_cast<uint32_t*>(base + off);
+  off += sizeof(uint32_t) * kThreads;
+  s.hist_w = reinterpret_cast<unsigned long long*>(base + off);
+  off += sizeof(unsigned long long) * 256;
+  s.mrg_c = reinterpret_cast<uint32_t*>(base + off);
+  off += sizeof(uint32_t) * 2 * 256;
+  s.mrg_w = reinterpret_cast<unsigned long long*>(base + off);
+  return s;
 }
 
-__device__ __forceinline__ float ex2_approx(float x) {
-  float r;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
-  return r;
-}
+// ---------------------------------------------------------------- slice access
 
-// Order-preserving key of y (larger y -> larger key); -0 is folded onto +0.
-__device__ __forceinline__ uint32_t ykey(float y) {
-  uint32_t b = __float_as_uint(y == 0.0f ? 0.0f : y);
-  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-__device__ __forceinline__ float key_to_y(uint32_t k) {
-  uint32_t b = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
-  return __uint_as_float(b);
-}
-
-// y = fl32(fl32(z - m) * invT), -inf for non-candidates.
-__device__ __forceinline__ float y_of(float z, float m, float invT) {
-  if (!(z > -INFINITY)) return -INFINITY;
-  float y = __fmul_rn(__fsub_rn(z, m), invT);
-  return y == 0.0f ? 0.0f : y;
-}
-
-// exp32: single-precision e^y for y <= 0 used by the top-p weights.  Cody-Waite
-// reduction y = n*ln2 + r (ln2 split into a 15-bit head and a tail), degree-7 Taylor
-// polynomial of e^r by Horner's rule with fused multiply-adds, scaling by 2^n.  Each
-// step is one correctly rounded IEEE operation.  e^-32 is below the 2^-40 resolution
-// of the weights, so y < -32 gives 0.
-__device__ __forceinline__ float exp32(float y) {
-  if (!(y >= -32.0f)) return 0.0f;
-  float n = rintf(__fmul_rn(y, 0x1.715476p+0f));
-  float r = __fmaf_rn(-n, 0x1.62e4p-1f, y);
-  r = __fmaf_rn(-n, 0x1.7f7d1cp-20f, r);
-  float q = 1.0f / 5040.0f;
-  q = __fmaf_rn(q, r, 1.0f / 720.0f);
-  q = __fmaf_rn(q, r, 1.0f / 120.0f);
-  q = __fmaf_rn(q, r, 1.0f / 24.0f);
-  q = __fmaf_rn(q, r, 1.0f / 6.0f);
-  q = __fmaf_rn(q, r, 0.5f);
-  q = __fmaf_rn(q, r, 1.0f);
-  q = __fmaf_rn(q, r, 1.0f);
-  return ldexpf(q, (int)n);
-}
-
-__device__ __forceinline__ unsigned long long weight_fx(float y) {
-  return __float2ull_rz(__fmul_rn(exp32(y), 0x1p40f));
-}
-
-// ceil(p * W) for p in (0, 1]: p = pm * 2^-s with a 24-bit integer pm.
-__device__ inline unsigned long long ceil_scaled(unsigned long long W, float p) {
-  int e;
-  float f = frexpf(p, &e);
-  unsigned long long pm = (unsigned long long)ldexpf(f, 24);
-  int s = 24 - e;
-  // prod = W * pm as a 128-bit value (hi:lo)
-  unsigned long long lo = W * pm;
-  unsigned long long hi = __umul64hi(W, pm);
-  if (s >= 128) return (lo | hi) ? 1ull : 0ull;
-  // add 2^s - 1 then shift right by s
-  unsigned long long add_lo, add_hi;
-  if (s >= 64) {
-    add_lo = ~0ull;
-    add_hi = (s == 64) ? 0ull : ((1ull << (s - 64)) - 1ull);
-  } else {
-    add_lo = (1ull << s) - 1ull;
-    add_hi = 0ull;
-  }
-  unsigned long long sum_lo = lo + add_lo;
-  unsigned long long carry = sum_lo < lo ? 1ull : 0ull;
-  unsigned long long sum_hi = hi + add_hi + carry;
-  if (s >= 64) return s == 64 ? sum_hi : (sum_hi >> (s - 64));
-  if (s == 0) return sum_lo;
-  return (sum_lo >> s) | (sum_hi << (64 - s));
-}
-
-// Philox4x32 with 10 rounds (Salmon, Moraes, Dror, Shaw, SC'11).
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k) {
-#pragma unroll
-  for (int i = 0; i < 10; ++i) {
-    if (i) {
-      k.x += 0x9E3779B9u;
-      k.y += 0xBB67AE85u;
+template <bool kBF16>
+struct Slice {
+  const unsigned char* raw;
+  // four raw logits of tokens 4f .. 4f+3 of the slice, widened to f32
+  __device__ __forceinline__ float4 load4(int f) const {
+    if (kBF16) {
+      const uint2 w = reinterpret_cast<const uint2*>(raw)[f];
+      return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u),
+                         __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
+    } else {
+      return reinterpret_cast<const float4*>(raw)[f];
     }
-    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
-    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
-    c = make_uint4(hi1 ^ c.y ^ k.x, lo1, hi0 ^ c.w ^ k.y, lo0);
   }
-  return c;
-}
-
-// U in (0,1) from one Philox output word: (top 23 bits + 1/2) / 2^23, exact in fp32.
-__device__ __forceinline__ float word_to_uniform(uint32_t x) {
-  return __fmul_rn(__fadd_rn(__uint2float_rn(x >> 9), 0.5f), 0x1p-23f);
-}
-
-// Race score of a kept token: y - ln E with E = -ln U (Gumbel form of argmax w / E).
-__device__ __forceinline__ float race_score(float y, uint32_t x) {
-  const float u = word_to_uniform(x);
-  const float e = -logf(u);
-  return __fsub_rn(y, logf(e));
-}
-
-// (value, id) "better": larger value, then lower id.
-__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
-  return v > bv || (v == bv && i < bi);
-}
-
-// Merge two (max, sum 2^((z-max)c)) pairs.
-__device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2, float c) {
-  const float mm = fmaxf(m, m2);
-  if (mm == -INFINITY) {
-    m = mm;
-    s = 0.0f;
-    return;
-  }
-  s = s * ex2_approx(__fmul_rn(m - mm, c)) + s2 * ex2_approx(__fmul_rn(m2 - mm, c));
-  m = mm;
-}
-
-// ---------------------------------------------------------------- block reductions
-
-template <typename T>
-__device__ __forceinline__ T shfl_down(T v, int d) {
-  return __shfl_down_sync(0xffffffffu, v, d);
-}
-
-__device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v, unsigned long long* red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int d = 16; d > 0; d >>= 1) v += shfl_down(v, d);
-  __syncthreads();
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  unsigned long long t = 0;
-  for (int w = 0; w < kWarps; ++w) t += red[w];
-  return t;
-}
-
-// ---------------------------------------------------------------- logits loaders
-
-struct LoadF32 {
-  const float* row;
-  int len;
-  bool vec;
-  __device__ __forceinline__ float4 load4(int e) const {
-    if (vec && e + 3 < len) return __ldcs(reinterpret_cast<const float4*>(row + e));
-    float4 v;
-    v.x = e + 0 < len ? __ldcs(row + e + 0) : 0.0f;
-    v.y = e + 1 < len ? __ldcs(row + e + 1) : 0.0f;
-    v.z = e + 2 < len ? __ldcs(row + e + 2) : 0.0f;
-    v.w = e + 3 < len ? __ldcs(row + e + 3) : 0.0f;
-    return v;
+  __device__ __forceinline__ float load1(int i) const {
+    if (kBF16) return __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(raw)[i] << 16);
+    return reinterpret_cast<const float*>(raw)[i];
   }
 };
 
-__device__ __forceinline__ float bf16_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
+__device__ __forceinline__ float comp(const float4& v, int j) {
+  return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
+}
 
-struct LoadBF16 {
-  const uint16_t* row;
-  int len;
-  bool vec;
-  __device__ __forceinline__ float4 load4(int e) const {
-    float4 v;
-    if (vec && e + 3 < len) {
-      const uint2 w = __ldcs(reinterpret_cast<const uint2*>(row + e));
-      v.x = bf16_to_f32(w.x & 0xFFFFu);
-      v.y = bf16_to_f32(w.x >> 16);
-      v.z = bf16_to_f32(w.y & 0xFFFFu);
-      v.w = bf16_to_f32(w.y >> 16);
-      return v;
-    }
-    v.x = e + 0 < len ? bf16_to_f32(__ldcs(row + e + 0)) : 0.0f;
-    v.y = e + 1 < len ? bf16_to_f32(__ldcs(row + e + 1)) : 0.0f;
-    v.z = e + 2 < len ? bf16_to_f32(__ldcs(row + e + 2)) : 0.0f;
-    v.w = e + 3 < len ? bf16_to_f32(__ldcs(row + e + 3)) : 0.0f;
-    return v;
-  }
-};
+// live bits of tokens 4f .. 4f+3
+__device__ __forceinline__ uint32_t live4(const uint32_t* live, int f) {
+  return (live[f >> 3] >> ((f & 7) * 4)) & 0xFu;
+}
 
 // ---------------------------------------------------------------- hash of penalised ids
 
-// Inserts local id l; returns the slot or -1 when the table is full (bounded probing).
+// Inserts local id l; returns its slot, or -1 when the table is full (bounded probing).
 __device__ __forceinline__ int hash_insert(uint32_t* hkey, uint32_t l) {
-  uint32_t h = (l * 2654435761u) & (kHashCap - 1);
+  const uint32_t h = (l * 2654435761u) & (kHashCap - 1);
   for (int probe = 0; probe < kHashCap; ++probe) {
     const uint32_t slot = (h + probe) & (kHashCap - 1);
     const uint32_t prev = atomicCAS(&hkey[slot], kEmpty, l);
@@ -344,144 +240,359 @@ __device__ __forceinline__ int hash_insert(uint32_t* hkey, uint32_t l) {
   return -1;
 }
 
-// ---------------------------------------------------------------- cluster radix select
-
-// Finds, among this row's candidates with y >= ylo, the key K* such that
-//   unweighted: K* is the `target`-th largest key (1-based, repeats counted);
-//   weighted:   the running fixed-point weight, summed from the largest key down,
-//               first reaches `target` at key K*.
-// Four passes of 8-bit digits, most significant first; each pass histograms the
-// elements that match the digits chosen so far, merges the C histograms through DSMEM
-// and picks the digit.  Returns K*, or sets *err if the histograms run dry (which the
-// callers' targets make impossible).
-template <bool kWeighted>
-__device__ uint32_t cluster_select(const cg::cluster_group& cluster, const Smem& S, int C, int chunk,
-                                   float m, float invT, float ylo, unsigned long long target,
-                                   int* sel_digit, unsigned long long* sel_above, int* err) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  uint32_t prefix = 0, pmask = 0;
-  const int nvec = chunk / 4;
-  const float4* z4p = reinterpret_cast<const float4*>(S.zs);
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    const int buf = pass & 1;
-    uint32_t* hc = S.hist_c + buf * 256;
-    unsigned long long* hw = S.hist_w + buf * 256;
-    if (tid < 256) {
-      hc[tid] = 0u;
-      hw[tid] = 0ull;
-    }
-    __syncthreads();
-    for (int base = 0; base < nvec; base += kThreads) {
-      const int f = base + tid;
-      float4 z4 = f < nvec ? z4p[f] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-      const float zz[4] = {z4.x, z4.y, z4.z, z4.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float y = y_of(zz[j], m, invT);
-        const uint32_t key = ykey(y);
-        const bool pred = (zz[j] > -INFINITY) && (y >= ylo) && ((key & pmask) == prefix);
-        const uint32_t digit = pred ? ((key >> shift) & 0xFFu) : 0xFFFFFFFFu;
-        if (!kWeighted) {
-          const uint32_t peers = __match_any_sync(0xffffffffu, digit);
-          if (pred && lane == __ffs(peers) - 1) atomicAdd(&hc[digit], (uint32_t)__popc(peers));
-        } else {
-          if (pred) atomicAdd(&hw[digit], weight_fx(y));
-        }
-      }
-    }
-    __syncthreads();
-    cluster.sync();  // every CTA's histogram of this pass is complete
-    if (tid < 256) {
-      unsigned long long sc = 0, sw = 0;
-      for (int r = 0; r < C; ++r) {
-        if (!kWeighted) {
-          const uint32_t* rc = cluster.map_shared_rank(hc, r);
-          sc += rc[tid];
-        } else {
-          const unsigned long long* rw = cluster.map_shared_rank(hw, r);
-          sw += rw[tid];
-        }
-      }
-      S.merged_c[tid] = kWeighted ? sw : sc;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      // lane l covers bins 255-8l .. 248-8l, scanned from the top down
-      unsigned long long v[8];
-      unsigned long long lsum = 0;
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        v[t] = S.merged_c[255 - 8 * lane - t];
-        lsum += v[t];
-      }
-      unsigned long long incl = lsum;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const unsigned long long o = __shfl_up_sync(0xffffffffu, incl, d);
-        if (lane >= d) incl += o;
-      }
-      const uint32_t hit = __ballot_sync(0xffffffffu, incl >= target);
-      const int first = hit ? __ffs(hit) - 1 : -1;
-      if (lane == (first < 0 ? 0 : first)) {
-        if (first < 0) {
-          *err = 1;
-          *sel_digit = 0;
-          *sel_above = 0;
-        } else {
-          unsigned long long cum = incl - lsum;
-          int d = 255 - 8 * lane - 7;
-          for (int t = 0; t < 8; ++t) {
-            if (cum + v[t] >= target) {
-              d = 255 - 8 * lane - t;
-              break;
-            }
-            cum += v[t];
-          }
-          *sel_digit = d;
-          *sel_above = cum;
-        }
-      }
-    }
-    __syncthreads();
-    prefix |= (uint32_t)(*sel_digit) << shift;
-    pmask |= 0xFFu << shift;
-    target -= *sel_above;
-    __syncthreads();
+// Slot of local id l (which must be present); -1 if absent (bounded probing).
+__device__ __forceinline__ int hash_find(const uint32_t* hkey, uint32_t l) {
+  const uint32_t h = (l * 2654435761u) & (kHashCap - 1);
+  for (int probe = 0; probe < kHashCap; ++probe) {
+    const uint32_t slot = (h + probe) & (kHashCap - 1);
+    const uint32_t k = hkey[slot];
+    if (k == l) return (int)slot;
+    if (k == kEmpty) return -1;
   }
-  return prefix;
+  return -1;
+}
+
+// ---------------------------------------------------------------- warp / block helpers
+
+__device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2, float c) {
+  const float mm = fmaxf(m, m2);
+  if (mm == -INFINITY) {
+    m = mm;
+    s = 0.0f;
+    return;
+  }
+  s = s * ex2_approx((m - mm) * c) + s2 * ex2_approx((m2 - mm) * c);
+  m = mm;
+}
+
+__device__ __forceinline__ int warp_min_i(int v) {
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, d));
+  return v;
+}
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+  return v;
+}
+
+// Block-wide sum of a u64 (all threads receive it).  `red` holds kWarps entries.
+__device__ unsigned long long block_sum_u64(unsigned long long v, unsigned long long* red) {
+  v = warp_sum_u64(v);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  unsigned long long t = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) t += red[w];
+  return t;
+}
+
+__device__ int block_min_i(int v, int* red) {
+  v = warp_min_i(v);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  int t = INT_MAX;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) t = min(t, red[w]);
+  return t;
+}
+
+// Race partials of one thread, reduced over the block into `out` (thread 0 writes).
+struct Race {
+  float s;      // best score
+  int tok;      // its id
+  float ybest;  // its y
+  int kept;
+  float ymin;
+  __device__ void init() {
+    s = -INFINITY;
+    tok = INT_MAX;
+    ybest = -INFINITY;
+    kept = 0;
+    ymin = INFINITY;
+  }
+  __device__ __forceinline__ void add(float y, int id, uint32_t word) {
+    ++kept;
+    ymin = fminf(ymin, y);
+    const float sc = race_score(y, word);
+    if (better(sc, id, s, tok)) {
+      s = sc;
+      tok = id;
+      ybest = y;
+    }
+  }
+  __device__ void merge(float s2, int t2, float yb2, int k2, float y2) {
+    if (better(s2, t2, s, tok)) {
+      s = s2;
+      tok = t2;
+      ybest = yb2;
+    }
+    kept += k2;
+    ymin = fminf(ymin, y2);
+  }
+  __device__ void merge(const X2& x) { merge(x.race_s, x.race_tok, x.ytok, x.kept, x.ymin); }
+  // a kept token that provably cannot win the race
+  __device__ __forceinline__ void count_only(float y) {
+    ++kept;
+    ymin = fminf(ymin, y);
+  }
+  __device__ void warp_reduce() {
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) {
+      const float s2 = __shfl_xor_sync(0xffffffffu, s, d);
+      const int t2 = __shfl_xor_sync(0xffffffffu, tok, d);
+      const float b2 = __shfl_xor_sync(0xffffffffu, ybest, d);
+      const int k2 = __shfl_xor_sync(0xffffffffu, kept, d);
+      const float y2 = __shfl_xor_sync(0xffffffffu, ymin, d);
+      merge(s2, t2, b2, k2, y2);
+    }
+  }
+  __device__ void to(X2& x) const {
+    x.race_s = s;
+    x.race_tok = tok;
+    x.ytok = ybest;
+    x.kept = kept;
+    x.ymin = ymin;
+  }
+};
+
+// Block reduction of the race; thread 0 receives the result.  `buf` holds kWarps X2.
+__device__ void block_reduce_race(Race& r, X2* buf) {
+  r.warp_reduce();
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) r.to(buf[threadIdx.x >> 5]);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    Race t;
+    t.init();
+    for (int w = 0; w < kWarps; ++w) t.merge(buf[w]);
+    r = t;
+  }
+}
+
+// Writes a sampled row's outputs.
+__device__ void write_sampled(const clsample_args_t& a, int row, const Race& r, float lnS, bool ok) {
+  ok = ok && r.tok != INT_MAX;
+  a.tokens[row] = ok ? r.tok : -1;
+  if (a.logprobs) a.logprobs[row] = ok ? r.ybest - lnS : -INFINITY;
+  if (a.row_status) a.row_status[row] = ok ? kRowOk : kRowOverflow;
+  if (a.dbg_kept_count) a.dbg_kept_count[row] = ok ? r.kept : 0;
+  if (a.dbg_cut) a.dbg_cut[row] = ok ? r.ymin : -INFINITY;
+}
+
+// Pushes the calling CTA's record `*mine` into slot `rank` of `dst` in every CTA of the
+// cluster (threads 0 .. C-1 each write one copy).  A cluster barrier must follow.
+template <typename T>
+__device__ __forceinline__ void push_all(const cg::cluster_group& cluster, T* dst, const T* mine, int rank,
+                                         int C) {
+  if ((int)threadIdx.x < C) *cluster.map_shared_rank(dst + rank, (unsigned)threadIdx.x) = *mine;
+}
+
+// ---------------------------------------------------------------- radix digit choice
+
+// Given a 256-bin histogram (top bin = largest keys), finds the bin where the running
+// total from the top first reaches `target`; writes the bin and the total above it.
+// Run by one full warp.  Sets *none when the histogram holds less than `target`.
+template <typename H>
+__device__ void pick_digit(const H* hist, unsigned long long target, int* digit, unsigned long long* above,
+                           int* none) {
+  const int lane = threadIdx.x & 31;
+  unsigned long long v[8];
+  unsigned long long lsum = 0;
+#pragma unroll
+  for (int t = 0; t < 8; ++t) {
+    v[t] = hist[255 - 8 * lane - t];
+    lsum += v[t];
+  }
+  unsigned long long incl = lsum;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const unsigned long long o = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += o;
+  }
+  const uint32_t hit = __ballot_sync(0xffffffffu, incl >= target);
+  if (hit == 0) {
+    if (lane == 0) {
+      *none = 1;
+      *digit = 0;
+      *above = 0;
+    }
+    return;
+  }
+  const int first = __ffs(hit) - 1;
+  if (lane == first) {
+    unsigned long long cum = incl - lsum;
+    int d = 255 - 8 * lane - 7;
+    for (int t = 0; t < 8; ++t) {
+      if (cum + v[t] >= target) {
+        d = 255 - 8 * lane - t;
+        break;
+      }
+      cum += v[t];
+    }
+    *none = 0;
+    *digit = d;
+    *above = cum;
+  }
+}
+
+// Adds one element to a local radix histogram with warp aggregation.  Every lane of the
+// warp must call it (pred false for lanes without an element).
+template <bool kWeighted>
+__device__ __forceinline__ void hist_add(uint32_t* hc, unsigned long long* hw, bool pred, uint32_t digit,
+                                         unsigned long long w) {
+  const uint32_t d = pred ? digit : 0xFFFFFFFFu;
+  const uint32_t peers = __match_any_sync(0xffffffffu, d);
+  const int lane = threadIdx.x & 31;
+  const bool leader = pred && lane == __ffs(peers) - 1;
+  if (!kWeighted) {
+    if (leader) atomicAdd(&hc[digit], (uint32_t)__popc(peers));
+  } else {
+    // weights < 2^41: sum the low 21 bits and the high part separately (each < 2^26)
+    const uint32_t lo = pred ? (uint32_t)(w & 0x1FFFFFu) : 0u;
+    const uint32_t hi = pred ? (uint32_t)(w >> 21) : 0u;
+    const uint32_t slo = __reduce_add_sync(peers, lo);
+    const uint32_t shi = __reduce_add_sync(peers, hi);
+    if (leader) atomicAdd(&hw[digit], ((unsigned long long)shi << 21) + slo);
+  }
+}
+
+// ---------------------------------------------------------------- per-token helpers
+
+// max of |a|, |b| that propagates NaN: a float4 is finite iff the max of its four
+// magnitudes is below +inf.
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ bool finite4(const float4& v) {
+  return max_nan(max_nan(fabsf(v.x), fabsf(v.y)), max_nan(fabsf(v.z), fabsf(v.w))) < INFINITY;
+}
+
+// Smallest float z with y_of(z, m, invT) >= theta (theta <= 0).  y_of is monotone in z,
+// so {candidates : y >= theta} = {candidates : z >= result} exactly.
+__device__ float z_threshold(float theta, float m, float invT) {
+  if (!(theta > -INFINITY)) return -INFINITY;
+  if (y_of(-FLT_MAX, m, invT) >= theta) return -FLT_MAX;
+  uint32_t lo = fkey(-FLT_MAX), hi = fkey(m);  // y(lo) < theta <= y(hi) = 0
+  while (hi - lo > 1u) {
+    const uint32_t mid = lo + (hi - lo) / 2u;
+    if (y_of(key_to_float(mid), m, invT) >= theta) hi = mid;
+    else lo = mid;
+  }
+  return key_to_float(hi);
+}
+
+// Warp-cooperative version of z_threshold: a 32-ary search over float keys (about
+// seven steps); every lane returns the result.  The whole warp must call it.
+__device__ float z_threshold_warp(float theta, float m, float invT) {
+  if (!(theta > -INFINITY)) return -INFINITY;
+  if (y_of(-FLT_MAX, m, invT) >= theta) return -FLT_MAX;
+  const int lane = threadIdx.x & 31;
+  uint32_t lo = fkey(-FLT_MAX), hi = fkey(m);  // y(lo) < theta <= y(hi)
+  while (hi - lo > 1u) {
+    const uint32_t s1 = hi - lo - 1u;  // probes lie in [lo + 1, hi - 1]
+    const uint32_t probe = lo + 1u + (uint32_t)(((unsigned long long)lane * s1) / 32ull);
+    const bool ok = y_of(key_to_float(probe), m, invT) >= theta;
+    const uint32_t bal = __ballot_sync(0xffffffffu, ok);
+    if (bal) {
+      const int first = __ffs(bal) - 1;
+      const uint32_t pf = __shfl_sync(0xffffffffu, probe, first);
+      const uint32_t pb = __shfl_sync(0xffffffffu, probe, first > 0 ? first - 1 : 0);
+      hi = pf;
+      if (first > 0) lo = pb;
+    } else {
+      lo = __shfl_sync(0xffffffffu, probe, 31);
+    }
+  }
+  return key_to_float(hi);
+}
+
+// -ln(-ln U) over the 23-bit uniform grid stays below 16.64, so a token with
+// y + kGumbelMax < best cannot win (or tie) the race.
+constexpr float kGumbelMax = 16.75f;
+
+// y-bins of the top-p histogram: bin b holds -(b+1)/4 < y <= -b/4; the last bin also
+// holds everything below.
+constexpr int kPBins = 64;
+__device__ __forceinline__ int pbin(float y) {
+  const int b = __float2int_rz(__fmul_rn(-y, 4.0f));
+  return b < kPBins - 1 ? b : kPBins - 1;
 }
 
 // ---------------------------------------------------------------- the kernel
 
-template <typename Loader, typename Elem>
+template <bool kBF16>
 __global__ void __launch_bounds__(kThreads, 2) sampler_kernel(const LaunchParams P) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  __shared__ Exchange xchg;
+  extern __shared__ __align__(128) unsigned char smem_base[];
+  __shared__ X1 x1[kMaxCluster];
+  __shared__ X2 x2[kMaxCluster];
+  __shared__ X1 x1_mine;
+  __shared__ X2 x2_mine;
+  __shared__ __align__(8) unsigned long long mbar_load;
+  __shared__ __align__(8) unsigned long long mbar_gather;
   __shared__ RowParams rp;
-  __shared__ unsigned long long red_u64[kWarps];
-  __shared__ float red_f[kWarps * 4];
-  __shared__ int red_i[kWarps * 4];
-  __shared__ int sh_flags;
-  __shared__ int sh_sel_digit;
-  __shared__ unsigned long long sh_sel_above;
-  __shared__ int sh_sel_err;
+  __shared__ RowState rs;
+  __shared__ float red_f[kWarps * 2];
+  __shared__ int red_i[kWarps * 2];
+  __shared__ unsigned long long red_u[kWarps];
+  __shared__ X2 red_x[kWarps];
+  __shared__ float red_wb[kWarps * 2];
+  __shared__ int sh_csr[4];
+  __shared__ float sh_zth, sh_res;
+  __shared__ int sh_bstar, sh_nl;
+  __shared__ int sh_flags, sh_count, sh_digit, sh_none;
+  __shared__ unsigned long long sh_above;
 
   const cg::cluster_group cluster = cg::this_cluster();
   const clsample_args_t& a = P.a;
   const int C = P.C;
   const int chunk = P.chunk;
+  const int cap = P.cap;
   const int rank = (int)cluster.block_rank();
   const int row = (int)(blockIdx.x / (unsigned)C);
   const int V = a.V;
   const int c0 = rank * chunk;
-  const int c1 = min(V, c0 + chunk);
-  const int len = max(0, c1 - c0);
+  const int len = max(0, min(V, c0 + chunk) - c0);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const Smem S = carve(smem_raw, chunk);
+  const int nvec = chunk / 4;
+  constexpr int kEsize = kBF16 ? 2 : 4;
+  const Smem S = carve(smem_base, chunk, kEsize);
+  const Slice<kBF16> sl{S.raw};
+  const unsigned char* gsrc =
+      reinterpret_cast<const unsigned char*>(a.logits) + ((long long)row * a.logits_row_stride + c0) * kEsize;
+  const int32_t* bmrow = a.bitmask ? a.bitmask + (long long)row * a.bitmask_row_stride : nullptr;
+  const bool has_hist = a.hist_offs != nullptr;
+  const bool has_bias = a.bias_offs != nullptr;
+  const bool has_mod = has_hist || has_bias;
+  const uint32_t bulk_bytes = P.bulk_ok ? (uint32_t)(((size_t)len * kEsize) & ~(size_t)15) : 0u;
 
-  // ---- row parameters (validated identically by every CTA of the cluster)
+  // DSMEM may only be touched once every CTA of the cluster runs: arrive now, wait just
+  // before the first push.
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+
+  // ---- 0. the slice's bulk copy starts first; the row's small inputs are fetched in
+  //         parallel by different warps (one memory round trip)
   if (tid == 0) {
+    sh_flags = 0;
+    sh_count = 0;
+    mbar_init(&mbar_load, 1);
+    mbar_init(&mbar_gather, (uint32_t)C);
+    fence_mbar_init();
+    if (bulk_bytes) {
+      mbar_arrive_expect_tx(&mbar_load, bulk_bytes);
+      const uint32_t piece = ((bulk_bytes + kBulkPieces - 1) / kBulkPieces + 15u) & ~15u;
+      for (uint32_t off = 0; off < bulk_bytes; off += piece) {
+        const uint32_t sz = bulk_bytes - off < piece ? bulk_bytes - off : piece;
+        bulk_copy_g2s(S.raw + off, gsrc + off, sz, &mbar_load);
+      }
+    } else {
+      mbar_arrive_local(&mbar_load);
+    }
+  } else if (tid == 32) {
     RowParams q;
     q.T = a.temperatures ? a.temperatures[row] : 1.0f;
     q.k = a.top_ks ? a.top_ks[row] : -1;
@@ -490,8 +601,8 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_kernel(const LaunchParams
     q.rep = a.rep ? a.rep[row] : 1.0f;
     q.freq = a.freq ? a.freq[row] : 0.0f;
     q.pres = a.pres ? a.pres[row] : 0.0f;
-    q.seed = a.seeds ? a.seeds[row] : 0ull;
-    q.pos = a.positions ? a.positions[row] : a.step;
+    q.seed = a.seeds ? (unsigned long long)a.seeds[row] : 0ull;
+    q.pos = (unsigned long long)(a.positions ? a.positions[row] : a.step);
     int bad = 0;
     bad |= (q.T != q.T) || (q.T == INFINITY);
     bad |= (q.k < -1);
@@ -500,13 +611,23 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_kernel(const LaunchParams
     bad |= !(q.rep > 0.0f) || (q.rep == INFINITY) || !isfinite(q.freq) || !isfinite(q.pres);
     q.invalid = bad;
     rp = q;
-    sh_flags = 0;
-    sh_sel_err = 0;
+  } else if (tid == 64) {
+    sh_csr[0] = has_hist ? a.hist_offs[row] : 0;
+    sh_csr[1] = has_hist ? a.hist_offs[row + 1] : 0;
+    sh_csr[2] = has_bias ? a.bias_offs[row] : 0;
+    sh_csr[3] = has_bias ? a.bias_offs[row + 1] : 0;
   }
-  const bool has_hist = a.hist_offs != nullptr;
-  const bool has_bias = a.bias_offs != nullptr;
-  const bool has_mod = has_hist || has_bias;
-  for (int i = tid; i < chunk / 32; i += kThreads) S.modbits[i] = 0u;
+  // live words: allowed by the bitmask and inside the row
+  for (int w = tid; w < chunk / 32; w += kThreads) {
+    const int e = 32 * w;
+    uint32_t word = 0u;
+    if (e < len) {
+      word = bmrow ? (uint32_t)__ldg(bmrow + (c0 >> 5) + w) : 0xFFFFFFFFu;
+      const int rem = len - e;
+      if (rem < 32) word &= (1u << rem) - 1u;
+    }
+    S.live[w] = word;
+  }
   if (has_mod) {
     for (int i = tid; i < kHashCap; i += kThreads) {
       S.hkey[i] = kEmpty;
@@ -514,19 +635,41 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_kernel(const LaunchParams
       S.hbias[i] = -1;
     }
   }
+  for (int i = tid; i < 2 * 256; i += kThreads) {
+    S.mrg_c[i] = 0u;
+    S.mrg_w[i] = 0ull;
+  }
   __syncthreads();
 
-  // ---- penalised / biased ids of this slice: count history occurrences and keep the
-  //      last bias entry per id (SGLang page, "Why logit_bias is built from triples")
+  // ---- penalised / biased tokens of this slice (SGLang page, "Order semantics of the
+  //      penalties" and "Why logit_bias is built from triples": last duplicate wins)
   if (has_mod) {
     int flags = 0;
-    if (has_hist) {
-      const int lo = a.hist_offs[row], hi = a.hist_offs[row + 1];
-      if (lo < 0 || hi < lo) {
-        flags |= kFlagInvalid;
-      } else {
-        for (int j = lo + tid; j < hi; j += kThreads) {
-          const int id = __ldg(a.hist_ids + j);
+    const int c1 = c0 + len;
+    const int hlo = sh_csr[0], hhi = sh_csr[1], blo = sh_csr[2], bhi = sh_csr[3];
+    if (hlo < 0 || hhi < hlo || blo < 0 || bhi < blo) flags |= kFlagInvalid;
+    const bool hok = has_hist && hlo >= 0 && hhi >= hlo;
+    const bool bok = has_bias && blo >= 0 && bhi >= blo;
+    // this thread's first bias entry is fetched together with the history ids
+    const int bj0 = blo + tid;
+    int bid0 = INT_MIN;
+    float bval0 = 0.0f;
+    if (bok && bj0 < bhi) {
+      bid0 = __ldg(a.bias_ids + bj0);
+      bval0 = __ldg(a.bias_vals + bj0);
+    }
+    if (hok) {
+      for (int base = hlo; base < hhi; base += 8 * kThreads) {
+        int ids[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int j = base + u * kThreads + tid;
+          ids[u] = j < hhi ? __ldg(a.hist_ids + j) : INT_MIN;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int id = ids[u];
+          if (id == INT_MIN) continue;
           if (id < 0 || id >= V) {
             flags |= kFlagInvalid;
           } else if (id >= c0 && id < c1) {
@@ -537,345 +680,979 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_kernel(const LaunchParams
         }
       }
     }
-    if (has_bias) {
-      const int lo = a.bias_offs[row], hi = a.bias_offs[row + 1];
-      if (lo < 0 || hi < lo) {
-        flags |= kFlagInvalid;
-      } else {
-        for (int j = lo + tid; j < hi; j += kThreads) {
-          const int id = __ldg(a.bias_ids + j);
-          const float b = __ldg(a.bias_vals + j);
-          if (id < 0 || id >= V || b != b) {
-            flags |= kFlagInvalid;
-          } else if (id >= c0 && id < c1) {
-            const int slot = hash_insert(S.hkey, (uint32_t)(id - c0));
-            if (slot < 0) flags |= kFlagOverflow;
-            else atomicMax(&S.hbias[slot], j);
-          }
+    // bias: the largest entry index per id wins; its owner then stores the value
+    int myslot = -1;
+    if (bok) {
+      for (int j = bj0; j < bhi; j += kThreads) {
+        const int id = j == bj0 ? bid0 : __ldg(a.bias_ids + j);
+        const float b = j == bj0 ? bval0 : __ldg(a.bias_vals + j);
+        if (id < 0 || id >= V || b != b) {
+          flags |= kFlagInvalid;
+        } else if (id >= c0 && id < c1) {
+          const int slot = hash_insert(S.hkey, (uint32_t)(id - c0));
+          if (slot < 0) flags |= kFlagOverflow;
+          else atomicMax(&S.hbias[slot], j);
+          if (j == bj0) myslot = slot;
         }
       }
     }
     if (flags) atomicOr(&sh_flags, flags);
     __syncthreads();
-    for (int i = tid; i < kHashCap; i += kThreads) {
-      const uint32_t l = S.hkey[i];
-      if (l != kEmpty) atomicOr(&S.modbits[l >> 5], 1u << (l & 31));
+    if (bok) {
+      for (int j = bj0; j < bhi; j += kThreads) {
+        const int slot = j == bj0 ? myslot : -2;
+        if (j == bj0) {
+          if (slot >= 0 && S.hbias[slot] == j) S.hval[slot] = bval0;
+        } else {
+          const int id = __ldg(a.bias_ids + j);
+          if (id >= c0 && id < c1) {
+            for (int i = 0; i < kHashCap; ++i)
+              if (S.hkey[i] == (uint32_t)(id - c0) && S.hbias[i] == j) S.hval[i] = __ldg(a.bias_vals + j);
+          }
+        }
+      }
     }
-    __syncthreads();
   }
 
-  // ---- pass 1: load the slice once from HBM, sanitise, mask, keep it in shared
-  //      memory; per-thread max / argmax / online sum of 2^((z'-max)c) / count over
-  //      the tokens that are not penalised or biased
-  const RowParams q = rp;
-  const bool greedy_rule = (q.T < kGreedyEps) || q.k == 0 || q.k == 1;
-  const float Teff = (q.T >= kGreedyEps) ? q.T : 1.0f;
-  const float c_log2 = 1.4426950408889634f / Teff;  // log2(e) / T for the normaliser
-  float tm = -INFINITY, ts = 0.0f;
-  int targ = INT_MAX, tcnt = 0;
+  // ---- 1. the slice has landed (bounded wait); rows that are not 16-byte aligned and
+  //         the ragged tail come in with plain loads
+  if (!mbar_wait(&mbar_load, 0)) atomicOr(&sh_flags, kFlagTimeout);
   {
-    Loader ld;
-    ld.row = reinterpret_cast<const Elem*>(a.logits) + (long long)row * a.logits_row_stride + c0;
-    ld.len = len;
-    ld.vec = P.vec_ok != 0;
-    const int32_t* bmrow = a.bitmask ? a.bitmask + (long long)row * a.bitmask_row_stride : nullptr;
-    const int nvec = chunk / 4;
-    constexpr int U = 4;
-    float4* z4p = reinterpret_cast<float4*>(S.zs);
-    for (int base = 0; base < nvec; base += kThreads * U) {
-      float4 v[U];
+    const int done = (int)(bulk_bytes / kEsize);
+    for (int i = done + tid; i < len; i += kThreads) {
+      if (kBF16)
+        reinterpret_cast<uint16_t*>(S.raw)[i] = __ldg(reinterpret_cast<const unsigned short*>(gsrc) + i);
+      else
+        reinterpret_cast<float*>(S.raw)[i] = __ldg(reinterpret_cast<const float*>(gsrc) + i);
+    }
+  }
+  __syncthreads();
+  const RowParams q = rp;
+
+  // ---- 2. final z' of the penalised / biased tokens (the mask applies to them too);
+  //         then they leave the live set and are marked in `modbits` (the histogram
+  //         area is free until pass A ends), so pass A can fold them in token order
+  uint32_t* modbits = S.hist_c;
+  if (has_mod) {
+    for (int i = tid; i < chunk / 32; i += kThreads) modbits[i] = 0u;
+    for (int i = tid; i < kHashCap; i += kThreads) {
+      const uint32_t l = S.hkey[i];
+      if (l == kEmpty) continue;
+      float z = sanitize(sl.load1((int)l));
+      if (!((S.live[l >> 5] >> (l & 31)) & 1u)) z = -INFINITY;
+      const uint32_t cnt = S.hcnt[i];
+      if (cnt) z = apply_penalties(z, cnt, q.freq, q.pres, q.rep);
+      if (S.hbias[i] >= 0) z = __fadd_rn(z, S.hval[i]);
+      S.hval[i] = guard(z);
+    }
+    __syncthreads();
+    for (int i = tid; i < kHashCap; i += kThreads) {
+      const uint32_t l = S.hkey[i];
+      if (l == kEmpty) continue;
+      atomicAnd(&S.live[l >> 5], ~(1u << (l & 31)));
+      atomicOr(&modbits[l >> 5], 1u << (l & 31));
+    }
+  }
+  if (a.dbg_transformed) {
+    float* out = a.dbg_transformed + (long long)row * V + c0;
+    for (int i = tid; i < len; i += kThreads) {
+      const int g = c0 + i;
+      const bool allowed = !bmrow || (((uint32_t)__ldg(bmrow + (g >> 5)) >> (g & 31)) & 1u);
+      out[i] = allowed ? sanitize(sl.load1(i)) : -INFINITY;
+    }
+    __syncthreads();
+    if (has_mod)
+      for (int i = tid; i < kHashCap; i += kThreads)
+        if (S.hkey[i] != kEmpty) out[S.hkey[i]] = S.hval[i];
+  }
+  __syncthreads();
+
+  // ---- 3. pass A: max, lazy argmax and online sum of exp((z' - max) / T_eff)
+  const bool greedy = (q.T < kGreedyEps) || q.k == 0 || q.k == 1;
+  const float Teff = (q.T >= kGreedyEps) ? q.T : 1.0f;
+  const float cS = 1.4426950408889634f / Teff;
+  // values of tokens 4f..4f+3 for pass A: live -> sanitised raw, penalised / biased ->
+  // their final z' from the hash, otherwise -inf
+  auto pass_a_values = [&](int f, uint32_t wd, const float4& v, float* z) {
+    const uint32_t md = has_mod ? live4(modbits, f) : 0u;
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int f = base + u * kThreads + tid;
-        v[u] = (f < nvec && 4 * f < len) ? ld.load4(4 * f) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < 4; ++j) {
+      if ((wd >> j) & 1u) {
+        z[j] = sanitize(comp(v, j));
+      } else if ((md >> j) & 1u) {
+        const int slot = hash_find(S.hkey, (uint32_t)(4 * f + j));
+        z[j] = slot >= 0 ? S.hval[slot] : -INFINITY;
+      } else {
+        z[j] = -INFINITY;
       }
+    }
+  };
+  // one online state: running max, sum of 2^((z - max) cS), first float4 reaching max
+  struct OnlineState {
+    float m, s;
+    int f;
+  };
+  auto pass_a_step = [&](OnlineState& st, int f) {
+    const uint32_t wd = live4(S.live, f);
+    if (!wd && !(has_mod && live4(modbits, f))) return;
+    const float4 v = sl.load4(f);
+    float z[4];
+    if (wd == 0xFu && finite4(v)) {
+      z[0] = v.x;
+      z[1] = v.y;
+      z[2] = v.z;
+      z[3] = v.w;
+    } else {
+      pass_a_values(f, wd, v, z);
+    }
+    const float fm = fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3]));
+    if (!(fm > -INFINITY)) return;
+    if (fm > st.m) {
+      st.s *= ex2_approx((st.m - fm) * cS);
+      st.m = fm;
+      st.f = f;
+    }
+    const float e0 = ex2_approx((z[0] - st.m) * cS), e1 = ex2_approx((z[1] - st.m) * cS);
+    const float e2 = ex2_approx((z[2] - st.m) * cS), e3 = ex2_approx((z[3] - st.m) * cS);
+    st.s += (e0 + e1) + (e2 + e3);
+  };
+  OnlineState st0{-INFINITY, 0.0f, -1}, st1{-INFINITY, 0.0f, -1};
+  for (int f = tid; f < nvec; f += 2 * kThreads) {
+    pass_a_step(st0, f);
+    if (f + kThreads < nvec) pass_a_step(st1, f + kThreads);
+  }
+  float sm = fmaxf(st0.m, st1.m), ss = 0.0f;
+  if (sm > -INFINITY) ss = st0.s * ex2_approx((st0.m - sm) * cS) + st1.s * ex2_approx((st1.m - sm) * cS);
+  // this thread's lowest id reaching its max: rescan the first float4 of each state
+  int targ = INT_MAX;
+  for (int t = 0; t < 2; ++t) {
+    const OnlineState& st = t == 0 ? st0 : st1;
+    if (st.f < 0 || st.m != sm) continue;
+    float z[4];
+    pass_a_values(st.f, live4(S.live, st.f), sl.load4(st.f), z);
+    for (int j = 0; j < 4; ++j)
+      if (z[j] == sm) {
+        targ = min(targ, c0 + 4 * st.f + j);
+        break;
+      }
+  }
+  // warp-level lower bounds of the top-k cut from the per-thread maxima (disjoint
+  // groups): a warp's j-th largest group max guarantees j tokens at or above it
+  const bool topk_row = !greedy && !q.invalid && q.k >= 2;
+  float wlk = -INFINITY, wlkc = INFINITY;
+  if (topk_row) {
+    uint32_t key = fkey(sm);
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int f = base + u * kThreads + tid;
-        if (f >= nvec) continue;
-        const int e = 4 * f;
-        uint32_t allow = 0xFu;
-        if (e + 4 > len) allow = (e >= len) ? 0u : ((1u << (len - e)) - 1u);
-        if (bmrow && e < len) allow &= ((uint32_t)__ldg(bmrow + ((c0 + e) >> 5)) >> (e & 31)) & 0xFu;
-        const uint32_t mod = has_mod ? ((S.modbits[e >> 5] >> (e & 31)) & 0xFu) : 0u;
-        float zz[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-        float bm = -INFINITY;
-        int bi = INT_MAX;
+    for (int kk = 2; kk <= 32; kk <<= 1) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          zz[j] = ((allow >> j) & 1u) ? sanitize(zz[j]) : -INFINITY;
-          if (!((mod >> j) & 1u) && zz[j] > -INFINITY) {
-            ++tcnt;
-            if (zz[j] > bm) {
-              bm = zz[j];
-              bi = c0 + e + j;
-            }
-          }
-        }
-        z4p[f] = make_float4(zz[0], zz[1], zz[2], zz[3]);
-        if (bm > -INFINITY) {
-          if (better(bm, bi, tm, targ)) {
-            if (bm > tm) {
-              ts = ts * ex2_approx(__fmul_rn(tm - bm, c_log2));
-              tm = bm;
-            }
-            targ = bi;
-          }
+      for (int j = kk >> 1; j > 0; j >>= 1) {
+        const uint32_t other = __shfl_xor_sync(0xffffffffu, key, j);
+        const bool up = (lane & kk) == 0;
+        const bool lower = (lane & j) == 0;
+        key = (lower == up) ? min(key, other) : max(key, other);
+      }
+    }
+    // ascending across lanes: the j-th largest sits in lane 32 - j
+    const int k1 = q.k, k2 = (q.k + kWarps * C - 1) / (kWarps * C);
+    const uint32_t v1 = __shfl_sync(0xffffffffu, key, k1 <= 32 ? 32 - k1 : 0);
+    const uint32_t v2 = __shfl_sync(0xffffffffu, key, k2 <= 32 ? 32 - k2 : 0);
+    wlk = k1 <= 32 ? key_to_float(v1) : -INFINITY;
+    wlkc = k2 <= 32 ? key_to_float(v2) : -INFINITY;
+  }
+  // block reduction of (max, sum, argmax) and of the bounds
+  {
+    float m2 = sm, s2 = ss;
+    int a2 = targ;
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (!((mod >> j) & 1u)) ts += ex2_approx(__fmul_rn(zz[j] - tm, c_log2));
-        }
+    for (int d = 16; d > 0; d >>= 1) {
+      const float om = __shfl_xor_sync(0xffffffffu, m2, d);
+      const float os = __shfl_xor_sync(0xffffffffu, s2, d);
+      const int oa = __shfl_xor_sync(0xffffffffu, a2, d);
+      if (better(om, oa, m2, a2)) a2 = oa;
+      merge_ms(m2, s2, om, os, cS);
+    }
+    if (lane == 0) {
+      red_f[warp * 2] = m2;
+      red_f[warp * 2 + 1] = s2;
+      red_i[warp * 2] = a2;
+      red_wb[warp * 2] = wlk;
+      red_wb[warp * 2 + 1] = wlkc;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const bool in = lane < kWarps;
+      float m = in ? red_f[lane * 2] : -INFINITY, s = in ? red_f[lane * 2 + 1] : 0.0f;
+      int arg = in ? red_i[lane * 2] : INT_MAX;
+      float lk = in ? red_wb[lane * 2] : -INFINITY, lkc = in ? red_wb[lane * 2 + 1] : INFINITY;
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) {
+        const float om = __shfl_xor_sync(0xffffffffu, m, d);
+        const float os = __shfl_xor_sync(0xffffffffu, s, d);
+        const int oa = __shfl_xor_sync(0xffffffffu, arg, d);
+        if (better(om, oa, m, arg)) arg = oa;
+        merge_ms(m, s, om, os, cS);
+        lk = fmaxf(lk, __shfl_xor_sync(0xffffffffu, lk, d));
+        lkc = fminf(lkc, __shfl_xor_sync(0xffffffffu, lkc, d));
+      }
+      if (lane == 0) {
+        x1_mine.m = m;
+        x1_mine.s = s;
+        x1_mine.arg = arg;
+        x1_mine.lk = lk;
+        x1_mine.lkc = topk_row ? lkc : -INFINITY;
+        x1_mine.flags = sh_flags;
       }
     }
   }
   __syncthreads();
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+  push_all(cluster, x1, &x1_mine, rank, C);
+  cluster.sync();  // exchange 1
 
-  // ---- penalties, then bias, on the slice's listed ids (SGLang page, "Order semantics
-  //      of the penalties"); the mask was already applied and -inf stays -inf
-  if (has_mod) {
-    for (int i = tid; i < kHashCap; i += kThreads) {
-      const uint32_t l = S.hkey[i];
-      if (l == kEmpty) continue;
-      float z = S.zs[l];
-      const uint32_t cnt = S.hcnt[i];
-      if (cnt > 0u) {
-        z = __fsub_rn(z, __fmul_rn(q.freq, (float)cnt));
-        z = __fsub_rn(z, q.pres);
-        z = (z > 0.0f) ? __fdiv_rn(z, q.rep) : __fmul_rn(z, q.rep);
-      }
-      const int bj = S.hbias[i];
-      if (bj >= 0) z = __fadd_rn(z, __ldg(a.bias_vals + bj));
-      z = guard(z);
-      S.zs[l] = z;
-      if (z > -INFINITY) {
-        ++tcnt;
-        const int gid = c0 + (int)l;
-        if (better(z, gid, tm, targ)) {
-          if (z > tm) {
-            ts = ts * ex2_approx(__fmul_rn(tm - z, c_log2));
-            tm = z;
-          }
-          targ = gid;
-        }
-        ts += ex2_approx(__fmul_rn(z - tm, c_log2));
-      }
-    }
-    __syncthreads();
-  }
-
-  if (a.dbg_transformed) {
-    float* out = a.dbg_transformed + (long long)row * V + c0;
-    for (int i = tid; i < len; i += kThreads) out[i] = S.zs[i];
-  }
-
-  // ---- block reduction of (max, argmax, sum, count)
-  {
+  // ---- 4. row statistics, combined identically by every CTA
+  if (warp == 0) {
+    const bool in = lane < C;
+    const float lm = in ? x1[lane].m : -INFINITY;
+    const int la = in ? x1[lane].arg : INT_MAX;
+    float m = lm;
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
+    int arg = (in && lm == m) ? la : INT_MAX;
+    arg = warp_min_i(arg);
+    const float term = (in && lm > -INFINITY) ? x1[lane].s * ex2_approx((lm - m) * cS) : 0.0f;
+    float tot = 0.0f;  // fixed order (lanes 0..31): every CTA gets the same bits
+    for (int r = 0; r < 32; ++r) tot += __shfl_sync(0xffffffffu, term, r);
+    int fl = in ? x1[lane].flags : 0;
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) fl |= __shfl_xor_sync(0xffffffffu, fl, d);
+    float lk = in ? x1[lane].lk : -INFINITY;
+    float lkc = in ? x1[lane].lkc : INFINITY;
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) {
-      const float om = shfl_down(tm, d);
-      const float os = shfl_down(ts, d);
-      const int oa = shfl_down(targ, d);
-      const int oc = shfl_down(tcnt, d);
-      float m2 = tm, s2 = ts;
-      merge_ms(m2, s2, om, os, c_log2);
-      if (better(om, oa, tm, targ)) targ = oa;
-      tm = m2;
-      ts = s2;
-      tcnt += oc;
+      lk = fmaxf(lk, __shfl_xor_sync(0xffffffffu, lk, d));
+      lkc = fminf(lkc, __shfl_xor_sync(0xffffffffu, lkc, d));
     }
     if (lane == 0) {
-      red_f[warp * 4 + 0] = tm;
-      red_f[warp * 4 + 1] = ts;
-      red_i[warp * 4 + 0] = targ;
-      red_i[warp * 4 + 1] = tcnt;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      float m = -INFINITY, s = 0.0f;
-      int arg = INT_MAX, cnt = 0;
-      for (int w = 0; w < kWarps; ++w) {
-        const float wm = red_f[w * 4 + 0];
-        const int wa = red_i[w * 4 + 0];
-        if (better(wm, wa, m, arg)) arg = wa;
-        merge_ms(m, s, wm, red_f[w * 4 + 1], c_log2);
-        cnt += red_i[w * 4 + 1];
-      }
-      xchg.m = m;
-      xchg.arg = arg;
-      xchg.S = s;
-      xchg.ncand = cnt;
-      xchg.flags = sh_flags;
+      rs.m = m;
+      rs.arg = arg;
+      rs.S = tot;
+      rs.flags = fl;
+      rs.bound = fmaxf(lk, lkc);
     }
   }
-  cluster.sync();  // exchange 1: slice statistics
-
-  // ---- row statistics, combined in rank order by every CTA (identical results)
-  float m = -INFINITY, Ssum = 0.0f;
-  int arg = INT_MAX, ncand = 0, flags = 0;
-  for (int r = 0; r < C; ++r) {
-    const Exchange* x = cluster.map_shared_rank(&xchg, r);
-    const float xm = x->m;
-    const int xa = x->arg;
-    if (better(xm, xa, m, arg)) arg = xa;
-    merge_ms(m, Ssum, xm, x->S, c_log2);
-    ncand += x->ncand;
-    flags |= x->flags;
-  }
+  __syncthreads();
+  const float m = rs.m;
   int status = kRowOk;
-  if (q.invalid || (flags & kFlagInvalid) || ncand == 0) status = kRowInvalid;
-  else if (flags & kFlagOverflow) status = kRowOverflow;
-  const float lnS = logf(Ssum);
+  if (q.invalid || (rs.flags & kFlagInvalid) || !(m > -INFINITY)) status = kRowInvalid;
+  else if (rs.flags & (kFlagOverflow | kFlagTimeout)) status = kRowOverflow;
+  const float lnS = logf(rs.S);
 
-  if (status != kRowOk || greedy_rule) {
+  if (status != kRowOk || greedy) {
     if (rank == 0 && tid == 0) {
       const bool ok = status == kRowOk;
-      a.tokens[row] = ok ? arg : -1;
+      a.tokens[row] = ok ? rs.arg : -1;
       if (a.logprobs) a.logprobs[row] = ok ? -lnS : -INFINITY;  // y of the argmax is 0
       if (a.row_status) a.row_status[row] = status;
       if (a.dbg_kept_count) a.dbg_kept_count[row] = ok ? 1 : 0;
       if (a.dbg_cut) a.dbg_cut[row] = ok ? 0.0f : -INFINITY;
     }
-    cluster.sync();  // no CTA leaves while another may still read its shared memory
-    return;
+    if (rs.flags & kFlagTimeout) mbar_wait(&mbar_load, 0);
+    return;  // every remote access of this row happened before the barrier
   }
 
-  // ---- truncation thresholds on y = (z' - m) * (1/T)
+  // ---- 5. truncation plan.  y = (z' - m) * (1/T); K = {y >= cut} is an upper set.
   const float invT = __frcp_rn(q.T);
+  const float L = q.mp > 0.0f ? (float)log((double)q.mp) : -INFINITY;  // min-p: y >= ln(min_p)
+  const bool kfin = q.k >= 2;
+  enum { kFast, kTopP, kUntrunc, kSlow };
+  int plan = kSlow;
+  bool needW = false;
+  float theta = -INFINITY;
+  if (kfin && rs.bound > -INFINITY) {
+    plan = kFast;  // every token of S_k has y >= y(bound)
+    theta = y_of(rs.bound, m, invT);
+    if (q.p >= 1.0f) theta = fmaxf(theta, L);
+  } else if (q.mp > 0.0f && (q.p >= 1.0f || !kfin)) {
+    plan = kFast;  // K lies in {y >= ln min_p}
+    theta = L;
+    needW = q.p < 1.0f;  // top-p renormalises over the whole row
+  } else if (!kfin && q.p >= 1.0f) {
+    plan = kUntrunc;  // K = every allowed token
+  } else if (!kfin) {
+    plan = kTopP;  // top-p alone
+  }
+  const unsigned long long seed = q.seed, pos = q.pos;
+  Cand* cand = S.cand;
+
+  // ---- the leader's part after a gather: top-k -> top-p -> min-p and the race over
+  //      the candidates every CTA stored into its slot of the leader's raw slice
+  const Cand* G = reinterpret_cast<const Cand*>(S.raw);
+  const int span = C * cap;
+  const int lgcap = __ffs(cap) - 1;  // cap is a power of two
+  auto gvalid = [&](int i) -> bool { return i < span && (i & (cap - 1)) < x2[i >> lgcap].count; };
+  // radix select over the gathered set (entries with y >= ylo); see pick_digit
+  auto local_select = [&](bool weighted, float ylo, unsigned long long target, bool* found) -> float {
+    uint32_t prefix = 0u, pmask = 0u;
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      if (tid < 256) {
+        S.hist_c[tid] = 0u;
+        S.hist_w[tid] = 0ull;
+      }
+      __syncthreads();
+      for (int base = 0; base < span; base += kThreads) {
+        const int i = base + tid;
+        const bool ok = gvalid(i);
+        const float y = ok ? G[i].y : -INFINITY;
+        const uint32_t key = fkey(y);
+        const bool pred = ok && y >= ylo && (key & pmask) == prefix;
+        if (weighted)
+          hist_add<true>(S.hist_c, S.hist_w, pred, (key >> shift) & 0xFFu, pred ? weight_fx(y) : 0ull);
+        else
+          hist_add<false>(S.hist_c, S.hist_w, pred, (key >> shift) & 0xFFu, 0ull);
+      }
+      __syncthreads();
+      if (warp == 0) {
+        if (weighted) pick_digit(S.hist_w, target, &sh_digit, &sh_above, &sh_none);
+        else pick_digit(S.hist_c, target, &sh_digit, &sh_above, &sh_none);
+      }
+      __syncthreads();
+      if (sh_none) {
+        *found = false;
+        __syncthreads();
+        return -INFINITY;
+      }
+      prefix |= (uint32_t)sh_digit << shift;
+      pmask |= 0xFFu << shift;
+      target -= sh_above;
+      __syncthreads();
+    }
+    *found = true;
+    return key_to_float(prefix);
+  };
+  // Exact select over the gathered set, entries with y >= ylo, all within [lo, hi]:
+  // one 1024-bucket histogram (bucket order follows y), then the crossing bucket's
+  // entries are resolved by counting.  Sets *resolved = false when that bucket holds
+  // more than 1024 entries (heavy ties); the caller then uses local_select.
+  auto bucket_select = [&](bool weighted, float lo, float hi, float ylo, unsigned long long target,
+                           bool* found, bool* resolved) -> float {
+    unsigned long long* bk = reinterpret_cast<unsigned long long*>(S.hist_c);  // hist + mrg: 10 KB
+    const float scale = hi > lo ? 1024.0f / (hi - lo) : 0.0f;
+    auto bucket = [&](float y) -> int {
+      const int b = __float2int_rz(__fmul_rn(hi - y, scale));
+      return b < 0 ? 0 : (b > 1023 ? 1023 : b);
+    };
+    bk[2 * tid] = 0ull;
+    bk[2 * tid + 1] = 0ull;
+    if (tid == 0) {
+      sh_nl = 0;
+      sh_bstar = -1;
+    }
+    __syncthreads();
+    for (int i = tid; i < span; i += kThreads) {
+      if (!gvalid(i)) continue;
+      const float y = G[i].y;
+      if (!(y >= ylo)) continue;
+      atomicAdd(&bk[bucket(y)], weighted ? weight_fx(y) : 1ull);
+    }
+    __syncthreads();
+    {
+      const unsigned long long v0 = bk[2 * tid], v1 = bk[2 * tid + 1], loc = v0 + v1;
+      unsigned long long x = loc;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const unsigned long long o = __shfl_up_sync(0xffffffffu, x, d);
+        if (lane >= d) x += o;
+      }
+      if (lane == 31) red_u[warp] = x;
+      __syncthreads();
+      unsigned long long before = 0;
+      for (int w = 0; w < warp; ++w) before += red_u[w];
+      const unsigned long long excl = before + x - loc, incl = before + x;
+      if (excl < target && target <= incl) {
+        if (excl + v0 >= target) {
+          sh_bstar = 2 * tid;
+          sh_above = excl;
+        } else {
+          sh_bstar = 2 * tid + 1;
+          sh_above = excl + v0;
+        }
+      }
+    }
+    __syncthreads();
+    const int bstar = sh_bstar;
+    if (bstar < 0) {
+      *found = false;
+      *resolved = true;
+      return -INFINITY;
+    }
+    const unsigned long long t2 = target - sh_above;
+    // the crossing bucket's entries, gathered into the (now free) histogram area
+    Cand* Lb = reinterpret_cast<Cand*>(S.hist_c);
+    for (int i = tid; i < span; i += kThreads) {
+      if (!gvalid(i)) continue;
+      const Cand cd = G[i];
+      if (!(cd.y >= ylo) || bucket(cd.y) != bstar) continue;
+      const int p = atomicAdd(&sh_nl, 1);
+      if (p < 1024) Lb[p] = cd;
+    }
+    __syncthreads();
+    const int nl = sh_nl;
+    if (nl > 1024) {
+      *resolved = false;
+      *found = false;
+      __syncthreads();
+      return -INFINITY;
+    }
+    for (int i = tid; i < nl; i += kThreads) {
+      const float yi = Lb[i].y;
+      unsigned long long gt = 0, ge = 0;
+      for (int j = 0; j < nl; ++j) {
+        const float yj = Lb[j].y;
+        const unsigned long long wj = weighted ? weight_fx(yj) : 1ull;
+        if (yj > yi) gt += wj;
+        if (yj >= yi) ge += wj;
+      }
+      if (gt < t2 && t2 <= ge) sh_res = yi;
+    }
+    __syncthreads();
+    *found = true;
+    *resolved = true;
+    return sh_res;
+  };
+  // selects with the bucket method, falling back to the radix select
+  auto leader_select = [&](bool weighted, float lo, float hi, float ylo, unsigned long long target,
+                           bool* found) -> float {
+    bool resolved;
+    const float v = bucket_select(weighted, lo, hi, ylo, target, found, &resolved);
+    if (resolved) return v;
+    return local_select(weighted, ylo, target, found);
+  };
+  // every CTA stores its `count` candidates into slot `rank` of the leader's raw slice
+  // and arrives on the leader's gather barrier; only the leader continues
+  auto gather = [&](int count) -> bool {
+    Cand* dst = cluster.map_shared_rank(reinterpret_cast<Cand*>(S.raw), 0u) + rank * cap;
+    for (int i = tid; i < count; i += kThreads) dst[i] = cand[i];
+    __syncthreads();
+    if (tid == 0) mbar_arrive_remote(&mbar_gather, 0u);
+    if (rank != 0) return false;
+    if (tid == 0) sh_none = mbar_wait_cluster(&mbar_gather, 0) ? 0 : 1;
+    __syncthreads();
+    return true;
+  };
+  // appends (y, id) to the slice's candidate list; the whole warp calls it
+  auto append = [&](bool keep, float y, int id) {
+    const uint32_t bal = __ballot_sync(0xffffffffu, keep);
+    if (!bal) return;
+    const int leader = __ffs(bal) - 1;
+    int basepos = 0;
+    if (lane == leader) basepos = atomicAdd(&sh_count, __popc(bal));
+    basepos = __shfl_sync(0xffffffffu, basepos, leader);
+    if (keep) {
+      const int p = basepos + __popc(bal & ((1u << lane) - 1u));
+      if (p < cap) cand[p] = Cand{y, id};
+    }
+  };
+  auto finish_mine = [&](unsigned long long w, const Race& race) {
+    __syncthreads();
+    if (tid == 0) {
+      x2_mine.count = sh_count;
+      x2_mine.flags = sh_count > cap ? kFlagOverflow : 0;
+      x2_mine.w = w;
+      race.to(x2_mine);
+    }
+    __syncthreads();
+    push_all(cluster, x2, &x2_mine, rank, C);
+    cluster.sync();
+  };
+
+  if (plan == kFast || plan == kUntrunc) {
+    // ---- pass B: compaction at z >= zth (exact), or the whole race
+    if (warp == 0) {
+      const float zt = z_threshold_warp(theta, m, invT);
+      if (lane == 0) sh_zth = zt;
+    }
+    __syncthreads();
+    const float zth = sh_zth;
+    unsigned long long w = 0;
+    Race race;
+    race.init();
+    for (int base = 0; base < nvec; base += kThreads) {
+      const int f = base + tid;
+      const uint32_t wd = f < nvec ? live4(S.live, f) : 0u;
+      float z[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      if (wd) {
+        const float4 v = sl.load4(f);
+        if (wd == 0xFu && finite4(v)) {
+          z[0] = v.x;
+          z[1] = v.y;
+          z[2] = v.z;
+          z[3] = v.w;
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) z[j] = ((wd >> j) & 1u) ? sanitize(comp(v, j)) : -INFINITY;
+        }
+        if (needW) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (z[j] > -INFINITY) w += weight_fx(y_of(z[j], m, invT));
+        }
+        if (plan == kUntrunc) {
+          float y[4];
+          bool live_any = false, worth = false;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            y[j] = z[j] > -INFINITY ? y_of(z[j], m, invT) : -INFINITY;
+            if (z[j] > -INFINITY) {
+              live_any = true;
+              worth |= y[j] + kGumbelMax >= race.s;
+            }
+          }
+          if (worth) {
+            const uint4 x = race_words((uint32_t)((c0 >> 2) + f), seed, pos);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (z[j] > -INFINITY) race.add(y[j], c0 + 4 * f + j, pick_word(x, j));
+          } else if (live_any) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (z[j] > -INFINITY) race.count_only(y[j]);
+          }
+        }
+      }
+      if (plan == kFast) {
+        const bool any = __any_sync(0xffffffffu, z[0] >= zth || z[1] >= zth || z[2] >= zth || z[3] >= zth);
+        if (any) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const bool keep = z[j] > -INFINITY && z[j] >= zth;
+            append(keep, keep ? y_of(z[j], m, invT) : 0.0f, c0 + 4 * f + j);
+          }
+        }
+      }
+    }
+    if (has_mod) {
+      for (int base = 0; base < kHashCap; base += kThreads) {
+        const int i = base + tid;
+        float z = -INFINITY;
+        if (S.hkey[i] != kEmpty) z = S.hval[i];
+        const int g = c0 + (int)S.hkey[i];
+        const float y = z > -INFINITY ? y_of(z, m, invT) : -INFINITY;
+        if (z > -INFINITY) {
+          if (needW) w += weight_fx(y);
+          if (plan == kUntrunc) race.add(y, g, pick_word(race_words((uint32_t)(g >> 2), seed, pos), g & 3));
+        }
+        if (plan == kFast) append(z > -INFINITY && z >= zth, y, g);
+      }
+    }
+    if (needW) w = block_sum_u64(w, red_u);
+    if (plan == kUntrunc) block_reduce_race(race, red_x);
+    finish_mine(w, race);  // exchange 2
+
+    if (plan == kUntrunc) {
+      // the winner is the same in every CTA; its owner writes the outputs
+      if (tid == 0) {
+        Race r;
+        r.init();
+        for (int c = 0; c < C; ++c) r.merge(x2[c]);
+        const int owner = r.tok == INT_MAX ? 0 : r.tok / chunk;
+        if (rank == owner) write_sampled(a, row, r, lnS, true);
+      }
+      if (rs.flags & kFlagTimeout) mbar_wait(&mbar_load, 0);
+      return;
+    }
+
+    bool overflow = false;
+    for (int c = 0; c < C; ++c) overflow |= (x2[c].flags & kFlagOverflow) != 0;
+    if (!overflow) {
+      if (!gather(x2[rank].count)) {
+        if (rs.flags & kFlagTimeout) mbar_wait(&mbar_load, 0);
+        return;
+      }
+      const bool gathered = sh_none == 0;
+      int ntot = 0;
+      for (int c = 0; c < C; ++c) ntot += x2[c].count;
+      float tk = -INFINITY;
+      if (kfin && ntot >= q.k) {
+        bool found;
+        const float v = leader_select(false, theta, 0.0f, -INFINITY, (unsigned long long)q.k, &found);
+        if (found) tk = v;
+      }
+      float tp = -INFINITY;
+      if (q.p < 1.0f) {
+        unsigned long long mset = 0;
+        for (int i = tid; i < span; i += kThreads)
+          if (gvalid(i) && G[i].y >= tk) mset += weight_fx(G[i].y);
+        mset = block_sum_u64(mset, red_u);
+        unsigned long long Wk = mset;
+        if (!kfin) {
+          Wk = 0;
+          for (int c = 0; c < C; ++c) Wk += x2[c].w;
+        }
+        const unsigned long long cth = ceil_scaled(Wk, q.p);
+        if (mset >= cth) {
+          bool found;
+          const float v = leader_select(true, theta, 0.0f, tk, cth, &found);
+          if (found) tp = v;
+        }
+      }
+      const float cut = fmaxf(tk, fmaxf(tp, L));
+      Race race2;
+      race2.init();
+      for (int i = tid; i < span; i += kThreads) {
+        if (!gvalid(i)) continue;
+        const Cand cd = G[i];
+        if (!(cd.y >= cut)) continue;
+        race2.add(cd.y, cd.id, pick_word(race_words((uint32_t)(cd.id >> 2), seed, pos), cd.id & 3));
+      }
+      block_reduce_race(race2, red_x);
+      if (tid == 0) write_sampled(a, row, race2, lnS, gathered);
+      if (rs.flags & kFlagTimeout) mbar_wait(&mbar_load, 0);
+      return;
+    }
+  } else if (plan == kTopP) {
+    // ---- pass B': exact top-p mass of the row and its histogram over quarter-unit y
+    //      bins (warp-private, in the candidate area)
+    unsigned long long* whist = reinterpret_cast<unsigned long long*>(S.cand);
+    for (int i = tid; i < kWarps * kPBins; i += kThreads) whist[i] = 0ull;
+    __syncthreads();
+    unsigned long long w = 0;
+    unsigned long long* mine = whist + warp * kPBins;
+    for (int f = tid; f < nvec; f += kThreads) {
+      const uint32_t wd = live4(S.live, f);
+      if (!wd) continue;
+      const float4 v = sl.load4(f);
+      const bool fastv = wd == 0xFu && finite4(v);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float z = fastv ? comp(v, j) : (((wd >> j) & 1u) ? sanitize(comp(v, j)) : -INFINITY);
+        if (!(z > -INFINITY)) continue;
+        const float y = y_of(z, m, invT);
+        const unsigned long long qw = weight_fx(y);
+        if (!qw) continue;
+        w += qw;
+        atomicAdd(mine + pbin(y), qw);
+      }
+    }
+    if (has_mod) {
+      for (int i = tid; i < kHashCap; i += kThreads) {
+        if (S.hkey[i] == kEmpty) continue;
+        const float z = S.hval[i];
+        if (!(z > -INFINITY)) continue;
+        const float y = y_of(z, m, invT);
+        const unsigned long long qw = weight_fx(y);
+        if (!qw) continue;
+        w += qw;
+        atomicAdd(mine + pbin(y), qw);
+      }
+    }
+    w = block_sum_u64(w, red_u);
+    // merge the warp histograms and push them into every CTA's merged copy
+    if (tid < kPBins) {
+      unsigned long long t = 0;
+      for (int wp = 0; wp < kWarps; ++wp) t += whist[wp * kPBins + tid];
+      if (t)
+        for (int r = 0; r < C; ++r) atomicAdd(cluster.map_shared_rank(S.mrg_w + tid, (unsigned)r), t);
+    }
+    Race none_race;
+    none_race.init();
+    finish_mine(w, none_race);  // exchange 2
+    unsigned long long W = 0;
+    for (int c = 0; c < C; ++c) W += x2[c].w;
+    const unsigned long long cth = ceil_scaled(W, q.p);
+    // crossing bin: the running mass from the top first reaches cth in bin bstar
+    int bstar = kPBins - 1;
+    unsigned long long above = 0;
+    {
+      unsigned long long cum = 0;
+      for (int b = 0; b < kPBins; ++b) {
+        const unsigned long long nb = cum + S.mrg_w[b];
+        if (nb >= cth) {
+          bstar = b;
+          above = cum;
+          break;
+        }
+        cum = nb;
+      }
+    }
+    if (bstar < kPBins - 1) {
+      // ---- pass C: tokens above the crossing bin are certainly kept: race them here;
+      //      tokens of the crossing bin go to the leader
+      const float yhi = -(float)bstar * 0.25f, ylo = -(float)(bstar + 1) * 0.25f;
+      __syncthreads();
+      if (tid == 0) sh_count = 0;
+      __syncthreads();
+      Race race;
+      race.init();
+      for (int base = 0; base < nvec; base += kThreads) {
+        const int f = base + tid;
+        const uint32_t wd = f < nvec ? live4(S.live, f) : 0u;
+        float y[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (wd) {
+          const float4 v = sl.load4(f);
+          const bool fastv = wd == 0xFu && finite4(v);
+          bool worth = false;
+          uint32_t sure = 0u;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float z = fastv ? comp(v, j) : (((wd >> j) & 1u) ? sanitize(comp(v, j)) : -INFINITY);
+            if (!(z > -INFINITY)) continue;
+            y[j] = y_of(z, m, invT);
+            if (y[j] > yhi) {
+              sure |= 1u << j;
+              worth |= y[j] + kGumbelMax >= race.s;
+            }
+          }
+          if (sure) {
+            if (worth) {
+              const uint4 x = race_words((uint32_t)((c0 >> 2) + f), seed, pos);
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                if ((sure >> j) & 1u) race.add(y[j], c0 + 4 * f + j, pick_word(x, j));
+            } else {
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                if ((sure >> j) & 1u) race.count_only(y[j]);
+            }
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) append(y[j] > ylo && y[j] <= yhi, y[j], c0 + 4 * f + j);
+      }
+      if (has_mod) {
+        for (int base = 0; base < kHashCap; base += kThreads) {
+          const int i = base + tid;
+          float y = -INFINITY;
+          int g = 0;
+          if (S.hkey[i] != kEmpty && S.hval[i] > -INFINITY) {
+            y = y_of(S.hval[i], m, invT);
+            g = c0 + (int)S.hkey[i];
+            if (y > yhi) race.add(y, g, pick_word(race_words((uint32_t)(g >> 2), seed, pos), g & 3));
+          }
+          append(y > ylo && y <= yhi, y, g);
+        }
+      }
+      block_reduce_race(race, red_x);
+      finish_mine(0ull, race);  // exchange 3
+      bool overflow = false;
+      for (int c = 0; c < C; ++c) overflow |= (x2[c].flags & kFlagOverflow) != 0;
+      if (!overflow) {
+        if (!gather(x2[rank].count)) {
+          if (rs.flags & kFlagTimeout) mbar_wait(&mbar_load, 0);
+          return;
+        }
+        const bool gathered = sh_none == 0;
+        // the cut lies in the crossing bin: a weighted select over its tokens
+        bool found;
+        const float vstar = leader_select(true, ylo, yhi, -INFINITY, cth - above, &found);
+        Race race2;
+        race2.init();
+        for (int i = tid; i < span; i += kThreads) {
+          if (!gvalid(i)) continue;
+          const Cand cd = G[i];
+          if (!(cd.y >= vstar)) continue;
+          race2.add(cd.y, cd.id, pick_word(race_words((uint32_t)(cd.id >> 2), seed, pos), cd.id & 3));
+        }
+        block_reduce_race(race2, red_x);
+        if (tid == 0) {
+          for (int c = 0; c < C; ++c) race2.merge(x2[c]);
+          write_sampled(a, row, race2, lnS, gathered && found);
+        }
+        if (rs.flags & kFlagTimeout) mbar_wait(&mbar_load, 0);
+        return;
+      }
+    }
+    // the crossing bin is the open-ended last one, or the band overflowed: slow path
+  }
+
+  // ---- slow path: cluster-wide radix selects over the resident slices.  Histograms
+  //      are pushed into every CTA's merged copy with DSMEM atomics, one barrier per
+  //      digit; the merged copies are double-buffered and cleared after use.
+  for (int i = tid; i < 2 * 256; i += kThreads) {
+    S.mrg_c[i] = 0u;
+    S.mrg_w[i] = 0ull;
+  }
+  cluster.sync();  // every merged copy is clear before the first push
+  int gpass = 0;
+  auto cluster_select = [&](bool weighted, float ylo, unsigned long long target, bool* found) -> float {
+    uint32_t prefix = 0u, pmask = 0u;
+    bool ok_all = true;
+    for (int pass = 0; pass < 4; ++pass, ++gpass) {
+      const int shift = 24 - 8 * pass;
+      const int buf = gpass & 1;
+      if (tid < 256) {
+        S.hist_c[tid] = 0u;
+        S.hist_w[tid] = 0ull;
+      }
+      __syncthreads();
+      for (int base = 0; base < nvec; base += kThreads) {
+        const int f = base + tid;
+        const uint32_t wd = f < nvec ? live4(S.live, f) : 0u;
+        const float4 v = wd ? sl.load4(f) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          bool pred = false;
+          float y = -INFINITY;
+          if ((wd >> j) & 1u) {
+            const float z = sanitize(comp(v, j));
+            if (z > -INFINITY) {
+              y = y_of(z, m, invT);
+              pred = y >= ylo && (fkey(y) & pmask) == prefix;
+            }
+          }
+          const uint32_t digit = (fkey(y) >> shift) & 0xFFu;
+          if (weighted)
+            hist_add<true>(S.hist_c, S.hist_w, pred, digit, pred ? weight_fx(y) : 0ull);
+          else
+            hist_add<false>(S.hist_c, S.hist_w, pred, digit, 0ull);
+        }
+      }
+      if (has_mod) {
+        for (int base = 0; base < kHashCap; base += kThreads) {
+          const int i = base + tid;
+          bool pred = false;
+          float y = -INFINITY;
+          if (S.hkey[i] != kEmpty) {
+            const float z = S.hval[i];
+            if (z > -INFINITY) {
+              y = y_of(z, m, invT);
+              pred = y >= ylo && (fkey(y) & pmask) == prefix;
+            }
+          }
+          const uint32_t digit = (fkey(y) >> shift) & 0xFFu;
+          if (weighted)
+            hist_add<true>(S.hist_c, S.hist_w, pred, digit, pred ? weight_fx(y) : 0ull);
+          else
+            hist_add<false>(S.hist_c, S.hist_w, pred, digit, 0ull);
+        }
+      }
+      __syncthreads();
+      for (int i = tid; i < 256 * C; i += kThreads) {
+        const int bin = i & 255, r = i >> 8;
+        if (weighted) {
+          const unsigned long long hv = S.hist_w[bin];
+          if (hv) atomicAdd(cluster.map_shared_rank(S.mrg_w + buf * 256 + bin, (unsigned)r), hv);
+        } else {
+          const uint32_t hv = S.hist_c[bin];
+          if (hv) atomicAdd(cluster.map_shared_rank(S.mrg_c + buf * 256 + bin, (unsigned)r), hv);
+        }
+      }
+      cluster.sync();
+      if (warp == 0) {
+        if (weighted) pick_digit(S.mrg_w + buf * 256, target, &sh_digit, &sh_above, &sh_none);
+        else pick_digit(S.mrg_c + buf * 256, target, &sh_digit, &sh_above, &sh_none);
+      }
+      __syncthreads();
+      const bool none = sh_none != 0;
+      const int dg = sh_digit;
+      const unsigned long long ab = sh_above;
+      // clear this buffer for its next use (two passes later, after another barrier)
+      if (tid < 256) {
+        S.mrg_c[buf * 256 + tid] = 0u;
+        S.mrg_w[buf * 256 + tid] = 0ull;
+      }
+      __syncthreads();
+      if (none) ok_all = false;
+      if (ok_all) {
+        prefix |= (uint32_t)dg << shift;
+        pmask |= 0xFFu << shift;
+        target -= ab;
+      }
+    }
+    *found = ok_all;
+    return ok_all ? key_to_float(prefix) : -INFINITY;
+  };
+
   float tk = -INFINITY;
-  if (q.k >= 2 && q.k < ncand) {
-    const uint32_t key = cluster_select<false>(cluster, S, C, chunk, m, invT, -INFINITY,
-                                               (unsigned long long)q.k, &sh_sel_digit, &sh_sel_above,
-                                               &sh_sel_err);
-    tk = key_to_y(key);
+  if (kfin) {
+    bool found;
+    const float v = cluster_select(false, -INFINITY, (unsigned long long)q.k, &found);
+    if (found) tk = v;  // fewer than k candidates: top-k keeps them all
   }
   float tp = -INFINITY;
   if (q.p < 1.0f) {
-    // W_k: exact fixed-point mass of S_k (the candidates with y >= tk)
     unsigned long long w = 0;
-    const float4* z4p = reinterpret_cast<const float4*>(S.zs);
-    for (int f = tid; f < chunk / 4; f += kThreads) {
-      const float4 z4 = z4p[f];
-      const float zz[4] = {z4.x, z4.y, z4.z, z4.w};
+    for (int f = tid; f < nvec; f += kThreads) {
+      const uint32_t wd = live4(S.live, f);
+      if (!wd) continue;
+      const float4 v = sl.load4(f);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float y = y_of(zz[j], m, invT);
-        if (zz[j] > -INFINITY && y >= tk) w += weight_fx(y);
+        if (!((wd >> j) & 1u)) continue;
+        const float z = sanitize(comp(v, j));
+        if (!(z > -INFINITY)) continue;
+        const float y = y_of(z, m, invT);
+        if (y >= tk) w += weight_fx(y);
       }
     }
-    w = block_sum_u64(w, red_u64);
-    if (tid == 0) xchg.W = w;
-    cluster.sync();  // exchange 2: top-k mass
-    unsigned long long W = 0;
-    for (int r = 0; r < C; ++r) W += cluster.map_shared_rank(&xchg, r)->W;
-    const unsigned long long Cth = ceil_scaled(W, q.p);
-    const uint32_t key = cluster_select<true>(cluster, S, C, chunk, m, invT, tk, Cth, &sh_sel_digit,
-                                              &sh_sel_above, &sh_sel_err);
-    tp = key_to_y(key);
-  }
-  float tm_cut = -INFINITY;
-  if (q.mp > 0.0f) tm_cut = (float)log((double)q.mp);
-  const float cut = fmaxf(tk, fmaxf(tp, tm_cut));
-
-  // ---- exponential race over K = {candidates : y >= cut}
-  float bs = -INFINITY, ymin = INFINITY;
-  int btok = INT_MAX, kept = 0;
-  {
-    const uint2 key = make_uint2((uint32_t)q.seed, (uint32_t)(q.seed >> 32));
-    const uint32_t plo = (uint32_t)(unsigned long long)q.pos, phi = (uint32_t)((unsigned long long)q.pos >> 32);
-    const float4* z4p = reinterpret_cast<const float4*>(S.zs);
-    for (int f = tid; f < chunk / 4; f += kThreads) {
-      const float4 z4 = z4p[f];
-      const float zz[4] = {z4.x, z4.y, z4.z, z4.w};
-      float yy[4];
-      uint32_t keep = 0;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        yy[j] = y_of(zz[j], m, invT);
-        if (zz[j] > -INFINITY && yy[j] >= cut) keep |= 1u << j;
+    if (has_mod)
+      for (int i = tid; i < kHashCap; i += kThreads) {
+        if (S.hkey[i] == kEmpty) continue;
+        const float z = S.hval[i];
+        if (!(z > -INFINITY)) continue;
+        const float y = y_of(z, m, invT);
+        if (y >= tk) w += weight_fx(y);
       }
-      if (!keep) continue;
-      const int gid0 = c0 + 4 * f;
-      const uint4 x = philox4x32_10(make_uint4((uint32_t)(gid0 >> 2), plo, phi, 0u), key);
-      const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if (!((keep >> j) & 1u)) continue;
-        ++kept;
-        ymin = fminf(ymin, yy[j]);
-        const float s = race_score(yy[j], xw[j]);
-        if (better(s, gid0 + j, bs, btok)) {
-          bs = s;
-          btok = gid0 + j;
-        }
-      }
-    }
-#pragma unroll
-    for (int d = 16; d > 0; d >>= 1) {
-      const float os = shfl_down(bs, d);
-      const int ot = shfl_down(btok, d);
-      const int ok = shfl_down(kept, d);
-      const float oy = shfl_down(ymin, d);
-      if (better(os, ot, bs, btok)) {
-        bs = os;
-        btok = ot;
-      }
-      kept += ok;
-      ymin = fminf(ymin, oy);
-    }
-    if (lane == 0) {
-      red_f[warp * 4 + 2] = bs;
-      red_f[warp * 4 + 3] = ymin;
-      red_i[warp * 4 + 2] = btok;
-      red_i[warp * 4 + 3] = kept;
-    }
+    w = block_sum_u64(w, red_u);
+    if (tid == 0) x2_mine.w = w;
     __syncthreads();
-    if (tid == 0) {
-      float s = -INFINITY, yl = INFINITY;
-      int t = INT_MAX, kc = 0;
-      for (int w = 0; w < kWarps; ++w) {
-        if (better(red_f[w * 4 + 2], red_i[w * 4 + 2], s, t)) {
-          s = red_f[w * 4 + 2];
-          t = red_i[w * 4 + 2];
-        }
-        yl = fminf(yl, red_f[w * 4 + 3]);
-        kc += red_i[w * 4 + 3];
-      }
-      xchg.race_s = s;
-      xchg.race_tok = t;
-      xchg.kept = kc;
-      xchg.ymin = yl;
-    }
+    push_all(cluster, x2, &x2_mine, rank, C);
+    cluster.sync();
+    unsigned long long W = 0;
+    for (int c = 0; c < C; ++c) W += x2[c].w;
+    bool found;
+    const float v = cluster_select(true, tk, ceil_scaled(W, q.p), &found);
+    if (found) tp = v;
   }
-  cluster.sync();  // exchange 3: race winners
-  if (rank == 0 && tid == 0) {
-    float s = -INFINITY, yl = INFINITY;
-    int t = INT_MAX, kc = 0;
-    for (int r = 0; r < C; ++r) {
-      const Exchange* x = cluster.map_shared_rank(&xchg, r);
-      if (better(x->race_s, x->race_tok, s, t)) {
-        s = x->race_s;
-        t = x->race_tok;
-      }
-      yl = fminf(yl, x->ymin);
-      kc += x->kept;
+  const float cut = fmaxf(tk, fmaxf(tp, L));
+  Race race;
+  race.init();
+  for (int f = tid; f < nvec; f += kThreads) {
+    const uint32_t wd = live4(S.live, f);
+    if (!wd) continue;
+    const float4 v = sl.load4(f);
+    float y[4];
+    uint32_t keep = 0u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      y[j] = -INFINITY;
+      if (!((wd >> j) & 1u)) continue;
+      const float z = sanitize(comp(v, j));
+      if (!(z > -INFINITY)) continue;
+      y[j] = y_of(z, m, invT);
+      if (y[j] >= cut) keep |= 1u << j;
     }
-    const bool ok = (t != INT_MAX) && !sh_sel_err;
-    a.tokens[row] = ok ? t : -1;
-    if (a.logprobs) {
-      // y of the drawn token, recomputed from its transformed logit
-      float lp = -INFINITY;
-      if (ok) {
-        const int owner = t / chunk;
-        const float* zsr = cluster.map_shared_rank(S.zs, owner);
-        lp = y_of(zsr[t - owner * chunk], m, invT) - lnS;
-      }
-      a.logprobs[row] = lp;
-    }
-    if (a.row_status) a.row_status[row] = ok ? kRowOk : kRowOverflow;
-    if (a.dbg_kept_count) a.dbg_kept_count[row] = kc;
-    if (a.dbg_cut) a.dbg_cut[row] = yl;
+    if (!keep) continue;
+    const uint4 x = race_words((uint32_t)((c0 >> 2) + f), seed, pos);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if ((keep >> j) & 1u) race.add(y[j], c0 + 4 * f + j, pick_word(x, j));
   }
-  cluster.sync();  // keep every CTA's shared memory alive until rank 0 is done
+  if (has_mod)
+    for (int i = tid; i < kHashCap; i += kThreads) {
+      if (S.hkey[i] == kEmpty) continue;
+      const float z = S.hval[i];
+      if (!(z > -INFINITY)) continue;
+      const float y = y_of(z, m, invT);
+      if (!(y >= cut)) continue;
+      const int g = c0 + (int)S.hkey[i];
+      race.add(y, g, pick_word(race_words((uint32_t)(g >> 2), seed, pos), g & 3));
+    }
+  block_reduce_race(race, red_x);
+  __syncthreads();
+  if (tid == 0) race.to(x2_mine);
+  __syncthreads();
+  push_all(cluster, x2, &x2_mine, rank, C);
+  cluster.sync();
+  // the winner is the same in every CTA; its owner writes the outputs
+  if (tid == 0) {
+    Race r;
+    r.init();
+    for (int c = 0; c < C; ++c) r.merge(x2[c]);
+    const int owner = r.tok == INT_MAX ? 0 : r.tok / chunk;
+    if (rank == owner) write_sampled(a, row, r, lnS, true);
+  }
+  if (rs.flags & kFlagTimeout) mbar_wait(&mbar_load, 0);
 }
 
 // ---------------------------------------------------------------- diagnostics kernels
@@ -889,31 +1666,33 @@ __global__ void debug_uniforms_kernel(const uint64_t* seeds, const int64_t* pos,
                                       int n) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
-  const unsigned long long s = seeds[i], p = (unsigned long long)pos[i];
   const long long t = tok[i];
-  const uint4 x = philox4x32_10(make_uint4((uint32_t)((unsigned long long)t >> 2), (uint32_t)p, (uint32_t)(p >> 32), 0u),
-                                make_uint2((uint32_t)s, (uint32_t)(s >> 32)));
-  const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
-  u[i] = word_to_uniform(xw[t & 3]);
+  const uint4 x = race_words((uint32_t)((unsigned long long)t >> 2), seeds[i], (unsigned long long)pos[i]);
+  u[i] = word_to_uniform(pick_word(x, (int)(t & 3)));
 }
 
 // ---------------------------------------------------------------- host side
 
-Geometry geometry_for(int vocab) {
-  Geometry g{0, 0, 0};
+Geometry geometry_for(int vocab, int esize) {
+  Geometry g{0, 0, 0, 0};
   if (vocab <= 0) return g;
   int C = (vocab + 2047) / 2048;
   if (C > 8) C = 8;
   if (C < 1) C = 1;
   int chunk = ((vocab + C - 1) / C + 31) / 32 * 32;
-  if (smem_bytes_for(chunk) > 112 * 1024 && C == 8) {  // two CTAs per SM no longer fit
+  if (smem_bytes_for(chunk, 4) > 112 * 1024 && C == 8) {  // two CTAs per SM no longer fit
     C = kMaxCluster;
     chunk = ((vocab + C - 1) / C + 31) / 32 * 32;
   }
+  if (chunk > kMaxChunk) return g;  // C = 0: vocabulary too large
   g.C = C;
   g.chunk = chunk;
-  g.smem = (int)smem_bytes_for(chunk);
-  if (g.smem > 227 * 1024) g.C = 0;
+  g.smem = (int)smem_bytes_for(chunk, esize);
+  const int by_raw = (int)((size_t)chunk * esize / (sizeof(Cand) * C));
+  int cap = 1;  // largest power of two within both limits
+  while (cap * 2 <= by_raw && cap * 2 <= kCandCap) cap *= 2;
+  g.cap = cap;
+  if ((int)smem_bytes_for(chunk, 4) > 227 * 1024) g.C = 0;
   return g;
 }
 
@@ -923,7 +1702,7 @@ struct clsample_handle {
   int max_batch;
   int vocab;
   int device;
-  Geometry g;
+  Geometry g32, g16;
 };
 
 extern "C" {
@@ -943,7 +1722,7 @@ const char* clsample_strerror(int code) {
 }
 
 int clsample_geometry(int32_t vocab, int32_t* cluster, int32_t* chunk, int32_t* smem_bytes) {
-  const Geometry g = geometry_for(vocab);
+  const Geometry g = geometry_for(vocab, 4);
   if (g.C == 0) return CLSAMPLE_ERR_VOCAB;
   if (cluster) *cluster = g.C;
   if (chunk) *chunk = g.chunk;
@@ -955,8 +1734,8 @@ int clsample_create(int32_t max_batch, int32_t vocab, clsample_t** out) {
   if (!out) return CLSAMPLE_ERR_NULL;
   *out = nullptr;
   if (max_batch < 0) return CLSAMPLE_ERR_BATCH;
-  const Geometry g = geometry_for(vocab);
-  if (g.C == 0) return CLSAMPLE_ERR_VOCAB;
+  const Geometry g32 = geometry_for(vocab, 4), g16 = geometry_for(vocab, 2);
+  if (g32.C == 0) return CLSAMPLE_ERR_VOCAB;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return CLSAMPLE_ERR_CUDA;
   int major = 0, minor = 0, optin = 0;
@@ -965,25 +1744,43 @@ int clsample_create(int32_t max_batch, int32_t vocab, clsample_t** out) {
       cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
     return CLSAMPLE_ERR_CUDA;
   if (major != 10 || minor != 3) return CLSAMPLE_ERR_DEVICE;
-  if (g.smem > optin) return CLSAMPLE_ERR_VOCAB;
-  const void* kernels[2] = {reinterpret_cast<const void*>(&sampler_kernel<LoadF32, float>),
-                            reinterpret_cast<const void*>(&sampler_kernel<LoadBF16, uint16_t>)};
-  for (const void* k : kernels) {
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem) != cudaSuccess)
-      return CLSAMPLE_ERR_CUDA;
-    if (g.C > 8 && cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+  if (g32.smem > optin) return CLSAMPLE_ERR_VOCAB;
+  const void* k32 = reinterpret_cast<const void*>(&sampler_kernel<false>);
+  const void* k16 = reinterpret_cast<const void*>(&sampler_kernel<true>);
+  if (cudaFuncSetAttribute(k32, cudaFuncAttributeMaxDynamicSharedMemorySize, g32.smem) != cudaSuccess ||
+      cudaFuncSetAttribute(k16, cudaFuncAttributeMaxDynamicSharedMemorySize, g16.smem) != cudaSuccess)
+    return CLSAMPLE_ERR_CUDA;
+  if (g32.C > 8) {
+    if (cudaFuncSetAttribute(k32, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess ||
+        cudaFuncSetAttribute(k16, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
       return CLSAMPLE_ERR_CUDA;
   }
   clsample_t* h = new clsample_t;
   h->max_batch = max_batch;
   h->vocab = vocab;
   h->device = dev;
-  h->g = g;
+  h->g32 = g32;
+  h->g16 = g16;
   *out = h;
   return CLSAMPLE_SUCCESS;
 }
 
 void clsample_destroy(clsample_t* h) { delete h; }
+
+static void fill_launch(const Geometry& g, unsigned nclusters, cudaStream_t stream, cudaLaunchConfig_t* cfg,
+                        cudaLaunchAttribute* attr) {
+  std::memset(cfg, 0, sizeof *cfg);
+  cfg->gridDim = dim3(nclusters * (unsigned)g.C, 1, 1);
+  cfg->blockDim = dim3(kThreads, 1, 1);
+  cfg->dynamicSmemBytes = (size_t)g.smem;
+  cfg->stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)g.C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg->attrs = attr;
+  cfg->numAttrs = 1;
+}
 
 int clsample_apply(clsample_t* h, const clsample_args_t* a, clsample_stream_t stream) {
   if (!h || !a) return CLSAMPLE_ERR_NULL;
@@ -1000,35 +1797,38 @@ int clsample_apply(clsample_t* h, const clsample_args_t* a, clsample_stream_t st
   if (cudaGetDevice(&dev) != cudaSuccess) return CLSAMPLE_ERR_CUDA;
   if (dev != h->device) return CLSAMPLE_ERR_DEVICE;
 
+  const bool bf16 = a->logits_dtype == CLSAMPLE_LOGITS_BF16;
+  const Geometry& g = bf16 ? h->g16 : h->g32;
+  const int esize = bf16 ? 2 : 4;
   LaunchParams P;
   P.a = *a;
-  P.C = h->g.C;
-  P.chunk = h->g.chunk;
+  P.C = g.C;
+  P.chunk = g.chunk;
+  P.cap = g.cap;
   const uintptr_t base = reinterpret_cast<uintptr_t>(a->logits);
-  if (a->logits_dtype == CLSAMPLE_LOGITS_F32)
-    P.vec_ok = (base % 16 == 0) && (a->logits_row_stride % 4 == 0);
-  else
-    P.vec_ok = (base % 8 == 0) && (a->logits_row_stride % 4 == 0);
+  P.bulk_ok = (base % 16 == 0) && (((long long)a->logits_row_stride * esize) % 16 == 0);
 
   cudaLaunchConfig_t cfg;
-  std::memset(&cfg, 0, sizeof cfg);
-  cfg.gridDim = dim3((unsigned)a->B * (unsigned)P.C, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = (size_t)h->g.smem;
-  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)P.C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t err;
-  if (a->logits_dtype == CLSAMPLE_LOGITS_F32)
-    err = cudaLaunchKernelEx(&cfg, sampler_kernel<LoadF32, float>, P);
-  else
-    err = cudaLaunchKernelEx(&cfg, sampler_kernel<LoadBF16, uint16_t>, P);
+  fill_launch(g, (unsigned)a->B, reinterpret_cast<cudaStream_t>(stream), &cfg, attr);
+  const cudaError_t err = bf16 ? cudaLaunchKernelEx(&cfg, sampler_kernel<true>, P)
+                               : cudaLaunchKernelEx(&cfg, sampler_kernel<false>, P);
   return err == cudaSuccess ? CLSAMPLE_SUCCESS : CLSAMPLE_ERR_CUDA;
+}
+
+int clsample_occupancy(clsample_t* h, int32_t logits_dtype, int32_t* max_active_clusters) {
+  if (!h || !max_active_clusters) return CLSAMPLE_ERR_NULL;
+  if (logits_dtype != CLSAMPLE_LOGITS_F32 && logits_dtype != CLSAMPLE_LOGITS_BF16) return CLSAMPLE_ERR_DTYPE;
+  const bool bf16 = logits_dtype == CLSAMPLE_LOGITS_BF16;
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  fill_launch(bf16 ? h->g16 : h->g32, 1u, nullptr, &cfg, attr);
+  int n = 0;
+  const cudaError_t err = bf16 ? cudaOccupancyMaxActiveClusters(&n, sampler_kernel<true>, &cfg)
+                               : cudaOccupancyMaxActiveClusters(&n, sampler_kernel<false>, &cfg);
+  if (err != cudaSuccess) return CLSAMPLE_ERR_CUDA;
+  *max_active_clusters = n;
+  return CLSAMPLE_SUCCESS;
 }
 
 int clsample_debug_weights(const float* y, uint64_t* w, int32_t n, clsample_stream_t stream) {

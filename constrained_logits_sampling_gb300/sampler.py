@@ -42,7 +42,7 @@ class Args(ctypes.Structure):
 
 
 EXPORTS = ("clsample_create", "clsample_destroy", "clsample_apply", "clsample_strerror",
-           "clsample_geometry", "clsample_debug_weights", "clsample_debug_uniforms")
+           "clsample_geometry", "clsample_occupancy", "clsample_debug_weights", "clsample_debug_uniforms")
 
 
 def load_library(path: str = LIB_PATH):
@@ -65,6 +65,8 @@ def load_library(path: str = LIB_PATH):
             L.clsample_geometry.argtypes = [ctypes.c_int32, ctypes.POINTER(ctypes.c_int32),
                                             ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]
             L.clsample_geometry.restype = ctypes.c_int
+            L.clsample_occupancy.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]
+            L.clsample_occupancy.restype = ctypes.c_int
             L.clsample_debug_weights.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]
             L.clsample_debug_weights.restype = ctypes.c_int
             L.clsample_debug_uniforms.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int32, ctypes.c_void_p]
@@ -125,6 +127,11 @@ class Sampler:
         _check(self._L.clsample_create(int(max_batch), int(vocab), ctypes.byref(h)))
         self._h = h
         self.max_batch, self.vocab = int(max_batch), int(vocab)
+
+    def max_active_clusters(self, bf16: bool = False) -> int:
+        n = ctypes.c_int32()
+        _check(self._L.clsample_occupancy(self._h, LOGITS_BF16 if bf16 else LOGITS_F32, ctypes.byref(n)))
+        return n.value
 
     def close(self):
         if getattr(self, "_h", None):

@@ -160,6 +160,10 @@ const char* clsample_strerror(int code);
  * needs no GPU.  Returns CLSAMPLE_SUCCESS or CLSAMPLE_ERR_VOCAB. */
 int clsample_geometry(int32_t vocab, int32_t* cluster, int32_t* chunk, int32_t* smem_bytes);
 
+/* How many thread-block clusters (rows) of this handle's launch can be resident on the
+ * device at once, from cudaOccupancyMaxActiveClusters.  Needs the handle's device. */
+int clsample_occupancy(clsample_t* handle, int32_t logits_dtype, int32_t* max_active_clusters);
+
 /* Diagnostics of the building blocks, on device arrays of length n (enqueued on
  * `stream`): the fixed-point top-p weight floor(exp32(y) * 2^40) of each y (y <= 0),
  * and the race uniform U of (seed, position, token).  They run the same device code

@@ -235,3 +235,34 @@ def test_batch_composition_independence_gpu():
     assert np.array_equal(g2["logprobs"], g["logprobs"][perm])
     g3 = run_gpu(b.rows([5, 5, 17]), debug=False)
     assert list(g3["tokens"]) == [g["tokens"][5], g["tokens"][5], g["tokens"][17]]
+
+
+# ----------------------------------------------------------------------------- every route of the kernel
+
+def test_routes_and_fallbacks():
+    """Rows that take each route: bounded top-k, min-p compaction (with and without
+    top-p), top-p alone (crossing bin resolved by the leader), top-p whose crossing bin
+    overflows (flat row) or is the open-ended last bin, top-k with k > 4096 (no bound:
+    cluster-wide radix select), and the untruncated race."""
+    V = 151936
+    rng = np.random.default_rng(21)
+    rows, params = [], []
+    base = (rng.standard_normal(V) * 3).astype(F32)
+    flat = np.zeros(V, F32)
+    spike = np.full(V, -20.0, F32)
+    spike[777] = 0.0
+    cases = [
+        (base, 1.0, 50, 1.0, 0.0), (base, 0.9, 1000, 0.9, 0.0), (base, 0.7, -1, 1.0, 0.05),
+        (base, 1.1, -1, 0.8, 0.05), (base, 1.0, -1, 0.9, 0.0), (base, 0.6, -1, 0.5, 0.0),
+        (flat, 1.0, -1, 0.5, 0.0), (spike, 1.0, -1, 0.9999, 0.0), (base, 1.0, 5000, 1.0, 0.0),
+        (base, 1.0, 6000, 0.9, 0.0), (base, 1.2, -1, 1.0, 0.0), (flat, 1.0, 20, 0.9, 0.0),
+    ]
+    for z, T, k, p, mp in cases:
+        rows.append(z)
+        params.append((T, k, p, mp))
+    B = len(rows)
+    b = small(np.stack(rows), temperatures=np.array([c[0] for c in params], F32),
+              top_ks=np.array([c[1] for c in params], np.int32), top_ps=np.array([c[2] for c in params], F32),
+              min_ps=np.array([c[3] for c in params], F32), seeds=np.arange(B, dtype=np.uint64) + 5,
+              positions=np.arange(B, dtype=np.int64) * 11)
+    compare(b, run_gpu(b), run_oracle(b), name="routes")

@@ -36,7 +36,7 @@ FALLBACK_HBM_GBS = 6800.0
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--steps", type=int, default=1000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", type=int, default=WORKLOAD)
@@ -63,9 +63,13 @@ def peaks():
 
 
 def kernel_source_hash():
+    """Hash of the CUDA sources and the C header (ties a committed ncu traffic figure
+    to the kernel it was measured on)."""
     h = hashlib.sha256()
-    for p in ("constrained_logits_sampling_gb300/csrc/clsample.cu", "include/clsample.h"):
-        with open(os.path.join(ROOT, p), "rb") as f:
+    csrc = os.path.join(ROOT, "constrained_logits_sampling_gb300", "csrc")
+    paths = sorted(os.path.join(csrc, n) for n in os.listdir(csrc) if n.endswith((".cu", ".cuh")))
+    for p in paths + [os.path.join(ROOT, "include", "clsample.h")]:
+        with open(p, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
@@ -85,7 +89,7 @@ def traffic_from_profile(workload_name):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons, sampled every 20 ms."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -100,7 +104,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
         except Exception:
@@ -228,7 +232,7 @@ def main():
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     clocks = ClockSampler(local)
     clocks.start()
-    time.sleep(0.3)
+    time.sleep(0.2)  # nvidia-smi's first sample lands before the timed region starts
     barrier()
     t_all0 = torch.cuda.Event(enable_timing=True)
     t_all1 = torch.cuda.Event(enable_timing=True)
@@ -239,13 +243,6 @@ def main():
         ends[i].record(stream)
     t_all1.record(stream)
     barrier()
-    # keep the GPU busy while the clock sampler catches up on a long-enough window
-    extra = 0
-    t_end = time.perf_counter() + 1.0
-    while time.perf_counter() < t_end:
-        s.apply(sets[extra % N_SETS][0], stream)
-        extra += 1
-    torch.cuda.synchronize()
     clk = clocks.stop()
     launch_ms = [a.elapsed_time(e) for a, e in zip(starts, ends)]
     total_ms = t_all0.elapsed_time(t_all1)

@@ -716,7 +716,8 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_kernel(const LaunchParams
 
   // ---- 1. the slice has landed (bounded wait); rows that are not 16-byte aligned and
   //         the ragged tail come in with plain loads
-  if (!mbar_wait(&mbar_load, 0)) atomicOr(&sh_flags, kFlagTimeout);
+  // one thread polls; the others sleep in the block barrier below
+  if (tid == 0 && !mbar_wait(&mbar_load, 0)) atomicOr(&sh_flags, kFlagTimeout);
   {
     const int done = (int)(bulk_bytes / kEsize);
     for (int i = done + tid; i < len; i += kThreads) {
@@ -727,6 +728,8 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_kernel(const LaunchParams
     }
   }
   __syncthreads();
+  // the phase is complete: one poll gives every thread its own acquire of the copy
+  (void)mbar_try_wait(&mbar_load, 0);
   const RowParams q = rp;
 
   // ---- 2. final z' of the penalised / biased tokens (the mask applies to them too);
@@ -956,7 +959,7 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_kernel(const LaunchParams
       if (a.dbg_kept_count) a.dbg_kept_count[row] = ok ? 1 : 0;
       if (a.dbg_cut) a.dbg_cut[row] = ok ? 0.0f : -INFINITY;
     }
-    if (rs.flags & kFlagTimeout) mbar_wait(&mbar_load, 0);
+    if ((rs.flags & kFlagTimeout) && tid == 0) mbar_wait(&mbar_load, 0);
     return;  // every remote access of this row happened before the barrier
   }
 
@@ -1138,6 +1141,7 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_kernel(const LaunchParams
     if (rank != 0) return false;
     if (tid == 0) sh_none = mbar_wait_cluster(&mbar_gather, 0) ? 0 : 1;
     __syncthreads();
+    (void)mbar_try_wait_cluster(&mbar_gather, 0);  // every thread acquires the peers' stores
     return true;
   };
   // appends (y, id) to the slice's candidate list; the whole warp calls it
@@ -1258,7 +1262,7 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_kernel(const LaunchParams
         const int owner = r.tok == INT_MAX ? 0 : r.tok / chunk;
         if (rank == owner) write_sampled(a, row, r, lnS, true);
       }
-      if (rs.flags & kFlagTimeout) mbar_wait(&mbar_load, 0);
+      if ((rs.flags & kFlagTimeout) && tid == 0) mbar_wait(&mbar_load, 0);
       return;
     }
 
@@ -1266,7 +1270,7 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_kernel(const LaunchParams
     for (int c = 0; c < C; ++c) overflow |= (x2[c].flags & kFlagOverflow) != 0;
     if (!overflow) {
       if (!gather(x2[rank].count)) {
-        if (rs.flags & kFlagTimeout) mbar_wait(&mbar_load, 0);
+        if ((rs.flags & kFlagTimeout) && tid == 0) mbar_wait(&mbar_load, 0);
         return;
       }
       const bool gathered = sh_none == 0;
@@ -1307,7 +1311,7 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_kernel(const LaunchParams
       }
       block_reduce_race(race2, red_x);
       if (tid == 0) write_sampled(a, row, race2, lnS, gathered);
-      if (rs.flags & kFlagTimeout) mbar_wait(&mbar_load, 0);
+      if ((rs.flags & kFlagTimeout) && tid == 0) mbar_wait(&mbar_load, 0);
       return;
     }
   } else if (plan == kTopP) {
@@ -1438,7 +1442,7 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_kernel(const LaunchParams
       for (int c = 0; c < C; ++c) overflow |= (x2[c].flags & kFlagOverflow) != 0;
       if (!overflow) {
         if (!gather(x2[rank].count)) {
-          if (rs.flags & kFlagTimeout) mbar_wait(&mbar_load, 0);
+          if ((rs.flags & kFlagTimeout) && tid == 0) mbar_wait(&mbar_load, 0);
           return;
         }
         const bool gathered = sh_none == 0;
@@ -1458,7 +1462,7 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_kernel(const LaunchParams
           for (int c = 0; c < C; ++c) race2.merge(x2[c]);
           write_sampled(a, row, race2, lnS, gathered && found);
         }
-        if (rs.flags & kFlagTimeout) mbar_wait(&mbar_load, 0);
+        if ((rs.flags & kFlagTimeout) && tid == 0) mbar_wait(&mbar_load, 0);
         return;
       }
     }
@@ -1652,7 +1656,7 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_kernel(const LaunchParams
     const int owner = r.tok == INT_MAX ? 0 : r.tok / chunk;
     if (rank == owner) write_sampled(a, row, r, lnS, true);
   }
-  if (rs.flags & kFlagTimeout) mbar_wait(&mbar_load, 0);
+  if ((rs.flags & kFlagTimeout) && tid == 0) mbar_wait(&mbar_load, 0);
 }
 
 // ---------------------------------------------------------------- diagnostics kernels

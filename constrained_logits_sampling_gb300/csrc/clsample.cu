@@ -2,26 +2,30 @@
 //
 // One thread-block cluster samples one row.  The row's V logits are split into C
 // contiguous slices (a multiple of 32 tokens, so that every CTA owns whole bitmask
-// words).  Each CTA pulls its slice into shared memory with a single TMA bulk copy
-// issued at entry, so the whole slice is in flight while the CTA reads the row's token
-// history and logit_bias lists; HBM sees every logit exactly once and nothing but the
+// words), one per CTA.  A CTA keeps only small tables in shared memory (about 51 KB), so
+// four CTAs share an SM and about 76 rows are in flight at once.  Logits move only
+// through the TMA unit: every pass over the slice streams it through a 4-stage ring of
+// 4 KB shared-memory buffers filled by bulk copies (cp.async.bulk) that complete on
+// mbarriers, so the SM's load/store queues stay free for shared-memory work, shuffles and
+// DSMEM.  The first pass reads HBM; later passes find the slice in L2.  Nothing but the
 // per-row outputs is written back.
 //
 //   pass A    sanitise + mask + penalties/bias (the few penalised tokens live in a small
-//             hash with their final value), slice max, lowest argmax and an online sum of
-//             exp((z' - max)/T); per-thread maxima give a lower bound of the top-k cut.
+//             hash and get their final value on the way), slice max, lowest argmax and an
+//             online sum of exp((z' - max)/T); per-thread maxima bound the top-k cut.
 //   exchange  every CTA pushes its slice statistics into every CTA's shared memory
 //             (DSMEM) and one cluster barrier publishes them.  Greedy rows end here.
 //   pass B    the tokens that can survive truncation (y >= a provable bound) are
 //             compacted; a leader CTA gathers them (DSMEM stores + a remote mbarrier
 //             arrive) and finishes top-k -> top-p -> min-p and the exponential race alone.
-//   slow path rows without a usable bound (top-p alone, very large k, compaction
-//             overflow) run cluster-wide radix selects over the resident slices.
+//   slow path rows without a usable bound (very large k, compaction overflow) run
+//             cluster-wide radix selects, one pass over the slice per digit.
 //
-// The arithmetic that decides integers (kept set, drawn id) is exact and identical on
-// any IEEE machine (sampler_math.cuh).  Page references: "SGLang source teardown (10):
-// Sampling, Grammar and structured output" (SGLang page) and "GLM-5.3 inference (7):
-// output side" (GLM page).
+// Cold, bulky steps are out-of-line functions so that the instruction stream of the hot
+// path stays small.  The arithmetic that decides integers (kept set, drawn id) is exact
+// and identical on any IEEE machine (sampler_math.cuh).  Page references: "SGLang source
+// teardown (10): Sampling, Grammar and structured output" (SGLang page) and "GLM-5.3
+// inference (7): output side" (GLM page).
 
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
@@ -42,27 +46,27 @@ namespace {
 
 using namespace clsample;
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kHashCap = 1024;   // distinct penalised / biased ids per slice
-constexpr int kCandCap = 512;    // compacted candidates per slice
-constexpr int kMaxCluster = 16;
+constexpr int kMinBlocks = 4;      // CTAs per SM the register budget is sized for
+constexpr int kHashCap = 1024;     // distinct penalised / biased ids per slice
+constexpr int kCandCap = 512;      // compacted candidates per slice
+constexpr int kMaxCluster = 8;     // portable cluster size
+constexpr int kGatherCap = kCandCap * kMaxCluster;
+constexpr int kMaxChunk = 32 * 1024;  // longest slice
+constexpr int kStageBytes = 4096;     // one ring stage: one 16-byte vector per thread
+constexpr int kStages = 4;            // ring depth
 constexpr uint32_t kEmpty = 0xFFFFFFFFu;
-// The slice's bulk copy is issued as this many TMA copies (all on one mbarrier).
-#ifndef CLSAMPLE_BULK_PIECES
-#define CLSAMPLE_BULK_PIECES 1
-#endif
-constexpr int kBulkPieces = CLSAMPLE_BULK_PIECES;
-// Longest slice: pass A keeps a bit per token of the slice in the histogram area.
-constexpr int kMaxChunk = 32 * 1024;
+constexpr uint32_t kAllowedBit = 0x80000000u;  // in hcnt: the bitmask allows the token
 
 enum : int { kRowOk = 0, kRowOverflow = 1, kRowInvalid = 2 };
-enum : int { kFlagInvalid = 1, kFlagOverflow = 2, kFlagTimeout = 4 };
+enum : int { kFlagInvalid = 1, kFlagOverflow = 2, kFlagRing = 4 };  // kFlagRing: a ring stage never landed
+enum : int { kPlanFast = 0, kPlanTopP = 1, kPlanUntrunc = 2, kPlanSlow = 3 };
 
 struct Geometry {
   int C;      // CTAs per row (cluster size)
   int chunk;  // tokens per CTA, multiple of 32
-  int smem;   // dynamic shared memory per CTA for this element size
+  int smem;   // dynamic shared memory per CTA
   int cap;    // compacted candidates per CTA the leader can gather
 };
 
@@ -71,7 +75,7 @@ struct LaunchParams {
   int C;
   int chunk;
   int cap;
-  int bulk_ok;  // every row start is 16-byte aligned: the slice can be bulk-copied
+  int vec_ok;  // every row start is 16-byte aligned: slices stream through the TMA ring
 };
 
 struct Cand {
@@ -86,7 +90,7 @@ struct X1 {
   float s;      // sum over the slice's candidates of 2^((z' - m) * log2(e) / T)
   int flags;    // kFlag*
   float lk;     // max over warps of the warp's k-th largest thread max of z' (-inf: unknown)
-  float lkc;    // min over warps of the ceil(k / (16 C))-th largest thread max (-inf: unknown)
+  float lkc;    // min over warps of the ceil(k / (kWarps C))-th largest thread max
 };
 
 // Slice results pushed to every CTA after pass B (and by the slow path).
@@ -109,114 +113,208 @@ struct RowParams {
   int invalid;
 };
 
+// Row statistics and the truncation plan, identical in every CTA after exchange 1.
 struct RowState {
-  float m;
-  int arg;
-  float S;
+  float m;      // max z'
+  int arg;      // lowest id reaching it
+  float S;      // sum of 2^((z' - m) cS)
   int flags;
   float bound;  // lower bound of the k-th largest z' (-inf if none)
+  float lnS;
+  float invT;
+  float L;      // min-p cut in y: ln(min_p), or -inf
+  float theta;  // lower bound of the kept set in y (kPlanFast)
+  int plan;
+  int needW;    // kPlanFast: the top-p mass is taken over the whole row
 };
 
-// ---------------------------------------------------------------- shared memory layout
+// ---------------------------------------------------------------- shared memory
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Dynamic shared memory of one CTA:
-//   raw       chunk * esize       the slice as loaded (f32 or bf16 bits); the leader
-//                                  reuses it to gather the cluster's candidates
-//   live      u32[chunk/32]       allowed by the bitmask, inside the row, not penalised
-//   hkey/hcnt/hbias/hval          hash of the slice's penalised / biased tokens: local id,
-//                                  history count, last bias entry, its value then final z'
-//   cand      Cand[kCandCap]      compacted candidates of the slice
-//   hist_c    u32[256]            local radix histogram (counts); also the sort buffer
-//   hist_w    u64[256]            local radix histogram (fixed-point weights)
-//   mrg_c     u32[2][256]         cluster-merged histograms (DSMEM atomics from every
-//   mrg_w     u64[2][256]         CTA), double-buffered across passes
+// Dynamic shared memory of one CTA (byte offsets):
+//   ring      kStages x kStageBytes   the slice's stream (TMA destination)
+//   live      u32[chunk/32]           allowed by the bitmask, inside the row, not penalised
+//   mod       u32[chunk/32]           penalised / biased tokens (their value is in the hash)
+//   hkey/hcnt/hbias/hval              hash of those tokens: local id; history count with
+//                                     kAllowedBit; last bias entry; its value, then z'
+//   mrg_c     u32[2][256]             cluster-merged histograms (DSMEM atomics from every
+//   mrg_w     u64[2][256]             CTA), double-buffered across passes
+//   gather    Cand[C * cap]           in the leader, once every CTA has finished reading
+//                                     its slice: the cluster's candidates (overlays the
+//                                     regions above)
+//   r2 (8 KB) cand Cand[kCandCap] | hist_c u32[256] | hist_w u64[256]; the top-p warp
+//             histograms (kWarps x 64 u64) overlay cand; the leader's bucket select
+//             overlays all of it (u64[1024] buckets, then Cand[1024])
+struct Layout {
+  uint32_t live, mod, hkey, hcnt, hbias, hval, mrg_c, mrg_w, r2, total;
+};
+
+__host__ __device__ inline Layout layout_for(int chunk) {
+  Layout L;
+  const size_t words = align_up(sizeof(uint32_t) * (size_t)(chunk / 32), 16);
+  size_t off = (size_t)kStages * kStageBytes;
+  L.live = (uint32_t)off;
+  off += words;
+  L.mod = (uint32_t)off;
+  off += words;
+  L.hkey = (uint32_t)off;
+  off += sizeof(uint32_t) * kHashCap;
+  L.hcnt = (uint32_t)off;
+  off += sizeof(uint32_t) * kHashCap;
+  L.hbias = (uint32_t)off;
+  off += sizeof(int32_t) * kHashCap;
+  L.hval = (uint32_t)off;
+  off += sizeof(float) * kHashCap;
+  L.mrg_c = (uint32_t)off;
+  off += sizeof(uint32_t) * 2 * 256;
+  L.mrg_w = (uint32_t)off;
+  off += sizeof(unsigned long long) * 2 * 256;
+  if (off < sizeof(Cand) * kGatherCap) off = sizeof(Cand) * kGatherCap;
+  off = align_up(off, 128);
+  L.r2 = (uint32_t)off;
+  off += 8 * 1024;
+  L.total = (uint32_t)off;
+  return L;
+}
+static_assert(sizeof(unsigned long long) * 1024 <= 8 * 1024 && sizeof(Cand) * 1024 <= 8 * 1024,
+              "bucket select does not fit r2");
+static_assert(sizeof(Cand) * kCandCap + sizeof(uint32_t) * 256 + sizeof(unsigned long long) * 256 <= 8 * 1024,
+              "r2 tables overflow");
+static_assert(sizeof(unsigned long long) * kWarps * 64 <= sizeof(Cand) * kCandCap,
+              "top-p histogram does not fit the candidate area");
+static_assert(1024 % kThreads == 0, "bucket scan assumes whole buckets per thread");
+static_assert(2 * sizeof(uint16_t) * (kMaxChunk / 32) + sizeof(float) * kHashCap <= 8 * 1024,
+              "penalised-token arrays do not fit r2");
+static_assert(kHashCap <= 65536, "ranks and slots are 16-bit");
+static_assert(kStageBytes % (16 * kThreads) == 0, "a stage holds whole vectors per thread");
+
+extern __shared__ __align__(128) unsigned char smem_dyn[];
+
 struct Smem {
-  unsigned char* raw;
+  unsigned char* ring;
   uint32_t* live;
+  uint32_t* mod;
   uint32_t* hkey;
   uint32_t* hcnt;
   int32_t* hbias;
   float* hval;
+  uint32_t* mrg_c;
+  unsigned long long* mrg_w;
+  Cand* gather;
   Cand* cand;
   uint32_t* hist_c;
   unsigned long long* hist_w;
-  uint32_t* mrg_c;
-  unsigned long long* mrg_w;
+  unsigned char* r2;
+  // until exchange 1, r2 holds the penalised tokens in token order: the rank of each
+  // mod word's first token, rank -> hash slot, and rank -> raw logit (filled by pass A)
+  uint16_t* prank;
+  uint16_t* pslot;
+  float* praw;
 };
 
-// The top-p histogram (kWarps x 64 bins of u64) reuses cand + hist_c + hist_w, which
-// are contiguous; pass A's per-token `modbits` (kMaxChunk bits) reuses hist_c + hist_w.
-static_assert(sizeof(uint32_t) * kThreads + sizeof(unsigned long long) * 256 >= kMaxChunk / 8,
-              "pass A modbits do not fit the histogram area");
-static_assert(sizeof(Cand) * kCandCap + sizeof(uint32_t) * kThreads + sizeof(unsigned long long) * 256 >=
-                  sizeof(unsigned long long) * kWarps * 64,
-              "top-p histogram does not fit the candidate area");
-
-__host__ __device__ inline size_t smem_bytes_for(int chunk, int esize) {
-  size_t b = align_up((size_t)chunk * esize, 128);
-  b += sizeof(uint32_t) * (size_t)(chunk / 32);
-  b = align_up(b, 16);
-  b += (sizeof(uint32_t) * 3 + sizeof(float)) * kHashCap;
-  b += sizeof(Cand) * kCandCap;
-  b = align_up(b, 16);
-  b += sizeof(uint32_t) * kThreads;  // >= 256 counts; sized for the 512-entry sort
-  b += sizeof(unsigned long long) * 256;
-  b += sizeof(uint32_t) * 2 * 256;
-  b += sizeof(unsigned long long) * 2 * 256;
-  return b;
+__device__ __forceinline__ Smem carve(int chunk) {
+  const Layout L = layout_for(chunk);
+  unsigned char* b = smem_dyn;
+  Smem s;
+  s.ring = b;
+  s.live = reinterpret_cast<uint32_t*>(b + L.live);
+  s.mod = reinterpret_cast<uint32_t*>(b + L.mod);
+  s.hkey = reinterpret_cast<uint32_t*>(b + L.hkey);
+  s.hcnt = reinterpret_cast<uint32_t*>(b + L.hcnt);
+  s.hbias = reinterpret_cast<int32_t*>(b + L.hbias);
+  s.hval = reinterpret_cast<float*>(b + L.hval);
+  s.mrg_c = reinterpret_cast<uint32_t*>(b + L.mrg_c);
+  s.mrg_w = reinterpret_cast<unsigned long long*>(b + L.mrg_w);
+  s.gather = reinterpret_cast<Cand*>(b);
+  s.cand = reinterpret_cast<Cand*>(b + L.r2);
+  s.hist_c = reinterpret_cast<uint32_t*>(b + L.r2 + sizeof(Cand) * kCandCap);
+  s.hist_w = reinterpret_cast<unsigned long long*>(b + L.r2 + sizeof(Cand) * kCandCap + sizeof(uint32_t) * 256);
+  s.r2 = b + L.r2;
+  s.prank = reinterpret_cast<uint16_t*>(b + L.r2);
+  s.pslot = reinterpret_cast<uint16_t*>(b + L.r2 + sizeof(uint16_t) * (kMaxChunk / 32));
+  s.praw = reinterpret_cast<float*>(b + L.r2 + 2 * sizeof(uint16_t) * (kMaxChunk / 32));
+  return s;
 }
 
-__device__ inline Smem carve(unsigned char* base, int chunk, int esize) {
-  Smem s;
-  size_t off = 0;
-  s.raw = base;
-  off = align_up((size_t)chunk * esize, 128);
-  s.live = reinterpret_cast<uint32_t*>(base + off);
-  off += sizeof(uint32_t) * (size_t)(chunk / 32);
-  off = align_up(off, 16);
-  s.hkey = reinterpret_cast<uint32_t*>(base + off);
-  off += sizeof(uint32_t) * kHashCap;
-  s.hcnt = reinterpret_cast<uint32_t*>(base + off);
-  off += sizeof(uint32_t) * kHashCap;
-  s.hbias = reinterpret_cast<int32_t*>(base + off);
-  off += sizeof(int32_t) * kHashCap;
-  s.hval = reinterpret_cast<float*>(base + off);
-  off += sizeof(float) * kHashCap;
-  s.cand = reinterpret_cast<Cand*>(base + off);
-  off += sizeof(Cand) * kCandCap;
-  off = align_up(off, 16);
-  s.hist_c = reinterpret_cast<uint32_t*>(base + off);
-  off += sizeof(uint32_t) * kThreads;
-  s.hist_w = reinterpret_cast<unsigned long long*>(base + off);
-  off += sizeof(unsigned long long) * 256;
-  s.mrg_c = reinterpret_cast<uint32_t*>(base + off);
-  off += sizeof(uint32_t) * 2 * 256;
-  s.mrg_w = reinterpret_cast<unsigned long long*>(base + off);
-  return s;
+// Static per-CTA state shared by the kernel's functions.
+struct Shared {
+  X1 x1[kMaxCluster];
+  X2 x2[kMaxCluster];
+  X1 x1_mine;
+  X2 x2_mine;
+  unsigned long long full[kStages];  // ring stage barriers (one arrival + the copy's bytes)
+  unsigned long long gather_bar;     // the leader's gather barrier (one arrival per CTA)
+  RowParams rp;
+  RowState rs;
+  float red_f[kWarps * 2];
+  int red_i[kWarps * 2];
+  unsigned long long red_u[kWarps];
+  X2 red_x[kWarps];
+  float red_wb[kWarps * 2];
+  int csr[4];
+  float zth, res;
+  int bstar, nl, flags, count, digit, none, npen;
+  unsigned long long above;
+};
+__shared__ Shared sh;
+
+// The calling CTA's place in the launch.
+struct Geo {
+  int C, chunk, cap, rank, row, c0, len, nvec;
+  int bulk_tokens;  // tokens of the slice that stream through the ring (0: none)
+  int nst;          // ring stages per pass
+  const unsigned char* g;  // the slice's first logit
+};
+
+template <bool kBF16>
+__device__ __forceinline__ Geo geo(const LaunchParams& P) {
+  constexpr int kEsize = kBF16 ? 2 : 4;
+  Geo g;
+  g.C = P.C;
+  g.chunk = P.chunk;
+  g.cap = P.cap;
+  g.rank = (int)cg::this_cluster().block_rank();
+  g.row = (int)(blockIdx.x / (unsigned)g.C);
+  g.c0 = g.rank * g.chunk;
+  g.len = max(0, min(P.a.V, g.c0 + g.chunk) - g.c0);
+  g.nvec = g.chunk / 4;
+  const int bulk = P.vec_ok ? (int)(((size_t)g.len * kEsize) & ~(size_t)15) : 0;
+  g.bulk_tokens = bulk / kEsize;
+  g.nst = (bulk + kStageBytes - 1) / kStageBytes;
+  g.g = reinterpret_cast<const unsigned char*>(P.a.logits) +
+        ((long long)g.row * P.a.logits_row_stride + g.c0) * kEsize;
+  return g;
 }
 
 // ---------------------------------------------------------------- slice access
 
+// Raw logit i of the slice from global memory, widened to f32.
 template <bool kBF16>
-struct Slice {
-  const unsigned char* raw;
-  // four raw logits of tokens 4f .. 4f+3 of the slice, widened to f32
-  __device__ __forceinline__ float4 load4(int f) const {
-    if (kBF16) {
-      const uint2 w = reinterpret_cast<const uint2*>(raw)[f];
-      return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u),
-                         __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
-    } else {
-      return reinterpret_cast<const float4*>(raw)[f];
-    }
+__device__ __forceinline__ float gload1(const unsigned char* g, int i) {
+  if (kBF16) return __uint_as_float((uint32_t)__ldg(reinterpret_cast<const unsigned short*>(g) + i) << 16);
+  return __ldg(reinterpret_cast<const float*>(g) + i);
+}
+
+// Tokens 4f .. 4f+3 from global memory (plain loads; tokens past the row read as 0).
+template <bool kBF16>
+__device__ __forceinline__ float4 gload4(const Geo& g, int f) {
+  const int i = 4 * f;
+  return make_float4(i < g.len ? gload1<kBF16>(g.g, i) : 0.0f, i + 1 < g.len ? gload1<kBF16>(g.g, i + 1) : 0.0f,
+                     i + 2 < g.len ? gload1<kBF16>(g.g, i + 2) : 0.0f,
+                     i + 3 < g.len ? gload1<kBF16>(g.g, i + 3) : 0.0f);
+}
+
+// Vector v (4 tokens) of a ring stage buffer, widened to f32.
+template <bool kBF16>
+__device__ __forceinline__ float4 sload4(const unsigned char* buf, int v) {
+  if (kBF16) {
+    const uint2 w = reinterpret_cast<const uint2*>(buf)[v];
+    return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u), __uint_as_float(w.y << 16),
+                       __uint_as_float(w.y & 0xFFFF0000u));
   }
-  __device__ __forceinline__ float load1(int i) const {
-    if (kBF16) return __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(raw)[i] << 16);
-    return reinterpret_cast<const float*>(raw)[i];
-  }
-};
+  return reinterpret_cast<const float4*>(buf)[v];
+}
 
 __device__ __forceinline__ float comp(const float4& v, int j) {
   return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
@@ -240,16 +338,13 @@ __device__ __forceinline__ int hash_insert(uint32_t* hkey, uint32_t l) {
   return -1;
 }
 
-// Slot of local id l (which must be present); -1 if absent (bounded probing).
-__device__ __forceinline__ int hash_find(const uint32_t* hkey, uint32_t l) {
-  const uint32_t h = (l * 2654435761u) & (kHashCap - 1);
-  for (int probe = 0; probe < kHashCap; ++probe) {
-    const uint32_t slot = (h + probe) & (kHashCap - 1);
-    const uint32_t k = hkey[slot];
-    if (k == l) return (int)slot;
-    if (k == kEmpty) return -1;
-  }
-  return -1;
+// ---------------------------------------------------------------- out-of-line math
+
+// The race score and the Philox words are long instruction sequences used at several
+// places; one out-of-line copy of each keeps the kernel's code small.
+__device__ __noinline__ float race_score_call(float y, uint32_t word) { return race_score(y, word); }
+__device__ __noinline__ uint4 race_words_call(uint32_t q, unsigned long long seed, unsigned long long pos) {
+  return race_words(q, seed, pos);
 }
 
 // ---------------------------------------------------------------- warp / block helpers
@@ -265,11 +360,6 @@ __device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2,
   m = mm;
 }
 
-__device__ __forceinline__ int warp_min_i(int v) {
-#pragma unroll
-  for (int d = 16; d > 0; d >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, d));
-  return v;
-}
 __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
 #pragma unroll
   for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
@@ -285,17 +375,6 @@ __device__ unsigned long long block_sum_u64(unsigned long long v, unsigned long 
   unsigned long long t = 0;
 #pragma unroll
   for (int w = 0; w < kWarps; ++w) t += red[w];
-  return t;
-}
-
-__device__ int block_min_i(int v, int* red) {
-  v = warp_min_i(v);
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-  __syncthreads();
-  int t = INT_MAX;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) t = min(t, red[w]);
   return t;
 }
 
@@ -316,7 +395,7 @@ struct Race {
   __device__ __forceinline__ void add(float y, int id, uint32_t word) {
     ++kept;
     ymin = fminf(ymin, y);
-    const float sc = race_score(y, word);
+    const float sc = race_score_call(y, word);
     if (better(sc, id, s, tok)) {
       s = sc;
       tok = id;
@@ -373,7 +452,7 @@ __device__ void block_reduce_race(Race& r, X2* buf) {
 }
 
 // Writes a sampled row's outputs.
-__device__ void write_sampled(const clsample_args_t& a, int row, const Race& r, float lnS, bool ok) {
+__device__ __noinline__ void write_sampled(const clsample_args_t& a, int row, const Race& r, float lnS, bool ok) {
   ok = ok && r.tok != INT_MAX;
   a.tokens[row] = ok ? r.tok : -1;
   if (a.logprobs) a.logprobs[row] = ok ? r.ybest - lnS : -INFINITY;
@@ -473,21 +552,9 @@ __device__ __forceinline__ bool finite4(const float4& v) {
 }
 
 // Smallest float z with y_of(z, m, invT) >= theta (theta <= 0).  y_of is monotone in z,
-// so {candidates : y >= theta} = {candidates : z >= result} exactly.
-__device__ float z_threshold(float theta, float m, float invT) {
-  if (!(theta > -INFINITY)) return -INFINITY;
-  if (y_of(-FLT_MAX, m, invT) >= theta) return -FLT_MAX;
-  uint32_t lo = fkey(-FLT_MAX), hi = fkey(m);  // y(lo) < theta <= y(hi) = 0
-  while (hi - lo > 1u) {
-    const uint32_t mid = lo + (hi - lo) / 2u;
-    if (y_of(key_to_float(mid), m, invT) >= theta) hi = mid;
-    else lo = mid;
-  }
-  return key_to_float(hi);
-}
-
-// Warp-cooperative version of z_threshold: a 32-ary search over float keys (about
-// seven steps); every lane returns the result.  The whole warp must call it.
+// so {candidates : y >= theta} = {candidates : z >= result} exactly.  Warp-cooperative:
+// a 32-ary search over float keys (about seven steps); every lane returns the result.
+// The whole warp must call it.
 __device__ float z_threshold_warp(float theta, float m, float invT) {
   if (!(theta > -INFINITY)) return -INFINITY;
   if (y_of(-FLT_MAX, m, invT) >= theta) return -FLT_MAX;
@@ -523,75 +590,123 @@ __device__ __forceinline__ int pbin(float y) {
   return b < kPBins - 1 ? b : kPBins - 1;
 }
 
-// ---------------------------------------------------------------- the kernel
+// ---------------------------------------------------------------- the TMA ring
 
+// Issues stage k of a pass (stage sequence number s picks the buffer) on its barrier.
+// Thread 0 only.
 template <bool kBF16>
-__global__ void __launch_bounds__(kThreads, 2) sampler_kernel(const LaunchParams P) {
-  extern __shared__ __align__(128) unsigned char smem_base[];
-  __shared__ X1 x1[kMaxCluster];
-  __shared__ X2 x2[kMaxCluster];
-  __shared__ X1 x1_mine;
-  __shared__ X2 x2_mine;
-  __shared__ __align__(8) unsigned long long mbar_load;
-  __shared__ __align__(8) unsigned long long mbar_gather;
-  __shared__ RowParams rp;
-  __shared__ RowState rs;
-  __shared__ float red_f[kWarps * 2];
-  __shared__ int red_i[kWarps * 2];
-  __shared__ unsigned long long red_u[kWarps];
-  __shared__ X2 red_x[kWarps];
-  __shared__ float red_wb[kWarps * 2];
-  __shared__ int sh_csr[4];
-  __shared__ float sh_zth, sh_res;
-  __shared__ int sh_bstar, sh_nl;
-  __shared__ int sh_flags, sh_count, sh_digit, sh_none;
-  __shared__ unsigned long long sh_above;
-
-  const cg::cluster_group cluster = cg::this_cluster();
-  const clsample_args_t& a = P.a;
-  const int C = P.C;
-  const int chunk = P.chunk;
-  const int cap = P.cap;
-  const int rank = (int)cluster.block_rank();
-  const int row = (int)(blockIdx.x / (unsigned)C);
-  const int V = a.V;
-  const int c0 = rank * chunk;
-  const int len = max(0, min(V, c0 + chunk) - c0);
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nvec = chunk / 4;
+__device__ __forceinline__ void ring_issue(const Geo& g, const Smem& S, int k, uint32_t s) {
   constexpr int kEsize = kBF16 ? 2 : 4;
-  const Smem S = carve(smem_base, chunk, kEsize);
-  const Slice<kBF16> sl{S.raw};
-  const unsigned char* gsrc =
-      reinterpret_cast<const unsigned char*>(a.logits) + ((long long)row * a.logits_row_stride + c0) * kEsize;
+  const int off = k * kStageBytes;
+  const uint32_t bytes = (uint32_t)min(kStageBytes, g.bulk_tokens * kEsize - off);
+  const uint32_t slot = s % kStages;
+  mbar_arrive_expect_tx(&sh.full[slot], bytes);
+  bulk_copy_g2s(S.ring + slot * kStageBytes, g.g + off, bytes, &sh.full[slot]);
+}
+
+// Issues the first stages of pass `pass` (thread 0 only).
+template <bool kBF16>
+__device__ __forceinline__ void ring_start(const Geo& g, const Smem& S, int pass) {
+  const uint32_t seq0 = (uint32_t)pass * (uint32_t)g.nst;
+  for (int k = 0; k < min(kStages, g.nst); ++k) ring_issue<kBF16>(g, S, k, seq0 + k);
+}
+
+// Waits (bounded, suspending) for ring stage s.  Thread 0 only; a stage that never lands
+// marks the row OVERFLOW.
+__device__ __forceinline__ void ring_wait(uint32_t s) {
+  if (!mbar_wait_sleep(&sh.full[s % kStages], (s / kStages) & 1u)) atomicOr(&sh.flags, kFlagRing);
+}
+
+// One pass over the slice: body(f, wd, v) for every 4-token vector f, with its live bits
+// wd and raw values v widened to f32 (valid for every vector that starts inside the row;
+// lanes without a vector get f = nvec, past the row, and wd = 0).
+// Stage sequence numbers continue across the CTA's passes (pass p uses p*nst ..
+// p*nst + nst - 1), which fixes each ring buffer's barrier parity.  Aligned rows stream
+// through the ring; the ragged tail and unaligned rows come in by plain loads.  Every
+// thread calls it; every lane of a warp makes the same number of body calls (wd = 0 where
+// it has no vector), so bodies may use warp collectives.  `started`: thread 0 already
+// issued the pass's first stages.
+template <bool kBF16, class Body>
+__device__ __forceinline__ void stream(const Geo& g, const Smem& S, int& pass, bool started, Body&& body) {
+  constexpr int kEsize = kBF16 ? 2 : 4;
+  constexpr int kVecPerStage = kStageBytes / (4 * kEsize);
+  constexpr int kVPT = kVecPerStage / kThreads;
+  const int tid = threadIdx.x;
+  if (g.nst > 0) {
+    const uint32_t seq0 = (uint32_t)pass * (uint32_t)g.nst;
+    if (tid == 0 && !started) ring_start<kBF16>(g, S, pass);
+#pragma unroll 1
+    for (int k = 0; k < g.nst; ++k) {
+      const uint32_t s = seq0 + (uint32_t)k;
+      // thread 0 sleeps on the stage's barrier; the block barrier then also says that
+      // every thread is done with stage k - 1, whose buffer is refilled at once
+      if (tid == 0) ring_wait(s);
+      __syncthreads();
+      if (tid == 0 && k >= 1 && k - 1 + kStages < g.nst)
+        ring_issue<kBF16>(g, S, k - 1 + kStages, s - 1 + kStages);
+      (void)mbar_try_wait(&sh.full[s % kStages], (s / kStages) & 1u);  // this thread's acquire
+      const unsigned char* buf = S.ring + (s % kStages) * kStageBytes;
+#pragma unroll
+      for (int t = 0; t < kVPT; ++t) {
+        const int fl = t * kThreads + tid;
+        const int f = k * kVecPerStage + fl;
+        const bool in = 4 * f < g.bulk_tokens;
+        const uint32_t wd = in ? live4(S.live, f) : 0u;
+        const float4 v = in ? sload4<kBF16>(buf, fl) : make_float4(0.f, 0.f, 0.f, 0.f);
+        body(in ? f : g.nvec, wd, v);  // vectors past the ring part: f = nvec (past the row)
+      }
+    }
+  }
+  // the ragged tail, and whole unaligned slices: plain loads
+  const int f_end = (g.len + 3) / 4;
+#pragma unroll 1
+  for (int base = g.bulk_tokens / 4; base < f_end; base += kThreads) {
+    const int f = base + tid;
+    const bool in = f < f_end;
+    const uint32_t wd = in ? live4(S.live, f) : 0u;
+    const float4 v = in ? gload4<kBF16>(g, f) : make_float4(0.f, 0.f, 0.f, 0.f);
+    body(in ? f : g.nvec, wd, v);
+  }
+  __syncthreads();  // the ring is free for the next pass; the bodies' shared writes are visible
+  ++pass;
+}
+
+// ---------------------------------------------------------------- prologue
+
+// Adds n occurrences of local id l to the history counts; kFlagOverflow if the hash is
+// full.
+__device__ __noinline__ int count_id(uint32_t* hkey, uint32_t* hcnt, uint32_t l, uint32_t n) {
+  const int slot = hash_insert(hkey, l);
+  if (slot < 0) return kFlagOverflow;
+  atomicAdd(&hcnt[slot], n);
+  return 0;
+}
+
+// Row parameters, the slice's live bits (bitmask words clipped to the row) and the hash
+// of its penalised / biased tokens (SGLang page, "Order semantics of the penalties" and
+// "Why logit_bias is built from triples": the last duplicate wins).  The first ring
+// stages of pass A are issued before anything else, so the slice is on its way while the
+// small inputs arrive.
+template <bool kBF16>
+__device__ __noinline__ void prologue(const LaunchParams& P) {
+  const Geo g = geo<kBF16>(P);
+  const Smem S = carve(g.chunk);
+  const clsample_args_t& a = P.a;
+  const int tid = threadIdx.x;
+  const int row = g.row, c0 = g.c0, len = g.len;
   const int32_t* bmrow = a.bitmask ? a.bitmask + (long long)row * a.bitmask_row_stride : nullptr;
   const bool has_hist = a.hist_offs != nullptr;
   const bool has_bias = a.bias_offs != nullptr;
   const bool has_mod = has_hist || has_bias;
-  const uint32_t bulk_bytes = P.bulk_ok ? (uint32_t)(((size_t)len * kEsize) & ~(size_t)15) : 0u;
 
-  // DSMEM may only be touched once every CTA of the cluster runs: arrive now, wait just
-  // before the first push.
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-
-  // ---- 0. the slice's bulk copy starts first; the row's small inputs are fetched in
-  //         parallel by different warps (one memory round trip)
   if (tid == 0) {
-    sh_flags = 0;
-    sh_count = 0;
-    mbar_init(&mbar_load, 1);
-    mbar_init(&mbar_gather, (uint32_t)C);
+    sh.flags = 0;
+    sh.count = 0;
+    sh.npen = 0;
+    for (int i = 0; i < kStages; ++i) mbar_init(&sh.full[i], 1);
+    mbar_init(&sh.gather_bar, (uint32_t)g.C);
     fence_mbar_init();
-    if (bulk_bytes) {
-      mbar_arrive_expect_tx(&mbar_load, bulk_bytes);
-      const uint32_t piece = ((bulk_bytes + kBulkPieces - 1) / kBulkPieces + 15u) & ~15u;
-      for (uint32_t off = 0; off < bulk_bytes; off += piece) {
-        const uint32_t sz = bulk_bytes - off < piece ? bulk_bytes - off : piece;
-        bulk_copy_g2s(S.raw + off, gsrc + off, sz, &mbar_load);
-      }
-    } else {
-      mbar_arrive_local(&mbar_load);
-    }
+    ring_start<kBF16>(g, S, 0);
   } else if (tid == 32) {
     RowParams q;
     q.T = a.temperatures ? a.temperatures[row] : 1.0f;
@@ -610,15 +725,14 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_kernel(const LaunchParams
     bad |= !(q.mp >= 0.0f && q.mp <= 1.0f);
     bad |= !(q.rep > 0.0f) || (q.rep == INFINITY) || !isfinite(q.freq) || !isfinite(q.pres);
     q.invalid = bad;
-    rp = q;
+    sh.rp = q;
   } else if (tid == 64) {
-    sh_csr[0] = has_hist ? a.hist_offs[row] : 0;
-    sh_csr[1] = has_hist ? a.hist_offs[row + 1] : 0;
-    sh_csr[2] = has_bias ? a.bias_offs[row] : 0;
-    sh_csr[3] = has_bias ? a.bias_offs[row + 1] : 0;
+    sh.csr[0] = has_hist ? a.hist_offs[row] : 0;
+    sh.csr[1] = has_hist ? a.hist_offs[row + 1] : 0;
+    sh.csr[2] = has_bias ? a.bias_offs[row] : 0;
+    sh.csr[3] = has_bias ? a.bias_offs[row + 1] : 0;
   }
-  // live words: allowed by the bitmask and inside the row
-  for (int w = tid; w < chunk / 32; w += kThreads) {
+  for (int w = tid; w < g.chunk / 32; w += kThreads) {
     const int e = 32 * w;
     uint32_t word = 0u;
     if (e < len) {
@@ -627,6 +741,7 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_kernel(const LaunchParams
       if (rem < 32) word &= (1u << rem) - 1u;
     }
     S.live[w] = word;
+    S.mod[w] = 0u;
   }
   if (has_mod) {
     for (int i = tid; i < kHashCap; i += kThreads) {
@@ -640,207 +755,207 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_kernel(const LaunchParams
     S.mrg_w[i] = 0ull;
   }
   __syncthreads();
+  if (!has_mod) return;
 
-  // ---- penalised / biased tokens of this slice (SGLang page, "Order semantics of the
-  //      penalties" and "Why logit_bias is built from triples": last duplicate wins)
-  if (has_mod) {
-    int flags = 0;
-    const int c1 = c0 + len;
-    const int hlo = sh_csr[0], hhi = sh_csr[1], blo = sh_csr[2], bhi = sh_csr[3];
-    if (hlo < 0 || hhi < hlo || blo < 0 || bhi < blo) flags |= kFlagInvalid;
-    const bool hok = has_hist && hlo >= 0 && hhi >= hlo;
-    const bool bok = has_bias && blo >= 0 && bhi >= blo;
-    // this thread's first bias entry is fetched together with the history ids
-    const int bj0 = blo + tid;
-    int bid0 = INT_MIN;
-    float bval0 = 0.0f;
-    if (bok && bj0 < bhi) {
-      bid0 = __ldg(a.bias_ids + bj0);
-      bval0 = __ldg(a.bias_vals + bj0);
-    }
-    if (hok) {
-      for (int base = hlo; base < hhi; base += 8 * kThreads) {
-        int ids[8];
+  int flags = 0;
+  const int c1 = c0 + len;
+  const int hlo = sh.csr[0], hhi = sh.csr[1], blo = sh.csr[2], bhi = sh.csr[3];
+  if (hlo < 0 || hhi < hlo || blo < 0 || bhi < blo) flags |= kFlagInvalid;
+  const bool hok = has_hist && hlo >= 0 && hhi >= hlo;
+  const bool bok = has_bias && blo >= 0 && bhi >= blo;
+  // this thread's first bias entry is fetched together with the history ids
+  const int bj0 = blo + tid;
+  int bid0 = INT_MIN;
+  float bval0 = 0.0f;
+  if (bok && bj0 < bhi) {
+    bid0 = __ldg(a.bias_ids + bj0);
+    bval0 = __ldg(a.bias_vals + bj0);
+  }
+  if (hok) {
+    for (int base = hlo; base < hhi; base += 16 * kThreads) {
+      int ids[16];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int j = base + u * kThreads + tid;
-          ids[u] = j < hhi ? __ldg(a.hist_ids + j) : INT_MIN;
-        }
+      for (int u = 0; u < 16; ++u) {
+        const int j = base + u * kThreads + tid;
+        ids[u] = j < hhi ? __ldg(a.hist_ids + j) : INT_MIN;
+      }
+      // duplicates within a warp are counted once per warp (Zipf-like histories repeat
+      // their frequent ids many times): one insert and one add per distinct id
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int id = ids[u];
-          if (id == INT_MIN) continue;
-          if (id < 0 || id >= V) {
-            flags |= kFlagInvalid;
-          } else if (id >= c0 && id < c1) {
-            const int slot = hash_insert(S.hkey, (uint32_t)(id - c0));
-            if (slot < 0) flags |= kFlagOverflow;
-            else atomicAdd(&S.hcnt[slot], 1u);
-          }
-        }
+      for (int u = 0; u < 16; ++u) {
+        const int id = ids[u];
+        if (id != INT_MIN && (id < 0 || id >= a.V)) flags |= kFlagInvalid;
+        const bool mine = id >= c0 && id < c1;
+        const uint32_t peers = __match_any_sync(0xffffffffu, mine ? id : -1);
+        if (mine && (threadIdx.x & 31) == __ffs(peers) - 1)
+          flags |= count_id(S.hkey, S.hcnt, (uint32_t)(id - c0), (uint32_t)__popc(peers));
       }
     }
-    // bias: the largest entry index per id wins; its owner then stores the value
-    int myslot = -1;
-    if (bok) {
-      for (int j = bj0; j < bhi; j += kThreads) {
-        const int id = j == bj0 ? bid0 : __ldg(a.bias_ids + j);
-        const float b = j == bj0 ? bval0 : __ldg(a.bias_vals + j);
-        if (id < 0 || id >= V || b != b) {
-          flags |= kFlagInvalid;
-        } else if (id >= c0 && id < c1) {
-          const int slot = hash_insert(S.hkey, (uint32_t)(id - c0));
-          if (slot < 0) flags |= kFlagOverflow;
-          else atomicMax(&S.hbias[slot], j);
-          if (j == bj0) myslot = slot;
-        }
+  }
+  // bias: the largest entry index per id wins; its owner then stores the value
+  int myslot = -1;
+  if (bok) {
+    for (int j = bj0; j < bhi; j += kThreads) {
+      const int id = j == bj0 ? bid0 : __ldg(a.bias_ids + j);
+      const float b = j == bj0 ? bval0 : __ldg(a.bias_vals + j);
+      if (id < 0 || id >= a.V || b != b) {
+        flags |= kFlagInvalid;
+      } else if (id >= c0 && id < c1) {
+        const int slot = hash_insert(S.hkey, (uint32_t)(id - c0));
+        if (slot < 0) flags |= kFlagOverflow;
+        else atomicMax(&S.hbias[slot], j);
+        if (j == bj0) myslot = slot;
       }
     }
-    if (flags) atomicOr(&sh_flags, flags);
-    __syncthreads();
-    if (bok) {
-      for (int j = bj0; j < bhi; j += kThreads) {
-        const int slot = j == bj0 ? myslot : -2;
-        if (j == bj0) {
-          if (slot >= 0 && S.hbias[slot] == j) S.hval[slot] = bval0;
-        } else {
-          const int id = __ldg(a.bias_ids + j);
-          if (id >= c0 && id < c1) {
-            for (int i = 0; i < kHashCap; ++i)
-              if (S.hkey[i] == (uint32_t)(id - c0) && S.hbias[i] == j) S.hval[i] = __ldg(a.bias_vals + j);
-          }
+  }
+  if (flags) atomicOr(&sh.flags, flags);
+  __syncthreads();
+  if (bok) {
+    for (int j = bj0; j < bhi; j += kThreads) {
+      if (j == bj0) {
+        if (myslot >= 0 && S.hbias[myslot] == j) S.hval[myslot] = bval0;
+      } else {
+        const int id = __ldg(a.bias_ids + j);
+        if (id >= c0 && id < c1) {
+          for (int i = 0; i < kHashCap; ++i)
+            if (S.hkey[i] == (uint32_t)(id - c0) && S.hbias[i] == j) S.hval[i] = __ldg(a.bias_vals + j);
         }
       }
     }
   }
-
-  // ---- 1. the slice has landed (bounded wait); rows that are not 16-byte aligned and
-  //         the ragged tail come in with plain loads
-  // one thread polls; the others sleep in the block barrier below
-  if (tid == 0 && !mbar_wait(&mbar_load, 0)) atomicOr(&sh_flags, kFlagTimeout);
+  // penalised / biased tokens leave the live set (pass A gives them their final value);
+  // the bitmask's verdict on each moves into its hash entry
+  for (int i = tid; i < kHashCap; i += kThreads) {
+    const uint32_t l = S.hkey[i];
+    if (l == kEmpty) continue;
+    const uint32_t bit = 1u << (l & 31);
+    if (S.live[l >> 5] & bit) S.hcnt[i] |= kAllowedBit;
+    atomicAnd(&S.live[l >> 5], ~bit);
+    atomicOr(&S.mod[l >> 5], bit);
+  }
+  __syncthreads();
+  // token-order ranks of the penalised tokens: an exclusive scan of the mod words'
+  // popcounts (consecutive words per thread), then rank -> hash slot
   {
-    const int done = (int)(bulk_bytes / kEsize);
-    for (int i = done + tid; i < len; i += kThreads) {
-      if (kBF16)
-        reinterpret_cast<uint16_t*>(S.raw)[i] = __ldg(reinterpret_cast<const unsigned short*>(gsrc) + i);
-      else
-        reinterpret_cast<float*>(S.raw)[i] = __ldg(reinterpret_cast<const float*>(gsrc) + i);
+    constexpr int kPer = (kMaxChunk / 32) / kThreads;
+    const int nw = g.chunk / 32;
+    const int lane = tid & 31, warp = tid >> 5;
+    int cnt[kPer], loc = 0;
+#pragma unroll
+    for (int t = 0; t < kPer; ++t) {
+      const int w = tid * kPer + t;
+      cnt[t] = w < nw ? __popc(S.mod[w]) : 0;
+      loc += cnt[t];
     }
+    int x = loc;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, x, d);
+      if (lane >= d) x += o;
+    }
+    if (lane == 31) sh.red_i[warp] = x;
+    __syncthreads();
+    int excl = x - loc;
+    for (int w = 0; w < warp; ++w) excl += sh.red_i[w];
+#pragma unroll
+    for (int t = 0; t < kPer; ++t) {
+      const int w = tid * kPer + t;
+      if (w < nw) S.prank[w] = (uint16_t)excl;
+      excl += cnt[t];
+    }
+    if (tid == kThreads - 1) sh.npen = excl;
   }
   __syncthreads();
-  // the phase is complete: one poll gives every thread its own acquire of the copy
-  (void)mbar_try_wait(&mbar_load, 0);
-  const RowParams q = rp;
-
-  // ---- 2. final z' of the penalised / biased tokens (the mask applies to them too);
-  //         then they leave the live set and are marked in `modbits` (the histogram
-  //         area is free until pass A ends), so pass A can fold them in token order
-  uint32_t* modbits = S.hist_c;
-  if (has_mod) {
-    for (int i = tid; i < chunk / 32; i += kThreads) modbits[i] = 0u;
-    for (int i = tid; i < kHashCap; i += kThreads) {
-      const uint32_t l = S.hkey[i];
-      if (l == kEmpty) continue;
-      float z = sanitize(sl.load1((int)l));
-      if (!((S.live[l >> 5] >> (l & 31)) & 1u)) z = -INFINITY;
-      const uint32_t cnt = S.hcnt[i];
-      if (cnt) z = apply_penalties(z, cnt, q.freq, q.pres, q.rep);
-      if (S.hbias[i] >= 0) z = __fadd_rn(z, S.hval[i]);
-      S.hval[i] = guard(z);
-    }
-    __syncthreads();
-    for (int i = tid; i < kHashCap; i += kThreads) {
-      const uint32_t l = S.hkey[i];
-      if (l == kEmpty) continue;
-      atomicAnd(&S.live[l >> 5], ~(1u << (l & 31)));
-      atomicOr(&modbits[l >> 5], 1u << (l & 31));
-    }
-  }
-  if (a.dbg_transformed) {
-    float* out = a.dbg_transformed + (long long)row * V + c0;
-    for (int i = tid; i < len; i += kThreads) {
-      const int g = c0 + i;
-      const bool allowed = !bmrow || (((uint32_t)__ldg(bmrow + (g >> 5)) >> (g & 31)) & 1u);
-      out[i] = allowed ? sanitize(sl.load1(i)) : -INFINITY;
-    }
-    __syncthreads();
-    if (has_mod)
-      for (int i = tid; i < kHashCap; i += kThreads)
-        if (S.hkey[i] != kEmpty) out[S.hkey[i]] = S.hval[i];
+  for (int i = tid; i < kHashCap; i += kThreads) {
+    const uint32_t l = S.hkey[i];
+    if (l == kEmpty) continue;
+    const int r = S.prank[l >> 5] + __popc(S.mod[l >> 5] & ((1u << (l & 31)) - 1u));
+    S.pslot[r] = (uint16_t)i;
   }
   __syncthreads();
+}
 
-  // ---- 3. pass A: max, lazy argmax and online sum of exp((z' - max) / T_eff)
+// ---------------------------------------------------------------- pass A
+
+// Pass A: slice max, lowest argmax and online sum of 2^((z' - max) cS), cS = log2(e)/T_eff;
+// per-warp lower bounds of the top-k cut from the per-thread maxima.  Leaves the slice
+// record in sh.x1_mine.
+template <bool kBF16>
+__device__ __noinline__ void pass_a(const LaunchParams& P) {
+  const Geo g = geo<kBF16>(P);
+  const Smem S = carve(g.chunk);
+  const clsample_args_t& a = P.a;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const RowParams q = sh.rp;
+  const bool has_mod = a.hist_offs != nullptr || a.bias_offs != nullptr;
   const bool greedy = (q.T < kGreedyEps) || q.k == 0 || q.k == 1;
   const float Teff = (q.T >= kGreedyEps) ? q.T : 1.0f;
   const float cS = 1.4426950408889634f / Teff;
-  // values of tokens 4f..4f+3 for pass A: live -> sanitised raw, penalised / biased ->
-  // their final z' from the hash, otherwise -inf
-  auto pass_a_values = [&](int f, uint32_t wd, const float4& v, float* z) {
-    const uint32_t md = has_mod ? live4(modbits, f) : 0u;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if ((wd >> j) & 1u) {
-        z[j] = sanitize(comp(v, j));
-      } else if ((md >> j) & 1u) {
-        const int slot = hash_find(S.hkey, (uint32_t)(4 * f + j));
-        z[j] = slot >= 0 ? S.hval[slot] : -INFINITY;
-      } else {
-        z[j] = -INFINITY;
-      }
-    }
-  };
-  // one online state: running max, sum of 2^((z - max) cS), first float4 reaching max
-  struct OnlineState {
-    float m, s;
-    int f;
-  };
-  auto pass_a_step = [&](OnlineState& st, int f) {
-    const uint32_t wd = live4(S.live, f);
-    if (!wd && !(has_mod && live4(modbits, f))) return;
-    const float4 v = sl.load4(f);
-    float z[4];
-    if (wd == 0xFu && finite4(v)) {
-      z[0] = v.x;
-      z[1] = v.y;
-      z[2] = v.z;
-      z[3] = v.w;
-    } else {
-      pass_a_values(f, wd, v, z);
-    }
-    const float fm = fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3]));
-    if (!(fm > -INFINITY)) return;
-    if (fm > st.m) {
-      st.s *= ex2_approx((st.m - fm) * cS);
-      st.m = fm;
-      st.f = f;
-    }
-    const float e0 = ex2_approx((z[0] - st.m) * cS), e1 = ex2_approx((z[1] - st.m) * cS);
-    const float e2 = ex2_approx((z[2] - st.m) * cS), e3 = ex2_approx((z[3] - st.m) * cS);
-    st.s += (e0 + e1) + (e2 + e3);
-  };
-  OnlineState st0{-INFINITY, 0.0f, -1}, st1{-INFINITY, 0.0f, -1};
-  for (int f = tid; f < nvec; f += 2 * kThreads) {
-    pass_a_step(st0, f);
-    if (f + kThreads < nvec) pass_a_step(st1, f + kThreads);
-  }
-  float sm = fmaxf(st0.m, st1.m), ss = 0.0f;
-  if (sm > -INFINITY) ss = st0.s * ex2_approx((st0.m - sm) * cS) + st1.s * ex2_approx((st1.m - sm) * cS);
-  // this thread's lowest id reaching its max: rescan the first float4 of each state
+  const int c0 = g.c0;
+
+  // the thread's online state; a thread visits its tokens in increasing order, so the
+  // first token reaching the running max is the lowest
+  float sm = -INFINITY, ss = 0.0f;
   int targ = INT_MAX;
-  for (int t = 0; t < 2; ++t) {
-    const OnlineState& st = t == 0 ? st0 : st1;
-    if (st.f < 0 || st.m != sm) continue;
-    float z[4];
-    pass_a_values(st.f, live4(S.live, st.f), sl.load4(st.f), z);
-    for (int j = 0; j < 4; ++j)
-      if (z[j] == sm) {
-        targ = min(targ, c0 + 4 * st.f + j);
-        break;
+  int pass = 0;
+  stream<kBF16>(g, S, pass, true, [&](int f, uint32_t wd, const float4& v) {
+    if (has_mod && 4 * f < g.len) {
+      // penalised / biased tokens: keep the raw logit (rank order) for the fold below
+      const uint32_t mw = S.mod[f >> 3];
+      const int sh4 = (f & 7) * 4;
+      const uint32_t md = (mw >> sh4) & 0xFu;
+      if (md) {
+        int r = S.prank[f >> 3] + __popc(mw & ((1u << sh4) - 1u));
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if ((md >> j) & 1u) S.praw[r++] = comp(v, j);
       }
+    }
+    if (!wd) return;
+    float4 z = v;
+    if (!(wd == 0xFu && finite4(v)))
+      z = make_float4((wd & 1u) ? sanitize(v.x) : -INFINITY, (wd & 2u) ? sanitize(v.y) : -INFINITY,
+                      (wd & 4u) ? sanitize(v.z) : -INFINITY, (wd & 8u) ? sanitize(v.w) : -INFINITY);
+    const float fm = fmaxf(fmaxf(z.x, z.y), fmaxf(z.z, z.w));
+    if (!(fm > -INFINITY)) return;
+    if (fm > sm) {
+      ss *= ex2_approx((sm - fm) * cS);
+      sm = fm;
+      targ = c0 + 4 * f + (z.x == fm ? 0 : z.y == fm ? 1 : z.z == fm ? 2 : 3);
+    }
+    const float e0 = ex2_approx((z.x - sm) * cS), e1 = ex2_approx((z.y - sm) * cS);
+    const float e2 = ex2_approx((z.z - sm) * cS), e3 = ex2_approx((z.w - sm) * cS);
+    ss += (e0 + e1) + (e2 + e3);
+  });
+  // the penalised / biased tokens in token order: penalties, then bias, on the sanitised
+  // raw logit (the mask applies to them too); the final z' goes into the hash and into
+  // the thread's online state
+  if (has_mod) {
+    const int npen = sh.npen;
+    for (int r = tid; r < npen; r += kThreads) {
+      const int slot = S.pslot[r];
+      const uint32_t c = S.hcnt[slot];
+      float zz = (c & kAllowedBit) ? sanitize(S.praw[r]) : -INFINITY;
+      const uint32_t cnt = c & ~kAllowedBit;
+      if (cnt) zz = apply_penalties(zz, cnt, q.freq, q.pres, q.rep);
+      if (S.hbias[slot] >= 0) zz = __fadd_rn(zz, S.hval[slot]);
+      zz = guard(zz);
+      S.hval[slot] = zz;
+      if (!(zz > -INFINITY)) continue;
+      const int id = c0 + (int)S.hkey[slot];
+      if (zz > sm) {
+        ss = ss * ex2_approx((sm - zz) * cS) + 1.0f;
+        sm = zz;
+        targ = id;
+      } else {
+        ss += ex2_approx((zz - sm) * cS);
+        if (zz == sm && id < targ) targ = id;
+      }
+    }
   }
+
   // warp-level lower bounds of the top-k cut from the per-thread maxima (disjoint
-  // groups): a warp's j-th largest group max guarantees j tokens at or above it
+  // groups): a warp's j-th largest thread max guarantees j tokens at or above it
   const bool topk_row = !greedy && !q.invalid && q.k >= 2;
   float wlk = -INFINITY, wlkc = INFINITY;
   if (topk_row) {
@@ -856,731 +971,840 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_kernel(const LaunchParams
       }
     }
     // ascending across lanes: the j-th largest sits in lane 32 - j
-    const int k1 = q.k, k2 = (q.k + kWarps * C - 1) / (kWarps * C);
+    const int k1 = q.k, k2 = (q.k + kWarps * g.C - 1) / (kWarps * g.C);
     const uint32_t v1 = __shfl_sync(0xffffffffu, key, k1 <= 32 ? 32 - k1 : 0);
     const uint32_t v2 = __shfl_sync(0xffffffffu, key, k2 <= 32 ? 32 - k2 : 0);
     wlk = k1 <= 32 ? key_to_float(v1) : -INFINITY;
     wlkc = k2 <= 32 ? key_to_float(v2) : -INFINITY;
   }
   // block reduction of (max, sum, argmax) and of the bounds
-  {
-    float m2 = sm, s2 = ss;
-    int a2 = targ;
+  float m2 = sm, s2 = ss;
+  int a2 = targ;
 #pragma unroll
-    for (int d = 16; d > 0; d >>= 1) {
-      const float om = __shfl_xor_sync(0xffffffffu, m2, d);
-      const float os = __shfl_xor_sync(0xffffffffu, s2, d);
-      const int oa = __shfl_xor_sync(0xffffffffu, a2, d);
-      if (better(om, oa, m2, a2)) a2 = oa;
-      merge_ms(m2, s2, om, os, cS);
-    }
-    if (lane == 0) {
-      red_f[warp * 2] = m2;
-      red_f[warp * 2 + 1] = s2;
-      red_i[warp * 2] = a2;
-      red_wb[warp * 2] = wlk;
-      red_wb[warp * 2 + 1] = wlkc;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      const bool in = lane < kWarps;
-      float m = in ? red_f[lane * 2] : -INFINITY, s = in ? red_f[lane * 2 + 1] : 0.0f;
-      int arg = in ? red_i[lane * 2] : INT_MAX;
-      float lk = in ? red_wb[lane * 2] : -INFINITY, lkc = in ? red_wb[lane * 2 + 1] : INFINITY;
-#pragma unroll
-      for (int d = 16; d > 0; d >>= 1) {
-        const float om = __shfl_xor_sync(0xffffffffu, m, d);
-        const float os = __shfl_xor_sync(0xffffffffu, s, d);
-        const int oa = __shfl_xor_sync(0xffffffffu, arg, d);
-        if (better(om, oa, m, arg)) arg = oa;
-        merge_ms(m, s, om, os, cS);
-        lk = fmaxf(lk, __shfl_xor_sync(0xffffffffu, lk, d));
-        lkc = fminf(lkc, __shfl_xor_sync(0xffffffffu, lkc, d));
-      }
-      if (lane == 0) {
-        x1_mine.m = m;
-        x1_mine.s = s;
-        x1_mine.arg = arg;
-        x1_mine.lk = lk;
-        x1_mine.lkc = topk_row ? lkc : -INFINITY;
-        x1_mine.flags = sh_flags;
-      }
-    }
+  for (int d = 16; d > 0; d >>= 1) {
+    const float om = __shfl_xor_sync(0xffffffffu, m2, d);
+    const float os = __shfl_xor_sync(0xffffffffu, s2, d);
+    const int oa = __shfl_xor_sync(0xffffffffu, a2, d);
+    if (better(om, oa, m2, a2)) a2 = oa;
+    merge_ms(m2, s2, om, os, cS);
+  }
+  if (lane == 0) {
+    sh.red_f[warp * 2] = m2;
+    sh.red_f[warp * 2 + 1] = s2;
+    sh.red_i[warp * 2] = a2;
+    sh.red_wb[warp * 2] = wlk;
+    sh.red_wb[warp * 2 + 1] = wlkc;
   }
   __syncthreads();
-  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-  push_all(cluster, x1, &x1_mine, rank, C);
-  cluster.sync();  // exchange 1
-
-  // ---- 4. row statistics, combined identically by every CTA
   if (warp == 0) {
-    const bool in = lane < C;
-    const float lm = in ? x1[lane].m : -INFINITY;
-    const int la = in ? x1[lane].arg : INT_MAX;
-    float m = lm;
-#pragma unroll
-    for (int d = 16; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
-    int arg = (in && lm == m) ? la : INT_MAX;
-    arg = warp_min_i(arg);
-    const float term = (in && lm > -INFINITY) ? x1[lane].s * ex2_approx((lm - m) * cS) : 0.0f;
-    float tot = 0.0f;  // fixed order (lanes 0..31): every CTA gets the same bits
-    for (int r = 0; r < 32; ++r) tot += __shfl_sync(0xffffffffu, term, r);
-    int fl = in ? x1[lane].flags : 0;
-#pragma unroll
-    for (int d = 16; d > 0; d >>= 1) fl |= __shfl_xor_sync(0xffffffffu, fl, d);
-    float lk = in ? x1[lane].lk : -INFINITY;
-    float lkc = in ? x1[lane].lkc : INFINITY;
+    const bool in = lane < kWarps;
+    float m = in ? sh.red_f[lane * 2] : -INFINITY, s = in ? sh.red_f[lane * 2 + 1] : 0.0f;
+    int arg = in ? sh.red_i[lane * 2] : INT_MAX;
+    float lk = in ? sh.red_wb[lane * 2] : -INFINITY, lkc = in ? sh.red_wb[lane * 2 + 1] : INFINITY;
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) {
+      const float om = __shfl_xor_sync(0xffffffffu, m, d);
+      const float os = __shfl_xor_sync(0xffffffffu, s, d);
+      const int oa = __shfl_xor_sync(0xffffffffu, arg, d);
+      if (better(om, oa, m, arg)) arg = oa;
+      merge_ms(m, s, om, os, cS);
       lk = fmaxf(lk, __shfl_xor_sync(0xffffffffu, lk, d));
       lkc = fminf(lkc, __shfl_xor_sync(0xffffffffu, lkc, d));
     }
     if (lane == 0) {
-      rs.m = m;
-      rs.arg = arg;
-      rs.S = tot;
-      rs.flags = fl;
-      rs.bound = fmaxf(lk, lkc);
+      sh.x1_mine.m = m;
+      sh.x1_mine.s = s;
+      sh.x1_mine.arg = arg;
+      sh.x1_mine.lk = lk;
+      sh.x1_mine.lkc = topk_row ? lkc : -INFINITY;
+      sh.x1_mine.flags = sh.flags;
+    }
+  }
+  // the transformed logits, on request (debugging aid): plain values first, then the
+  // penalised / biased tokens' final z' from the hash
+  if (a.dbg_transformed) {
+    float* out = a.dbg_transformed + (long long)g.row * a.V + c0;
+    const int32_t* bmrow = a.bitmask ? a.bitmask + (long long)g.row * a.bitmask_row_stride : nullptr;
+    for (int i = tid; i < g.len; i += kThreads) {
+      const int gi = c0 + i;
+      const bool allowed = !bmrow || (((uint32_t)__ldg(bmrow + (gi >> 5)) >> (gi & 31)) & 1u);
+      out[i] = allowed ? sanitize(gload1<kBF16>(g.g, i)) : -INFINITY;
+    }
+    __syncthreads();
+    if (has_mod)
+      for (int i = tid; i < kHashCap; i += kThreads)
+        if (S.hkey[i] != kEmpty) out[S.hkey[i]] = S.hval[i];
+  }
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------- exchange 1
+
+// Every CTA pushes its slice record into every CTA (DSMEM) and one cluster barrier
+// publishes them; every CTA then combines them in the same order into sh.rs.
+__device__ __noinline__ void exchange1(const LaunchParams& P) {
+  const cg::cluster_group cluster = cg::this_cluster();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int C = P.C;
+  const int rank = (int)cluster.block_rank();
+  const RowParams q = sh.rp;
+  const float Teff = (q.T >= kGreedyEps) ? q.T : 1.0f;
+  const float cS = 1.4426950408889634f / Teff;
+  // DSMEM may only be touched once every CTA of the cluster runs (the kernel arrived on
+  // the cluster barrier at entry)
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+  push_all(cluster, sh.x1, &sh.x1_mine, rank, C);
+  cluster.sync();
+  if (warp == 0) {
+    const bool in = lane < C;
+    const float lm = in ? sh.x1[lane].m : -INFINITY;
+    const int la = in ? sh.x1[lane].arg : INT_MAX;
+    const float ls = in ? sh.x1[lane].s : 0.0f;
+    int fl = in ? sh.x1[lane].flags : 0;
+    float lk = in ? sh.x1[lane].lk : -INFINITY;
+    float lkc = in ? sh.x1[lane].lkc : INFINITY;
+    float m = lm;
+#pragma unroll
+    for (int d = 4; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
+    m = __shfl_sync(0xffffffffu, m, 0);  // lanes >= C may hold their own partial maxima
+    int arg = (in && lm == m) ? la : INT_MAX;
+    const float term = (in && lm > -INFINITY) ? ls * ex2_approx((lm - m) * cS) : 0.0f;
+#pragma unroll
+    for (int d = 4; d > 0; d >>= 1) {
+      arg = min(arg, __shfl_xor_sync(0xffffffffu, arg, d));
+      fl |= __shfl_xor_sync(0xffffffffu, fl, d);
+      lk = fmaxf(lk, __shfl_xor_sync(0xffffffffu, lk, d));
+      lkc = fminf(lkc, __shfl_xor_sync(0xffffffffu, lkc, d));
+    }
+    // the sum in a fixed order (ranks 0 .. C-1): every CTA gets the same bits
+    float tot = 0.0f;
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r) tot += __shfl_sync(0xffffffffu, term, r);
+    if (lane == 0) {
+      sh.rs.m = m;
+      sh.rs.arg = arg;
+      sh.rs.S = tot;
+      sh.rs.flags = fl;
+      sh.rs.bound = fmaxf(lk, lkc);
+      sh.rs.lnS = logf(tot);
     }
   }
   __syncthreads();
-  const float m = rs.m;
+}
+// ---------------------------------------------------------------- row end and plan
+
+// Greedy, INVALID and OVERFLOW rows end after exchange 1; rank 0 writes the argmax (its
+// y is 0, so its logprob is -ln S).  Returns true (in every thread) if the row ended.
+__device__ __noinline__ bool finish_early(const LaunchParams& P) {
+  const RowParams q = sh.rp;
+  const float m = sh.rs.m;
+  const int fl = sh.rs.flags;
   int status = kRowOk;
-  if (q.invalid || (rs.flags & kFlagInvalid) || !(m > -INFINITY)) status = kRowInvalid;
-  else if (rs.flags & (kFlagOverflow | kFlagTimeout)) status = kRowOverflow;
-  const float lnS = logf(rs.S);
-
-  if (status != kRowOk || greedy) {
-    if (rank == 0 && tid == 0) {
-      const bool ok = status == kRowOk;
-      a.tokens[row] = ok ? rs.arg : -1;
-      if (a.logprobs) a.logprobs[row] = ok ? -lnS : -INFINITY;  // y of the argmax is 0
-      if (a.row_status) a.row_status[row] = status;
-      if (a.dbg_kept_count) a.dbg_kept_count[row] = ok ? 1 : 0;
-      if (a.dbg_cut) a.dbg_cut[row] = ok ? 0.0f : -INFINITY;
-    }
-    if ((rs.flags & kFlagTimeout) && tid == 0) mbar_wait(&mbar_load, 0);
-    return;  // every remote access of this row happened before the barrier
+  if (q.invalid || (fl & kFlagInvalid) || !(m > -INFINITY)) status = kRowInvalid;
+  else if (fl & (kFlagOverflow | kFlagRing)) status = kRowOverflow;
+  const bool greedy = (q.T < kGreedyEps) || q.k == 0 || q.k == 1;
+  if (status == kRowOk && !greedy) return false;
+  if (threadIdx.x == 0 && cg::this_cluster().block_rank() == 0) {
+    const clsample_args_t& a = P.a;
+    const int row = (int)(blockIdx.x / (unsigned)P.C);
+    const bool ok = status == kRowOk;
+    a.tokens[row] = ok ? sh.rs.arg : -1;
+    if (a.logprobs) a.logprobs[row] = ok ? -sh.rs.lnS : -INFINITY;
+    if (a.row_status) a.row_status[row] = status;
+    if (a.dbg_kept_count) a.dbg_kept_count[row] = ok ? 1 : 0;
+    if (a.dbg_cut) a.dbg_cut[row] = ok ? 0.0f : -INFINITY;
   }
+  return true;
+}
 
-  // ---- 5. truncation plan.  y = (z' - m) * (1/T); K = {y >= cut} is an upper set.
-  const float invT = __frcp_rn(q.T);
-  const float L = q.mp > 0.0f ? (float)log((double)q.mp) : -INFINITY;  // min-p: y >= ln(min_p)
-  const bool kfin = q.k >= 2;
-  enum { kFast, kTopP, kUntrunc, kSlow };
-  int plan = kSlow;
-  bool needW = false;
-  float theta = -INFINITY;
-  if (kfin && rs.bound > -INFINITY) {
-    plan = kFast;  // every token of S_k has y >= y(bound)
-    theta = y_of(rs.bound, m, invT);
-    if (q.p >= 1.0f) theta = fmaxf(theta, L);
-  } else if (q.mp > 0.0f && (q.p >= 1.0f || !kfin)) {
-    plan = kFast;  // K lies in {y >= ln min_p}
-    theta = L;
-    needW = q.p < 1.0f;  // top-p renormalises over the whole row
-  } else if (!kfin && q.p >= 1.0f) {
-    plan = kUntrunc;  // K = every allowed token
-  } else if (!kfin) {
-    plan = kTopP;  // top-p alone
+// Truncation plan.  y = (z' - m) * (1/T); the kept set K = {y >= cut} is an upper set.
+__device__ __noinline__ void plan_row() {
+  if (threadIdx.x == 0) {
+    const RowParams q = sh.rp;
+    RowState& rs = sh.rs;
+    rs.invT = __frcp_rn(q.T);
+    rs.L = q.mp > 0.0f ? (float)log((double)q.mp) : -INFINITY;  // min-p: y >= ln(min_p)
+    const bool kfin = q.k >= 2;
+    int plan = kPlanSlow, needW = 0;
+    float theta = -INFINITY;
+    if (kfin && rs.bound > -INFINITY) {
+      plan = kPlanFast;  // every token of S_k has y >= y(bound)
+      theta = y_of(rs.bound, rs.m, rs.invT);
+      if (q.p >= 1.0f) theta = fmaxf(theta, rs.L);
+    } else if (q.mp > 0.0f && (q.p >= 1.0f || !kfin)) {
+      plan = kPlanFast;  // K lies in {y >= ln min_p}
+      theta = rs.L;
+      needW = q.p < 1.0f;  // top-p renormalises over the whole row
+    } else if (!kfin && q.p >= 1.0f) {
+      plan = kPlanUntrunc;  // K = every allowed token
+    } else if (!kfin) {
+      plan = kPlanTopP;  // top-p alone
+    }
+    rs.plan = plan;
+    rs.needW = needW;
+    rs.theta = theta;
   }
-  const unsigned long long seed = q.seed, pos = q.pos;
-  Cand* cand = S.cand;
+  __syncthreads();
+}
 
-  // ---- the leader's part after a gather: top-k -> top-p -> min-p and the race over
-  //      the candidates every CTA stored into its slot of the leader's raw slice
-  const Cand* G = reinterpret_cast<const Cand*>(S.raw);
-  const int span = C * cap;
-  const int lgcap = __ffs(cap) - 1;  // cap is a power of two
-  auto gvalid = [&](int i) -> bool { return i < span && (i & (cap - 1)) < x2[i >> lgcap].count; };
-  // radix select over the gathered set (entries with y >= ylo); see pick_digit
-  auto local_select = [&](bool weighted, float ylo, unsigned long long target, bool* found) -> float {
-    uint32_t prefix = 0u, pmask = 0u;
-    for (int pass = 0; pass < 4; ++pass) {
-      const int shift = 24 - 8 * pass;
-      if (tid < 256) {
-        S.hist_c[tid] = 0u;
-        S.hist_w[tid] = 0ull;
-      }
-      __syncthreads();
-      for (int base = 0; base < span; base += kThreads) {
-        const int i = base + tid;
-        const bool ok = gvalid(i);
-        const float y = ok ? G[i].y : -INFINITY;
-        const uint32_t key = fkey(y);
-        const bool pred = ok && y >= ylo && (key & pmask) == prefix;
-        if (weighted)
-          hist_add<true>(S.hist_c, S.hist_w, pred, (key >> shift) & 0xFFu, pred ? weight_fx(y) : 0ull);
-        else
-          hist_add<false>(S.hist_c, S.hist_w, pred, (key >> shift) & 0xFFu, 0ull);
-      }
-      __syncthreads();
-      if (warp == 0) {
-        if (weighted) pick_digit(S.hist_w, target, &sh_digit, &sh_above, &sh_none);
-        else pick_digit(S.hist_c, target, &sh_digit, &sh_above, &sh_none);
-      }
-      __syncthreads();
-      if (sh_none) {
-        *found = false;
-        __syncthreads();
-        return -INFINITY;
-      }
-      prefix |= (uint32_t)sh_digit << shift;
-      pmask |= 0xFFu << shift;
-      target -= sh_above;
-      __syncthreads();
-    }
-    *found = true;
-    return key_to_float(prefix);
-  };
-  // Exact select over the gathered set, entries with y >= ylo, all within [lo, hi]:
-  // one 1024-bucket histogram (bucket order follows y), then the crossing bucket's
-  // entries are resolved by counting.  Sets *resolved = false when that bucket holds
-  // more than 1024 entries (heavy ties); the caller then uses local_select.
-  auto bucket_select = [&](bool weighted, float lo, float hi, float ylo, unsigned long long target,
-                           bool* found, bool* resolved) -> float {
-    unsigned long long* bk = reinterpret_cast<unsigned long long*>(S.hist_c);  // hist + mrg: 10 KB
-    const float scale = hi > lo ? 1024.0f / (hi - lo) : 0.0f;
-    auto bucket = [&](float y) -> int {
-      const int b = __float2int_rz(__fmul_rn(hi - y, scale));
-      return b < 0 ? 0 : (b > 1023 ? 1023 : b);
-    };
-    bk[2 * tid] = 0ull;
-    bk[2 * tid + 1] = 0ull;
-    if (tid == 0) {
-      sh_nl = 0;
-      sh_bstar = -1;
-    }
-    __syncthreads();
-    for (int i = tid; i < span; i += kThreads) {
-      if (!gvalid(i)) continue;
-      const float y = G[i].y;
-      if (!(y >= ylo)) continue;
-      atomicAdd(&bk[bucket(y)], weighted ? weight_fx(y) : 1ull);
-    }
-    __syncthreads();
-    {
-      const unsigned long long v0 = bk[2 * tid], v1 = bk[2 * tid + 1], loc = v0 + v1;
-      unsigned long long x = loc;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const unsigned long long o = __shfl_up_sync(0xffffffffu, x, d);
-        if (lane >= d) x += o;
-      }
-      if (lane == 31) red_u[warp] = x;
-      __syncthreads();
-      unsigned long long before = 0;
-      for (int w = 0; w < warp; ++w) before += red_u[w];
-      const unsigned long long excl = before + x - loc, incl = before + x;
-      if (excl < target && target <= incl) {
-        if (excl + v0 >= target) {
-          sh_bstar = 2 * tid;
-          sh_above = excl;
-        } else {
-          sh_bstar = 2 * tid + 1;
-          sh_above = excl + v0;
-        }
-      }
-    }
-    __syncthreads();
-    const int bstar = sh_bstar;
-    if (bstar < 0) {
-      *found = false;
-      *resolved = true;
-      return -INFINITY;
-    }
-    const unsigned long long t2 = target - sh_above;
-    // the crossing bucket's entries, gathered into the (now free) histogram area
-    Cand* Lb = reinterpret_cast<Cand*>(S.hist_c);
-    for (int i = tid; i < span; i += kThreads) {
-      if (!gvalid(i)) continue;
-      const Cand cd = G[i];
-      if (!(cd.y >= ylo) || bucket(cd.y) != bstar) continue;
-      const int p = atomicAdd(&sh_nl, 1);
-      if (p < 1024) Lb[p] = cd;
-    }
-    __syncthreads();
-    const int nl = sh_nl;
-    if (nl > 1024) {
-      *resolved = false;
-      *found = false;
-      __syncthreads();
-      return -INFINITY;
-    }
-    for (int i = tid; i < nl; i += kThreads) {
-      const float yi = Lb[i].y;
-      unsigned long long gt = 0, ge = 0;
-      for (int j = 0; j < nl; ++j) {
-        const float yj = Lb[j].y;
-        const unsigned long long wj = weighted ? weight_fx(yj) : 1ull;
-        if (yj > yi) gt += wj;
-        if (yj >= yi) ge += wj;
-      }
-      if (gt < t2 && t2 <= ge) sh_res = yi;
-    }
-    __syncthreads();
-    *found = true;
-    *resolved = true;
-    return sh_res;
-  };
-  // selects with the bucket method, falling back to the radix select
-  auto leader_select = [&](bool weighted, float lo, float hi, float ylo, unsigned long long target,
-                           bool* found) -> float {
-    bool resolved;
-    const float v = bucket_select(weighted, lo, hi, ylo, target, found, &resolved);
-    if (resolved) return v;
-    return local_select(weighted, ylo, target, found);
-  };
-  // every CTA stores its `count` candidates into slot `rank` of the leader's raw slice
-  // and arrives on the leader's gather barrier; only the leader continues
-  auto gather = [&](int count) -> bool {
-    Cand* dst = cluster.map_shared_rank(reinterpret_cast<Cand*>(S.raw), 0u) + rank * cap;
-    for (int i = tid; i < count; i += kThreads) dst[i] = cand[i];
-    __syncthreads();
-    if (tid == 0) mbar_arrive_remote(&mbar_gather, 0u);
-    if (rank != 0) return false;
-    if (tid == 0) sh_none = mbar_wait_cluster(&mbar_gather, 0) ? 0 : 1;
-    __syncthreads();
-    (void)mbar_try_wait_cluster(&mbar_gather, 0);  // every thread acquires the peers' stores
-    return true;
-  };
-  // appends (y, id) to the slice's candidate list; the whole warp calls it
-  auto append = [&](bool keep, float y, int id) {
-    const uint32_t bal = __ballot_sync(0xffffffffu, keep);
-    if (!bal) return;
-    const int leader = __ffs(bal) - 1;
-    int basepos = 0;
-    if (lane == leader) basepos = atomicAdd(&sh_count, __popc(bal));
-    basepos = __shfl_sync(0xffffffffu, basepos, leader);
-    if (keep) {
-      const int p = basepos + __popc(bal & ((1u << lane) - 1u));
-      if (p < cap) cand[p] = Cand{y, id};
-    }
-  };
-  auto finish_mine = [&](unsigned long long w, const Race& race) {
-    __syncthreads();
-    if (tid == 0) {
-      x2_mine.count = sh_count;
-      x2_mine.flags = sh_count > cap ? kFlagOverflow : 0;
-      x2_mine.w = w;
-      race.to(x2_mine);
-    }
-    __syncthreads();
-    push_all(cluster, x2, &x2_mine, rank, C);
-    cluster.sync();
-  };
+// ---------------------------------------------------------------- candidates and the leader
 
-  if (plan == kFast || plan == kUntrunc) {
-    // ---- pass B: compaction at z >= zth (exact), or the whole race
+// Appends (y, id) to the slice's candidate list; the whole warp calls it.
+__device__ __forceinline__ void append(Cand* cand, int cap, bool keep, float y, int id) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t bal = __ballot_sync(0xffffffffu, keep);
+  if (!bal) return;
+  const int leader = __ffs(bal) - 1;
+  int basepos = 0;
+  if (lane == leader) basepos = atomicAdd(&sh.count, __popc(bal));
+  basepos = __shfl_sync(0xffffffffu, basepos, leader);
+  if (keep) {
+    const int p = basepos + __popc(bal & ((1u << lane) - 1u));
+    if (p < cap) cand[p] = Cand{y, id};
+  }
+}
+
+// Publishes the slice's pass-B record (candidate count, top-p mass partial, race) to
+// every CTA: exchange 2 (or 3).
+__device__ void finish_mine(int cap, unsigned long long w, const Race& race) {
+  const cg::cluster_group cluster = cg::this_cluster();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    sh.x2_mine.count = sh.count;
+    sh.x2_mine.flags = (sh.count > cap ? kFlagOverflow : 0) | (sh.flags & kFlagRing);
+    sh.x2_mine.w = w;
+    race.to(sh.x2_mine);
+  }
+  __syncthreads();
+  push_all(cluster, sh.x2, &sh.x2_mine, (int)cluster.block_rank(), (int)cluster.num_blocks());
+  cluster.sync();
+}
+
+__device__ __forceinline__ int x2_flags(int C) {
+  int f = 0;
+  for (int c = 0; c < C; ++c) f |= sh.x2[c].flags;
+  return f;
+}
+
+// Every CTA stores its candidates into slot `rank` of the leader's gather area and
+// arrives on the leader's gather barrier; only the leader (rank 0) continues (returns
+// true).  Every CTA has finished reading its slice (a cluster barrier came before), so
+// the leader's ring and tables are free to be overwritten.
+__device__ bool gather_to_leader(const Smem& S, int cap, int count) {
+  const cg::cluster_group cluster = cg::this_cluster();
+  const int tid = threadIdx.x;
+  const int rank = (int)cluster.block_rank();
+  Cand* dst = cluster.map_shared_rank(S.gather, 0u) + rank * cap;
+  for (int i = tid; i < count; i += kThreads) dst[i] = S.cand[i];
+  __syncthreads();
+  if (tid == 0) mbar_arrive_remote(&sh.gather_bar, 0u);
+  if (rank != 0) return false;
+  if (tid == 0) sh.none = mbar_wait_cluster(&sh.gather_bar, 0) ? 0 : 1;
+  __syncthreads();
+  (void)mbar_try_wait_cluster(&sh.gather_bar, 0);  // every thread acquires the peers' stores
+  return true;
+}
+
+// Slot i of the gathered set belongs to CTA i / cap and is valid below that CTA's count.
+__device__ __forceinline__ bool gvalid(int i, int span, int cap) {
+  return i < span && (i & (cap - 1)) < sh.x2[i / cap].count;
+}
+
+// Radix select over the gathered set (entries with y >= ylo): the largest value v such
+// that the count (or fixed-point weight) of entries >= v reaches `target`.
+__device__ __noinline__ float local_select(int chunk, int span, int cap, bool weighted, float ylo,
+                                           unsigned long long target, bool* found) {
+  const Smem S = carve(chunk);
+  const Cand* G = S.gather;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  uint32_t prefix = 0u, pmask = 0u;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    if (tid < 256) {
+      S.hist_c[tid] = 0u;
+      S.hist_w[tid] = 0ull;
+    }
+    __syncthreads();
+    for (int base = 0; base < span; base += kThreads) {
+      const int i = base + tid;
+      const bool ok = gvalid(i, span, cap);
+      const float y = ok ? G[i].y : -INFINITY;
+      const uint32_t key = fkey(y);
+      const bool pred = ok && y >= ylo && (key & pmask) == prefix;
+      if (weighted)
+        hist_add<true>(S.hist_c, S.hist_w, pred, (key >> shift) & 0xFFu, pred ? weight_fx(y) : 0ull);
+      else
+        hist_add<false>(S.hist_c, S.hist_w, pred, (key >> shift) & 0xFFu, 0ull);
+    }
+    __syncthreads();
     if (warp == 0) {
-      const float zt = z_threshold_warp(theta, m, invT);
-      if (lane == 0) sh_zth = zt;
+      if (weighted) pick_digit(S.hist_w, target, &sh.digit, &sh.above, &sh.none);
+      else pick_digit(S.hist_c, target, &sh.digit, &sh.above, &sh.none);
     }
     __syncthreads();
-    const float zth = sh_zth;
-    unsigned long long w = 0;
-    Race race;
-    race.init();
-    for (int base = 0; base < nvec; base += kThreads) {
-      const int f = base + tid;
-      const uint32_t wd = f < nvec ? live4(S.live, f) : 0u;
-      float z[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      if (wd) {
-        const float4 v = sl.load4(f);
-        if (wd == 0xFu && finite4(v)) {
-          z[0] = v.x;
-          z[1] = v.y;
-          z[2] = v.z;
-          z[3] = v.w;
-        } else {
+    if (sh.none) {
+      *found = false;
+      __syncthreads();
+      return -INFINITY;
+    }
+    prefix |= (uint32_t)sh.digit << shift;
+    pmask |= 0xFFu << shift;
+    target -= sh.above;
+    __syncthreads();
+  }
+  *found = true;
+  return key_to_float(prefix);
+}
+
+// Exact select over the gathered set, entries with y >= ylo, all within [lo, hi]: one
+// 1024-bucket histogram (bucket order follows y), then the crossing bucket's entries are
+// resolved by counting.  Falls back to local_select when that bucket holds more than
+// 1024 entries (heavy ties).
+__device__ __noinline__ float leader_select(int chunk, int span, int cap, bool weighted, float lo, float hi,
+                                            float ylo, unsigned long long target, bool* found) {
+  const Smem S = carve(chunk);
+  const Cand* G = S.gather;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  unsigned long long* bk = reinterpret_cast<unsigned long long*>(S.r2);
+  constexpr int kPer = 1024 / kThreads;  // consecutive buckets per thread
+  const float scale = hi > lo ? 1024.0f / (hi - lo) : 0.0f;
+  auto bucket = [&](float y) -> int {
+    const int b = __float2int_rz(__fmul_rn(hi - y, scale));
+    return b < 0 ? 0 : (b > 1023 ? 1023 : b);
+  };
 #pragma unroll
-          for (int j = 0; j < 4; ++j) z[j] = ((wd >> j) & 1u) ? sanitize(comp(v, j)) : -INFINITY;
+  for (int t = 0; t < kPer; ++t) bk[kPer * tid + t] = 0ull;
+  if (tid == 0) {
+    sh.nl = 0;
+    sh.bstar = -1;
+  }
+  __syncthreads();
+  for (int i = tid; i < span; i += kThreads) {
+    if (!gvalid(i, span, cap)) continue;
+    const float y = G[i].y;
+    if (!(y >= ylo)) continue;
+    atomicAdd(&bk[bucket(y)], weighted ? weight_fx(y) : 1ull);
+  }
+  __syncthreads();
+  {
+    unsigned long long vb[kPer], loc = 0;
+#pragma unroll
+    for (int t = 0; t < kPer; ++t) {
+      vb[t] = bk[kPer * tid + t];
+      loc += vb[t];
+    }
+    unsigned long long x = loc;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const unsigned long long o = __shfl_up_sync(0xffffffffu, x, d);
+      if (lane >= d) x += o;
+    }
+    if (lane == 31) sh.red_u[warp] = x;
+    __syncthreads();
+    unsigned long long before = 0;
+    for (int w = 0; w < warp; ++w) before += sh.red_u[w];
+    const unsigned long long excl = before + x - loc, incl = before + x;
+    if (excl < target && target <= incl) {
+      unsigned long long cum = excl;
+      for (int t = 0; t < kPer; ++t) {
+        if (cum + vb[t] >= target) {
+          sh.bstar = kPer * tid + t;
+          sh.above = cum;
+          break;
         }
-        if (needW) {
+        cum += vb[t];
+      }
+    }
+  }
+  __syncthreads();
+  const int bstar = sh.bstar;
+  if (bstar < 0) {
+    *found = false;
+    return -INFINITY;
+  }
+  const unsigned long long t2 = target - sh.above;
+  // the crossing bucket's entries, gathered into the (now free) bucket area
+  Cand* Lb = reinterpret_cast<Cand*>(S.r2);
+  __syncthreads();
+  for (int i = tid; i < span; i += kThreads) {
+    if (!gvalid(i, span, cap)) continue;
+    const Cand cd = G[i];
+    if (!(cd.y >= ylo) || bucket(cd.y) != bstar) continue;
+    const int p = atomicAdd(&sh.nl, 1);
+    if (p < 1024) Lb[p] = cd;
+  }
+  __syncthreads();
+  const int nl = sh.nl;
+  if (nl > 1024) {
+    __syncthreads();
+    return local_select(chunk, span, cap, weighted, ylo, target, found);
+  }
+  for (int i = tid; i < nl; i += kThreads) {
+    const float yi = Lb[i].y;
+    unsigned long long gt = 0, ge = 0;
+    for (int j = 0; j < nl; ++j) {
+      const float yj = Lb[j].y;
+      const unsigned long long wj = weighted ? weight_fx(yj) : 1ull;
+      if (yj > yi) gt += wj;
+      if (yj >= yi) ge += wj;
+    }
+    if (gt < t2 && t2 <= ge) sh.res = yi;
+  }
+  __syncthreads();
+  *found = true;
+  return sh.res;
+}
+
+// The race over the gathered entries with y >= cut (block-reduced into thread 0).
+__device__ __noinline__ Race leader_race(int chunk, int span, int cap, float cut, unsigned long long seed,
+                                         unsigned long long pos) {
+  const Smem S = carve(chunk);
+  const Cand* G = S.gather;
+  Race r;
+  r.init();
+  for (int i = threadIdx.x; i < span; i += kThreads) {
+    if (!gvalid(i, span, cap)) continue;
+    const Cand cd = G[i];
+    if (!(cd.y >= cut)) continue;
+    r.add(cd.y, cd.id, pick_word(race_words_call((uint32_t)(cd.id >> 2), seed, pos), cd.id & 3));
+  }
+  block_reduce_race(r, sh.red_x);
+  return r;
+}
+
+// ---------------------------------------------------------------- routes
+
+// Rows with a provable bound (top-k, min-p) and untruncated rows.  Pass B compacts the
+// tokens at z >= zth (the exact z-space image of the y bound) and/or races every token;
+// the leader finishes top-k -> top-p -> min-p and the race over the gathered candidates.
+// Returns false when a compaction overflowed (the slow path takes over).
+template <bool kBF16>
+__device__ __noinline__ bool route_fast(const LaunchParams& P, int& pass) {
+  const Geo g = geo<kBF16>(P);
+  const Smem S = carve(g.chunk);
+  const clsample_args_t& a = P.a;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const RowParams q = sh.rp;
+  const float m = sh.rs.m, invT = sh.rs.invT, lnS = sh.rs.lnS, L = sh.rs.L, theta = sh.rs.theta;
+  const int plan = sh.rs.plan;
+  const bool needW = sh.rs.needW != 0;
+  const bool has_mod = a.hist_offs != nullptr || a.bias_offs != nullptr;
+  const bool kfin = q.k >= 2;
+  const unsigned long long seed = q.seed, pos = q.pos;
+  const int c0 = g.c0, cap = g.cap, C = g.C;
+  if (warp == 0) {
+    const float zt = z_threshold_warp(theta, m, invT);
+    if (lane == 0) sh.zth = zt;
+  }
+  __syncthreads();
+  const float zth = sh.zth;
+  unsigned long long w = 0;
+  Race race;
+  race.init();
+  stream<kBF16>(g, S, pass, false, [&](int f, uint32_t wd, const float4& v) {
+    float z[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    if (wd) {
+      if (wd == 0xFu && finite4(v)) {
+        z[0] = v.x;
+        z[1] = v.y;
+        z[2] = v.z;
+        z[3] = v.w;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) z[j] = ((wd >> j) & 1u) ? sanitize(comp(v, j)) : -INFINITY;
+      }
+      if (needW) {
+#pragma unroll 1
+        for (int j = 0; j < 4; ++j)
+          if (z[j] > -INFINITY) w += weight_fx(y_of(z[j], m, invT));
+      }
+      if (plan == kPlanUntrunc) {
+        float y[4];
+        bool live_any = false, worth = false;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          y[j] = z[j] > -INFINITY ? y_of(z[j], m, invT) : -INFINITY;
+          if (z[j] > -INFINITY) {
+            live_any = true;
+            worth |= y[j] + kGumbelMax >= race.s;
+          }
+        }
+        if (worth) {
+          const uint4 x = race_words_call((uint32_t)((c0 >> 2) + f), seed, pos);
+#pragma unroll 1
+          for (int j = 0; j < 4; ++j)
+            if (z[j] > -INFINITY) race.add(y[j], c0 + 4 * f + j, pick_word(x, j));
+        } else if (live_any) {
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            if (z[j] > -INFINITY) w += weight_fx(y_of(z[j], m, invT));
-        }
-        if (plan == kUntrunc) {
-          float y[4];
-          bool live_any = false, worth = false;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            y[j] = z[j] > -INFINITY ? y_of(z[j], m, invT) : -INFINITY;
-            if (z[j] > -INFINITY) {
-              live_any = true;
-              worth |= y[j] + kGumbelMax >= race.s;
-            }
-          }
-          if (worth) {
-            const uint4 x = race_words((uint32_t)((c0 >> 2) + f), seed, pos);
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if (z[j] > -INFINITY) race.add(y[j], c0 + 4 * f + j, pick_word(x, j));
-          } else if (live_any) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if (z[j] > -INFINITY) race.count_only(y[j]);
-          }
-        }
-      }
-      if (plan == kFast) {
-        const bool any = __any_sync(0xffffffffu, z[0] >= zth || z[1] >= zth || z[2] >= zth || z[3] >= zth);
-        if (any) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const bool keep = z[j] > -INFINITY && z[j] >= zth;
-            append(keep, keep ? y_of(z[j], m, invT) : 0.0f, c0 + 4 * f + j);
-          }
+            if (z[j] > -INFINITY) race.count_only(y[j]);
         }
       }
     }
-    if (has_mod) {
-      for (int base = 0; base < kHashCap; base += kThreads) {
-        const int i = base + tid;
-        float z = -INFINITY;
-        if (S.hkey[i] != kEmpty) z = S.hval[i];
-        const int g = c0 + (int)S.hkey[i];
-        const float y = z > -INFINITY ? y_of(z, m, invT) : -INFINITY;
-        if (z > -INFINITY) {
-          if (needW) w += weight_fx(y);
-          if (plan == kUntrunc) race.add(y, g, pick_word(race_words((uint32_t)(g >> 2), seed, pos), g & 3));
+    if (plan == kPlanFast) {
+      const bool any = __any_sync(0xffffffffu, z[0] >= zth || z[1] >= zth || z[2] >= zth || z[3] >= zth);
+      if (any) {
+#pragma unroll 1
+        for (int j = 0; j < 4; ++j) {
+          const bool keep = z[j] > -INFINITY && z[j] >= zth;
+          append(S.cand, cap, keep, keep ? y_of(z[j], m, invT) : 0.0f, c0 + 4 * f + j);
         }
-        if (plan == kFast) append(z > -INFINITY && z >= zth, y, g);
       }
     }
-    if (needW) w = block_sum_u64(w, red_u);
-    if (plan == kUntrunc) block_reduce_race(race, red_x);
-    finish_mine(w, race);  // exchange 2
+  });
+  if (has_mod) {
+    for (int base = 0; base < kHashCap; base += kThreads) {
+      const int i = base + tid;
+      float z = -INFINITY;
+      if (S.hkey[i] != kEmpty) z = S.hval[i];
+      const int gi = c0 + (int)S.hkey[i];
+      const float y = z > -INFINITY ? y_of(z, m, invT) : -INFINITY;
+      if (z > -INFINITY) {
+        if (needW) w += weight_fx(y);
+        if (plan == kPlanUntrunc) race.add(y, gi, pick_word(race_words_call((uint32_t)(gi >> 2), seed, pos), gi & 3));
+      }
+      if (plan == kPlanFast) append(S.cand, cap, z > -INFINITY && z >= zth, y, gi);
+    }
+  }
+  if (needW) w = block_sum_u64(w, sh.red_u);
+  if (plan == kPlanUntrunc) block_reduce_race(race, sh.red_x);
+  finish_mine(cap, w, race);  // exchange 2
+  const int fl = x2_flags(C);
 
-    if (plan == kUntrunc) {
-      // the winner is the same in every CTA; its owner writes the outputs
-      if (tid == 0) {
-        Race r;
-        r.init();
-        for (int c = 0; c < C; ++c) r.merge(x2[c]);
-        const int owner = r.tok == INT_MAX ? 0 : r.tok / chunk;
-        if (rank == owner) write_sampled(a, row, r, lnS, true);
-      }
-      if ((rs.flags & kFlagTimeout) && tid == 0) mbar_wait(&mbar_load, 0);
-      return;
+  if (plan == kPlanUntrunc) {
+    // the winner is the same in every CTA; its owner writes the outputs
+    if (tid == 0) {
+      Race r;
+      r.init();
+      for (int c = 0; c < C; ++c) r.merge(sh.x2[c]);
+      const int owner = r.tok == INT_MAX ? 0 : r.tok / g.chunk;
+      if (g.rank == owner) write_sampled(a, g.row, r, lnS, !(fl & kFlagRing));
     }
+    return true;
+  }
+  if (fl & kFlagOverflow) return false;
+  if (!gather_to_leader(S, cap, sh.x2[g.rank].count)) return true;
+  const bool gathered = sh.none == 0 && !(fl & kFlagRing);
+  const int span = C * cap;
+  int ntot = 0;
+  for (int c = 0; c < C; ++c) ntot += sh.x2[c].count;
+  float tk = -INFINITY;
+  if (kfin && ntot >= q.k) {
+    bool found;
+    const float v = leader_select(g.chunk, span, cap, false, theta, 0.0f, -INFINITY, (unsigned long long)q.k, &found);
+    if (found) tk = v;
+  }
+  float tp = -INFINITY;
+  if (q.p < 1.0f) {
+    unsigned long long mset = 0;
+    for (int i = tid; i < span; i += kThreads)
+      if (gvalid(i, span, cap) && S.gather[i].y >= tk) mset += weight_fx(S.gather[i].y);
+    mset = block_sum_u64(mset, sh.red_u);
+    unsigned long long Wk = mset;
+    if (!kfin) {
+      Wk = 0;
+      for (int c = 0; c < C; ++c) Wk += sh.x2[c].w;
+    }
+    const unsigned long long cth = ceil_scaled(Wk, q.p);
+    if (mset >= cth) {
+      bool found;
+      const float v = leader_select(g.chunk, span, cap, true, theta, 0.0f, tk, cth, &found);
+      if (found) tp = v;
+    }
+  }
+  const float cut = fmaxf(tk, fmaxf(tp, L));
+  const Race r = leader_race(g.chunk, span, cap, cut, seed, pos);
+  if (tid == 0) write_sampled(a, g.row, r, lnS, gathered);
+  return true;
+}
 
-    bool overflow = false;
-    for (int c = 0; c < C; ++c) overflow |= (x2[c].flags & kFlagOverflow) != 0;
-    if (!overflow) {
-      if (!gather(x2[rank].count)) {
-        if ((rs.flags & kFlagTimeout) && tid == 0) mbar_wait(&mbar_load, 0);
-        return;
-      }
-      const bool gathered = sh_none == 0;
-      int ntot = 0;
-      for (int c = 0; c < C; ++c) ntot += x2[c].count;
-      float tk = -INFINITY;
-      if (kfin && ntot >= q.k) {
-        bool found;
-        const float v = leader_select(false, theta, 0.0f, -INFINITY, (unsigned long long)q.k, &found);
-        if (found) tk = v;
-      }
-      float tp = -INFINITY;
-      if (q.p < 1.0f) {
-        unsigned long long mset = 0;
-        for (int i = tid; i < span; i += kThreads)
-          if (gvalid(i) && G[i].y >= tk) mset += weight_fx(G[i].y);
-        mset = block_sum_u64(mset, red_u);
-        unsigned long long Wk = mset;
-        if (!kfin) {
-          Wk = 0;
-          for (int c = 0; c < C; ++c) Wk += x2[c].w;
-        }
-        const unsigned long long cth = ceil_scaled(Wk, q.p);
-        if (mset >= cth) {
-          bool found;
-          const float v = leader_select(true, theta, 0.0f, tk, cth, &found);
-          if (found) tp = v;
-        }
-      }
-      const float cut = fmaxf(tk, fmaxf(tp, L));
-      Race race2;
-      race2.init();
-      for (int i = tid; i < span; i += kThreads) {
-        if (!gvalid(i)) continue;
-        const Cand cd = G[i];
-        if (!(cd.y >= cut)) continue;
-        race2.add(cd.y, cd.id, pick_word(race_words((uint32_t)(cd.id >> 2), seed, pos), cd.id & 3));
-      }
-      block_reduce_race(race2, red_x);
-      if (tid == 0) write_sampled(a, row, race2, lnS, gathered);
-      if ((rs.flags & kFlagTimeout) && tid == 0) mbar_wait(&mbar_load, 0);
-      return;
+// Top-p alone: the exact top-p mass of the row and its histogram over quarter-unit y bins
+// (warp-private, in the candidate area) fix the crossing bin (exchange 2); pass C races
+// the tokens above it in place and sends the crossing bin's tokens to the leader, which
+// resolves the cut inside the bin.  Returns false (slow path) when the crossing bin is
+// the open-ended last one or the band overflowed.
+template <bool kBF16>
+__device__ __noinline__ bool route_topp(const LaunchParams& P, int& pass) {
+  const Geo g = geo<kBF16>(P);
+  const Smem S = carve(g.chunk);
+  const clsample_args_t& a = P.a;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const RowParams q = sh.rp;
+  const float m = sh.rs.m, invT = sh.rs.invT, lnS = sh.rs.lnS;
+  const bool has_mod = a.hist_offs != nullptr || a.bias_offs != nullptr;
+  const unsigned long long seed = q.seed, pos = q.pos;
+  const int c0 = g.c0, cap = g.cap, C = g.C;
+  const cg::cluster_group cluster = cg::this_cluster();
+
+  unsigned long long* whist = reinterpret_cast<unsigned long long*>(S.cand);
+  for (int i = tid; i < kWarps * kPBins; i += kThreads) whist[i] = 0ull;
+  __syncthreads();
+  unsigned long long w = 0;
+  unsigned long long* mine = whist + warp * kPBins;
+  stream<kBF16>(g, S, pass, false, [&](int f, uint32_t wd, const float4& v) {
+    if (!wd) return;
+    const bool fastv = wd == 0xFu && finite4(v);
+#pragma unroll 1
+    for (int j = 0; j < 4; ++j) {
+      const float z = fastv ? comp(v, j) : (((wd >> j) & 1u) ? sanitize(comp(v, j)) : -INFINITY);
+      if (!(z > -INFINITY)) continue;
+      const float y = y_of(z, m, invT);
+      const unsigned long long qw = weight_fx(y);
+      if (!qw) continue;
+      w += qw;
+      atomicAdd(mine + pbin(y), qw);
     }
-  } else if (plan == kTopP) {
-    // ---- pass B': exact top-p mass of the row and its histogram over quarter-unit y
-    //      bins (warp-private, in the candidate area)
-    unsigned long long* whist = reinterpret_cast<unsigned long long*>(S.cand);
-    for (int i = tid; i < kWarps * kPBins; i += kThreads) whist[i] = 0ull;
-    __syncthreads();
-    unsigned long long w = 0;
-    unsigned long long* mine = whist + warp * kPBins;
-    for (int f = tid; f < nvec; f += kThreads) {
-      const uint32_t wd = live4(S.live, f);
-      if (!wd) continue;
-      const float4 v = sl.load4(f);
+  });
+  if (has_mod) {
+    for (int i = tid; i < kHashCap; i += kThreads) {
+      if (S.hkey[i] == kEmpty) continue;
+      const float z = S.hval[i];
+      if (!(z > -INFINITY)) continue;
+      const float y = y_of(z, m, invT);
+      const unsigned long long qw = weight_fx(y);
+      if (!qw) continue;
+      w += qw;
+      atomicAdd(mine + pbin(y), qw);
+    }
+  }
+  w = block_sum_u64(w, sh.red_u);
+  // merge the warp histograms and push them into every CTA's merged copy
+  if (tid < kPBins) {
+    unsigned long long t = 0;
+    for (int wp = 0; wp < kWarps; ++wp) t += whist[wp * kPBins + tid];
+    if (t)
+      for (int r = 0; r < C; ++r) atomicAdd(cluster.map_shared_rank(S.mrg_w + tid, (unsigned)r), t);
+  }
+  Race none_race;
+  none_race.init();
+  finish_mine(cap, w, none_race);  // exchange 2
+  unsigned long long W = 0;
+  for (int c = 0; c < C; ++c) W += sh.x2[c].w;
+  const unsigned long long cth = ceil_scaled(W, q.p);
+  // crossing bin: the running mass from the top first reaches cth in bin bstar
+  int bstar = kPBins - 1;
+  unsigned long long above = 0;
+  {
+    unsigned long long cum = 0;
+    for (int b = 0; b < kPBins; ++b) {
+      const unsigned long long nb = cum + S.mrg_w[b];
+      if (nb >= cth) {
+        bstar = b;
+        above = cum;
+        break;
+      }
+      cum = nb;
+    }
+  }
+  if (bstar >= kPBins - 1) return false;
+  // pass C: tokens above the crossing bin are certainly kept: race them here; tokens of
+  // the crossing bin go to the leader
+  const float yhi = -(float)bstar * 0.25f, ylo = -(float)(bstar + 1) * 0.25f;
+  __syncthreads();
+  if (tid == 0) sh.count = 0;
+  __syncthreads();
+  Race race;
+  race.init();
+  stream<kBF16>(g, S, pass, false, [&](int f, uint32_t wd, const float4& v) {
+    float y[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    if (wd) {
       const bool fastv = wd == 0xFu && finite4(v);
+      bool worth = false;
+      uint32_t sure = 0u;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const float z = fastv ? comp(v, j) : (((wd >> j) & 1u) ? sanitize(comp(v, j)) : -INFINITY);
         if (!(z > -INFINITY)) continue;
-        const float y = y_of(z, m, invT);
-        const unsigned long long qw = weight_fx(y);
-        if (!qw) continue;
-        w += qw;
-        atomicAdd(mine + pbin(y), qw);
-      }
-    }
-    if (has_mod) {
-      for (int i = tid; i < kHashCap; i += kThreads) {
-        if (S.hkey[i] == kEmpty) continue;
-        const float z = S.hval[i];
-        if (!(z > -INFINITY)) continue;
-        const float y = y_of(z, m, invT);
-        const unsigned long long qw = weight_fx(y);
-        if (!qw) continue;
-        w += qw;
-        atomicAdd(mine + pbin(y), qw);
-      }
-    }
-    w = block_sum_u64(w, red_u);
-    // merge the warp histograms and push them into every CTA's merged copy
-    if (tid < kPBins) {
-      unsigned long long t = 0;
-      for (int wp = 0; wp < kWarps; ++wp) t += whist[wp * kPBins + tid];
-      if (t)
-        for (int r = 0; r < C; ++r) atomicAdd(cluster.map_shared_rank(S.mrg_w + tid, (unsigned)r), t);
-    }
-    Race none_race;
-    none_race.init();
-    finish_mine(w, none_race);  // exchange 2
-    unsigned long long W = 0;
-    for (int c = 0; c < C; ++c) W += x2[c].w;
-    const unsigned long long cth = ceil_scaled(W, q.p);
-    // crossing bin: the running mass from the top first reaches cth in bin bstar
-    int bstar = kPBins - 1;
-    unsigned long long above = 0;
-    {
-      unsigned long long cum = 0;
-      for (int b = 0; b < kPBins; ++b) {
-        const unsigned long long nb = cum + S.mrg_w[b];
-        if (nb >= cth) {
-          bstar = b;
-          above = cum;
-          break;
+        y[j] = y_of(z, m, invT);
+        if (y[j] > yhi) {
+          sure |= 1u << j;
+          worth |= y[j] + kGumbelMax >= race.s;
         }
-        cum = nb;
       }
-    }
-    if (bstar < kPBins - 1) {
-      // ---- pass C: tokens above the crossing bin are certainly kept: race them here;
-      //      tokens of the crossing bin go to the leader
-      const float yhi = -(float)bstar * 0.25f, ylo = -(float)(bstar + 1) * 0.25f;
-      __syncthreads();
-      if (tid == 0) sh_count = 0;
-      __syncthreads();
-      Race race;
-      race.init();
-      for (int base = 0; base < nvec; base += kThreads) {
-        const int f = base + tid;
-        const uint32_t wd = f < nvec ? live4(S.live, f) : 0u;
-        float y[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        if (wd) {
-          const float4 v = sl.load4(f);
-          const bool fastv = wd == 0xFu && finite4(v);
-          bool worth = false;
-          uint32_t sure = 0u;
+      if (sure) {
+        if (worth) {
+          const uint4 x = race_words_call((uint32_t)((c0 >> 2) + f), seed, pos);
+#pragma unroll 1
+          for (int j = 0; j < 4; ++j)
+            if ((sure >> j) & 1u) race.add(y[j], c0 + 4 * f + j, pick_word(x, j));
+        } else {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float z = fastv ? comp(v, j) : (((wd >> j) & 1u) ? sanitize(comp(v, j)) : -INFINITY);
-            if (!(z > -INFINITY)) continue;
-            y[j] = y_of(z, m, invT);
-            if (y[j] > yhi) {
-              sure |= 1u << j;
-              worth |= y[j] + kGumbelMax >= race.s;
-            }
-          }
-          if (sure) {
-            if (worth) {
-              const uint4 x = race_words((uint32_t)((c0 >> 2) + f), seed, pos);
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-                if ((sure >> j) & 1u) race.add(y[j], c0 + 4 * f + j, pick_word(x, j));
-            } else {
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-                if ((sure >> j) & 1u) race.count_only(y[j]);
-            }
-          }
+          for (int j = 0; j < 4; ++j)
+            if ((sure >> j) & 1u) race.count_only(y[j]);
         }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) append(y[j] > ylo && y[j] <= yhi, y[j], c0 + 4 * f + j);
-      }
-      if (has_mod) {
-        for (int base = 0; base < kHashCap; base += kThreads) {
-          const int i = base + tid;
-          float y = -INFINITY;
-          int g = 0;
-          if (S.hkey[i] != kEmpty && S.hval[i] > -INFINITY) {
-            y = y_of(S.hval[i], m, invT);
-            g = c0 + (int)S.hkey[i];
-            if (y > yhi) race.add(y, g, pick_word(race_words((uint32_t)(g >> 2), seed, pos), g & 3));
-          }
-          append(y > ylo && y <= yhi, y, g);
-        }
-      }
-      block_reduce_race(race, red_x);
-      finish_mine(0ull, race);  // exchange 3
-      bool overflow = false;
-      for (int c = 0; c < C; ++c) overflow |= (x2[c].flags & kFlagOverflow) != 0;
-      if (!overflow) {
-        if (!gather(x2[rank].count)) {
-          if ((rs.flags & kFlagTimeout) && tid == 0) mbar_wait(&mbar_load, 0);
-          return;
-        }
-        const bool gathered = sh_none == 0;
-        // the cut lies in the crossing bin: a weighted select over its tokens
-        bool found;
-        const float vstar = leader_select(true, ylo, yhi, -INFINITY, cth - above, &found);
-        Race race2;
-        race2.init();
-        for (int i = tid; i < span; i += kThreads) {
-          if (!gvalid(i)) continue;
-          const Cand cd = G[i];
-          if (!(cd.y >= vstar)) continue;
-          race2.add(cd.y, cd.id, pick_word(race_words((uint32_t)(cd.id >> 2), seed, pos), cd.id & 3));
-        }
-        block_reduce_race(race2, red_x);
-        if (tid == 0) {
-          for (int c = 0; c < C; ++c) race2.merge(x2[c]);
-          write_sampled(a, row, race2, lnS, gathered && found);
-        }
-        if ((rs.flags & kFlagTimeout) && tid == 0) mbar_wait(&mbar_load, 0);
-        return;
       }
     }
-    // the crossing bin is the open-ended last one, or the band overflowed: slow path
+    const bool any = __any_sync(0xffffffffu, (y[0] > ylo && y[0] <= yhi) || (y[1] > ylo && y[1] <= yhi) ||
+                                                 (y[2] > ylo && y[2] <= yhi) || (y[3] > ylo && y[3] <= yhi));
+    if (any) {
+#pragma unroll 1
+      for (int j = 0; j < 4; ++j) append(S.cand, cap, y[j] > ylo && y[j] <= yhi, y[j], c0 + 4 * f + j);
+    }
+  });
+  if (has_mod) {
+    for (int base = 0; base < kHashCap; base += kThreads) {
+      const int i = base + tid;
+      float y = -INFINITY;
+      int gi = 0;
+      if (S.hkey[i] != kEmpty && S.hval[i] > -INFINITY) {
+        y = y_of(S.hval[i], m, invT);
+        gi = c0 + (int)S.hkey[i];
+        if (y > yhi) race.add(y, gi, pick_word(race_words_call((uint32_t)(gi >> 2), seed, pos), gi & 3));
+      }
+      append(S.cand, cap, y > ylo && y <= yhi, y, gi);
+    }
   }
+  block_reduce_race(race, sh.red_x);
+  finish_mine(cap, 0ull, race);  // exchange 3
+  const int fl = x2_flags(C);
+  if (fl & kFlagOverflow) return false;
+  if (!gather_to_leader(S, cap, sh.x2[g.rank].count)) return true;
+  const bool gathered = sh.none == 0 && !(fl & kFlagRing);
+  // the cut lies in the crossing bin: a weighted select over its tokens
+  bool found;
+  const int span = C * cap;
+  const float vstar = leader_select(g.chunk, span, cap, true, ylo, yhi, -INFINITY, cth - above, &found);
+  Race r = leader_race(g.chunk, span, cap, vstar, seed, pos);
+  if (tid == 0) {
+    for (int c = 0; c < C; ++c) r.merge(sh.x2[c]);
+    write_sampled(a, g.row, r, lnS, gathered && found);
+  }
+  return true;
+}
 
-  // ---- slow path: cluster-wide radix selects over the resident slices.  Histograms
-  //      are pushed into every CTA's merged copy with DSMEM atomics, one barrier per
-  //      digit; the merged copies are double-buffered and cleared after use.
+// Cluster-wide radix select over the slices (one pass over the slice per 8-bit digit):
+// the largest value v such that the count (or fixed-point weight) of kept-side tokens
+// with y >= v reaches `target`, among tokens with y >= ylo.  Histograms are pushed into
+// every CTA's merged copy with DSMEM atomics, one cluster barrier per digit; the merged
+// copies are double-buffered and cleared after use.
+template <bool kBF16>
+__device__ __noinline__ float cluster_select(const LaunchParams& P, int& pass, int& gpass, bool weighted, float ylo,
+                                             unsigned long long target, bool* found) {
+  const Geo g = geo<kBF16>(P);
+  const Smem S = carve(g.chunk);
+  const clsample_args_t& a = P.a;
+  const cg::cluster_group cluster = cg::this_cluster();
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const float m = sh.rs.m, invT = sh.rs.invT;
+  const bool has_mod = a.hist_offs != nullptr || a.bias_offs != nullptr;
+  uint32_t prefix = 0u, pmask = 0u;
+  bool ok_all = true;
+  for (int dpass = 0; dpass < 4; ++dpass, ++gpass) {
+    const int shift = 24 - 8 * dpass;
+    const int buf = gpass & 1;
+    if (tid < 256) {
+      S.hist_c[tid] = 0u;
+      S.hist_w[tid] = 0ull;
+    }
+    __syncthreads();
+    stream<kBF16>(g, S, pass, false, [&](int f, uint32_t wd, const float4& v) {
+#pragma unroll 1
+      for (int j = 0; j < 4; ++j) {
+        bool pred = false;
+        float y = -INFINITY;
+        if ((wd >> j) & 1u) {
+          const float z = sanitize(comp(v, j));
+          if (z > -INFINITY) {
+            y = y_of(z, m, invT);
+            pred = y >= ylo && (fkey(y) & pmask) == prefix;
+          }
+        }
+        const uint32_t digit = (fkey(y) >> shift) & 0xFFu;
+        if (weighted)
+          hist_add<true>(S.hist_c, S.hist_w, pred, digit, pred ? weight_fx(y) : 0ull);
+        else
+          hist_add<false>(S.hist_c, S.hist_w, pred, digit, 0ull);
+      }
+    });
+    if (has_mod) {
+      for (int base = 0; base < kHashCap; base += kThreads) {
+        const int i = base + tid;
+        bool pred = false;
+        float y = -INFINITY;
+        if (S.hkey[i] != kEmpty) {
+          const float z = S.hval[i];
+          if (z > -INFINITY) {
+            y = y_of(z, m, invT);
+            pred = y >= ylo && (fkey(y) & pmask) == prefix;
+          }
+        }
+        const uint32_t digit = (fkey(y) >> shift) & 0xFFu;
+        if (weighted)
+          hist_add<true>(S.hist_c, S.hist_w, pred, digit, pred ? weight_fx(y) : 0ull);
+        else
+          hist_add<false>(S.hist_c, S.hist_w, pred, digit, 0ull);
+      }
+    }
+    __syncthreads();
+    for (int i = tid; i < 256 * g.C; i += kThreads) {
+      const int bin = i & 255, r = i >> 8;
+      if (weighted) {
+        const unsigned long long hv = S.hist_w[bin];
+        if (hv) atomicAdd(cluster.map_shared_rank(S.mrg_w + buf * 256 + bin, (unsigned)r), hv);
+      } else {
+        const uint32_t hv = S.hist_c[bin];
+        if (hv) atomicAdd(cluster.map_shared_rank(S.mrg_c + buf * 256 + bin, (unsigned)r), hv);
+      }
+    }
+    cluster.sync();
+    if (warp == 0) {
+      if (weighted) pick_digit(S.mrg_w + buf * 256, target, &sh.digit, &sh.above, &sh.none);
+      else pick_digit(S.mrg_c + buf * 256, target, &sh.digit, &sh.above, &sh.none);
+    }
+    __syncthreads();
+    const bool none = sh.none != 0;
+    const int dg = sh.digit;
+    const unsigned long long ab = sh.above;
+    // clear this buffer for its next use (two digits later, after another barrier)
+    if (tid < 256) {
+      S.mrg_c[buf * 256 + tid] = 0u;
+      S.mrg_w[buf * 256 + tid] = 0ull;
+    }
+    __syncthreads();
+    if (none) ok_all = false;
+    if (ok_all) {
+      prefix |= (uint32_t)dg << shift;
+      pmask |= 0xFFu << shift;
+      target -= ab;
+    }
+  }
+  *found = ok_all;
+  return ok_all ? key_to_float(prefix) : -INFINITY;
+}
+
+// Rows without a usable bound (very large k, compaction overflow, top-p with an
+// open-ended crossing bin): exact cluster-wide selects, then the race in place.
+template <bool kBF16>
+__device__ __noinline__ void route_slow(const LaunchParams& P, int& pass) {
+  const Geo g = geo<kBF16>(P);
+  const Smem S = carve(g.chunk);
+  const clsample_args_t& a = P.a;
+  const cg::cluster_group cluster = cg::this_cluster();
+  const int tid = threadIdx.x;
+  const RowParams q = sh.rp;
+  const float m = sh.rs.m, invT = sh.rs.invT, lnS = sh.rs.lnS, L = sh.rs.L;
+  const bool has_mod = a.hist_offs != nullptr || a.bias_offs != nullptr;
+  const unsigned long long seed = q.seed, pos = q.pos;
+  const int c0 = g.c0, C = g.C;
+  const bool kfin = q.k >= 2;
+
   for (int i = tid; i < 2 * 256; i += kThreads) {
     S.mrg_c[i] = 0u;
     S.mrg_w[i] = 0ull;
   }
   cluster.sync();  // every merged copy is clear before the first push
   int gpass = 0;
-  auto cluster_select = [&](bool weighted, float ylo, unsigned long long target, bool* found) -> float {
-    uint32_t prefix = 0u, pmask = 0u;
-    bool ok_all = true;
-    for (int pass = 0; pass < 4; ++pass, ++gpass) {
-      const int shift = 24 - 8 * pass;
-      const int buf = gpass & 1;
-      if (tid < 256) {
-        S.hist_c[tid] = 0u;
-        S.hist_w[tid] = 0ull;
-      }
-      __syncthreads();
-      for (int base = 0; base < nvec; base += kThreads) {
-        const int f = base + tid;
-        const uint32_t wd = f < nvec ? live4(S.live, f) : 0u;
-        const float4 v = wd ? sl.load4(f) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          bool pred = false;
-          float y = -INFINITY;
-          if ((wd >> j) & 1u) {
-            const float z = sanitize(comp(v, j));
-            if (z > -INFINITY) {
-              y = y_of(z, m, invT);
-              pred = y >= ylo && (fkey(y) & pmask) == prefix;
-            }
-          }
-          const uint32_t digit = (fkey(y) >> shift) & 0xFFu;
-          if (weighted)
-            hist_add<true>(S.hist_c, S.hist_w, pred, digit, pred ? weight_fx(y) : 0ull);
-          else
-            hist_add<false>(S.hist_c, S.hist_w, pred, digit, 0ull);
-        }
-      }
-      if (has_mod) {
-        for (int base = 0; base < kHashCap; base += kThreads) {
-          const int i = base + tid;
-          bool pred = false;
-          float y = -INFINITY;
-          if (S.hkey[i] != kEmpty) {
-            const float z = S.hval[i];
-            if (z > -INFINITY) {
-              y = y_of(z, m, invT);
-              pred = y >= ylo && (fkey(y) & pmask) == prefix;
-            }
-          }
-          const uint32_t digit = (fkey(y) >> shift) & 0xFFu;
-          if (weighted)
-            hist_add<true>(S.hist_c, S.hist_w, pred, digit, pred ? weight_fx(y) : 0ull);
-          else
-            hist_add<false>(S.hist_c, S.hist_w, pred, digit, 0ull);
-        }
-      }
-      __syncthreads();
-      for (int i = tid; i < 256 * C; i += kThreads) {
-        const int bin = i & 255, r = i >> 8;
-        if (weighted) {
-          const unsigned long long hv = S.hist_w[bin];
-          if (hv) atomicAdd(cluster.map_shared_rank(S.mrg_w + buf * 256 + bin, (unsigned)r), hv);
-        } else {
-          const uint32_t hv = S.hist_c[bin];
-          if (hv) atomicAdd(cluster.map_shared_rank(S.mrg_c + buf * 256 + bin, (unsigned)r), hv);
-        }
-      }
-      cluster.sync();
-      if (warp == 0) {
-        if (weighted) pick_digit(S.mrg_w + buf * 256, target, &sh_digit, &sh_above, &sh_none);
-        else pick_digit(S.mrg_c + buf * 256, target, &sh_digit, &sh_above, &sh_none);
-      }
-      __syncthreads();
-      const bool none = sh_none != 0;
-      const int dg = sh_digit;
-      const unsigned long long ab = sh_above;
-      // clear this buffer for its next use (two passes later, after another barrier)
-      if (tid < 256) {
-        S.mrg_c[buf * 256 + tid] = 0u;
-        S.mrg_w[buf * 256 + tid] = 0ull;
-      }
-      __syncthreads();
-      if (none) ok_all = false;
-      if (ok_all) {
-        prefix |= (uint32_t)dg << shift;
-        pmask |= 0xFFu << shift;
-        target -= ab;
-      }
-    }
-    *found = ok_all;
-    return ok_all ? key_to_float(prefix) : -INFINITY;
-  };
-
   float tk = -INFINITY;
   if (kfin) {
     bool found;
-    const float v = cluster_select(false, -INFINITY, (unsigned long long)q.k, &found);
+    const float v = cluster_select<kBF16>(P, pass, gpass, false, -INFINITY, (unsigned long long)q.k, &found);
     if (found) tk = v;  // fewer than k candidates: top-k keeps them all
   }
   float tp = -INFINITY;
   if (q.p < 1.0f) {
     unsigned long long w = 0;
-    for (int f = tid; f < nvec; f += kThreads) {
-      const uint32_t wd = live4(S.live, f);
-      if (!wd) continue;
-      const float4 v = sl.load4(f);
-#pragma unroll
+    stream<kBF16>(g, S, pass, false, [&](int f, uint32_t wd, const float4& v) {
+#pragma unroll 1
       for (int j = 0; j < 4; ++j) {
         if (!((wd >> j) & 1u)) continue;
         const float z = sanitize(comp(v, j));
@@ -1588,7 +1812,7 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_kernel(const LaunchParams
         const float y = y_of(z, m, invT);
         if (y >= tk) w += weight_fx(y);
       }
-    }
+    });
     if (has_mod)
       for (int i = tid; i < kHashCap; i += kThreads) {
         if (S.hkey[i] == kEmpty) continue;
@@ -1597,24 +1821,21 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_kernel(const LaunchParams
         const float y = y_of(z, m, invT);
         if (y >= tk) w += weight_fx(y);
       }
-    w = block_sum_u64(w, red_u);
-    if (tid == 0) x2_mine.w = w;
+    w = block_sum_u64(w, sh.red_u);
+    if (tid == 0) sh.x2_mine.w = w;
     __syncthreads();
-    push_all(cluster, x2, &x2_mine, rank, C);
+    push_all(cluster, sh.x2, &sh.x2_mine, g.rank, C);
     cluster.sync();
     unsigned long long W = 0;
-    for (int c = 0; c < C; ++c) W += x2[c].w;
+    for (int c = 0; c < C; ++c) W += sh.x2[c].w;
     bool found;
-    const float v = cluster_select(true, tk, ceil_scaled(W, q.p), &found);
+    const float v = cluster_select<kBF16>(P, pass, gpass, true, tk, ceil_scaled(W, q.p), &found);
     if (found) tp = v;
   }
   const float cut = fmaxf(tk, fmaxf(tp, L));
   Race race;
   race.init();
-  for (int f = tid; f < nvec; f += kThreads) {
-    const uint32_t wd = live4(S.live, f);
-    if (!wd) continue;
-    const float4 v = sl.load4(f);
+  stream<kBF16>(g, S, pass, false, [&](int f, uint32_t wd, const float4& v) {
     float y[4];
     uint32_t keep = 0u;
 #pragma unroll
@@ -1626,12 +1847,12 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_kernel(const LaunchParams
       y[j] = y_of(z, m, invT);
       if (y[j] >= cut) keep |= 1u << j;
     }
-    if (!keep) continue;
-    const uint4 x = race_words((uint32_t)((c0 >> 2) + f), seed, pos);
-#pragma unroll
+    if (!keep) return;
+    const uint4 x = race_words_call((uint32_t)((c0 >> 2) + f), seed, pos);
+#pragma unroll 1
     for (int j = 0; j < 4; ++j)
       if ((keep >> j) & 1u) race.add(y[j], c0 + 4 * f + j, pick_word(x, j));
-  }
+  });
   if (has_mod)
     for (int i = tid; i < kHashCap; i += kThreads) {
       if (S.hkey[i] == kEmpty) continue;
@@ -1639,27 +1860,52 @@ __global__ void __launch_bounds__(kThreads, 2) sampler_kernel(const LaunchParams
       if (!(z > -INFINITY)) continue;
       const float y = y_of(z, m, invT);
       if (!(y >= cut)) continue;
-      const int g = c0 + (int)S.hkey[i];
-      race.add(y, g, pick_word(race_words((uint32_t)(g >> 2), seed, pos), g & 3));
+      const int gi = c0 + (int)S.hkey[i];
+      race.add(y, gi, pick_word(race_words_call((uint32_t)(gi >> 2), seed, pos), gi & 3));
     }
-  block_reduce_race(race, red_x);
+  block_reduce_race(race, sh.red_x);
   __syncthreads();
-  if (tid == 0) race.to(x2_mine);
+  if (tid == 0) {
+    race.to(sh.x2_mine);
+    sh.x2_mine.flags = sh.flags & kFlagRing;
+  }
   __syncthreads();
-  push_all(cluster, x2, &x2_mine, rank, C);
+  push_all(cluster, sh.x2, &sh.x2_mine, g.rank, C);
   cluster.sync();
   // the winner is the same in every CTA; its owner writes the outputs
   if (tid == 0) {
     Race r;
     r.init();
-    for (int c = 0; c < C; ++c) r.merge(x2[c]);
-    const int owner = r.tok == INT_MAX ? 0 : r.tok / chunk;
-    if (rank == owner) write_sampled(a, row, r, lnS, true);
+    for (int c = 0; c < C; ++c) r.merge(sh.x2[c]);
+    const int owner = r.tok == INT_MAX ? 0 : r.tok / g.chunk;
+    if (g.rank == owner) write_sampled(a, g.row, r, lnS, !(x2_flags(C) & kFlagRing));
   }
-  if ((rs.flags & kFlagTimeout) && tid == 0) mbar_wait(&mbar_load, 0);
+}
+
+// ---------------------------------------------------------------- the kernel
+
+template <bool kBF16>
+__global__ void __launch_bounds__(kThreads, kMinBlocks) sampler_kernel(const __grid_constant__ LaunchParams P) {
+  // DSMEM may only be touched once every CTA of the cluster runs: arrive now, wait just
+  // before the first push (exchange1)
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  prologue<kBF16>(P);
+  pass_a<kBF16>(P);
+  exchange1(P);
+  if (finish_early(P)) return;
+  plan_row();
+  int pass = 1;
+  const int plan = sh.rs.plan;
+  if (plan == kPlanFast || plan == kPlanUntrunc) {
+    if (route_fast<kBF16>(P, pass)) return;
+  } else if (plan == kPlanTopP) {
+    if (route_topp<kBF16>(P, pass)) return;
+  }
+  route_slow<kBF16>(P, pass);
 }
 
 // ---------------------------------------------------------------- diagnostics kernels
+
 
 __global__ void debug_weights_kernel(const float* y, unsigned long long* w, int n) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -1671,32 +1917,26 @@ __global__ void debug_uniforms_kernel(const uint64_t* seeds, const int64_t* pos,
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
   const long long t = tok[i];
-  const uint4 x = race_words((uint32_t)((unsigned long long)t >> 2), seeds[i], (unsigned long long)pos[i]);
+  const uint4 x = race_words_call((uint32_t)((unsigned long long)t >> 2), seeds[i], (unsigned long long)pos[i]);
   u[i] = word_to_uniform(pick_word(x, (int)(t & 3)));
 }
 
 // ---------------------------------------------------------------- host side
 
-Geometry geometry_for(int vocab, int esize) {
+// C = ceil(V / 2048) CTAs per row, at most the portable cluster size; slices are whole
+// bitmask words.  Shared memory does not depend on the logits type.
+Geometry geometry_for(int vocab) {
   Geometry g{0, 0, 0, 0};
   if (vocab <= 0) return g;
   int C = (vocab + 2047) / 2048;
-  if (C > 8) C = 8;
-  if (C < 1) C = 1;
-  int chunk = ((vocab + C - 1) / C + 31) / 32 * 32;
-  if (smem_bytes_for(chunk, 4) > 112 * 1024 && C == 8) {  // two CTAs per SM no longer fit
-    C = kMaxCluster;
-    chunk = ((vocab + C - 1) / C + 31) / 32 * 32;
-  }
+  if (C > kMaxCluster) C = kMaxCluster;
+  const int chunk = ((vocab + C - 1) / C + 31) / 32 * 32;
   if (chunk > kMaxChunk) return g;  // C = 0: vocabulary too large
   g.C = C;
   g.chunk = chunk;
-  g.smem = (int)smem_bytes_for(chunk, esize);
-  const int by_raw = (int)((size_t)chunk * esize / (sizeof(Cand) * C));
-  int cap = 1;  // largest power of two within both limits
-  while (cap * 2 <= by_raw && cap * 2 <= kCandCap) cap *= 2;
-  g.cap = cap;
-  if ((int)smem_bytes_for(chunk, 4) > 227 * 1024) g.C = 0;
+  g.smem = (int)layout_for(chunk).total;
+  g.cap = kCandCap;
+  static_assert(kCandCap * kMaxCluster <= kGatherCap, "the leader cannot gather every candidate");
   return g;
 }
 
@@ -1706,7 +1946,7 @@ struct clsample_handle {
   int max_batch;
   int vocab;
   int device;
-  Geometry g32, g16;
+  Geometry g;
 };
 
 extern "C" {
@@ -1726,7 +1966,7 @@ const char* clsample_strerror(int code) {
 }
 
 int clsample_geometry(int32_t vocab, int32_t* cluster, int32_t* chunk, int32_t* smem_bytes) {
-  const Geometry g = geometry_for(vocab, 4);
+  const Geometry g = geometry_for(vocab);
   if (g.C == 0) return CLSAMPLE_ERR_VOCAB;
   if (cluster) *cluster = g.C;
   if (chunk) *chunk = g.chunk;
@@ -1738,8 +1978,8 @@ int clsample_create(int32_t max_batch, int32_t vocab, clsample_t** out) {
   if (!out) return CLSAMPLE_ERR_NULL;
   *out = nullptr;
   if (max_batch < 0) return CLSAMPLE_ERR_BATCH;
-  const Geometry g32 = geometry_for(vocab, 4), g16 = geometry_for(vocab, 2);
-  if (g32.C == 0) return CLSAMPLE_ERR_VOCAB;
+  const Geometry g = geometry_for(vocab);
+  if (g.C == 0) return CLSAMPLE_ERR_VOCAB;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return CLSAMPLE_ERR_CUDA;
   int major = 0, minor = 0, optin = 0;
@@ -1748,23 +1988,17 @@ int clsample_create(int32_t max_batch, int32_t vocab, clsample_t** out) {
       cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
     return CLSAMPLE_ERR_CUDA;
   if (major != 10 || minor != 3) return CLSAMPLE_ERR_DEVICE;
-  if (g32.smem > optin) return CLSAMPLE_ERR_VOCAB;
+  if (g.smem > optin) return CLSAMPLE_ERR_DEVICE;
   const void* k32 = reinterpret_cast<const void*>(&sampler_kernel<false>);
   const void* k16 = reinterpret_cast<const void*>(&sampler_kernel<true>);
-  if (cudaFuncSetAttribute(k32, cudaFuncAttributeMaxDynamicSharedMemorySize, g32.smem) != cudaSuccess ||
-      cudaFuncSetAttribute(k16, cudaFuncAttributeMaxDynamicSharedMemorySize, g16.smem) != cudaSuccess)
+  if (cudaFuncSetAttribute(k32, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem) != cudaSuccess ||
+      cudaFuncSetAttribute(k16, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem) != cudaSuccess)
     return CLSAMPLE_ERR_CUDA;
-  if (g32.C > 8) {
-    if (cudaFuncSetAttribute(k32, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess ||
-        cudaFuncSetAttribute(k16, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-      return CLSAMPLE_ERR_CUDA;
-  }
   clsample_t* h = new clsample_t;
   h->max_batch = max_batch;
   h->vocab = vocab;
   h->device = dev;
-  h->g32 = g32;
-  h->g16 = g16;
+  h->g = g;
   *out = h;
   return CLSAMPLE_SUCCESS;
 }
@@ -1802,7 +2036,7 @@ int clsample_apply(clsample_t* h, const clsample_args_t* a, clsample_stream_t st
   if (dev != h->device) return CLSAMPLE_ERR_DEVICE;
 
   const bool bf16 = a->logits_dtype == CLSAMPLE_LOGITS_BF16;
-  const Geometry& g = bf16 ? h->g16 : h->g32;
+  const Geometry& g = h->g;
   const int esize = bf16 ? 2 : 4;
   LaunchParams P;
   P.a = *a;
@@ -1810,7 +2044,7 @@ int clsample_apply(clsample_t* h, const clsample_args_t* a, clsample_stream_t st
   P.chunk = g.chunk;
   P.cap = g.cap;
   const uintptr_t base = reinterpret_cast<uintptr_t>(a->logits);
-  P.bulk_ok = (base % 16 == 0) && (((long long)a->logits_row_stride * esize) % 16 == 0);
+  P.vec_ok = (base % 16 == 0) && (((long long)a->logits_row_stride * esize) % 16 == 0);
 
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
@@ -1826,7 +2060,7 @@ int clsample_occupancy(clsample_t* h, int32_t logits_dtype, int32_t* max_active_
   const bool bf16 = logits_dtype == CLSAMPLE_LOGITS_BF16;
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
-  fill_launch(bf16 ? h->g16 : h->g32, 1u, nullptr, &cfg, attr);
+  fill_launch(h->g, 1u, nullptr, &cfg, attr);
   int n = 0;
   const cudaError_t err = bf16 ? cudaOccupancyMaxActiveClusters(&n, sampler_kernel<true>, &cfg)
                                : cudaOccupancyMaxActiveClusters(&n, sampler_kernel<false>, &cfg);

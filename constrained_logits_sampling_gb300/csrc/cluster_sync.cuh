@@ -1,6 +1,6 @@
-// Inline-PTX wrappers for the asynchronous copies and barriers the sampler uses on
-// sm_103a: mbarriers (local and remote arrive), the 1-D TMA bulk copy global -> shared,
-// and DSMEM address mapping.  Every wait is bounded.
+// Inline-PTX wrappers for the barriers and bulk memory operations the sampler uses on
+// sm_103a: mbarriers (local and remote arrive, cluster-scope acquire), the 1-D TMA bulk
+// copy global -> shared and the TMA bulk prefetch into L2.  Every wait is bounded.
 #pragma once
 
 #include <cstdint>
@@ -68,10 +68,32 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(unsigned long long* bar, u
   return ok != 0;
 }
 
+// One poll that may suspend the thread for up to kSuspendNs before it reports the
+// phase as incomplete, so a waiting warp does not take issue slots from the others.
+constexpr uint32_t kSuspendNs = 20000;
+constexpr uint32_t kSleepLimit = 1u << 16;  // suspending polls before a wait gives up
+__device__ __forceinline__ bool mbar_try_wait_sleep(unsigned long long* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendNs)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded waits: false when the phase did not complete within kSpinLimit polls.
 __device__ __forceinline__ bool mbar_wait(unsigned long long* bar, uint32_t parity) {
   for (uint32_t i = 0; i < kSpinLimit; ++i)
     if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+// Bounded wait by suspending polls (at most kSleepLimit of them, about a second).
+__device__ __forceinline__ bool mbar_wait_sleep(unsigned long long* bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kSleepLimit; ++i)
+    if (mbar_try_wait_sleep(bar, parity)) return true;
   return false;
 }
 __device__ __forceinline__ bool mbar_wait_cluster(unsigned long long* bar, uint32_t parity) {
@@ -80,8 +102,9 @@ __device__ __forceinline__ bool mbar_wait_cluster(unsigned long long* bar, uint3
   return false;
 }
 
-// 1-D bulk copy (TMA) of `bytes` from global to this CTA's shared memory, completing
-// on `bar`.  Both addresses 16-byte aligned, bytes a multiple of 16.
+// 1-D bulk copy (TMA) of `bytes` from global memory into this CTA's shared memory,
+// completing on `bar` (complete_tx).  Both addresses 16-byte aligned, bytes a multiple
+// of 16.
 __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
                                               unsigned long long* bar) {
   asm volatile(
@@ -89,6 +112,13 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
           smem_addr(dst)),
       "l"(src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
+}
+
+// Asks the TMA unit to bring `bytes` of global memory into L2 (no completion signal;
+// later loads of those lines hit L2 or join the fetch in flight).  The address must be
+// 16-byte aligned and bytes a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 }  // namespace clsample

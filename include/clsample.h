@@ -66,7 +66,7 @@ enum {
   CLSAMPLE_SUCCESS = 0,
   CLSAMPLE_ERR_NULL = -1,       /* a required pointer is NULL */
   CLSAMPLE_ERR_BATCH = -2,      /* B < 0 or B > max_batch */
-  CLSAMPLE_ERR_VOCAB = -3,      /* V <= 0, V != the handle's vocab, or vocab too large */
+  CLSAMPLE_ERR_VOCAB = -3,      /* V <= 0, V != the handle's vocab, or V > 262144 */
   CLSAMPLE_ERR_STRIDE = -4,     /* logits_row_stride < V or bitmask_row_stride < ceil(V/32) */
   CLSAMPLE_ERR_DTYPE = -5,      /* logits_dtype is not a CLSAMPLE_LOGITS_* value */
   CLSAMPLE_ERR_CUDA = -6,       /* a CUDA runtime call failed (launch, attribute, device) */
@@ -104,9 +104,10 @@ enum {
  * dbg_kept_count    i32[B] output or NULL: size of the kept set K (1 for greedy rows).
  * dbg_cut           f32[B] output or NULL: min over K of y = (z' - max z') * (1/T).
  *
- * Limits: per row, at most 1024 distinct penalised or biased ids may fall inside one
- * vocabulary slice of ceil(V / cluster) tokens (cluster = 8 for V > 14336); a row that
- * exceeds it gets status OVERFLOW.  Histories of up to 4096 ids never exceed it.
+ * Limits: V <= 262144 (8 slices of at most 32768 tokens).  Per row, at most 1024
+ * distinct penalised or biased ids may fall inside one vocabulary slice of
+ * ceil(V / cluster) tokens (cluster = 8 for V > 14336); a row that exceeds it gets
+ * status OVERFLOW.  Histories of up to 4096 ids never exceed it.
  */
 typedef struct {
   int32_t B, V;

@@ -50,7 +50,10 @@ def test_strerror_and_geometry(lib):
         assert lib.clsample_strerror(code) != b"unknown error"
     g = sampler.geometry(151936)
     assert g == {"cluster": 8, "chunk": 19008, "smem_bytes": g["smem_bytes"]}
-    assert g["smem_bytes"] <= 112 * 1024  # two CTAs per SM
+    assert g["smem_bytes"] <= 54 * 1024  # four CTAs per SM
+    assert sampler.geometry(262144)["cluster"] == 8
+    with pytest.raises(sampler.ClsampleError):
+        sampler.geometry(262145)
     assert sampler.geometry(8)["cluster"] == 1
     assert sampler.geometry(32000)["chunk"] * sampler.geometry(32000)["cluster"] >= 32000
     with pytest.raises(sampler.ClsampleError):

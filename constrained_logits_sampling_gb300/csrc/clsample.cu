@@ -49,15 +49,21 @@ using namespace clsample;
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMinBlocks = 4;      // CTAs per SM the register budget is sized for
-constexpr int kHashCap = 1024;     // distinct penalised / biased ids per slice
-constexpr int kCandCap = 512;      // compacted candidates per slice
+constexpr int kHashCap = 1024;     // hash slots of the penalty kernel
+constexpr int kPenCap = 512;       // distinct penalised / biased ids per slice
+constexpr int kCandCap = 4096;     // compacted candidates per slice (global scratch)
+constexpr int kWhistBytes = 4096;  // top-p warp histograms (kWarps x 64 split counters)
 constexpr int kMaxCluster = 8;     // portable cluster size
-constexpr int kGatherCap = kCandCap * kMaxCluster;
+constexpr int kGatherCap = 4096;   // candidates the leader keeps in shared memory
 constexpr int kMaxChunk = 32 * 1024;  // longest slice
-constexpr int kStageBytes = 4096;     // one ring stage: one 16-byte vector per thread
+constexpr int kStageBytes = 8192;     // one ring stage: two 16-byte vectors per thread
 constexpr int kStages = 4;            // ring depth
 constexpr uint32_t kEmpty = 0xFFFFFFFFu;
-constexpr uint32_t kAllowedBit = 0x80000000u;  // in hcnt: the bitmask allows the token
+// penalised-token table: count | kBiasBit (a logit_bias entry applies) | kAllowedBit
+constexpr uint32_t kAllowedBit = 0x80000000u;
+constexpr uint32_t kBiasBit = 0x40000000u;
+constexpr uint32_t kCountMask = 0x3FFFFFFFu;
+constexpr uint32_t kPenBias = 0x80000000u;  // in PenEntry::id
 
 enum : int { kRowOk = 0, kRowOverflow = 1, kRowInvalid = 2 };
 enum : int { kFlagInvalid = 1, kFlagOverflow = 2, kFlagRing = 4 };  // kFlagRing: a ring stage never landed
@@ -70,27 +76,48 @@ struct Geometry {
   int cap;    // compacted candidates per CTA the leader can gather
 };
 
-struct LaunchParams {
-  clsample_args_t a;
-  int C;
-  int chunk;
-  int cap;
-  int vec_ok;  // every row start is 16-byte aligned: slices stream through the TMA ring
-};
-
 struct Cand {
   float y;
   int id;
 };
 
+// One penalised / biased token of a slice, as the penalty kernel lists it.
+struct __align__(16) PenEntry {
+  uint32_t id;     // local id | kPenBias when a logit_bias entry applies
+  uint32_t count;  // occurrences in the row's history (saturates at kCountMask)
+  float bias;      // the last bias entry's value
+  uint32_t pad;
+};
+
+struct LaunchParams {
+  clsample_args_t a;
+  int C;
+  int chunk;
+  int cap;
+  int vec_ok;         // every row start is 16-byte aligned: slices stream through the TMA ring
+  PenEntry* pen;      // [B * C][kPenCap] penalised-token lists (scratch)
+  int2* pen_n;        // [B * C] list length, flags
+  Cand* cand;         // [B * C][kCandCap] compacted candidates (scratch)
+};
+
 // Slice statistics pushed to every CTA after pass A.
+// Lower bounds of the k-th largest z' come from maxima of disjoint token groups: each
+// thread keeps one maximum per stage slot (kGroups groups), and the 32 maxima of one slot
+// across a warp form a "group set".  A set whose j-th largest maximum is L guarantees j
+// tokens at or above L.  For j = 2^i (i < kNJ) every CTA reports the minimum of L over
+// its sets that reach j maxima above -inf, and how many sets do; n such sets guarantee
+// n*j tokens.
+constexpr int kNJ = 6;  // j = 1, 2, 4, ..., 32
+
 struct X1 {
-  float m;      // slice max of z' (-inf if no candidate)
-  int arg;      // lowest id reaching m (INT_MAX if none)
-  float s;      // sum over the slice's candidates of 2^((z' - m) * log2(e) / T)
-  int flags;    // kFlag*
-  float lk;     // max over warps of the warp's k-th largest thread max of z' (-inf: unknown)
-  float lkc;    // min over warps of the ceil(k / (kWarps C))-th largest thread max
+  float m;         // slice max of z' (-inf if no candidate)
+  int arg;         // lowest id reaching m (INT_MAX if none)
+  float s;         // sum over the slice's candidates of 2^((z' - m) * log2(e) / T)
+  int flags;       // kFlag*
+  float lk;        // max over warps of the warp's k-th largest thread max (k <= 32; else -inf)
+  float lj[kNJ];   // min over the CTA's groups reaching 2^i maxima of the 2^i-th largest
+  unsigned char nj[8];  // how many groups reach 2^i (i < kNJ)
+  int nallowed;    // allowed tokens of the slice (at least its candidates)
 };
 
 // Slice results pushed to every CTA after pass B (and by the slow path).
@@ -120,74 +147,77 @@ struct RowState {
   float S;      // sum of 2^((z' - m) cS)
   int flags;
   float bound;  // lower bound of the k-th largest z' (-inf if none)
+  int nallowed_max;  // the largest per-slice allowed-token count
   float lnS;
   float invT;
   float L;      // min-p cut in y: ln(min_p), or -inf
   float theta;  // lower bound of the kept set in y (kPlanFast)
   int plan;
   int needW;    // kPlanFast: the top-p mass is taken over the whole row
+  int all;      // kPlanFast: every candidate of the row is compacted (theta = -inf)
+  float s0;     // race score of the argmax token, which every kept set contains: a lower
+                // bound of the winning score that seeds every race
 };
 
 // ---------------------------------------------------------------- shared memory
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+constexpr size_t kOffHistC = kWhistBytes;                                   // 4 KB
+constexpr size_t kOffHistW = kOffHistC + sizeof(uint32_t) * 256;            // 5 KB
+constexpr size_t kOffMrgC = kOffHistW + sizeof(unsigned long long) * 256;  // 7 KB
+constexpr size_t kR2Bytes = 9 * 1024;
+
 // Dynamic shared memory of one CTA (byte offsets):
-//   ring      kStages x kStageBytes   the slice's stream (TMA destination)
+//   ring      kStages x kStageBytes   the slice's stream (TMA destination); in the
+//                                     leader, once every CTA has finished reading its
+//                                     slice: the cluster's gathered candidates
 //   live      u32[chunk/32]           allowed by the bitmask, inside the row, not penalised
-//   mod       u32[chunk/32]           penalised / biased tokens (their value is in the hash)
-//   hkey/hcnt/hbias/hval              hash of those tokens: local id; history count with
-//                                     kAllowedBit; last bias entry; its value, then z'
-//   mrg_c     u32[2][256]             cluster-merged histograms (DSMEM atomics from every
-//   mrg_w     u64[2][256]             CTA), double-buffered across passes
-//   gather    Cand[C * cap]           in the leader, once every CTA has finished reading
-//                                     its slice: the cluster's candidates (overlays the
-//                                     regions above)
-//   r2 (8 KB) cand Cand[kCandCap] | hist_c u32[256] | hist_w u64[256]; the top-p warp
-//             histograms (kWarps x 64 u64) overlay cand; the leader's bucket select
-//             overlays all of it (u64[1024] buckets, then Cand[1024])
+//   mod       u32[chunk/32]           penalised / biased tokens
+//   prank     u16[chunk/32]           rank of each mod word's first penalised token
+//   pid/pcnt/pbias/pz [kPenCap]       the penalised tokens in token order: local id;
+//                                     count | kBiasBit | kAllowedBit; bias; raw logit in
+//                                     pass A, then the final z'
+//   r2 (9 KB) cand Cand[512] | hist_c u32[256] | hist_w u64[256] | mrg_c u32[2][256];
+//             mrg_w u64[2][256] overlays cand (slow path); the top-p warp histograms
+//             (kWarps x 64 u64) overlay cand and their merged copy is the start of
+//             mrg_c; the leader's bucket select overlays [0, 8 KB)
 struct Layout {
-  uint32_t live, mod, hkey, hcnt, hbias, hval, mrg_c, mrg_w, r2, total;
+  uint32_t live, mod, prank, pid, pcnt, pbias, pz, r2, total;
 };
 
 __host__ __device__ inline Layout layout_for(int chunk) {
   Layout L;
-  const size_t words = align_up(sizeof(uint32_t) * (size_t)(chunk / 32), 16);
+  const size_t words = (size_t)(chunk / 32);
   size_t off = (size_t)kStages * kStageBytes;
   L.live = (uint32_t)off;
-  off += words;
+  off = align_up(off + sizeof(uint32_t) * words, 16);
   L.mod = (uint32_t)off;
-  off += words;
-  L.hkey = (uint32_t)off;
-  off += sizeof(uint32_t) * kHashCap;
-  L.hcnt = (uint32_t)off;
-  off += sizeof(uint32_t) * kHashCap;
-  L.hbias = (uint32_t)off;
-  off += sizeof(int32_t) * kHashCap;
-  L.hval = (uint32_t)off;
-  off += sizeof(float) * kHashCap;
-  L.mrg_c = (uint32_t)off;
-  off += sizeof(uint32_t) * 2 * 256;
-  L.mrg_w = (uint32_t)off;
-  off += sizeof(unsigned long long) * 2 * 256;
-  if (off < sizeof(Cand) * kGatherCap) off = sizeof(Cand) * kGatherCap;
-  off = align_up(off, 128);
-  L.r2 = (uint32_t)off;
-  off += 8 * 1024;
-  L.total = (uint32_t)off;
+  off = align_up(off + sizeof(uint32_t) * words, 16);
+  L.prank = (uint32_t)off;
+  off = align_up(off + sizeof(uint16_t) * words, 16);
+  L.pid = (uint32_t)off;
+  off = align_up(off + sizeof(uint16_t) * kPenCap, 16);
+  L.pcnt = (uint32_t)off;
+  off += sizeof(uint32_t) * kPenCap;
+  L.pbias = (uint32_t)off;
+  off += sizeof(float) * kPenCap;
+  L.pz = (uint32_t)off;
+  off += sizeof(float) * kPenCap;
+  L.r2 = (uint32_t)align_up(off, 128);
+  L.total = L.r2 + kR2Bytes;
   return L;
 }
-static_assert(sizeof(unsigned long long) * 1024 <= 8 * 1024 && sizeof(Cand) * 1024 <= 8 * 1024,
-              "bucket select does not fit r2");
-static_assert(sizeof(Cand) * kCandCap + sizeof(uint32_t) * 256 + sizeof(unsigned long long) * 256 <= 8 * 1024,
-              "r2 tables overflow");
-static_assert(sizeof(unsigned long long) * kWarps * 64 <= sizeof(Cand) * kCandCap,
-              "top-p histogram does not fit the candidate area");
+static_assert(sizeof(Cand) * kGatherCap <= (size_t)kStages * kStageBytes, "gather area overflows the ring");
+static_assert(kR2Bytes >= kOffMrgC + sizeof(uint32_t) * 2 * 256, "r2 tables overflow");
+static_assert(sizeof(unsigned long long) * 2 * 256 <= kOffHistC, "mrg_w overlaps the histograms");
+static_assert(sizeof(unsigned long long) * 1024 <= kR2Bytes && sizeof(Cand) * 1024 <= kR2Bytes,
+              "bucket select does not fit r2");  // in the leader every r2 table is dead
+static_assert(2 * sizeof(uint32_t) * kWarps * 64 <= kWhistBytes, "top-p histogram does not fit r2");
+static_assert(sizeof(float) * kWarps * 4 * kNJ <= kOffMrgC, "pass A group-set bounds overlap the merged bins");
 static_assert(1024 % kThreads == 0, "bucket scan assumes whole buckets per thread");
-static_assert(2 * sizeof(uint16_t) * (kMaxChunk / 32) + sizeof(float) * kHashCap <= 8 * 1024,
-              "penalised-token arrays do not fit r2");
-static_assert(kHashCap <= 65536, "ranks and slots are 16-bit");
 static_assert(kStageBytes % (16 * kThreads) == 0, "a stage holds whole vectors per thread");
+static_assert(kPenCap % kThreads == 0 && kPenCap <= 65536 && kMaxChunk <= 65536, "16-bit ids and ranks");
 
 extern __shared__ __align__(128) unsigned char smem_dyn[];
 
@@ -195,22 +225,17 @@ struct Smem {
   unsigned char* ring;
   uint32_t* live;
   uint32_t* mod;
-  uint32_t* hkey;
-  uint32_t* hcnt;
-  int32_t* hbias;
-  float* hval;
+  uint16_t* prank;
+  uint16_t* pid;
+  uint32_t* pcnt;
+  float* pbias;
+  float* pz;
   uint32_t* mrg_c;
   unsigned long long* mrg_w;
   Cand* gather;
-  Cand* cand;
   uint32_t* hist_c;
   unsigned long long* hist_w;
   unsigned char* r2;
-  // until exchange 1, r2 holds the penalised tokens in token order: the rank of each
-  // mod word's first token, rank -> hash slot, and rank -> raw logit (filled by pass A)
-  uint16_t* prank;
-  uint16_t* pslot;
-  float* praw;
 };
 
 __device__ __forceinline__ Smem carve(int chunk) {
@@ -220,20 +245,17 @@ __device__ __forceinline__ Smem carve(int chunk) {
   s.ring = b;
   s.live = reinterpret_cast<uint32_t*>(b + L.live);
   s.mod = reinterpret_cast<uint32_t*>(b + L.mod);
-  s.hkey = reinterpret_cast<uint32_t*>(b + L.hkey);
-  s.hcnt = reinterpret_cast<uint32_t*>(b + L.hcnt);
-  s.hbias = reinterpret_cast<int32_t*>(b + L.hbias);
-  s.hval = reinterpret_cast<float*>(b + L.hval);
-  s.mrg_c = reinterpret_cast<uint32_t*>(b + L.mrg_c);
-  s.mrg_w = reinterpret_cast<unsigned long long*>(b + L.mrg_w);
-  s.gather = reinterpret_cast<Cand*>(b);
-  s.cand = reinterpret_cast<Cand*>(b + L.r2);
-  s.hist_c = reinterpret_cast<uint32_t*>(b + L.r2 + sizeof(Cand) * kCandCap);
-  s.hist_w = reinterpret_cast<unsigned long long*>(b + L.r2 + sizeof(Cand) * kCandCap + sizeof(uint32_t) * 256);
+  s.prank = reinterpret_cast<uint16_t*>(b + L.prank);
+  s.pid = reinterpret_cast<uint16_t*>(b + L.pid);
+  s.pcnt = reinterpret_cast<uint32_t*>(b + L.pcnt);
+  s.pbias = reinterpret_cast<float*>(b + L.pbias);
+  s.pz = reinterpret_cast<float*>(b + L.pz);
   s.r2 = b + L.r2;
-  s.prank = reinterpret_cast<uint16_t*>(b + L.r2);
-  s.pslot = reinterpret_cast<uint16_t*>(b + L.r2 + sizeof(uint16_t) * (kMaxChunk / 32));
-  s.praw = reinterpret_cast<float*>(b + L.r2 + 2 * sizeof(uint16_t) * (kMaxChunk / 32));
+  s.hist_c = reinterpret_cast<uint32_t*>(s.r2 + kOffHistC);
+  s.hist_w = reinterpret_cast<unsigned long long*>(s.r2 + kOffHistW);
+  s.mrg_c = reinterpret_cast<uint32_t*>(s.r2 + kOffMrgC);
+  s.mrg_w = reinterpret_cast<unsigned long long*>(s.r2);
+  s.gather = reinterpret_cast<Cand*>(b);
   return s;
 }
 
@@ -244,7 +266,6 @@ struct Shared {
   X1 x1_mine;
   X2 x2_mine;
   unsigned long long full[kStages];  // ring stage barriers (one arrival + the copy's bytes)
-  unsigned long long gather_bar;     // the leader's gather barrier (one arrival per CTA)
   RowParams rp;
   RowState rs;
   float red_f[kWarps * 2];
@@ -255,6 +276,8 @@ struct Shared {
   int csr[4];
   float zth, res;
   int bstar, nl, flags, count, digit, none, npen;
+  int pre;  // the pass whose first ring stages were issued ahead of time (-1: none)
+  int nallowed;
   unsigned long long above;
 };
 __shared__ Shared sh;
@@ -340,8 +363,9 @@ __device__ __forceinline__ int hash_insert(uint32_t* hkey, uint32_t l) {
 
 // ---------------------------------------------------------------- out-of-line math
 
-// The race score and the Philox words are long instruction sequences used at several
-// places; one out-of-line copy of each keeps the kernel's code small.
+// The exact race score and the Philox words are long instruction sequences; the cold
+// call sites share one out-of-line copy of each (the per-vector race loops inline Philox,
+// and the exact score is rare behind the fast screen in Race::add).
 __device__ __noinline__ float race_score_call(float y, uint32_t word) { return race_score(y, word); }
 __device__ __noinline__ uint4 race_words_call(uint32_t q, unsigned long long seed, unsigned long long pos) {
   return race_words(q, seed, pos);
@@ -379,14 +403,16 @@ __device__ unsigned long long block_sum_u64(unsigned long long v, unsigned long 
 }
 
 // Race partials of one thread, reduced over the block into `out` (thread 0 writes).
+constexpr float kScoreMargin = 1e-3f;
+
 struct Race {
   float s;      // best score
   int tok;      // its id
   float ybest;  // its y
   int kept;
   float ymin;
-  __device__ void init() {
-    s = -INFINITY;
+  __device__ void init(float s0 = -INFINITY) {
+    s = s0;
     tok = INT_MAX;
     ybest = -INFINITY;
     kept = 0;
@@ -395,6 +421,14 @@ struct Race {
   __device__ __forceinline__ void add(float y, int id, uint32_t word) {
     ++kept;
     ymin = fminf(ymin, y);
+    // screen with a fast score (within 1e-4 of the exact one): a token whose fast score
+    // stays kScoreMargin below the best cannot win, so only near-winners pay for the
+    // exact score.  E = -ln U: the fast logarithm for U <= 7/8; above, with t = 1 - U
+    // (exact), the series t (1 + t/2 + t^2/3 + t^3/4), relative error below 1e-4.
+    const float u = word_to_uniform(word);
+    const float t = 1.0f - u;
+    const float e = u <= 0.875f ? -__logf(u) : t * (1.0f + t * (0.5f + t * (0.33333334f + t * 0.25f)));
+    if (y - __logf(e) + kScoreMargin < s) return;
     const float sc = race_score_call(y, word);
     if (better(sc, id, s, tok)) {
       s = sc;
@@ -467,6 +501,18 @@ template <typename T>
 __device__ __forceinline__ void push_all(const cg::cluster_group& cluster, T* dst, const T* mine, int rank,
                                          int C) {
   if ((int)threadIdx.x < C) *cluster.map_shared_rank(dst + rank, (unsigned)threadIdx.x) = *mine;
+}
+
+// Adds a weight (<= 2^40) to a split 64-bit shared counter {c[0]: units of 1, c[1]: units
+// of 2^21} with native 32-bit atomics; a wrap of c[0] (the adder sees it) carries 2^11
+// into c[1].  Exact for up to 8191 additions; read it back with split_get.
+__device__ __forceinline__ void split_add(uint32_t* c, unsigned long long w) {
+  const uint32_t lo = (uint32_t)(w & 0x1FFFFFu);
+  const uint32_t old = atomicAdd(c, lo);
+  atomicAdd(c + 1, (uint32_t)(w >> 21) + (old + lo < old ? (1u << 11) : 0u));
+}
+__device__ __forceinline__ unsigned long long split_get(const uint32_t* c) {
+  return ((unsigned long long)c[1] << 21) + c[0];
 }
 
 // ---------------------------------------------------------------- radix digit choice
@@ -626,7 +672,7 @@ __device__ __forceinline__ void ring_wait(uint32_t s) {
 // thread calls it; every lane of a warp makes the same number of body calls (wd = 0 where
 // it has no vector), so bodies may use warp collectives.  `started`: thread 0 already
 // issued the pass's first stages.
-template <bool kBF16, class Body>
+template <bool kBF16, bool kSlot = false, class Body>
 __device__ __forceinline__ void stream(const Geo& g, const Smem& S, int& pass, bool started, Body&& body) {
   constexpr int kEsize = kBF16 ? 2 : 4;
   constexpr int kVecPerStage = kStageBytes / (4 * kEsize);
@@ -634,7 +680,7 @@ __device__ __forceinline__ void stream(const Geo& g, const Smem& S, int& pass, b
   const int tid = threadIdx.x;
   if (g.nst > 0) {
     const uint32_t seq0 = (uint32_t)pass * (uint32_t)g.nst;
-    if (tid == 0 && !started) ring_start<kBF16>(g, S, pass);
+    if (tid == 0 && !started && sh.pre != pass) ring_start<kBF16>(g, S, pass);
 #pragma unroll 1
     for (int k = 0; k < g.nst; ++k) {
       const uint32_t s = seq0 + (uint32_t)k;
@@ -653,7 +699,10 @@ __device__ __forceinline__ void stream(const Geo& g, const Smem& S, int& pass, b
         const bool in = 4 * f < g.bulk_tokens;
         const uint32_t wd = in ? live4(S.live, f) : 0u;
         const float4 v = in ? sload4<kBF16>(buf, fl) : make_float4(0.f, 0.f, 0.f, 0.f);
-        body(in ? f : g.nvec, wd, v);  // vectors past the ring part: f = nvec (past the row)
+        // vectors past the ring part: f = nvec (past the row).  With kSlot the body also
+        // gets the vector's slot t in the stage (a compile-time constant after unrolling)
+        if constexpr (kSlot) body(in ? f : g.nvec, wd, v, t);
+        else body(in ? f : g.nvec, wd, v);
       }
     }
   }
@@ -665,13 +714,34 @@ __device__ __forceinline__ void stream(const Geo& g, const Smem& S, int& pass, b
     const bool in = f < f_end;
     const uint32_t wd = in ? live4(S.live, f) : 0u;
     const float4 v = in ? gload4<kBF16>(g, f) : make_float4(0.f, 0.f, 0.f, 0.f);
-    body(in ? f : g.nvec, wd, v);
+    if constexpr (kSlot) body(in ? f : g.nvec, wd, v, 0);
+    else body(in ? f : g.nvec, wd, v);
   }
   __syncthreads();  // the ring is free for the next pass; the bodies' shared writes are visible
   ++pass;
 }
 
-// ---------------------------------------------------------------- prologue
+// Sampling rows always stream their slice once more after exchange 1: the first stages
+// of that pass are issued now, so they load during the exchange.  Thread 0 only.
+template <bool kBF16>
+__device__ __noinline__ void ring_prefetch_pass(const LaunchParams& P, int pass) {
+  if (threadIdx.x != 0) return;
+  const RowParams q = sh.rp;
+  const bool greedy = (q.T < kGreedyEps) || q.k == 0 || q.k == 1;
+  const Geo g = geo<kBF16>(P);
+  if (greedy || q.invalid || g.nst == 0) return;
+  ring_start<kBF16>(g, carve(g.chunk), pass);
+  sh.pre = pass;
+}
+
+// A row that ends without using the stages issued ahead of time waits for them, so no
+// copy into this CTA's shared memory is in flight when it exits.  Thread 0 only.
+template <bool kBF16>
+__device__ __noinline__ void ring_drain(const LaunchParams& P) {
+  if (threadIdx.x != 0 || sh.pre < 0) return;
+  const Geo g = geo<kBF16>(P);
+  for (int k = 0; k < min(kStages, g.nst); ++k) ring_wait((uint32_t)sh.pre * (uint32_t)g.nst + (uint32_t)k);
+}
 
 // Adds n occurrences of local id l to the history counts; kFlagOverflow if the hash is
 // full.
@@ -682,29 +752,189 @@ __device__ __noinline__ int count_id(uint32_t* hkey, uint32_t* hcnt, uint32_t l,
   return 0;
 }
 
-// Row parameters, the slice's live bits (bitmask words clipped to the row) and the hash
-// of its penalised / biased tokens (SGLang page, "Order semantics of the penalties" and
-// "Why logit_bias is built from triples": the last duplicate wins).  The first ring
-// stages of pass A are issued before anything else, so the slice is on its way while the
-// small inputs arrive.
+// ---------------------------------------------------------------- penalty / bias scatter
+
+// One CTA per (row, slice), ahead of the sampler: the slice's distinct penalised or
+// biased token ids with their history count and the last bias entry (SGLang page, "Order
+// semantics of the penalties" and "Why logit_bias is built from triples": the last
+// duplicate wins), sorted by id, into the scratch list of the slice.  Duplicate history
+// ids are counted once per warp (Zipf-like histories repeat their frequent ids many
+// times).  A slice with more than kPenCap distinct ids is flagged OVERFLOW.
+__global__ void __launch_bounds__(kThreads) penalty_kernel(const __grid_constant__ LaunchParams P) {
+  __shared__ uint32_t hkey[kHashCap];
+  __shared__ uint32_t hcnt[kHashCap];
+  __shared__ int32_t hbias[kHashCap];
+  __shared__ float hval[kHashCap];
+  __shared__ uint32_t mod[kMaxChunk / 32];
+  __shared__ int red[kWarps];
+  __shared__ int csr[4];
+  __shared__ int flags_sh;
+  const clsample_args_t& a = P.a;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int rc = (int)blockIdx.x;  // row * C + slice
+  const int row = rc / P.C, c0 = (rc % P.C) * P.chunk;
+  const int len = max(0, min(a.V, c0 + P.chunk) - c0);
+  const int c1 = c0 + len;
+  const bool has_hist = a.hist_offs != nullptr;
+  const bool has_bias = a.bias_offs != nullptr;
+  if (tid == 0) {
+    csr[0] = has_hist ? a.hist_offs[row] : 0;
+    csr[1] = has_hist ? a.hist_offs[row + 1] : 0;
+    csr[2] = has_bias ? a.bias_offs[row] : 0;
+    csr[3] = has_bias ? a.bias_offs[row + 1] : 0;
+    flags_sh = 0;
+  }
+  for (int i = tid; i < kHashCap; i += kThreads) {
+    hkey[i] = kEmpty;
+    hcnt[i] = 0u;
+    hbias[i] = -1;
+  }
+  for (int w = tid; w < P.chunk / 32; w += kThreads) mod[w] = 0u;
+  __syncthreads();
+
+  int flags = 0;
+  const int hlo = csr[0], hhi = csr[1], blo = csr[2], bhi = csr[3];
+  if (hlo < 0 || hhi < hlo || blo < 0 || bhi < blo) flags |= kFlagInvalid;
+  const bool hok = has_hist && hlo >= 0 && hhi >= hlo;
+  const bool bok = has_bias && blo >= 0 && bhi >= blo;
+  // this thread's first bias entry is fetched together with the history ids
+  const int bj0 = blo + tid;
+  int bid0 = INT_MIN;
+  float bval0 = 0.0f;
+  if (bok && bj0 < bhi) {
+    bid0 = __ldg(a.bias_ids + bj0);
+    bval0 = __ldg(a.bias_vals + bj0);
+  }
+  if (hok) {
+    for (int base = hlo; base < hhi; base += 16 * kThreads) {
+      int ids[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int j = base + u * kThreads + tid;
+        ids[u] = j < hhi ? __ldg(a.hist_ids + j) : INT_MIN;
+      }
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int id = ids[u];
+        if (id != INT_MIN && (id < 0 || id >= a.V)) flags |= kFlagInvalid;
+        const bool mine = id >= c0 && id < c1;
+        const uint32_t peers = __match_any_sync(0xffffffffu, mine ? id : -1);
+        if (mine && lane == __ffs(peers) - 1) flags |= count_id(hkey, hcnt, (uint32_t)(id - c0), (uint32_t)__popc(peers));
+      }
+    }
+  }
+  // bias: the largest entry index per id wins; its owner then stores the value
+  int myslot = -1;
+  if (bok) {
+    for (int j = bj0; j < bhi; j += kThreads) {
+      const int id = j == bj0 ? bid0 : __ldg(a.bias_ids + j);
+      const float b = j == bj0 ? bval0 : __ldg(a.bias_vals + j);
+      if (id < 0 || id >= a.V || b != b) {
+        flags |= kFlagInvalid;
+      } else if (id >= c0 && id < c1) {
+        const int slot = hash_insert(hkey, (uint32_t)(id - c0));
+        if (slot < 0) flags |= kFlagOverflow;
+        else atomicMax(&hbias[slot], j);
+        if (j == bj0) myslot = slot;
+      }
+    }
+  }
+  if (flags) atomicOr(&flags_sh, flags);
+  __syncthreads();
+  if (bok) {
+    for (int j = bj0; j < bhi; j += kThreads) {
+      if (j == bj0) {
+        if (myslot >= 0 && hbias[myslot] == j) hval[myslot] = bval0;
+      } else {
+        const int id = __ldg(a.bias_ids + j);
+        if (id >= c0 && id < c1) {
+          for (int i = 0; i < kHashCap; ++i)
+            if (hkey[i] == (uint32_t)(id - c0) && hbias[i] == j) hval[i] = __ldg(a.bias_vals + j);
+        }
+      }
+    }
+  }
+  for (int i = tid; i < kHashCap; i += kThreads) {
+    const uint32_t l = hkey[i];
+    if (l != kEmpty) atomicOr(&mod[l >> 5], 1u << (l & 31));
+  }
+  __syncthreads();
+  // rank of every id = ids below it: an exclusive scan of the words' popcounts
+  constexpr int kPer = (kMaxChunk / 32) / kThreads;
+  const int nw = P.chunk / 32;
+  int cnt[kPer], loc = 0;
+#pragma unroll
+  for (int t = 0; t < kPer; ++t) {
+    const int w = tid * kPer + t;
+    cnt[t] = w < nw ? __popc(mod[w]) : 0;
+    loc += cnt[t];
+  }
+  int x = loc;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, x, d);
+    if (lane >= d) x += o;
+  }
+  if (lane == 31) red[warp] = x;
+  __syncthreads();
+  int total = 0;
+  for (int w = 0; w < kWarps; ++w) total += red[w];
+  int before = 0;
+  for (int w = 0; w < warp; ++w) before += red[w];
+  // prefix of each of this thread's words, kept in registers for the entries below
+  __shared__ int wbase[kMaxChunk / 32];
+  int e = before + x - loc;
+#pragma unroll
+  for (int t = 0; t < kPer; ++t) {
+    const int w = tid * kPer + t;
+    if (w < nw) wbase[w] = e;
+    e += cnt[t];
+  }
+  __syncthreads();
+  PenEntry* out = P.pen + (size_t)rc * kPenCap;
+  for (int i = tid; i < kHashCap; i += kThreads) {
+    const uint32_t l = hkey[i];
+    if (l == kEmpty) continue;
+    const int r = wbase[l >> 5] + __popc(mod[l >> 5] & ((1u << (l & 31)) - 1u));
+    if (r >= kPenCap) continue;
+    PenEntry en;
+    en.id = l | (hbias[i] >= 0 ? kPenBias : 0u);
+    en.count = min(hcnt[i], kCountMask);
+    en.bias = hbias[i] >= 0 ? hval[i] : 0.0f;
+    en.pad = 0u;
+    out[r] = en;
+  }
+  if (tid == 0) {
+    int f = flags_sh;
+    if (total > kPenCap) f |= kFlagOverflow;
+    P.pen_n[rc] = make_int2(min(total, kPenCap), f);
+  }
+}
+
+// ---------------------------------------------------------------- prologue
+
+// Row parameters, the slice's live bits (bitmask words clipped to the row) and its
+// penalised / biased tokens from the penalty kernel's list (sorted by id, so an entry's
+// index is the token's rank); the bitmask's verdict on each moves into its entry.  The
+// first ring stages of pass A are issued before anything else, so the slice is on its
+// way while the small inputs arrive.
 template <bool kBF16>
 __device__ __noinline__ void prologue(const LaunchParams& P) {
   const Geo g = geo<kBF16>(P);
   const Smem S = carve(g.chunk);
   const clsample_args_t& a = P.a;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int row = g.row, c0 = g.c0, len = g.len;
   const int32_t* bmrow = a.bitmask ? a.bitmask + (long long)row * a.bitmask_row_stride : nullptr;
-  const bool has_hist = a.hist_offs != nullptr;
-  const bool has_bias = a.bias_offs != nullptr;
-  const bool has_mod = has_hist || has_bias;
+  const bool has_mod = a.hist_offs != nullptr || a.bias_offs != nullptr;
+  const int rc = row * g.C + g.rank;
 
   if (tid == 0) {
     sh.flags = 0;
     sh.count = 0;
-    sh.npen = 0;
+    sh.pre = -1;
+    sh.nallowed = 0;
     for (int i = 0; i < kStages; ++i) mbar_init(&sh.full[i], 1);
-    mbar_init(&sh.gather_bar, (uint32_t)g.C);
     fence_mbar_init();
     ring_start<kBF16>(g, S, 0);
   } else if (tid == 32) {
@@ -727,10 +957,15 @@ __device__ __noinline__ void prologue(const LaunchParams& P) {
     q.invalid = bad;
     sh.rp = q;
   } else if (tid == 64) {
-    sh.csr[0] = has_hist ? a.hist_offs[row] : 0;
-    sh.csr[1] = has_hist ? a.hist_offs[row + 1] : 0;
-    sh.csr[2] = has_bias ? a.bias_offs[row] : 0;
-    sh.csr[3] = has_bias ? a.bias_offs[row + 1] : 0;
+    const int2 nf = has_mod ? P.pen_n[rc] : make_int2(0, 0);
+    sh.npen = nf.x;
+    sh.csr[0] = nf.y;  // the penalty kernel's flags
+  }
+  // the list is loaded whole (its length arrives with it): two entries per thread
+  PenEntry en[kPenCap / kThreads];
+  if (has_mod) {
+#pragma unroll
+    for (int t = 0; t < kPenCap / kThreads; ++t) en[t] = P.pen[(size_t)rc * kPenCap + t * kThreads + tid];
   }
   for (int w = tid; w < g.chunk / 32; w += kThreads) {
     const int e = 32 * w;
@@ -743,103 +978,39 @@ __device__ __noinline__ void prologue(const LaunchParams& P) {
     S.live[w] = word;
     S.mod[w] = 0u;
   }
-  if (has_mod) {
-    for (int i = tid; i < kHashCap; i += kThreads) {
-      S.hkey[i] = kEmpty;
-      S.hcnt[i] = 0u;
-      S.hbias[i] = -1;
-    }
-  }
-  for (int i = tid; i < 2 * 256; i += kThreads) {
-    S.mrg_c[i] = 0u;
-    S.mrg_w[i] = 0ull;
-  }
+  if (tid < 128) S.mrg_c[tid] = 0u;  // the top-p route's merged bins (peers add into them)
   __syncthreads();
-  if (!has_mod) return;
-
-  int flags = 0;
-  const int c1 = c0 + len;
-  const int hlo = sh.csr[0], hhi = sh.csr[1], blo = sh.csr[2], bhi = sh.csr[3];
-  if (hlo < 0 || hhi < hlo || blo < 0 || bhi < blo) flags |= kFlagInvalid;
-  const bool hok = has_hist && hlo >= 0 && hhi >= hlo;
-  const bool bok = has_bias && blo >= 0 && bhi >= blo;
-  // this thread's first bias entry is fetched together with the history ids
-  const int bj0 = blo + tid;
-  int bid0 = INT_MIN;
-  float bval0 = 0.0f;
-  if (bok && bj0 < bhi) {
-    bid0 = __ldg(a.bias_ids + bj0);
-    bval0 = __ldg(a.bias_vals + bj0);
+  if (!has_mod) {
+    int na = 0;
+    for (int w = tid; w < g.chunk / 32; w += kThreads) na += __popc(S.live[w]);
+    na = __reduce_add_sync(0xffffffffu, na);
+    if (lane == 0 && na) atomicAdd(&sh.nallowed, na);
+    return;
   }
-  if (hok) {
-    for (int base = hlo; base < hhi; base += 16 * kThreads) {
-      int ids[16];
+  const int npen = sh.npen;
+  if (tid == 0 && sh.csr[0]) sh.flags |= sh.csr[0];
+  // the bitmask's verdict on each penalised token moves into its entry; the token
+  // leaves the live set (pass A gives it its final value)
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int j = base + u * kThreads + tid;
-        ids[u] = j < hhi ? __ldg(a.hist_ids + j) : INT_MIN;
-      }
-      // duplicates within a warp are counted once per warp (Zipf-like histories repeat
-      // their frequent ids many times): one insert and one add per distinct id
-#pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int id = ids[u];
-        if (id != INT_MIN && (id < 0 || id >= a.V)) flags |= kFlagInvalid;
-        const bool mine = id >= c0 && id < c1;
-        const uint32_t peers = __match_any_sync(0xffffffffu, mine ? id : -1);
-        if (mine && (threadIdx.x & 31) == __ffs(peers) - 1)
-          flags |= count_id(S.hkey, S.hcnt, (uint32_t)(id - c0), (uint32_t)__popc(peers));
-      }
-    }
-  }
-  // bias: the largest entry index per id wins; its owner then stores the value
-  int myslot = -1;
-  if (bok) {
-    for (int j = bj0; j < bhi; j += kThreads) {
-      const int id = j == bj0 ? bid0 : __ldg(a.bias_ids + j);
-      const float b = j == bj0 ? bval0 : __ldg(a.bias_vals + j);
-      if (id < 0 || id >= a.V || b != b) {
-        flags |= kFlagInvalid;
-      } else if (id >= c0 && id < c1) {
-        const int slot = hash_insert(S.hkey, (uint32_t)(id - c0));
-        if (slot < 0) flags |= kFlagOverflow;
-        else atomicMax(&S.hbias[slot], j);
-        if (j == bj0) myslot = slot;
-      }
-    }
-  }
-  if (flags) atomicOr(&sh.flags, flags);
-  __syncthreads();
-  if (bok) {
-    for (int j = bj0; j < bhi; j += kThreads) {
-      if (j == bj0) {
-        if (myslot >= 0 && S.hbias[myslot] == j) S.hval[myslot] = bval0;
-      } else {
-        const int id = __ldg(a.bias_ids + j);
-        if (id >= c0 && id < c1) {
-          for (int i = 0; i < kHashCap; ++i)
-            if (S.hkey[i] == (uint32_t)(id - c0) && S.hbias[i] == j) S.hval[i] = __ldg(a.bias_vals + j);
-        }
-      }
-    }
-  }
-  // penalised / biased tokens leave the live set (pass A gives them their final value);
-  // the bitmask's verdict on each moves into its hash entry
-  for (int i = tid; i < kHashCap; i += kThreads) {
-    const uint32_t l = S.hkey[i];
-    if (l == kEmpty) continue;
+  for (int t = 0; t < kPenCap / kThreads; ++t) {
+    const int r = t * kThreads + tid;
+    if (r >= npen) continue;
+    const uint32_t l = en[t].id & ~kPenBias;
     const uint32_t bit = 1u << (l & 31);
-    if (S.live[l >> 5] & bit) S.hcnt[i] |= kAllowedBit;
+    uint32_t c = en[t].count & kCountMask;
+    if (en[t].id & kPenBias) c |= kBiasBit;
+    if (S.live[l >> 5] & bit) c |= kAllowedBit;
+    S.pid[r] = (uint16_t)l;
+    S.pcnt[r] = c;
+    S.pbias[r] = en[t].bias;
     atomicAnd(&S.live[l >> 5], ~bit);
     atomicOr(&S.mod[l >> 5], bit);
   }
   __syncthreads();
-  // token-order ranks of the penalised tokens: an exclusive scan of the mod words'
-  // popcounts (consecutive words per thread), then rank -> hash slot
+  // token-order rank of each mod word's first token: an exclusive scan of the popcounts
   {
     constexpr int kPer = (kMaxChunk / 32) / kThreads;
     const int nw = g.chunk / 32;
-    const int lane = tid & 31, warp = tid >> 5;
     int cnt[kPer], loc = 0;
 #pragma unroll
     for (int t = 0; t < kPer; ++t) {
@@ -863,14 +1034,14 @@ __device__ __noinline__ void prologue(const LaunchParams& P) {
       if (w < nw) S.prank[w] = (uint16_t)excl;
       excl += cnt[t];
     }
-    if (tid == kThreads - 1) sh.npen = excl;
   }
-  __syncthreads();
-  for (int i = tid; i < kHashCap; i += kThreads) {
-    const uint32_t l = S.hkey[i];
-    if (l == kEmpty) continue;
-    const int r = S.prank[l >> 5] + __popc(S.mod[l >> 5] & ((1u << (l & 31)) - 1u));
-    S.pslot[r] = (uint16_t)i;
+  // allowed tokens of the slice: plain live ones plus allowed penalised ones
+  {
+    int na = 0;
+    for (int w = tid; w < g.chunk / 32; w += kThreads) na += __popc(S.live[w]);
+    for (int r = tid; r < npen; r += kThreads) na += (S.pcnt[r] & kAllowedBit) ? 1 : 0;
+    na = __reduce_add_sync(0xffffffffu, na);
+    if (lane == 0 && na) atomicAdd(&sh.nallowed, na);
   }
   __syncthreads();
 }
@@ -892,13 +1063,20 @@ __device__ __noinline__ void pass_a(const LaunchParams& P) {
   const float Teff = (q.T >= kGreedyEps) ? q.T : 1.0f;
   const float cS = 1.4426950408889634f / Teff;
   const int c0 = g.c0;
+  constexpr int kGroups = kStageBytes / (4 * (kBF16 ? 2 : 4)) / kThreads;  // vectors per thread per stage
+  static_assert(kGroups <= 4, "red_j holds four group sets per warp");
 
   // the thread's online state; a thread visits its tokens in increasing order, so the
   // first token reaching the running max is the lowest
   float sm = -INFINITY, ss = 0.0f;
   int targ = INT_MAX;
+  // the maxima of the thread's vectors in each stage slot: kGroups disjoint token groups
+  // per thread for the top-k bounds
+  float gm[kGroups];
+#pragma unroll
+  for (int t = 0; t < kGroups; ++t) gm[t] = -INFINITY;
   int pass = 0;
-  stream<kBF16>(g, S, pass, true, [&](int f, uint32_t wd, const float4& v) {
+  stream<kBF16, true>(g, S, pass, true, [&](int f, uint32_t wd, const float4& v, int t) {
     if (has_mod && 4 * f < g.len) {
       // penalised / biased tokens: keep the raw logit (rank order) for the fold below
       const uint32_t mw = S.mod[f >> 3];
@@ -908,7 +1086,7 @@ __device__ __noinline__ void pass_a(const LaunchParams& P) {
         int r = S.prank[f >> 3] + __popc(mw & ((1u << sh4) - 1u));
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          if ((md >> j) & 1u) S.praw[r++] = comp(v, j);
+          if ((md >> j) & 1u) S.pz[r++] = comp(v, j);
       }
     }
     if (!wd) return;
@@ -918,6 +1096,7 @@ __device__ __noinline__ void pass_a(const LaunchParams& P) {
                       (wd & 4u) ? sanitize(v.z) : -INFINITY, (wd & 8u) ? sanitize(v.w) : -INFINITY);
     const float fm = fmaxf(fmaxf(z.x, z.y), fmaxf(z.z, z.w));
     if (!(fm > -INFINITY)) return;
+    gm[t] = fmaxf(gm[t], fm);
     if (fm > sm) {
       ss *= ex2_approx((sm - fm) * cS);
       sm = fm;
@@ -933,16 +1112,16 @@ __device__ __noinline__ void pass_a(const LaunchParams& P) {
   if (has_mod) {
     const int npen = sh.npen;
     for (int r = tid; r < npen; r += kThreads) {
-      const int slot = S.pslot[r];
-      const uint32_t c = S.hcnt[slot];
-      float zz = (c & kAllowedBit) ? sanitize(S.praw[r]) : -INFINITY;
-      const uint32_t cnt = c & ~kAllowedBit;
+      const uint32_t c = S.pcnt[r];
+      float zz = (c & kAllowedBit) ? sanitize(S.pz[r]) : -INFINITY;
+      const uint32_t cnt = c & kCountMask;
       if (cnt) zz = apply_penalties(zz, cnt, q.freq, q.pres, q.rep);
-      if (S.hbias[slot] >= 0) zz = __fadd_rn(zz, S.hval[slot]);
+      if (c & kBiasBit) zz = __fadd_rn(zz, S.pbias[r]);
       zz = guard(zz);
-      S.hval[slot] = zz;
+      S.pz[r] = zz;
       if (!(zz > -INFINITY)) continue;
-      const int id = c0 + (int)S.hkey[slot];
+      const int id = c0 + (int)S.pid[r];
+      gm[0] = fmaxf(gm[0], zz);  // a disjoint token set joins the thread's first group
       if (zz > sm) {
         ss = ss * ex2_approx((sm - zz) * cS) + 1.0f;
         sm = zz;
@@ -954,28 +1133,34 @@ __device__ __noinline__ void pass_a(const LaunchParams& P) {
     }
   }
 
-  // warp-level lower bounds of the top-k cut from the per-thread maxima (disjoint
-  // groups): a warp's j-th largest thread max guarantees j tokens at or above it
+  // group-set lower bounds of the top-k cut (see X1); lane i < kNJ of set t holds its
+  // 2^i-th largest maximum
   const bool topk_row = !greedy && !q.invalid && q.k >= 2;
-  float wlk = -INFINITY, wlkc = INFINITY;
+  float wlk = -INFINITY;
+  float wlj[kGroups];
+#pragma unroll
+  for (int t = 0; t < kGroups; ++t) wlj[t] = -INFINITY;
   if (topk_row) {
-    uint32_t key = fkey(sm);
 #pragma unroll
-    for (int kk = 2; kk <= 32; kk <<= 1) {
+    for (int t = 0; t < kGroups; ++t) {
+      uint32_t key = fkey(gm[t]);
 #pragma unroll
-      for (int j = kk >> 1; j > 0; j >>= 1) {
-        const uint32_t other = __shfl_xor_sync(0xffffffffu, key, j);
-        const bool up = (lane & kk) == 0;
-        const bool lower = (lane & j) == 0;
-        key = (lower == up) ? min(key, other) : max(key, other);
+      for (int kk = 2; kk <= 32; kk <<= 1) {
+#pragma unroll
+        for (int j = kk >> 1; j > 0; j >>= 1) {
+          const uint32_t other = __shfl_xor_sync(0xffffffffu, key, j);
+          const bool up = (lane & kk) == 0;
+          const bool lower = (lane & j) == 0;
+          key = (lower == up) ? min(key, other) : max(key, other);
+        }
       }
+      // ascending across lanes: the j-th largest sits in lane 32 - j
+      const int k1 = q.k;
+      const uint32_t v1 = __shfl_sync(0xffffffffu, key, k1 <= 32 ? 32 - k1 : 0);
+      if (k1 <= 32) wlk = fmaxf(wlk, key_to_float(v1));
+      const uint32_t vj = __shfl_sync(0xffffffffu, key, 32 - (1 << min(lane, kNJ - 1)));
+      wlj[t] = lane < kNJ ? key_to_float(vj) : -INFINITY;
     }
-    // ascending across lanes: the j-th largest sits in lane 32 - j
-    const int k1 = q.k, k2 = (q.k + kWarps * g.C - 1) / (kWarps * g.C);
-    const uint32_t v1 = __shfl_sync(0xffffffffu, key, k1 <= 32 ? 32 - k1 : 0);
-    const uint32_t v2 = __shfl_sync(0xffffffffu, key, k2 <= 32 ? 32 - k2 : 0);
-    wlk = k1 <= 32 ? key_to_float(v1) : -INFINITY;
-    wlkc = k2 <= 32 ? key_to_float(v2) : -INFINITY;
   }
   // block reduction of (max, sum, argmax) and of the bounds
   float m2 = sm, s2 = ss;
@@ -993,14 +1178,18 @@ __device__ __noinline__ void pass_a(const LaunchParams& P) {
     sh.red_f[warp * 2 + 1] = s2;
     sh.red_i[warp * 2] = a2;
     sh.red_wb[warp * 2] = wlk;
-    sh.red_wb[warp * 2 + 1] = wlkc;
   }
+  // per group set, in r2 (free until exchange 1; the top-p merged bins are not touched)
+  float(*red_j)[kNJ] = reinterpret_cast<float(*)[kNJ]>(S.r2);
+#pragma unroll
+  for (int t = 0; t < kGroups; ++t)
+    if (lane < kNJ) red_j[warp * kGroups + t][lane] = wlj[t];
   __syncthreads();
   if (warp == 0) {
     const bool in = lane < kWarps;
     float m = in ? sh.red_f[lane * 2] : -INFINITY, s = in ? sh.red_f[lane * 2 + 1] : 0.0f;
     int arg = in ? sh.red_i[lane * 2] : INT_MAX;
-    float lk = in ? sh.red_wb[lane * 2] : -INFINITY, lkc = in ? sh.red_wb[lane * 2 + 1] : INFINITY;
+    float lk = in ? sh.red_wb[lane * 2] : -INFINITY;
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) {
       const float om = __shfl_xor_sync(0xffffffffu, m, d);
@@ -1009,15 +1198,29 @@ __device__ __noinline__ void pass_a(const LaunchParams& P) {
       if (better(om, oa, m, arg)) arg = oa;
       merge_ms(m, s, om, os, cS);
       lk = fmaxf(lk, __shfl_xor_sync(0xffffffffu, lk, d));
-      lkc = fminf(lkc, __shfl_xor_sync(0xffffffffu, lkc, d));
+    }
+    // lane i < kNJ: the 2^i bounds over the group sets that reach 2^i maxima
+    float lj = INFINITY;
+    uint32_t nj = 0;
+    if (lane < kNJ)
+      for (int w = 0; w < kWarps * kGroups; ++w) {
+        const float v = red_j[w][lane];
+        if (v > -INFINITY) {
+          lj = fminf(lj, v);
+          ++nj;
+        }
+      }
+    if (lane < kNJ) {
+      sh.x1_mine.lj[lane] = topk_row ? lj : INFINITY;
+      sh.x1_mine.nj[lane] = topk_row ? (unsigned char)nj : 0;
     }
     if (lane == 0) {
       sh.x1_mine.m = m;
       sh.x1_mine.s = s;
       sh.x1_mine.arg = arg;
       sh.x1_mine.lk = lk;
-      sh.x1_mine.lkc = topk_row ? lkc : -INFINITY;
       sh.x1_mine.flags = sh.flags;
+      sh.x1_mine.nallowed = sh.nallowed;
     }
   }
   // the transformed logits, on request (debugging aid): plain values first, then the
@@ -1032,8 +1235,7 @@ __device__ __noinline__ void pass_a(const LaunchParams& P) {
     }
     __syncthreads();
     if (has_mod)
-      for (int i = tid; i < kHashCap; i += kThreads)
-        if (S.hkey[i] != kEmpty) out[S.hkey[i]] = S.hval[i];
+      for (int r = tid; r < sh.npen; r += kThreads) out[S.pid[r]] = S.pz[r];
   }
   __syncthreads();
 }
@@ -1062,7 +1264,7 @@ __device__ __noinline__ void exchange1(const LaunchParams& P) {
     const float ls = in ? sh.x1[lane].s : 0.0f;
     int fl = in ? sh.x1[lane].flags : 0;
     float lk = in ? sh.x1[lane].lk : -INFINITY;
-    float lkc = in ? sh.x1[lane].lkc : INFINITY;
+    int nal = in ? sh.x1[lane].nallowed : 0;
     float m = lm;
 #pragma unroll
     for (int d = 4; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
@@ -1074,8 +1276,20 @@ __device__ __noinline__ void exchange1(const LaunchParams& P) {
       arg = min(arg, __shfl_xor_sync(0xffffffffu, arg, d));
       fl |= __shfl_xor_sync(0xffffffffu, fl, d);
       lk = fmaxf(lk, __shfl_xor_sync(0xffffffffu, lk, d));
-      lkc = fminf(lkc, __shfl_xor_sync(0xffffffffu, lkc, d));
+      nal = max(nal, __shfl_xor_sync(0xffffffffu, nal, d));
     }
+    // the 2^i bounds: lane i combines the CTAs; usable when its warps guarantee k tokens
+    float bj = -INFINITY;
+    if (lane < kNJ) {
+      float lj = INFINITY;
+      uint32_t n = 0;
+      for (int c = 0; c < C; ++c) {
+        lj = fminf(lj, sh.x1[c].lj[lane]);
+        n += sh.x1[c].nj[lane];
+      }
+      if (n > 0 && (unsigned long long)n << lane >= (unsigned long long)max(sh.rp.k, 0)) bj = lj;
+    }
+    for (int d = 4; d > 0; d >>= 1) bj = fmaxf(bj, __shfl_xor_sync(0xffffffffu, bj, d));
     // the sum in a fixed order (ranks 0 .. C-1): every CTA gets the same bits
     float tot = 0.0f;
 #pragma unroll
@@ -1085,7 +1299,8 @@ __device__ __noinline__ void exchange1(const LaunchParams& P) {
       sh.rs.arg = arg;
       sh.rs.S = tot;
       sh.rs.flags = fl;
-      sh.rs.bound = fmaxf(lk, lkc);
+      sh.rs.bound = fmaxf(lk, bj);
+      sh.rs.nallowed_max = nal;
       sh.rs.lnS = logf(tot);
     }
   }
@@ -1118,19 +1333,22 @@ __device__ __noinline__ bool finish_early(const LaunchParams& P) {
 }
 
 // Truncation plan.  y = (z' - m) * (1/T); the kept set K = {y >= cut} is an upper set.
-__device__ __noinline__ void plan_row() {
+__device__ __noinline__ void plan_row(const LaunchParams& P) {
   if (threadIdx.x == 0) {
     const RowParams q = sh.rp;
     RowState& rs = sh.rs;
     rs.invT = __frcp_rn(q.T);
     rs.L = q.mp > 0.0f ? (float)log((double)q.mp) : -INFINITY;  // min-p: y >= ln(min_p)
     const bool kfin = q.k >= 2;
-    int plan = kPlanSlow, needW = 0;
+    int plan = kPlanSlow, needW = 0, all = 0;
     float theta = -INFINITY;
     if (kfin && rs.bound > -INFINITY) {
       plan = kPlanFast;  // every token of S_k has y >= y(bound)
       theta = y_of(rs.bound, rs.m, rs.invT);
       if (q.p >= 1.0f) theta = fmaxf(theta, rs.L);
+    } else if (rs.nallowed_max <= kCandCap) {
+      plan = kPlanFast;  // few candidates: the leader sees all of them
+      all = 1;
     } else if (q.mp > 0.0f && (q.p >= 1.0f || !kfin)) {
       plan = kPlanFast;  // K lies in {y >= ln min_p}
       theta = rs.L;
@@ -1142,7 +1360,10 @@ __device__ __noinline__ void plan_row() {
     }
     rs.plan = plan;
     rs.needW = needW;
+    rs.all = all;
     rs.theta = theta;
+    const int arg = rs.arg;  // its y is 0
+    rs.s0 = race_score(0.0f, pick_word(race_words_call((uint32_t)(arg >> 2), q.seed, q.pos), arg & 3));
   }
   __syncthreads();
 }
@@ -1168,6 +1389,7 @@ __device__ __forceinline__ void append(Cand* cand, int cap, bool keep, float y, 
 // every CTA: exchange 2 (or 3).
 __device__ void finish_mine(int cap, unsigned long long w, const Race& race) {
   const cg::cluster_group cluster = cg::this_cluster();
+  __threadfence();  // the compacted candidates (global) before the cluster barrier
   __syncthreads();
   if (threadIdx.x == 0) {
     sh.x2_mine.count = sh.count;
@@ -1186,36 +1408,58 @@ __device__ __forceinline__ int x2_flags(int C) {
   return f;
 }
 
-// Every CTA stores its candidates into slot `rank` of the leader's gather area and
-// arrives on the leader's gather barrier; only the leader (rank 0) continues (returns
-// true).  Every CTA has finished reading its slice (a cluster barrier came before), so
-// the leader's ring and tables are free to be overwritten.
-__device__ bool gather_to_leader(const Smem& S, int cap, int count) {
+// After the last exchange every CTA's candidates sit in its global segment (the counts
+// are known to every CTA).  Only the leader (rank 0) continues: it packs them, in rank
+// order, into its shared gather area (the ring is free: every CTA has finished reading
+// its slice), or, when there are more than kGatherCap, into its own global segments.
+// Returns the packed array (nullptr in the other CTAs) and their number in *n.
+__device__ const Cand* collect_at_leader(const LaunchParams& P, const Smem& S, int* n) {
   const cg::cluster_group cluster = cg::this_cluster();
+  if (cluster.block_rank() != 0) return nullptr;
   const int tid = threadIdx.x;
-  const int rank = (int)cluster.block_rank();
-  Cand* dst = cluster.map_shared_rank(S.gather, 0u) + rank * cap;
-  for (int i = tid; i < count; i += kThreads) dst[i] = S.cand[i];
-  __syncthreads();
-  if (tid == 0) mbar_arrive_remote(&sh.gather_bar, 0u);
-  if (rank != 0) return false;
-  if (tid == 0) sh.none = mbar_wait_cluster(&sh.gather_bar, 0) ? 0 : 1;
-  __syncthreads();
-  (void)mbar_try_wait_cluster(&sh.gather_bar, 0);  // every thread acquires the peers' stores
-  return true;
-}
-
-// Slot i of the gathered set belongs to CTA i / cap and is valid below that CTA's count.
-__device__ __forceinline__ bool gvalid(int i, int span, int cap) {
-  return i < span && (i & (cap - 1)) < sh.x2[i / cap].count;
+  const int C = P.C;
+  const int row = (int)(blockIdx.x / (unsigned)C);
+  Cand* seg = P.cand + (size_t)row * C * kCandCap;
+  int ntot = 0;
+  for (int c = 0; c < C; ++c) ntot += sh.x2[c].count;
+  *n = ntot;
+  if (ntot <= kGatherCap) {
+    int off = 0;
+    for (int c = 0; c < C; ++c) {
+      const int cnt = sh.x2[c].count;
+      for (int i = tid; i < cnt; i += kThreads) S.gather[off + i] = seg[(size_t)c * kCandCap + i];
+      off += cnt;
+    }
+    __syncthreads();
+    return S.gather;
+  }
+  // in place, segment by segment: each moves towards lower addresses, read whole first
+  int off = sh.x2[0].count;
+  for (int c = 1; c < C; ++c) {
+    const int cnt = sh.x2[c].count;
+    Cand tmp[kCandCap / kThreads];
+#pragma unroll
+    for (int t = 0; t < kCandCap / kThreads; ++t) {
+      const int i = t * kThreads + tid;
+      if (i < cnt) tmp[t] = seg[(size_t)c * kCandCap + i];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int t = 0; t < kCandCap / kThreads; ++t) {
+      const int i = t * kThreads + tid;
+      if (i < cnt) seg[off + i] = tmp[t];
+    }
+    __syncthreads();
+    off += cnt;
+  }
+  return seg;
 }
 
 // Radix select over the gathered set (entries with y >= ylo): the largest value v such
 // that the count (or fixed-point weight) of entries >= v reaches `target`.
-__device__ __noinline__ float local_select(int chunk, int span, int cap, bool weighted, float ylo,
+__device__ __noinline__ float local_select(int chunk, const Cand* G, int n, bool weighted, float ylo,
                                            unsigned long long target, bool* found) {
   const Smem S = carve(chunk);
-  const Cand* G = S.gather;
   const int tid = threadIdx.x, warp = tid >> 5;
   uint32_t prefix = 0u, pmask = 0u;
   for (int pass = 0; pass < 4; ++pass) {
@@ -1225,9 +1469,9 @@ __device__ __noinline__ float local_select(int chunk, int span, int cap, bool we
       S.hist_w[tid] = 0ull;
     }
     __syncthreads();
-    for (int base = 0; base < span; base += kThreads) {
+    for (int base = 0; base < n; base += kThreads) {
       const int i = base + tid;
-      const bool ok = gvalid(i, span, cap);
+      const bool ok = i < n;
       const float y = ok ? G[i].y : -INFINITY;
       const uint32_t key = fkey(y);
       const bool pred = ok && y >= ylo && (key & pmask) == prefix;
@@ -1260,12 +1504,11 @@ __device__ __noinline__ float local_select(int chunk, int span, int cap, bool we
 // 1024-bucket histogram (bucket order follows y), then the crossing bucket's entries are
 // resolved by counting.  Falls back to local_select when that bucket holds more than
 // 1024 entries (heavy ties).
-__device__ __noinline__ float leader_select(int chunk, int span, int cap, bool weighted, float lo, float hi,
+__device__ __noinline__ float leader_select(int chunk, const Cand* G, int n, bool weighted, float lo, float hi,
                                             float ylo, unsigned long long target, bool* found) {
   const Smem S = carve(chunk);
-  const Cand* G = S.gather;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  unsigned long long* bk = reinterpret_cast<unsigned long long*>(S.r2);
+  uint32_t* bk = reinterpret_cast<uint32_t*>(S.r2);  // split counters, two u32 per bucket
   constexpr int kPer = 1024 / kThreads;  // consecutive buckets per thread
   const float scale = hi > lo ? 1024.0f / (hi - lo) : 0.0f;
   auto bucket = [&](float y) -> int {
@@ -1273,24 +1516,23 @@ __device__ __noinline__ float leader_select(int chunk, int span, int cap, bool w
     return b < 0 ? 0 : (b > 1023 ? 1023 : b);
   };
 #pragma unroll
-  for (int t = 0; t < kPer; ++t) bk[kPer * tid + t] = 0ull;
+  for (int t = 0; t < 2 * kPer; ++t) bk[2 * kPer * tid + t] = 0u;
   if (tid == 0) {
     sh.nl = 0;
     sh.bstar = -1;
   }
   __syncthreads();
-  for (int i = tid; i < span; i += kThreads) {
-    if (!gvalid(i, span, cap)) continue;
+  for (int i = tid; i < n; i += kThreads) {
     const float y = G[i].y;
     if (!(y >= ylo)) continue;
-    atomicAdd(&bk[bucket(y)], weighted ? weight_fx(y) : 1ull);
+    split_add(bk + 2 * bucket(y), weighted ? weight_fx(y) : 1ull);
   }
   __syncthreads();
   {
     unsigned long long vb[kPer], loc = 0;
 #pragma unroll
     for (int t = 0; t < kPer; ++t) {
-      vb[t] = bk[kPer * tid + t];
+      vb[t] = split_get(bk + 2 * (kPer * tid + t));
       loc += vb[t];
     }
     unsigned long long x = loc;
@@ -1326,8 +1568,7 @@ __device__ __noinline__ float leader_select(int chunk, int span, int cap, bool w
   // the crossing bucket's entries, gathered into the (now free) bucket area
   Cand* Lb = reinterpret_cast<Cand*>(S.r2);
   __syncthreads();
-  for (int i = tid; i < span; i += kThreads) {
-    if (!gvalid(i, span, cap)) continue;
+  for (int i = tid; i < n; i += kThreads) {
     const Cand cd = G[i];
     if (!(cd.y >= ylo) || bucket(cd.y) != bstar) continue;
     const int p = atomicAdd(&sh.nl, 1);
@@ -1337,7 +1578,7 @@ __device__ __noinline__ float leader_select(int chunk, int span, int cap, bool w
   const int nl = sh.nl;
   if (nl > 1024) {
     __syncthreads();
-    return local_select(chunk, span, cap, weighted, ylo, target, found);
+    return local_select(chunk, G, n, weighted, ylo, target, found);
   }
   for (int i = tid; i < nl; i += kThreads) {
     const float yi = Lb[i].y;
@@ -1356,14 +1597,11 @@ __device__ __noinline__ float leader_select(int chunk, int span, int cap, bool w
 }
 
 // The race over the gathered entries with y >= cut (block-reduced into thread 0).
-__device__ __noinline__ Race leader_race(int chunk, int span, int cap, float cut, unsigned long long seed,
+__device__ __noinline__ Race leader_race(const Cand* G, int n, float cut, unsigned long long seed,
                                          unsigned long long pos) {
-  const Smem S = carve(chunk);
-  const Cand* G = S.gather;
   Race r;
-  r.init();
-  for (int i = threadIdx.x; i < span; i += kThreads) {
-    if (!gvalid(i, span, cap)) continue;
+  r.init(sh.rs.s0);
+  for (int i = threadIdx.x; i < n; i += kThreads) {
     const Cand cd = G[i];
     if (!(cd.y >= cut)) continue;
     r.add(cd.y, cd.id, pick_word(race_words_call((uint32_t)(cd.id >> 2), seed, pos), cd.id & 3));
@@ -1391,7 +1629,8 @@ __device__ __noinline__ bool route_fast(const LaunchParams& P, int& pass) {
   const bool has_mod = a.hist_offs != nullptr || a.bias_offs != nullptr;
   const bool kfin = q.k >= 2;
   const unsigned long long seed = q.seed, pos = q.pos;
-  const int c0 = g.c0, cap = g.cap, C = g.C;
+  const int c0 = g.c0, cap = kCandCap, C = g.C;
+  Cand* mycand = P.cand + ((size_t)g.row * C + g.rank) * kCandCap;  // this slice's segment
   if (warp == 0) {
     const float zt = z_threshold_warp(theta, m, invT);
     if (lane == 0) sh.zth = zt;
@@ -1400,7 +1639,7 @@ __device__ __noinline__ bool route_fast(const LaunchParams& P, int& pass) {
   const float zth = sh.zth;
   unsigned long long w = 0;
   Race race;
-  race.init();
+  race.init(sh.rs.s0);
   stream<kBF16>(g, S, pass, false, [&](int f, uint32_t wd, const float4& v) {
     float z[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
     if (wd) {
@@ -1430,7 +1669,7 @@ __device__ __noinline__ bool route_fast(const LaunchParams& P, int& pass) {
           }
         }
         if (worth) {
-          const uint4 x = race_words_call((uint32_t)((c0 >> 2) + f), seed, pos);
+          const uint4 x = race_words((uint32_t)((c0 >> 2) + f), seed, pos);
 #pragma unroll 1
           for (int j = 0; j < 4; ++j)
             if (z[j] > -INFINITY) race.add(y[j], c0 + 4 * f + j, pick_word(x, j));
@@ -1447,23 +1686,23 @@ __device__ __noinline__ bool route_fast(const LaunchParams& P, int& pass) {
 #pragma unroll 1
         for (int j = 0; j < 4; ++j) {
           const bool keep = z[j] > -INFINITY && z[j] >= zth;
-          append(S.cand, cap, keep, keep ? y_of(z[j], m, invT) : 0.0f, c0 + 4 * f + j);
+          append(mycand, cap, keep, keep ? y_of(z[j], m, invT) : 0.0f, c0 + 4 * f + j);
         }
       }
     }
   });
   if (has_mod) {
-    for (int base = 0; base < kHashCap; base += kThreads) {
+    const int npen = sh.npen;
+    for (int base = 0; base < npen; base += kThreads) {
       const int i = base + tid;
-      float z = -INFINITY;
-      if (S.hkey[i] != kEmpty) z = S.hval[i];
-      const int gi = c0 + (int)S.hkey[i];
+      const float z = i < npen ? S.pz[i] : -INFINITY;
+      const int gi = c0 + (i < npen ? (int)S.pid[i] : 0);
       const float y = z > -INFINITY ? y_of(z, m, invT) : -INFINITY;
       if (z > -INFINITY) {
         if (needW) w += weight_fx(y);
         if (plan == kPlanUntrunc) race.add(y, gi, pick_word(race_words_call((uint32_t)(gi >> 2), seed, pos), gi & 3));
       }
-      if (plan == kPlanFast) append(S.cand, cap, z > -INFINITY && z >= zth, y, gi);
+      if (plan == kPlanFast) append(mycand, cap, z > -INFINITY && z >= zth, y, gi);
     }
   }
   if (needW) w = block_sum_u64(w, sh.red_u);
@@ -1483,37 +1722,53 @@ __device__ __noinline__ bool route_fast(const LaunchParams& P, int& pass) {
     return true;
   }
   if (fl & kFlagOverflow) return false;
-  if (!gather_to_leader(S, cap, sh.x2[g.rank].count)) return true;
-  const bool gathered = sh.none == 0 && !(fl & kFlagRing);
-  const int span = C * cap;
   int ntot = 0;
-  for (int c = 0; c < C; ++c) ntot += sh.x2[c].count;
+  const Cand* G = collect_at_leader(P, S, &ntot);
+  if (!G) return true;
+  const bool gathered = !(fl & kFlagRing);
+  // the bucket range: [theta, 0], or the gathered candidates' finite range
+  float lo = theta;
+  if (!(lo > -INFINITY)) {
+    float ymin = INFINITY;
+    for (int i = tid; i < ntot; i += kThreads) {
+      const float y = G[i].y;
+      if (y > -INFINITY) ymin = fminf(ymin, y);
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) ymin = fminf(ymin, __shfl_xor_sync(0xffffffffu, ymin, d));
+    if (lane == 0) sh.red_f[warp] = ymin;
+    __syncthreads();
+    lo = INFINITY;
+    for (int w = 0; w < kWarps; ++w) lo = fminf(lo, sh.red_f[w]);
+    if (!(lo < 0.0f)) lo = -1.0f;
+    __syncthreads();
+  }
   float tk = -INFINITY;
   if (kfin && ntot >= q.k) {
     bool found;
-    const float v = leader_select(g.chunk, span, cap, false, theta, 0.0f, -INFINITY, (unsigned long long)q.k, &found);
+    const float v = leader_select(g.chunk, G, ntot, false, lo, 0.0f, -INFINITY, (unsigned long long)q.k, &found);
     if (found) tk = v;
   }
   float tp = -INFINITY;
   if (q.p < 1.0f) {
     unsigned long long mset = 0;
-    for (int i = tid; i < span; i += kThreads)
-      if (gvalid(i, span, cap) && S.gather[i].y >= tk) mset += weight_fx(S.gather[i].y);
+    for (int i = tid; i < ntot; i += kThreads)
+      if (G[i].y >= tk) mset += weight_fx(G[i].y);
     mset = block_sum_u64(mset, sh.red_u);
-    unsigned long long Wk = mset;
-    if (!kfin) {
+    unsigned long long Wk = mset;  // top-k set (or every candidate) gathered: its mass
+    if (!kfin && !sh.rs.all) {
       Wk = 0;
       for (int c = 0; c < C; ++c) Wk += sh.x2[c].w;
     }
     const unsigned long long cth = ceil_scaled(Wk, q.p);
     if (mset >= cth) {
       bool found;
-      const float v = leader_select(g.chunk, span, cap, true, theta, 0.0f, tk, cth, &found);
+      const float v = leader_select(g.chunk, G, ntot, true, lo, 0.0f, tk, cth, &found);
       if (found) tp = v;
     }
   }
   const float cut = fmaxf(tk, fmaxf(tp, L));
-  const Race r = leader_race(g.chunk, span, cap, cut, seed, pos);
+  const Race r = leader_race(G, ntot, cut, seed, pos);
   if (tid == 0) write_sampled(a, g.row, r, lnS, gathered);
   return true;
 }
@@ -1533,14 +1788,16 @@ __device__ __noinline__ bool route_topp(const LaunchParams& P, int& pass) {
   const float m = sh.rs.m, invT = sh.rs.invT, lnS = sh.rs.lnS;
   const bool has_mod = a.hist_offs != nullptr || a.bias_offs != nullptr;
   const unsigned long long seed = q.seed, pos = q.pos;
-  const int c0 = g.c0, cap = g.cap, C = g.C;
+  const int c0 = g.c0, cap = kCandCap, C = g.C;
+  Cand* mycand = P.cand + ((size_t)g.row * C + g.rank) * kCandCap;  // this slice's segment
   const cg::cluster_group cluster = cg::this_cluster();
 
-  unsigned long long* whist = reinterpret_cast<unsigned long long*>(S.cand);
-  for (int i = tid; i < kWarps * kPBins; i += kThreads) whist[i] = 0ull;
+  // warp-private split counters (two u32 per bin): a warp adds at most 4160 weights
+  uint32_t* whist = reinterpret_cast<uint32_t*>(S.r2);
+  for (int i = tid; i < 2 * kWarps * kPBins; i += kThreads) whist[i] = 0u;
   __syncthreads();
-  unsigned long long w = 0;
-  unsigned long long* mine = whist + warp * kPBins;
+  unsigned long long w = 0, wlast = 0;
+  uint32_t* mine = whist + 2 * warp * kPBins;
   stream<kBF16>(g, S, pass, false, [&](int f, uint32_t wd, const float4& v) {
     if (!wd) return;
     const bool fastv = wd == 0xFu && finite4(v);
@@ -1552,28 +1809,34 @@ __device__ __noinline__ bool route_topp(const LaunchParams& P, int& pass) {
       const unsigned long long qw = weight_fx(y);
       if (!qw) continue;
       w += qw;
-      atomicAdd(mine + pbin(y), qw);
+      const int b = pbin(y);
+      if (b == kPBins - 1) wlast += qw;  // the open-ended last bin: one add per thread below
+      else split_add(mine + 2 * b, qw);
     }
   });
   if (has_mod) {
-    for (int i = tid; i < kHashCap; i += kThreads) {
-      if (S.hkey[i] == kEmpty) continue;
-      const float z = S.hval[i];
+    for (int i = tid; i < sh.npen; i += kThreads) {
+      const float z = S.pz[i];
       if (!(z > -INFINITY)) continue;
       const float y = y_of(z, m, invT);
       const unsigned long long qw = weight_fx(y);
       if (!qw) continue;
       w += qw;
-      atomicAdd(mine + pbin(y), qw);
+      split_add(mine + 2 * pbin(y), qw);
     }
+  }
+  {
+    const unsigned long long wl = warp_sum_u64(wlast);  // < 2^53: split_add holds it
+    if ((tid & 31) == 0 && wl) split_add(mine + 2 * (kPBins - 1), wl);
   }
   w = block_sum_u64(w, sh.red_u);
   // merge the warp histograms and push them into every CTA's merged copy
+  unsigned long long* pmrg = reinterpret_cast<unsigned long long*>(S.mrg_c);  // zeroed by the prologue
   if (tid < kPBins) {
     unsigned long long t = 0;
-    for (int wp = 0; wp < kWarps; ++wp) t += whist[wp * kPBins + tid];
+    for (int wp = 0; wp < kWarps; ++wp) t += split_get(whist + 2 * (wp * kPBins + tid));
     if (t)
-      for (int r = 0; r < C; ++r) atomicAdd(cluster.map_shared_rank(S.mrg_w + tid, (unsigned)r), t);
+      for (int r = 0; r < C; ++r) atomicAdd(cluster.map_shared_rank(pmrg + tid, (unsigned)r), t);
   }
   Race none_race;
   none_race.init();
@@ -1587,7 +1850,7 @@ __device__ __noinline__ bool route_topp(const LaunchParams& P, int& pass) {
   {
     unsigned long long cum = 0;
     for (int b = 0; b < kPBins; ++b) {
-      const unsigned long long nb = cum + S.mrg_w[b];
+      const unsigned long long nb = cum + pmrg[b];
       if (nb >= cth) {
         bstar = b;
         above = cum;
@@ -1604,7 +1867,7 @@ __device__ __noinline__ bool route_topp(const LaunchParams& P, int& pass) {
   if (tid == 0) sh.count = 0;
   __syncthreads();
   Race race;
-  race.init();
+  race.init(sh.rs.s0);
   stream<kBF16>(g, S, pass, false, [&](int f, uint32_t wd, const float4& v) {
     float y[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
     if (wd) {
@@ -1638,33 +1901,35 @@ __device__ __noinline__ bool route_topp(const LaunchParams& P, int& pass) {
                                                  (y[2] > ylo && y[2] <= yhi) || (y[3] > ylo && y[3] <= yhi));
     if (any) {
 #pragma unroll 1
-      for (int j = 0; j < 4; ++j) append(S.cand, cap, y[j] > ylo && y[j] <= yhi, y[j], c0 + 4 * f + j);
+      for (int j = 0; j < 4; ++j) append(mycand, cap, y[j] > ylo && y[j] <= yhi, y[j], c0 + 4 * f + j);
     }
   });
   if (has_mod) {
-    for (int base = 0; base < kHashCap; base += kThreads) {
+    const int npen = sh.npen;
+    for (int base = 0; base < npen; base += kThreads) {
       const int i = base + tid;
       float y = -INFINITY;
       int gi = 0;
-      if (S.hkey[i] != kEmpty && S.hval[i] > -INFINITY) {
-        y = y_of(S.hval[i], m, invT);
-        gi = c0 + (int)S.hkey[i];
+      if (i < npen && S.pz[i] > -INFINITY) {
+        y = y_of(S.pz[i], m, invT);
+        gi = c0 + (int)S.pid[i];
         if (y > yhi) race.add(y, gi, pick_word(race_words_call((uint32_t)(gi >> 2), seed, pos), gi & 3));
       }
-      append(S.cand, cap, y > ylo && y <= yhi, y, gi);
+      append(mycand, cap, y > ylo && y <= yhi, y, gi);
     }
   }
   block_reduce_race(race, sh.red_x);
   finish_mine(cap, 0ull, race);  // exchange 3
   const int fl = x2_flags(C);
   if (fl & kFlagOverflow) return false;
-  if (!gather_to_leader(S, cap, sh.x2[g.rank].count)) return true;
-  const bool gathered = sh.none == 0 && !(fl & kFlagRing);
+  int ntot = 0;
+  const Cand* G = collect_at_leader(P, S, &ntot);
+  if (!G) return true;
+  const bool gathered = !(fl & kFlagRing);
   // the cut lies in the crossing bin: a weighted select over its tokens
   bool found;
-  const int span = C * cap;
-  const float vstar = leader_select(g.chunk, span, cap, true, ylo, yhi, -INFINITY, cth - above, &found);
-  Race r = leader_race(g.chunk, span, cap, vstar, seed, pos);
+  const float vstar = leader_select(g.chunk, G, ntot, true, ylo, yhi, -INFINITY, cth - above, &found);
+  Race r = leader_race(G, ntot, vstar, seed, pos);
   if (tid == 0) {
     for (int c = 0; c < C; ++c) r.merge(sh.x2[c]);
     write_sampled(a, g.row, r, lnS, gathered && found);
@@ -1717,12 +1982,13 @@ __device__ __noinline__ float cluster_select(const LaunchParams& P, int& pass, i
       }
     });
     if (has_mod) {
-      for (int base = 0; base < kHashCap; base += kThreads) {
+      const int npen = sh.npen;
+      for (int base = 0; base < npen; base += kThreads) {
         const int i = base + tid;
         bool pred = false;
         float y = -INFINITY;
-        if (S.hkey[i] != kEmpty) {
-          const float z = S.hval[i];
+        if (i < npen) {
+          const float z = S.pz[i];
           if (z > -INFINITY) {
             y = y_of(z, m, invT);
             pred = y >= ylo && (fkey(y) & pmask) == prefix;
@@ -1814,9 +2080,8 @@ __device__ __noinline__ void route_slow(const LaunchParams& P, int& pass) {
       }
     });
     if (has_mod)
-      for (int i = tid; i < kHashCap; i += kThreads) {
-        if (S.hkey[i] == kEmpty) continue;
-        const float z = S.hval[i];
+      for (int i = tid; i < sh.npen; i += kThreads) {
+        const float z = S.pz[i];
         if (!(z > -INFINITY)) continue;
         const float y = y_of(z, m, invT);
         if (y >= tk) w += weight_fx(y);
@@ -1834,7 +2099,7 @@ __device__ __noinline__ void route_slow(const LaunchParams& P, int& pass) {
   }
   const float cut = fmaxf(tk, fmaxf(tp, L));
   Race race;
-  race.init();
+  race.init(sh.rs.s0);
   stream<kBF16>(g, S, pass, false, [&](int f, uint32_t wd, const float4& v) {
     float y[4];
     uint32_t keep = 0u;
@@ -1848,19 +2113,18 @@ __device__ __noinline__ void route_slow(const LaunchParams& P, int& pass) {
       if (y[j] >= cut) keep |= 1u << j;
     }
     if (!keep) return;
-    const uint4 x = race_words_call((uint32_t)((c0 >> 2) + f), seed, pos);
+    const uint4 x = race_words((uint32_t)((c0 >> 2) + f), seed, pos);
 #pragma unroll 1
     for (int j = 0; j < 4; ++j)
       if ((keep >> j) & 1u) race.add(y[j], c0 + 4 * f + j, pick_word(x, j));
   });
   if (has_mod)
-    for (int i = tid; i < kHashCap; i += kThreads) {
-      if (S.hkey[i] == kEmpty) continue;
-      const float z = S.hval[i];
+    for (int i = tid; i < sh.npen; i += kThreads) {
+      const float z = S.pz[i];
       if (!(z > -INFINITY)) continue;
       const float y = y_of(z, m, invT);
       if (!(y >= cut)) continue;
-      const int gi = c0 + (int)S.hkey[i];
+      const int gi = c0 + (int)S.pid[i];
       race.add(y, gi, pick_word(race_words_call((uint32_t)(gi >> 2), seed, pos), gi & 3));
     }
   block_reduce_race(race, sh.red_x);
@@ -1891,9 +2155,13 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) sampler_kernel(const __g
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   prologue<kBF16>(P);
   pass_a<kBF16>(P);
+  ring_prefetch_pass<kBF16>(P, 1);
   exchange1(P);
-  if (finish_early(P)) return;
-  plan_row();
+  if (finish_early(P)) {
+    ring_drain<kBF16>(P);
+    return;
+  }
+  plan_row(P);
   int pass = 1;
   const int plan = sh.rs.plan;
   if (plan == kPlanFast || plan == kPlanUntrunc) {
@@ -1936,7 +2204,6 @@ Geometry geometry_for(int vocab) {
   g.chunk = chunk;
   g.smem = (int)layout_for(chunk).total;
   g.cap = kCandCap;
-  static_assert(kCandCap * kMaxCluster <= kGatherCap, "the leader cannot gather every candidate");
   return g;
 }
 
@@ -1947,6 +2214,9 @@ struct clsample_handle {
   int vocab;
   int device;
   Geometry g;
+  PenEntry* pen;  // penalised-token lists, [max_batch * C][kPenCap]
+  int2* pen_n;    // their lengths and flags, [max_batch * C]
+  Cand* cand;     // compacted candidates, [max_batch * C][kCandCap]
 };
 
 extern "C" {
@@ -1994,16 +2264,38 @@ int clsample_create(int32_t max_batch, int32_t vocab, clsample_t** out) {
   if (cudaFuncSetAttribute(k32, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem) != cudaSuccess ||
       cudaFuncSetAttribute(k16, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem) != cudaSuccess)
     return CLSAMPLE_ERR_CUDA;
+  PenEntry* pen = nullptr;
+  int2* pen_n = nullptr;
+  Cand* cand = nullptr;
+  if (max_batch > 0) {
+    const size_t lists = (size_t)max_batch * (size_t)g.C;
+    if (cudaMalloc(&pen, lists * kPenCap * sizeof(PenEntry)) != cudaSuccess ||
+        cudaMalloc(&pen_n, lists * sizeof(int2)) != cudaSuccess ||
+        cudaMalloc(&cand, lists * kCandCap * sizeof(Cand)) != cudaSuccess) {
+      if (pen) cudaFree(pen);
+      if (pen_n) cudaFree(pen_n);
+      return CLSAMPLE_ERR_CUDA;
+    }
+  }
   clsample_t* h = new clsample_t;
   h->max_batch = max_batch;
   h->vocab = vocab;
   h->device = dev;
   h->g = g;
+  h->pen = pen;
+  h->pen_n = pen_n;
+  h->cand = cand;
   *out = h;
   return CLSAMPLE_SUCCESS;
 }
 
-void clsample_destroy(clsample_t* h) { delete h; }
+void clsample_destroy(clsample_t* h) {
+  if (!h) return;
+  if (h->pen) cudaFree(h->pen);
+  if (h->pen_n) cudaFree(h->pen_n);
+  if (h->cand) cudaFree(h->cand);
+  delete h;
+}
 
 static void fill_launch(const Geometry& g, unsigned nclusters, cudaStream_t stream, cudaLaunchConfig_t* cfg,
                         cudaLaunchAttribute* attr) {
@@ -2045,10 +2337,18 @@ int clsample_apply(clsample_t* h, const clsample_args_t* a, clsample_stream_t st
   P.cap = g.cap;
   const uintptr_t base = reinterpret_cast<uintptr_t>(a->logits);
   P.vec_ok = (base % 16 == 0) && (((long long)a->logits_row_stride * esize) % 16 == 0);
+  P.pen = h->pen;
+  P.pen_n = h->pen_n;
+  P.cand = h->cand;
 
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (a->hist_offs || a->bias_offs) {
+    penalty_kernel<<<(unsigned)(a->B * g.C), kThreads, 0, st>>>(P);
+    if (cudaGetLastError() != cudaSuccess) return CLSAMPLE_ERR_CUDA;
+  }
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
-  fill_launch(g, (unsigned)a->B, reinterpret_cast<cudaStream_t>(stream), &cfg, attr);
+  fill_launch(g, (unsigned)a->B, st, &cfg, attr);
   const cudaError_t err = bf16 ? cudaLaunchKernelEx(&cfg, sampler_kernel<true>, P)
                                : cudaLaunchKernelEx(&cfg, sampler_kernel<false>, P);
   return err == cudaSuccess ? CLSAMPLE_SUCCESS : CLSAMPLE_ERR_CUDA;

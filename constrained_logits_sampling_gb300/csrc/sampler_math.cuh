@@ -73,7 +73,8 @@ __device__ __forceinline__ float exp32(float y) {
   q = __fmaf_rn(q, r, 0.5f);
   q = __fmaf_rn(q, r, 1.0f);
   q = __fmaf_rn(q, r, 1.0f);
-  return ldexpf(q, (int)n);
+  // q * 2^n is exact: n >= -47, so 2^n is a normal float and the product stays normal
+  return __fmul_rn(q, __int_as_float(((int)n + 127) << 23));
 }
 
 // Top-p weight of a token in 2^-40 fixed point, rounded down.  Sums of these are exact

@@ -58,6 +58,7 @@ constexpr int kGatherCap = 4096;   // candidates the leader keeps in shared memo
 constexpr int kMaxChunk = 32 * 1024;  // longest slice
 constexpr int kStageBytes = 8192;     // one ring stage: two 16-byte vectors per thread
 constexpr int kStages = 4;            // ring depth
+constexpr int kReload = 4;            // 16-byte loads in flight per thread when re-reading
 constexpr uint32_t kEmpty = 0xFFFFFFFFu;
 // penalised-token table: count | kBiasBit (a logit_bias entry applies) | kAllowedBit
 constexpr uint32_t kAllowedBit = 0x80000000u;
@@ -98,7 +99,15 @@ struct LaunchParams {
   PenEntry* pen;      // [B * C][kPenCap] penalised-token lists (scratch)
   int2* pen_n;        // [B * C] list length, flags
   Cand* cand;         // [B * C][kCandCap] compacted candidates (scratch)
+  int* row_class;     // [B] cost class of each row (scratch)
+  int* row_order;     // [B] the row each cluster samples, heaviest class first (scratch)
+  unsigned* ticket;   // CTAs of the preparation kernel that have finished (scratch)
 };
+
+// The row sampled by the calling CTA's cluster (clusters take rows heaviest first).
+__device__ __forceinline__ int cluster_row(const LaunchParams& P) {
+  return __ldg(P.row_order + blockIdx.x / (unsigned)P.C);
+}
 
 // Slice statistics pushed to every CTA after pass A.
 // Lower bounds of the k-th largest z' come from maxima of disjoint token groups: each
@@ -276,7 +285,6 @@ struct Shared {
   int csr[4];
   float zth, res;
   int bstar, nl, flags, count, digit, none, npen;
-  int pre;  // the pass whose first ring stages were issued ahead of time (-1: none)
   int nallowed;
   unsigned long long above;
 };
@@ -298,7 +306,7 @@ __device__ __forceinline__ Geo geo(const LaunchParams& P) {
   g.chunk = P.chunk;
   g.cap = P.cap;
   g.rank = (int)cg::this_cluster().block_rank();
-  g.row = (int)(blockIdx.x / (unsigned)g.C);
+  g.row = cluster_row(P);
   g.c0 = g.rank * g.chunk;
   g.len = max(0, min(P.a.V, g.c0 + g.chunk) - g.c0);
   g.nvec = g.chunk / 4;
@@ -326,6 +334,18 @@ __device__ __forceinline__ float4 gload4(const Geo& g, int f) {
   return make_float4(i < g.len ? gload1<kBF16>(g.g, i) : 0.0f, i + 1 < g.len ? gload1<kBF16>(g.g, i + 1) : 0.0f,
                      i + 2 < g.len ? gload1<kBF16>(g.g, i + 2) : 0.0f,
                      i + 3 < g.len ? gload1<kBF16>(g.g, i + 3) : 0.0f);
+}
+
+// Tokens 4f .. 4f+3 by one aligned load (the slice start is 16-byte aligned and the
+// vector lies inside the row), widened to f32.
+template <bool kBF16>
+__device__ __forceinline__ float4 vload4(const Geo& g, int f) {
+  if (kBF16) {
+    const uint2 w = __ldg(reinterpret_cast<const uint2*>(g.g) + f);
+    return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u), __uint_as_float(w.y << 16),
+                       __uint_as_float(w.y & 0xFFFF0000u));
+  }
+  return __ldg(reinterpret_cast<const float4*>(g.g) + f);
 }
 
 // Vector v (4 tokens) of a ring stage buffer, widened to f32.
@@ -678,9 +698,9 @@ __device__ __forceinline__ void stream(const Geo& g, const Smem& S, int& pass, b
   constexpr int kVecPerStage = kStageBytes / (4 * kEsize);
   constexpr int kVPT = kVecPerStage / kThreads;
   const int tid = threadIdx.x;
-  if (g.nst > 0) {
-    const uint32_t seq0 = (uint32_t)pass * (uint32_t)g.nst;
-    if (tid == 0 && !started && sh.pre != pass) ring_start<kBF16>(g, S, pass);
+  if (pass == 0 && g.nst > 0) {
+    const uint32_t seq0 = 0u;
+    if (tid == 0 && !started) ring_start<kBF16>(g, S, pass);
 #pragma unroll 1
     for (int k = 0; k < g.nst; ++k) {
       const uint32_t s = seq0 + (uint32_t)k;
@@ -706,6 +726,29 @@ __device__ __forceinline__ void stream(const Geo& g, const Smem& S, int& pass, b
       }
     }
   }
+  if (pass > 0 && g.bulk_tokens > 0) {
+    // later passes find the slice in L2: plain 16-byte loads, kReload per thread in
+    // flight (bulk copies would queue behind the HBM copies of other CTAs' first passes)
+    const int nv = g.bulk_tokens / 4;
+#pragma unroll 1
+    for (int base = 0; base < nv; base += kReload * kThreads) {
+      float4 v[kReload];
+      uint32_t wd[kReload];
+#pragma unroll
+      for (int u = 0; u < kReload; ++u) {
+        const int f = base + u * kThreads + tid;
+        const bool in = f < nv;
+        wd[u] = in ? live4(S.live, f) : 0u;  // later passes read only live tokens
+        v[u] = wd[u] ? vload4<kBF16>(g, f) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kReload; ++u) {
+        const int f = base + u * kThreads + tid;
+        if constexpr (kSlot) body(f < nv ? f : g.nvec, wd[u], v[u], 0);
+        else body(f < nv ? f : g.nvec, wd[u], v[u]);
+      }
+    }
+  }
   // the ragged tail, and whole unaligned slices: plain loads
   const int f_end = (g.len + 3) / 4;
 #pragma unroll 1
@@ -721,58 +764,60 @@ __device__ __forceinline__ void stream(const Geo& g, const Smem& S, int& pass, b
   ++pass;
 }
 
-// Sampling rows always stream their slice once more after exchange 1: the first stages
-// of that pass are issued now, so they load during the exchange.  Thread 0 only.
-template <bool kBF16>
-__device__ __noinline__ void ring_prefetch_pass(const LaunchParams& P, int pass) {
-  if (threadIdx.x != 0) return;
-  const RowParams q = sh.rp;
-  const bool greedy = (q.T < kGreedyEps) || q.k == 0 || q.k == 1;
-  const Geo g = geo<kBF16>(P);
-  if (greedy || q.invalid || g.nst == 0) return;
-  ring_start<kBF16>(g, carve(g.chunk), pass);
-  sh.pre = pass;
-}
-
-// A row that ends without using the stages issued ahead of time waits for them, so no
-// copy into this CTA's shared memory is in flight when it exits.  Thread 0 only.
-template <bool kBF16>
-__device__ __noinline__ void ring_drain(const LaunchParams& P) {
-  if (threadIdx.x != 0 || sh.pre < 0) return;
-  const Geo g = geo<kBF16>(P);
-  for (int k = 0; k < min(kStages, g.nst); ++k) ring_wait((uint32_t)sh.pre * (uint32_t)g.nst + (uint32_t)k);
-}
-
 // Adds n occurrences of local id l to the history counts; kFlagOverflow if the hash is
 // full.
-__device__ __noinline__ int count_id(uint32_t* hkey, uint32_t* hcnt, uint32_t l, uint32_t n) {
+__device__ __forceinline__ int count_id(uint32_t* hkey, uint32_t* hcnt, uint32_t l, uint32_t n) {
   const int slot = hash_insert(hkey, l);
   if (slot < 0) return kFlagOverflow;
   atomicAdd(&hcnt[slot], n);
   return 0;
 }
 
-// ---------------------------------------------------------------- penalty / bias scatter
+// ---------------------------------------------------------------- row preparation
 
-// One CTA per (row, slice), ahead of the sampler: the slice's distinct penalised or
-// biased token ids with their history count and the last bias entry (SGLang page, "Order
-// semantics of the penalties" and "Why logit_bias is built from triples": the last
-// duplicate wins), sorted by id, into the scratch list of the slice.  Duplicate history
-// ids are counted once per warp (Zipf-like histories repeat their frequent ids many
-// times).  A slice with more than kPenCap distinct ids is flagged OVERFLOW.
-__global__ void __launch_bounds__(kThreads) penalty_kernel(const __grid_constant__ LaunchParams P) {
+constexpr int kPrepThreads = 128;
+constexpr int kPrepWarps = kPrepThreads / 32;
+constexpr int kClasses = 5;
+
+// Expected cost class of a row from its parameters alone (0 = heaviest): top-p alone,
+// then untruncated or very large k, then large k or top-p over a min-p set, then the
+// other sampling rows, then greedy or invalid rows.  Only the launch order uses it.
+__device__ __forceinline__ int row_class(const clsample_args_t& a, int row) {
+  const float T = a.temperatures ? a.temperatures[row] : 1.0f;
+  const int k = a.top_ks ? a.top_ks[row] : -1;
+  const float p = a.top_ps ? a.top_ps[row] : 1.0f;
+  const float mp = a.min_ps ? a.min_ps[row] : 0.0f;
+  if (!(T >= kGreedyEps) || k == 0 || k == 1 || k < -1) return 4;
+  const bool kfin = k >= 2;
+  if (!kfin && p < 1.0f && !(mp > 0.0f)) return 0;
+  if ((!kfin && !(mp > 0.0f)) || k >= 512) return 1;
+  if (k >= 64 || (!kfin && p < 1.0f)) return 2;
+  return 3;
+}
+
+// One CTA per (row, slice), ahead of the sampler.
+//  * The slice's distinct penalised or biased token ids with their history count and the
+//    last bias entry (SGLang page, "Order semantics of the penalties" and "Why
+//    logit_bias is built from triples": the last duplicate wins), sorted by id, into the
+//    slice's scratch list.  Duplicate history ids are counted once per warp (Zipf-like
+//    histories repeat their frequent ids many times).  A slice with more than kPenCap
+//    distinct ids is flagged OVERFLOW.
+//  * The launch order of the sampler's rows, heaviest first: every slice-0 CTA writes
+//    its row's class; the last CTA to finish (a ticket counter) sorts the rows by class,
+//    stably, and resets the ticket.
+__global__ void __launch_bounds__(kPrepThreads) prep_kernel(const __grid_constant__ LaunchParams P) {
   __shared__ uint32_t hkey[kHashCap];
   __shared__ uint32_t hcnt[kHashCap];
   __shared__ int32_t hbias[kHashCap];
-  __shared__ float hval[kHashCap];
   __shared__ uint32_t mod[kMaxChunk / 32];
-  __shared__ int red[kWarps];
+  __shared__ uint16_t wbase[kMaxChunk / 32];
+  __shared__ int red[kPrepWarps * kClasses];
   __shared__ int csr[4];
-  __shared__ int flags_sh;
+  __shared__ int flags_sh, last_sh;
   const clsample_args_t& a = P.a;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int rc = (int)blockIdx.x;  // row * C + slice
-  const int row = rc / P.C, c0 = (rc % P.C) * P.chunk;
+  const int row = rc / P.C, slice = rc % P.C, c0 = slice * P.chunk;
   const int len = max(0, min(a.V, c0 + P.chunk) - c0);
   const int c1 = c0 + len;
   const bool has_hist = a.hist_offs != nullptr;
@@ -783,132 +828,160 @@ __global__ void __launch_bounds__(kThreads) penalty_kernel(const __grid_constant
     csr[2] = has_bias ? a.bias_offs[row] : 0;
     csr[3] = has_bias ? a.bias_offs[row + 1] : 0;
     flags_sh = 0;
+    if (slice == 0) P.row_class[row] = row_class(a, row);
   }
-  for (int i = tid; i < kHashCap; i += kThreads) {
-    hkey[i] = kEmpty;
-    hcnt[i] = 0u;
-    hbias[i] = -1;
+  if (has_hist || has_bias) {
+    for (int i = tid; i < kHashCap; i += kPrepThreads) {
+      hkey[i] = kEmpty;
+      hcnt[i] = 0u;
+      hbias[i] = -1;
+    }
+    for (int w = tid; w < P.chunk / 32; w += kPrepThreads) mod[w] = 0u;
   }
-  for (int w = tid; w < P.chunk / 32; w += kThreads) mod[w] = 0u;
   __syncthreads();
 
-  int flags = 0;
-  const int hlo = csr[0], hhi = csr[1], blo = csr[2], bhi = csr[3];
-  if (hlo < 0 || hhi < hlo || blo < 0 || bhi < blo) flags |= kFlagInvalid;
-  const bool hok = has_hist && hlo >= 0 && hhi >= hlo;
-  const bool bok = has_bias && blo >= 0 && bhi >= blo;
-  // this thread's first bias entry is fetched together with the history ids
-  const int bj0 = blo + tid;
-  int bid0 = INT_MIN;
-  float bval0 = 0.0f;
-  if (bok && bj0 < bhi) {
-    bid0 = __ldg(a.bias_ids + bj0);
-    bval0 = __ldg(a.bias_vals + bj0);
-  }
-  if (hok) {
-    for (int base = hlo; base < hhi; base += 16 * kThreads) {
-      int ids[16];
+  if (has_hist || has_bias) {
+    int flags = 0;
+    const int hlo = csr[0], hhi = csr[1], blo = csr[2], bhi = csr[3];
+    if (hlo < 0 || hhi < hlo || blo < 0 || bhi < blo) flags |= kFlagInvalid;
+    const bool hok = has_hist && hlo >= 0 && hhi >= hlo;
+    const bool bok = has_bias && blo >= 0 && bhi >= blo;
+    if (hok) {
+      for (int base = hlo; base < hhi; base += 16 * kPrepThreads) {
+        int ids[16];
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int j = base + u * kThreads + tid;
-        ids[u] = j < hhi ? __ldg(a.hist_ids + j) : INT_MIN;
-      }
+        for (int u = 0; u < 16; ++u) {
+          const int j = base + u * kPrepThreads + tid;
+          ids[u] = j < hhi ? __ldg(a.hist_ids + j) : INT_MIN;
+        }
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int id = ids[u];
-        if (id != INT_MIN && (id < 0 || id >= a.V)) flags |= kFlagInvalid;
-        const bool mine = id >= c0 && id < c1;
-        const uint32_t peers = __match_any_sync(0xffffffffu, mine ? id : -1);
-        if (mine && lane == __ffs(peers) - 1) flags |= count_id(hkey, hcnt, (uint32_t)(id - c0), (uint32_t)__popc(peers));
-      }
-    }
-  }
-  // bias: the largest entry index per id wins; its owner then stores the value
-  int myslot = -1;
-  if (bok) {
-    for (int j = bj0; j < bhi; j += kThreads) {
-      const int id = j == bj0 ? bid0 : __ldg(a.bias_ids + j);
-      const float b = j == bj0 ? bval0 : __ldg(a.bias_vals + j);
-      if (id < 0 || id >= a.V || b != b) {
-        flags |= kFlagInvalid;
-      } else if (id >= c0 && id < c1) {
-        const int slot = hash_insert(hkey, (uint32_t)(id - c0));
-        if (slot < 0) flags |= kFlagOverflow;
-        else atomicMax(&hbias[slot], j);
-        if (j == bj0) myslot = slot;
-      }
-    }
-  }
-  if (flags) atomicOr(&flags_sh, flags);
-  __syncthreads();
-  if (bok) {
-    for (int j = bj0; j < bhi; j += kThreads) {
-      if (j == bj0) {
-        if (myslot >= 0 && hbias[myslot] == j) hval[myslot] = bval0;
-      } else {
-        const int id = __ldg(a.bias_ids + j);
-        if (id >= c0 && id < c1) {
-          for (int i = 0; i < kHashCap; ++i)
-            if (hkey[i] == (uint32_t)(id - c0) && hbias[i] == j) hval[i] = __ldg(a.bias_vals + j);
+        for (int u = 0; u < 16; ++u) {
+          const int id = ids[u];
+          if (id != INT_MIN && (id < 0 || id >= a.V)) flags |= kFlagInvalid;
+          const bool mine = id >= c0 && id < c1;
+          const uint32_t peers = __match_any_sync(0xffffffffu, mine ? id : -1);
+          if (mine && lane == __ffs(peers) - 1)
+            flags |= count_id(hkey, hcnt, (uint32_t)(id - c0), (uint32_t)__popc(peers));
         }
       }
     }
+    // bias: the largest entry index per id wins (its value is read back at the end)
+    if (bok) {
+      for (int j = blo + tid; j < bhi; j += kPrepThreads) {
+        const int id = __ldg(a.bias_ids + j);
+        const float b = __ldg(a.bias_vals + j);
+        if (id < 0 || id >= a.V || b != b) {
+          flags |= kFlagInvalid;
+        } else if (id >= c0 && id < c1) {
+          const int slot = hash_insert(hkey, (uint32_t)(id - c0));
+          if (slot < 0) flags |= kFlagOverflow;
+          else atomicMax(&hbias[slot], j);
+        }
+      }
+    }
+    if (flags) atomicOr(&flags_sh, flags);
+    __syncthreads();
+    for (int i = tid; i < kHashCap; i += kPrepThreads) {
+      const uint32_t l = hkey[i];
+      if (l != kEmpty) atomicOr(&mod[l >> 5], 1u << (l & 31));
+    }
+    __syncthreads();
+    // rank of every id = ids below it: an exclusive scan of the words' popcounts
+    constexpr int kPer = (kMaxChunk / 32) / kPrepThreads;
+    const int nw = P.chunk / 32;
+    int cnt[kPer], loc = 0;
+#pragma unroll
+    for (int t = 0; t < kPer; ++t) {
+      const int w = tid * kPer + t;
+      cnt[t] = w < nw ? __popc(mod[w]) : 0;
+      loc += cnt[t];
+    }
+    int x = loc;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, x, d);
+      if (lane >= d) x += o;
+    }
+    if (lane == 31) red[warp] = x;
+    __syncthreads();
+    int total = 0, before = 0;
+    for (int w = 0; w < kPrepWarps; ++w) {
+      total += red[w];
+      if (w < warp) before += red[w];
+    }
+    int e = before + x - loc;
+#pragma unroll
+    for (int t = 0; t < kPer; ++t) {
+      const int w = tid * kPer + t;
+      if (w < nw) wbase[w] = (uint16_t)e;
+      e += cnt[t];
+    }
+    __syncthreads();
+    PenEntry* out = P.pen + (size_t)rc * kPenCap;
+    for (int i = tid; i < kHashCap; i += kPrepThreads) {
+      const uint32_t l = hkey[i];
+      if (l == kEmpty) continue;
+      const int r = wbase[l >> 5] + __popc(mod[l >> 5] & ((1u << (l & 31)) - 1u));
+      if (r >= kPenCap) continue;
+      PenEntry en;
+      const int bj = hbias[i];
+      en.id = l | (bj >= 0 ? kPenBias : 0u);
+      en.count = min(hcnt[i], kCountMask);
+      en.bias = bj >= 0 ? __ldg(a.bias_vals + bj) : 0.0f;
+      en.pad = 0u;
+      out[r] = en;
+    }
+    if (tid == 0) {
+      int f = flags_sh;
+      if (total > kPenCap) f |= kFlagOverflow;
+      P.pen_n[rc] = make_int2(min(total, kPenCap), f);
+    }
   }
-  for (int i = tid; i < kHashCap; i += kThreads) {
-    const uint32_t l = hkey[i];
-    if (l != kEmpty) atomicOr(&mod[l >> 5], 1u << (l & 31));
+
+  // the launch order, by the CTA that finishes last
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) last_sh = atomicAdd(P.ticket, 1u) == gridDim.x - 1 ? 1 : 0;
+  __syncthreads();
+  if (!last_sh) return;
+  __threadfence();
+  const int B = a.B;
+  const int per = (B + kPrepThreads - 1) / kPrepThreads;  // consecutive rows per thread
+  const int r0 = min(B, tid * per), r1 = min(B, r0 + per);
+  int cnt[kClasses] = {0, 0, 0, 0, 0};
+  for (int r = r0; r < r1; ++r) ++cnt[__ldcg(P.row_class + r)];
+  // exclusive scan over threads, per class; then class offsets
+  int base[kClasses];
+  int cls_total[kClasses];
+#pragma unroll
+  for (int c = 0; c < kClasses; ++c) {
+    int x = cnt[c];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, x, d);
+      if (lane >= d) x += o;
+    }
+    if (lane == 31) red[warp * kClasses + c] = x;
+    base[c] = x - cnt[c];
   }
   __syncthreads();
-  // rank of every id = ids below it: an exclusive scan of the words' popcounts
-  constexpr int kPer = (kMaxChunk / 32) / kThreads;
-  const int nw = P.chunk / 32;
-  int cnt[kPer], loc = 0;
 #pragma unroll
-  for (int t = 0; t < kPer; ++t) {
-    const int w = tid * kPer + t;
-    cnt[t] = w < nw ? __popc(mod[w]) : 0;
-    loc += cnt[t];
+  for (int c = 0; c < kClasses; ++c) {
+    int tot = 0;
+    for (int w = 0; w < kPrepWarps; ++w) {
+      if (w < warp) base[c] += red[w * kClasses + c];
+      tot += red[w * kClasses + c];
+    }
+    cls_total[c] = tot;
   }
-  int x = loc;
+  int start = 0;
 #pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const int o = __shfl_up_sync(0xffffffffu, x, d);
-    if (lane >= d) x += o;
+  for (int c = 0; c < kClasses; ++c) {
+    base[c] += start;
+    start += cls_total[c];
   }
-  if (lane == 31) red[warp] = x;
-  __syncthreads();
-  int total = 0;
-  for (int w = 0; w < kWarps; ++w) total += red[w];
-  int before = 0;
-  for (int w = 0; w < warp; ++w) before += red[w];
-  // prefix of each of this thread's words, kept in registers for the entries below
-  __shared__ int wbase[kMaxChunk / 32];
-  int e = before + x - loc;
-#pragma unroll
-  for (int t = 0; t < kPer; ++t) {
-    const int w = tid * kPer + t;
-    if (w < nw) wbase[w] = e;
-    e += cnt[t];
-  }
-  __syncthreads();
-  PenEntry* out = P.pen + (size_t)rc * kPenCap;
-  for (int i = tid; i < kHashCap; i += kThreads) {
-    const uint32_t l = hkey[i];
-    if (l == kEmpty) continue;
-    const int r = wbase[l >> 5] + __popc(mod[l >> 5] & ((1u << (l & 31)) - 1u));
-    if (r >= kPenCap) continue;
-    PenEntry en;
-    en.id = l | (hbias[i] >= 0 ? kPenBias : 0u);
-    en.count = min(hcnt[i], kCountMask);
-    en.bias = hbias[i] >= 0 ? hval[i] : 0.0f;
-    en.pad = 0u;
-    out[r] = en;
-  }
-  if (tid == 0) {
-    int f = flags_sh;
-    if (total > kPenCap) f |= kFlagOverflow;
-    P.pen_n[rc] = make_int2(min(total, kPenCap), f);
-  }
+  for (int r = r0; r < r1; ++r) P.row_order[base[__ldcg(P.row_class + r)]++] = r;
+  if (tid == 0) *P.ticket = 0u;  // ready for the next call on this stream
 }
 
 // ---------------------------------------------------------------- prologue
@@ -932,7 +1005,6 @@ __device__ __noinline__ void prologue(const LaunchParams& P) {
   if (tid == 0) {
     sh.flags = 0;
     sh.count = 0;
-    sh.pre = -1;
     sh.nallowed = 0;
     for (int i = 0; i < kStages; ++i) mbar_init(&sh.full[i], 1);
     fence_mbar_init();
@@ -978,7 +1050,7 @@ __device__ __noinline__ void prologue(const LaunchParams& P) {
     S.live[w] = word;
     S.mod[w] = 0u;
   }
-  if (tid < 128) S.mrg_c[tid] = 0u;  // the top-p route's merged bins (peers add into them)
+  S.mrg_c[tid] = 0u;  // merged histograms peers add into (top-p bins, top-k refinement)
   __syncthreads();
   if (!has_mod) {
     int na = 0;
@@ -1321,7 +1393,7 @@ __device__ __noinline__ bool finish_early(const LaunchParams& P) {
   if (status == kRowOk && !greedy) return false;
   if (threadIdx.x == 0 && cg::this_cluster().block_rank() == 0) {
     const clsample_args_t& a = P.a;
-    const int row = (int)(blockIdx.x / (unsigned)P.C);
+    const int row = cluster_row(P);
     const bool ok = status == kRowOk;
     a.tokens[row] = ok ? sh.rs.arg : -1;
     if (a.logprobs) a.logprobs[row] = ok ? -sh.rs.lnS : -INFINITY;
@@ -1418,7 +1490,7 @@ __device__ const Cand* collect_at_leader(const LaunchParams& P, const Smem& S, i
   if (cluster.block_rank() != 0) return nullptr;
   const int tid = threadIdx.x;
   const int C = P.C;
-  const int row = (int)(blockIdx.x / (unsigned)C);
+  const int row = cluster_row(P);
   Cand* seg = P.cand + (size_t)row * C * kCandCap;
   int ntot = 0;
   for (int c = 0; c < C; ++c) ntot += sh.x2[c].count;
@@ -1612,6 +1684,73 @@ __device__ __noinline__ Race leader_race(const Cand* G, int n, float cut, unsign
 
 // ---------------------------------------------------------------- routes
 
+// A top-k row whose candidates exceed the leader's shared area: a cluster-wide histogram
+// of the candidates' y over 256 equal buckets of [lo, 0] (pushed with DSMEM atomics into
+// every CTA's merged copy, zeroed by the prologue) fixes the bucket where the count from
+// the top first reaches k; every CTA then keeps, in place, only its candidates in that
+// bucket or above (an upper set that still holds the top-k set) and the counts are
+// exchanged again.
+__device__ __noinline__ void refine_topk(const LaunchParams& P, const Smem& S, Cand* mycand, float lo, int k) {
+  const cg::cluster_group cluster = cg::this_cluster();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int C = P.C, rank = (int)cluster.block_rank();
+  const int cnt = min(sh.x2[rank].count, kCandCap);
+  const float scale = 256.0f / -lo;
+  auto bucket = [&](float y) -> int {
+    const int b = __float2int_rz(__fmul_rn(-y, scale));
+    return b < 0 ? 0 : (b > 255 ? 255 : b);
+  };
+  S.hist_c[tid] = 0u;
+  __syncthreads();
+  Cand mine[kCandCap / kThreads];
+#pragma unroll
+  for (int t = 0; t < kCandCap / kThreads; ++t) {
+    const int i = t * kThreads + tid;
+    if (i < cnt) {
+      mine[t] = mycand[i];
+      atomicAdd(&S.hist_c[bucket(mine[t].y)], 1u);
+    }
+  }
+  __syncthreads();
+  {
+    const uint32_t v = S.hist_c[tid];
+    if (v)
+      for (int r = 0; r < C; ++r) atomicAdd(cluster.map_shared_rank(S.mrg_c + tid, (unsigned)r), v);
+  }
+  cluster.sync();
+  // the bucket where the running count from the top (bucket 0) first reaches k
+  {
+    const uint32_t v = S.mrg_c[tid];
+    uint32_t x = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const uint32_t o = __shfl_up_sync(0xffffffffu, x, d);
+      if (lane >= d) x += o;
+    }
+    if (lane == 31) sh.red_i[warp] = (int)x;
+    if (tid == 0) sh.bstar = 255;
+    __syncthreads();
+    uint32_t before = 0;
+    for (int w = 0; w < warp; ++w) before += (uint32_t)sh.red_i[w];
+    if (before + x >= (uint32_t)k && before + x - v < (uint32_t)k) sh.bstar = tid;
+  }
+  __syncthreads();
+  const int bstar = sh.bstar;
+  if (tid == 0) sh.count = 0;
+  __syncthreads();
+#pragma unroll
+  for (int t = 0; t < kCandCap / kThreads; ++t) {
+    const int i = t * kThreads + tid;
+    if (i < cnt && bucket(mine[t].y) <= bstar) mycand[atomicAdd(&sh.count, 1)] = mine[t];
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) sh.x2_mine.count = sh.count;
+  __syncthreads();
+  push_all(cluster, sh.x2, &sh.x2_mine, rank, C);
+  cluster.sync();
+}
+
 // Rows with a provable bound (top-k, min-p) and untruncated rows.  Pass B compacts the
 // tokens at z >= zth (the exact z-space image of the y bound) and/or races every token;
 // the leader finishes top-k -> top-p -> min-p and the race over the gathered candidates.
@@ -1722,6 +1861,11 @@ __device__ __noinline__ bool route_fast(const LaunchParams& P, int& pass) {
     return true;
   }
   if (fl & kFlagOverflow) return false;
+  {
+    int n = 0;
+    for (int c = 0; c < C; ++c) n += sh.x2[c].count;
+    if (kfin && n > kGatherCap && theta > -INFINITY && theta < 0.0f) refine_topk(P, S, mycand, theta, q.k);
+  }
   int ntot = 0;
   const Cand* G = collect_at_leader(P, S, &ntot);
   if (!G) return true;
@@ -2155,12 +2299,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) sampler_kernel(const __g
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   prologue<kBF16>(P);
   pass_a<kBF16>(P);
-  ring_prefetch_pass<kBF16>(P, 1);
   exchange1(P);
-  if (finish_early(P)) {
-    ring_drain<kBF16>(P);
-    return;
-  }
+  if (finish_early(P)) return;
   plan_row(P);
   int pass = 1;
   const int plan = sh.rs.plan;
@@ -2217,6 +2357,7 @@ struct clsample_handle {
   PenEntry* pen;  // penalised-token lists, [max_batch * C][kPenCap]
   int2* pen_n;    // their lengths and flags, [max_batch * C]
   Cand* cand;     // compacted candidates, [max_batch * C][kCandCap]
+  int* rows;      // row classes and launch order, [2 * max_batch], then the ticket
 };
 
 extern "C" {
@@ -2267,13 +2408,18 @@ int clsample_create(int32_t max_batch, int32_t vocab, clsample_t** out) {
   PenEntry* pen = nullptr;
   int2* pen_n = nullptr;
   Cand* cand = nullptr;
+  int* rows = nullptr;
   if (max_batch > 0) {
     const size_t lists = (size_t)max_batch * (size_t)g.C;
     if (cudaMalloc(&pen, lists * kPenCap * sizeof(PenEntry)) != cudaSuccess ||
         cudaMalloc(&pen_n, lists * sizeof(int2)) != cudaSuccess ||
-        cudaMalloc(&cand, lists * kCandCap * sizeof(Cand)) != cudaSuccess) {
+        cudaMalloc(&cand, lists * kCandCap * sizeof(Cand)) != cudaSuccess ||
+        cudaMalloc(&rows, (2 * (size_t)max_batch + 1) * sizeof(int)) != cudaSuccess ||
+        cudaMemset(rows, 0, (2 * (size_t)max_batch + 1) * sizeof(int)) != cudaSuccess) {
       if (pen) cudaFree(pen);
       if (pen_n) cudaFree(pen_n);
+      if (cand) cudaFree(cand);
+      if (rows) cudaFree(rows);
       return CLSAMPLE_ERR_CUDA;
     }
   }
@@ -2285,6 +2431,7 @@ int clsample_create(int32_t max_batch, int32_t vocab, clsample_t** out) {
   h->pen = pen;
   h->pen_n = pen_n;
   h->cand = cand;
+  h->rows = rows;
   *out = h;
   return CLSAMPLE_SUCCESS;
 }
@@ -2294,6 +2441,7 @@ void clsample_destroy(clsample_t* h) {
   if (h->pen) cudaFree(h->pen);
   if (h->pen_n) cudaFree(h->pen_n);
   if (h->cand) cudaFree(h->cand);
+  if (h->rows) cudaFree(h->rows);
   delete h;
 }
 
@@ -2340,12 +2488,13 @@ int clsample_apply(clsample_t* h, const clsample_args_t* a, clsample_stream_t st
   P.pen = h->pen;
   P.pen_n = h->pen_n;
   P.cand = h->cand;
+  P.row_class = h->rows;
+  P.row_order = h->rows + h->max_batch;
+  P.ticket = reinterpret_cast<unsigned*>(h->rows + 2 * (size_t)h->max_batch);
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (a->hist_offs || a->bias_offs) {
-    penalty_kernel<<<(unsigned)(a->B * g.C), kThreads, 0, st>>>(P);
-    if (cudaGetLastError() != cudaSuccess) return CLSAMPLE_ERR_CUDA;
-  }
+  prep_kernel<<<(unsigned)(a->B * g.C), kPrepThreads, 0, st>>>(P);
+  if (cudaGetLastError() != cudaSuccess) return CLSAMPLE_ERR_CUDA;
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
   fill_launch(g, (unsigned)a->B, st, &cfg, attr);

@@ -26,11 +26,13 @@
  *      log-softmax (SGLang page, section "Numerical consistency of logprobs").
  *
  * Threading and ownership.  A handle is bound to the CUDA device that was current at
- * clsample_create and holds no device memory.  Every array in clsample_args_t is a
- * DEVICE pointer owned by the caller; it must stay valid until the work enqueued on
- * the stream has finished.  The logits are read-only (never written in place).  Calls
- * on one handle from several host threads are safe; calls on different streams may
- * overlap freely (the kernels keep no state between calls).
+ * clsample_create and owns device scratch sized for max_batch rows (the penalised-token
+ * lists, the compacted candidates and the rows' launch order; about 320 KB per row for
+ * V = 151936).  Every array in clsample_args_t is a DEVICE pointer owned by the caller;
+ * it must stay valid until the work enqueued on the stream has finished.  The logits
+ * are read-only (never written in place).  Calls on one handle must be ordered (one
+ * stream, or streams joined by events): they share the handle's scratch.  Separate
+ * handles are independent.
  *
  * Errors.  Every entry point validates its arguments on the host, without any device
  * synchronisation, and returns a negative CLSAMPLE_ERR_* code on a bad argument;
@@ -141,16 +143,18 @@ typedef struct {
 } clsample_args_t;
 
 /* Creates a handle for batches of up to max_batch rows over a vocabulary of `vocab`
- * tokens on the current CUDA device.  Sets the kernels' shared-memory and cluster
- * attributes; allocates no device memory.  Returns CLSAMPLE_SUCCESS and *out, or a
- * negative code (*out = NULL). */
+ * tokens on the current CUDA device.  Sets the kernels' shared-memory attributes and
+ * allocates the handle's device scratch (cudaMalloc; freed by clsample_destroy).
+ * Returns CLSAMPLE_SUCCESS and *out, or a negative code (*out = NULL; nothing kept). */
 int clsample_create(int32_t max_batch, int32_t vocab, clsample_t** out);
 
-/* Releases a handle (NULL is ignored).  Does not synchronise. */
+/* Releases a handle and its scratch (NULL is ignored).  cudaFree synchronises the
+ * device, so no call on the handle may still be running. */
 void clsample_destroy(clsample_t* handle);
 
-/* Enqueues one sampler call on `stream` (one kernel launch; nothing when B == 0).
- * Returns after enqueueing; results are valid once the stream reaches this point. */
+/* Enqueues one sampler call on `stream`: a row-preparation kernel (penalised-token
+ * lists, launch order) and the sampler kernel; nothing when B == 0.  Returns after
+ * enqueueing; results are valid once the stream reaches this point. */
 int clsample_apply(clsample_t* handle, const clsample_args_t* args, clsample_stream_t stream);
 
 /* Static description of a return code. */

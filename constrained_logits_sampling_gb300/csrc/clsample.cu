@@ -2460,7 +2460,12 @@ static void fill_launch(const Geometry& g, unsigned nclusters, cudaStream_t stre
   cfg->numAttrs = 1;
 }
 
-int clsample_apply(clsample_t* h, const clsample_args_t* a, clsample_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Validates a call against the handle and fills the launch parameters (host only).
+int make_params(const clsample_t* h, const clsample_args_t* a, LaunchParams* P) {
   if (!h || !a) return CLSAMPLE_ERR_NULL;
   if (a->B < 0 || a->B > h->max_batch) return CLSAMPLE_ERR_BATCH;
   if (a->V != h->vocab) return CLSAMPLE_ERR_VOCAB;
@@ -2474,33 +2479,63 @@ int clsample_apply(clsample_t* h, const clsample_args_t* a, clsample_stream_t st
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return CLSAMPLE_ERR_CUDA;
   if (dev != h->device) return CLSAMPLE_ERR_DEVICE;
-
   const bool bf16 = a->logits_dtype == CLSAMPLE_LOGITS_BF16;
   const Geometry& g = h->g;
   const int esize = bf16 ? 2 : 4;
-  LaunchParams P;
-  P.a = *a;
-  P.C = g.C;
-  P.chunk = g.chunk;
-  P.cap = g.cap;
+  P->a = *a;
+  P->C = g.C;
+  P->chunk = g.chunk;
+  P->cap = g.cap;
   const uintptr_t base = reinterpret_cast<uintptr_t>(a->logits);
-  P.vec_ok = (base % 16 == 0) && (((long long)a->logits_row_stride * esize) % 16 == 0);
-  P.pen = h->pen;
-  P.pen_n = h->pen_n;
-  P.cand = h->cand;
-  P.row_class = h->rows;
-  P.row_order = h->rows + h->max_batch;
-  P.ticket = reinterpret_cast<unsigned*>(h->rows + 2 * (size_t)h->max_batch);
+  P->vec_ok = (base % 16 == 0) && (((long long)a->logits_row_stride * esize) % 16 == 0);
+  P->pen = h->pen;
+  P->pen_n = h->pen_n;
+  P->cand = h->cand;
+  P->row_class = h->rows;
+  P->row_order = h->rows + h->max_batch;
+  P->ticket = reinterpret_cast<unsigned*>(h->rows + 2 * (size_t)h->max_batch);
+  return CLSAMPLE_SUCCESS;
+}
 
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  prep_kernel<<<(unsigned)(a->B * g.C), kPrepThreads, 0, st>>>(P);
-  if (cudaGetLastError() != cudaSuccess) return CLSAMPLE_ERR_CUDA;
+int launch_prep(const LaunchParams& P, cudaStream_t st) {
+  prep_kernel<<<(unsigned)(P.a.B * P.C), kPrepThreads, 0, st>>>(P);
+  return cudaGetLastError() == cudaSuccess ? CLSAMPLE_SUCCESS : CLSAMPLE_ERR_CUDA;
+}
+
+int launch_sampler(const Geometry& g, const LaunchParams& P, cudaStream_t st) {
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
-  fill_launch(g, (unsigned)a->B, st, &cfg, attr);
-  const cudaError_t err = bf16 ? cudaLaunchKernelEx(&cfg, sampler_kernel<true>, P)
-                               : cudaLaunchKernelEx(&cfg, sampler_kernel<false>, P);
+  fill_launch(g, (unsigned)P.a.B, st, &cfg, attr);
+  const cudaError_t err = P.a.logits_dtype == CLSAMPLE_LOGITS_BF16 ? cudaLaunchKernelEx(&cfg, sampler_kernel<true>, P)
+                                                                    : cudaLaunchKernelEx(&cfg, sampler_kernel<false>, P);
   return err == cudaSuccess ? CLSAMPLE_SUCCESS : CLSAMPLE_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int clsample_apply(clsample_t* h, const clsample_args_t* a, clsample_stream_t stream) {
+  LaunchParams P;
+  const int rc = make_params(h, a, &P);
+  if (rc != CLSAMPLE_SUCCESS || a->B == 0) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int rp = launch_prep(P, st);
+  return rp != CLSAMPLE_SUCCESS ? rp : launch_sampler(h->g, P, st);
+}
+
+int clsample_prepare(clsample_t* h, const clsample_args_t* a, clsample_stream_t stream) {
+  LaunchParams P;
+  const int rc = make_params(h, a, &P);
+  if (rc != CLSAMPLE_SUCCESS || a->B == 0) return rc;
+  return launch_prep(P, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int clsample_sample(clsample_t* h, const clsample_args_t* a, clsample_stream_t stream) {
+  LaunchParams P;
+  const int rc = make_params(h, a, &P);
+  if (rc != CLSAMPLE_SUCCESS || a->B == 0) return rc;
+  return launch_sampler(h->g, P, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int clsample_occupancy(clsample_t* h, int32_t logits_dtype, int32_t* max_active_clusters) {

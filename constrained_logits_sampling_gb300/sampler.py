@@ -41,8 +41,9 @@ class Args(ctypes.Structure):
     ]
 
 
-EXPORTS = ("clsample_create", "clsample_destroy", "clsample_apply", "clsample_strerror",
-           "clsample_geometry", "clsample_occupancy", "clsample_debug_weights", "clsample_debug_uniforms")
+EXPORTS = ("clsample_create", "clsample_destroy", "clsample_apply", "clsample_prepare", "clsample_sample",
+           "clsample_strerror", "clsample_geometry", "clsample_occupancy", "clsample_debug_weights",
+           "clsample_debug_uniforms")
 
 
 def load_library(path: str = LIB_PATH):
@@ -58,8 +59,9 @@ def load_library(path: str = LIB_PATH):
             L.clsample_create.restype = ctypes.c_int
             L.clsample_destroy.argtypes = [ctypes.c_void_p]
             L.clsample_destroy.restype = None
-            L.clsample_apply.argtypes = [ctypes.c_void_p, ctypes.POINTER(Args), ctypes.c_void_p]
-            L.clsample_apply.restype = ctypes.c_int
+            for name in ("clsample_apply", "clsample_prepare", "clsample_sample"):
+                getattr(L, name).argtypes = [ctypes.c_void_p, ctypes.POINTER(Args), ctypes.c_void_p]
+                getattr(L, name).restype = ctypes.c_int
             L.clsample_strerror.argtypes = [ctypes.c_int]
             L.clsample_strerror.restype = ctypes.c_char_p
             L.clsample_geometry.argtypes = [ctypes.c_int32, ctypes.POINTER(ctypes.c_int32),
@@ -201,6 +203,15 @@ class Sampler:
     def apply(self, args: Args, stream: Optional[torch.cuda.Stream] = None):
         """Enqueue one call (``clsample_apply``) on ``stream`` (default: current)."""
         _check(self._L.clsample_apply(self._h, ctypes.byref(args), _stream_ptr(stream)))
+
+    def prepare(self, args: Args, stream: Optional[torch.cuda.Stream] = None):
+        """Enqueue the row-preparation half of a call (``clsample_prepare``)."""
+        _check(self._L.clsample_prepare(self._h, ctypes.byref(args), _stream_ptr(stream)))
+
+    def sample(self, args: Args, stream: Optional[torch.cuda.Stream] = None):
+        """Enqueue the sampler half of a call (``clsample_sample``); reads what the
+        last ``prepare`` on this handle wrote."""
+        _check(self._L.clsample_sample(self._h, ctypes.byref(args), _stream_ptr(stream)))
 
     def __call__(self, logits: torch.Tensor, *, debug: bool = False, stream=None,
                  **kw) -> Dict[str, torch.Tensor]:

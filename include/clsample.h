@@ -157,6 +157,14 @@ void clsample_destroy(clsample_t* handle);
  * enqueueing; results are valid once the stream reaches this point. */
 int clsample_apply(clsample_t* handle, const clsample_args_t* args, clsample_stream_t stream);
 
+/* The two halves of clsample_apply, for callers that schedule or time them apart:
+ * clsample_prepare enqueues the row-preparation kernel, clsample_sample the sampler
+ * kernel, which reads what the last clsample_prepare on this handle wrote.  The pair,
+ * with the same arguments on one stream, equals clsample_apply.  Same validation and
+ * return codes. */
+int clsample_prepare(clsample_t* handle, const clsample_args_t* args, clsample_stream_t stream);
+int clsample_sample(clsample_t* handle, const clsample_args_t* args, clsample_stream_t stream);
+
 /* Static description of a return code. */
 const char* clsample_strerror(int code);
 

@@ -35,6 +35,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "clsample.h"
 #include "cluster_sync.cuh"
@@ -2349,16 +2350,85 @@ Geometry geometry_for(int vocab) {
 
 }  // namespace
 
-struct clsample_handle {
+namespace {
+
+// Device scratch of one call: sized for max_batch rows of up to kMaxCluster slices.
+struct Scratch {
   int max_batch;
-  int vocab;
-  int device;
-  Geometry g;
   PenEntry* pen;  // penalised-token lists, [max_batch * C][kPenCap]
   int2* pen_n;    // their lengths and flags, [max_batch * C]
   Cand* cand;     // compacted candidates, [max_batch * C][kCandCap]
   int* rows;      // row classes and launch order, [2 * max_batch], then the ticket
 };
+
+// Checks the device (compute capability 10.3, enough shared memory) and raises the
+// kernels' dynamic shared-memory limit to what the longest slice needs.
+int setup_device(int dev) {
+  int major = 0, minor = 0, optin = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    return CLSAMPLE_ERR_CUDA;
+  if (major != 10 || minor != 3) return CLSAMPLE_ERR_DEVICE;
+  const int smem = (int)layout_for(kMaxChunk).total;
+  if (smem > optin) return CLSAMPLE_ERR_DEVICE;
+  const void* k32 = reinterpret_cast<const void*>(&sampler_kernel<false>);
+  const void* k16 = reinterpret_cast<const void*>(&sampler_kernel<true>);
+  if (cudaFuncSetAttribute(k32, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+      cudaFuncSetAttribute(k16, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return CLSAMPLE_ERR_CUDA;
+  return CLSAMPLE_SUCCESS;
+}
+
+}  // namespace
+
+struct clsample_handle {
+  int max_batch;
+  int vocab;
+  int device;
+  Geometry g;
+  Scratch sc;
+};
+
+namespace {
+
+// Scratch of clsample_apply_static: a fixed device array compiled into the library
+// (zero at load, so the preparation kernel's ticket starts at 0), for kStaticRows rows.
+constexpr int kStaticRows = 64;
+constexpr size_t kStaticLists = (size_t)kStaticRows * kMaxCluster;
+constexpr size_t kStaticOffPenN = align_up(kStaticLists * kPenCap * sizeof(PenEntry), 256);
+constexpr size_t kStaticOffCand = kStaticOffPenN + align_up(kStaticLists * sizeof(int2), 256);
+constexpr size_t kStaticOffRows = kStaticOffCand + align_up(kStaticLists * kCandCap * sizeof(Cand), 256);
+constexpr size_t kStaticBytes = kStaticOffRows + align_up((2 * (size_t)kStaticRows + 1) * sizeof(int), 256);
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mutex;
+unsigned char* g_static_base[kMaxDevices];  // the array's address on each device, once set up
+
+// The static scratch of device `dev` (its address taken and the kernels set up once per
+// device); nullptr with *rc set on failure.
+unsigned char* static_scratch(int dev, int* rc) {
+  if (dev < 0 || dev >= kMaxDevices) {
+    *rc = CLSAMPLE_ERR_DEVICE;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_static_mutex);
+  if (!g_static_base[dev]) {
+    *rc = setup_device(dev);
+    if (*rc != CLSAMPLE_SUCCESS) return nullptr;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) {
+      *rc = CLSAMPLE_ERR_CUDA;
+      return nullptr;
+    }
+    g_static_base[dev] = static_cast<unsigned char*>(p);
+  }
+  *rc = CLSAMPLE_SUCCESS;
+  return g_static_base[dev];
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -2393,18 +2463,8 @@ int clsample_create(int32_t max_batch, int32_t vocab, clsample_t** out) {
   if (g.C == 0) return CLSAMPLE_ERR_VOCAB;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return CLSAMPLE_ERR_CUDA;
-  int major = 0, minor = 0, optin = 0;
-  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
-    return CLSAMPLE_ERR_CUDA;
-  if (major != 10 || minor != 3) return CLSAMPLE_ERR_DEVICE;
-  if (g.smem > optin) return CLSAMPLE_ERR_DEVICE;
-  const void* k32 = reinterpret_cast<const void*>(&sampler_kernel<false>);
-  const void* k16 = reinterpret_cast<const void*>(&sampler_kernel<true>);
-  if (cudaFuncSetAttribute(k32, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem) != cudaSuccess ||
-      cudaFuncSetAttribute(k16, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem) != cudaSuccess)
-    return CLSAMPLE_ERR_CUDA;
+  const int rc = setup_device(dev);
+  if (rc != CLSAMPLE_SUCCESS) return rc;
   PenEntry* pen = nullptr;
   int2* pen_n = nullptr;
   Cand* cand = nullptr;
@@ -2428,20 +2488,17 @@ int clsample_create(int32_t max_batch, int32_t vocab, clsample_t** out) {
   h->vocab = vocab;
   h->device = dev;
   h->g = g;
-  h->pen = pen;
-  h->pen_n = pen_n;
-  h->cand = cand;
-  h->rows = rows;
+  h->sc = Scratch{max_batch, pen, pen_n, cand, rows};
   *out = h;
   return CLSAMPLE_SUCCESS;
 }
 
 void clsample_destroy(clsample_t* h) {
   if (!h) return;
-  if (h->pen) cudaFree(h->pen);
-  if (h->pen_n) cudaFree(h->pen_n);
-  if (h->cand) cudaFree(h->cand);
-  if (h->rows) cudaFree(h->rows);
+  if (h->sc.pen) cudaFree(h->sc.pen);
+  if (h->sc.pen_n) cudaFree(h->sc.pen_n);
+  if (h->sc.cand) cudaFree(h->sc.cand);
+  if (h->sc.rows) cudaFree(h->sc.rows);
   delete h;
 }
 
@@ -2464,11 +2521,13 @@ static void fill_launch(const Geometry& g, unsigned nclusters, cudaStream_t stre
 
 namespace {
 
-// Validates a call against the handle and fills the launch parameters (host only).
-int make_params(const clsample_t* h, const clsample_args_t* a, LaunchParams* P) {
-  if (!h || !a) return CLSAMPLE_ERR_NULL;
-  if (a->B < 0 || a->B > h->max_batch) return CLSAMPLE_ERR_BATCH;
-  if (a->V != h->vocab) return CLSAMPLE_ERR_VOCAB;
+// Validates a call and fills the launch parameters (host only): the vocabulary must be
+// `vocab`, the batch at most the scratch's rows, and `dev` the current device.
+int make_params(const Geometry& g, int vocab, int dev, const Scratch& sc, const clsample_args_t* a,
+                LaunchParams* P) {
+  if (!a) return CLSAMPLE_ERR_NULL;
+  if (a->B < 0 || a->B > sc.max_batch) return CLSAMPLE_ERR_BATCH;
+  if (a->V != vocab) return CLSAMPLE_ERR_VOCAB;
   if (a->logits_dtype != CLSAMPLE_LOGITS_F32 && a->logits_dtype != CLSAMPLE_LOGITS_BF16) return CLSAMPLE_ERR_DTYPE;
   if (a->B == 0) return CLSAMPLE_SUCCESS;
   if (!a->logits || !a->tokens) return CLSAMPLE_ERR_NULL;
@@ -2476,11 +2535,10 @@ int make_params(const clsample_t* h, const clsample_args_t* a, LaunchParams* P) 
   if (a->bias_offs && (!a->bias_ids || !a->bias_vals)) return CLSAMPLE_ERR_NULL;
   if (a->logits_row_stride < a->V) return CLSAMPLE_ERR_STRIDE;
   if (a->bitmask && a->bitmask_row_stride < (a->V + 31) / 32) return CLSAMPLE_ERR_STRIDE;
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return CLSAMPLE_ERR_CUDA;
-  if (dev != h->device) return CLSAMPLE_ERR_DEVICE;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return CLSAMPLE_ERR_CUDA;
+  if (cur != dev) return CLSAMPLE_ERR_DEVICE;
   const bool bf16 = a->logits_dtype == CLSAMPLE_LOGITS_BF16;
-  const Geometry& g = h->g;
   const int esize = bf16 ? 2 : 4;
   P->a = *a;
   P->C = g.C;
@@ -2488,13 +2546,18 @@ int make_params(const clsample_t* h, const clsample_args_t* a, LaunchParams* P) 
   P->cap = g.cap;
   const uintptr_t base = reinterpret_cast<uintptr_t>(a->logits);
   P->vec_ok = (base % 16 == 0) && (((long long)a->logits_row_stride * esize) % 16 == 0);
-  P->pen = h->pen;
-  P->pen_n = h->pen_n;
-  P->cand = h->cand;
-  P->row_class = h->rows;
-  P->row_order = h->rows + h->max_batch;
-  P->ticket = reinterpret_cast<unsigned*>(h->rows + 2 * (size_t)h->max_batch);
+  P->pen = sc.pen;
+  P->pen_n = sc.pen_n;
+  P->cand = sc.cand;
+  P->row_class = sc.rows;
+  P->row_order = sc.rows + sc.max_batch;
+  P->ticket = reinterpret_cast<unsigned*>(sc.rows + 2 * (size_t)sc.max_batch);
   return CLSAMPLE_SUCCESS;
+}
+
+int make_params(const clsample_t* h, const clsample_args_t* a, LaunchParams* P) {
+  if (!h) return CLSAMPLE_ERR_NULL;
+  return make_params(h->g, h->vocab, h->device, h->sc, a, P);
 }
 
 int launch_prep(const LaunchParams& P, cudaStream_t st) {
@@ -2536,6 +2599,26 @@ int clsample_sample(clsample_t* h, const clsample_args_t* a, clsample_stream_t s
   const int rc = make_params(h, a, &P);
   if (rc != CLSAMPLE_SUCCESS || a->B == 0) return rc;
   return launch_sampler(h->g, P, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int clsample_apply_static(const clsample_args_t* a, clsample_stream_t stream) {
+  if (!a) return CLSAMPLE_ERR_NULL;
+  const Geometry g = geometry_for(a->V);
+  if (g.C == 0) return CLSAMPLE_ERR_VOCAB;
+  if (a->B < 0 || a->B > kStaticRows) return CLSAMPLE_ERR_BATCH;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CLSAMPLE_ERR_CUDA;
+  int rc = CLSAMPLE_SUCCESS;
+  unsigned char* base = static_scratch(dev, &rc);
+  if (!base) return rc;
+  const Scratch sc{kStaticRows, reinterpret_cast<PenEntry*>(base), reinterpret_cast<int2*>(base + kStaticOffPenN),
+                   reinterpret_cast<Cand*>(base + kStaticOffCand), reinterpret_cast<int*>(base + kStaticOffRows)};
+  LaunchParams P;
+  rc = make_params(g, a->V, dev, sc, a, &P);
+  if (rc != CLSAMPLE_SUCCESS || a->B == 0) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  rc = launch_prep(P, st);
+  return rc != CLSAMPLE_SUCCESS ? rc : launch_sampler(g, P, st);
 }
 
 int clsample_occupancy(clsample_t* h, int32_t logits_dtype, int32_t* max_active_clusters) {

@@ -42,8 +42,8 @@ class Args(ctypes.Structure):
 
 
 EXPORTS = ("clsample_create", "clsample_destroy", "clsample_apply", "clsample_prepare", "clsample_sample",
-           "clsample_strerror", "clsample_geometry", "clsample_occupancy", "clsample_debug_weights",
-           "clsample_debug_uniforms")
+           "clsample_apply_static", "clsample_strerror", "clsample_geometry", "clsample_occupancy",
+           "clsample_debug_weights", "clsample_debug_uniforms")
 
 
 def load_library(path: str = LIB_PATH):
@@ -62,6 +62,8 @@ def load_library(path: str = LIB_PATH):
             for name in ("clsample_apply", "clsample_prepare", "clsample_sample"):
                 getattr(L, name).argtypes = [ctypes.c_void_p, ctypes.POINTER(Args), ctypes.c_void_p]
                 getattr(L, name).restype = ctypes.c_int
+            L.clsample_apply_static.argtypes = [ctypes.POINTER(Args), ctypes.c_void_p]
+            L.clsample_apply_static.restype = ctypes.c_int
             L.clsample_strerror.argtypes = [ctypes.c_int]
             L.clsample_strerror.restype = ctypes.c_char_p
             L.clsample_geometry.argtypes = [ctypes.c_int32, ctypes.POINTER(ctypes.c_int32),
@@ -234,6 +236,12 @@ class Sampler:
                               dbg_kept_count=out.get("kept_count"), dbg_cut=out.get("cut"), **kw)
         self.apply(args, stream)
         return out
+
+
+def apply_static(args: Args, stream: Optional[torch.cuda.Stream] = None):
+    """One call through ``clsample_apply_static`` (no handle, no allocation; at most 64
+    rows; calls on one device must be ordered)."""
+    _check(load_library().clsample_apply_static(ctypes.byref(args), _stream_ptr(stream)))
 
 
 def debug_weights(y: torch.Tensor) -> torch.Tensor:

@@ -165,6 +165,20 @@ int clsample_apply(clsample_t* handle, const clsample_args_t* args, clsample_str
 int clsample_prepare(clsample_t* handle, const clsample_args_t* args, clsample_stream_t stream);
 int clsample_sample(clsample_t* handle, const clsample_args_t* args, clsample_stream_t stream);
 
+/* One sampler call without a handle that allocates nothing.  The pages have no
+ * counterpart: this is a deployment convenience of this library, and it samples
+ * exactly like clsample_apply.  Its scratch is one fixed device array compiled into
+ * the library (about 21 MB, zero when the library loads); no cudaMalloc or cudaFree
+ * ever happens.  The first call on a device looks up the array's address on that
+ * device (cudaGetSymbolAddress) and sets the kernels' shared-memory limit, once per
+ * device, under a host lock.  Limits: B <= 64 (else CLSAMPLE_ERR_BATCH) and
+ * V <= 262144 (else CLSAMPLE_ERR_VOCAB); nothing is enqueued on an error.
+ * Races: every call on a device, from any host thread or stream, uses the same array,
+ * so calls of this entry point on one device must be ordered (one stream, or streams
+ * joined by events); two overlapping calls corrupt each other's lists and candidates.
+ * Calls through handles are unaffected, and each process has its own array. */
+int clsample_apply_static(const clsample_args_t* args, clsample_stream_t stream);
+
 /* Static description of a return code. */
 const char* clsample_strerror(int code);
 

@@ -1,33 +1,38 @@
 // Batched constrained logits sampler for GB300 (sm_103a).
 //
-// One thread-block cluster samples one row.  The row's V logits are split into C
-// contiguous slices (a multiple of 32 tokens, so that every CTA owns whole bitmask
-// words), one per CTA.  A CTA keeps only small tables in shared memory (about 51 KB), so
-// four CTAs share an SM and about 76 rows are in flight at once.  Logits move only
-// through the TMA unit: every pass over the slice streams it through a 4-stage ring of
-// 4 KB shared-memory buffers filled by bulk copies (cp.async.bulk) that complete on
-// mbarriers, so the SM's load/store queues stay free for shared-memory work, shuffles and
-// DSMEM.  The first pass reads HBM; later passes find the slice in L2.  Nothing but the
-// per-row outputs is written back.
+// A row's V logits are split into C slices of `chunk` tokens (a multiple of 32, so a
+// slice owns whole bitmask words).  The sampler is one persistent kernel: every CTA
+// (four per SM) takes work items from a global list, in order, with an atomic counter,
+// and no CTA ever waits for another one's work except where the list says so.
 //
-//   pass A    sanitise + mask + penalties/bias (the few penalised tokens live in a small
-//             hash and get their final value on the way), slice max, lowest argmax and an
-//             online sum of exp((z' - max)/T); per-thread maxima bound the top-k cut.
-//   exchange  every CTA pushes its slice statistics into every CTA's shared memory
-//             (DSMEM) and one cluster barrier publishes them.  Greedy rows end here.
-//   pass B    the tokens that can survive truncation (y >= a provable bound) are
-//             compacted; a leader CTA gathers them (DSMEM stores + a remote mbarrier
-//             arrive) and finishes top-k -> top-p -> min-p and the exponential race alone.
-//   slow path rows without a usable bound (very large k, compaction overflow) run
-//             cluster-wide radix selects, one pass over the slice per digit.
+//   P1 item   (row, slice): the slice's penalised / biased tokens from the row's
+//             history and logit_bias lists, then pass A: the slice streams from HBM
+//             through a 4-stage TMA ring (cp.async.bulk into shared memory, completing
+//             on mbarriers) and gives its max, lowest argmax, online sum of
+//             2^((z' - max) log2(e) / T), top-k bounds from per-thread maxima, and a
+//             table of per-(thread, stage) maxima that later lets the row re-read only
+//             the vectors that can hold candidates.  The slice record goes to global
+//             memory and a per-row ticket counts the slices; the CTA that finishes the
+//             row's last slice carries on with the row (no one waits for it).
+//   row end   the last arriver combines the slice records, picks the truncation plan
+//             and, for greedy and top-k / min-p rows, finishes the row alone: it reads
+//             the tables, re-reads the few vectors above the top-k bound from L2,
+//             compacts the candidates, finds top-k -> top-p -> min-p by exact selects
+//             and runs the exponential race.
+//   phases    rows that need every token a second time (top-p alone, min-p with top-p,
+//             no truncation) get further per-slice items placed later in the list
+//             (after about one wave of other items, so their first pass is done when
+//             they are taken); an item of phase p waits, bounded, until the row's phase
+//             p - 1 is complete, and the last arriver of each phase moves the row on.
+//             Every wait is on items earlier in the list, which running CTAs took, so
+//             the list cannot deadlock.
 //
-// Cold, bulky steps are out-of-line functions so that the instruction stream of the hot
-// path stays small.  The arithmetic that decides integers (kept set, drawn id) is exact
-// and identical on any IEEE machine (sampler_math.cuh).  Page references: "SGLang source
+// A one-CTA kernel ahead of the sampler orders the rows heaviest first and writes the
+// work list.  The arithmetic that decides integers (kept set, drawn id) is exact and
+// identical on any IEEE machine (sampler_math.cuh).  Page references: "SGLang source
 // teardown (10): Sampling, Grammar and structured output" (SGLang page) and "GLM-5.3
 // inference (7): output side" (GLM page).
 
-#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
 #include <cfloat>
@@ -41,8 +46,6 @@
 #include "cluster_sync.cuh"
 #include "sampler_math.cuh"
 
-namespace cg = cooperative_groups;
-
 namespace {
 
 using namespace clsample;
@@ -50,32 +53,33 @@ using namespace clsample;
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMinBlocks = 4;      // CTAs per SM the register budget is sized for
-constexpr int kHashCap = 1024;     // hash slots of the penalty kernel
 constexpr int kPenCap = 512;       // distinct penalised / biased ids per slice
-constexpr int kCandCap = 4096;     // compacted candidates per slice (global scratch)
+constexpr int kCandCap = 4096;     // compacted candidates per slice segment (global scratch)
 constexpr int kWhistBytes = 4096;  // top-p warp histograms (kWarps x 64 split counters)
-constexpr int kMaxCluster = 8;     // portable cluster size
-constexpr int kGatherCap = 4096;   // candidates the leader keeps in shared memory
+constexpr int kMaxSlices = 8;      // slices per row
+constexpr int kGatherCap = 4096;   // candidates the finishing CTA keeps in shared memory
 constexpr int kMaxChunk = 32 * 1024;  // longest slice
-constexpr int kStageBytes = 8192;     // one ring stage: two 16-byte vectors per thread
+constexpr int kStageBytes = 8192;     // one ring stage
 constexpr int kStages = 4;            // ring depth
 constexpr int kReload = 4;            // 16-byte loads in flight per thread when re-reading
-constexpr uint32_t kEmpty = 0xFFFFFFFFu;
-// penalised-token table: count | kBiasBit (a logit_bias entry applies) | kAllowedBit
+constexpr int kTabMax = kMaxChunk * 4 / kStageBytes * kThreads;  // table entries per slice
+constexpr int kHitCap = kStages * kStageBytes / 4;                // table hits the row end keeps
+constexpr int kOrderThreads = 1024;
+constexpr int kSmallRow = 2048;   // allowed tokens of a row that the row end takes all of
+// penalised-token flags next to the history count
 constexpr uint32_t kAllowedBit = 0x80000000u;
 constexpr uint32_t kBiasBit = 0x40000000u;
 constexpr uint32_t kCountMask = 0x3FFFFFFFu;
-constexpr uint32_t kPenBias = 0x80000000u;  // in PenEntry::id
+constexpr uint32_t kWaitLimit = 1u << 20;  // polls (<= 1 us apart) of a phase wait
 
 enum : int { kRowOk = 0, kRowOverflow = 1, kRowInvalid = 2 };
-enum : int { kFlagInvalid = 1, kFlagOverflow = 2, kFlagRing = 4 };  // kFlagRing: a ring stage never landed
-enum : int { kPlanFast = 0, kPlanTopP = 1, kPlanUntrunc = 2, kPlanSlow = 3 };
+enum : int { kFlagInvalid = 1, kFlagOverflow = 2, kFlagRing = 4 };  // kFlagRing: a wait gave up
+enum : int { kPlanFast = 0, kPlanTopP = 1, kPlanUntrunc = 2, kPlanSlow = 3, kPlanDone = 4 };
 
 struct Geometry {
-  int C;      // CTAs per row (cluster size)
-  int chunk;  // tokens per CTA, multiple of 32
+  int C;      // slices per row
+  int chunk;  // tokens per slice, multiple of 32
   int smem;   // dynamic shared memory per CTA
-  int cap;    // compacted candidates per CTA the leader can gather
 };
 
 struct Cand {
@@ -83,54 +87,29 @@ struct Cand {
   int id;
 };
 
-// One penalised / biased token of a slice, as the penalty kernel lists it.
-struct __align__(16) PenEntry {
-  uint32_t id;     // local id | kPenBias when a logit_bias entry applies
-  uint32_t count;  // occurrences in the row's history (saturates at kCountMask)
-  float bias;      // the last bias entry's value
-  uint32_t pad;
-};
-
-struct LaunchParams {
-  clsample_args_t a;
-  int C;
-  int chunk;
-  int cap;
-  int vec_ok;         // every row start is 16-byte aligned: slices stream through the TMA ring
-  PenEntry* pen;      // [B * C][kPenCap] penalised-token lists (scratch)
-  int2* pen_n;        // [B * C] list length, flags
-  Cand* cand;         // [B * C][kCandCap] compacted candidates (scratch)
-  int* row_class;     // [B] cost class of each row (scratch)
-  int* row_order;     // [B] the row each cluster samples, heaviest class first (scratch)
-  unsigned* ticket;   // CTAs of the preparation kernel that have finished (scratch)
-};
-
-// The row sampled by the calling CTA's cluster (clusters take rows heaviest first).
-__device__ __forceinline__ int cluster_row(const LaunchParams& P) {
-  return __ldg(P.row_order + blockIdx.x / (unsigned)P.C);
-}
-
-// Slice statistics pushed to every CTA after pass A.
 // Lower bounds of the k-th largest z' come from maxima of disjoint token groups: each
 // thread keeps one maximum per stage slot (kGroups groups), and the 32 maxima of one slot
 // across a warp form a "group set".  A set whose j-th largest maximum is L guarantees j
-// tokens at or above L.  For j = 2^i (i < kNJ) every CTA reports the minimum of L over
+// tokens at or above L.  For j = 2^i (i < kNJ) every slice reports the minimum of L over
 // its sets that reach j maxima above -inf, and how many sets do; n such sets guarantee
 // n*j tokens.
 constexpr int kNJ = 6;  // j = 1, 2, 4, ..., 32
 
+// Slice record of pass A.
 struct X1 {
   float m;         // slice max of z' (-inf if no candidate)
   int arg;         // lowest id reaching m (INT_MAX if none)
   float s;         // sum over the slice's candidates of 2^((z' - m) * log2(e) / T)
   int flags;       // kFlag*
   float lk;        // max over warps of the warp's k-th largest thread max (k <= 32; else -inf)
-  float lj[kNJ];   // min over the CTA's groups reaching 2^i maxima of the 2^i-th largest
+  float lj[kNJ];   // min over the slice's groups reaching 2^i maxima of the 2^i-th largest
   unsigned char nj[8];  // how many groups reach 2^i (i < kNJ)
-  int nallowed;    // allowed tokens of the slice (at least its candidates)
+  int nallowed;    // allowed tokens of the slice
+  int npen;        // penalised / biased tokens listed (at most kPenCap)
+  int tab;         // 1: the table of vector maxima covers the slice's bulk part
 };
 
-// Slice results pushed to every CTA after pass B (and by the slow path).
+// Slice record of a later phase.
 struct X2 {
   int count;                // compacted candidates (may exceed the capacity)
   int flags;
@@ -150,7 +129,8 @@ struct RowParams {
   int invalid;
 };
 
-// Row statistics and the truncation plan, identical in every CTA after exchange 1.
+// Row statistics and the truncation plan, set by the row's first phase end and read by
+// its later phases.
 struct RowState {
   float m;      // max z'
   int arg;      // lowest id reaching it
@@ -158,6 +138,7 @@ struct RowState {
   int flags;
   float bound;  // lower bound of the k-th largest z' (-inf if none)
   int nallowed_max;  // the largest per-slice allowed-token count
+  int nallowed_sum;  // allowed tokens of the row
   float lnS;
   float invT;
   float L;      // min-p cut in y: ln(min_p), or -inf
@@ -167,31 +148,54 @@ struct RowState {
   int all;      // kPlanFast: every candidate of the row is compacted (theta = -inf)
   float s0;     // race score of the argmax token, which every kept set contains: a lower
                 // bound of the winning score that seeds every race
+  int bstar;    // top-p alone: the crossing bin
+  unsigned long long above, cth;  // top-p alone: mass above the crossing bin; ceil(p W)
+};
+
+struct LaunchParams {
+  clsample_args_t a;
+  int C;
+  int chunk;
+  int vec_ok;         // every row start is 16-byte aligned: slices stream through the TMA ring
+  int gap;            // rows of the work list between a heavy row's phases
+  // scratch (device)
+  unsigned* ctl;      // [0] next item, [1] CTAs done, [2] work-list segments
+  unsigned* ticket;   // [B][4] items of each phase of the row that have finished
+  unsigned* phase_done;  // [B] the row's last completed phase
+  unsigned* bad;      // [B] a phase wait of the row gave up
+  unsigned* seg;      // [3 B] work list: row | phase << 24 | phases << 28, C items each
+  int* order;         // [B] rows, heaviest class first
+  RowState* rows;     // [B]
+  X1* x1;             // [B * C]
+  X2* x2;             // [B * C]
+  uint2* pen;         // [B * C][kPenCap] penalised tokens: local id, bits of z'
+  uint16_t* tab;      // [B * C][kTabMax] per-(stage, thread) maxima
+  unsigned long long* phist;  // [B * C][kPBins] top-p bin masses
+  Cand* cand;         // [B * C][kCandCap] compacted candidates
 };
 
 // ---------------------------------------------------------------- shared memory
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+constexpr int kPBins = 64;
 constexpr size_t kOffHistC = kWhistBytes;                                   // 4 KB
 constexpr size_t kOffHistW = kOffHistC + sizeof(uint32_t) * 256;            // 5 KB
-constexpr size_t kOffMrgC = kOffHistW + sizeof(unsigned long long) * 256;  // 7 KB
 constexpr size_t kR2Bytes = 9 * 1024;
 
 // Dynamic shared memory of one CTA (byte offsets):
-//   ring      kStages x kStageBytes   the slice's stream (TMA destination); in the
-//                                     leader, once every CTA has finished reading its
-//                                     slice: the cluster's gathered candidates
+//   ring      kStages x kStageBytes   the slice's stream (TMA destination); at a row end:
+//                                     table hits, then the gathered candidates
 //   live      u32[chunk/32]           allowed by the bitmask, inside the row, not penalised
 //   mod       u32[chunk/32]           penalised / biased tokens
 //   prank     u16[chunk/32]           rank of each mod word's first penalised token
 //   pid/pcnt/pbias/pz [kPenCap]       the penalised tokens in token order: local id;
-//                                     count | kBiasBit | kAllowedBit; bias; raw logit in
-//                                     pass A, then the final z'
-//   r2 (9 KB) cand Cand[512] | hist_c u32[256] | hist_w u64[256] | mrg_c u32[2][256];
-//             mrg_w u64[2][256] overlays cand (slow path); the top-p warp histograms
-//             (kWarps x 64 u64) overlay cand and their merged copy is the start of
-//             mrg_c; the leader's bucket select overlays [0, 8 KB)
+//                                     count | kBiasBit | kAllowedBit (pass A) ; bias
+//                                     entry, then its value; raw logit in pass A, then the
+//                                     final z'
+//   r2 (9 KB) pass A: the table of vector maxima; later: top-p warp histograms [0, 4 KB),
+//             hist_c u32[256] at 4 KB, hist_w u64[256] at 5 KB; at a row end the listed
+//             penalised ids of every slice, then the bucket select
 struct Layout {
   uint32_t live, mod, prank, pid, pcnt, pbias, pz, r2, total;
 };
@@ -219,15 +223,17 @@ __host__ __device__ inline Layout layout_for(int chunk) {
   return L;
 }
 static_assert(sizeof(Cand) * kGatherCap <= (size_t)kStages * kStageBytes, "gather area overflows the ring");
-static_assert(kR2Bytes >= kOffMrgC + sizeof(uint32_t) * 2 * 256, "r2 tables overflow");
-static_assert(sizeof(unsigned long long) * 2 * 256 <= kOffHistC, "mrg_w overlaps the histograms");
+static_assert(sizeof(uint16_t) * kTabMax <= kR2Bytes, "table of vector maxima overflows r2");
+static_assert(sizeof(uint16_t) * kPenCap * kMaxSlices <= kR2Bytes, "penalised ids overflow r2");
+static_assert(kOffHistW + sizeof(unsigned long long) * 256 <= kR2Bytes, "r2 tables overflow");
 static_assert(sizeof(unsigned long long) * 1024 <= kR2Bytes && sizeof(Cand) * 1024 <= kR2Bytes,
-              "bucket select does not fit r2");  // in the leader every r2 table is dead
-static_assert(2 * sizeof(uint32_t) * kWarps * 64 <= kWhistBytes, "top-p histogram does not fit r2");
-static_assert(sizeof(float) * kWarps * 4 * kNJ <= kOffMrgC, "pass A group-set bounds overlap the merged bins");
+              "bucket select does not fit r2");
+static_assert(2 * sizeof(uint32_t) * kWarps * kPBins <= kWhistBytes, "top-p histogram does not fit r2");
+static_assert(sizeof(float) * kWarps * 4 * kNJ <= (size_t)kStages * kStageBytes, "group-set bounds overflow the ring");
 static_assert(1024 % kThreads == 0, "bucket scan assumes whole buckets per thread");
 static_assert(kStageBytes % (16 * kThreads) == 0, "a stage holds whole vectors per thread");
 static_assert(kPenCap % kThreads == 0 && kPenCap <= 65536 && kMaxChunk <= 65536, "16-bit ids and ranks");
+static_assert(kTabMax <= 4096 && kMaxSlices <= 16, "hit codes: slice << 16 | entry");
 
 extern __shared__ __align__(128) unsigned char smem_dyn[];
 
@@ -240,8 +246,6 @@ struct Smem {
   uint32_t* pcnt;
   float* pbias;
   float* pz;
-  uint32_t* mrg_c;
-  unsigned long long* mrg_w;
   Cand* gather;
   uint32_t* hist_c;
   unsigned long long* hist_w;
@@ -263,16 +267,14 @@ __device__ __forceinline__ Smem carve(int chunk) {
   s.r2 = b + L.r2;
   s.hist_c = reinterpret_cast<uint32_t*>(s.r2 + kOffHistC);
   s.hist_w = reinterpret_cast<unsigned long long*>(s.r2 + kOffHistW);
-  s.mrg_c = reinterpret_cast<uint32_t*>(s.r2 + kOffMrgC);
-  s.mrg_w = reinterpret_cast<unsigned long long*>(s.r2);
   s.gather = reinterpret_cast<Cand*>(b);
   return s;
 }
 
 // Static per-CTA state shared by the kernel's functions.
 struct Shared {
-  X1 x1[kMaxCluster];
-  X2 x2[kMaxCluster];
+  X1 x1[kMaxSlices];
+  X2 x2[kMaxSlices];
   X1 x1_mine;
   X2 x2_mine;
   unsigned long long full[kStages];  // ring stage barriers (one arrival + the copy's bytes)
@@ -284,39 +286,73 @@ struct Shared {
   X2 red_x[kWarps];
   float red_wb[kWarps * 2];
   int csr[4];
+  int poff[kMaxSlices + 1];
   float zth, res;
-  int bstar, nl, flags, count, digit, none, npen;
-  int nallowed;
+  int bstar, nl, flags, count, digit, none, npen, nallowed, nhits, nhist, last, ok;
+  unsigned item;
+  uint32_t seq;  // ring stages consumed by this CTA so far (fixes each buffer's parity)
+  uint64_t policy;  // L2 policy of the current slice's stream
+  unsigned long long tbar;  // the row end's table copies
+  uint32_t tpar;     // its phase parity
   unsigned long long above;
 };
 __shared__ Shared sh;
 
-// The calling CTA's place in the launch.
+// The calling CTA's slice of a row.
 struct Geo {
-  int C, chunk, cap, rank, row, c0, len, nvec;
+  int C, chunk, slice, row, c0, len, nvec;
   int bulk_tokens;  // tokens of the slice that stream through the ring (0: none)
   int nst;          // ring stages per pass
   const unsigned char* g;  // the slice's first logit
 };
 
 template <bool kBF16>
-__device__ __forceinline__ Geo geo(const LaunchParams& P) {
+__device__ __forceinline__ Geo geo(const LaunchParams& P, int row, int slice) {
   constexpr int kEsize = kBF16 ? 2 : 4;
   Geo g;
   g.C = P.C;
   g.chunk = P.chunk;
-  g.cap = P.cap;
-  g.rank = (int)cg::this_cluster().block_rank();
-  g.row = cluster_row(P);
-  g.c0 = g.rank * g.chunk;
+  g.slice = slice;
+  g.row = row;
+  g.c0 = slice * g.chunk;
   g.len = max(0, min(P.a.V, g.c0 + g.chunk) - g.c0);
   g.nvec = g.chunk / 4;
   const int bulk = P.vec_ok ? (int)(((size_t)g.len * kEsize) & ~(size_t)15) : 0;
   g.bulk_tokens = bulk / kEsize;
   g.nst = (bulk + kStageBytes - 1) / kStageBytes;
   g.g = reinterpret_cast<const unsigned char*>(P.a.logits) +
-        ((long long)g.row * P.a.logits_row_stride + g.c0) * kEsize;
+        ((long long)row * P.a.logits_row_stride + g.c0) * kEsize;
   return g;
+}
+
+// ---------------------------------------------------------------- global memory between CTAs
+
+// Data another CTA wrote during this launch is read at L2 (the L1 is not coherent).
+template <typename T>
+__device__ __forceinline__ void ldcg_copy(T* dst, const T* src) {
+  static_assert(sizeof(T) % 4 == 0, "word copy");
+  const uint32_t* s = reinterpret_cast<const uint32_t*>(src);
+  uint32_t* d = reinterpret_cast<uint32_t*>(dst);
+#pragma unroll
+  for (int i = 0; i < (int)(sizeof(T) / 4); ++i) d[i] = __ldcg(s + i);
+}
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// A candidate of a gathered array in shared memory or (when `global`) in the scratch.
+__device__ __forceinline__ Cand ldcand(const Cand* G, int i, bool global) {
+  if (global) {
+    const float2 v = __ldcg(reinterpret_cast<const float2*>(G) + i);
+    return Cand{v.x, __float_as_int(v.y)};
+  }
+  return G[i];
 }
 
 // ---------------------------------------------------------------- slice access
@@ -340,13 +376,13 @@ __device__ __forceinline__ float4 gload4(const Geo& g, int f) {
 // Tokens 4f .. 4f+3 by one aligned load (the slice start is 16-byte aligned and the
 // vector lies inside the row), widened to f32.
 template <bool kBF16>
-__device__ __forceinline__ float4 vload4(const Geo& g, int f) {
+__device__ __forceinline__ float4 vload4(const unsigned char* base, int f) {
   if (kBF16) {
-    const uint2 w = __ldg(reinterpret_cast<const uint2*>(g.g) + f);
+    const uint2 w = __ldg(reinterpret_cast<const uint2*>(base) + f);
     return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u), __uint_as_float(w.y << 16),
                        __uint_as_float(w.y & 0xFFFF0000u));
   }
-  return __ldg(reinterpret_cast<const float4*>(g.g) + f);
+  return __ldg(reinterpret_cast<const float4*>(base) + f);
 }
 
 // Vector v (4 tokens) of a ring stage buffer, widened to f32.
@@ -369,17 +405,14 @@ __device__ __forceinline__ uint32_t live4(const uint32_t* live, int f) {
   return (live[f >> 3] >> ((f & 7) * 4)) & 0xFu;
 }
 
-// ---------------------------------------------------------------- hash of penalised ids
-
-// Inserts local id l; returns its slot, or -1 when the table is full (bounded probing).
-__device__ __forceinline__ int hash_insert(uint32_t* hkey, uint32_t l) {
-  const uint32_t h = (l * 2654435761u) & (kHashCap - 1);
-  for (int probe = 0; probe < kHashCap; ++probe) {
-    const uint32_t slot = (h + probe) & (kHashCap - 1);
-    const uint32_t prev = atomicCAS(&hkey[slot], kEmpty, l);
-    if (prev == kEmpty || prev == l) return (int)slot;
-  }
-  return -1;
+// Bitmask word w of a row's slice (32 tokens from c0 + 32 w), clipped to the row.
+__device__ __forceinline__ uint32_t mask_word(const int32_t* bmrow, int c0, int len, int w) {
+  const int e = 32 * w;
+  if (e >= len) return 0u;
+  uint32_t word = bmrow ? (uint32_t)__ldg(bmrow + (c0 >> 5) + w) : 0xFFFFFFFFu;
+  const int rem = len - e;
+  if (rem < 32) word &= (1u << rem) - 1u;
+  return word;
 }
 
 // ---------------------------------------------------------------- out-of-line math
@@ -516,14 +549,6 @@ __device__ __noinline__ void write_sampled(const clsample_args_t& a, int row, co
   if (a.dbg_cut) a.dbg_cut[row] = ok ? r.ymin : -INFINITY;
 }
 
-// Pushes the calling CTA's record `*mine` into slot `rank` of `dst` in every CTA of the
-// cluster (threads 0 .. C-1 each write one copy).  A cluster barrier must follow.
-template <typename T>
-__device__ __forceinline__ void push_all(const cg::cluster_group& cluster, T* dst, const T* mine, int rank,
-                                         int C) {
-  if ((int)threadIdx.x < C) *cluster.map_shared_rank(dst + rank, (unsigned)threadIdx.x) = *mine;
-}
-
 // Adds a weight (<= 2^40) to a split 64-bit shared counter {c[0]: units of 1, c[1]: units
 // of 2^21} with native 32-bit atomics; a wrap of c[0] (the adder sees it) carries 2^11
 // into c[1].  Exact for up to 8191 additions; read it back with split_get.
@@ -651,15 +676,22 @@ constexpr float kGumbelMax = 16.75f;
 
 // y-bins of the top-p histogram: bin b holds -(b+1)/4 < y <= -b/4; the last bin also
 // holds everything below.
-constexpr int kPBins = 64;
 __device__ __forceinline__ int pbin(float y) {
   const int b = __float2int_rz(__fmul_rn(-y, 4.0f));
   return b < kPBins - 1 ? b : kPBins - 1;
 }
 
+// Table entry of a group of tokens: 0 if none is live, else the top 16 bits of the
+// order-preserving key of their largest z (so "entry >= top 16 bits of key(zth)" holds
+// for every group with a live token at or above zth).
+__device__ __forceinline__ uint16_t tab_entry(bool any, float vmax) {
+  return any ? (uint16_t)(fkey(vmax) >> 16) : (uint16_t)0;
+}
+__device__ __forceinline__ uint32_t tab_threshold(float zth) { return fkey(zth) >> 16; }
+
 // ---------------------------------------------------------------- the TMA ring
 
-// Issues stage k of a pass (stage sequence number s picks the buffer) on its barrier.
+// Issues stage k of the slice (stage sequence number s picks the buffer) on its barrier.
 // Thread 0 only.
 template <bool kBF16>
 __device__ __forceinline__ void ring_issue(const Geo& g, const Smem& S, int k, uint32_t s) {
@@ -668,14 +700,15 @@ __device__ __forceinline__ void ring_issue(const Geo& g, const Smem& S, int k, u
   const uint32_t bytes = (uint32_t)min(kStageBytes, g.bulk_tokens * kEsize - off);
   const uint32_t slot = s % kStages;
   mbar_arrive_expect_tx(&sh.full[slot], bytes);
-  bulk_copy_g2s(S.ring + slot * kStageBytes, g.g + off, bytes, &sh.full[slot]);
+  bulk_copy_g2s_hint(S.ring + slot * kStageBytes, g.g + off, bytes, &sh.full[slot], sh.policy);
 }
 
-// Issues the first stages of pass `pass` (thread 0 only).
+// Issues the first stages of the slice, continuing the CTA's stage sequence at seq0.
+// Thread 0 only; the ring's previous contents (any proxy) are dead.
 template <bool kBF16>
-__device__ __forceinline__ void ring_start(const Geo& g, const Smem& S, int pass) {
-  const uint32_t seq0 = (uint32_t)pass * (uint32_t)g.nst;
-  for (int k = 0; k < min(kStages, g.nst); ++k) ring_issue<kBF16>(g, S, k, seq0 + k);
+__device__ __forceinline__ void ring_start(const Geo& g, const Smem& S, uint32_t seq0) {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  for (int k = 0; k < min(kStages, g.nst); ++k) ring_issue<kBF16>(g, S, k, seq0 + (uint32_t)k);
 }
 
 // Waits (bounded, suspending) for ring stage s.  Thread 0 only; a stage that never lands
@@ -684,52 +717,60 @@ __device__ __forceinline__ void ring_wait(uint32_t s) {
   if (!mbar_wait_sleep(&sh.full[s % kStages], (s / kStages) & 1u)) atomicOr(&sh.flags, kFlagRing);
 }
 
-// One pass over the slice: body(f, wd, v) for every 4-token vector f, with its live bits
-// wd and raw values v widened to f32 (valid for every vector that starts inside the row;
-// lanes without a vector get f = nvec, past the row, and wd = 0).
-// Stage sequence numbers continue across the CTA's passes (pass p uses p*nst ..
-// p*nst + nst - 1), which fixes each ring buffer's barrier parity.  Aligned rows stream
-// through the ring; the ragged tail and unaligned rows come in by plain loads.  Every
-// thread calls it; every lane of a warp makes the same number of body calls (wd = 0 where
-// it has no vector), so bodies may use warp collectives.  `started`: thread 0 already
-// issued the pass's first stages.
-template <bool kBF16, bool kSlot = false, class Body>
-__device__ __forceinline__ void stream(const Geo& g, const Smem& S, int& pass, bool started, Body&& body) {
+// Pass A's walk over the slice: body(t, f, wd, v) for every 4-token vector f (slot t of
+// its stage), with its live bits wd and raw values v widened to f32, and stage_end(k)
+// after every stage of the ring part.  Lanes without a vector get f = nvec (past the
+// row) and wd = 0; every lane of a warp makes the same number of body calls.  The ring
+// part streams through the TMA ring (thread 0 started its first stages); the ragged
+// tail and unaligned rows come in by plain loads (slot 0, no stage_end).
+template <bool kBF16, class Body, class StageEnd>
+__device__ __forceinline__ void stream_ring(const Geo& g, const Smem& S, Body&& body, StageEnd&& stage_end) {
   constexpr int kEsize = kBF16 ? 2 : 4;
   constexpr int kVecPerStage = kStageBytes / (4 * kEsize);
   constexpr int kVPT = kVecPerStage / kThreads;
   const int tid = threadIdx.x;
-  if (pass == 0 && g.nst > 0) {
-    const uint32_t seq0 = 0u;
-    if (tid == 0 && !started) ring_start<kBF16>(g, S, pass);
+  const uint32_t seq0 = sh.seq;
 #pragma unroll 1
-    for (int k = 0; k < g.nst; ++k) {
-      const uint32_t s = seq0 + (uint32_t)k;
-      // thread 0 sleeps on the stage's barrier; the block barrier then also says that
-      // every thread is done with stage k - 1, whose buffer is refilled at once
-      if (tid == 0) ring_wait(s);
-      __syncthreads();
-      if (tid == 0 && k >= 1 && k - 1 + kStages < g.nst)
-        ring_issue<kBF16>(g, S, k - 1 + kStages, s - 1 + kStages);
-      (void)mbar_try_wait(&sh.full[s % kStages], (s / kStages) & 1u);  // this thread's acquire
-      const unsigned char* buf = S.ring + (s % kStages) * kStageBytes;
+  for (int k = 0; k < g.nst; ++k) {
+    const uint32_t s = seq0 + (uint32_t)k;
+    // thread 0 sleeps on the stage's barrier; the block barrier then also says that
+    // every thread is done with stage k - 1, whose buffer is refilled at once
+    if (tid == 0) ring_wait(s);
+    __syncthreads();
+    if (tid == 0 && k >= 1 && k - 1 + kStages < g.nst) ring_issue<kBF16>(g, S, k - 1 + kStages, s - 1 + kStages);
+    (void)mbar_try_wait(&sh.full[s % kStages], (s / kStages) & 1u);  // this thread's acquire
+    const unsigned char* buf = S.ring + (s % kStages) * kStageBytes;
 #pragma unroll
-      for (int t = 0; t < kVPT; ++t) {
-        const int fl = t * kThreads + tid;
-        const int f = k * kVecPerStage + fl;
-        const bool in = 4 * f < g.bulk_tokens;
-        const uint32_t wd = in ? live4(S.live, f) : 0u;
-        const float4 v = in ? sload4<kBF16>(buf, fl) : make_float4(0.f, 0.f, 0.f, 0.f);
-        // vectors past the ring part: f = nvec (past the row).  With kSlot the body also
-        // gets the vector's slot t in the stage (a compile-time constant after unrolling)
-        if constexpr (kSlot) body(in ? f : g.nvec, wd, v, t);
-        else body(in ? f : g.nvec, wd, v);
-      }
+    for (int t = 0; t < kVPT; ++t) {
+      const int fl = t * kThreads + tid;
+      const int f = k * kVecPerStage + fl;
+      const bool in = 4 * f < g.bulk_tokens;
+      const uint32_t wd = in ? live4(S.live, f) : 0u;
+      const float4 v = in ? sload4<kBF16>(buf, fl) : make_float4(0.f, 0.f, 0.f, 0.f);
+      body(t, in ? f : g.nvec, wd, v);
     }
+    stage_end(k);
   }
-  if (pass > 0 && g.bulk_tokens > 0) {
-    // later passes find the slice in L2: plain 16-byte loads, kReload per thread in
-    // flight (bulk copies would queue behind the HBM copies of other CTAs' first passes)
+  const int f_end = (g.len + 3) / 4;
+#pragma unroll 1
+  for (int base = g.bulk_tokens / 4; base < f_end; base += kThreads) {
+    const int f = base + tid;
+    const bool in = f < f_end;
+    const uint32_t wd = in ? live4(S.live, f) : 0u;
+    const float4 v = in ? gload4<kBF16>(g, f) : make_float4(0.f, 0.f, 0.f, 0.f);
+    body(0, in ? f : g.nvec, wd, v);
+  }
+  __syncthreads();  // the ring is free; the bodies' shared writes are visible
+  if (tid == 0) sh.seq = seq0 + (uint32_t)g.nst;
+}
+
+// A later pass over the slice, which is in L2 by now: body(f, wd, v) for every vector
+// with a live token (plain 16-byte loads, kReload per thread in flight), lanes without
+// one get f = nvec and wd = 0 (every lane of a warp makes the same number of calls).
+template <bool kBF16, class Body>
+__device__ __forceinline__ void stream_ldg(const Geo& g, const Smem& S, Body&& body) {
+  const int tid = threadIdx.x;
+  if (g.bulk_tokens > 0) {
     const int nv = g.bulk_tokens / 4;
 #pragma unroll 1
     for (int base = 0; base < nv; base += kReload * kThreads) {
@@ -739,18 +780,16 @@ __device__ __forceinline__ void stream(const Geo& g, const Smem& S, int& pass, b
       for (int u = 0; u < kReload; ++u) {
         const int f = base + u * kThreads + tid;
         const bool in = f < nv;
-        wd[u] = in ? live4(S.live, f) : 0u;  // later passes read only live tokens
-        v[u] = wd[u] ? vload4<kBF16>(g, f) : make_float4(0.f, 0.f, 0.f, 0.f);
+        wd[u] = in ? live4(S.live, f) : 0u;
+        v[u] = wd[u] ? vload4<kBF16>(g.g, f) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int u = 0; u < kReload; ++u) {
         const int f = base + u * kThreads + tid;
-        if constexpr (kSlot) body(f < nv ? f : g.nvec, wd[u], v[u], 0);
-        else body(f < nv ? f : g.nvec, wd[u], v[u]);
+        body(f < nv ? f : g.nvec, wd[u], v[u]);
       }
     }
   }
-  // the ragged tail, and whole unaligned slices: plain loads
   const int f_end = (g.len + 3) / 4;
 #pragma unroll 1
   for (int base = g.bulk_tokens / 4; base < f_end; base += kThreads) {
@@ -758,360 +797,390 @@ __device__ __forceinline__ void stream(const Geo& g, const Smem& S, int& pass, b
     const bool in = f < f_end;
     const uint32_t wd = in ? live4(S.live, f) : 0u;
     const float4 v = in ? gload4<kBF16>(g, f) : make_float4(0.f, 0.f, 0.f, 0.f);
-    if constexpr (kSlot) body(in ? f : g.nvec, wd, v, 0);
-    else body(in ? f : g.nvec, wd, v);
+    body(in ? f : g.nvec, wd, v);
   }
-  __syncthreads();  // the ring is free for the next pass; the bodies' shared writes are visible
-  ++pass;
+  __syncthreads();
 }
 
-// Adds n occurrences of local id l to the history counts; kFlagOverflow if the hash is
-// full.
-__device__ __forceinline__ int count_id(uint32_t* hkey, uint32_t* hcnt, uint32_t l, uint32_t n) {
-  const int slot = hash_insert(hkey, l);
-  if (slot < 0) return kFlagOverflow;
-  atomicAdd(&hcnt[slot], n);
-  return 0;
-}
+// ---------------------------------------------------------------- the work list
 
-// ---------------------------------------------------------------- row preparation
-
-constexpr int kPrepThreads = 128;
-constexpr int kPrepWarps = kPrepThreads / 32;
 constexpr int kClasses = 5;
+constexpr int kOrderPer = 8;  // rows per thread of the ordering kernel kept in registers
 
-// Expected cost class of a row from its parameters alone (0 = heaviest): top-p alone,
-// then untruncated or very large k, then large k or top-p over a min-p set, then the
-// other sampling rows, then greedy or invalid rows.  Only the launch order uses it.
-__device__ __forceinline__ int row_class(const clsample_args_t& a, int row) {
-  const float T = a.temperatures ? a.temperatures[row] : 1.0f;
-  const int k = a.top_ks ? a.top_ks[row] : -1;
-  const float p = a.top_ps ? a.top_ps[row] : 1.0f;
-  const float mp = a.min_ps ? a.min_ps[row] : 0.0f;
-  if (!(T >= kGreedyEps) || k == 0 || k == 1 || k < -1) return 4;
+// Cost class of a row from its parameters alone (0 = heaviest: top-p alone, then
+// untruncated or very large k, then large k or top-p over a min-p set, then the other
+// sampling rows, then greedy or invalid rows; only the order of the work list uses it),
+// and its work-list phases: rows that need every token a second time get one more
+// per-slice pass (top-p mass over the whole row with min-p; the race over every token
+// when nothing is truncated) or two (top-p alone: the mass histogram, then the race);
+// every other row ends at the end of its first phase.
+__device__ __forceinline__ void row_info(const clsample_args_t& a, int row, int* cls, int* nph) {
+  const float T = a.temperatures ? __ldg(a.temperatures + row) : 1.0f;
+  const int k = a.top_ks ? __ldg(a.top_ks + row) : -1;
+  const float p = a.top_ps ? __ldg(a.top_ps + row) : 1.0f;
+  const float mp = a.min_ps ? __ldg(a.min_ps + row) : 0.0f;
+  if (!(T >= kGreedyEps) || k == 0 || k == 1 || k < -1) {
+    *cls = 4;
+    *nph = 1;
+    return;
+  }
   const bool kfin = k >= 2;
-  if (!kfin && p < 1.0f && !(mp > 0.0f)) return 0;
-  if ((!kfin && !(mp > 0.0f)) || k >= 512) return 1;
-  if (k >= 64 || (!kfin && p < 1.0f)) return 2;
-  return 3;
+  if (!kfin && p < 1.0f && !(mp > 0.0f)) *cls = 0;
+  else if ((!kfin && !(mp > 0.0f)) || k >= 512) *cls = 1;
+  else if (k >= 64 || (!kfin && p < 1.0f)) *cls = 2;
+  else *cls = 3;
+  if (kfin) *nph = 1;
+  else if (p < 1.0f) *nph = mp > 0.0f ? 2 : 3;
+  else *nph = mp > 0.0f ? 1 : 2;
 }
 
-// One CTA per (row, slice), ahead of the sampler.
-//  * The slice's distinct penalised or biased token ids with their history count and the
-//    last bias entry (SGLang page, "Order semantics of the penalties" and "Why
-//    logit_bias is built from triples": the last duplicate wins), sorted by id, into the
-//    slice's scratch list.  Duplicate history ids are counted once per warp (Zipf-like
-//    histories repeat their frequent ids many times).  A slice with more than kPenCap
-//    distinct ids is flagged OVERFLOW.
-//  * The launch order of the sampler's rows, heaviest first: every slice-0 CTA writes
-//    its row's class; the last CTA to finish (a ticket counter) sorts the rows by class,
-//    stably, and resets the ticket.
-__global__ void __launch_bounds__(kPrepThreads) prep_kernel(const __grid_constant__ LaunchParams P) {
-  __shared__ uint32_t hkey[kHashCap];
-  __shared__ uint32_t hcnt[kHashCap];
-  __shared__ int32_t hbias[kHashCap];
-  __shared__ uint32_t mod[kMaxChunk / 32];
-  __shared__ uint16_t wbase[kMaxChunk / 32];
-  __shared__ int red[kPrepWarps * kClasses];
-  __shared__ int csr[4];
-  __shared__ int flags_sh, last_sh;
+// Block-wide exclusive scan of one int per thread (kOrderThreads threads); returns the
+// thread's offset, *total the sum.
+__device__ int order_scan(int x, int* red, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = x;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += o;
+  }
+  __syncthreads();
+  if (lane == 31) red[warp] = incl;
+  __syncthreads();
+  int before = 0, tot = 0;
+  for (int w = 0; w < kOrderThreads / 32; ++w) {
+    if (w < warp) before += red[w];
+    tot += red[w];
+  }
+  *total = tot;
+  return before + incl - x;
+}
+
+// One CTA ahead of the sampler: resets the scratch's counters, orders the rows by class
+// (stable, heaviest first; order[] holds row | phases << 24) and writes the work list.
+// List slot j holds the first phase of order[j], then the second phase of order[j - gap]
+// and the third of order[j - 2 gap] where those rows have them (slots j >= B hold only
+// those), so that a row's next phase comes about one wave of items after its previous
+// one.
+__global__ void __launch_bounds__(kOrderThreads) order_kernel(const __grid_constant__ LaunchParams P) {
+  __shared__ int red[kOrderThreads / 32];
   const clsample_args_t& a = P.a;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int rc = (int)blockIdx.x;  // row * C + slice
-  const int row = rc / P.C, slice = rc % P.C, c0 = slice * P.chunk;
-  const int len = max(0, min(a.V, c0 + P.chunk) - c0);
-  const int c1 = c0 + len;
-  const bool has_hist = a.hist_offs != nullptr;
-  const bool has_bias = a.bias_offs != nullptr;
+  const int B = a.B, tid = threadIdx.x;
+  for (int r = tid; r < B; r += kOrderThreads) {
+    reinterpret_cast<uint4*>(P.ticket)[r] = make_uint4(0u, 0u, 0u, 0u);
+    P.phase_done[r] = 0u;
+    P.bad[r] = 0u;
+  }
   if (tid == 0) {
-    csr[0] = has_hist ? a.hist_offs[row] : 0;
-    csr[1] = has_hist ? a.hist_offs[row + 1] : 0;
-    csr[2] = has_bias ? a.bias_offs[row] : 0;
-    csr[3] = has_bias ? a.bias_offs[row + 1] : 0;
-    flags_sh = 0;
-    if (slice == 0) P.row_class[row] = row_class(a, row);
+    P.ctl[0] = 0u;
+    P.ctl[1] = 0u;
   }
-  if (has_hist || has_bias) {
-    for (int i = tid; i < kHashCap; i += kPrepThreads) {
-      hkey[i] = kEmpty;
-      hcnt[i] = 0u;
-      hbias[i] = -1;
-    }
-    for (int w = tid; w < P.chunk / 32; w += kPrepThreads) mod[w] = 0u;
-  }
-  __syncthreads();
-
-  if (has_hist || has_bias) {
-    int flags = 0;
-    const int hlo = csr[0], hhi = csr[1], blo = csr[2], bhi = csr[3];
-    if (hlo < 0 || hhi < hlo || blo < 0 || bhi < blo) flags |= kFlagInvalid;
-    const bool hok = has_hist && hlo >= 0 && hhi >= hlo;
-    const bool bok = has_bias && blo >= 0 && bhi >= blo;
-    if (hok) {
-      for (int base = hlo; base < hhi; base += 16 * kPrepThreads) {
-        int ids[16];
+  // classes -> order: consecutive rows per thread, one scan per class
+  {
+    const int per = (B + kOrderThreads - 1) / kOrderThreads;
+    const int r0 = min(B, tid * per), r1 = min(B, r0 + per);
+    int cls[kOrderPer], nph[kOrderPer];
+    int cnt[kClasses] = {0, 0, 0, 0, 0};
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const int j = base + u * kPrepThreads + tid;
-          ids[u] = j < hhi ? __ldg(a.hist_ids + j) : INT_MIN;
-        }
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const int id = ids[u];
-          if (id != INT_MIN && (id < 0 || id >= a.V)) flags |= kFlagInvalid;
-          const bool mine = id >= c0 && id < c1;
-          const uint32_t peers = __match_any_sync(0xffffffffu, mine ? id : -1);
-          if (mine && lane == __ffs(peers) - 1)
-            flags |= count_id(hkey, hcnt, (uint32_t)(id - c0), (uint32_t)__popc(peers));
-        }
+    for (int u = 0; u < kOrderPer; ++u)
+      if (r0 + u < r1) {
+        row_info(a, r0 + u, &cls[u], &nph[u]);
+        ++cnt[cls[u]];
       }
+    for (int r = r0 + kOrderPer; r < r1; ++r) {
+      int c, n;
+      row_info(a, r, &c, &n);
+      ++cnt[c];
     }
-    // bias: the largest entry index per id wins (its value is read back at the end)
-    if (bok) {
-      for (int j = blo + tid; j < bhi; j += kPrepThreads) {
-        const int id = __ldg(a.bias_ids + j);
-        const float b = __ldg(a.bias_vals + j);
-        if (id < 0 || id >= a.V || b != b) {
-          flags |= kFlagInvalid;
-        } else if (id >= c0 && id < c1) {
-          const int slot = hash_insert(hkey, (uint32_t)(id - c0));
-          if (slot < 0) flags |= kFlagOverflow;
-          else atomicMax(&hbias[slot], j);
-        }
-      }
-    }
-    if (flags) atomicOr(&flags_sh, flags);
-    __syncthreads();
-    for (int i = tid; i < kHashCap; i += kPrepThreads) {
-      const uint32_t l = hkey[i];
-      if (l != kEmpty) atomicOr(&mod[l >> 5], 1u << (l & 31));
-    }
-    __syncthreads();
-    // rank of every id = ids below it: an exclusive scan of the words' popcounts
-    constexpr int kPer = (kMaxChunk / 32) / kPrepThreads;
-    const int nw = P.chunk / 32;
-    int cnt[kPer], loc = 0;
+    int base[kClasses], start = 0;
 #pragma unroll
-    for (int t = 0; t < kPer; ++t) {
-      const int w = tid * kPer + t;
-      cnt[t] = w < nw ? __popc(mod[w]) : 0;
-      loc += cnt[t];
+    for (int c = 0; c < kClasses; ++c) {
+      int tot;
+      base[c] = order_scan(cnt[c], red, &tot) + start;
+      start += tot;
     }
-    int x = loc;
 #pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int o = __shfl_up_sync(0xffffffffu, x, d);
-      if (lane >= d) x += o;
-    }
-    if (lane == 31) red[warp] = x;
-    __syncthreads();
-    int total = 0, before = 0;
-    for (int w = 0; w < kPrepWarps; ++w) {
-      total += red[w];
-      if (w < warp) before += red[w];
-    }
-    int e = before + x - loc;
-#pragma unroll
-    for (int t = 0; t < kPer; ++t) {
-      const int w = tid * kPer + t;
-      if (w < nw) wbase[w] = (uint16_t)e;
-      e += cnt[t];
-    }
-    __syncthreads();
-    PenEntry* out = P.pen + (size_t)rc * kPenCap;
-    for (int i = tid; i < kHashCap; i += kPrepThreads) {
-      const uint32_t l = hkey[i];
-      if (l == kEmpty) continue;
-      const int r = wbase[l >> 5] + __popc(mod[l >> 5] & ((1u << (l & 31)) - 1u));
-      if (r >= kPenCap) continue;
-      PenEntry en;
-      const int bj = hbias[i];
-      en.id = l | (bj >= 0 ? kPenBias : 0u);
-      en.count = min(hcnt[i], kCountMask);
-      en.bias = bj >= 0 ? __ldg(a.bias_vals + bj) : 0.0f;
-      en.pad = 0u;
-      out[r] = en;
-    }
-    if (tid == 0) {
-      int f = flags_sh;
-      if (total > kPenCap) f |= kFlagOverflow;
-      P.pen_n[rc] = make_int2(min(total, kPenCap), f);
+    for (int u = 0; u < kOrderPer; ++u)
+      if (r0 + u < r1) P.order[base[cls[u]]++] = (r0 + u) | (nph[u] << 24);
+    for (int r = r0 + kOrderPer; r < r1; ++r) {
+      int c, n;
+      row_info(a, r, &c, &n);
+      P.order[base[c]++] = r | (n << 24);
     }
   }
-
-  // the launch order, by the CTA that finishes last
-  __threadfence();
+  __threadfence_block();
   __syncthreads();
-  if (tid == 0) last_sh = atomicAdd(P.ticket, 1u) == gridDim.x - 1 ? 1 : 0;
-  __syncthreads();
-  if (!last_sh) return;
-  __threadfence();
-  const int B = a.B;
-  const int per = (B + kPrepThreads - 1) / kPrepThreads;  // consecutive rows per thread
-  const int r0 = min(B, tid * per), r1 = min(B, r0 + per);
-  int cnt[kClasses] = {0, 0, 0, 0, 0};
-  for (int r = r0; r < r1; ++r) ++cnt[__ldcg(P.row_class + r)];
-  // exclusive scan over threads, per class; then class offsets
-  int base[kClasses];
-  int cls_total[kClasses];
-#pragma unroll
-  for (int c = 0; c < kClasses; ++c) {
-    int x = cnt[c];
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int o = __shfl_up_sync(0xffffffffu, x, d);
-      if (lane >= d) x += o;
+  // the work list
+  const int G = P.gap;
+  const int J = B + 2 * G;
+  const int per = (J + kOrderThreads - 1) / kOrderThreads;
+  const int j0 = min(J, tid * per), j1 = min(J, j0 + per);
+  auto entries = [&](int j, unsigned* out) -> int {
+    int n = 0;
+    const int o1 = j < B ? __ldcg(P.order + j) : -1;
+    const int o2 = (j - G >= 0 && j - G < B) ? __ldcg(P.order + j - G) : -1;
+    const int o3 = (j - 2 * G >= 0 && j - 2 * G < B) ? __ldcg(P.order + j - 2 * G) : -1;
+    if (o1 >= 0) {
+      if (out) out[n] = ((unsigned)o1 & 0xFFFFFFu) | (1u << 24) | ((unsigned)(o1 >> 24) << 28);
+      ++n;
     }
-    if (lane == 31) red[warp * kClasses + c] = x;
-    base[c] = x - cnt[c];
-  }
-  __syncthreads();
-#pragma unroll
-  for (int c = 0; c < kClasses; ++c) {
-    int tot = 0;
-    for (int w = 0; w < kPrepWarps; ++w) {
-      if (w < warp) base[c] += red[w * kClasses + c];
-      tot += red[w * kClasses + c];
+    if (o2 >= 0 && (o2 >> 24) >= 2) {
+      if (out) out[n] = ((unsigned)o2 & 0xFFFFFFu) | (2u << 24) | ((unsigned)(o2 >> 24) << 28);
+      ++n;
     }
-    cls_total[c] = tot;
+    if (o3 >= 0 && (o3 >> 24) >= 3) {
+      if (out) out[n] = ((unsigned)o3 & 0xFFFFFFu) | (3u << 24) | ((unsigned)(o3 >> 24) << 28);
+      ++n;
+    }
+    return n;
+  };
+  int mine = 0;
+  for (int j = j0; j < j1; ++j) mine += entries(j, nullptr);
+  int total;
+  int pos = order_scan(mine, red, &total);
+  for (int j = j0; j < j1; ++j) {
+    unsigned e[3];
+    const int n = entries(j, e);
+    for (int i = 0; i < n; ++i) P.seg[pos++] = e[i];
   }
-  int start = 0;
-#pragma unroll
-  for (int c = 0; c < kClasses; ++c) {
-    base[c] += start;
-    start += cls_total[c];
-  }
-  for (int r = r0; r < r1; ++r) P.row_order[base[__ldcg(P.row_class + r)]++] = r;
-  if (tid == 0) *P.ticket = 0u;  // ready for the next call on this stream
+  if (tid == 0) P.ctl[2] = (unsigned)total;
 }
 
-// ---------------------------------------------------------------- prologue
+// ---------------------------------------------------------------- first phase: setup
 
-// Row parameters, the slice's live bits (bitmask words clipped to the row) and its
-// penalised / biased tokens from the penalty kernel's list (sorted by id, so an entry's
-// index is the token's rank); the bitmask's verdict on each moves into its entry.  The
-// first ring stages of pass A are issued before anything else, so the slice is on its
-// way while the small inputs arrive.
+// Row parameters and their validity.
+__device__ __forceinline__ RowParams load_params(const clsample_args_t& a, int row) {
+  RowParams q;
+  q.T = a.temperatures ? a.temperatures[row] : 1.0f;
+  q.k = a.top_ks ? a.top_ks[row] : -1;
+  q.p = a.top_ps ? a.top_ps[row] : 1.0f;
+  q.mp = a.min_ps ? a.min_ps[row] : 0.0f;
+  q.rep = a.rep ? a.rep[row] : 1.0f;
+  q.freq = a.freq ? a.freq[row] : 0.0f;
+  q.pres = a.pres ? a.pres[row] : 0.0f;
+  q.seed = a.seeds ? (unsigned long long)a.seeds[row] : 0ull;
+  q.pos = (unsigned long long)(a.positions ? a.positions[row] : a.step);
+  int bad = 0;
+  bad |= (q.T != q.T) || (q.T == INFINITY);
+  bad |= (q.k < -1);
+  bad |= !(q.p > 0.0f && q.p <= 1.0f);
+  bad |= !(q.mp >= 0.0f && q.mp <= 1.0f);
+  bad |= !(q.rep > 0.0f) || (q.rep == INFINITY) || !isfinite(q.freq) || !isfinite(q.pres);
+  q.invalid = bad;
+  return q;
+}
+
+__device__ __forceinline__ bool params_greedy(const RowParams& q) {
+  return (q.T < kGreedyEps) || q.k == 0 || q.k == 1;
+}
+
+// Exclusive scan of the mod words' popcounts into prank (token-order rank of each word's
+// first penalised token); returns the total in every thread.
+__device__ int rank_words(const Smem& S, int nw) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int kPer = (kMaxChunk / 32) / kThreads;
+  int cnt[kPer], loc = 0;
+#pragma unroll
+  for (int t = 0; t < kPer; ++t) {
+    const int w = tid * kPer + t;
+    cnt[t] = w < nw ? __popc(S.mod[w]) : 0;
+    loc += cnt[t];
+  }
+  int x = loc;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, x, d);
+    if (lane >= d) x += o;
+  }
+  if (lane == 31) sh.red_i[warp] = x;
+  __syncthreads();
+  int excl = x - loc, total = 0;
+  for (int w = 0; w < kWarps; ++w) {
+    if (w < warp) excl += sh.red_i[w];
+    total += sh.red_i[w];
+  }
+#pragma unroll
+  for (int t = 0; t < kPer; ++t) {
+    const int w = tid * kPer + t;
+    if (w < nw) S.prank[w] = (uint16_t)excl;
+    excl += cnt[t];
+  }
+  __syncthreads();
+  return total;
+}
+
+// First phase of a slice, before pass A: thread 0 starts the slice's first ring stages,
+// then the row parameters, the live bits (bitmask words clipped to the row) and the
+// slice's penalised / biased tokens: the row's history and logit_bias ids that fall in
+// the slice are marked in `mod` (SGLang page, "Order semantics of the penalties" and
+// "Why logit_bias is built from triples") while the history's in-slice ids are compacted
+// into r2; a scan ranks the marked ids in token order, then every compacted id adds one
+// to its rank's count (a history whose in-slice ids overflow r2 is read a second time)
+// and every bias entry leaves its index, so that the last one wins.  The bitmask's
+// verdict on each listed token moves into its entry and the token leaves the live set
+// (pass A gives it its final value).  A slice with more than kPenCap distinct ids is
+// flagged OVERFLOW.
 template <bool kBF16>
-__device__ __noinline__ void prologue(const LaunchParams& P) {
-  const Geo g = geo<kBF16>(P);
+__device__ __noinline__ void setup_p1(const LaunchParams& P, int row, int slice, int nph) {
+  const Geo g = geo<kBF16>(P, row, slice);
   const Smem S = carve(g.chunk);
   const clsample_args_t& a = P.a;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int row = g.row, c0 = g.c0, len = g.len;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int c0 = g.c0, c1 = g.c0 + g.len, nw = g.chunk / 32;
   const int32_t* bmrow = a.bitmask ? a.bitmask + (long long)row * a.bitmask_row_stride : nullptr;
-  const bool has_mod = a.hist_offs != nullptr || a.bias_offs != nullptr;
-  const int rc = row * g.C + g.rank;
+  const bool has_hist = a.hist_offs != nullptr, has_bias = a.bias_offs != nullptr;
+  int* pbidx = reinterpret_cast<int*>(S.pbias);
+  uint16_t* hbuf = reinterpret_cast<uint16_t*>(S.r2);  // the history's in-slice ids
+  constexpr int kHbufCap = (int)(kR2Bytes / sizeof(uint16_t));
 
   if (tid == 0) {
     sh.flags = 0;
     sh.count = 0;
     sh.nallowed = 0;
-    for (int i = 0; i < kStages; ++i) mbar_init(&sh.full[i], 1);
-    fence_mbar_init();
-    ring_start<kBF16>(g, S, 0);
+    sh.npen = 0;
+    sh.nhist = 0;
+    // a row that later phases read again whole keeps its lines in L2; the others are
+    // read once (the row end re-reads a few vectors) and go first when L2 needs room, so
+    // that the slice records, lists and tables the row ends read stay in L2
+    sh.policy = nph >= 2 ? make_policy_evict_normal() : make_policy_evict_first();
+    ring_start<kBF16>(g, S, sh.seq);
   } else if (tid == 32) {
-    RowParams q;
-    q.T = a.temperatures ? a.temperatures[row] : 1.0f;
-    q.k = a.top_ks ? a.top_ks[row] : -1;
-    q.p = a.top_ps ? a.top_ps[row] : 1.0f;
-    q.mp = a.min_ps ? a.min_ps[row] : 0.0f;
-    q.rep = a.rep ? a.rep[row] : 1.0f;
-    q.freq = a.freq ? a.freq[row] : 0.0f;
-    q.pres = a.pres ? a.pres[row] : 0.0f;
-    q.seed = a.seeds ? (unsigned long long)a.seeds[row] : 0ull;
-    q.pos = (unsigned long long)(a.positions ? a.positions[row] : a.step);
-    int bad = 0;
-    bad |= (q.T != q.T) || (q.T == INFINITY);
-    bad |= (q.k < -1);
-    bad |= !(q.p > 0.0f && q.p <= 1.0f);
-    bad |= !(q.mp >= 0.0f && q.mp <= 1.0f);
-    bad |= !(q.rep > 0.0f) || (q.rep == INFINITY) || !isfinite(q.freq) || !isfinite(q.pres);
-    q.invalid = bad;
-    sh.rp = q;
+    sh.rp = load_params(a, row);
   } else if (tid == 64) {
-    const int2 nf = has_mod ? P.pen_n[rc] : make_int2(0, 0);
-    sh.npen = nf.x;
-    sh.csr[0] = nf.y;  // the penalty kernel's flags
+    sh.csr[0] = has_hist ? a.hist_offs[row] : 0;
+    sh.csr[1] = has_hist ? a.hist_offs[row + 1] : 0;
+    sh.csr[2] = has_bias ? a.bias_offs[row] : 0;
+    sh.csr[3] = has_bias ? a.bias_offs[row + 1] : 0;
   }
-  // the list is loaded whole (its length arrives with it): two entries per thread
-  PenEntry en[kPenCap / kThreads];
-  if (has_mod) {
-#pragma unroll
-    for (int t = 0; t < kPenCap / kThreads; ++t) en[t] = P.pen[(size_t)rc * kPenCap + t * kThreads + tid];
-  }
-  for (int w = tid; w < g.chunk / 32; w += kThreads) {
-    const int e = 32 * w;
-    uint32_t word = 0u;
-    if (e < len) {
-      word = bmrow ? (uint32_t)__ldg(bmrow + (c0 >> 5) + w) : 0xFFFFFFFFu;
-      const int rem = len - e;
-      if (rem < 32) word &= (1u << rem) - 1u;
-    }
-    S.live[w] = word;
+  for (int w = tid; w < nw; w += kThreads) {
+    S.live[w] = mask_word(bmrow, c0, g.len, w);
     S.mod[w] = 0u;
   }
-  S.mrg_c[tid] = 0u;  // merged histograms peers add into (top-p bins, top-k refinement)
+  for (int r = tid; r < kPenCap; r += kThreads) {
+    S.pcnt[r] = 0u;
+    pbidx[r] = -1;
+  }
   __syncthreads();
-  if (!has_mod) {
+  if (!has_hist && !has_bias) {
     int na = 0;
-    for (int w = tid; w < g.chunk / 32; w += kThreads) na += __popc(S.live[w]);
+    for (int w = tid; w < nw; w += kThreads) na += __popc(S.live[w]);
     na = __reduce_add_sync(0xffffffffu, na);
     if (lane == 0 && na) atomicAdd(&sh.nallowed, na);
+    __syncthreads();
     return;
   }
-  const int npen = sh.npen;
-  if (tid == 0 && sh.csr[0]) sh.flags |= sh.csr[0];
-  // the bitmask's verdict on each penalised token moves into its entry; the token
-  // leaves the live set (pass A gives it its final value)
+  int flags = 0;
+  const int hlo = sh.csr[0], hhi = sh.csr[1], blo = sh.csr[2], bhi = sh.csr[3];
+  if (hlo < 0 || hhi < hlo || blo < 0 || bhi < blo) flags |= kFlagInvalid;
+  const bool hok = has_hist && hlo >= 0 && hhi >= hlo;
+  const bool bok = has_bias && blo >= 0 && bhi >= blo;
+  if (hok) {
+#pragma unroll 1
+    for (int base = hlo; base < hhi; base += 16 * kThreads) {
+      int ids[16];
 #pragma unroll
-  for (int t = 0; t < kPenCap / kThreads; ++t) {
-    const int r = t * kThreads + tid;
-    if (r >= npen) continue;
-    const uint32_t l = en[t].id & ~kPenBias;
-    const uint32_t bit = 1u << (l & 31);
-    uint32_t c = en[t].count & kCountMask;
-    if (en[t].id & kPenBias) c |= kBiasBit;
-    if (S.live[l >> 5] & bit) c |= kAllowedBit;
-    S.pid[r] = (uint16_t)l;
-    S.pcnt[r] = c;
-    S.pbias[r] = en[t].bias;
-    atomicAnd(&S.live[l >> 5], ~bit);
-    atomicOr(&S.mod[l >> 5], bit);
+      for (int u = 0; u < 16; ++u) {
+        const int j = base + u * kThreads + tid;
+        ids[u] = j < hhi ? __ldg(a.hist_ids + j) : INT_MIN;
+      }
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int id = ids[u];
+        if (id != INT_MIN && (id < 0 || id >= a.V)) flags |= kFlagInvalid;
+        const bool mine = id >= c0 && id < c1;
+        const uint32_t l = mine ? (uint32_t)(id - c0) : 0u;
+        if (mine) {
+          const uint32_t bit = 1u << (l & 31);
+          if (!(S.mod[l >> 5] & bit)) atomicOr(&S.mod[l >> 5], bit);
+        }
+        const uint32_t bal = __ballot_sync(0xffffffffu, mine);
+        if (bal) {
+          const int leader = __ffs(bal) - 1;
+          int pos = 0;
+          if (lane == leader) pos = atomicAdd(&sh.nhist, __popc(bal));
+          pos = __shfl_sync(0xffffffffu, pos, leader) + __popc(bal & ((1u << lane) - 1u));
+          if (mine && pos < kHbufCap) hbuf[pos] = (uint16_t)l;
+        }
+      }
+    }
+  }
+  if (bok) {
+    for (int j = blo + tid; j < bhi; j += kThreads) {
+      const int id = __ldg(a.bias_ids + j);
+      const float b = __ldg(a.bias_vals + j);
+      if (id < 0 || id >= a.V || b != b) {
+        flags |= kFlagInvalid;
+      } else if (id >= c0 && id < c1) {
+        const uint32_t l = (uint32_t)(id - c0);
+        atomicOr(&S.mod[l >> 5], 1u << (l & 31));
+      }
+    }
+  }
+  if (flags) atomicOr(&sh.flags, flags);
+  __syncthreads();
+  const int total = rank_words(S, nw);
+  const int npen = min(total, kPenCap);
+  if (tid == 0) {
+    sh.npen = npen;
+    if (total > kPenCap) sh.flags |= kFlagOverflow;
+  }
+  // the listed ids in token order
+  for (int w = tid; w < nw; w += kThreads) {
+    uint32_t bits = S.mod[w];
+    int r = S.prank[w];
+    while (bits && r < kPenCap) {
+      const int b = __ffs(bits) - 1;
+      bits &= bits - 1u;
+      S.pid[r++] = (uint16_t)(32 * w + b);
+    }
+  }
+  auto rank_of = [&](uint32_t l) -> int {
+    return S.prank[l >> 5] + __popc(S.mod[l >> 5] & ((1u << (l & 31)) - 1u));
+  };
+  const int nhist = sh.nhist;
+  if (nhist <= kHbufCap) {
+    for (int i = tid; i < nhist; i += kThreads) {
+      const int r = rank_of(hbuf[i]);
+      if (r < kPenCap) atomicAdd(&S.pcnt[r], 1u);
+    }
+  } else if (hok) {
+    for (int j = hlo + tid; j < hhi; j += kThreads) {
+      const int id = __ldg(a.hist_ids + j);
+      if (id >= c0 && id < c1) {
+        const int r = rank_of((uint32_t)(id - c0));
+        if (r < kPenCap) atomicAdd(&S.pcnt[r], 1u);
+      }
+    }
+  }
+  if (bok) {
+    for (int j = blo + tid; j < bhi; j += kThreads) {
+      const int id = __ldg(a.bias_ids + j);
+      const float b = __ldg(a.bias_vals + j);
+      if (id >= c0 && id < c1 && b == b) {
+        const int r = rank_of((uint32_t)(id - c0));
+        if (r < kPenCap) atomicMax(&pbidx[r], j);
+      }
+    }
   }
   __syncthreads();
-  // token-order rank of each mod word's first token: an exclusive scan of the popcounts
-  {
-    constexpr int kPer = (kMaxChunk / 32) / kThreads;
-    const int nw = g.chunk / 32;
-    int cnt[kPer], loc = 0;
-#pragma unroll
-    for (int t = 0; t < kPer; ++t) {
-      const int w = tid * kPer + t;
-      cnt[t] = w < nw ? __popc(S.mod[w]) : 0;
-      loc += cnt[t];
+  // the bitmask's verdict and the bias value move into each entry; the token leaves the
+  // live set
+  for (int r = tid; r < npen; r += kThreads) {
+    const uint32_t l = S.pid[r], bit = 1u << (l & 31);
+    uint32_t c = min(S.pcnt[r], kCountMask);
+    const int bj = pbidx[r];
+    if (bj >= 0) {
+      c |= kBiasBit;
+      S.pbias[r] = __ldg(a.bias_vals + bj);
     }
-    int x = loc;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int o = __shfl_up_sync(0xffffffffu, x, d);
-      if (lane >= d) x += o;
-    }
-    if (lane == 31) sh.red_i[warp] = x;
-    __syncthreads();
-    int excl = x - loc;
-    for (int w = 0; w < warp; ++w) excl += sh.red_i[w];
-#pragma unroll
-    for (int t = 0; t < kPer; ++t) {
-      const int w = tid * kPer + t;
-      if (w < nw) S.prank[w] = (uint16_t)excl;
-      excl += cnt[t];
-    }
+    if (S.live[l >> 5] & bit) c |= kAllowedBit;
+    S.pcnt[r] = c;
+    atomicAnd(&S.live[l >> 5], ~bit);
   }
-  // allowed tokens of the slice: plain live ones plus allowed penalised ones
+  __syncthreads();
   {
     int na = 0;
-    for (int w = tid; w < g.chunk / 32; w += kThreads) na += __popc(S.live[w]);
+    for (int w = tid; w < nw; w += kThreads) na += __popc(S.live[w]);
     for (int r = tid; r < npen; r += kThreads) na += (S.pcnt[r] & kAllowedBit) ? 1 : 0;
     na = __reduce_add_sync(0xffffffffu, na);
     if (lane == 0 && na) atomicAdd(&sh.nallowed, na);
@@ -1122,22 +1191,23 @@ __device__ __noinline__ void prologue(const LaunchParams& P) {
 // ---------------------------------------------------------------- pass A
 
 // Pass A: slice max, lowest argmax and online sum of 2^((z' - max) cS), cS = log2(e)/T_eff;
-// per-warp lower bounds of the top-k cut from the per-thread maxima.  Leaves the slice
-// record in sh.x1_mine.
+// per-warp lower bounds of the top-k cut from the per-thread maxima; the table of
+// per-(stage, thread) maxima in r2.  Leaves the slice record in sh.x1_mine.
 template <bool kBF16>
-__device__ __noinline__ void pass_a(const LaunchParams& P) {
-  const Geo g = geo<kBF16>(P);
+__device__ __noinline__ void pass_a(const LaunchParams& P, int row, int slice) {
+  const Geo g = geo<kBF16>(P, row, slice);
   const Smem S = carve(g.chunk);
   const clsample_args_t& a = P.a;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const RowParams q = sh.rp;
   const bool has_mod = a.hist_offs != nullptr || a.bias_offs != nullptr;
-  const bool greedy = (q.T < kGreedyEps) || q.k == 0 || q.k == 1;
+  const bool greedy = params_greedy(q);
   const float Teff = (q.T >= kGreedyEps) ? q.T : 1.0f;
   const float cS = 1.4426950408889634f / Teff;
   const int c0 = g.c0;
   constexpr int kGroups = kStageBytes / (4 * (kBF16 ? 2 : 4)) / kThreads;  // vectors per thread per stage
-  static_assert(kGroups <= 4, "red_j holds four group sets per warp");
+  static_assert(kGroups <= 4, "four group sets per warp at most");
+  uint16_t* tab = reinterpret_cast<uint16_t*>(S.r2);
 
   // the thread's online state; a thread visits its tokens in increasing order, so the
   // first token reaching the running max is the lowest
@@ -1148,39 +1218,52 @@ __device__ __noinline__ void pass_a(const LaunchParams& P) {
   float gm[kGroups];
 #pragma unroll
   for (int t = 0; t < kGroups; ++t) gm[t] = -INFINITY;
-  int pass = 0;
-  stream<kBF16, true>(g, S, pass, true, [&](int f, uint32_t wd, const float4& v, int t) {
-    if (has_mod && 4 * f < g.len) {
-      // penalised / biased tokens: keep the raw logit (rank order) for the fold below
-      const uint32_t mw = S.mod[f >> 3];
-      const int sh4 = (f & 7) * 4;
-      const uint32_t md = (mw >> sh4) & 0xFu;
-      if (md) {
-        int r = S.prank[f >> 3] + __popc(mw & ((1u << sh4) - 1u));
+  float tmax = -INFINITY;  // this stage's maximum (table)
+  bool tany = false;
+  stream_ring<kBF16>(
+      g, S,
+      [&](int t, int f, uint32_t wd, const float4& v) {
+        if (has_mod && 4 * f < g.len) {
+          // penalised / biased tokens: keep the raw logit (rank order) for the fold below
+          const uint32_t mw = S.mod[f >> 3];
+          const int sh4 = (f & 7) * 4;
+          const uint32_t md = (mw >> sh4) & 0xFu;
+          if (md) {
+            int r = S.prank[f >> 3] + __popc(mw & ((1u << sh4) - 1u));
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if ((md >> j) & 1u) S.pz[r++] = comp(v, j);
-      }
-    }
-    if (!wd) return;
-    float4 z = v;
-    if (!(wd == 0xFu && finite4(v)))
-      z = make_float4((wd & 1u) ? sanitize(v.x) : -INFINITY, (wd & 2u) ? sanitize(v.y) : -INFINITY,
-                      (wd & 4u) ? sanitize(v.z) : -INFINITY, (wd & 8u) ? sanitize(v.w) : -INFINITY);
-    const float fm = fmaxf(fmaxf(z.x, z.y), fmaxf(z.z, z.w));
-    if (!(fm > -INFINITY)) return;
-    gm[t] = fmaxf(gm[t], fm);
-    if (fm > sm) {
-      ss *= ex2_approx((sm - fm) * cS);
-      sm = fm;
-      targ = c0 + 4 * f + (z.x == fm ? 0 : z.y == fm ? 1 : z.z == fm ? 2 : 3);
-    }
-    const float e0 = ex2_approx((z.x - sm) * cS), e1 = ex2_approx((z.y - sm) * cS);
-    const float e2 = ex2_approx((z.z - sm) * cS), e3 = ex2_approx((z.w - sm) * cS);
-    ss += (e0 + e1) + (e2 + e3);
-  });
+            for (int j = 0; j < 4; ++j)
+              if ((md >> j) & 1u) {
+                if (r < kPenCap) S.pz[r] = comp(v, j);
+                ++r;
+              }
+          }
+        }
+        if (!wd) return;
+        float4 z = v;
+        if (!(wd == 0xFu && finite4(v)))
+          z = make_float4((wd & 1u) ? sanitize(v.x) : -INFINITY, (wd & 2u) ? sanitize(v.y) : -INFINITY,
+                          (wd & 4u) ? sanitize(v.z) : -INFINITY, (wd & 8u) ? sanitize(v.w) : -INFINITY);
+        const float fm = fmaxf(fmaxf(z.x, z.y), fmaxf(z.z, z.w));
+        tany = true;
+        tmax = fmaxf(tmax, fm);
+        if (!(fm > -INFINITY)) return;
+        gm[t] = fmaxf(gm[t], fm);
+        if (fm > sm) {
+          ss *= ex2_approx((sm - fm) * cS);
+          sm = fm;
+          targ = c0 + 4 * f + (z.x == fm ? 0 : z.y == fm ? 1 : z.z == fm ? 2 : 3);
+        }
+        const float e0 = ex2_approx((z.x - sm) * cS), e1 = ex2_approx((z.y - sm) * cS);
+        const float e2 = ex2_approx((z.z - sm) * cS), e3 = ex2_approx((z.w - sm) * cS);
+        ss += (e0 + e1) + (e2 + e3);
+      },
+      [&](int k) {
+        tab[k * kThreads + tid] = tab_entry(tany, tmax);
+        tany = false;
+        tmax = -INFINITY;
+      });
   // the penalised / biased tokens in token order: penalties, then bias, on the sanitised
-  // raw logit (the mask applies to them too); the final z' goes into the hash and into
+  // raw logit (the mask applies to them too); the final z' replaces the raw one and joins
   // the thread's online state
   if (has_mod) {
     const int npen = sh.npen;
@@ -1252,8 +1335,8 @@ __device__ __noinline__ void pass_a(const LaunchParams& P) {
     sh.red_i[warp * 2] = a2;
     sh.red_wb[warp * 2] = wlk;
   }
-  // per group set, in r2 (free until exchange 1; the top-p merged bins are not touched)
-  float(*red_j)[kNJ] = reinterpret_cast<float(*)[kNJ]>(S.r2);
+  // per group set, in the ring (free after the stream)
+  float(*red_j)[kNJ] = reinterpret_cast<float(*)[kNJ]>(S.ring);
 #pragma unroll
   for (int t = 0; t < kGroups; ++t)
     if (lane < kNJ) red_j[warp * kGroups + t][lane] = wlj[t];
@@ -1294,10 +1377,12 @@ __device__ __noinline__ void pass_a(const LaunchParams& P) {
       sh.x1_mine.lk = lk;
       sh.x1_mine.flags = sh.flags;
       sh.x1_mine.nallowed = sh.nallowed;
+      sh.x1_mine.npen = has_mod ? sh.npen : 0;
+      sh.x1_mine.tab = P.vec_ok;
     }
   }
   // the transformed logits, on request (debugging aid): plain values first, then the
-  // penalised / biased tokens' final z' from the hash
+  // penalised / biased tokens' final z'
   if (a.dbg_transformed) {
     float* out = a.dbg_transformed + (long long)g.row * a.V + c0;
     const int32_t* bmrow = a.bitmask ? a.bitmask + (long long)g.row * a.bitmask_row_stride : nullptr;
@@ -1313,23 +1398,57 @@ __device__ __noinline__ void pass_a(const LaunchParams& P) {
   __syncthreads();
 }
 
-// ---------------------------------------------------------------- exchange 1
+// End of a first-phase item: the slice record, its penalised tokens (local id and final
+// z', token order) and its table go to the scratch, then the row's ticket.  Returns true
+// in every thread of the CTA that finished the row's last slice (the phase's ticket is
+// reset for the next call).
+template <bool kBF16>
+__device__ __noinline__ bool publish_p1(const LaunchParams& P, int row, int slice) {
+  const Geo g = geo<kBF16>(P, row, slice);
+  const Smem S = carve(g.chunk);
+  const int tid = threadIdx.x;
+  const size_t idx = (size_t)row * P.C + slice;
+  const RowParams q = sh.rp;
+  const bool sampling = !params_greedy(q) && !q.invalid;  // only sampling rows read lists and tables again
+  if (tid == 0) P.x1[idx] = sh.x1_mine;
+  if (sampling) {
+    const int npen = sh.x1_mine.npen;
+    uint2* pl = P.pen + idx * kPenCap;
+    for (int r = tid; r < npen; r += kThreads) pl[r] = make_uint2(S.pid[r], __float_as_uint(S.pz[r]));
+    if (P.vec_ok && g.nst > 0) {
+      const uint4* src = reinterpret_cast<const uint4*>(S.r2);
+      uint4* dst = reinterpret_cast<uint4*>(P.tab + idx * kTabMax);
+      const int n16 = g.nst * kThreads * (int)sizeof(uint16_t) / 16;
+      for (int i = tid; i < n16; i += kThreads) dst[i] = src[i];
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const bool last = atomicAdd(P.ticket + 4 * row + 1, 1u) == (unsigned)P.C - 1u;
+    if (last) P.ticket[4 * row + 1] = 0u;
+    sh.last = last ? 1 : 0;
+  }
+  __syncthreads();
+  if (!sh.last) return false;
+  __threadfence();
+  return true;
+}
 
-// Every CTA pushes its slice record into every CTA (DSMEM) and one cluster barrier
-// publishes them; every CTA then combines them in the same order into sh.rs.
-__device__ __noinline__ void exchange1(const LaunchParams& P) {
-  const cg::cluster_group cluster = cg::this_cluster();
+// ---------------------------------------------------------------- row end: combine and plan
+
+// The last arriver of a row's first phase: the C slice records, combined in slice order
+// (every float sum in a fixed order) into sh.rs.  The top-k bound is the larger of the
+// warps' k-th largest thread maxima and, for each j = 2^i whose group sets guarantee k
+// tokens (n * j >= k), the minimum over those sets of their j-th largest maximum.
+__device__ __noinline__ void combine_row(const LaunchParams& P, int row) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int C = P.C;
-  const int rank = (int)cluster.block_rank();
   const RowParams q = sh.rp;
   const float Teff = (q.T >= kGreedyEps) ? q.T : 1.0f;
   const float cS = 1.4426950408889634f / Teff;
-  // DSMEM may only be touched once every CTA of the cluster runs (the kernel arrived on
-  // the cluster barrier at entry)
-  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-  push_all(cluster, sh.x1, &sh.x1_mine, rank, C);
-  cluster.sync();
+  if (tid < C) ldcg_copy(&sh.x1[tid], P.x1 + (size_t)row * C + tid);
+  __syncthreads();
   if (warp == 0) {
     const bool in = lane < C;
     const float lm = in ? sh.x1[lane].m : -INFINITY;
@@ -1338,10 +1457,11 @@ __device__ __noinline__ void exchange1(const LaunchParams& P) {
     int fl = in ? sh.x1[lane].flags : 0;
     float lk = in ? sh.x1[lane].lk : -INFINITY;
     int nal = in ? sh.x1[lane].nallowed : 0;
+    const int nsum = __reduce_add_sync(0xffffffffu, nal);
     float m = lm;
 #pragma unroll
     for (int d = 4; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
-    m = __shfl_sync(0xffffffffu, m, 0);  // lanes >= C may hold their own partial maxima
+    m = __shfl_sync(0xffffffffu, m, 0);  // lanes >= 8 may hold their own partial maxima
     int arg = (in && lm == m) ? la : INT_MAX;
     const float term = (in && lm > -INFINITY) ? ls * ex2_approx((lm - m) * cS) : 0.0f;
 #pragma unroll
@@ -1351,7 +1471,6 @@ __device__ __noinline__ void exchange1(const LaunchParams& P) {
       lk = fmaxf(lk, __shfl_xor_sync(0xffffffffu, lk, d));
       nal = max(nal, __shfl_xor_sync(0xffffffffu, nal, d));
     }
-    // the 2^i bounds: lane i combines the CTAs; usable when its warps guarantee k tokens
     float bj = -INFINITY;
     if (lane < kNJ) {
       float lj = INFINITY;
@@ -1360,13 +1479,13 @@ __device__ __noinline__ void exchange1(const LaunchParams& P) {
         lj = fminf(lj, sh.x1[c].lj[lane]);
         n += sh.x1[c].nj[lane];
       }
-      if (n > 0 && (unsigned long long)n << lane >= (unsigned long long)max(sh.rp.k, 0)) bj = lj;
+      if (n > 0 && (unsigned long long)n << lane >= (unsigned long long)max(q.k, 0)) bj = lj;
     }
     for (int d = 4; d > 0; d >>= 1) bj = fmaxf(bj, __shfl_xor_sync(0xffffffffu, bj, d));
-    // the sum in a fixed order (ranks 0 .. C-1): every CTA gets the same bits
+    // the sum in a fixed order (slices 0 .. C-1)
     float tot = 0.0f;
 #pragma unroll
-    for (int r = 0; r < kMaxCluster; ++r) tot += __shfl_sync(0xffffffffu, term, r);
+    for (int r = 0; r < kMaxSlices; ++r) tot += __shfl_sync(0xffffffffu, term, r);
     if (lane == 0) {
       sh.rs.m = m;
       sh.rs.arg = arg;
@@ -1374,27 +1493,25 @@ __device__ __noinline__ void exchange1(const LaunchParams& P) {
       sh.rs.flags = fl;
       sh.rs.bound = fmaxf(lk, bj);
       sh.rs.nallowed_max = nal;
+      sh.rs.nallowed_sum = nsum;
       sh.rs.lnS = logf(tot);
     }
   }
   __syncthreads();
 }
-// ---------------------------------------------------------------- row end and plan
 
-// Greedy, INVALID and OVERFLOW rows end after exchange 1; rank 0 writes the argmax (its
-// y is 0, so its logprob is -ln S).  Returns true (in every thread) if the row ended.
-__device__ __noinline__ bool finish_early(const LaunchParams& P) {
+// Greedy, INVALID and OVERFLOW rows end after the first phase: the argmax (its y is 0,
+// so its logprob is -ln S).  Returns true (in every thread) if the row ended.
+__device__ __noinline__ bool finish_early(const LaunchParams& P, int row) {
   const RowParams q = sh.rp;
   const float m = sh.rs.m;
   const int fl = sh.rs.flags;
   int status = kRowOk;
   if (q.invalid || (fl & kFlagInvalid) || !(m > -INFINITY)) status = kRowInvalid;
   else if (fl & (kFlagOverflow | kFlagRing)) status = kRowOverflow;
-  const bool greedy = (q.T < kGreedyEps) || q.k == 0 || q.k == 1;
-  if (status == kRowOk && !greedy) return false;
-  if (threadIdx.x == 0 && cg::this_cluster().block_rank() == 0) {
+  if (status == kRowOk && !params_greedy(q)) return false;
+  if (threadIdx.x == 0) {
     const clsample_args_t& a = P.a;
-    const int row = cluster_row(P);
     const bool ok = status == kRowOk;
     a.tokens[row] = ok ? sh.rs.arg : -1;
     if (a.logprobs) a.logprobs[row] = ok ? -sh.rs.lnS : -INFINITY;
@@ -1406,7 +1523,13 @@ __device__ __noinline__ bool finish_early(const LaunchParams& P) {
 }
 
 // Truncation plan.  y = (z' - m) * (1/T); the kept set K = {y >= cut} is an upper set.
-__device__ __noinline__ void plan_row(const LaunchParams& P) {
+//  * top-k rows: the row end compacts the tokens at or above a lower bound of the k-th
+//    largest (the group-set bound, tightened by the table of group maxima);
+//  * rows with few allowed tokens: the row end compacts all of them;
+//  * min-p rows: K lies in {y >= ln min_p} (with top-p, its mass is taken over the whole
+//    row in a later phase);
+//  * untruncated rows and top-p alone: later phases over every slice.
+__device__ __noinline__ void plan_row() {
   if (threadIdx.x == 0) {
     const RowParams q = sh.rp;
     RowState& rs = sh.rs;
@@ -1415,20 +1538,20 @@ __device__ __noinline__ void plan_row(const LaunchParams& P) {
     const bool kfin = q.k >= 2;
     int plan = kPlanSlow, needW = 0, all = 0;
     float theta = -INFINITY;
-    if (kfin && rs.bound > -INFINITY) {
+    if (kfin) {
       plan = kPlanFast;  // every token of S_k has y >= y(bound)
-      theta = y_of(rs.bound, rs.m, rs.invT);
+      if (rs.bound > -INFINITY) theta = y_of(rs.bound, rs.m, rs.invT);
       if (q.p >= 1.0f) theta = fmaxf(theta, rs.L);
-    } else if (rs.nallowed_max <= kCandCap) {
-      plan = kPlanFast;  // few candidates: the leader sees all of them
+    } else if (rs.nallowed_sum <= kSmallRow) {
+      plan = kPlanFast;  // few candidates: the row end sees all of them
       all = 1;
-    } else if (q.mp > 0.0f && (q.p >= 1.0f || !kfin)) {
+    } else if (q.mp > 0.0f) {
       plan = kPlanFast;  // K lies in {y >= ln min_p}
       theta = rs.L;
       needW = q.p < 1.0f;  // top-p renormalises over the whole row
-    } else if (!kfin && q.p >= 1.0f) {
+    } else if (q.p >= 1.0f) {
       plan = kPlanUntrunc;  // K = every allowed token
-    } else if (!kfin) {
+    } else {
       plan = kPlanTopP;  // top-p alone
     }
     rs.plan = plan;
@@ -1441,9 +1564,24 @@ __device__ __noinline__ void plan_row(const LaunchParams& P) {
   __syncthreads();
 }
 
-// ---------------------------------------------------------------- candidates and the leader
+// Moves the row past phase `ph` (thread 0): the row's last listed phase resets its
+// counter for the next call; otherwise the row state (plan kPlanDone when the row has
+// ended) is published, then the phase number with release semantics.
+__device__ void row_advance(const LaunchParams& P, int row, int ph, int nph, bool done) {
+  if (threadIdx.x != 0) return;
+  if (ph >= nph) {
+    P.phase_done[row] = 0u;
+    return;
+  }
+  if (done) sh.rs.plan = kPlanDone;
+  P.rows[row] = sh.rs;
+  __threadfence();
+  st_release(P.phase_done + row, (unsigned)ph);
+}
 
-// Appends (y, id) to the slice's candidate list; the whole warp calls it.
+// ---------------------------------------------------------------- candidates and selects
+
+// Appends (y, id) to a candidate array with a shared counter; the whole warp calls it.
 __device__ __forceinline__ void append(Cand* cand, int cap, bool keep, float y, int id) {
   const int lane = threadIdx.x & 31;
   const uint32_t bal = __ballot_sync(0xffffffffu, keep);
@@ -1457,80 +1595,15 @@ __device__ __forceinline__ void append(Cand* cand, int cap, bool keep, float y, 
     if (p < cap) cand[p] = Cand{y, id};
   }
 }
-
-// Publishes the slice's pass-B record (candidate count, top-p mass partial, race) to
-// every CTA: exchange 2 (or 3).
-__device__ void finish_mine(int cap, unsigned long long w, const Race& race) {
-  const cg::cluster_group cluster = cg::this_cluster();
-  __threadfence();  // the compacted candidates (global) before the cluster barrier
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    sh.x2_mine.count = sh.count;
-    sh.x2_mine.flags = (sh.count > cap ? kFlagOverflow : 0) | (sh.flags & kFlagRing);
-    sh.x2_mine.w = w;
-    race.to(sh.x2_mine);
-  }
-  __syncthreads();
-  push_all(cluster, sh.x2, &sh.x2_mine, (int)cluster.block_rank(), (int)cluster.num_blocks());
-  cluster.sync();
+// The same for one thread.
+__device__ __forceinline__ void append1(Cand* cand, int cap, float y, int id) {
+  const int p = atomicAdd(&sh.count, 1);
+  if (p < cap) cand[p] = Cand{y, id};
 }
 
-__device__ __forceinline__ int x2_flags(int C) {
-  int f = 0;
-  for (int c = 0; c < C; ++c) f |= sh.x2[c].flags;
-  return f;
-}
-
-// After the last exchange every CTA's candidates sit in its global segment (the counts
-// are known to every CTA).  Only the leader (rank 0) continues: it packs them, in rank
-// order, into its shared gather area (the ring is free: every CTA has finished reading
-// its slice), or, when there are more than kGatherCap, into its own global segments.
-// Returns the packed array (nullptr in the other CTAs) and their number in *n.
-__device__ const Cand* collect_at_leader(const LaunchParams& P, const Smem& S, int* n) {
-  const cg::cluster_group cluster = cg::this_cluster();
-  if (cluster.block_rank() != 0) return nullptr;
-  const int tid = threadIdx.x;
-  const int C = P.C;
-  const int row = cluster_row(P);
-  Cand* seg = P.cand + (size_t)row * C * kCandCap;
-  int ntot = 0;
-  for (int c = 0; c < C; ++c) ntot += sh.x2[c].count;
-  *n = ntot;
-  if (ntot <= kGatherCap) {
-    int off = 0;
-    for (int c = 0; c < C; ++c) {
-      const int cnt = sh.x2[c].count;
-      for (int i = tid; i < cnt; i += kThreads) S.gather[off + i] = seg[(size_t)c * kCandCap + i];
-      off += cnt;
-    }
-    __syncthreads();
-    return S.gather;
-  }
-  // in place, segment by segment: each moves towards lower addresses, read whole first
-  int off = sh.x2[0].count;
-  for (int c = 1; c < C; ++c) {
-    const int cnt = sh.x2[c].count;
-    Cand tmp[kCandCap / kThreads];
-#pragma unroll
-    for (int t = 0; t < kCandCap / kThreads; ++t) {
-      const int i = t * kThreads + tid;
-      if (i < cnt) tmp[t] = seg[(size_t)c * kCandCap + i];
-    }
-    __syncthreads();
-#pragma unroll
-    for (int t = 0; t < kCandCap / kThreads; ++t) {
-      const int i = t * kThreads + tid;
-      if (i < cnt) seg[off + i] = tmp[t];
-    }
-    __syncthreads();
-    off += cnt;
-  }
-  return seg;
-}
-
-// Radix select over the gathered set (entries with y >= ylo): the largest value v such
+// Radix select over a gathered set (entries with y >= ylo): the largest value v such
 // that the count (or fixed-point weight) of entries >= v reaches `target`.
-__device__ __noinline__ float local_select(int chunk, const Cand* G, int n, bool weighted, float ylo,
+__device__ __noinline__ float local_select(int chunk, const Cand* G, int n, bool global, bool weighted, float ylo,
                                            unsigned long long target, bool* found) {
   const Smem S = carve(chunk);
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -1545,7 +1618,7 @@ __device__ __noinline__ float local_select(int chunk, const Cand* G, int n, bool
     for (int base = 0; base < n; base += kThreads) {
       const int i = base + tid;
       const bool ok = i < n;
-      const float y = ok ? G[i].y : -INFINITY;
+      const float y = ok ? ldcand(G, i, global).y : -INFINITY;
       const uint32_t key = fkey(y);
       const bool pred = ok && y >= ylo && (key & pmask) == prefix;
       if (weighted)
@@ -1573,12 +1646,12 @@ __device__ __noinline__ float local_select(int chunk, const Cand* G, int n, bool
   return key_to_float(prefix);
 }
 
-// Exact select over the gathered set, entries with y >= ylo, all within [lo, hi]: one
+// Exact select over a gathered set, entries with y >= ylo, all within [lo, hi]: one
 // 1024-bucket histogram (bucket order follows y), then the crossing bucket's entries are
 // resolved by counting.  Falls back to local_select when that bucket holds more than
 // 1024 entries (heavy ties).
-__device__ __noinline__ float leader_select(int chunk, const Cand* G, int n, bool weighted, float lo, float hi,
-                                            float ylo, unsigned long long target, bool* found) {
+__device__ __noinline__ float leader_select(int chunk, const Cand* G, int n, bool global, bool weighted, float lo,
+                                            float hi, float ylo, unsigned long long target, bool* found) {
   const Smem S = carve(chunk);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t* bk = reinterpret_cast<uint32_t*>(S.r2);  // split counters, two u32 per bucket
@@ -1596,7 +1669,7 @@ __device__ __noinline__ float leader_select(int chunk, const Cand* G, int n, boo
   }
   __syncthreads();
   for (int i = tid; i < n; i += kThreads) {
-    const float y = G[i].y;
+    const float y = ldcand(G, i, global).y;
     if (!(y >= ylo)) continue;
     split_add(bk + 2 * bucket(y), weighted ? weight_fx(y) : 1ull);
   }
@@ -1642,7 +1715,7 @@ __device__ __noinline__ float leader_select(int chunk, const Cand* G, int n, boo
   Cand* Lb = reinterpret_cast<Cand*>(S.r2);
   __syncthreads();
   for (int i = tid; i < n; i += kThreads) {
-    const Cand cd = G[i];
+    const Cand cd = ldcand(G, i, global);
     if (!(cd.y >= ylo) || bucket(cd.y) != bstar) continue;
     const int p = atomicAdd(&sh.nl, 1);
     if (p < 1024) Lb[p] = cd;
@@ -1651,7 +1724,7 @@ __device__ __noinline__ float leader_select(int chunk, const Cand* G, int n, boo
   const int nl = sh.nl;
   if (nl > 1024) {
     __syncthreads();
-    return local_select(chunk, G, n, weighted, ylo, target, found);
+    return local_select(chunk, G, n, global, weighted, ylo, target, found);
   }
   for (int i = tid; i < nl; i += kThreads) {
     const float yi = Lb[i].y;
@@ -1670,12 +1743,12 @@ __device__ __noinline__ float leader_select(int chunk, const Cand* G, int n, boo
 }
 
 // The race over the gathered entries with y >= cut (block-reduced into thread 0).
-__device__ __noinline__ Race leader_race(const Cand* G, int n, float cut, unsigned long long seed,
+__device__ __noinline__ Race leader_race(const Cand* G, int n, bool global, float cut, unsigned long long seed,
                                          unsigned long long pos) {
   Race r;
   r.init(sh.rs.s0);
   for (int i = threadIdx.x; i < n; i += kThreads) {
-    const Cand cd = G[i];
+    const Cand cd = ldcand(G, i, global);
     if (!(cd.y >= cut)) continue;
     r.add(cd.y, cd.id, pick_word(race_words_call((uint32_t)(cd.id >> 2), seed, pos), cd.id & 3));
   }
@@ -1683,200 +1756,83 @@ __device__ __noinline__ Race leader_race(const Cand* G, int n, float cut, unsign
   return r;
 }
 
-// ---------------------------------------------------------------- routes
-
-// A top-k row whose candidates exceed the leader's shared area: a cluster-wide histogram
-// of the candidates' y over 256 equal buckets of [lo, 0] (pushed with DSMEM atomics into
-// every CTA's merged copy, zeroed by the prologue) fixes the bucket where the count from
-// the top first reaches k; every CTA then keeps, in place, only its candidates in that
-// bucket or above (an upper set that still holds the top-k set) and the counts are
-// exchanged again.
-__device__ __noinline__ void refine_topk(const LaunchParams& P, const Smem& S, Cand* mycand, float lo, int k) {
-  const cg::cluster_group cluster = cg::this_cluster();
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int C = P.C, rank = (int)cluster.block_rank();
-  const int cnt = min(sh.x2[rank].count, kCandCap);
-  const float scale = 256.0f / -lo;
-  auto bucket = [&](float y) -> int {
-    const int b = __float2int_rz(__fmul_rn(-y, scale));
-    return b < 0 ? 0 : (b > 255 ? 255 : b);
-  };
-  S.hist_c[tid] = 0u;
-  __syncthreads();
-  Cand mine[kCandCap / kThreads];
-#pragma unroll
-  for (int t = 0; t < kCandCap / kThreads; ++t) {
-    const int i = t * kThreads + tid;
-    if (i < cnt) {
-      mine[t] = mycand[i];
-      atomicAdd(&S.hist_c[bucket(mine[t].y)], 1u);
-    }
+// Copies n candidates from the scratch into the gather area when they fit; returns the
+// array the selects read and sets *global.
+__device__ const Cand* gather_small(const Smem& S, const Cand* src, int n, bool* global) {
+  if (n > kGatherCap) {
+    *global = true;
+    return src;
   }
+  const float2* s = reinterpret_cast<const float2*>(src);
+  float2* d = reinterpret_cast<float2*>(S.gather);
+  for (int i = threadIdx.x; i < n; i += kThreads) d[i] = __ldcg(s + i);
   __syncthreads();
-  {
-    const uint32_t v = S.hist_c[tid];
-    if (v)
-      for (int r = 0; r < C; ++r) atomicAdd(cluster.map_shared_rank(S.mrg_c + tid, (unsigned)r), v);
-  }
-  cluster.sync();
-  // the bucket where the running count from the top (bucket 0) first reaches k
-  {
-    const uint32_t v = S.mrg_c[tid];
-    uint32_t x = v;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const uint32_t o = __shfl_up_sync(0xffffffffu, x, d);
-      if (lane >= d) x += o;
-    }
-    if (lane == 31) sh.red_i[warp] = (int)x;
-    if (tid == 0) sh.bstar = 255;
-    __syncthreads();
-    uint32_t before = 0;
-    for (int w = 0; w < warp; ++w) before += (uint32_t)sh.red_i[w];
-    if (before + x >= (uint32_t)k && before + x - v < (uint32_t)k) sh.bstar = tid;
-  }
-  __syncthreads();
-  const int bstar = sh.bstar;
-  if (tid == 0) sh.count = 0;
-  __syncthreads();
-#pragma unroll
-  for (int t = 0; t < kCandCap / kThreads; ++t) {
-    const int i = t * kThreads + tid;
-    if (i < cnt && bucket(mine[t].y) <= bstar) mycand[atomicAdd(&sh.count, 1)] = mine[t];
-  }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) sh.x2_mine.count = sh.count;
-  __syncthreads();
-  push_all(cluster, sh.x2, &sh.x2_mine, rank, C);
-  cluster.sync();
+  *global = false;
+  return S.gather;
 }
 
-// Rows with a provable bound (top-k, min-p) and untruncated rows.  Pass B compacts the
-// tokens at z >= zth (the exact z-space image of the y bound) and/or races every token;
-// the leader finishes top-k -> top-p -> min-p and the race over the gathered candidates.
-// Returns false when a compaction overflowed (the slow path takes over).
-template <bool kBF16>
-__device__ __noinline__ bool route_fast(const LaunchParams& P, int& pass) {
-  const Geo g = geo<kBF16>(P);
-  const Smem S = carve(g.chunk);
-  const clsample_args_t& a = P.a;
+// The per-slice segments of a later phase (counts in sh.x2), packed in slice order: into
+// the gather area when they fit, else in place into the row's contiguous segments (each
+// segment moves towards lower addresses, read whole first).
+__device__ const Cand* collect_segments(const LaunchParams& P, const Smem& S, int row, int* n, bool* global) {
+  const int tid = threadIdx.x, C = P.C;
+  Cand* seg = P.cand + (size_t)row * C * kCandCap;
+  int ntot = 0;
+  for (int c = 0; c < C; ++c) ntot += sh.x2[c].count;
+  *n = ntot;
+  if (ntot <= kGatherCap) {
+    int off = 0;
+    for (int c = 0; c < C; ++c) {
+      const int cnt = sh.x2[c].count;
+      const float2* s = reinterpret_cast<const float2*>(seg + (size_t)c * kCandCap);
+      float2* d = reinterpret_cast<float2*>(S.gather + off);
+      for (int i = tid; i < cnt; i += kThreads) d[i] = __ldcg(s + i);
+      off += cnt;
+    }
+    __syncthreads();
+    *global = false;
+    return S.gather;
+  }
+  int off = sh.x2[0].count;
+  for (int c = 1; c < C; ++c) {
+    const int cnt = sh.x2[c].count;
+    float2 tmp[kCandCap / kThreads];
+    const float2* s = reinterpret_cast<const float2*>(seg + (size_t)c * kCandCap);
+#pragma unroll
+    for (int t = 0; t < kCandCap / kThreads; ++t) {
+      const int i = t * kThreads + tid;
+      if (i < cnt) tmp[t] = __ldcg(s + i);
+    }
+    __syncthreads();
+    float2* d = reinterpret_cast<float2*>(seg + off);
+#pragma unroll
+    for (int t = 0; t < kCandCap / kThreads; ++t) {
+      const int i = t * kThreads + tid;
+      if (i < cnt) d[i] = tmp[t];
+    }
+    __threadfence_block();
+    __syncthreads();
+    off += cnt;
+  }
+  *global = true;
+  return seg;
+}
+
+// Top-k -> top-p -> min-p over the gathered candidates (an upper set of the row that
+// holds every kept token; `Wrow` is the row's top-p mass when top-p renormalises over the
+// whole row), then the race, then the outputs.  Thread 0 writes.
+__device__ __noinline__ void leader_finish(const LaunchParams& P, int row, const Cand* G, int ntot, bool global,
+                                           unsigned long long Wrow) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const RowParams q = sh.rp;
-  const float m = sh.rs.m, invT = sh.rs.invT, lnS = sh.rs.lnS, L = sh.rs.L, theta = sh.rs.theta;
-  const int plan = sh.rs.plan;
-  const bool needW = sh.rs.needW != 0;
-  const bool has_mod = a.hist_offs != nullptr || a.bias_offs != nullptr;
+  const float theta = sh.rs.theta, L = sh.rs.L, lnS = sh.rs.lnS;
   const bool kfin = q.k >= 2;
-  const unsigned long long seed = q.seed, pos = q.pos;
-  const int c0 = g.c0, cap = kCandCap, C = g.C;
-  Cand* mycand = P.cand + ((size_t)g.row * C + g.rank) * kCandCap;  // this slice's segment
-  if (warp == 0) {
-    const float zt = z_threshold_warp(theta, m, invT);
-    if (lane == 0) sh.zth = zt;
-  }
-  __syncthreads();
-  const float zth = sh.zth;
-  unsigned long long w = 0;
-  Race race;
-  race.init(sh.rs.s0);
-  stream<kBF16>(g, S, pass, false, [&](int f, uint32_t wd, const float4& v) {
-    float z[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-    if (wd) {
-      if (wd == 0xFu && finite4(v)) {
-        z[0] = v.x;
-        z[1] = v.y;
-        z[2] = v.z;
-        z[3] = v.w;
-      } else {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) z[j] = ((wd >> j) & 1u) ? sanitize(comp(v, j)) : -INFINITY;
-      }
-      if (needW) {
-#pragma unroll 1
-        for (int j = 0; j < 4; ++j)
-          if (z[j] > -INFINITY) w += weight_fx(y_of(z[j], m, invT));
-      }
-      if (plan == kPlanUntrunc) {
-        float y[4];
-        bool live_any = false, worth = false;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          y[j] = z[j] > -INFINITY ? y_of(z[j], m, invT) : -INFINITY;
-          if (z[j] > -INFINITY) {
-            live_any = true;
-            worth |= y[j] + kGumbelMax >= race.s;
-          }
-        }
-        if (worth) {
-          const uint4 x = race_words((uint32_t)((c0 >> 2) + f), seed, pos);
-#pragma unroll 1
-          for (int j = 0; j < 4; ++j)
-            if (z[j] > -INFINITY) race.add(y[j], c0 + 4 * f + j, pick_word(x, j));
-        } else if (live_any) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (z[j] > -INFINITY) race.count_only(y[j]);
-        }
-      }
-    }
-    if (plan == kPlanFast) {
-      const bool any = __any_sync(0xffffffffu, z[0] >= zth || z[1] >= zth || z[2] >= zth || z[3] >= zth);
-      if (any) {
-#pragma unroll 1
-        for (int j = 0; j < 4; ++j) {
-          const bool keep = z[j] > -INFINITY && z[j] >= zth;
-          append(mycand, cap, keep, keep ? y_of(z[j], m, invT) : 0.0f, c0 + 4 * f + j);
-        }
-      }
-    }
-  });
-  if (has_mod) {
-    const int npen = sh.npen;
-    for (int base = 0; base < npen; base += kThreads) {
-      const int i = base + tid;
-      const float z = i < npen ? S.pz[i] : -INFINITY;
-      const int gi = c0 + (i < npen ? (int)S.pid[i] : 0);
-      const float y = z > -INFINITY ? y_of(z, m, invT) : -INFINITY;
-      if (z > -INFINITY) {
-        if (needW) w += weight_fx(y);
-        if (plan == kPlanUntrunc) race.add(y, gi, pick_word(race_words_call((uint32_t)(gi >> 2), seed, pos), gi & 3));
-      }
-      if (plan == kPlanFast) append(mycand, cap, z > -INFINITY && z >= zth, y, gi);
-    }
-  }
-  if (needW) w = block_sum_u64(w, sh.red_u);
-  if (plan == kPlanUntrunc) block_reduce_race(race, sh.red_x);
-  finish_mine(cap, w, race);  // exchange 2
-  const int fl = x2_flags(C);
-
-  if (plan == kPlanUntrunc) {
-    // the winner is the same in every CTA; its owner writes the outputs
-    if (tid == 0) {
-      Race r;
-      r.init();
-      for (int c = 0; c < C; ++c) r.merge(sh.x2[c]);
-      const int owner = r.tok == INT_MAX ? 0 : r.tok / g.chunk;
-      if (g.rank == owner) write_sampled(a, g.row, r, lnS, !(fl & kFlagRing));
-    }
-    return true;
-  }
-  if (fl & kFlagOverflow) return false;
-  {
-    int n = 0;
-    for (int c = 0; c < C; ++c) n += sh.x2[c].count;
-    if (kfin && n > kGatherCap && theta > -INFINITY && theta < 0.0f) refine_topk(P, S, mycand, theta, q.k);
-  }
-  int ntot = 0;
-  const Cand* G = collect_at_leader(P, S, &ntot);
-  if (!G) return true;
-  const bool gathered = !(fl & kFlagRing);
   // the bucket range: [theta, 0], or the gathered candidates' finite range
   float lo = theta;
   if (!(lo > -INFINITY)) {
     float ymin = INFINITY;
     for (int i = tid; i < ntot; i += kThreads) {
-      const float y = G[i].y;
+      const float y = ldcand(G, i, global).y;
       if (y > -INFINITY) ymin = fminf(ymin, y);
     }
 #pragma unroll
@@ -1891,59 +1847,707 @@ __device__ __noinline__ bool route_fast(const LaunchParams& P, int& pass) {
   float tk = -INFINITY;
   if (kfin && ntot >= q.k) {
     bool found;
-    const float v = leader_select(g.chunk, G, ntot, false, lo, 0.0f, -INFINITY, (unsigned long long)q.k, &found);
+    const float v = leader_select(P.chunk, G, ntot, global, false, lo, 0.0f, -INFINITY, (unsigned long long)q.k,
+                                  &found);
     if (found) tk = v;
   }
   float tp = -INFINITY;
   if (q.p < 1.0f) {
     unsigned long long mset = 0;
-    for (int i = tid; i < ntot; i += kThreads)
-      if (G[i].y >= tk) mset += weight_fx(G[i].y);
+    for (int i = tid; i < ntot; i += kThreads) {
+      const float y = ldcand(G, i, global).y;
+      if (y >= tk) mset += weight_fx(y);
+    }
     mset = block_sum_u64(mset, sh.red_u);
     unsigned long long Wk = mset;  // top-k set (or every candidate) gathered: its mass
-    if (!kfin && !sh.rs.all) {
-      Wk = 0;
-      for (int c = 0; c < C; ++c) Wk += sh.x2[c].w;
-    }
+    if (!kfin && !sh.rs.all) Wk = Wrow;
     const unsigned long long cth = ceil_scaled(Wk, q.p);
     if (mset >= cth) {
       bool found;
-      const float v = leader_select(g.chunk, G, ntot, true, lo, 0.0f, tk, cth, &found);
+      const float v = leader_select(P.chunk, G, ntot, global, true, lo, 0.0f, tk, cth, &found);
       if (found) tp = v;
     }
   }
   const float cut = fmaxf(tk, fmaxf(tp, L));
-  const Race r = leader_race(G, ntot, cut, seed, pos);
-  if (tid == 0) write_sampled(a, g.row, r, lnS, gathered);
+  const Race r = leader_race(G, ntot, global, cut, q.seed, q.pos);
+  if (tid == 0) write_sampled(P.a, row, r, lnS, true);
+}
+
+// ---------------------------------------------------------------- re-reading a slice
+
+// Slice state for a later pass over slice `slice`: the live bits (bitmask words clipped
+// to the row, penalised tokens removed) and the first phase's list of penalised tokens
+// with their final z'.  Needs sh.x1[slice].
+template <bool kBF16>
+__device__ __noinline__ void setup_re(const LaunchParams& P, int row, int slice) {
+  const Geo g = geo<kBF16>(P, row, slice);
+  const Smem S = carve(g.chunk);
+  const clsample_args_t& a = P.a;
+  const int tid = threadIdx.x;
+  const int32_t* bmrow = a.bitmask ? a.bitmask + (long long)row * a.bitmask_row_stride : nullptr;
+  const int npen = min(sh.x1[slice].npen, kPenCap);
+  const uint2* pl = P.pen + ((size_t)row * P.C + slice) * kPenCap;
+  __syncthreads();  // the previous user of these tables is done
+  for (int w = tid; w < g.chunk / 32; w += kThreads) S.live[w] = mask_word(bmrow, g.c0, g.len, w);
+  for (int r = tid; r < npen; r += kThreads) {
+    const uint2 e = __ldcg(pl + r);
+    S.pid[r] = (uint16_t)e.x;
+    S.pz[r] = __uint_as_float(e.y);
+  }
+  __syncthreads();
+  for (int r = tid; r < npen; r += kThreads) {
+    const uint32_t l = S.pid[r];
+    atomicAnd(&S.live[l >> 5], ~(1u << (l & 31)));
+  }
+  if (tid == 0) sh.npen = npen;
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------- fast rows at the row end
+
+// Is local id l of slice s listed as penalised?  Binary search in the row end's copy of
+// the slices' sorted id lists (r2).
+__device__ __forceinline__ bool listed(const uint16_t* pids, int s, uint32_t l) {
+  int lo = sh.poff[s], hi = sh.poff[s + 1];
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    const uint32_t v = pids[mid];
+    if (v == l) return true;
+    if (v < l) lo = mid + 1;
+    else hi = mid;
+  }
+  return false;
+}
+
+// Tokens of slice s's ring part (bulk); *len gets the slice's length.
+template <bool kBF16>
+__device__ __forceinline__ int bulk_of(const LaunchParams& P, int s, int* len) {
+  constexpr int kEsize = kBF16 ? 2 : 4;
+  const int c0 = s * P.chunk;
+  *len = max(0, min(P.a.V, c0 + P.chunk) - c0);
+  return P.vec_ok ? (int)(((size_t)*len * kEsize) & ~(size_t)15) / kEsize : 0;
+}
+
+// Shared-memory areas of the row end (the ring and the r2 tables are free).
+constexpr int kHitList = 4096;                 // hit codes (u32) then their entries (u16)
+constexpr int kCandSmem = (kStages * kStageBytes - kHitList * 6) / (int)sizeof(Cand);
+constexpr int kPidsBytes = kPenCap * kMaxSlices * (int)sizeof(uint16_t);
+static_assert(kCandSmem >= 1024, "row-end candidate area");
+static_assert(kPidsBytes + 256 * (int)sizeof(uint32_t) <= (int)kR2Bytes, "row-end r2 tables");
+
+// Appends (y, id) to the candidates: the shared copy while it fits, and the row's
+// segments in the scratch; the whole warp calls it.
+__device__ __forceinline__ void append2(Cand* sm, int smcap, Cand* gl, int glcap, bool keep, float y, int id) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t bal = __ballot_sync(0xffffffffu, keep);
+  if (!bal) return;
+  const int leader = __ffs(bal) - 1;
+  int basepos = 0;
+  if (lane == leader) basepos = atomicAdd(&sh.count, __popc(bal));
+  basepos = __shfl_sync(0xffffffffu, basepos, leader);
+  if (keep) {
+    const int p = basepos + __popc(bal & ((1u << lane) - 1u));
+    if (p < smcap) sm[p] = Cand{y, id};
+    if (p < glcap) gl[p] = Cand{y, id};
+  }
+}
+__device__ __forceinline__ void append2_1(Cand* sm, int smcap, Cand* gl, int glcap, float y, int id) {
+  const int p = atomicAdd(&sh.count, 1);
+  if (p < smcap) sm[p] = Cand{y, id};
+  if (p < glcap) gl[p] = Cand{y, id};
+}
+
+
+// A bound E on the table entries (at least k groups reach E, so the k-th largest z' is
+// at least key^-1(E << 16)) in the y order the cuts use: y = fl(fl(z - m) (1/T)) can
+// merge neighbouring z, so the tokens kept by top-k are those with z at or above the
+// smallest z whose y reaches y(key^-1(E << 16)).  Warp 0 computes it into sh.res; every
+// thread returns it after the barrier.
+__device__ float entry_bound_z(uint32_t E, float m, float invT) {
+  if (threadIdx.x < 32) {
+    const float ye = y_of(key_to_float(E << 16), m, invT);
+    const float zt = z_threshold_warp(fminf(ye, 0.0f), m, invT);
+    if (threadIdx.x == 0) sh.res = zt;
+  }
+  __syncthreads();
+  const float r = sh.res;
+  __syncthreads();
+  return r;
+}
+
+// Candidates of a fast row: every token with z >= zth (the exact z image of theta) that
+// can be kept; for a top-k row only those in groups that can reach the k-th largest.
+// Found by the CTA that ends the row's first phase, with few rounds of loads:
+//  1. the listed penalised tokens of every slice (by their z'), the slices' ragged tails
+//     and their tables of group maxima, loaded together: groups whose entry reaches
+//     key(zth) are listed, and for a top-k row a histogram of those entries fixes the
+//     k-th largest entry E (at least k groups, hence k tokens, reach E, so every token of
+//     the top-k set lies in a group whose entry reaches E); the list keeps the groups
+//     reaching E;
+//  2. the listed groups' vectors, re-read from L2 with their bitmask words.
+// Slices without a table, and every slice when the list overflows, are re-read whole.
+// Then top-k -> top-p -> min-p and the race.  Returns false when the candidates overflow
+// the row's segments.
+template <bool kBF16>
+__device__ __noinline__ bool fast_serial_global(const LaunchParams& P, int row) {
+  constexpr int kEsize = kBF16 ? 2 : 4;
+  constexpr int kVecPerStage = kStageBytes / (4 * kEsize);
+  constexpr int kVPT = kVecPerStage / kThreads;
+  constexpr int kTabLoads = 5;  // 16-byte table loads per thread per round
+  constexpr int kPenLoads = 4;  // list entries per thread per round
+  const Smem S = carve(P.chunk);
+  const clsample_args_t& a = P.a;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int C = P.C, chunk = P.chunk;
+  const RowParams q = sh.rp;
+  const bool kfin = q.k >= 2;
+  const float m = sh.rs.m, invT = sh.rs.invT, theta = sh.rs.theta;
+  const int cap = C * kCandCap;
+  Cand* seg = P.cand + (size_t)row * C * kCandCap;
+  uint16_t* pids = reinterpret_cast<uint16_t*>(S.r2);
+  uint32_t* bins = reinterpret_cast<uint32_t*>(S.r2 + kPidsBytes);
+  uint32_t* hits = reinterpret_cast<uint32_t*>(S.ring);
+  uint16_t* hval = reinterpret_cast<uint16_t*>(S.ring + kHitList * 4);
+  Cand* csm = reinterpret_cast<Cand*>(S.ring + kHitList * 6);
+  const int32_t* bmrow = a.bitmask ? a.bitmask + (long long)row * a.bitmask_row_stride : nullptr;
+  const unsigned char* lrow =
+      reinterpret_cast<const unsigned char*>(a.logits) + (long long)row * a.logits_row_stride * kEsize;
+  if (warp == 0) {
+    const float zt = z_threshold_warp(theta, m, invT);
+    if (lane == 0) sh.zth = zt;
+  }
+  if (tid == 0) {
+    sh.count = 0;
+    sh.nhits = 0;
+    int o = 0;
+    for (int s = 0; s < C; ++s) {
+      sh.poff[s] = o;
+      o += min(sh.x1[s].npen, kPenCap);
+    }
+    sh.poff[C] = o;
+  }
+  bins[tid] = 0u;
+  __syncthreads();
+  const float zth = sh.zth;
+  float zcut = zth;  // candidates: z >= zcut (tightened for top-k rows below)
+  uint32_t thr = tab_threshold(zth);
+  const uint32_t top = fkey(m) >> 16;
+  int shift = 0;
+  while (((top - min(top, thr)) >> shift) >= 256u) ++shift;
+  int any_full = 0;
+  for (int s = 0; s < C; ++s) any_full |= !sh.x1[s].tab;
+  const int n16max = (int)((((size_t)chunk * kEsize) + kStageBytes - 1) / kStageBytes) * kThreads * 2 / 16;
+  const int nchunks = C * n16max;
+  const int npen_all = sh.poff[C];
+  const int rounds = max((npen_all + kPenLoads * kThreads - 1) / (kPenLoads * kThreads),
+                         (nchunks + kTabLoads * kThreads - 1) / (kTabLoads * kThreads));
+
+  // 1. lists, tails and tables
+  float tz = -INFINITY;  // this thread's tail token (threads < 8 C)
+  int tgi = -1;
+  if (tid < C * 8) {
+    const int s = tid >> 3;
+    int len;
+    const int l = bulk_of<kBF16>(P, s, &len) + (tid & 7);
+    if (sh.x1[s].tab && l < len) {
+      const int gi = s * chunk + l;
+      const bool allowed = !bmrow || (((uint32_t)__ldg(bmrow + (gi >> 5)) >> (gi & 31)) & 1u);
+      tgi = gi;
+      tz = allowed ? sanitize(gload1<kBF16>(lrow, gi)) : -INFINITY;
+    }
+  }
+  auto table_round = [&](int rd, bool count, bool with_values) {
+    uint4 te[kTabLoads];
+    bool tok[kTabLoads];
+#pragma unroll
+    for (int u = 0; u < kTabLoads; ++u) {
+      const int i = rd * kTabLoads * kThreads + u * kThreads + tid;
+      const int s = i / n16max, c = i - s * n16max;
+      int len;
+      const int bulk = s < C ? bulk_of<kBF16>(P, s, &len) : 0;
+      const int n16 = (bulk * kEsize + kStageBytes - 1) / kStageBytes * kThreads * 2 / 16;
+      tok[u] = i < nchunks && sh.x1[s].tab && c < n16;
+      te[u] = tok[u] ? __ldcg(reinterpret_cast<const uint4*>(P.tab + ((size_t)row * C + s) * kTabMax) + c)
+                     : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < kTabLoads; ++u) {
+      const int i = rd * kTabLoads * kThreads + u * kThreads + tid;
+      const int s = i / n16max, c = i - s * n16max;
+      const uint32_t w4[4] = {te[u].x, te[u].y, te[u].z, te[u].w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t ent = (w4[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
+        const bool hit = tok[u] && ent >= thr;
+        if (count && hit) atomicAdd(&bins[min((ent - thr) >> shift, 255u)], 1u);
+        const uint32_t bal = __ballot_sync(0xffffffffu, hit);
+        if (!bal) continue;
+        const int leader = __ffs(bal) - 1;
+        int pos = 0;
+        if (lane == leader) pos = atomicAdd(&sh.nhits, __popc(bal));
+        pos = __shfl_sync(0xffffffffu, pos, leader) + __popc(bal & ((1u << lane) - 1u));
+        if (hit && pos < kHitList) {
+          hits[pos] = ((uint32_t)s << 16) | (uint32_t)(8 * c + j);
+          if (with_values) hval[pos] = (uint16_t)ent;
+        }
+      }
+    }
+  };
+  const int trounds = (nchunks + kTabLoads * kThreads - 1) / (kTabLoads * kThreads);
+  const int prounds = (npen_all + kPenLoads * kThreads - 1) / (kPenLoads * kThreads);
+#pragma unroll 1
+  for (int rd = 0; rd < max(trounds, prounds); ++rd) {
+    if (rd < prounds) {
+      uint2 pe[kPenLoads];
+#pragma unroll
+      for (int u = 0; u < kPenLoads; ++u) {
+        const int i = rd * kPenLoads * kThreads + u * kThreads + tid;
+        int s = 0;
+        while (s + 1 < C && sh.poff[s + 1] <= i) ++s;
+        pe[u] = i < npen_all ? __ldcg(P.pen + ((size_t)row * C + s) * kPenCap + (i - sh.poff[s]))
+                             : make_uint2(0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < kPenLoads; ++u) {
+        const int i = rd * kPenLoads * kThreads + u * kThreads + tid;
+        if (i >= npen_all) continue;
+        int s = 0;
+        while (s + 1 < C && sh.poff[s + 1] <= i) ++s;
+        pids[i] = (uint16_t)pe[u].x;
+        const float z = __uint_as_float(pe[u].y);
+        if (z > -INFINITY && z >= zth) append2_1(csm, kCandSmem, seg, cap, y_of(z, m, invT), s * chunk + (int)pe[u].x);
+      }
+    }
+    if (rd < trounds) table_round(rd, kfin, true);
+  }
+  __syncthreads();  // every list id is in shared memory
+  if (tgi >= 0 && tz > -INFINITY && tz >= zth && !listed(pids, tgi / chunk, (uint32_t)(tgi % chunk)))
+    append2_1(csm, kCandSmem, seg, cap, y_of(tz, m, invT), tgi);
+  // the k-th largest entry: the histogram's crossing bin
+  if (kfin) {
+    if (warp == 0) pick_digit(bins, (unsigned long long)q.k, &sh.digit, &sh.above, &sh.none);
+    __syncthreads();
+    if (!sh.none) {
+      zcut = fmaxf(zth, entry_bound_z(thr + ((uint32_t)sh.digit << shift), m, invT));
+      thr = tab_threshold(zcut);
+    }
+  }
+  int nh = sh.nhits;
+  bool overflow = nh > kHitList;
+  if (overflow && kfin) {
+    // the list overflowed at key(zth): list the groups again at the tightened threshold
+    __syncthreads();
+    if (tid == 0) sh.nhits = 0;
+    __syncthreads();
+#pragma unroll 1
+    for (int rd = 0; rd < trounds; ++rd) table_round(rd, false, false);
+    __syncthreads();
+    nh = sh.nhits;
+    overflow = nh > kHitList;
+  } else if (!overflow && kfin) {
+    // keep the listed groups that reach the tightened threshold
+    constexpr int kPer = kHitList / kThreads;
+    uint32_t hc[kPer];
+    bool keep[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int h = u * kThreads + tid;
+      keep[u] = h < nh && hval[h] >= thr;
+      hc[u] = keep[u] ? hits[h] : 0u;
+    }
+    __syncthreads();
+    if (tid == 0) sh.nhits = 0;
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const uint32_t bal = __ballot_sync(0xffffffffu, keep[u]);
+      if (!bal) continue;
+      const int leader = __ffs(bal) - 1;
+      int pos = 0;
+      if (lane == leader) pos = atomicAdd(&sh.nhits, __popc(bal));
+      pos = __shfl_sync(0xffffffffu, pos, leader) + __popc(bal & ((1u << lane) - 1u));
+      if (keep[u]) hits[pos] = hc[u];
+    }
+    __syncthreads();
+    nh = sh.nhits;
+  }
+  if (!overflow) {
+    // 2. the listed groups' vectors with their bitmask words
+    constexpr int kHitBatch = kBF16 ? 1 : 2;
+#pragma unroll 1
+    for (int h0 = 0; h0 < nh; h0 += kHitBatch * kThreads) {
+      float4 v[kHitBatch][kVPT];
+      uint32_t mw[kHitBatch][kVPT];
+      int hs[kHitBatch], hf[kHitBatch];
+#pragma unroll
+      for (int b = 0; b < kHitBatch; ++b) {
+        const int h = h0 + b * kThreads + tid;
+        const bool valid = h < nh;
+        const uint32_t code = valid ? hits[h] : 0u;
+        const int s = (int)(code >> 16), e = (int)(code & 0xFFFFu);
+        const int k = e / kThreads, tt = e % kThreads;
+        const int c0s = s * chunk;
+        int len;
+        const int bulk = bulk_of<kBF16>(P, s, &len);
+        hs[b] = s;
+        hf[b] = k * kVecPerStage + tt;
+#pragma unroll
+        for (int u = 0; u < kVPT; ++u) {
+          const int f = hf[b] + u * kThreads;
+          const bool in = valid && 4 * f < bulk;
+          v[b][u] = in ? vload4<kBF16>(lrow + (size_t)c0s * kEsize, f) : make_float4(0.f, 0.f, 0.f, 0.f);
+          mw[b][u] = in ? ((bmrow ? (uint32_t)__ldg(bmrow + ((c0s + 4 * f) >> 5)) : 0xFFFFFFFFu) >> ((4 * f) & 31)) & 0xFu
+                        : 0u;
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < kHitBatch; ++b) {
+#pragma unroll
+        for (int u = 0; u < kVPT; ++u) {
+          const int f = hf[b] + u * kThreads;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            bool keep = false;
+            float z = -INFINITY;
+            if ((mw[b][u] >> j) & 1u) {
+              z = sanitize(comp(v[b][u], j));
+              keep = z > -INFINITY && z >= zcut && !listed(pids, hs[b], (uint32_t)(4 * f + j));
+            }
+            append2(csm, kCandSmem, seg, cap, keep, keep ? y_of(z, m, invT) : 0.0f, hs[b] * chunk + 4 * f + j);
+          }
+        }
+      }
+    }
+  }
+  // slices without a table (or all of them after an overflow of the list): whole
+  if (any_full || overflow) {
+    if (overflow) {
+      __syncthreads();
+      if (tid == 0) sh.count = 0;  // start over: every slice is re-read whole
+      __syncthreads();
+      // the listed penalised tokens again
+      for (int i = tid; i < npen_all; i += kThreads) {
+        int s = 0;
+        while (s + 1 < C && sh.poff[s + 1] <= i) ++s;
+        const uint2 e = __ldcg(P.pen + ((size_t)row * C + s) * kPenCap + (i - sh.poff[s]));
+        const float z = __uint_as_float(e.y);
+        if (z > -INFINITY && z >= zth) append2_1(csm, kCandSmem, seg, cap, y_of(z, m, invT), s * chunk + (int)e.x);
+      }
+    }
+    for (int s = 0; s < C; ++s) {
+      if (sh.x1[s].tab && !overflow) continue;
+      setup_re<kBF16>(P, row, s);
+      const Geo g = geo<kBF16>(P, row, s);
+      stream_ldg<kBF16>(g, S, [&](int f, uint32_t wd, const float4& v) {
+        float z[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) z[j] = ((wd >> j) & 1u) ? sanitize(comp(v, j)) : -INFINITY;
+        const bool any = __any_sync(0xffffffffu, z[0] >= zth || z[1] >= zth || z[2] >= zth || z[3] >= zth);
+        if (any) {
+#pragma unroll 1
+          for (int j = 0; j < 4; ++j) {
+            const bool keep = z[j] > -INFINITY && z[j] >= zth;
+            append2(csm, kCandSmem, seg, cap, keep, keep ? y_of(z[j], m, invT) : 0.0f, g.c0 + 4 * f + j);
+          }
+        }
+      });
+    }
+  }
+  __threadfence_block();
+  __syncthreads();
+  const int n = sh.count;
+  if (n > cap) return false;
+  const bool global = n > kCandSmem;
+  leader_finish(P, row, global ? seg : csm, n, global, 0ull);
   return true;
 }
 
-// Top-p alone: the exact top-p mass of the row and its histogram over quarter-unit y bins
-// (warp-private, in the candidate area) fix the crossing bin (exchange 2); pass C races
-// the tokens above it in place and sends the crossing bin's tokens to the leader, which
-// resolves the cut inside the bin.  Returns false (slow path) when the crossing bin is
-// the open-ended last one or the band overflowed.
-template <bool kBF16>
-__device__ __noinline__ bool route_topp(const LaunchParams& P, int& pass) {
-  const Geo g = geo<kBF16>(P);
-  const Smem S = carve(g.chunk);
-  const clsample_args_t& a = P.a;
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const RowParams q = sh.rp;
-  const float m = sh.rs.m, invT = sh.rs.invT, lnS = sh.rs.lnS;
-  const bool has_mod = a.hist_offs != nullptr || a.bias_offs != nullptr;
-  const unsigned long long seed = q.seed, pos = q.pos;
-  const int c0 = g.c0, cap = kCandCap, C = g.C;
-  Cand* mycand = P.cand + ((size_t)g.row * C + g.rank) * kCandCap;  // this slice's segment
-  const cg::cluster_group cluster = cg::this_cluster();
 
+// Block-wide sum of one int per thread (every thread gets it).
+__device__ __forceinline__ int block_sum_int(int v) {
+  v = __reduce_add_sync(0xffffffffu, v);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) sh.red_i[threadIdx.x >> 5] = v;
+  __syncthreads();
+  int t = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) t += sh.red_i[w];
+  return t;
+}
+
+// Entries >= thr among this thread's share of the tables in shared memory (chunks of 8
+// entries, `nch` chunks in all).
+__device__ __forceinline__ int count_entries(const uint4* tabs, int nch, uint32_t thr) {
+  int c = 0;
+  for (int i = threadIdx.x; i < nch; i += kThreads) {
+    const uint4 e = tabs[i];
+    const uint32_t w4[4] = {e.x, e.y, e.z, e.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) c += ((w4[j] & 0xFFFFu) >= thr) + ((w4[j] >> 16) >= thr);
+  }
+  return c;
+}
+
+// Candidates of a fast row (every token with z >= zth, the exact z image of theta, that
+// can be kept), found by the CTA that ends the row's first phase:
+//  1. one bulk copy (TMA) brings every slice's table of group maxima into shared memory
+//     while the threads load the slices' listed penalised tokens (candidates by their
+//     z') and ragged tails;
+//  2. for a top-k row, a binary search over the table entries finds the largest E with
+//     at least k entries >= E (at least k groups, hence k tokens, reach E, so every token
+//     of the top-k set lies in a group whose entry reaches E); the groups whose entry
+//     reaches the threshold are listed in table order by a block scan;
+//  3. the listed groups' vectors are re-read from L2 with their bitmask words.
+// Then top-k -> top-p -> min-p and the race.  Rows whose tables do not fit in shared
+// memory take fast_serial_global.  Returns false when the candidates overflow the row's
+// segments.
+template <bool kBF16>
+__device__ __noinline__ bool fast_serial(const LaunchParams& P, int row) {
+  constexpr int kEsize = kBF16 ? 2 : 4;
+  constexpr int kVecPerStage = kStageBytes / (4 * kEsize);
+  constexpr int kVPT = kVecPerStage / kThreads;
+  const Smem S = carve(P.chunk);
+  const Layout Lo = layout_for(P.chunk);
+  const clsample_args_t& a = P.a;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int C = P.C, chunk = P.chunk;
+  const int nst_max = (int)(((size_t)chunk * kEsize + kStageBytes - 1) / kStageBytes);
+  const int tabstride = nst_max * kThreads * (int)sizeof(uint16_t);  // bytes per slice
+  const int tabbytes = C * tabstride;
+  const int hitcap = ((int)Lo.r2 - tabbytes) / 4;
+  if (!P.vec_ok || hitcap < 256) return fast_serial_global<kBF16>(P, row);
+  const RowParams q = sh.rp;
+  const bool kfin = q.k >= 2;
+  const float m = sh.rs.m, invT = sh.rs.invT, theta = sh.rs.theta;
+  const int cap = C * kCandCap;
+  const int csmcap = tabbytes / (int)sizeof(Cand);
+  Cand* seg = P.cand + (size_t)row * C * kCandCap;
+  unsigned char* tabs = smem_dyn;                                  // [0, tabbytes)
+  uint32_t* hits = reinterpret_cast<uint32_t*>(smem_dyn + tabbytes);  // [tabbytes, r2)
+  Cand* csm = reinterpret_cast<Cand*>(smem_dyn);                   // after the tables are done
+  uint16_t* pids = reinterpret_cast<uint16_t*>(S.r2);
+  const int32_t* bmrow = a.bitmask ? a.bitmask + (long long)row * a.bitmask_row_stride : nullptr;
+  const unsigned char* lrow =
+      reinterpret_cast<const unsigned char*>(a.logits) + (long long)row * a.logits_row_stride * kEsize;
+  if (tid == 0) {
+    // every slice's table, one bulk copy each, on the row end's barrier; the tables are
+    // other CTAs' ordinary stores (acquired through the ticket), read here by the async
+    // proxy: the proxy fence orders them (global and shared state spaces)
+    asm volatile("fence.proxy.async;" ::: "memory");
+    uint32_t bytes = 0;
+    for (int s = 0; s < C; ++s) {
+      int len;
+      const int bulk = bulk_of<kBF16>(P, s, &len);
+      bytes += (uint32_t)((bulk * kEsize + kStageBytes - 1) / kStageBytes * kThreads * 2);
+    }
+    mbar_arrive_expect_tx(&sh.tbar, bytes);
+    for (int s = 0; s < C; ++s) {
+      int len;
+      const int bulk = bulk_of<kBF16>(P, s, &len);
+      const uint32_t b = (uint32_t)((bulk * kEsize + kStageBytes - 1) / kStageBytes * kThreads * 2);
+      if (b) bulk_copy_g2s(tabs + (size_t)s * tabstride, P.tab + ((size_t)row * C + s) * kTabMax, b, &sh.tbar);
+    }
+    sh.count = 0;
+    int o = 0;
+    for (int s = 0; s < C; ++s) {
+      sh.poff[s] = o;
+      o += min(sh.x1[s].npen, kPenCap);
+    }
+    sh.poff[C] = o;
+  }
+  if (warp == 1) {
+    const float zt = z_threshold_warp(theta, m, invT);
+    if (lane == 0) sh.zth = zt;
+  }
+  // this thread's tail token (threads < 8 C)
+  float tz = -INFINITY;
+  int tgi = -1;
+  if (tid < C * 8) {
+    const int s = tid >> 3;
+    int len;
+    const int l = bulk_of<kBF16>(P, s, &len) + (tid & 7);
+    if (l < len) {
+      const int gi = s * chunk + l;
+      const bool allowed = !bmrow || (((uint32_t)__ldg(bmrow + (gi >> 5)) >> (gi & 31)) & 1u);
+      tgi = gi;
+      tz = allowed ? sanitize(gload1<kBF16>(lrow, gi)) : -INFINITY;
+    }
+  }
+  __syncthreads();
+  const float zth = sh.zth;
+  // listed penalised tokens: ids for the check below, candidates by their z' (the
+  // candidates go to the row's segments only until the tables are done)
+  {
+    const int npen_all = sh.poff[C];
+    for (int base = 0; base < npen_all; base += 4 * kThreads) {
+      uint2 e[4];
+      int si[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = base + u * kThreads + tid;
+        int s = 0;
+        while (s + 1 < C && sh.poff[s + 1] <= i) ++s;
+        si[u] = s;
+        e[u] = i < npen_all ? __ldcg(P.pen + ((size_t)row * C + s) * kPenCap + (i - sh.poff[s])) : make_uint2(0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = base + u * kThreads + tid;
+        if (i >= npen_all) continue;
+        pids[i] = (uint16_t)e[u].x;
+        const float z = __uint_as_float(e[u].y);
+        if (z > -INFINITY && z >= zth) append1(seg, cap, y_of(z, m, invT), si[u] * chunk + (int)e[u].x);
+      }
+    }
+    __threadfence();  // read back below by other threads of the CTA
+  }
+  // the tables
+  if (tid == 0 && !mbar_wait_sleep(&sh.tbar, sh.tpar)) atomicOr(&sh.flags, kFlagRing);
+  __syncthreads();
+  (void)mbar_try_wait(&sh.tbar, sh.tpar);
+  const int nch = tabbytes / 16;
+  const uint4* t4 = reinterpret_cast<const uint4*>(tabs);
+  float zcut = zth;  // candidates: z >= zcut (tightened for top-k rows below)
+  uint32_t thr = tab_threshold(zth);
+  if (kfin && !(sh.flags & kFlagRing)) {
+    // largest E in [thr, top] with at least k entries >= E
+    uint32_t lo = thr, hi = (fkey(m) >> 16) + 1u;  // count(>= lo) >= k is checked first
+    if (block_sum_int(count_entries(t4, nch, lo)) >= q.k) {
+      while (hi - lo > 1u) {
+        const uint32_t mid = (lo + hi) >> 1;
+        if (block_sum_int(count_entries(t4, nch, mid)) >= q.k) lo = mid;
+        else hi = mid;
+      }
+      zcut = fmaxf(zth, entry_bound_z(lo, m, invT));
+      thr = tab_threshold(zcut);
+    }
+  }
+  // the groups at or above the threshold, in table order
+  int nh;
+  {
+    int c = 0;
+    for (int i = tid; i < nch; i += kThreads) {
+      const uint4 e = t4[i];
+      const uint32_t w4[4] = {e.x, e.y, e.z, e.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) c += ((w4[j] & 0xFFFFu) >= thr) + ((w4[j] >> 16) >= thr);
+    }
+    int x = c;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, x, d);
+      if (lane >= d) x += o;
+    }
+    __syncthreads();
+    if (lane == 31) sh.red_i[warp] = x;
+    __syncthreads();
+    int pos = x - c;
+    nh = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      if (w < warp) pos += sh.red_i[w];
+      nh += sh.red_i[w];
+    }
+    if (nh <= hitcap) {
+      for (int i = tid; i < nch; i += kThreads) {
+        const uint4 e = t4[i];
+        const uint32_t w4[4] = {e.x, e.y, e.z, e.w};
+        const int s = (i * 16) / tabstride, e0 = (i * 16 - s * tabstride) / 2;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t ent = (w4[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
+          if (ent >= thr) hits[pos++] = ((uint32_t)s << 16) | (uint32_t)(e0 + j);
+        }
+      }
+    }
+  }
+  __syncthreads();  // the tables are done: the candidate area is free
+  const bool tfail = (sh.flags & kFlagRing) != 0;
+  if (tid == 0) sh.tpar ^= 1u;  // the barrier's next phase
+  if (nh > hitcap || tfail) return fast_serial_global<kBF16>(P, row);
+  // the candidates found so far (listed penalised tokens) into the shared copy
+  {
+    const int n0 = sh.count;
+    for (int i = tid; i < min(n0, csmcap); i += kThreads) {
+      const float2 v = __ldcg(reinterpret_cast<const float2*>(seg) + i);
+      csm[i] = Cand{v.x, __float_as_int(v.y)};
+    }
+  }
+  if (tgi >= 0 && tz > -INFINITY && tz >= zth && !listed(pids, tgi / chunk, (uint32_t)(tgi % chunk)))
+    append2_1(csm, csmcap, seg, cap, y_of(tz, m, invT), tgi);
+  // the listed groups' vectors with their bitmask words
+  constexpr int kHitBatch = kBF16 ? 1 : 2;
+#pragma unroll 1
+  for (int h0 = 0; h0 < nh; h0 += kHitBatch * kThreads) {
+    float4 v[kHitBatch][kVPT];
+    uint32_t mw[kHitBatch][kVPT];
+    int hs[kHitBatch], hf[kHitBatch];
+#pragma unroll
+    for (int b = 0; b < kHitBatch; ++b) {
+      const int h = h0 + b * kThreads + tid;
+      const bool valid = h < nh;
+      const uint32_t code = valid ? hits[h] : 0u;
+      const int s = (int)(code >> 16), e = (int)(code & 0xFFFFu);
+      const int k = e / kThreads, tt = e % kThreads;
+      const int c0s = s * chunk;
+      int len;
+      const int bulk = bulk_of<kBF16>(P, s, &len);
+      hs[b] = s;
+      hf[b] = k * kVecPerStage + tt;
+#pragma unroll
+      for (int u = 0; u < kVPT; ++u) {
+        const int f = hf[b] + u * kThreads;
+        const bool in = valid && 4 * f < bulk;
+        v[b][u] = in ? vload4<kBF16>(lrow + (size_t)c0s * kEsize, f) : make_float4(0.f, 0.f, 0.f, 0.f);
+        mw[b][u] = in ? ((bmrow ? (uint32_t)__ldg(bmrow + ((c0s + 4 * f) >> 5)) : 0xFFFFFFFFu) >> ((4 * f) & 31)) & 0xFu
+                      : 0u;
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < kHitBatch; ++b) {
+#pragma unroll
+      for (int u = 0; u < kVPT; ++u) {
+        const int f = hf[b] + u * kThreads;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          bool keep = false;
+          float z = -INFINITY;
+          if ((mw[b][u] >> j) & 1u) {
+            z = sanitize(comp(v[b][u], j));
+            keep = z > -INFINITY && z >= zcut && !listed(pids, hs[b], (uint32_t)(4 * f + j));
+          }
+          append2(csm, csmcap, seg, cap, keep, keep ? y_of(z, m, invT) : 0.0f, hs[b] * chunk + 4 * f + j);
+        }
+      }
+    }
+  }
+  __threadfence_block();
+  __syncthreads();
+  const int n = sh.count;
+  if (n > cap) return false;
+  const bool global = n > csmcap;
+  leader_finish(P, row, global ? seg : csm, n, global, 0ull);
+  return true;
+}
+
+// ---------------------------------------------------------------- later phases: slice passes
+
+// Top-p alone, phase 2: the exact top-p mass of the slice and its histogram over
+// quarter-unit y bins (warp-private split counters in r2, the open-ended last bin in
+// registers), merged per bin into the slice's row of the scratch.
+template <bool kBF16>
+__device__ __noinline__ void topp_hist(const LaunchParams& P, int row, int slice) {
+  const Geo g = geo<kBF16>(P, row, slice);
+  const Smem S = carve(g.chunk);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const float m = sh.rs.m, invT = sh.rs.invT;
+  const size_t idx = (size_t)row * P.C + slice;
   // warp-private split counters (two u32 per bin): a warp adds at most 4160 weights
   uint32_t* whist = reinterpret_cast<uint32_t*>(S.r2);
   for (int i = tid; i < 2 * kWarps * kPBins; i += kThreads) whist[i] = 0u;
   __syncthreads();
   unsigned long long w = 0, wlast = 0;
   uint32_t* mine = whist + 2 * warp * kPBins;
-  stream<kBF16>(g, S, pass, false, [&](int f, uint32_t wd, const float4& v) {
+  stream_ldg<kBF16>(g, S, [&](int f, uint32_t wd, const float4& v) {
     if (!wd) return;
     const bool fastv = wd == 0xFu && finite4(v);
 #pragma unroll 1
@@ -1959,61 +2563,54 @@ __device__ __noinline__ bool route_topp(const LaunchParams& P, int& pass) {
       else split_add(mine + 2 * b, qw);
     }
   });
-  if (has_mod) {
-    for (int i = tid; i < sh.npen; i += kThreads) {
-      const float z = S.pz[i];
-      if (!(z > -INFINITY)) continue;
-      const float y = y_of(z, m, invT);
-      const unsigned long long qw = weight_fx(y);
-      if (!qw) continue;
-      w += qw;
-      split_add(mine + 2 * pbin(y), qw);
-    }
+  for (int i = tid; i < sh.npen; i += kThreads) {
+    const float z = S.pz[i];
+    if (!(z > -INFINITY)) continue;
+    const float y = y_of(z, m, invT);
+    const unsigned long long qw = weight_fx(y);
+    if (!qw) continue;
+    w += qw;
+    split_add(mine + 2 * pbin(y), qw);
   }
   {
     const unsigned long long wl = warp_sum_u64(wlast);  // < 2^53: split_add holds it
     if ((tid & 31) == 0 && wl) split_add(mine + 2 * (kPBins - 1), wl);
   }
   w = block_sum_u64(w, sh.red_u);
-  // merge the warp histograms and push them into every CTA's merged copy
-  unsigned long long* pmrg = reinterpret_cast<unsigned long long*>(S.mrg_c);  // zeroed by the prologue
   if (tid < kPBins) {
     unsigned long long t = 0;
     for (int wp = 0; wp < kWarps; ++wp) t += split_get(whist + 2 * (wp * kPBins + tid));
-    if (t)
-      for (int r = 0; r < C; ++r) atomicAdd(cluster.map_shared_rank(pmrg + tid, (unsigned)r), t);
+    P.phist[idx * kPBins + tid] = t;
   }
-  Race none_race;
-  none_race.init();
-  finish_mine(cap, w, none_race);  // exchange 2
-  unsigned long long W = 0;
-  for (int c = 0; c < C; ++c) W += sh.x2[c].w;
-  const unsigned long long cth = ceil_scaled(W, q.p);
-  // crossing bin: the running mass from the top first reaches cth in bin bstar
-  int bstar = kPBins - 1;
-  unsigned long long above = 0;
-  {
-    unsigned long long cum = 0;
-    for (int b = 0; b < kPBins; ++b) {
-      const unsigned long long nb = cum + pmrg[b];
-      if (nb >= cth) {
-        bstar = b;
-        above = cum;
-        break;
-      }
-      cum = nb;
-    }
+  if (tid == 0) {
+    Race none;
+    none.init();
+    none.to(sh.x2_mine);
+    sh.x2_mine.count = 0;
+    sh.x2_mine.flags = 0;
+    sh.x2_mine.w = w;
   }
-  if (bstar >= kPBins - 1) return false;
-  // pass C: tokens above the crossing bin are certainly kept: race them here; tokens of
-  // the crossing bin go to the leader
+}
+
+// Top-p alone, phase 3: tokens above the crossing bin are certainly kept: raced here;
+// tokens of the crossing bin go to the slice's candidate segment for the row end.
+template <bool kBF16>
+__device__ __noinline__ void topp_race(const LaunchParams& P, int row, int slice) {
+  const Geo g = geo<kBF16>(P, row, slice);
+  const Smem S = carve(g.chunk);
+  const int tid = threadIdx.x;
+  const RowParams q = sh.rp;
+  const float m = sh.rs.m, invT = sh.rs.invT;
+  const unsigned long long seed = q.seed, pos = q.pos;
+  const int c0 = g.c0, cap = kCandCap;
+  Cand* mycand = P.cand + ((size_t)row * P.C + slice) * kCandCap;
+  const int bstar = sh.rs.bstar;
   const float yhi = -(float)bstar * 0.25f, ylo = -(float)(bstar + 1) * 0.25f;
-  __syncthreads();
   if (tid == 0) sh.count = 0;
   __syncthreads();
   Race race;
   race.init(sh.rs.s0);
-  stream<kBF16>(g, S, pass, false, [&](int f, uint32_t wd, const float4& v) {
+  stream_ldg<kBF16>(g, S, [&](int f, uint32_t wd, const float4& v) {
     float y[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
     if (wd) {
       const bool fastv = wd == 0xFu && finite4(v);
@@ -2049,7 +2646,7 @@ __device__ __noinline__ bool route_topp(const LaunchParams& P, int& pass) {
       for (int j = 0; j < 4; ++j) append(mycand, cap, y[j] > ylo && y[j] <= yhi, y[j], c0 + 4 * f + j);
     }
   });
-  if (has_mod) {
+  {
     const int npen = sh.npen;
     for (int base = 0; base < npen; base += kThreads) {
       const int i = base + tid;
@@ -2064,257 +2661,499 @@ __device__ __noinline__ bool route_topp(const LaunchParams& P, int& pass) {
     }
   }
   block_reduce_race(race, sh.red_x);
-  finish_mine(cap, 0ull, race);  // exchange 3
-  const int fl = x2_flags(C);
-  if (fl & kFlagOverflow) return false;
-  int ntot = 0;
-  const Cand* G = collect_at_leader(P, S, &ntot);
-  if (!G) return true;
-  const bool gathered = !(fl & kFlagRing);
-  // the cut lies in the crossing bin: a weighted select over its tokens
-  bool found;
-  const float vstar = leader_select(g.chunk, G, ntot, true, ylo, yhi, -INFINITY, cth - above, &found);
-  Race r = leader_race(G, ntot, vstar, seed, pos);
+  __syncthreads();
   if (tid == 0) {
-    for (int c = 0; c < C; ++c) r.merge(sh.x2[c]);
-    write_sampled(a, g.row, r, lnS, gathered && found);
+    race.to(sh.x2_mine);
+    sh.x2_mine.count = sh.count;
+    sh.x2_mine.flags = sh.count > cap ? kFlagOverflow : 0;
+    sh.x2_mine.w = 0ull;
   }
-  return true;
 }
 
-// Cluster-wide radix select over the slices (one pass over the slice per 8-bit digit):
-// the largest value v such that the count (or fixed-point weight) of kept-side tokens
-// with y >= v reaches `target`, among tokens with y >= ylo.  Histograms are pushed into
-// every CTA's merged copy with DSMEM atomics, one cluster barrier per digit; the merged
-// copies are double-buffered and cleared after use.
+// Min-p with top-p over the whole row, phase 2: the slice's exact top-p mass and its
+// tokens with z >= zth (the exact z image of ln min_p) into the slice's segment.
 template <bool kBF16>
-__device__ __noinline__ float cluster_select(const LaunchParams& P, int& pass, int& gpass, bool weighted, float ylo,
-                                             unsigned long long target, bool* found) {
-  const Geo g = geo<kBF16>(P);
+__device__ __noinline__ void minp_pass(const LaunchParams& P, int row, int slice) {
+  const Geo g = geo<kBF16>(P, row, slice);
   const Smem S = carve(g.chunk);
-  const clsample_args_t& a = P.a;
-  const cg::cluster_group cluster = cg::this_cluster();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float m = sh.rs.m, invT = sh.rs.invT, theta = sh.rs.theta;
+  const int c0 = g.c0, cap = kCandCap;
+  Cand* mycand = P.cand + ((size_t)row * P.C + slice) * kCandCap;
+  if (warp == 0) {
+    const float zt = z_threshold_warp(theta, m, invT);
+    if (lane == 0) {
+      sh.zth = zt;
+      sh.count = 0;
+    }
+  }
+  __syncthreads();
+  const float zth = sh.zth;
+  unsigned long long w = 0;
+  stream_ldg<kBF16>(g, S, [&](int f, uint32_t wd, const float4& v) {
+    float z[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    if (wd) {
+      if (wd == 0xFu && finite4(v)) {
+        z[0] = v.x;
+        z[1] = v.y;
+        z[2] = v.z;
+        z[3] = v.w;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) z[j] = ((wd >> j) & 1u) ? sanitize(comp(v, j)) : -INFINITY;
+      }
+#pragma unroll 1
+      for (int j = 0; j < 4; ++j)
+        if (z[j] > -INFINITY) w += weight_fx(y_of(z[j], m, invT));
+    }
+    const bool any = __any_sync(0xffffffffu, z[0] >= zth || z[1] >= zth || z[2] >= zth || z[3] >= zth);
+    if (any) {
+#pragma unroll 1
+      for (int j = 0; j < 4; ++j) {
+        const bool keep = z[j] > -INFINITY && z[j] >= zth;
+        append(mycand, cap, keep, keep ? y_of(z[j], m, invT) : 0.0f, c0 + 4 * f + j);
+      }
+    }
+  });
+  {
+    const int npen = sh.npen;
+    for (int base = 0; base < npen; base += kThreads) {
+      const int i = base + tid;
+      const float z = i < npen ? S.pz[i] : -INFINITY;
+      const int gi = c0 + (i < npen ? (int)S.pid[i] : 0);
+      const float y = z > -INFINITY ? y_of(z, m, invT) : -INFINITY;
+      if (z > -INFINITY) w += weight_fx(y);
+      append(mycand, cap, z > -INFINITY && z >= zth, y, gi);
+    }
+  }
+  w = block_sum_u64(w, sh.red_u);
+  if (tid == 0) {
+    Race none;
+    none.init();
+    none.to(sh.x2_mine);
+    sh.x2_mine.count = sh.count;
+    sh.x2_mine.flags = sh.count > cap ? kFlagOverflow : 0;
+    sh.x2_mine.w = w;
+  }
+}
+
+// No truncation, phase 2: the race over every allowed token of the slice.  A vector
+// whose every y is kGumbelMax below the best score so far cannot win and skips Philox.
+template <bool kBF16>
+__device__ __noinline__ void untrunc_pass(const LaunchParams& P, int row, int slice) {
+  const Geo g = geo<kBF16>(P, row, slice);
+  const Smem S = carve(g.chunk);
+  const int tid = threadIdx.x;
+  const RowParams q = sh.rp;
+  const float m = sh.rs.m, invT = sh.rs.invT;
+  const unsigned long long seed = q.seed, pos = q.pos;
+  const int c0 = g.c0;
+  Race race;
+  race.init(sh.rs.s0);
+  stream_ldg<kBF16>(g, S, [&](int f, uint32_t wd, const float4& v) {
+    if (!wd) return;
+    float y[4];
+    bool live_any = false, worth = false;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float z = ((wd >> j) & 1u) ? sanitize(comp(v, j)) : -INFINITY;
+      y[j] = z > -INFINITY ? y_of(z, m, invT) : -INFINITY;
+      if (z > -INFINITY) {
+        live_any = true;
+        worth |= y[j] + kGumbelMax >= race.s;
+      }
+    }
+    if (worth) {
+      const uint4 x = race_words((uint32_t)((c0 >> 2) + f), seed, pos);
+#pragma unroll 1
+      for (int j = 0; j < 4; ++j)
+        if (y[j] > -INFINITY) race.add(y[j], c0 + 4 * f + j, pick_word(x, j));
+    } else if (live_any) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (y[j] > -INFINITY) race.count_only(y[j]);
+    }
+  });
+  for (int i = tid; i < sh.npen; i += kThreads) {
+    const float z = S.pz[i];
+    if (!(z > -INFINITY)) continue;
+    const float y = y_of(z, m, invT);
+    const int gi = c0 + (int)S.pid[i];
+    race.add(y, gi, pick_word(race_words_call((uint32_t)(gi >> 2), seed, pos), gi & 3));
+  }
+  block_reduce_race(race, sh.red_x);
+  __syncthreads();
+  if (tid == 0) {
+    race.to(sh.x2_mine);
+    sh.x2_mine.count = 0;
+    sh.x2_mine.flags = 0;
+    sh.x2_mine.w = 0ull;
+  }
+}
+
+// ---------------------------------------------------------------- rows without a usable bound
+
+// Exact radix select over the whole row by one CTA (one pass over every slice per 8-bit
+// digit): the largest value v such that the count (or fixed-point weight) of tokens with
+// y >= v reaches `target`, among tokens with y >= ylo.  Needs sh.x1 of every slice.
+template <bool kBF16>
+__device__ __noinline__ float row_select(const LaunchParams& P, int row, bool weighted, float ylo,
+                                         unsigned long long target, bool* found) {
+  const Smem S = carve(P.chunk);
   const int tid = threadIdx.x, warp = tid >> 5;
   const float m = sh.rs.m, invT = sh.rs.invT;
-  const bool has_mod = a.hist_offs != nullptr || a.bias_offs != nullptr;
   uint32_t prefix = 0u, pmask = 0u;
-  bool ok_all = true;
-  for (int dpass = 0; dpass < 4; ++dpass, ++gpass) {
+  for (int dpass = 0; dpass < 4; ++dpass) {
     const int shift = 24 - 8 * dpass;
-    const int buf = gpass & 1;
     if (tid < 256) {
       S.hist_c[tid] = 0u;
       S.hist_w[tid] = 0ull;
     }
-    __syncthreads();
-    stream<kBF16>(g, S, pass, false, [&](int f, uint32_t wd, const float4& v) {
-#pragma unroll 1
-      for (int j = 0; j < 4; ++j) {
+    for (int s = 0; s < P.C; ++s) {
+      setup_re<kBF16>(P, row, s);
+      const Geo g = geo<kBF16>(P, row, s);
+      auto add = [&](bool live, float z) {
         bool pred = false;
         float y = -INFINITY;
-        if ((wd >> j) & 1u) {
-          const float z = sanitize(comp(v, j));
-          if (z > -INFINITY) {
-            y = y_of(z, m, invT);
-            pred = y >= ylo && (fkey(y) & pmask) == prefix;
-          }
+        if (live && z > -INFINITY) {
+          y = y_of(z, m, invT);
+          pred = y >= ylo && (fkey(y) & pmask) == prefix;
         }
         const uint32_t digit = (fkey(y) >> shift) & 0xFFu;
-        if (weighted)
-          hist_add<true>(S.hist_c, S.hist_w, pred, digit, pred ? weight_fx(y) : 0ull);
-        else
-          hist_add<false>(S.hist_c, S.hist_w, pred, digit, 0ull);
-      }
-    });
-    if (has_mod) {
+        if (weighted) hist_add<true>(S.hist_c, S.hist_w, pred, digit, pred ? weight_fx(y) : 0ull);
+        else hist_add<false>(S.hist_c, S.hist_w, pred, digit, 0ull);
+      };
+      stream_ldg<kBF16>(g, S, [&](int f, uint32_t wd, const float4& v) {
+#pragma unroll 1
+        for (int j = 0; j < 4; ++j) add(((wd >> j) & 1u) != 0u, sanitize(comp(v, j)));
+      });
       const int npen = sh.npen;
       for (int base = 0; base < npen; base += kThreads) {
         const int i = base + tid;
-        bool pred = false;
-        float y = -INFINITY;
-        if (i < npen) {
-          const float z = S.pz[i];
-          if (z > -INFINITY) {
-            y = y_of(z, m, invT);
-            pred = y >= ylo && (fkey(y) & pmask) == prefix;
-          }
-        }
-        const uint32_t digit = (fkey(y) >> shift) & 0xFFu;
-        if (weighted)
-          hist_add<true>(S.hist_c, S.hist_w, pred, digit, pred ? weight_fx(y) : 0ull);
-        else
-          hist_add<false>(S.hist_c, S.hist_w, pred, digit, 0ull);
+        add(i < npen, i < npen ? S.pz[i] : -INFINITY);
       }
     }
     __syncthreads();
-    for (int i = tid; i < 256 * g.C; i += kThreads) {
-      const int bin = i & 255, r = i >> 8;
-      if (weighted) {
-        const unsigned long long hv = S.hist_w[bin];
-        if (hv) atomicAdd(cluster.map_shared_rank(S.mrg_w + buf * 256 + bin, (unsigned)r), hv);
-      } else {
-        const uint32_t hv = S.hist_c[bin];
-        if (hv) atomicAdd(cluster.map_shared_rank(S.mrg_c + buf * 256 + bin, (unsigned)r), hv);
-      }
-    }
-    cluster.sync();
     if (warp == 0) {
-      if (weighted) pick_digit(S.mrg_w + buf * 256, target, &sh.digit, &sh.above, &sh.none);
-      else pick_digit(S.mrg_c + buf * 256, target, &sh.digit, &sh.above, &sh.none);
+      if (weighted) pick_digit(S.hist_w, target, &sh.digit, &sh.above, &sh.none);
+      else pick_digit(S.hist_c, target, &sh.digit, &sh.above, &sh.none);
     }
     __syncthreads();
-    const bool none = sh.none != 0;
-    const int dg = sh.digit;
-    const unsigned long long ab = sh.above;
-    // clear this buffer for its next use (two digits later, after another barrier)
-    if (tid < 256) {
-      S.mrg_c[buf * 256 + tid] = 0u;
-      S.mrg_w[buf * 256 + tid] = 0ull;
+    if (sh.none) {
+      *found = false;
+      __syncthreads();
+      return -INFINITY;
     }
+    prefix |= (uint32_t)sh.digit << shift;
+    pmask |= 0xFFu << shift;
+    target -= sh.above;
     __syncthreads();
-    if (none) ok_all = false;
-    if (ok_all) {
-      prefix |= (uint32_t)dg << shift;
-      pmask |= 0xFFu << shift;
-      target -= ab;
-    }
   }
-  *found = ok_all;
-  return ok_all ? key_to_float(prefix) : -INFINITY;
+  *found = true;
+  return key_to_float(prefix);
 }
 
-// Rows without a usable bound (very large k, compaction overflow, top-p with an
-// open-ended crossing bin): exact cluster-wide selects, then the race in place.
+// Rows without a usable bound (very large k, candidate overflow, top-p with an
+// open-ended crossing bin): exact selects over the whole row, then the race, all by the
+// calling CTA.  Slow, and rare.  Needs sh.x1 of every slice.
 template <bool kBF16>
-__device__ __noinline__ void route_slow(const LaunchParams& P, int& pass) {
-  const Geo g = geo<kBF16>(P);
-  const Smem S = carve(g.chunk);
-  const clsample_args_t& a = P.a;
-  const cg::cluster_group cluster = cg::this_cluster();
+__device__ __noinline__ void slow_serial(const LaunchParams& P, int row) {
+  const Smem S = carve(P.chunk);
   const int tid = threadIdx.x;
   const RowParams q = sh.rp;
   const float m = sh.rs.m, invT = sh.rs.invT, lnS = sh.rs.lnS, L = sh.rs.L;
-  const bool has_mod = a.hist_offs != nullptr || a.bias_offs != nullptr;
-  const unsigned long long seed = q.seed, pos = q.pos;
-  const int c0 = g.c0, C = g.C;
   const bool kfin = q.k >= 2;
-
-  for (int i = tid; i < 2 * 256; i += kThreads) {
-    S.mrg_c[i] = 0u;
-    S.mrg_w[i] = 0ull;
-  }
-  cluster.sync();  // every merged copy is clear before the first push
-  int gpass = 0;
   float tk = -INFINITY;
   if (kfin) {
     bool found;
-    const float v = cluster_select<kBF16>(P, pass, gpass, false, -INFINITY, (unsigned long long)q.k, &found);
+    const float v = row_select<kBF16>(P, row, false, -INFINITY, (unsigned long long)q.k, &found);
     if (found) tk = v;  // fewer than k candidates: top-k keeps them all
   }
   float tp = -INFINITY;
   if (q.p < 1.0f) {
     unsigned long long w = 0;
-    stream<kBF16>(g, S, pass, false, [&](int f, uint32_t wd, const float4& v) {
+    for (int s = 0; s < P.C; ++s) {
+      setup_re<kBF16>(P, row, s);
+      const Geo g = geo<kBF16>(P, row, s);
+      stream_ldg<kBF16>(g, S, [&](int f, uint32_t wd, const float4& v) {
 #pragma unroll 1
-      for (int j = 0; j < 4; ++j) {
-        if (!((wd >> j) & 1u)) continue;
-        const float z = sanitize(comp(v, j));
-        if (!(z > -INFINITY)) continue;
-        const float y = y_of(z, m, invT);
-        if (y >= tk) w += weight_fx(y);
-      }
-    });
-    if (has_mod)
+        for (int j = 0; j < 4; ++j) {
+          if (!((wd >> j) & 1u)) continue;
+          const float z = sanitize(comp(v, j));
+          if (!(z > -INFINITY)) continue;
+          const float y = y_of(z, m, invT);
+          if (y >= tk) w += weight_fx(y);
+        }
+      });
       for (int i = tid; i < sh.npen; i += kThreads) {
         const float z = S.pz[i];
         if (!(z > -INFINITY)) continue;
         const float y = y_of(z, m, invT);
         if (y >= tk) w += weight_fx(y);
       }
+    }
     w = block_sum_u64(w, sh.red_u);
-    if (tid == 0) sh.x2_mine.w = w;
-    __syncthreads();
-    push_all(cluster, sh.x2, &sh.x2_mine, g.rank, C);
-    cluster.sync();
-    unsigned long long W = 0;
-    for (int c = 0; c < C; ++c) W += sh.x2[c].w;
     bool found;
-    const float v = cluster_select<kBF16>(P, pass, gpass, true, tk, ceil_scaled(W, q.p), &found);
+    const float v = row_select<kBF16>(P, row, true, tk, ceil_scaled(w, q.p), &found);
     if (found) tp = v;
   }
   const float cut = fmaxf(tk, fmaxf(tp, L));
   Race race;
   race.init(sh.rs.s0);
-  stream<kBF16>(g, S, pass, false, [&](int f, uint32_t wd, const float4& v) {
-    float y[4];
-    uint32_t keep = 0u;
+  for (int s = 0; s < P.C; ++s) {
+    setup_re<kBF16>(P, row, s);
+    const Geo g = geo<kBF16>(P, row, s);
+    const int c0 = g.c0;
+    stream_ldg<kBF16>(g, S, [&](int f, uint32_t wd, const float4& v) {
+      float y[4];
+      uint32_t keep = 0u;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      y[j] = -INFINITY;
-      if (!((wd >> j) & 1u)) continue;
-      const float z = sanitize(comp(v, j));
-      if (!(z > -INFINITY)) continue;
-      y[j] = y_of(z, m, invT);
-      if (y[j] >= cut) keep |= 1u << j;
-    }
-    if (!keep) return;
-    const uint4 x = race_words((uint32_t)((c0 >> 2) + f), seed, pos);
+      for (int j = 0; j < 4; ++j) {
+        y[j] = -INFINITY;
+        if (!((wd >> j) & 1u)) continue;
+        const float z = sanitize(comp(v, j));
+        if (!(z > -INFINITY)) continue;
+        y[j] = y_of(z, m, invT);
+        if (y[j] >= cut) keep |= 1u << j;
+      }
+      if (!keep) return;
+      const uint4 x = race_words((uint32_t)((c0 >> 2) + f), q.seed, q.pos);
 #pragma unroll 1
-    for (int j = 0; j < 4; ++j)
-      if ((keep >> j) & 1u) race.add(y[j], c0 + 4 * f + j, pick_word(x, j));
-  });
-  if (has_mod)
+      for (int j = 0; j < 4; ++j)
+        if ((keep >> j) & 1u) race.add(y[j], c0 + 4 * f + j, pick_word(x, j));
+    });
     for (int i = tid; i < sh.npen; i += kThreads) {
       const float z = S.pz[i];
       if (!(z > -INFINITY)) continue;
       const float y = y_of(z, m, invT);
       if (!(y >= cut)) continue;
       const int gi = c0 + (int)S.pid[i];
-      race.add(y, gi, pick_word(race_words_call((uint32_t)(gi >> 2), seed, pos), gi & 3));
+      race.add(y, gi, pick_word(race_words_call((uint32_t)(gi >> 2), q.seed, q.pos), gi & 3));
     }
+  }
   block_reduce_race(race, sh.red_x);
+  if (tid == 0) write_sampled(P.a, row, race, lnS, true);
   __syncthreads();
+}
+
+// ---------------------------------------------------------------- items
+
+// A first-phase item; the CTA that finishes the row's last slice ends the row or hands
+// it to the next phase.
+template <bool kBF16>
+__device__ __noinline__ void p1_item(const LaunchParams& P, int row, int slice, int nph) {
+  setup_p1<kBF16>(P, row, slice, nph);
+  pass_a<kBF16>(P, row, slice);
+  if (!publish_p1<kBF16>(P, row, slice)) return;
+  combine_row(P, row);
+  if (finish_early(P, row)) {
+    row_advance(P, row, 1, nph, true);
+    return;
+  }
+  plan_row();
+  const int plan = sh.rs.plan;
+  if (plan == kPlanFast && !sh.rs.needW) {
+    if (!fast_serial<kBF16>(P, row)) slow_serial<kBF16>(P, row);
+    row_advance(P, row, 1, nph, true);
+    return;
+  }
+  const int need = plan == kPlanTopP ? 3 : 2;  // phases the plan takes
+  if (plan == kPlanSlow || nph < need) {
+    slow_serial<kBF16>(P, row);
+    row_advance(P, row, 1, nph, true);
+    return;
+  }
+  row_advance(P, row, 1, nph, false);
+}
+
+// The last arriver of a later phase.  `what` is the pass the phase ran (0: none).
+template <bool kBF16>
+__device__ __noinline__ void phase_end(const LaunchParams& P, int row, int ph, int nph, int what) {
+  const Smem S = carve(P.chunk);
+  const int tid = threadIdx.x, C = P.C;
+  const RowParams q = sh.rp;
+  const bool bad = __ldcg(P.bad + row) != 0u;
+  if (bad || !sh.ok) {
+    // a wait gave up: the row's records are incomplete
+    if (tid == 0 && !(sh.ok && sh.rs.plan == kPlanDone)) {
+      Race r;
+      r.init();
+      write_sampled(P.a, row, r, 0.0f, false);
+    }
+    row_advance(P, row, ph, nph, true);
+    return;
+  }
+  if (what == 0) {
+    if (sh.rs.plan != kPlanDone) slow_serial<kBF16>(P, row);  // a plan without this phase: not reached
+    row_advance(P, row, ph, nph, true);
+    return;
+  }
+  int fl = 0;
+  for (int c = 0; c < C; ++c) fl |= sh.x2[c].flags;
+  if (what == 1) {
+    // top-p alone: the crossing bin, where the running mass from the top first reaches
+    // ceil(p W)
+    unsigned long long W = 0;
+    for (int c = 0; c < C; ++c) W += sh.x2[c].w;
+    const unsigned long long cth = ceil_scaled(W, q.p);
+    if (tid < kPBins) {
+      unsigned long long t = 0;
+      for (int c = 0; c < C; ++c) t += __ldcg(P.phist + ((size_t)row * C + c) * kPBins + tid);
+      S.hist_w[tid] = t;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int bstar = kPBins - 1;
+      unsigned long long above = 0, cum = 0;
+      for (int b = 0; b < kPBins; ++b) {
+        const unsigned long long nb = cum + S.hist_w[b];
+        if (nb >= cth) {
+          bstar = b;
+          above = cum;
+          break;
+        }
+        cum = nb;
+      }
+      sh.rs.bstar = bstar;
+      sh.rs.above = above;
+      sh.rs.cth = cth;
+    }
+    __syncthreads();
+    if (sh.rs.bstar >= kPBins - 1) {
+      slow_serial<kBF16>(P, row);
+      row_advance(P, row, ph, nph, true);
+    } else {
+      row_advance(P, row, ph, nph, false);
+    }
+    return;
+  }
+  if (what == 4) {
+    if (tid == 0) {
+      Race r;
+      r.init();
+      for (int c = 0; c < C; ++c) r.merge(sh.x2[c]);
+      write_sampled(P.a, row, r, sh.rs.lnS, true);
+    }
+    row_advance(P, row, ph, nph, true);
+    return;
+  }
+  if (fl & kFlagOverflow) {
+    slow_serial<kBF16>(P, row);
+    row_advance(P, row, ph, nph, true);
+    return;
+  }
+  int ntot = 0;
+  bool global = false;
+  const Cand* G = collect_segments(P, S, row, &ntot, &global);
+  if (what == 2) {
+    // top-p alone: the cut lies in the crossing bin: a weighted select over its tokens
+    const int bstar = sh.rs.bstar;
+    const float yhi = -(float)bstar * 0.25f, ylo = -(float)(bstar + 1) * 0.25f;
+    bool found;
+    const float vstar =
+        leader_select(P.chunk, G, ntot, global, true, ylo, yhi, -INFINITY, sh.rs.cth - sh.rs.above, &found);
+    Race r = leader_race(G, ntot, global, vstar, q.seed, q.pos);
+    if (tid == 0) {
+      for (int c = 0; c < C; ++c) r.merge(sh.x2[c]);
+      write_sampled(P.a, row, r, sh.rs.lnS, found);
+    }
+  } else {
+    unsigned long long W = 0;
+    for (int c = 0; c < C; ++c) W += sh.x2[c].w;
+    leader_finish(P, row, G, ntot, global, W);
+  }
+  row_advance(P, row, ph, nph, true);
+}
+
+// An item of a later phase: waits (bounded) until the row's previous phase is complete,
+// runs the phase's pass over its slice, publishes the slice record and takes the ticket.
+template <bool kBF16>
+__device__ __noinline__ void phase_item(const LaunchParams& P, int row, int slice, int ph, int nph) {
+  const int tid = threadIdx.x, C = P.C;
+  const size_t idx = (size_t)row * C + slice;
   if (tid == 0) {
-    race.to(sh.x2_mine);
-    sh.x2_mine.flags = sh.flags & kFlagRing;
+    unsigned v = ld_acquire(P.phase_done + row);
+    for (uint32_t i = 0; v < (unsigned)(ph - 1) && i < kWaitLimit; ++i) {
+      __nanosleep(i < 64u ? 100u : 1000u);
+      v = ld_acquire(P.phase_done + row);
+    }
+    sh.ok = v >= (unsigned)(ph - 1) ? 1 : 0;
+    sh.rp = load_params(P.a, row);
   }
   __syncthreads();
-  push_all(cluster, sh.x2, &sh.x2_mine, g.rank, C);
-  cluster.sync();
-  // the winner is the same in every CTA; its owner writes the outputs
-  if (tid == 0) {
-    Race r;
-    r.init();
-    for (int c = 0; c < C; ++c) r.merge(sh.x2[c]);
-    const int owner = r.tok == INT_MAX ? 0 : r.tok / g.chunk;
-    if (g.rank == owner) write_sampled(a, g.row, r, lnS, !(x2_flags(C) & kFlagRing));
+  if (tid == 0 && sh.ok) ldcg_copy(&sh.rs, P.rows + row);
+  if (tid < C) ldcg_copy(&sh.x1[tid], P.x1 + (size_t)row * C + tid);
+  __syncthreads();
+  const bool ok = sh.ok != 0;
+  if (!ok && tid == 0) atomicOr(P.bad + row, 1u);
+  const int plan = ok ? sh.rs.plan : kPlanDone;
+  int what = 0;
+  if (plan == kPlanTopP && ph == 2) what = 1;
+  else if (plan == kPlanTopP && ph == 3) what = 2;
+  else if (plan == kPlanFast && sh.rs.needW && ph == 2) what = 3;
+  else if (plan == kPlanUntrunc && ph == 2) what = 4;
+  if (what) {
+    setup_re<kBF16>(P, row, slice);
+    if (what == 1) topp_hist<kBF16>(P, row, slice);
+    else if (what == 2) topp_race<kBF16>(P, row, slice);
+    else if (what == 3) minp_pass<kBF16>(P, row, slice);
+    else untrunc_pass<kBF16>(P, row, slice);
+    __syncthreads();
+    if (tid == 0) P.x2[idx] = sh.x2_mine;
   }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const bool last = atomicAdd(P.ticket + 4 * row + ph, 1u) == (unsigned)C - 1u;
+    if (last) P.ticket[4 * row + ph] = 0u;
+    sh.last = last ? 1 : 0;
+  }
+  __syncthreads();
+  if (!sh.last) return;
+  __threadfence();
+  if (tid < C) ldcg_copy(&sh.x2[tid], P.x2 + (size_t)row * C + tid);
+  __syncthreads();
+  phase_end<kBF16>(P, row, ph, nph, what);
 }
 
 // ---------------------------------------------------------------- the kernel
 
 template <bool kBF16>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) sampler_kernel(const __grid_constant__ LaunchParams P) {
-  // DSMEM may only be touched once every CTA of the cluster runs: arrive now, wait just
-  // before the first push (exchange1)
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-  prologue<kBF16>(P);
-  pass_a<kBF16>(P);
-  exchange1(P);
-  if (finish_early(P)) return;
-  plan_row(P);
-  int pass = 1;
-  const int plan = sh.rs.plan;
-  if (plan == kPlanFast || plan == kPlanUntrunc) {
-    if (route_fast<kBF16>(P, pass)) return;
-  } else if (plan == kPlanTopP) {
-    if (route_topp<kBF16>(P, pass)) return;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) mbar_init(&sh.full[i], 1);
+    mbar_init(&sh.tbar, 1);
+    fence_mbar_init();
+    sh.seq = 0u;
+    sh.tpar = 0u;
   }
-  route_slow<kBF16>(P, pass);
+  __syncthreads();
+  const unsigned C = (unsigned)P.C;
+  const unsigned nitems = P.ctl[2] * C;  // work-list segments (the order kernel wrote them)
+  for (;;) {
+    if (tid == 0) sh.item = atomicAdd(P.ctl, 1u);
+    __syncthreads();
+    const unsigned item = sh.item;
+    if (item >= nitems) break;
+    const unsigned e = P.seg[item / C];
+    const int row = (int)(e & 0xFFFFFFu), ph = (int)((e >> 24) & 0xFu), nph = (int)(e >> 28);
+    const int slice = (int)(item % C);
+    if (ph == 1) p1_item<kBF16>(P, row, slice, nph);
+    else phase_item<kBF16>(P, row, slice, ph, nph);
+    __syncthreads();
+  }
+  // the last CTA out resets the claim counter (a later launch may reuse the list)
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(P.ctl + 1, 1u) == gridDim.x - 1u) {
+      P.ctl[0] = 0u;
+      P.ctl[1] = 0u;
+    }
+  }
 }
 
 // ---------------------------------------------------------------- diagnostics kernels
-
 
 __global__ void debug_weights_kernel(const float* y, unsigned long long* w, int n) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -2332,33 +3171,57 @@ __global__ void debug_uniforms_kernel(const uint64_t* seeds, const int64_t* pos,
 
 // ---------------------------------------------------------------- host side
 
-// C = ceil(V / 2048) CTAs per row, at most the portable cluster size; slices are whole
-// bitmask words.  Shared memory does not depend on the logits type.
+// C = ceil(V / 2048) slices per row, at most kMaxSlices; slices are whole bitmask words.
+// Shared memory does not depend on the logits type.
 Geometry geometry_for(int vocab) {
-  Geometry g{0, 0, 0, 0};
+  Geometry g{0, 0, 0};
   if (vocab <= 0) return g;
   int C = (vocab + 2047) / 2048;
-  if (C > kMaxCluster) C = kMaxCluster;
+  if (C > kMaxSlices) C = kMaxSlices;
   const int chunk = ((vocab + C - 1) / C + 31) / 32 * 32;
   if (chunk > kMaxChunk) return g;  // C = 0: vocabulary too large
   g.C = C;
   g.chunk = chunk;
   g.smem = (int)layout_for(chunk).total;
-  g.cap = kCandCap;
   return g;
 }
 
-}  // namespace
+// Byte offsets of the scratch arrays for B rows of C slices (one allocation).
+struct ScratchLayout {
+  size_t ctl, ticket, phase_done, bad, seg, order, rows, x1, x2, pen, tab, phist, cand, total;
+};
 
-namespace {
+constexpr size_t take(size_t& off, size_t bytes) {
+  const size_t o = off;
+  off = align_up(off + bytes, 256);
+  return o;
+}
 
-// Device scratch of one call: sized for max_batch rows of up to kMaxCluster slices.
+constexpr ScratchLayout scratch_layout(size_t B, size_t C) {
+  ScratchLayout L{};
+  size_t off = 0;
+  L.ctl = take(off, 4 * sizeof(unsigned));
+  L.ticket = take(off, 4 * B * sizeof(unsigned));
+  L.phase_done = take(off, B * sizeof(unsigned));
+  L.bad = take(off, B * sizeof(unsigned));
+  L.seg = take(off, 3 * B * sizeof(unsigned));
+  L.order = take(off, B * sizeof(int));
+  L.rows = take(off, B * sizeof(RowState));
+  L.x1 = take(off, B * C * sizeof(X1));
+  L.x2 = take(off, B * C * sizeof(X2));
+  L.pen = take(off, B * C * kPenCap * sizeof(uint2));
+  L.tab = take(off, B * C * kTabMax * sizeof(uint16_t));
+  L.phist = take(off, B * C * kPBins * sizeof(unsigned long long));
+  L.cand = take(off, B * C * kCandCap * sizeof(Cand));
+  L.total = off;
+  return L;
+}
+
+// Device scratch of one call: sized for max_batch rows of up to C slices.
 struct Scratch {
   int max_batch;
-  PenEntry* pen;  // penalised-token lists, [max_batch * C][kPenCap]
-  int2* pen_n;    // their lengths and flags, [max_batch * C]
-  Cand* cand;     // compacted candidates, [max_batch * C][kCandCap]
-  int* rows;      // row classes and launch order, [2 * max_batch], then the ticket
+  int C;
+  unsigned char* base;
 };
 
 // Checks the device (compute capability 10.3, enough shared memory) and raises the
@@ -2374,9 +3237,30 @@ int setup_device(int dev) {
   if (smem > optin) return CLSAMPLE_ERR_DEVICE;
   const void* k32 = reinterpret_cast<const void*>(&sampler_kernel<false>);
   const void* k16 = reinterpret_cast<const void*>(&sampler_kernel<true>);
+  const void* ko = reinterpret_cast<const void*>(&order_kernel);
+  // every kernel asks for the largest shared-memory carveout, so that the SMs need not
+  // change their L1 / shared split between the ordering kernel and the sampler
   if (cudaFuncSetAttribute(k32, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
-      cudaFuncSetAttribute(k16, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      cudaFuncSetAttribute(k16, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+      cudaFuncSetAttribute(k32, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(k16, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(ko, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared) !=
+          cudaSuccess)
     return CLSAMPLE_ERR_CUDA;
+  return CLSAMPLE_SUCCESS;
+}
+
+// CTAs of the persistent sampler kernel: as many as can be resident on device `dev`.
+int resident_ctas(const Geometry& g, bool bf16, int dev, int* out) {
+  int sms = 0, per = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return CLSAMPLE_ERR_CUDA;
+  const cudaError_t err =
+      bf16 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, sampler_kernel<true>, kThreads, (size_t)g.smem)
+           : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, sampler_kernel<false>, kThreads, (size_t)g.smem);
+  if (err != cudaSuccess) return CLSAMPLE_ERR_CUDA;
+  *out = sms * (per > 0 ? per : 1);
   return CLSAMPLE_SUCCESS;
 }
 
@@ -2388,18 +3272,15 @@ struct clsample_handle {
   int device;
   Geometry g;
   Scratch sc;
+  int grid[2];  // resident CTAs for f32 and bf16 logits
 };
 
 namespace {
 
 // Scratch of clsample_apply_static: a fixed device array compiled into the library
-// (zero at load, so the preparation kernel's ticket starts at 0), for kStaticRows rows.
+// (zero at load), for kStaticRows rows of up to kMaxSlices slices.
 constexpr int kStaticRows = 64;
-constexpr size_t kStaticLists = (size_t)kStaticRows * kMaxCluster;
-constexpr size_t kStaticOffPenN = align_up(kStaticLists * kPenCap * sizeof(PenEntry), 256);
-constexpr size_t kStaticOffCand = kStaticOffPenN + align_up(kStaticLists * sizeof(int2), 256);
-constexpr size_t kStaticOffRows = kStaticOffCand + align_up(kStaticLists * kCandCap * sizeof(Cand), 256);
-constexpr size_t kStaticBytes = kStaticOffRows + align_up((2 * (size_t)kStaticRows + 1) * sizeof(int), 256);
+constexpr size_t kStaticBytes = scratch_layout(kStaticRows, kMaxSlices).total;
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticBytes];
 
 constexpr int kMaxDevices = 64;
@@ -2446,10 +3327,10 @@ const char* clsample_strerror(int code) {
   }
 }
 
-int clsample_geometry(int32_t vocab, int32_t* cluster, int32_t* chunk, int32_t* smem_bytes) {
+int clsample_geometry(int32_t vocab, int32_t* slices, int32_t* chunk, int32_t* smem_bytes) {
   const Geometry g = geometry_for(vocab);
   if (g.C == 0) return CLSAMPLE_ERR_VOCAB;
-  if (cluster) *cluster = g.C;
+  if (slices) *slices = g.C;
   if (chunk) *chunk = g.chunk;
   if (smem_bytes) *smem_bytes = g.smem;
   return CLSAMPLE_SUCCESS;
@@ -2458,63 +3339,43 @@ int clsample_geometry(int32_t vocab, int32_t* cluster, int32_t* chunk, int32_t* 
 int clsample_create(int32_t max_batch, int32_t vocab, clsample_t** out) {
   if (!out) return CLSAMPLE_ERR_NULL;
   *out = nullptr;
-  if (max_batch < 0) return CLSAMPLE_ERR_BATCH;
+  if (max_batch < 0 || max_batch > (1 << 24) - 1) return CLSAMPLE_ERR_BATCH;
   const Geometry g = geometry_for(vocab);
   if (g.C == 0) return CLSAMPLE_ERR_VOCAB;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return CLSAMPLE_ERR_CUDA;
-  const int rc = setup_device(dev);
+  int rc = setup_device(dev);
   if (rc != CLSAMPLE_SUCCESS) return rc;
-  PenEntry* pen = nullptr;
-  int2* pen_n = nullptr;
-  Cand* cand = nullptr;
-  int* rows = nullptr;
+  int grid[2];
+  if ((rc = resident_ctas(g, false, dev, &grid[0])) != CLSAMPLE_SUCCESS) return rc;
+  if ((rc = resident_ctas(g, true, dev, &grid[1])) != CLSAMPLE_SUCCESS) return rc;
+  unsigned char* base = nullptr;
   if (max_batch > 0) {
-    const size_t lists = (size_t)max_batch * (size_t)g.C;
-    if (cudaMalloc(&pen, lists * kPenCap * sizeof(PenEntry)) != cudaSuccess ||
-        cudaMalloc(&pen_n, lists * sizeof(int2)) != cudaSuccess ||
-        cudaMalloc(&cand, lists * kCandCap * sizeof(Cand)) != cudaSuccess ||
-        cudaMalloc(&rows, (2 * (size_t)max_batch + 1) * sizeof(int)) != cudaSuccess ||
-        cudaMemset(rows, 0, (2 * (size_t)max_batch + 1) * sizeof(int)) != cudaSuccess) {
-      if (pen) cudaFree(pen);
-      if (pen_n) cudaFree(pen_n);
-      if (cand) cudaFree(cand);
-      if (rows) cudaFree(rows);
+    const size_t bytes = scratch_layout((size_t)max_batch, (size_t)g.C).total;
+    void* p = nullptr;
+    if (cudaMalloc(&p, bytes) != cudaSuccess) return CLSAMPLE_ERR_CUDA;
+    if (cudaMemset(p, 0, bytes) != cudaSuccess) {
+      cudaFree(p);
       return CLSAMPLE_ERR_CUDA;
     }
+    base = static_cast<unsigned char*>(p);
   }
   clsample_t* h = new clsample_t;
   h->max_batch = max_batch;
   h->vocab = vocab;
   h->device = dev;
   h->g = g;
-  h->sc = Scratch{max_batch, pen, pen_n, cand, rows};
+  h->sc = Scratch{max_batch, g.C, base};
+  h->grid[0] = grid[0];
+  h->grid[1] = grid[1];
   *out = h;
   return CLSAMPLE_SUCCESS;
 }
 
 void clsample_destroy(clsample_t* h) {
   if (!h) return;
-  if (h->sc.pen) cudaFree(h->sc.pen);
-  if (h->sc.pen_n) cudaFree(h->sc.pen_n);
-  if (h->sc.cand) cudaFree(h->sc.cand);
-  if (h->sc.rows) cudaFree(h->sc.rows);
+  if (h->sc.base) cudaFree(h->sc.base);
   delete h;
-}
-
-static void fill_launch(const Geometry& g, unsigned nclusters, cudaStream_t stream, cudaLaunchConfig_t* cfg,
-                        cudaLaunchAttribute* attr) {
-  std::memset(cfg, 0, sizeof *cfg);
-  cfg->gridDim = dim3(nclusters * (unsigned)g.C, 1, 1);
-  cfg->blockDim = dim3(kThreads, 1, 1);
-  cfg->dynamicSmemBytes = (size_t)g.smem;
-  cfg->stream = stream;
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)g.C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg->attrs = attr;
-  cfg->numAttrs = 1;
 }
 
 }  // extern "C"
@@ -2523,7 +3384,7 @@ namespace {
 
 // Validates a call and fills the launch parameters (host only): the vocabulary must be
 // `vocab`, the batch at most the scratch's rows, and `dev` the current device.
-int make_params(const Geometry& g, int vocab, int dev, const Scratch& sc, const clsample_args_t* a,
+int make_params(const Geometry& g, int vocab, int dev, const Scratch& sc, int grid, const clsample_args_t* a,
                 LaunchParams* P) {
   if (!a) return CLSAMPLE_ERR_NULL;
   if (a->B < 0 || a->B > sc.max_batch) return CLSAMPLE_ERR_BATCH;
@@ -2543,35 +3404,45 @@ int make_params(const Geometry& g, int vocab, int dev, const Scratch& sc, const 
   P->a = *a;
   P->C = g.C;
   P->chunk = g.chunk;
-  P->cap = g.cap;
-  const uintptr_t base = reinterpret_cast<uintptr_t>(a->logits);
-  P->vec_ok = (base % 16 == 0) && (((long long)a->logits_row_stride * esize) % 16 == 0);
-  P->pen = sc.pen;
-  P->pen_n = sc.pen_n;
-  P->cand = sc.cand;
-  P->row_class = sc.rows;
-  P->row_order = sc.rows + sc.max_batch;
-  P->ticket = reinterpret_cast<unsigned*>(sc.rows + 2 * (size_t)sc.max_batch);
+  const uintptr_t lb = reinterpret_cast<uintptr_t>(a->logits);
+  P->vec_ok = (lb % 16 == 0) && (((long long)a->logits_row_stride * esize) % 16 == 0);
+  P->gap = grid / g.C > 1 ? grid / g.C : 1;
+  const ScratchLayout L = scratch_layout((size_t)sc.max_batch, (size_t)sc.C);
+  unsigned char* b = sc.base;
+  P->ctl = reinterpret_cast<unsigned*>(b + L.ctl);
+  P->ticket = reinterpret_cast<unsigned*>(b + L.ticket);
+  P->phase_done = reinterpret_cast<unsigned*>(b + L.phase_done);
+  P->bad = reinterpret_cast<unsigned*>(b + L.bad);
+  P->seg = reinterpret_cast<unsigned*>(b + L.seg);
+  P->order = reinterpret_cast<int*>(b + L.order);
+  P->rows = reinterpret_cast<RowState*>(b + L.rows);
+  P->x1 = reinterpret_cast<X1*>(b + L.x1);
+  P->x2 = reinterpret_cast<X2*>(b + L.x2);
+  P->pen = reinterpret_cast<uint2*>(b + L.pen);
+  P->tab = reinterpret_cast<uint16_t*>(b + L.tab);
+  P->phist = reinterpret_cast<unsigned long long*>(b + L.phist);
+  P->cand = reinterpret_cast<Cand*>(b + L.cand);
   return CLSAMPLE_SUCCESS;
 }
 
-int make_params(const clsample_t* h, const clsample_args_t* a, LaunchParams* P) {
+int make_params(const clsample_t* h, const clsample_args_t* a, LaunchParams* P, int* grid) {
   if (!h) return CLSAMPLE_ERR_NULL;
-  return make_params(h->g, h->vocab, h->device, h->sc, a, P);
+  if (!a) return CLSAMPLE_ERR_NULL;
+  *grid = h->grid[a->logits_dtype == CLSAMPLE_LOGITS_BF16 ? 1 : 0];
+  return make_params(h->g, h->vocab, h->device, h->sc, *grid, a, P);
 }
 
-int launch_prep(const LaunchParams& P, cudaStream_t st) {
-  prep_kernel<<<(unsigned)(P.a.B * P.C), kPrepThreads, 0, st>>>(P);
+int launch_order(const LaunchParams& P, cudaStream_t st) {
+  order_kernel<<<1, kOrderThreads, 0, st>>>(P);
   return cudaGetLastError() == cudaSuccess ? CLSAMPLE_SUCCESS : CLSAMPLE_ERR_CUDA;
 }
 
-int launch_sampler(const Geometry& g, const LaunchParams& P, cudaStream_t st) {
-  cudaLaunchConfig_t cfg;
-  cudaLaunchAttribute attr[1];
-  fill_launch(g, (unsigned)P.a.B, st, &cfg, attr);
-  const cudaError_t err = P.a.logits_dtype == CLSAMPLE_LOGITS_BF16 ? cudaLaunchKernelEx(&cfg, sampler_kernel<true>, P)
-                                                                    : cudaLaunchKernelEx(&cfg, sampler_kernel<false>, P);
-  return err == cudaSuccess ? CLSAMPLE_SUCCESS : CLSAMPLE_ERR_CUDA;
+int launch_sampler(const Geometry& g, int grid, const LaunchParams& P, cudaStream_t st) {
+  if (P.a.logits_dtype == CLSAMPLE_LOGITS_BF16)
+    sampler_kernel<true><<<(unsigned)grid, kThreads, (size_t)g.smem, st>>>(P);
+  else
+    sampler_kernel<false><<<(unsigned)grid, kThreads, (size_t)g.smem, st>>>(P);
+  return cudaGetLastError() == cudaSuccess ? CLSAMPLE_SUCCESS : CLSAMPLE_ERR_CUDA;
 }
 
 }  // namespace
@@ -2580,25 +3451,28 @@ extern "C" {
 
 int clsample_apply(clsample_t* h, const clsample_args_t* a, clsample_stream_t stream) {
   LaunchParams P;
-  const int rc = make_params(h, a, &P);
+  int grid = 0;
+  const int rc = make_params(h, a, &P, &grid);
   if (rc != CLSAMPLE_SUCCESS || a->B == 0) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const int rp = launch_prep(P, st);
-  return rp != CLSAMPLE_SUCCESS ? rp : launch_sampler(h->g, P, st);
+  const int ro = launch_order(P, st);
+  return ro != CLSAMPLE_SUCCESS ? ro : launch_sampler(h->g, grid, P, st);
 }
 
 int clsample_prepare(clsample_t* h, const clsample_args_t* a, clsample_stream_t stream) {
   LaunchParams P;
-  const int rc = make_params(h, a, &P);
+  int grid = 0;
+  const int rc = make_params(h, a, &P, &grid);
   if (rc != CLSAMPLE_SUCCESS || a->B == 0) return rc;
-  return launch_prep(P, reinterpret_cast<cudaStream_t>(stream));
+  return launch_order(P, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int clsample_sample(clsample_t* h, const clsample_args_t* a, clsample_stream_t stream) {
   LaunchParams P;
-  const int rc = make_params(h, a, &P);
+  int grid = 0;
+  const int rc = make_params(h, a, &P, &grid);
   if (rc != CLSAMPLE_SUCCESS || a->B == 0) return rc;
-  return launch_sampler(h->g, P, reinterpret_cast<cudaStream_t>(stream));
+  return launch_sampler(h->g, grid, P, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int clsample_apply_static(const clsample_args_t* a, clsample_stream_t stream) {
@@ -2611,28 +3485,22 @@ int clsample_apply_static(const clsample_args_t* a, clsample_stream_t stream) {
   int rc = CLSAMPLE_SUCCESS;
   unsigned char* base = static_scratch(dev, &rc);
   if (!base) return rc;
-  const Scratch sc{kStaticRows, reinterpret_cast<PenEntry*>(base), reinterpret_cast<int2*>(base + kStaticOffPenN),
-                   reinterpret_cast<Cand*>(base + kStaticOffCand), reinterpret_cast<int*>(base + kStaticOffRows)};
+  const bool bf16 = a->logits_dtype == CLSAMPLE_LOGITS_BF16;
+  int grid = 0;
+  if ((rc = resident_ctas(g, bf16, dev, &grid)) != CLSAMPLE_SUCCESS) return rc;
+  const Scratch sc{kStaticRows, kMaxSlices, base};
   LaunchParams P;
-  rc = make_params(g, a->V, dev, sc, a, &P);
+  rc = make_params(g, a->V, dev, sc, grid, a, &P);
   if (rc != CLSAMPLE_SUCCESS || a->B == 0) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  rc = launch_prep(P, st);
-  return rc != CLSAMPLE_SUCCESS ? rc : launch_sampler(g, P, st);
+  rc = launch_order(P, st);
+  return rc != CLSAMPLE_SUCCESS ? rc : launch_sampler(g, grid, P, st);
 }
 
-int clsample_occupancy(clsample_t* h, int32_t logits_dtype, int32_t* max_active_clusters) {
-  if (!h || !max_active_clusters) return CLSAMPLE_ERR_NULL;
+int clsample_occupancy(clsample_t* h, int32_t logits_dtype, int32_t* resident_ctas_out) {
+  if (!h || !resident_ctas_out) return CLSAMPLE_ERR_NULL;
   if (logits_dtype != CLSAMPLE_LOGITS_F32 && logits_dtype != CLSAMPLE_LOGITS_BF16) return CLSAMPLE_ERR_DTYPE;
-  const bool bf16 = logits_dtype == CLSAMPLE_LOGITS_BF16;
-  cudaLaunchConfig_t cfg;
-  cudaLaunchAttribute attr[1];
-  fill_launch(h->g, 1u, nullptr, &cfg, attr);
-  int n = 0;
-  const cudaError_t err = bf16 ? cudaOccupancyMaxActiveClusters(&n, sampler_kernel<true>, &cfg)
-                               : cudaOccupancyMaxActiveClusters(&n, sampler_kernel<false>, &cfg);
-  if (err != cudaSuccess) return CLSAMPLE_ERR_CUDA;
-  *max_active_clusters = n;
+  *resident_ctas_out = h->grid[logits_dtype == CLSAMPLE_LOGITS_BF16 ? 1 : 0];
   return CLSAMPLE_SUCCESS;
 }
 

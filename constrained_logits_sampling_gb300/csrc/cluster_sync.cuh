@@ -1,6 +1,7 @@
 // Inline-PTX wrappers for the barriers and bulk memory operations the sampler uses on
 // sm_103a: mbarriers (local and remote arrive, cluster-scope acquire), the 1-D TMA bulk
-// copy global -> shared and the TMA bulk prefetch into L2.  Every wait is bounded.
+// copy global -> shared (optionally with an L2 eviction policy) and the TMA bulk
+// prefetch into L2.  Every wait is bounded.
 #pragma once
 
 #include <cstdint>
@@ -112,6 +113,30 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
           smem_addr(dst)),
       "l"(src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
+}
+
+// The same copy with an L2 eviction policy (from make_policy_evict_first or
+// make_policy_evict_normal) for the lines it brings into L2.
+__device__ __forceinline__ void bulk_copy_g2s_hint(void* dst, const void* src, uint32_t bytes,
+                                                   unsigned long long* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+      "%4;" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+// L2 policies: lines a stream reads once go first when L2 needs room; normal lines stay
+// as long as the usual replacement keeps them.
+__device__ __forceinline__ uint64_t make_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t make_policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 
 // Asks the TMA unit to bring `bytes` of global memory into L2 (no completion signal;

@@ -95,7 +95,7 @@ def geometry(vocab: int):
     L = load_library()
     c, k, s = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
     _check(L.clsample_geometry(vocab, ctypes.byref(c), ctypes.byref(k), ctypes.byref(s)))
-    return {"cluster": c.value, "chunk": k.value, "smem_bytes": s.value}
+    return {"slices": c.value, "chunk": k.value, "smem_bytes": s.value}
 
 
 def _stream_ptr(stream: Optional[torch.cuda.Stream]) -> int:
@@ -132,7 +132,8 @@ class Sampler:
         self._h = h
         self.max_batch, self.vocab = int(max_batch), int(vocab)
 
-    def max_active_clusters(self, bf16: bool = False) -> int:
+    def resident_ctas(self, bf16: bool = False) -> int:
+        """CTAs of the persistent sampler kernel (``clsample_occupancy``)."""
         n = ctypes.c_int32()
         _check(self._L.clsample_occupancy(self._h, LOGITS_BF16 if bf16 else LOGITS_F32, ctypes.byref(n)))
         return n.value
@@ -207,7 +208,7 @@ class Sampler:
         _check(self._L.clsample_apply(self._h, ctypes.byref(args), _stream_ptr(stream)))
 
     def prepare(self, args: Args, stream: Optional[torch.cuda.Stream] = None):
-        """Enqueue the row-preparation half of a call (``clsample_prepare``)."""
+        """Enqueue the ordering half of a call (``clsample_prepare``)."""
         _check(self._L.clsample_prepare(self._h, ctypes.byref(args), _stream_ptr(stream)))
 
     def sample(self, args: Args, stream: Optional[torch.cuda.Stream] = None):

@@ -26,13 +26,13 @@
  *      log-softmax (SGLang page, section "Numerical consistency of logprobs").
  *
  * Threading and ownership.  A handle is bound to the CUDA device that was current at
- * clsample_create and owns device scratch sized for max_batch rows (the penalised-token
- * lists, the compacted candidates and the rows' launch order; about 320 KB per row for
- * V = 151936).  Every array in clsample_args_t is a DEVICE pointer owned by the caller;
- * it must stay valid until the work enqueued on the stream has finished.  The logits
- * are read-only (never written in place).  Calls on one handle must be ordered (one
- * stream, or streams joined by events): they share the handle's scratch.  Separate
- * handles are independent.
+ * clsample_create and owns device scratch sized for max_batch rows (the rows' order and
+ * work list, per-slice records, penalised-token lists, tables of vector maxima and
+ * compacted candidates; about 370 KB per row for V = 151936).  Every array in
+ * clsample_args_t is a DEVICE pointer owned by the caller; it must stay valid until the
+ * work enqueued on the stream has finished.  The logits are read-only (never written in
+ * place).  Calls on one handle must be ordered (one stream, or streams joined by
+ * events): they share the handle's scratch.  Separate handles are independent.
  *
  * Errors.  Every entry point validates its arguments on the host, without any device
  * synchronisation, and returns a negative CLSAMPLE_ERR_* code on a bad argument;
@@ -106,10 +106,10 @@ enum {
  * dbg_kept_count    i32[B] output or NULL: size of the kept set K (1 for greedy rows).
  * dbg_cut           f32[B] output or NULL: min over K of y = (z' - max z') * (1/T).
  *
- * Limits: V <= 262144 (8 slices of at most 32768 tokens).  Per row, at most 1024
- * distinct penalised or biased ids may fall inside one vocabulary slice of
- * ceil(V / cluster) tokens (cluster = 8 for V > 14336); a row that exceeds it gets
- * status OVERFLOW.  Histories of up to 4096 ids never exceed it.
+ * Limits: V <= 262144 (at most 8 slices of at most 32768 tokens per row).  Per row, at
+ * most 512 distinct penalised or biased ids may fall inside one vocabulary slice of
+ * ceil(V / slices) tokens (slices = 8 for V > 14336); a row that exceeds it gets status
+ * OVERFLOW.
  */
 typedef struct {
   int32_t B, V;
@@ -152,44 +152,46 @@ int clsample_create(int32_t max_batch, int32_t vocab, clsample_t** out);
  * device, so no call on the handle may still be running. */
 void clsample_destroy(clsample_t* handle);
 
-/* Enqueues one sampler call on `stream`: a row-preparation kernel (penalised-token
- * lists, launch order) and the sampler kernel; nothing when B == 0.  Returns after
- * enqueueing; results are valid once the stream reaches this point. */
+/* Enqueues one sampler call on `stream`: a one-CTA kernel that orders the rows (heaviest
+ * first) and writes the work list, then the persistent sampler kernel (one CTA per
+ * resident slot; every CTA takes (row, slice) items from the list); nothing when B == 0.
+ * Returns after enqueueing; results are valid once the stream reaches this point. */
 int clsample_apply(clsample_t* handle, const clsample_args_t* args, clsample_stream_t stream);
 
 /* The two halves of clsample_apply, for callers that schedule or time them apart:
- * clsample_prepare enqueues the row-preparation kernel, clsample_sample the sampler
- * kernel, which reads what the last clsample_prepare on this handle wrote.  The pair,
- * with the same arguments on one stream, equals clsample_apply.  Same validation and
- * return codes. */
+ * clsample_prepare enqueues the ordering kernel, clsample_sample the sampler kernel,
+ * which reads the work list the last clsample_prepare on this handle wrote (the list
+ * may be sampled again with the same arguments).  The pair, with the same arguments on
+ * one stream, equals clsample_apply.  Same validation and return codes. */
 int clsample_prepare(clsample_t* handle, const clsample_args_t* args, clsample_stream_t stream);
 int clsample_sample(clsample_t* handle, const clsample_args_t* args, clsample_stream_t stream);
 
 /* One sampler call without a handle that allocates nothing.  The pages have no
  * counterpart: this is a deployment convenience of this library, and it samples
  * exactly like clsample_apply.  Its scratch is one fixed device array compiled into
- * the library (about 21 MB, zero when the library loads); no cudaMalloc or cudaFree
+ * the library (about 23 MB, zero when the library loads); no cudaMalloc or cudaFree
  * ever happens.  The first call on a device looks up the array's address on that
  * device (cudaGetSymbolAddress) and sets the kernels' shared-memory limit, once per
  * device, under a host lock.  Limits: B <= 64 (else CLSAMPLE_ERR_BATCH) and
  * V <= 262144 (else CLSAMPLE_ERR_VOCAB); nothing is enqueued on an error.
  * Races: every call on a device, from any host thread or stream, uses the same array,
  * so calls of this entry point on one device must be ordered (one stream, or streams
- * joined by events); two overlapping calls corrupt each other's lists and candidates.
+ * joined by events); two overlapping calls corrupt each other's work lists and records.
  * Calls through handles are unaffected, and each process has its own array. */
 int clsample_apply_static(const clsample_args_t* args, clsample_stream_t stream);
 
 /* Static description of a return code. */
 const char* clsample_strerror(int code);
 
-/* Launch geometry chosen for a vocabulary size: CTAs per row (one thread-block
- * cluster per row), tokens per CTA and dynamic shared memory per CTA.  Host-only;
- * needs no GPU.  Returns CLSAMPLE_SUCCESS or CLSAMPLE_ERR_VOCAB. */
-int clsample_geometry(int32_t vocab, int32_t* cluster, int32_t* chunk, int32_t* smem_bytes);
+/* Launch geometry chosen for a vocabulary size: slices per row, tokens per slice and
+ * dynamic shared memory per CTA.  Host-only; needs no GPU.  Returns CLSAMPLE_SUCCESS or
+ * CLSAMPLE_ERR_VOCAB. */
+int clsample_geometry(int32_t vocab, int32_t* slices, int32_t* chunk, int32_t* smem_bytes);
 
-/* How many thread-block clusters (rows) of this handle's launch can be resident on the
- * device at once, from cudaOccupancyMaxActiveClusters.  Needs the handle's device. */
-int clsample_occupancy(clsample_t* handle, int32_t logits_dtype, int32_t* max_active_clusters);
+/* How many CTAs the persistent sampler kernel of this handle launches: as many as can be
+ * resident on the device at once (cudaOccupancyMaxActiveBlocksPerMultiprocessor times
+ * the SM count), computed at clsample_create. */
+int clsample_occupancy(clsample_t* handle, int32_t logits_dtype, int32_t* resident_ctas);
 
 /* Diagnostics of the building blocks, on device arrays of length n (enqueued on
  * `stream`): the fixed-point top-p weight floor(exp32(y) * 2^40) of each y (y <= 0),

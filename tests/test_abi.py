@@ -49,13 +49,13 @@ def test_strerror_and_geometry(lib):
     for code in range(-7, 0):
         assert lib.clsample_strerror(code) != b"unknown error"
     g = sampler.geometry(151936)
-    assert g == {"cluster": 8, "chunk": 19008, "smem_bytes": g["smem_bytes"]}
+    assert g == {"slices": 8, "chunk": 19008, "smem_bytes": g["smem_bytes"]}
     assert g["smem_bytes"] <= 54 * 1024  # four CTAs per SM
-    assert sampler.geometry(262144)["cluster"] == 8
+    assert sampler.geometry(262144)["slices"] == 8
     with pytest.raises(sampler.ClsampleError):
         sampler.geometry(262145)
-    assert sampler.geometry(8)["cluster"] == 1
-    assert sampler.geometry(32000)["chunk"] * sampler.geometry(32000)["cluster"] >= 32000
+    assert sampler.geometry(8)["slices"] == 1
+    assert sampler.geometry(32000)["chunk"] * sampler.geometry(32000)["slices"] >= 32000
     with pytest.raises(sampler.ClsampleError):
         sampler.geometry(0)
 

@@ -241,9 +241,9 @@ def test_batch_composition_independence_gpu():
 
 def test_routes_and_fallbacks():
     """Rows that take each route: bounded top-k, min-p compaction (with and without
-    top-p), top-p alone (crossing bin resolved by the leader), top-p whose crossing bin
+    top-p), top-p alone (crossing bin resolved at the row end), top-p whose crossing bin
     overflows (flat row) or is the open-ended last bin, top-k with k > 4096 (no bound:
-    cluster-wide radix select), and the untruncated race."""
+    radix select over the whole row), and the untruncated race."""
     V = 151936
     rng = np.random.default_rng(21)
     rows, params = [], []

@@ -63,8 +63,7 @@ constexpr int kStageBytes = 8192;     // one ring stage
 constexpr int kStages = 4;            // ring depth
 constexpr int kReload = 4;            // 16-byte loads in flight per thread when re-reading
 constexpr int kTabMax = kMaxChunk * 4 / kStageBytes * kThreads;  // table entries per slice
-constexpr int kHitCap = kStages * kStageBytes / 4;                // table hits the row end keeps
-constexpr int kOrderThreads = 1024;
+constexpr int kOrderThreads = 512;
 constexpr int kSmallRow = 2048;   // allowed tokens of a row that the row end takes all of
 // penalised-token flags next to the history count
 constexpr uint32_t kAllowedBit = 0x80000000u;
@@ -152,6 +151,15 @@ struct RowState {
   unsigned long long above, cth;  // top-p alone: mass above the crossing bin; ceil(p W)
 };
 
+// One penalised / biased token of a slice, as the row preparation lists it.
+constexpr uint32_t kPenBias = 0x80000000u;  // in PenEntry::id: a logit_bias entry applies
+struct __align__(16) PenEntry {
+  uint32_t id;     // local id | kPenBias
+  uint32_t count;  // occurrences in the row's history (saturates at kCountMask)
+  float bias;      // the last bias entry's value
+  uint32_t pad;
+};
+
 struct LaunchParams {
   clsample_args_t a;
   int C;
@@ -168,7 +176,9 @@ struct LaunchParams {
   RowState* rows;     // [B]
   X1* x1;             // [B * C]
   X2* x2;             // [B * C]
-  uint2* pen;         // [B * C][kPenCap] penalised tokens: local id, bits of z'
+  PenEntry* plist;    // [B * C][kPenCap] penalised / biased tokens by id (row preparation)
+  int2* plist_n;      // [B * C] their number, flags
+  uint2* pen;         // [B * C][kPenCap] penalised tokens: local id, bits of z' (first phase)
   uint16_t* tab;      // [B * C][kTabMax] per-(stage, thread) maxima
   unsigned long long* phist;  // [B * C][kPBins] top-p bin masses
   Cand* cand;         // [B * C][kCandCap] compacted candidates
@@ -288,12 +298,13 @@ struct Shared {
   int csr[4];
   int poff[kMaxSlices + 1];
   float zth, res;
-  int bstar, nl, flags, count, digit, none, npen, nallowed, nhits, nhist, last, ok;
+  int bstar, nl, flags, count, digit, none, npen, nallowed, nhits, last, ok;
   unsigned item;
   uint32_t seq;  // ring stages consumed by this CTA so far (fixes each buffer's parity)
   uint64_t policy;  // L2 policy of the current slice's stream
   unsigned long long tbar;  // the row end's table copies
   uint32_t tpar;     // its phase parity
+  int tissued, tfail;  // copies issued and not yet waited for; a wait gave up
   unsigned long long above;
 };
 __shared__ Shared sh;
@@ -711,6 +722,8 @@ __device__ __forceinline__ void ring_start(const Geo& g, const Smem& S, uint32_t
   for (int k = 0; k < min(kStages, g.nst); ++k) ring_issue<kBF16>(g, S, k, seq0 + (uint32_t)k);
 }
 
+
+
 // Waits (bounded, suspending) for ring stage s.  Thread 0 only; a stage that never lands
 // marks the row OVERFLOW.
 __device__ __forceinline__ void ring_wait(uint32_t s) {
@@ -856,13 +869,196 @@ __device__ int order_scan(int x, int* red, int* total) {
   return before + incl - x;
 }
 
-// One CTA ahead of the sampler: resets the scratch's counters, orders the rows by class
-// (stable, heaviest first; order[] holds row | phases << 24) and writes the work list.
+
+constexpr int kRowPen = kPenCap * kMaxSlices;  // distinct penalised / biased ids of a row
+
+// Shared memory of a row preparation CTA for a vocabulary of V tokens.
+__host__ __device__ inline size_t prep_smem_bytes(int V) {
+  const size_t W = (size_t)(V + 31) / 32;
+  return sizeof(uint32_t) * 2 * W + sizeof(uint32_t) * 2 * kRowPen;
+}
+
+// Row preparation: one CTA of the ordering launch per row.  The row's history and
+// logit_bias ids are marked in a bitmap of the vocabulary (shared memory), ranked in
+// token order by a scan of the words' popcounts, counted (duplicates in a warp counted
+// once: Zipf-like histories repeat their frequent ids many times), and every bias entry
+// leaves its index at its id's rank, so that the last entry of an id wins (SGLang page,
+// "Order semantics of the penalties" and "Why logit_bias is built from triples").  Then
+// every slice gets its list of (local id, count, bias) in id order, with its length and
+// flags: INVALID for ids outside [0, V), decreasing CSR offsets or NaN bias values,
+// OVERFLOW for a slice with more than kPenCap distinct ids.
+__device__ __noinline__ void prep_row(const LaunchParams& P, int row) {
+  const clsample_args_t& a = P.a;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int W = (a.V + 31) / 32, C = P.C, chunk = P.chunk;
+  uint32_t* bits = reinterpret_cast<uint32_t*>(smem_dyn);  // [W]
+  uint32_t* prk = bits + W;                                 // [W] rank of each word's first id
+  uint32_t* cnt = prk + W;                                  // [kRowPen]
+  int* bidx = reinterpret_cast<int*>(cnt + kRowPen);        // [kRowPen]
+  __shared__ int pcsr[4], pflags, ptot;
+  __shared__ int pred[kOrderThreads / 32];
+  const bool has_hist = a.hist_offs != nullptr, has_bias = a.bias_offs != nullptr;
+  if (tid == 0) {
+    pcsr[0] = has_hist ? a.hist_offs[row] : 0;
+    pcsr[1] = has_hist ? a.hist_offs[row + 1] : 0;
+    pcsr[2] = has_bias ? a.bias_offs[row] : 0;
+    pcsr[3] = has_bias ? a.bias_offs[row + 1] : 0;
+    pflags = 0;
+  }
+  for (int w = tid; w < W; w += kOrderThreads) bits[w] = 0u;
+  for (int r = tid; r < kRowPen; r += kOrderThreads) {
+    cnt[r] = 0u;
+    bidx[r] = -1;
+  }
+  __syncthreads();
+  int flags = 0;
+  const int hlo = pcsr[0], hhi = pcsr[1], blo = pcsr[2], bhi = pcsr[3];
+  if (hlo < 0 || hhi < hlo || blo < 0 || bhi < blo) flags |= kFlagInvalid;
+  const bool hok = has_hist && hlo >= 0 && hhi >= hlo;
+  const bool bok = has_bias && blo >= 0 && bhi >= blo;
+  constexpr int kBatch = 8;
+  if (hok) {
+#pragma unroll 1
+    for (int base = hlo; base < hhi; base += kBatch * kOrderThreads) {
+      int ids[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int j = base + u * kOrderThreads + tid;
+        ids[u] = j < hhi ? __ldg(a.hist_ids + j) : INT_MIN;
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int id = ids[u];
+        if (id == INT_MIN) continue;
+        if (id < 0 || id >= a.V) {
+          flags |= kFlagInvalid;
+          continue;
+        }
+        const uint32_t bit = 1u << (id & 31);
+        if (!(bits[id >> 5] & bit)) atomicOr(&bits[id >> 5], bit);
+      }
+    }
+  }
+  if (bok) {
+    for (int j = blo + tid; j < bhi; j += kOrderThreads) {
+      const int id = __ldg(a.bias_ids + j);
+      const float b = __ldg(a.bias_vals + j);
+      if (id < 0 || id >= a.V || b != b) flags |= kFlagInvalid;
+      else atomicOr(&bits[id >> 5], 1u << (id & 31));
+    }
+  }
+  if (flags) atomicOr(&pflags, flags);
+  __syncthreads();
+  // ranks: an exclusive scan of the words' popcounts, consecutive words per thread
+  {
+    const int per = (W + kOrderThreads - 1) / kOrderThreads;
+    const int w0 = min(W, tid * per), w1 = min(W, w0 + per);
+    int loc = 0;
+    for (int w = w0; w < w1; ++w) loc += __popc(bits[w]);
+    int x = loc;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, x, d);
+      if (lane >= d) x += o;
+    }
+    if (lane == 31) pred[warp] = x;
+    __syncthreads();
+    int e = x - loc, tot = 0;
+    for (int wp = 0; wp < kOrderThreads / 32; ++wp) {
+      if (wp < warp) e += pred[wp];
+      tot += pred[wp];
+    }
+    for (int w = w0; w < w1; ++w) {
+      prk[w] = (uint32_t)e;
+      e += __popc(bits[w]);
+    }
+    if (tid == 0) ptot = tot;
+  }
+  __syncthreads();
+  auto rank_of = [&](int id) -> uint32_t {
+    return prk[id >> 5] + __popc(bits[id >> 5] & ((1u << (id & 31)) - 1u));
+  };
+  if (hok) {
+#pragma unroll 1
+    for (int base = hlo; base < hhi; base += kBatch * kOrderThreads) {
+      int ids[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int j = base + u * kOrderThreads + tid;
+        ids[u] = j < hhi ? __ldg(a.hist_ids + j) : INT_MIN;
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int id = ids[u];
+        int r = -1;
+        if (id >= 0 && id < a.V) {
+          const uint32_t rr = rank_of(id);
+          r = rr < (uint32_t)kRowPen ? (int)rr : -1;
+        }
+        const uint32_t peers = __match_any_sync(0xffffffffu, r);
+        if (r >= 0 && lane == __ffs(peers) - 1) atomicAdd(&cnt[r], (uint32_t)__popc(peers));
+      }
+    }
+  }
+  if (bok) {
+    for (int j = blo + tid; j < bhi; j += kOrderThreads) {
+      const int id = __ldg(a.bias_ids + j);
+      const float b = __ldg(a.bias_vals + j);
+      if (id >= 0 && id < a.V && b == b) {
+        const uint32_t r = rank_of(id);
+        if (r < (uint32_t)kRowPen) atomicMax(&bidx[r], j);
+      }
+    }
+  }
+  __syncthreads();
+  // the slices' lists, in id order
+  PenEntry* out = P.plist + (size_t)row * C * kPenCap;
+  for (int w = tid; w < W; w += kOrderThreads) {
+    uint32_t b = bits[w];
+    uint32_t r = prk[w];
+    while (b) {
+      const int bit = __ffs(b) - 1;
+      b &= b - 1u;
+      const int id = 32 * w + bit;
+      const int sl = id / chunk;
+      const uint32_t rs = prk[(sl * chunk) >> 5];
+      const uint32_t p = r - rs;
+      if (r < (uint32_t)kRowPen && p < (uint32_t)kPenCap) {
+        const int bj = bidx[r];
+        PenEntry en;
+        en.id = (uint32_t)(id - sl * chunk) | (bj >= 0 ? kPenBias : 0u);
+        en.count = min(cnt[r], kCountMask);
+        en.bias = bj >= 0 ? __ldg(a.bias_vals + bj) : 0.0f;
+        en.pad = 0u;
+        out[(size_t)sl * kPenCap + p] = en;
+      }
+      ++r;
+    }
+  }
+  if (tid < C) {
+    const uint32_t r0 = prk[(tid * chunk) >> 5];
+    const uint32_t r1 = tid + 1 < C ? prk[((tid + 1) * chunk) >> 5] : (uint32_t)ptot;
+    int f = pflags;
+    if (r1 - r0 > (uint32_t)kPenCap || r1 > (uint32_t)kRowPen) f |= kFlagOverflow;
+    P.plist_n[(size_t)row * C + tid] = make_int2((int)min(r1 - r0, (uint32_t)kPenCap), f);
+  }
+}
+
+// The ordering launch ahead of the sampler.  CTA 0 resets the scratch's counters, orders
+// the rows by class (stable, heaviest first; order[] holds row | phases << 24) and writes
+// the work list; CTAs 1 .. B (when the call has penalties or logit_bias) prepare the rows'
+// penalised-token lists.
 // List slot j holds the first phase of order[j], then the second phase of order[j - gap]
 // and the third of order[j - 2 gap] where those rows have them (slots j >= B hold only
 // those), so that a row's next phase comes about one wave of items after its previous
 // one.
-__global__ void __launch_bounds__(kOrderThreads) order_kernel(const __grid_constant__ LaunchParams P) {
+__global__ void __launch_bounds__(kOrderThreads, 2) order_kernel(const __grid_constant__ LaunchParams P) {
+  // the sampler may be scheduled now: it waits for this grid's results (griddepcontrol.wait)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (blockIdx.x > 0) {
+    prep_row(P, (int)blockIdx.x - 1);
+    return;
+  }
   __shared__ int red[kOrderThreads / 32];
   const clsample_args_t& a = P.a;
   const int B = a.B, tid = threadIdx.x;
@@ -1011,57 +1207,46 @@ __device__ int rank_words(const Smem& S, int nw) {
 
 // First phase of a slice, before pass A: thread 0 starts the slice's first ring stages,
 // then the row parameters, the live bits (bitmask words clipped to the row) and the
-// slice's penalised / biased tokens: the row's history and logit_bias ids that fall in
-// the slice are marked in `mod` (SGLang page, "Order semantics of the penalties" and
-// "Why logit_bias is built from triples") while the history's in-slice ids are compacted
-// into r2; a scan ranks the marked ids in token order, then every compacted id adds one
-// to its rank's count (a history whose in-slice ids overflow r2 is read a second time)
-// and every bias entry leaves its index, so that the last one wins.  The bitmask's
-// verdict on each listed token moves into its entry and the token leaves the live set
-// (pass A gives it its final value).  A slice with more than kPenCap distinct ids is
-// flagged OVERFLOW.
+// slice's penalised / biased tokens from the row preparation's list (in id order, so an
+// entry's index is the token's rank); the bitmask's verdict on each moves into its entry
+// and the token leaves the live set (pass A gives it its final value).
 template <bool kBF16>
 __device__ __noinline__ void setup_p1(const LaunchParams& P, int row, int slice, int nph) {
   const Geo g = geo<kBF16>(P, row, slice);
   const Smem S = carve(g.chunk);
   const clsample_args_t& a = P.a;
   const int tid = threadIdx.x, lane = tid & 31;
-  const int c0 = g.c0, c1 = g.c0 + g.len, nw = g.chunk / 32;
+  const int nw = g.chunk / 32;
   const int32_t* bmrow = a.bitmask ? a.bitmask + (long long)row * a.bitmask_row_stride : nullptr;
-  const bool has_hist = a.hist_offs != nullptr, has_bias = a.bias_offs != nullptr;
-  int* pbidx = reinterpret_cast<int*>(S.pbias);
-  uint16_t* hbuf = reinterpret_cast<uint16_t*>(S.r2);  // the history's in-slice ids
-  constexpr int kHbufCap = (int)(kR2Bytes / sizeof(uint16_t));
-
+  const bool has_mod = a.hist_offs != nullptr || a.bias_offs != nullptr;
+  const size_t rc = (size_t)row * P.C + slice;
+  (void)nph;
   if (tid == 0) {
     sh.flags = 0;
     sh.count = 0;
-    sh.nallowed = 0;
-    sh.npen = 0;
-    sh.nhist = 0;
-    // a row that later phases read again whole keeps its lines in L2; the others are
-    // read once (the row end re-reads a few vectors) and go first when L2 needs room, so
-    // that the slice records, lists and tables the row ends read stay in L2
-    sh.policy = nph >= 2 ? make_policy_evict_normal() : make_policy_evict_first();
+    sh.nallowed = 0;  // (sh.npen is thread 64's)
+    // the row end (or a later phase) reads parts of the slice again soon: normal lines
+    sh.policy = make_policy_evict_normal();
     ring_start<kBF16>(g, S, sh.seq);
   } else if (tid == 32) {
     sh.rp = load_params(a, row);
   } else if (tid == 64) {
-    sh.csr[0] = has_hist ? a.hist_offs[row] : 0;
-    sh.csr[1] = has_hist ? a.hist_offs[row + 1] : 0;
-    sh.csr[2] = has_bias ? a.bias_offs[row] : 0;
-    sh.csr[3] = has_bias ? a.bias_offs[row + 1] : 0;
+    const int2 nf = has_mod ? P.plist_n[rc] : make_int2(0, 0);
+    sh.npen = nf.x;
+    sh.csr[0] = nf.y;  // the row preparation's flags
+  }
+  // the list is loaded whole (its length arrives with it): kPenCap / kThreads per thread
+  PenEntry en[kPenCap / kThreads];
+  if (has_mod) {
+#pragma unroll
+    for (int t = 0; t < kPenCap / kThreads; ++t) en[t] = P.plist[rc * kPenCap + t * kThreads + tid];
   }
   for (int w = tid; w < nw; w += kThreads) {
-    S.live[w] = mask_word(bmrow, c0, g.len, w);
+    S.live[w] = mask_word(bmrow, g.c0, g.len, w);
     S.mod[w] = 0u;
   }
-  for (int r = tid; r < kPenCap; r += kThreads) {
-    S.pcnt[r] = 0u;
-    pbidx[r] = -1;
-  }
   __syncthreads();
-  if (!has_hist && !has_bias) {
+  if (!has_mod) {
     int na = 0;
     for (int w = tid; w < nw; w += kThreads) na += __popc(S.live[w]);
     na = __reduce_add_sync(0xffffffffu, na);
@@ -1069,115 +1254,25 @@ __device__ __noinline__ void setup_p1(const LaunchParams& P, int row, int slice,
     __syncthreads();
     return;
   }
-  int flags = 0;
-  const int hlo = sh.csr[0], hhi = sh.csr[1], blo = sh.csr[2], bhi = sh.csr[3];
-  if (hlo < 0 || hhi < hlo || blo < 0 || bhi < blo) flags |= kFlagInvalid;
-  const bool hok = has_hist && hlo >= 0 && hhi >= hlo;
-  const bool bok = has_bias && blo >= 0 && bhi >= blo;
-  if (hok) {
-#pragma unroll 1
-    for (int base = hlo; base < hhi; base += 16 * kThreads) {
-      int ids[16];
+  const int npen = sh.npen;
+  if (tid == 0 && sh.csr[0]) sh.flags |= sh.csr[0];
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int j = base + u * kThreads + tid;
-        ids[u] = j < hhi ? __ldg(a.hist_ids + j) : INT_MIN;
-      }
-#pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int id = ids[u];
-        if (id != INT_MIN && (id < 0 || id >= a.V)) flags |= kFlagInvalid;
-        const bool mine = id >= c0 && id < c1;
-        const uint32_t l = mine ? (uint32_t)(id - c0) : 0u;
-        if (mine) {
-          const uint32_t bit = 1u << (l & 31);
-          if (!(S.mod[l >> 5] & bit)) atomicOr(&S.mod[l >> 5], bit);
-        }
-        const uint32_t bal = __ballot_sync(0xffffffffu, mine);
-        if (bal) {
-          const int leader = __ffs(bal) - 1;
-          int pos = 0;
-          if (lane == leader) pos = atomicAdd(&sh.nhist, __popc(bal));
-          pos = __shfl_sync(0xffffffffu, pos, leader) + __popc(bal & ((1u << lane) - 1u));
-          if (mine && pos < kHbufCap) hbuf[pos] = (uint16_t)l;
-        }
-      }
-    }
-  }
-  if (bok) {
-    for (int j = blo + tid; j < bhi; j += kThreads) {
-      const int id = __ldg(a.bias_ids + j);
-      const float b = __ldg(a.bias_vals + j);
-      if (id < 0 || id >= a.V || b != b) {
-        flags |= kFlagInvalid;
-      } else if (id >= c0 && id < c1) {
-        const uint32_t l = (uint32_t)(id - c0);
-        atomicOr(&S.mod[l >> 5], 1u << (l & 31));
-      }
-    }
-  }
-  if (flags) atomicOr(&sh.flags, flags);
-  __syncthreads();
-  const int total = rank_words(S, nw);
-  const int npen = min(total, kPenCap);
-  if (tid == 0) {
-    sh.npen = npen;
-    if (total > kPenCap) sh.flags |= kFlagOverflow;
-  }
-  // the listed ids in token order
-  for (int w = tid; w < nw; w += kThreads) {
-    uint32_t bits = S.mod[w];
-    int r = S.prank[w];
-    while (bits && r < kPenCap) {
-      const int b = __ffs(bits) - 1;
-      bits &= bits - 1u;
-      S.pid[r++] = (uint16_t)(32 * w + b);
-    }
-  }
-  auto rank_of = [&](uint32_t l) -> int {
-    return S.prank[l >> 5] + __popc(S.mod[l >> 5] & ((1u << (l & 31)) - 1u));
-  };
-  const int nhist = sh.nhist;
-  if (nhist <= kHbufCap) {
-    for (int i = tid; i < nhist; i += kThreads) {
-      const int r = rank_of(hbuf[i]);
-      if (r < kPenCap) atomicAdd(&S.pcnt[r], 1u);
-    }
-  } else if (hok) {
-    for (int j = hlo + tid; j < hhi; j += kThreads) {
-      const int id = __ldg(a.hist_ids + j);
-      if (id >= c0 && id < c1) {
-        const int r = rank_of((uint32_t)(id - c0));
-        if (r < kPenCap) atomicAdd(&S.pcnt[r], 1u);
-      }
-    }
-  }
-  if (bok) {
-    for (int j = blo + tid; j < bhi; j += kThreads) {
-      const int id = __ldg(a.bias_ids + j);
-      const float b = __ldg(a.bias_vals + j);
-      if (id >= c0 && id < c1 && b == b) {
-        const int r = rank_of((uint32_t)(id - c0));
-        if (r < kPenCap) atomicMax(&pbidx[r], j);
-      }
-    }
-  }
-  __syncthreads();
-  // the bitmask's verdict and the bias value move into each entry; the token leaves the
-  // live set
-  for (int r = tid; r < npen; r += kThreads) {
-    const uint32_t l = S.pid[r], bit = 1u << (l & 31);
-    uint32_t c = min(S.pcnt[r], kCountMask);
-    const int bj = pbidx[r];
-    if (bj >= 0) {
-      c |= kBiasBit;
-      S.pbias[r] = __ldg(a.bias_vals + bj);
-    }
+  for (int t = 0; t < kPenCap / kThreads; ++t) {
+    const int r = t * kThreads + tid;
+    if (r >= npen) continue;
+    const uint32_t l = en[t].id & ~kPenBias;
+    const uint32_t bit = 1u << (l & 31);
+    uint32_t c = min(en[t].count, kCountMask);
+    if (en[t].id & kPenBias) c |= kBiasBit;
     if (S.live[l >> 5] & bit) c |= kAllowedBit;
+    S.pid[r] = (uint16_t)l;
     S.pcnt[r] = c;
+    S.pbias[r] = en[t].bias;
     atomicAnd(&S.live[l >> 5], ~bit);
+    atomicOr(&S.mod[l >> 5], bit);
   }
   __syncthreads();
+  (void)rank_words(S, nw);
   {
     int na = 0;
     for (int w = tid; w < nw; w += kThreads) na += __popc(S.live[w]);
@@ -1975,317 +2070,113 @@ __device__ float entry_bound_z(uint32_t E, float m, float invT) {
   return r;
 }
 
-// Candidates of a fast row: every token with z >= zth (the exact z image of theta) that
-// can be kept; for a top-k row only those in groups that can reach the k-th largest.
-// Found by the CTA that ends the row's first phase, with few rounds of loads:
-//  1. the listed penalised tokens of every slice (by their z'), the slices' ragged tails
-//     and their tables of group maxima, loaded together: groups whose entry reaches
-//     key(zth) are listed, and for a top-k row a histogram of those entries fixes the
-//     k-th largest entry E (at least k groups, hence k tokens, reach E, so every token of
-//     the top-k set lies in a group whose entry reaches E); the list keeps the groups
-//     reaching E;
-//  2. the listed groups' vectors, re-read from L2 with their bitmask words.
-// Slices without a table, and every slice when the list overflows, are re-read whole.
-// Then top-k -> top-p -> min-p and the race.  Returns false when the candidates overflow
-// the row's segments.
+// The fallback of fast_serial (unaligned rows, tables too large for shared memory, too
+// many listed groups, a table copy that never landed): every slice is re-read whole and
+// its tokens with z >= zth (the exact z image of theta) are compacted, listed penalised
+// tokens by their z'.  Then top-k -> top-p -> min-p and the race.  Returns false when
+// the candidates overflow the row's segments.
 template <bool kBF16>
 __device__ __noinline__ bool fast_serial_global(const LaunchParams& P, int row) {
-  constexpr int kEsize = kBF16 ? 2 : 4;
-  constexpr int kVecPerStage = kStageBytes / (4 * kEsize);
-  constexpr int kVPT = kVecPerStage / kThreads;
-  constexpr int kTabLoads = 5;  // 16-byte table loads per thread per round
-  constexpr int kPenLoads = 4;  // list entries per thread per round
   const Smem S = carve(P.chunk);
-  const clsample_args_t& a = P.a;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int C = P.C, chunk = P.chunk;
-  const RowParams q = sh.rp;
-  const bool kfin = q.k >= 2;
+  const int C = P.C;
   const float m = sh.rs.m, invT = sh.rs.invT, theta = sh.rs.theta;
   const int cap = C * kCandCap;
   Cand* seg = P.cand + (size_t)row * C * kCandCap;
-  uint16_t* pids = reinterpret_cast<uint16_t*>(S.r2);
-  uint32_t* bins = reinterpret_cast<uint32_t*>(S.r2 + kPidsBytes);
-  uint32_t* hits = reinterpret_cast<uint32_t*>(S.ring);
-  uint16_t* hval = reinterpret_cast<uint16_t*>(S.ring + kHitList * 4);
-  Cand* csm = reinterpret_cast<Cand*>(S.ring + kHitList * 6);
-  const int32_t* bmrow = a.bitmask ? a.bitmask + (long long)row * a.bitmask_row_stride : nullptr;
-  const unsigned char* lrow =
-      reinterpret_cast<const unsigned char*>(a.logits) + (long long)row * a.logits_row_stride * kEsize;
+  __syncthreads();
   if (warp == 0) {
     const float zt = z_threshold_warp(theta, m, invT);
-    if (lane == 0) sh.zth = zt;
-  }
-  if (tid == 0) {
-    sh.count = 0;
-    sh.nhits = 0;
-    int o = 0;
-    for (int s = 0; s < C; ++s) {
-      sh.poff[s] = o;
-      o += min(sh.x1[s].npen, kPenCap);
+    if (lane == 0) {
+      sh.zth = zt;
+      sh.count = 0;
     }
-    sh.poff[C] = o;
   }
-  bins[tid] = 0u;
   __syncthreads();
   const float zth = sh.zth;
-  float zcut = zth;  // candidates: z >= zcut (tightened for top-k rows below)
-  uint32_t thr = tab_threshold(zth);
-  const uint32_t top = fkey(m) >> 16;
-  int shift = 0;
-  while (((top - min(top, thr)) >> shift) >= 256u) ++shift;
-  int any_full = 0;
-  for (int s = 0; s < C; ++s) any_full |= !sh.x1[s].tab;
-  const int n16max = (int)((((size_t)chunk * kEsize) + kStageBytes - 1) / kStageBytes) * kThreads * 2 / 16;
-  const int nchunks = C * n16max;
-  const int npen_all = sh.poff[C];
-  const int rounds = max((npen_all + kPenLoads * kThreads - 1) / (kPenLoads * kThreads),
-                         (nchunks + kTabLoads * kThreads - 1) / (kTabLoads * kThreads));
-
-  // 1. lists, tails and tables
-  float tz = -INFINITY;  // this thread's tail token (threads < 8 C)
-  int tgi = -1;
-  if (tid < C * 8) {
-    const int s = tid >> 3;
-    int len;
-    const int l = bulk_of<kBF16>(P, s, &len) + (tid & 7);
-    if (sh.x1[s].tab && l < len) {
-      const int gi = s * chunk + l;
-      const bool allowed = !bmrow || (((uint32_t)__ldg(bmrow + (gi >> 5)) >> (gi & 31)) & 1u);
-      tgi = gi;
-      tz = allowed ? sanitize(gload1<kBF16>(lrow, gi)) : -INFINITY;
-    }
-  }
-  auto table_round = [&](int rd, bool count, bool with_values) {
-    uint4 te[kTabLoads];
-    bool tok[kTabLoads];
+#pragma unroll 1
+  for (int s = 0; s < C; ++s) {
+    setup_re<kBF16>(P, row, s);
+    const Geo g = geo<kBF16>(P, row, s);
+    stream_ldg<kBF16>(g, S, [&](int f, uint32_t wd, const float4& v) {
+      float z[4];
 #pragma unroll
-    for (int u = 0; u < kTabLoads; ++u) {
-      const int i = rd * kTabLoads * kThreads + u * kThreads + tid;
-      const int s = i / n16max, c = i - s * n16max;
-      int len;
-      const int bulk = s < C ? bulk_of<kBF16>(P, s, &len) : 0;
-      const int n16 = (bulk * kEsize + kStageBytes - 1) / kStageBytes * kThreads * 2 / 16;
-      tok[u] = i < nchunks && sh.x1[s].tab && c < n16;
-      te[u] = tok[u] ? __ldcg(reinterpret_cast<const uint4*>(P.tab + ((size_t)row * C + s) * kTabMax) + c)
-                     : make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int u = 0; u < kTabLoads; ++u) {
-      const int i = rd * kTabLoads * kThreads + u * kThreads + tid;
-      const int s = i / n16max, c = i - s * n16max;
-      const uint32_t w4[4] = {te[u].x, te[u].y, te[u].z, te[u].w};
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint32_t ent = (w4[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
-        const bool hit = tok[u] && ent >= thr;
-        if (count && hit) atomicAdd(&bins[min((ent - thr) >> shift, 255u)], 1u);
-        const uint32_t bal = __ballot_sync(0xffffffffu, hit);
-        if (!bal) continue;
-        const int leader = __ffs(bal) - 1;
-        int pos = 0;
-        if (lane == leader) pos = atomicAdd(&sh.nhits, __popc(bal));
-        pos = __shfl_sync(0xffffffffu, pos, leader) + __popc(bal & ((1u << lane) - 1u));
-        if (hit && pos < kHitList) {
-          hits[pos] = ((uint32_t)s << 16) | (uint32_t)(8 * c + j);
-          if (with_values) hval[pos] = (uint16_t)ent;
+      for (int j = 0; j < 4; ++j) z[j] = ((wd >> j) & 1u) ? sanitize(comp(v, j)) : -INFINITY;
+      const bool any = __any_sync(0xffffffffu, z[0] >= zth || z[1] >= zth || z[2] >= zth || z[3] >= zth);
+      if (any) {
+#pragma unroll 1
+        for (int j = 0; j < 4; ++j) {
+          const bool keep = z[j] > -INFINITY && z[j] >= zth;
+          append(seg, cap, keep, keep ? y_of(z[j], m, invT) : 0.0f, g.c0 + 4 * f + j);
         }
       }
-    }
-  };
-  const int trounds = (nchunks + kTabLoads * kThreads - 1) / (kTabLoads * kThreads);
-  const int prounds = (npen_all + kPenLoads * kThreads - 1) / (kPenLoads * kThreads);
-#pragma unroll 1
-  for (int rd = 0; rd < max(trounds, prounds); ++rd) {
-    if (rd < prounds) {
-      uint2 pe[kPenLoads];
-#pragma unroll
-      for (int u = 0; u < kPenLoads; ++u) {
-        const int i = rd * kPenLoads * kThreads + u * kThreads + tid;
-        int s = 0;
-        while (s + 1 < C && sh.poff[s + 1] <= i) ++s;
-        pe[u] = i < npen_all ? __ldcg(P.pen + ((size_t)row * C + s) * kPenCap + (i - sh.poff[s]))
-                             : make_uint2(0u, 0u);
-      }
-#pragma unroll
-      for (int u = 0; u < kPenLoads; ++u) {
-        const int i = rd * kPenLoads * kThreads + u * kThreads + tid;
-        if (i >= npen_all) continue;
-        int s = 0;
-        while (s + 1 < C && sh.poff[s + 1] <= i) ++s;
-        pids[i] = (uint16_t)pe[u].x;
-        const float z = __uint_as_float(pe[u].y);
-        if (z > -INFINITY && z >= zth) append2_1(csm, kCandSmem, seg, cap, y_of(z, m, invT), s * chunk + (int)pe[u].x);
-      }
-    }
-    if (rd < trounds) table_round(rd, kfin, true);
-  }
-  __syncthreads();  // every list id is in shared memory
-  if (tgi >= 0 && tz > -INFINITY && tz >= zth && !listed(pids, tgi / chunk, (uint32_t)(tgi % chunk)))
-    append2_1(csm, kCandSmem, seg, cap, y_of(tz, m, invT), tgi);
-  // the k-th largest entry: the histogram's crossing bin
-  if (kfin) {
-    if (warp == 0) pick_digit(bins, (unsigned long long)q.k, &sh.digit, &sh.above, &sh.none);
-    __syncthreads();
-    if (!sh.none) {
-      zcut = fmaxf(zth, entry_bound_z(thr + ((uint32_t)sh.digit << shift), m, invT));
-      thr = tab_threshold(zcut);
-    }
-  }
-  int nh = sh.nhits;
-  bool overflow = nh > kHitList;
-  if (overflow && kfin) {
-    // the list overflowed at key(zth): list the groups again at the tightened threshold
-    __syncthreads();
-    if (tid == 0) sh.nhits = 0;
-    __syncthreads();
-#pragma unroll 1
-    for (int rd = 0; rd < trounds; ++rd) table_round(rd, false, false);
-    __syncthreads();
-    nh = sh.nhits;
-    overflow = nh > kHitList;
-  } else if (!overflow && kfin) {
-    // keep the listed groups that reach the tightened threshold
-    constexpr int kPer = kHitList / kThreads;
-    uint32_t hc[kPer];
-    bool keep[kPer];
-#pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-      const int h = u * kThreads + tid;
-      keep[u] = h < nh && hval[h] >= thr;
-      hc[u] = keep[u] ? hits[h] : 0u;
-    }
-    __syncthreads();
-    if (tid == 0) sh.nhits = 0;
-    __syncthreads();
-#pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-      const uint32_t bal = __ballot_sync(0xffffffffu, keep[u]);
-      if (!bal) continue;
-      const int leader = __ffs(bal) - 1;
-      int pos = 0;
-      if (lane == leader) pos = atomicAdd(&sh.nhits, __popc(bal));
-      pos = __shfl_sync(0xffffffffu, pos, leader) + __popc(bal & ((1u << lane) - 1u));
-      if (keep[u]) hits[pos] = hc[u];
-    }
-    __syncthreads();
-    nh = sh.nhits;
-  }
-  if (!overflow) {
-    // 2. the listed groups' vectors with their bitmask words
-    constexpr int kHitBatch = kBF16 ? 1 : 2;
-#pragma unroll 1
-    for (int h0 = 0; h0 < nh; h0 += kHitBatch * kThreads) {
-      float4 v[kHitBatch][kVPT];
-      uint32_t mw[kHitBatch][kVPT];
-      int hs[kHitBatch], hf[kHitBatch];
-#pragma unroll
-      for (int b = 0; b < kHitBatch; ++b) {
-        const int h = h0 + b * kThreads + tid;
-        const bool valid = h < nh;
-        const uint32_t code = valid ? hits[h] : 0u;
-        const int s = (int)(code >> 16), e = (int)(code & 0xFFFFu);
-        const int k = e / kThreads, tt = e % kThreads;
-        const int c0s = s * chunk;
-        int len;
-        const int bulk = bulk_of<kBF16>(P, s, &len);
-        hs[b] = s;
-        hf[b] = k * kVecPerStage + tt;
-#pragma unroll
-        for (int u = 0; u < kVPT; ++u) {
-          const int f = hf[b] + u * kThreads;
-          const bool in = valid && 4 * f < bulk;
-          v[b][u] = in ? vload4<kBF16>(lrow + (size_t)c0s * kEsize, f) : make_float4(0.f, 0.f, 0.f, 0.f);
-          mw[b][u] = in ? ((bmrow ? (uint32_t)__ldg(bmrow + ((c0s + 4 * f) >> 5)) : 0xFFFFFFFFu) >> ((4 * f) & 31)) & 0xFu
-                        : 0u;
-        }
-      }
-#pragma unroll
-      for (int b = 0; b < kHitBatch; ++b) {
-#pragma unroll
-        for (int u = 0; u < kVPT; ++u) {
-          const int f = hf[b] + u * kThreads;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            bool keep = false;
-            float z = -INFINITY;
-            if ((mw[b][u] >> j) & 1u) {
-              z = sanitize(comp(v[b][u], j));
-              keep = z > -INFINITY && z >= zcut && !listed(pids, hs[b], (uint32_t)(4 * f + j));
-            }
-            append2(csm, kCandSmem, seg, cap, keep, keep ? y_of(z, m, invT) : 0.0f, hs[b] * chunk + 4 * f + j);
-          }
-        }
-      }
-    }
-  }
-  // slices without a table (or all of them after an overflow of the list): whole
-  if (any_full || overflow) {
-    if (overflow) {
-      __syncthreads();
-      if (tid == 0) sh.count = 0;  // start over: every slice is re-read whole
-      __syncthreads();
-      // the listed penalised tokens again
-      for (int i = tid; i < npen_all; i += kThreads) {
-        int s = 0;
-        while (s + 1 < C && sh.poff[s + 1] <= i) ++s;
-        const uint2 e = __ldcg(P.pen + ((size_t)row * C + s) * kPenCap + (i - sh.poff[s]));
-        const float z = __uint_as_float(e.y);
-        if (z > -INFINITY && z >= zth) append2_1(csm, kCandSmem, seg, cap, y_of(z, m, invT), s * chunk + (int)e.x);
-      }
-    }
-    for (int s = 0; s < C; ++s) {
-      if (sh.x1[s].tab && !overflow) continue;
-      setup_re<kBF16>(P, row, s);
-      const Geo g = geo<kBF16>(P, row, s);
-      stream_ldg<kBF16>(g, S, [&](int f, uint32_t wd, const float4& v) {
-        float z[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) z[j] = ((wd >> j) & 1u) ? sanitize(comp(v, j)) : -INFINITY;
-        const bool any = __any_sync(0xffffffffu, z[0] >= zth || z[1] >= zth || z[2] >= zth || z[3] >= zth);
-        if (any) {
-#pragma unroll 1
-          for (int j = 0; j < 4; ++j) {
-            const bool keep = z[j] > -INFINITY && z[j] >= zth;
-            append2(csm, kCandSmem, seg, cap, keep, keep ? y_of(z[j], m, invT) : 0.0f, g.c0 + 4 * f + j);
-          }
-        }
-      });
+    });
+    for (int r = tid; r < sh.npen; r += kThreads) {
+      const float z = S.pz[r];
+      if (z > -INFINITY && z >= zth) append1(seg, cap, y_of(z, m, invT), g.c0 + (int)S.pid[r]);
     }
   }
   __threadfence_block();
   __syncthreads();
   const int n = sh.count;
   if (n > cap) return false;
-  const bool global = n > kCandSmem;
-  leader_finish(P, row, global ? seg : csm, n, global, 0ull);
+  bool global;
+  const Cand* G = gather_small(S, seg, n, &global);
+  leader_finish(P, row, G, n, global, 0ull);
   return true;
 }
 
 
-// Block-wide sum of one int per thread (every thread gets it).
-__device__ __forceinline__ int block_sum_int(int v) {
-  v = __reduce_add_sync(0xffffffffu, v);
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) sh.red_i[threadIdx.x >> 5] = v;
-  __syncthreads();
-  int t = 0;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) t += sh.red_i[w];
-  return t;
+
+
+// The row end's bulk copies of every slice's table into shared memory [0, C * tabstride),
+// on the row end's barrier (thread 0).  The tables are other CTAs' ordinary stores
+// (acquired through the ticket), read here by the async proxy: the proxy fence orders
+// them (global and shared state spaces).
+template <bool kBF16>
+__device__ void tables_issue(const LaunchParams& P, int row) {
+  constexpr int kEsize = kBF16 ? 2 : 4;
+  const int C = P.C;
+  const int nst_max = (int)(((size_t)P.chunk * kEsize + kStageBytes - 1) / kStageBytes);
+  const int tabstride = nst_max * kThreads * (int)sizeof(uint16_t);
+  asm volatile("fence.proxy.async;" ::: "memory");
+  uint32_t bytes = 0;
+  for (int s = 0; s < C; ++s) {
+    const int c0 = s * P.chunk;
+    const int len = max(0, min(P.a.V, c0 + P.chunk) - c0);
+    const int bulk = P.vec_ok ? (int)(((size_t)len * kEsize) & ~(size_t)15) : 0;
+    bytes += (uint32_t)((bulk + kStageBytes - 1) / kStageBytes * kThreads * 2);
+  }
+  mbar_arrive_expect_tx(&sh.tbar, bytes);
+  for (int s = 0; s < C; ++s) {
+    const int c0 = s * P.chunk;
+    const int len = max(0, min(P.a.V, c0 + P.chunk) - c0);
+    const int bulk = P.vec_ok ? (int)(((size_t)len * kEsize) & ~(size_t)15) : 0;
+    const uint32_t b = (uint32_t)((bulk + kStageBytes - 1) / kStageBytes * kThreads * 2);
+    if (b) bulk_copy_g2s(smem_dyn + (size_t)s * tabstride, P.tab + ((size_t)row * C + s) * kTabMax, b, &sh.tbar);
+  }
+  sh.tissued = 1;
 }
 
-// Entries >= thr among this thread's share of the tables in shared memory (chunks of 8
-// entries, `nch` chunks in all).
-__device__ __forceinline__ int count_entries(const uint4* tabs, int nch, uint32_t thr) {
-  int c = 0;
-  for (int i = threadIdx.x; i < nch; i += kThreads) {
-    const uint4 e = tabs[i];
-    const uint32_t w4[4] = {e.x, e.y, e.z, e.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) c += ((w4[j] & 0xFFFFu) >= thr) + ((w4[j] >> 16) >= thr);
+// Waits for the table copies (thread 0, bounded) and moves the barrier to its next phase;
+// returns false in every thread if they never landed.  Every thread calls it.
+__device__ bool tables_wait() {
+  if (threadIdx.x == 0 && !mbar_wait_sleep(&sh.tbar, sh.tpar)) sh.tfail = 1;
+  __syncthreads();
+  (void)mbar_try_wait(&sh.tbar, sh.tpar);
+  const bool ok = !sh.tfail;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    sh.tpar ^= 1u;
+    sh.tissued = 0;
+    sh.tfail = 0;
   }
-  return c;
+  return ok;
+}
+
+// Whether a row's first-phase end is certain to gather candidates from the tables: top-k
+// rows whose parameters are valid (their data can still end them early).
+__device__ __forceinline__ bool tables_likely(const RowParams& q) {
+  return !q.invalid && !params_greedy(q) && q.k >= 2;
 }
 
 // Candidates of a fast row (every token with z >= zth, the exact z image of theta, that
@@ -2315,7 +2206,10 @@ __device__ __noinline__ bool fast_serial(const LaunchParams& P, int row) {
   const int tabstride = nst_max * kThreads * (int)sizeof(uint16_t);  // bytes per slice
   const int tabbytes = C * tabstride;
   const int hitcap = ((int)Lo.r2 - tabbytes) / 4;
-  if (!P.vec_ok || hitcap < 256) return fast_serial_global<kBF16>(P, row);
+  if (!P.vec_ok || hitcap < kWarps * 128) {
+    if (sh.tissued) (void)tables_wait();
+    return fast_serial_global<kBF16>(P, row);
+  }
   const RowParams q = sh.rp;
   const bool kfin = q.k >= 2;
   const float m = sh.rs.m, invT = sh.rs.invT, theta = sh.rs.theta;
@@ -2330,23 +2224,7 @@ __device__ __noinline__ bool fast_serial(const LaunchParams& P, int row) {
   const unsigned char* lrow =
       reinterpret_cast<const unsigned char*>(a.logits) + (long long)row * a.logits_row_stride * kEsize;
   if (tid == 0) {
-    // every slice's table, one bulk copy each, on the row end's barrier; the tables are
-    // other CTAs' ordinary stores (acquired through the ticket), read here by the async
-    // proxy: the proxy fence orders them (global and shared state spaces)
-    asm volatile("fence.proxy.async;" ::: "memory");
-    uint32_t bytes = 0;
-    for (int s = 0; s < C; ++s) {
-      int len;
-      const int bulk = bulk_of<kBF16>(P, s, &len);
-      bytes += (uint32_t)((bulk * kEsize + kStageBytes - 1) / kStageBytes * kThreads * 2);
-    }
-    mbar_arrive_expect_tx(&sh.tbar, bytes);
-    for (int s = 0; s < C; ++s) {
-      int len;
-      const int bulk = bulk_of<kBF16>(P, s, &len);
-      const uint32_t b = (uint32_t)((bulk * kEsize + kStageBytes - 1) / kStageBytes * kThreads * 2);
-      if (b) bulk_copy_g2s(tabs + (size_t)s * tabstride, P.tab + ((size_t)row * C + s) * kTabMax, b, &sh.tbar);
-    }
+    if (!sh.tissued) tables_issue<kBF16>(P, row);
     sh.count = 0;
     int o = 0;
     for (int s = 0; s < C; ++s) {
@@ -2402,23 +2280,45 @@ __device__ __noinline__ bool fast_serial(const LaunchParams& P, int row) {
     __threadfence();  // read back below by other threads of the CTA
   }
   // the tables
-  if (tid == 0 && !mbar_wait_sleep(&sh.tbar, sh.tpar)) atomicOr(&sh.flags, kFlagRing);
-  __syncthreads();
-  (void)mbar_try_wait(&sh.tbar, sh.tpar);
+  const bool tok = tables_wait();
   const int nch = tabbytes / 16;
   const uint4* t4 = reinterpret_cast<const uint4*>(tabs);
   float zcut = zth;  // candidates: z >= zcut (tightened for top-k rows below)
   uint32_t thr = tab_threshold(zth);
-  if (kfin && !(sh.flags & kFlagRing)) {
-    // largest E in [thr, top] with at least k entries >= E
-    uint32_t lo = thr, hi = (fkey(m) >> 16) + 1u;  // count(>= lo) >= k is checked first
-    if (block_sum_int(count_entries(t4, nch, lo)) >= q.k) {
-      while (hi - lo > 1u) {
-        const uint32_t mid = (lo + hi) >> 1;
-        if (block_sum_int(count_entries(t4, nch, mid)) >= q.k) lo = mid;
-        else hi = mid;
+  if (kfin && tok) {
+    // the k-th largest entry: per-warp histograms of the entries at or above thr (two
+    // 16-bit counters a word, in the free area after the tables), merged per bin
+    const uint32_t top = fkey(m) >> 16;
+    int shift = 0;
+    while (((top - min(top, thr)) >> shift) >= 256u) ++shift;
+    uint32_t* wh = hits;  // kWarps x 128 words
+    uint32_t* bins = reinterpret_cast<uint32_t*>(S.r2 + kPidsBytes);
+    for (int i = tid; i < kWarps * 128; i += kThreads) wh[i] = 0u;
+    __syncthreads();
+    uint32_t* mine = wh + warp * 128;
+    for (int i = tid; i < nch; i += kThreads) {
+      const uint4 e = t4[i];
+      const uint32_t w4[4] = {e.x, e.y, e.z, e.w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t ent = (w4[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
+        if (ent >= thr) {
+          const uint32_t bin = min((ent - thr) >> shift, 255u);
+          atomicAdd(&mine[bin >> 1], 1u << (16 * (bin & 1)));
+        }
       }
-      zcut = fmaxf(zth, entry_bound_z(lo, m, invT));
+    }
+    __syncthreads();
+    {
+      uint32_t t = 0;
+      for (int w = 0; w < kWarps; ++w) t += (wh[w * 128 + (tid >> 1)] >> (16 * (tid & 1))) & 0xFFFFu;
+      bins[tid] = t;
+    }
+    __syncthreads();
+    if (warp == 0) pick_digit(bins, (unsigned long long)q.k, &sh.digit, &sh.above, &sh.none);
+    __syncthreads();
+    if (!sh.none) {
+      zcut = fmaxf(zth, entry_bound_z(thr + ((uint32_t)sh.digit << shift), m, invT));
       thr = tab_threshold(zcut);
     }
   }
@@ -2461,9 +2361,7 @@ __device__ __noinline__ bool fast_serial(const LaunchParams& P, int row) {
     }
   }
   __syncthreads();  // the tables are done: the candidate area is free
-  const bool tfail = (sh.flags & kFlagRing) != 0;
-  if (tid == 0) sh.tpar ^= 1u;  // the barrier's next phase
-  if (nh > hitcap || tfail) return fast_serial_global<kBF16>(P, row);
+  if (nh > hitcap || !tok) return fast_serial_global<kBF16>(P, row);
   // the candidates found so far (listed penalised tokens) into the shared copy
   {
     const int n0 = sh.count;
@@ -2475,7 +2373,7 @@ __device__ __noinline__ bool fast_serial(const LaunchParams& P, int row) {
   if (tgi >= 0 && tz > -INFINITY && tz >= zth && !listed(pids, tgi / chunk, (uint32_t)(tgi % chunk)))
     append2_1(csm, csmcap, seg, cap, y_of(tz, m, invT), tgi);
   // the listed groups' vectors with their bitmask words
-  constexpr int kHitBatch = kBF16 ? 1 : 2;
+  constexpr int kHitBatch = 1;
 #pragma unroll 1
   for (int h0 = 0; h0 < nh; h0 += kHitBatch * kThreads) {
     float4 v[kHitBatch][kVPT];
@@ -2507,7 +2405,7 @@ __device__ __noinline__ bool fast_serial(const LaunchParams& P, int row) {
 #pragma unroll
       for (int u = 0; u < kVPT; ++u) {
         const int f = hf[b] + u * kThreads;
-#pragma unroll
+#pragma unroll 1
         for (int j = 0; j < 4; ++j) {
           bool keep = false;
           float z = -INFINITY;
@@ -2945,8 +2843,11 @@ __device__ __noinline__ void p1_item(const LaunchParams& P, int row, int slice, 
   setup_p1<kBF16>(P, row, slice, nph);
   pass_a<kBF16>(P, row, slice);
   if (!publish_p1<kBF16>(P, row, slice)) return;
+  // a top-k row's end reads every table: their copies start before anything else
+  if (threadIdx.x == 0 && tables_likely(sh.rp)) tables_issue<kBF16>(P, row);
   combine_row(P, row);
   if (finish_early(P, row)) {
+    if (sh.tissued) (void)tables_wait();
     row_advance(P, row, 1, nph, true);
     return;
   }
@@ -2957,6 +2858,7 @@ __device__ __noinline__ void p1_item(const LaunchParams& P, int row, int slice, 
     row_advance(P, row, 1, nph, true);
     return;
   }
+  if (sh.tissued) (void)tables_wait();
   const int need = plan == kPlanTopP ? 3 : 2;  // phases the plan takes
   if (plan == kPlanSlow || nph < need) {
     slow_serial<kBF16>(P, row);
@@ -3127,10 +3029,15 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) sampler_kernel(const __g
     fence_mbar_init();
     sh.seq = 0u;
     sh.tpar = 0u;
+    sh.tissued = 0;
+    sh.tfail = 0;
   }
+  // the ordering launch ahead of this one (programmatic dependent launch) has finished and
+  // its results are visible after this
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   __syncthreads();
   const unsigned C = (unsigned)P.C;
-  const unsigned nitems = P.ctl[2] * C;  // work-list segments (the order kernel wrote them)
+  const unsigned nitems = P.ctl[2] * C;  // work-list segments (the ordering launch wrote them)
   for (;;) {
     if (tid == 0) sh.item = atomicAdd(P.ctl, 1u);
     __syncthreads();
@@ -3188,7 +3095,7 @@ Geometry geometry_for(int vocab) {
 
 // Byte offsets of the scratch arrays for B rows of C slices (one allocation).
 struct ScratchLayout {
-  size_t ctl, ticket, phase_done, bad, seg, order, rows, x1, x2, pen, tab, phist, cand, total;
+  size_t ctl, ticket, phase_done, bad, seg, order, rows, x1, x2, plist, plist_n, pen, tab, phist, cand, total;
 };
 
 constexpr size_t take(size_t& off, size_t bytes) {
@@ -3209,6 +3116,8 @@ constexpr ScratchLayout scratch_layout(size_t B, size_t C) {
   L.rows = take(off, B * sizeof(RowState));
   L.x1 = take(off, B * C * sizeof(X1));
   L.x2 = take(off, B * C * sizeof(X2));
+  L.plist = take(off, B * C * kPenCap * sizeof(PenEntry));
+  L.plist_n = take(off, B * C * sizeof(int2));
   L.pen = take(off, B * C * kPenCap * sizeof(uint2));
   L.tab = take(off, B * C * kTabMax * sizeof(uint16_t));
   L.phist = take(off, B * C * kPBins * sizeof(unsigned long long));
@@ -3238,6 +3147,9 @@ int setup_device(int dev) {
   const void* k32 = reinterpret_cast<const void*>(&sampler_kernel<false>);
   const void* k16 = reinterpret_cast<const void*>(&sampler_kernel<true>);
   const void* ko = reinterpret_cast<const void*>(&order_kernel);
+  if (cudaFuncSetAttribute(ko, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)prep_smem_bytes(kMaxSlices * kMaxChunk)) !=
+      cudaSuccess)
+    return CLSAMPLE_ERR_CUDA;
   // every kernel asks for the largest shared-memory carveout, so that the SMs need not
   // change their L1 / shared split between the ordering kernel and the sampler
   if (cudaFuncSetAttribute(k32, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
@@ -3418,6 +3330,8 @@ int make_params(const Geometry& g, int vocab, int dev, const Scratch& sc, int gr
   P->rows = reinterpret_cast<RowState*>(b + L.rows);
   P->x1 = reinterpret_cast<X1*>(b + L.x1);
   P->x2 = reinterpret_cast<X2*>(b + L.x2);
+  P->plist = reinterpret_cast<PenEntry*>(b + L.plist);
+  P->plist_n = reinterpret_cast<int2*>(b + L.plist_n);
   P->pen = reinterpret_cast<uint2*>(b + L.pen);
   P->tab = reinterpret_cast<uint16_t*>(b + L.tab);
   P->phist = reinterpret_cast<unsigned long long*>(b + L.phist);
@@ -3433,16 +3347,30 @@ int make_params(const clsample_t* h, const clsample_args_t* a, LaunchParams* P, 
 }
 
 int launch_order(const LaunchParams& P, cudaStream_t st) {
-  order_kernel<<<1, kOrderThreads, 0, st>>>(P);
+  const bool has_mod = P.a.hist_offs != nullptr || P.a.bias_offs != nullptr;
+  const unsigned grid = has_mod ? 1u + (unsigned)P.a.B : 1u;
+  order_kernel<<<grid, kOrderThreads, has_mod ? prep_smem_bytes(P.a.V) : 0, st>>>(P);
   return cudaGetLastError() == cudaSuccess ? CLSAMPLE_SUCCESS : CLSAMPLE_ERR_CUDA;
 }
 
+// The sampler kernel, launched with programmatic stream serialisation: its CTAs may start
+// while the ordering launch ahead of it finishes, and wait for it (griddepcontrol.wait)
+// before they read the work list.
 int launch_sampler(const Geometry& g, int grid, const LaunchParams& P, cudaStream_t st) {
-  if (P.a.logits_dtype == CLSAMPLE_LOGITS_BF16)
-    sampler_kernel<true><<<(unsigned)grid, kThreads, (size_t)g.smem, st>>>(P);
-  else
-    sampler_kernel<false><<<(unsigned)grid, kThreads, (size_t)g.smem, st>>>(P);
-  return cudaGetLastError() == cudaSuccess ? CLSAMPLE_SUCCESS : CLSAMPLE_ERR_CUDA;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof cfg);
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)g.smem;
+  cfg.stream = st;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t err = P.a.logits_dtype == CLSAMPLE_LOGITS_BF16 ? cudaLaunchKernelEx(&cfg, sampler_kernel<true>, P)
+                                                                    : cudaLaunchKernelEx(&cfg, sampler_kernel<false>, P);
+  return err == cudaSuccess ? CLSAMPLE_SUCCESS : CLSAMPLE_ERR_CUDA;
 }
 
 }  // namespace

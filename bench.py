@@ -355,7 +355,7 @@ def main():
             "traffic": traffic_from_profile(b.name),
             "algorithmic_bytes_per_launch": alg_sampler,
             "mean_launch_us": mean_launch_ms * 1e3,
-            "kernel": "sampler_kernel (persistent, one launch per step, after order_kernel)",
+            "kernel": "sampler_kernel (persistent, one launch per step, after the ordering launch: order_kernel with the row preparation blocks)",
             "order_kernel_us": order_ms * 1e3,
         },
         "gpu_launches": 2 * args.steps,

@@ -28,7 +28,7 @@
  * Threading and ownership.  A handle is bound to the CUDA device that was current at
  * clsample_create and owns device scratch sized for max_batch rows (the rows' order and
  * work list, per-slice records, penalised-token lists, tables of vector maxima and
- * compacted candidates; about 370 KB per row for V = 151936).  Every array in
+ * compacted candidates; about 430 KB per row for V = 151936).  Every array in
  * clsample_args_t is a DEVICE pointer owned by the caller; it must stay valid until the
  * work enqueued on the stream has finished.  The logits are read-only (never written in
  * place).  Calls on one handle must be ordered (one stream, or streams joined by
@@ -152,14 +152,16 @@ int clsample_create(int32_t max_batch, int32_t vocab, clsample_t** out);
  * device, so no call on the handle may still be running. */
 void clsample_destroy(clsample_t* handle);
 
-/* Enqueues one sampler call on `stream`: a one-CTA kernel that orders the rows (heaviest
- * first) and writes the work list, then the persistent sampler kernel (one CTA per
- * resident slot; every CTA takes (row, slice) items from the list); nothing when B == 0.
- * Returns after enqueueing; results are valid once the stream reaches this point. */
+/* Enqueues one sampler call on `stream`: the ordering launch (one CTA orders the rows,
+ * heaviest first, and writes the work list; when the call has penalties or logit_bias,
+ * one more CTA per row prepares the row's per-slice lists of penalised ids), then the
+ * persistent sampler kernel (one CTA per resident slot; every CTA takes (row, slice)
+ * items from the list); nothing when B == 0.  Returns after enqueueing; results are
+ * valid once the stream reaches this point. */
 int clsample_apply(clsample_t* handle, const clsample_args_t* args, clsample_stream_t stream);
 
 /* The two halves of clsample_apply, for callers that schedule or time them apart:
- * clsample_prepare enqueues the ordering kernel, clsample_sample the sampler kernel,
+ * clsample_prepare enqueues the ordering launch, clsample_sample the sampler kernel,
  * which reads the work list the last clsample_prepare on this handle wrote (the list
  * may be sampled again with the same arguments).  The pair, with the same arguments on
  * one stream, equals clsample_apply.  Same validation and return codes. */
@@ -169,7 +171,7 @@ int clsample_sample(clsample_t* handle, const clsample_args_t* args, clsample_st
 /* One sampler call without a handle that allocates nothing.  The pages have no
  * counterpart: this is a deployment convenience of this library, and it samples
  * exactly like clsample_apply.  Its scratch is one fixed device array compiled into
- * the library (about 23 MB, zero when the library loads); no cudaMalloc or cudaFree
+ * the library (about 28 MB, zero when the library loads); no cudaMalloc or cudaFree
  * ever happens.  The first call on a device looks up the array's address on that
  * device (cudaGetSymbolAddress) and sets the kernels' shared-memory limit, once per
  * device, under a host lock.  Limits: B <= 64 (else CLSAMPLE_ERR_BATCH) and

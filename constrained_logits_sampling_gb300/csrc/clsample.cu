@@ -305,6 +305,7 @@ struct Shared {
   unsigned long long tbar;  // the row end's table copies
   uint32_t tpar;     // its phase parity
   int tissued, tfail;  // copies issued and not yet waited for; a wait gave up
+  uint32_t lean;       // pass A: stages whose tokens are all live or penalised
   unsigned long long above;
 };
 __shared__ Shared sh;
@@ -696,7 +697,7 @@ __device__ __forceinline__ int pbin(float y) {
 // order-preserving key of their largest z (so "entry >= top 16 bits of key(zth)" holds
 // for every group with a live token at or above zth).
 __device__ __forceinline__ uint16_t tab_entry(bool any, float vmax) {
-  return any ? (uint16_t)(fkey(vmax) >> 16) : (uint16_t)0;
+  return (any && vmax > -INFINITY) ? (uint16_t)(fkey(vmax) >> 16) : (uint16_t)0;
 }
 __device__ __forceinline__ uint32_t tab_threshold(float zth) { return fkey(zth) >> 16; }
 
@@ -733,11 +734,15 @@ __device__ __forceinline__ void ring_wait(uint32_t s) {
 // Pass A's walk over the slice: body(t, f, wd, v) for every 4-token vector f (slot t of
 // its stage), with its live bits wd and raw values v widened to f32, and stage_end(k)
 // after every stage of the ring part.  Lanes without a vector get f = nvec (past the
-// row) and wd = 0; every lane of a warp makes the same number of body calls.  The ring
-// part streams through the TMA ring (thread 0 started its first stages); the ragged
-// tail and unaligned rows come in by plain loads (slot 0, no stage_end).
-template <bool kBF16, class Body, class StageEnd>
-__device__ __forceinline__ void stream_ring(const Geo& g, const Smem& S, Body&& body, StageEnd&& stage_end) {
+// row) and wd = 0; every lane of a warp makes the same number of body calls.  A stage
+// whose bit is set in `lean` (every token live or penalised) first gets patch(k, buf)
+// (the penalised tokens leave the buffer), then lean(t, f, v) for every vector, with no
+// per-token checks.  The ring part streams through the TMA ring (thread 0 started its
+// first stages); the ragged tail and unaligned rows come in by plain loads (slot 0, no
+// stage_end).
+template <bool kBF16, class Body, class Lean, class Patch, class StageEnd>
+__device__ __forceinline__ void stream_ring(const Geo& g, const Smem& S, uint32_t lean, Body&& body, Lean&& lean_body,
+                                            Patch&& patch, StageEnd&& stage_end) {
   constexpr int kEsize = kBF16 ? 2 : 4;
   constexpr int kVecPerStage = kStageBytes / (4 * kEsize);
   constexpr int kVPT = kVecPerStage / kThreads;
@@ -752,15 +757,24 @@ __device__ __forceinline__ void stream_ring(const Geo& g, const Smem& S, Body&& 
     __syncthreads();
     if (tid == 0 && k >= 1 && k - 1 + kStages < g.nst) ring_issue<kBF16>(g, S, k - 1 + kStages, s - 1 + kStages);
     (void)mbar_try_wait(&sh.full[s % kStages], (s / kStages) & 1u);  // this thread's acquire
-    const unsigned char* buf = S.ring + (s % kStages) * kStageBytes;
+    unsigned char* buf = S.ring + (s % kStages) * kStageBytes;
+    if ((lean >> k) & 1u) {
+      patch(k, buf);
 #pragma unroll
-    for (int t = 0; t < kVPT; ++t) {
-      const int fl = t * kThreads + tid;
-      const int f = k * kVecPerStage + fl;
-      const bool in = 4 * f < g.bulk_tokens;
-      const uint32_t wd = in ? live4(S.live, f) : 0u;
-      const float4 v = in ? sload4<kBF16>(buf, fl) : make_float4(0.f, 0.f, 0.f, 0.f);
-      body(t, in ? f : g.nvec, wd, v);
+      for (int t = 0; t < kVPT; ++t) {
+        const int fl = t * kThreads + tid;
+        lean_body(t, k * kVecPerStage + fl, sload4<kBF16>(buf, fl));
+      }
+    } else {
+#pragma unroll
+      for (int t = 0; t < kVPT; ++t) {
+        const int fl = t * kThreads + tid;
+        const int f = k * kVecPerStage + fl;
+        const bool in = 4 * f < g.bulk_tokens;
+        const uint32_t wd = in ? live4(S.live, f) : 0u;
+        const float4 v = in ? sload4<kBF16>(buf, fl) : make_float4(0.f, 0.f, 0.f, 0.f);
+        body(t, in ? f : g.nvec, wd, v);
+      }
     }
     stage_end(k);
   }
@@ -813,6 +827,16 @@ __device__ __forceinline__ void stream_ldg(const Geo& g, const Smem& S, Body&& b
     body(in ? f : g.nvec, wd, v);
   }
   __syncthreads();
+}
+
+// A later-phase pass over the slice through the TMA ring: body(f, wd, v) for every
+// vector, as stream_ldg gives them, but 32 KB in flight per CTA instead of kReload loads
+// per thread.  Thread 0 started the ring (ring_start) before the pass.
+template <bool kBF16, class Body>
+__device__ __forceinline__ void stream_phase(const Geo& g, const Smem& S, Body&& body) {
+  stream_ring<kBF16>(
+      g, S, 0u, [&](int, int f, uint32_t wd, const float4& v) { body(f, wd, v); }, [](int, int, const float4&) {},
+      [](int, unsigned char*) {}, [](int) {});
 }
 
 // ---------------------------------------------------------------- the work list
@@ -1223,10 +1247,9 @@ __device__ __noinline__ void setup_p1(const LaunchParams& P, int row, int slice,
   (void)nph;
   if (tid == 0) {
     sh.flags = 0;
+    sh.lean = 0u;
     sh.count = 0;
     sh.nallowed = 0;  // (sh.npen is thread 64's)
-    // the row end (or a later phase) reads parts of the slice again soon: normal lines
-    sh.policy = make_policy_evict_normal();
     ring_start<kBF16>(g, S, sh.seq);
   } else if (tid == 32) {
     sh.rp = load_params(a, row);
@@ -1304,59 +1327,130 @@ __device__ __noinline__ void pass_a(const LaunchParams& P, int row, int slice) {
   static_assert(kGroups <= 4, "four group sets per warp at most");
   uint16_t* tab = reinterpret_cast<uint16_t*>(S.r2);
 
+  constexpr int kTokPerStage = kStageBytes / (kBF16 ? 2 : 4);
+  constexpr int kWordsPerStage = kTokPerStage / 32;
+  const int nw = g.chunk / 32;
+
+  // lean stages: every token live (allowed, inside the row) or penalised / biased, and
+  // the whole stage inside the ring part (one warp per stage)
+  for (int k = warp; k < g.nst; k += kWarps) {
+    const int w0 = k * kWordsPerStage;
+    bool all = (k + 1) * kTokPerStage <= g.bulk_tokens;
+    for (int w = w0 + lane; w < w0 + kWordsPerStage; w += 32) all = all && (S.live[w] | S.mod[w]) == 0xFFFFFFFFu;
+    if (__all_sync(0xffffffffu, all) && lane == 0) atomicOr(&sh.lean, 1u << k);
+  }
+  __syncthreads();
+  uint32_t lean = sh.lean;
+
   // the thread's online state; a thread visits its tokens in increasing order, so the
   // first token reaching the running max is the lowest
-  float sm = -INFINITY, ss = 0.0f;
-  int targ = INT_MAX;
+  float sm, ss;
+  int targ;
   // the maxima of the thread's vectors in each stage slot: kGroups disjoint token groups
   // per thread for the top-k bounds
   float gm[kGroups];
+  float tmax;  // this stage's maximum (table)
+  bool tany;
+  float gmin;  // lean stages: the smallest vector maximum (-inf: a vector of -inf logits)
+  for (;;) {
+    sm = -INFINITY;
+    ss = 0.0f;
+    targ = INT_MAX;
 #pragma unroll
-  for (int t = 0; t < kGroups; ++t) gm[t] = -INFINITY;
-  float tmax = -INFINITY;  // this stage's maximum (table)
-  bool tany = false;
-  stream_ring<kBF16>(
-      g, S,
-      [&](int t, int f, uint32_t wd, const float4& v) {
-        if (has_mod && 4 * f < g.len) {
-          // penalised / biased tokens: keep the raw logit (rank order) for the fold below
-          const uint32_t mw = S.mod[f >> 3];
-          const int sh4 = (f & 7) * 4;
-          const uint32_t md = (mw >> sh4) & 0xFu;
-          if (md) {
-            int r = S.prank[f >> 3] + __popc(mw & ((1u << sh4) - 1u));
+    for (int t = 0; t < kGroups; ++t) gm[t] = -INFINITY;
+    tmax = -INFINITY;
+    tany = false;
+    gmin = INFINITY;
+    stream_ring<kBF16>(
+        g, S, lean,
+        [&](int t, int f, uint32_t wd, const float4& v) {
+          if (has_mod && 4 * f < g.len) {
+            // penalised / biased tokens: keep the raw logit (rank order) for the fold below
+            const uint32_t mw = S.mod[f >> 3];
+            const int sh4 = (f & 7) * 4;
+            const uint32_t md = (mw >> sh4) & 0xFu;
+            if (md) {
+              int r = S.prank[f >> 3] + __popc(mw & ((1u << sh4) - 1u));
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if ((md >> j) & 1u) {
-                if (r < kPenCap) S.pz[r] = comp(v, j);
-                ++r;
-              }
+              for (int j = 0; j < 4; ++j)
+                if ((md >> j) & 1u) {
+                  if (r < kPenCap) S.pz[r] = comp(v, j);
+                  ++r;
+                }
+            }
           }
-        }
-        if (!wd) return;
-        float4 z = v;
-        if (!(wd == 0xFu && finite4(v)))
-          z = make_float4((wd & 1u) ? sanitize(v.x) : -INFINITY, (wd & 2u) ? sanitize(v.y) : -INFINITY,
-                          (wd & 4u) ? sanitize(v.z) : -INFINITY, (wd & 8u) ? sanitize(v.w) : -INFINITY);
-        const float fm = fmaxf(fmaxf(z.x, z.y), fmaxf(z.z, z.w));
-        tany = true;
-        tmax = fmaxf(tmax, fm);
-        if (!(fm > -INFINITY)) return;
-        gm[t] = fmaxf(gm[t], fm);
-        if (fm > sm) {
-          ss *= ex2_approx((sm - fm) * cS);
-          sm = fm;
-          targ = c0 + 4 * f + (z.x == fm ? 0 : z.y == fm ? 1 : z.z == fm ? 2 : 3);
-        }
-        const float e0 = ex2_approx((z.x - sm) * cS), e1 = ex2_approx((z.y - sm) * cS);
-        const float e2 = ex2_approx((z.z - sm) * cS), e3 = ex2_approx((z.w - sm) * cS);
-        ss += (e0 + e1) + (e2 + e3);
-      },
-      [&](int k) {
-        tab[k * kThreads + tid] = tab_entry(tany, tmax);
-        tany = false;
-        tmax = -INFINITY;
-      });
+          if (!wd) return;
+          float4 z = v;
+          if (!(wd == 0xFu && finite4(v)))
+            z = make_float4((wd & 1u) ? sanitize(v.x) : -INFINITY, (wd & 2u) ? sanitize(v.y) : -INFINITY,
+                            (wd & 4u) ? sanitize(v.z) : -INFINITY, (wd & 8u) ? sanitize(v.w) : -INFINITY);
+          const float fm = fmaxf(fmaxf(z.x, z.y), fmaxf(z.z, z.w));
+          tany = true;
+          tmax = fmaxf(tmax, fm);
+          if (!(fm > -INFINITY)) return;
+          gm[t] = fmaxf(gm[t], fm);
+          if (fm > sm) {
+            ss *= ex2_approx((sm - fm) * cS);
+            sm = fm;
+            targ = c0 + 4 * f + (z.x == fm ? 0 : z.y == fm ? 1 : z.z == fm ? 2 : 3);
+          }
+          const float e0 = ex2_approx((z.x - sm) * cS), e1 = ex2_approx((z.y - sm) * cS);
+          const float e2 = ex2_approx((z.z - sm) * cS), e3 = ex2_approx((z.w - sm) * cS);
+          ss += (e0 + e1) + (e2 + e3);
+        },
+        // lean vector: no mask, penalty or finiteness checks (a non-finite logit shows in
+        // ss or gmin, and the slice is then walked again with the checks)
+        [&](int t, int f, const float4& v) {
+          const float fm = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+          gmin = fminf(gmin, fm);
+          tany = true;
+          tmax = fmaxf(tmax, fm);
+          gm[t] = fmaxf(gm[t], fm);
+          if (fm > sm) {
+            ss *= ex2_approx((sm - fm) * cS);
+            sm = fm;
+            targ = c0 + 4 * f + (v.x == fm ? 0 : v.y == fm ? 1 : v.z == fm ? 2 : 3);
+          }
+          const float e0 = ex2_approx((v.x - sm) * cS), e1 = ex2_approx((v.y - sm) * cS);
+          const float e2 = ex2_approx((v.z - sm) * cS), e3 = ex2_approx((v.w - sm) * cS);
+          ss += (e0 + e1) + (e2 + e3);
+        },
+        // a lean stage's penalised / biased tokens: raw logit to the fold below, -inf in
+        // the buffer (a -inf lean token counts for nothing)
+        [&](int k, unsigned char* buf) {
+          if (!has_mod) return;
+          const int w0 = k * kWordsPerStage, w1 = w0 + kWordsPerStage;
+          const int r0 = S.prank[w0];
+          const int r1 = w1 < nw ? (int)S.prank[w1] : (int)S.prank[nw - 1] + __popc(S.mod[nw - 1]);
+          if (r1 <= r0) return;  // the same in every thread
+          for (int r = r0 + tid; r < min(r1, kPenCap); r += kThreads) {
+            const int i = (int)S.pid[r] - k * kTokPerStage;
+            if (kBF16) {
+              uint16_t* b16 = reinterpret_cast<uint16_t*>(buf);
+              S.pz[r] = __uint_as_float((uint32_t)b16[i] << 16);
+              b16[i] = (uint16_t)0xFF80u;
+            } else {
+              float* b32 = reinterpret_cast<float*>(buf);
+              S.pz[r] = b32[i];
+              b32[i] = -INFINITY;
+            }
+          }
+          // the buffer is refilled by the async proxy later
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncthreads();
+        },
+        [&](int k) {
+          tab[k * kThreads + tid] = tab_entry(tany, tmax);
+          tany = false;
+          tmax = -INFINITY;
+        });
+    // a lean stage saw NaN / +inf (ss is NaN) or a vector of -inf logits: walk the slice
+    // again with every check (thread 0 restarts the ring)
+    const bool bad = lean != 0u && (!(ss <= FLT_MAX) || gmin == -INFINITY);
+    if (!__syncthreads_or(bad)) break;
+    lean = 0u;
+    if (tid == 0) ring_start<kBF16>(g, S, sh.seq);
+  }
   // the penalised / biased tokens in token order: penalties, then bias, on the sanitised
   // raw logit (the mask applies to them too); the final z' replaces the raw one and joins
   // the thread's online state
@@ -2445,7 +2539,7 @@ __device__ __noinline__ void topp_hist(const LaunchParams& P, int row, int slice
   __syncthreads();
   unsigned long long w = 0, wlast = 0;
   uint32_t* mine = whist + 2 * warp * kPBins;
-  stream_ldg<kBF16>(g, S, [&](int f, uint32_t wd, const float4& v) {
+  stream_phase<kBF16>(g, S, [&](int f, uint32_t wd, const float4& v) {
     if (!wd) return;
     const bool fastv = wd == 0xFu && finite4(v);
 #pragma unroll 1
@@ -2508,7 +2602,7 @@ __device__ __noinline__ void topp_race(const LaunchParams& P, int row, int slice
   __syncthreads();
   Race race;
   race.init(sh.rs.s0);
-  stream_ldg<kBF16>(g, S, [&](int f, uint32_t wd, const float4& v) {
+  stream_phase<kBF16>(g, S, [&](int f, uint32_t wd, const float4& v) {
     float y[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
     if (wd) {
       const bool fastv = wd == 0xFu && finite4(v);
@@ -2588,7 +2682,7 @@ __device__ __noinline__ void minp_pass(const LaunchParams& P, int row, int slice
   __syncthreads();
   const float zth = sh.zth;
   unsigned long long w = 0;
-  stream_ldg<kBF16>(g, S, [&](int f, uint32_t wd, const float4& v) {
+  stream_phase<kBF16>(g, S, [&](int f, uint32_t wd, const float4& v) {
     float z[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
     if (wd) {
       if (wd == 0xFu && finite4(v)) {
@@ -2648,7 +2742,7 @@ __device__ __noinline__ void untrunc_pass(const LaunchParams& P, int row, int sl
   const int c0 = g.c0;
   Race race;
   race.init(sh.rs.s0);
-  stream_ldg<kBF16>(g, S, [&](int f, uint32_t wd, const float4& v) {
+  stream_phase<kBF16>(g, S, [&](int f, uint32_t wd, const float4& v) {
     if (!wd) return;
     float y[4];
     bool live_any = false, worth = false;
@@ -2995,6 +3089,7 @@ __device__ __noinline__ void phase_item(const LaunchParams& P, int row, int slic
   else if (plan == kPlanFast && sh.rs.needW && ph == 2) what = 3;
   else if (plan == kPlanUntrunc && ph == 2) what = 4;
   if (what) {
+    if (tid == 0) ring_start<kBF16>(geo<kBF16>(P, row, slice), carve(P.chunk), sh.seq);
     setup_re<kBF16>(P, row, slice);
     if (what == 1) topp_hist<kBF16>(P, row, slice);
     else if (what == 2) topp_race<kBF16>(P, row, slice);
@@ -3028,6 +3123,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) sampler_kernel(const __g
     mbar_init(&sh.tbar, 1);
     fence_mbar_init();
     sh.seq = 0u;
+    // every ring copy's L2 policy (set before any item, first phase or later): the row
+    // end or a later phase reads parts of the slice again soon, so normal lines
+    sh.policy = make_policy_evict_normal();
     sh.tpar = 0u;
     sh.tissued = 0;
     sh.tfail = 0;

@@ -49,9 +49,11 @@ def test_strerror_and_geometry(lib):
     for code in range(-7, 0):
         assert lib.clsample_strerror(code) != b"unknown error"
     g = sampler.geometry(151936)
-    assert g == {"slices": 8, "chunk": 19008, "smem_bytes": g["smem_bytes"]}
-    assert g["smem_bytes"] <= 54 * 1024  # four CTAs per SM
-    assert sampler.geometry(262144)["slices"] == 8
+    assert g == {"slices": 10, "chunk": 15232, "smem_bytes": g["smem_bytes"]}
+    assert g["smem_bytes"] <= 72 * 1024  # three CTAs per SM
+    g = sampler.geometry(262144)
+    assert g["slices"] == 18 and g["chunk"] % 128 == 0
+    assert (g["slices"] - 1) * g["chunk"] < 262144 <= g["slices"] * g["chunk"]
     with pytest.raises(sampler.ClsampleError):
         sampler.geometry(262145)
     assert sampler.geometry(8)["slices"] == 1

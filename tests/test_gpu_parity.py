@@ -163,18 +163,22 @@ def test_padded_row_stride_and_unaligned_rows():
         compare(b, g, o, name=f"pad {pad}")
 
 
-def test_history_overflow_is_reported():
-    """More distinct penalised ids in one slice than the per-slice table holds: the row
-    reports OVERFLOW instead of sampling from a wrong distribution."""
+def test_many_penalised_ids_in_one_slice():
+    """More distinct penalised and biased ids in one vocabulary slice than one table round
+    holds (512): the transforms run in several rounds and stay bit-exact."""
     V = 151936
-    z = np.zeros((2, V), F32)
-    hist = np.arange(0, 4000, dtype=np.int32)  # 4000 distinct ids in the first slice
-    b = small(z, hist_offs=np.array([0, 4000, 4001], np.int32),
-              hist_ids=np.concatenate([hist, np.array([5], np.int32)]),
-              freq=np.full(2, 0.1, F32), temperatures=np.zeros(2, F32))
-    g = run_gpu(b, debug=False)
-    assert g["status"][0] == 1 and g["tokens"][0] == -1
-    assert g["status"][1] == 0
+    rng = np.random.default_rng(5)
+    z = (rng.standard_normal((3, V)) * 3).astype(F32)
+    hist = np.concatenate([np.arange(0, 4000), np.arange(0, 4000, 7), rng.integers(0, V, 300)]).astype(np.int32)
+    offs = np.array([0, len(hist), len(hist) + 1, len(hist) + 1], np.int32)
+    bias_ids = np.arange(100, 1400, 3).astype(np.int32)
+    b = small(z, hist_offs=offs, hist_ids=np.concatenate([hist, np.array([5], np.int32)]),
+              freq=np.full(3, 0.1, F32), pres=np.full(3, 0.2, F32), rep=np.full(3, 1.2, F32),
+              bias_offs=np.array([0, len(bias_ids), len(bias_ids), len(bias_ids)], np.int32),
+              bias_ids=bias_ids, bias_vals=rng.uniform(-3, 3, len(bias_ids)).astype(F32),
+              temperatures=np.array([0.0, 0.8, 1.0], F32), top_ks=np.array([-1, 40, -1], np.int32),
+              top_ps=np.array([1.0, 0.9, 0.95], F32), positions=np.arange(3, dtype=np.int64))
+    compare(b, run_gpu(b), run_oracle(b), name="many penalised")
 
 
 # ----------------------------------------------------------------------------- laws and invariants

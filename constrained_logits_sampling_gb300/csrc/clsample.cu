@@ -56,8 +56,7 @@ constexpr int kMaxSlices = (kMaxVocab + kSliceMax - 1) / kSliceMax;
 constexpr int kKMax = 1024;        // top-k rows with k <= kKMax finish from candidates
 constexpr int kCandCap = 2048;     // compacted candidates per slice (global scratch)
 constexpr int kPen = 512;          // penalised / biased tokens applied per round
-constexpr int kHBins = 1024;       // aux words for the local top-k sample
-constexpr int kSample = 512;       // sampled tokens per slice for the local top-k bound
+constexpr int kHList = 1024;       // the slice's history ids cached in shared memory
 constexpr int kYBins = 64;         // heavy rows: quarter-unit y bins, the last one open-ended
 constexpr int kDigitBins = 2048;   // radix selects: 11-bit digits
 constexpr uint32_t kWaitPolls = 1u << 22;  // row-barrier polls (about 1 us apart at most)
@@ -152,7 +151,7 @@ constexpr int kBufMin = kFinHistBytes + 1024 * 8;    // room for them and 1024 i
 // Bytes of buf: the slice, and at least the finisher's area.
 __host__ __device__ constexpr int buf_bytes(int chunk) { return chunk * 4 > kBufMin ? chunk * 4 : kBufMin; }
 struct Layout {
-  uint32_t claim, prefix, aux, total;
+  uint32_t claim, prefix, hlist, mask, aux, total;
 };
 __host__ __device__ inline Layout layout_for(int chunk) {
   Layout L;
@@ -161,12 +160,16 @@ __host__ __device__ inline Layout layout_for(int chunk) {
   off = align_up(off + sizeof(uint32_t) * (size_t)(chunk / 32), 16);
   L.prefix = (uint32_t)off;
   off = align_up(off + sizeof(uint16_t) * (size_t)(chunk / 32), 16);
+  L.hlist = (uint32_t)off;
+  off = align_up(off + sizeof(uint16_t) * (size_t)kHList, 16);
+  L.mask = (uint32_t)off;
+  off = align_up(off + sizeof(uint32_t) * (size_t)(chunk / 32), 16);
   L.aux = (uint32_t)off;
   L.total = (uint32_t)(off + kAuxBytes);
   return L;
 }
 static_assert(kPen * (2 + 4 + 4) <= (int)kAuxBytes, "transform tables overflow aux");
-static_assert(kHBins * 4 <= (int)kAuxBytes, "top-k histogram overflows aux");
+static_assert(kThreads * 8 <= (int)kAuxBytes, "per-thread maxima overflow aux");
 static_assert(sizeof(SBins) <= kAuxBytes, "y bins overflow aux");
 static_assert(kSliceMax % 128 == 0 && kSliceMax <= 65535, "16-bit local ids and ranks");
 static_assert(kMaxSlices <= 31, "slice sets are 32-bit masks");
@@ -178,6 +181,8 @@ struct Smem {
   float* buf;
   uint32_t* claim;
   uint16_t* prefix;
+  uint16_t* hlist;      // the slice's history ids (local), in scan order
+  uint32_t* mask;       // the slice's bitmask words
   uint16_t* pid;        // aux: rank -> local id
   uint32_t* pcnt;       // aux: rank -> history count
   int* pbias;           // aux: rank -> last bias entry (-1: none)
@@ -192,6 +197,8 @@ __device__ __forceinline__ Smem carve(int chunk) {
   s.buf = reinterpret_cast<float*>(b);
   s.claim = reinterpret_cast<uint32_t*>(b + L.claim);
   s.prefix = reinterpret_cast<uint16_t*>(b + L.prefix);
+  s.hlist = reinterpret_cast<uint16_t*>(b + L.hlist);
+  s.mask = reinterpret_cast<uint32_t*>(b + L.mask);
   s.pid = reinterpret_cast<uint16_t*>(b + L.aux);
   s.pcnt = reinterpret_cast<uint32_t*>(b + L.aux + 2 * kPen);
   s.pbias = reinterpret_cast<int*>(b + L.aux + 6 * kPen);
@@ -212,6 +219,7 @@ struct Shared {
   unsigned long long red_u[kWarps];
   int row_id, slice, c0, n, nv;
   int ntouch, flag, cnt, last, spill;
+  int nhist;    // history ids of the slice (cached in hlist while at most kHList)
   int nal_row;  // light top-k rows with a mask: allowed tokens of the whole row (by the mask)
   // heavy rows: the bin plan
   int blo, bhi;
@@ -323,6 +331,17 @@ __device__ float block_min_f(float v) {
   return r;
 }
 
+__device__ uint32_t block_min_u32(uint32_t v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = min(v, __shfl_xor_sync(~0u, v, o));
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) sh.red_i[threadIdx.x >> 5] = (int)v;
+  __syncthreads();
+  uint32_t r = (uint32_t)sh.red_i[0];
+  for (int i = 1; i < kWarps; ++i) r = min(r, (uint32_t)sh.red_i[i]);
+  return r;
+}
+
 // Exclusive prefix sum over the block (thread order); *total gets the sum.
 __device__ int block_scan_i(int x, int* total) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -357,6 +376,74 @@ __device__ __forceinline__ void add_mass(uint32_t* lo, uint32_t* hi, unsigned lo
 }
 __device__ __forceinline__ unsigned long long get_mass(const uint32_t* lo, const uint32_t* hi) {
   return ((unsigned long long)*hi << 32) + *lo;
+}
+
+// ---------------------------------------------------------------- block sort
+
+// Compare-exchange of a bitonic stage: element i keeps max(a, partner) if it is the pair's
+// first element in a descending block (or the second in an ascending one), else the min.
+__device__ __forceinline__ unsigned long long bitonic_pick(unsigned long long a, unsigned long long o, int i, int size,
+                                                           int stride) {
+  const bool keep_max = ((i & stride) == 0) == ((i & size) == 0);
+  return keep_max ? (a > o ? a : o) : (a < o ? a : o);
+}
+
+// Sorts np = 256 * E 64-bit keys at k (shared memory) in descending order, bitonic:
+// thread t holds keys [t E, t E + E) in registers; strides below E swap inside a
+// thread, strides below 32 E between lanes by shuffles, wider ones through shared memory
+// (the only stages with a block barrier).  The stage loops stay rolled (small code); the
+// in-thread strides are dispatched to fixed register pairs.
+template <int E>
+__device__ void block_sort_desc(unsigned long long* k) {
+  constexpr int np = kThreads * E;
+  const int t = threadIdx.x;
+  unsigned long long v[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) v[e] = k[t * E + e];
+#pragma unroll 1
+  for (int size = 2; size <= np; size <<= 1) {
+#pragma unroll 1
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      if (stride >= 32 * E) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) k[t * E + e] = v[e];
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < E; ++e) v[e] = bitonic_pick(v[e], k[(t * E + e) ^ stride], t * E + e, size, stride);
+        __syncthreads();
+      } else if (stride >= E) {
+        const int lm = stride / E;
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+          v[e] = bitonic_pick(v[e], __shfl_xor_sync(~0u, v[e], lm), t * E + e, size, stride);
+      } else {
+        unsigned long long w[E];
+#pragma unroll
+        for (int st = 1; st < E; st <<= 1) {
+          if (st != stride) continue;
+#pragma unroll
+          for (int e = 0; e < E; ++e) w[e] = bitonic_pick(v[e], v[e ^ st], t * E + e, size, st);
+#pragma unroll
+          for (int e = 0; e < E; ++e) v[e] = w[e];
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e) k[t * E + e] = v[e];
+  __syncthreads();
+}
+
+// Sorts n <= 2048 keys (padded with zeros to 256 E) descending.
+__device__ void sort_desc(unsigned long long* k, int n) {
+  int np = kThreads;
+  while (np < n) np <<= 1;
+  for (int i = n + threadIdx.x; i < np; i += kThreads) k[i] = 0ull;
+  __syncthreads();
+  if (np <= kThreads) block_sort_desc<1>(k);
+  else if (np <= 2 * kThreads) block_sort_desc<2>(k);
+  else if (np <= 4 * kThreads) block_sort_desc<4>(k);
+  else block_sort_desc<8>(k);
 }
 
 // ---------------------------------------------------------------- row parameters
@@ -551,10 +638,33 @@ __device__ void claim_tokens(const LaunchParams& P, const Smem& S, const RowPara
   __syncthreads();
   int bad = 0;
   const int V = P.a.V;
-  for (int j = q.hlo + threadIdx.x; j < q.hhi; j += kThreads) {
-    const int id = __ldg(P.a.hist_ids + j);
-    if (id < 0 || id >= V) bad = 1;
-    else if ((unsigned)(id - c0) < (unsigned)n) atomicOr(&S.claim[(id - c0) >> 5], 1u << ((id - c0) & 31));
+  if (threadIdx.x == 0) sh.nhist = 0;
+  __syncthreads();
+  // history ids, eight loads in flight per thread; the slice's ids are also listed
+  for (int j0 = q.hlo; j0 < q.hhi; j0 += 8 * kThreads) {
+    int ids[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int j = j0 + u * kThreads + threadIdx.x;
+      ids[u] = j < q.hhi ? __ldg(P.a.hist_ids + j) : INT_MIN;
+    }
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int id = ids[u];
+      if (id != INT_MIN && (id < 0 || id >= V)) bad = 1;
+      const bool in = id != INT_MIN && (unsigned)(id - c0) < (unsigned)n;
+      const unsigned inb = __ballot_sync(~0u, in);
+      if (!inb) continue;
+      // repeated ids of one warp (frequent tokens) mark the bitmap once
+      const unsigned peers = __match_any_sync(~0u, in ? id : -1);
+      if (in && (__ffs(peers & inb) - 1) == lane) atomicOr(&S.claim[(id - c0) >> 5], 1u << ((id - c0) & 31));
+      int base = 0;
+      if (lane == 0) base = atomicAdd(&sh.nhist, __popc(inb));
+      base = __shfl_sync(~0u, base, 0);
+      const int pos = base + __popc(inb & ((1u << lane) - 1u));
+      if (in && pos < kHList) S.hlist[pos] = (uint16_t)(id - c0);
+    }
   }
   for (int j = q.blo + threadIdx.x; j < q.bhi; j += kThreads) {
     const int id = __ldg(P.a.bias_ids + j);
@@ -600,11 +710,36 @@ __device__ void transforms_prep(const LaunchParams& P, const Smem& S, const RowP
   }
   __syncthreads();
   const int V = P.a.V;
-  for (int j = q.hlo + threadIdx.x; j < q.hhi; j += kThreads) {
-    const int id = __ldg(P.a.hist_ids + j);
-    if (id < 0 || id >= V || (unsigned)(id - c0) >= (unsigned)n) continue;
-    const int r = claim_rank(S, id - c0) - r0;
-    if ((unsigned)r < (unsigned)kPen) atomicAdd(&S.pcnt[r], 1u);
+  const int nh = sh.nhist;
+  if (nh <= kHList) {
+    const int lane = threadIdx.x & 31;
+    for (int i0 = 0; i0 < nh; i0 += kThreads) {
+      const int i = i0 + threadIdx.x;
+      int r = -1;
+      if (i < nh) {
+        r = claim_rank(S, S.hlist[i]) - r0;
+        if ((unsigned)r >= (unsigned)kPen) r = -1;
+      }
+      // one atomic per distinct rank of the warp, adding its multiplicity
+      const unsigned peers = __match_any_sync(~0u, r);
+      if (r >= 0 && (__ffs(peers) - 1) == lane) atomicAdd(&S.pcnt[r], (unsigned)__popc(peers));
+    }
+  } else {
+    for (int j0 = q.hlo; j0 < q.hhi; j0 += 8 * kThreads) {
+      int ids[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = j0 + u * kThreads + threadIdx.x;
+        ids[u] = j < q.hhi ? __ldg(P.a.hist_ids + j) : -1;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int id = ids[u];
+        if (id < 0 || id >= V || (unsigned)(id - c0) >= (unsigned)n) continue;
+        const int r = claim_rank(S, id - c0) - r0;
+        if ((unsigned)r < (unsigned)kPen) atomicAdd(&S.pcnt[r], 1u);
+      }
+    }
   }
   for (int j = q.blo + threadIdx.x; j < q.bhi; j += kThreads) {
     const int id = __ldg(P.a.bias_ids + j);
@@ -636,8 +771,8 @@ __device__ void transforms_apply(const LaunchParams& P, const Smem& S, const Row
 
 __device__ __forceinline__ bool claimed(const Smem& S, int l) { return (S.claim[l >> 5] >> (l & 31)) & 1u; }
 
-__device__ __forceinline__ uint32_t mask_nibble(const int32_t* mrow, int c0, int f) {
-  return mrow ? ((uint32_t)__ldg(mrow + (c0 >> 5) + (f >> 3)) >> ((f & 7) * 4)) & 0xFu : 0xFu;
+__device__ __forceinline__ uint32_t mask_nibble(const uint32_t* mw, int f) {
+  return mw ? (mw[f >> 3] >> ((f & 7) * 4)) & 0xFu : 0xFu;
 }
 
 // The slice's max, lowest argmax, allowed count and sum of 2^((z' - max) c).  Writes the
@@ -646,19 +781,22 @@ __device__ __forceinline__ uint32_t mask_nibble(const int32_t* mrow, int c0, int
 // with per-token sanitising (claimed tokens already hold their final value).
 __device__ void pass_a(const LaunchParams& P, const Smem& S, const RowParams& q, int row, int c0, int n) {
   const int nv = (n + 3) >> 2;
-  const int32_t* mrow = P.a.bitmask ? P.a.bitmask + (long long)row * P.a.bitmask_row_stride : nullptr;
+  const uint32_t* mw = P.a.bitmask ? S.mask : nullptr;
   const uint32_t tail = (n & 3) ? ((1u << (n & 3)) - 1u) : 0xFu;
   float4* b4 = reinterpret_cast<float4*>(S.buf);
   if (threadIdx.x == 0 && (n & 3)) {
     for (int j = n; j < 4 * nv; ++j) S.buf[j] = 0.0f;  // pads: finite, masked below
   }
   __syncthreads();
-  float tmax = -INFINITY, chk = 0.0f;
+  // one walk: max, first vector reaching it, and the sum of 2^((z' - tmax) c) against a
+  // running per-thread max (rescaled when it grows)
+  const float c = __fmul_rn(1.4426950408889634f, q.invT);
+  float tmax = -INFINITY, tsum = 0.0f, chk = 0.0f;
   int tf = INT_MAX, nal = 0;
   for (int f = threadIdx.x; f < nv; f += kThreads) {
     float4 v = b4[f];
     chk += (v.x + v.y) + (v.z + v.w);
-    uint32_t bits = mask_nibble(mrow, c0, f);
+    uint32_t bits = mask_nibble(mw, f);
     if (f == nv - 1) bits &= tail;
     if (bits != 0xFu) {
       if (!(bits & 1u)) v.x = -INFINITY;
@@ -670,9 +808,13 @@ __device__ void pass_a(const LaunchParams& P, const Smem& S, const RowParams& q,
     nal += __popc(bits);
     const float a4 = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
     if (a4 > tmax) {
+      tsum *= ex2_approx((tmax - a4) * c);
       tmax = a4;
       tf = f;
     }
+    if (tmax > -INFINITY)
+      tsum += (ex2_approx((v.x - tmax) * c) + ex2_approx((v.y - tmax) * c)) +
+              (ex2_approx((v.z - tmax) * c) + ex2_approx((v.w - tmax) * c));
   }
   const int nonfinite = __syncthreads_or(!(fabsf(chk) < INFINITY));
   if (nonfinite) {
@@ -683,22 +825,28 @@ __device__ void pass_a(const LaunchParams& P, const Smem& S, const RowParams& q,
     for (int l = threadIdx.x; l < 4 * nv; l += kThreads) {
       float z = -INFINITY;
       if (l < n) {
-        const bool ok = mrow ? (((uint32_t)__ldg(mrow + ((c0 + l) >> 5)) >> ((c0 + l) & 31)) & 1u) : true;
+        const bool ok = mw ? ((mw[l >> 5] >> (l & 31)) & 1u) : true;
         if (ok) z = claimed(S, l) ? S.buf[l] : sanitize(S.buf[l]);
       }
       S.buf[l] = z;
     }
     __syncthreads();
+    tsum = 0.0f;
     for (int f = threadIdx.x; f < nv; f += kThreads) {
       const float4 v = b4[f];
       nal += (v.x > -INFINITY) + (v.y > -INFINITY) + (v.z > -INFINITY) + (v.w > -INFINITY);
       const float a4 = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
       if (a4 > tmax) {
+        tsum *= ex2_approx((tmax - a4) * c);
         tmax = a4;
         tf = f;
       }
+      if (tmax > -INFINITY)
+        tsum += (ex2_approx((v.x - tmax) * c) + ex2_approx((v.y - tmax) * c)) +
+                (ex2_approx((v.z - tmax) * c) + ex2_approx((v.w - tmax) * c));
     }
   }
+  S.hist[threadIdx.x] = tmax > -INFINITY ? fkey(tmax) : 0u;  // per-thread maxima for the top-k bound
   int arg = INT_MAX;
   if (tf != INT_MAX && tmax > -INFINITY) {
     const float4 v = b4[tf];
@@ -708,16 +856,8 @@ __device__ void pass_a(const LaunchParams& P, const Smem& S, const RowParams& q,
   float M = tmax;
   block_argmax(M, arg);
   nal = block_sum_i(nal);
-  float s = 0.0f;
-  if (M > -INFINITY) {
-    const float c = __fmul_rn(1.4426950408889634f, q.invT);
-    for (int f = threadIdx.x; f < nv; f += kThreads) {
-      const float4 v = b4[f];
-      s += (ex2_approx((v.x - M) * c) + ex2_approx((v.y - M) * c)) +
-           (ex2_approx((v.z - M) * c) + ex2_approx((v.w - M) * c));
-    }
-    s = block_sum_f(s);
-  }
+  // the block's sum against M, added in a fixed order
+  const float s = block_sum_f(M > -INFINITY && tmax > -INFINITY ? tsum * ex2_approx((tmax - M) * c) : 0.0f);
   if (threadIdx.x == 0) {
     sh.rec.m = M;
     sh.rec.arg = M > -INFINITY ? arg : INT_MAX;
@@ -761,21 +901,24 @@ __device__ __forceinline__ Item* cand_area(const LaunchParams& P, int row, int s
 
 // Items (z', id) of the slice's tokens with z' >= zc and z' > -inf, in token order per
 // warp step; returns how many there are (only the first `cap` are written).
+// `active` false: the calling thread's vectors hold no such token (its maximum is below),
+// so a warp whose threads are all inactive skips the walk.
 template <class Pred>
-__device__ int compact_if(const Smem& S, int c0, int n, Pred&& keep, Item* dst, int cap) {
+__device__ int compact_if(const Smem& S, int c0, int n, Pred&& keep, Item* dst, int cap, bool active = true) {
   const int nv = (n + 3) >> 2;
   const float4* b4 = reinterpret_cast<const float4*>(S.buf);
   if (threadIdx.x == 0) sh.cnt = 0;
   __syncthreads();
   const int lane = threadIdx.x & 31;
   const unsigned lt = (1u << lane) - 1u;
-  for (int f0 = 0; f0 < nv; f0 += kThreads) {
+  const bool warp_active = __any_sync(~0u, active);
+  for (int f0 = 0; warp_active && f0 < nv; f0 += kThreads) {
     const int f = f0 + threadIdx.x;
     const float4 v = f < nv ? b4[f] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
     const float e[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const bool pr = e[j] > -INFINITY && keep(e[j]);
+      const bool pr = active && e[j] > -INFINITY && keep(e[j]);
       const unsigned bal = __ballot_sync(~0u, pr);
       if (bal) {
         int base = 0;
@@ -790,8 +933,8 @@ __device__ int compact_if(const Smem& S, int c0, int n, Pred&& keep, Item* dst, 
   return sh.cnt;
 }
 
-__device__ int compact(const Smem& S, int c0, int n, float zc, Item* dst, int cap) {
-  return compact_if(S, c0, n, [zc](float z) { return z >= zc; }, dst, cap);
+__device__ int compact(const Smem& S, int c0, int n, float zc, Item* dst, int cap, bool active = true) {
+  return compact_if(S, c0, n, [zc](float z) { return z >= zc; }, dst, cap, active);
 }
 
 // compact() that also counts the tokens at or above `hi_edge` (into *hi).
@@ -836,57 +979,41 @@ __device__ void light_candidates(const LaunchParams& P, const Smem& S, const Row
     // of the slice (the row end checks that every token left out is below the k-th)
     const int nal = sh.rec.nallowed;
     const float share = P.a.bitmask ? (float)nal / (float)max(1, sh.nal_row) : (float)n / (float)P.a.V;
-    const int target = (int)ceilf(1.5f * (float)q.k * share) + 32;
     int nc = -1;
-    if (target < nal) {
-      uint32_t* smp = S.hist;
-      const int ns = min(n, kSample);
-      for (int i = threadIdx.x; i < kSample; i += kThreads) {
-        uint32_t key = 0u;  // padding and masked tokens sort last
-        if (i < ns) {
-          const float z = S.buf[(int)(((long long)i * n) / ns)];
-          if (z > -INFINITY) key = fkey(z);
-        }
-        smp[i] = key;
-      }
-      __syncthreads();
-      for (int size = 2; size <= kSample; size <<= 1)
+    // the need-th largest per-thread maximum of pass A has at least `need` tokens at or
+    // above it, so the compaction keeps at least that many
+    const int need = (int)ceilf(1.2f * (float)q.k * share) + 16;
+    if (need < nal && need <= kThreads) {
+      // each warp sorts its 32 per-thread maxima (shuffles only); the smallest over the
+      // warps of their q-th largest, q = ceil(need / kWarps), has q tokens at or above it
+      // in every warp
+      const uint32_t mine = S.hist[threadIdx.x];  // this thread's maximum (order key)
+      uint32_t key = mine;
+      const int lane = threadIdx.x & 31;
+#pragma unroll
+      for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
-          for (int t = threadIdx.x; t < kSample / 2; t += kThreads) {
-            const int i = 2 * t - (t & (stride - 1)), j = i + stride;
-            const bool desc = (i & size) == 0;
-            const uint32_t a = smp[i], b = smp[j];
-            if ((a < b) == desc) {
-              smp[i] = b;
-              smp[j] = a;
-            }
-          }
-          __syncthreads();
+          const uint32_t o = __shfl_xor_sync(~0u, key, stride);
+          const bool keep_max = ((lane & stride) == 0) == ((lane & size) == 0);
+          key = keep_max ? max(key, o) : min(key, o);
         }
-      // the compaction's exact count must reach 1.2 k times the share (a sample quantile
-      // alone is too noisy at small ranks); too few: a lower sample, too many: a higher one
-      const int need = (int)ceilf(1.2f * (float)q.k * share) + 16;
-      int j = min(ns - 1, (int)ceilf((float)target * (float)ns / (float)n));
-      for (int tries = 0; tries < 4; ++tries) {
-        const uint32_t key = smp[j];
-        if (key == 0u) break;  // the sample runs out of allowed tokens: take them all
-        const float edge = key_to_float(key);
-        const int c = compact(S, c0, n, edge, cand_area(P, row, slice), kCandCap);
-        if (c < need) {
-          if (j == ns - 1) break;
-          j = min(ns - 1, 2 * j + 4);
-          continue;
-        }
+      int qj = min(31, (need + kWarps - 1) / kWarps - 1);
+      for (int tries = 0; tries < 3; ++tries) {
+        const uint32_t thr = block_min_u32(__shfl_sync(~0u, key, qj));
+        if (thr == 0u) break;  // a warp has fewer live threads: take every allowed token
+        const float edge = key_to_float(thr);
+        const int c = compact(S, c0, n, edge, cand_area(P, row, slice), kCandCap, mine >= thr);
         if (c <= kCandCap) {
           zc = edge;
           nc = c;
           break;
         }
-        if (j == 0) {
-          nc = c;  // too many even at the largest sample: spill below
+        if (qj == 0) {
+          nc = c;  // too many even at the warps' maxima: spill below
           break;
         }
-        j >>= 1;
+        qj >>= 1;
       }
     }
     if (threadIdx.x == 0) sh.flag = nc;
@@ -899,7 +1026,7 @@ __device__ void light_candidates(const LaunchParams& P, const Smem& S, const Row
   int nc = 0;
   if (M > -INFINITY) {
     if (q.route == kRouteTopK && sh.flag >= 0) nc = sh.flag;  // compacted while the bound was chosen
-    else nc = compact(S, c0, n, zc, cand_area(P, row, slice), kCandCap);
+    else nc = compact(S, c0, n, zc, cand_area(P, row, slice), kCandCap, !(zc > -INFINITY) || S.hist[threadIdx.x] >= fkey(zc));
     if (nc > kCandCap) {
       nc = spill_slice(P, S, row, slice, c0, n);
       if (threadIdx.x == 0) sh.rec.spilled = nc >= 0;
@@ -934,10 +1061,15 @@ __device__ __forceinline__ Item ldcg_item(const Item* p) {
   return Item{__int_as_float(v.x), v.y};
 }
 
-// Publishes this CTA's record (thread 0 writes it) and everything the CTA wrote before.
+// Publishes this CTA's record and everything the CTA wrote before: the block barrier
+// orders every thread's writes before thread 0's, and thread 0's fence (cumulative) makes
+// them visible device-wide before the ticket or barrier arrival that follows.
 __device__ void publish_rec(const LaunchParams& P, int row, int slice) {
-  if (threadIdx.x == 0) P.srec[(size_t)row * P.C + slice] = sh.rec;
-  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    P.srec[(size_t)row * P.C + slice] = sh.rec;
+    __threadfence();
+  }
   __syncthreads();
 }
 
@@ -1055,27 +1187,31 @@ __device__ void gather_items(const Smem& S, int chunk, float m, float invT) {
   __syncthreads();
   const int lane = threadIdx.x & 31;
   const float zmin = sh.zmin;
-  for (int s = 0; s < sh.nseg; ++s) {
-    const Item* g = sh.seg[s];
-    const int n = sh.segn[s];
-    for (int i0 = 0; i0 < n; i0 += 8 * kThreads) {
-      Item x[8];  // eight loads in flight per thread
+  // one index space over the segments, eight loads in flight per thread
+  int total = 0;
+  for (int s = 0; s < sh.nseg; ++s) total += sh.segn[s];
+  for (int i0 = 0; i0 < total; i0 += 8 * kThreads) {
+    Item x[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int i = i0 + j * kThreads + threadIdx.x;
-        x[j] = i < n ? ldcg_item(g + i) : Item{-INFINITY, 0};
+    for (int j = 0; j < 8; ++j) {
+      int i = i0 + j * kThreads + threadIdx.x;
+      x[j] = Item{-INFINITY, 0};
+      if (i < total) {
+        int s = 0;
+        while (i >= sh.segn[s]) i -= sh.segn[s++];
+        x[j] = ldcg_item(sh.seg[s] + i);
       }
+    }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const bool pr = x[j].z > -INFINITY && x[j].z >= zmin;
-        const unsigned bal = __ballot_sync(~0u, pr);
-        if (!bal) continue;
-        int base = 0;
-        if (lane == 0) base = atomicAdd(&sh.cnt, __popc(bal));
-        base = __shfl_sync(~0u, base, 0);
-        const int pos = base + __popc(bal & ((1u << lane) - 1u));
-        if (pr && pos < cap) it[pos] = Item{y_of(x[j].z, m, invT), x[j].id};
-      }
+    for (int j = 0; j < 8; ++j) {
+      const bool pr = x[j].z > -INFINITY && x[j].z >= zmin;
+      const unsigned bal = __ballot_sync(~0u, pr);
+      if (!bal) continue;
+      int base = 0;
+      if (lane == 0) base = atomicAdd(&sh.cnt, __popc(bal));
+      base = __shfl_sync(~0u, base, 0);
+      const int pos = base + __popc(bal & ((1u << lane) - 1u));
+      if (pr && pos < cap) it[pos] = Item{y_of(x[j].z, m, invT), x[j].id};
     }
   }
   __syncthreads();
@@ -1268,8 +1404,6 @@ constexpr int kSortCap = 2048;  // items the sorted finisher takes (its masses f
 // composites (order key << 32 | ~id), bitonic, padded to a power of two with zeros.
 __device__ void sort_items(const Smem& S, int n) {
   unsigned long long* k = reinterpret_cast<unsigned long long*>(fin_items(S));
-  int np = 1;
-  while (np < n) np <<= 1;
   static_assert(kSortCap <= 8 * kThreads, "eight items per thread");
   unsigned long long v[8];
 #pragma unroll
@@ -1285,24 +1419,10 @@ __device__ void sort_items(const Smem& S, int n) {
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const int i = threadIdx.x + j * kThreads;
-    if (i < np) k[i] = v[j];
+    if (i < n) k[i] = v[j];
   }
   __syncthreads();
-  for (int size = 2; size <= np; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int t = threadIdx.x; t < np / 2; t += kThreads) {
-        const int i = 2 * t - (t & (stride - 1));
-        const int j = i + stride;
-        const bool desc = (i & size) == 0;
-        const unsigned long long a = k[i], b = k[j];
-        if ((a < b) == desc) {
-          k[i] = b;
-          k[j] = a;
-        }
-      }
-      __syncthreads();
-    }
-  }
+  sort_desc(k, n);
 }
 
 __device__ __forceinline__ float sorted_y(unsigned long long v) { return key_to_float((uint32_t)(v >> 32)); }
@@ -1775,6 +1895,10 @@ __device__ void slice_front(const LaunchParams& P, const Smem& S, const RowParam
   claim_tokens(P, S, q, c0, n);
   const int ntouch = sh.ntouch;
   if (ntouch > 0) transforms_prep(P, S, q, c0, n, 0);
+  if (P.a.bitmask) {
+    const int32_t* mrow = P.a.bitmask + (long long)row * P.a.bitmask_row_stride + (c0 >> 5);
+    for (int w = threadIdx.x; w < ((n + 31) >> 5); w += kThreads) S.mask[w] = (uint32_t)__ldg(mrow + w);
+  }
   if (q.route == kRouteTopK && P.a.bitmask) {
     const int V = P.a.V, W = (V + 31) >> 5;
     const int32_t* mrow = P.a.bitmask + (long long)row * P.a.bitmask_row_stride;
@@ -1921,7 +2045,7 @@ constexpr ScratchLayout scratch_layout(size_t B, size_t C, size_t chunk, size_t 
   return L;
 }
 
-constexpr int kSpillRows = 16;  // rows of one call whose items may spill (handle scratch)
+constexpr int kSpillRows = 16;  // at least this many spill rows per handle (max_batch / 8 for big batches)
 
 struct Scratch {
   int max_batch;
@@ -2054,7 +2178,8 @@ int clsample_create(int32_t max_batch, int32_t vocab, clsample_t** out) {
   int grid[2];
   if ((rc = resident_ctas(g, false, dev, &grid[0])) != CLSAMPLE_SUCCESS) return rc;
   if ((rc = resident_ctas(g, true, dev, &grid[1])) != CLSAMPLE_SUCCESS) return rc;
-  const int spill_rows = max_batch < kSpillRows ? max_batch : kSpillRows;
+  int spill_rows = max_batch / 8 > kSpillRows ? max_batch / 8 : kSpillRows;
+  if (spill_rows > max_batch) spill_rows = max_batch;
   unsigned char* base = nullptr;
   if (max_batch > 0) {
     const size_t bytes = scratch_layout((size_t)max_batch, (size_t)g.C, (size_t)g.chunk, (size_t)spill_rows).total;

@@ -120,6 +120,25 @@ struct RowParams {
   int hlo, hhi, blo, bhi;  // CSR ranges (hhi < hlo: none / invalid handled by flags)
 };
 
+// One penalised or biased token of a row, as the preparation launch lists it (the
+// entries of a slice are contiguous).
+struct __align__(16) PenEntry {
+  int lid;       // id within its slice
+  unsigned cnt;  // occurrences in the history
+  int bj;        // the last valid logit_bias entry of the id (-1: none)
+  int pad;
+};
+constexpr int kPenRowCap = 8192;   // listed tokens per row (more: the slices scan themselves)
+constexpr int kHashSlots = 4096;   // the preparation CTA's hash of a row's ids
+
+// Per-row facts from the preparation launch.
+struct RowInfo {
+  int flags;  // kFlagInvalid: bad CSR offsets, ids out of range, NaN bias values
+  int nal;    // allowed tokens by the bitmask (V without one)
+  int ready;  // the row's entries are listed (else each slice scans the CSRs itself)
+  int pad;
+};
+
 struct LaunchParams {
   clsample_args_t a;
   int C;
@@ -134,6 +153,10 @@ struct LaunchParams {
   Bins* bins;         // [B * C]
   Item* cand;         // [B * C][kCandCap]
   Item* spill;        // [spill_rows][C * chunk]
+  RowInfo* rinfo;     // [B]
+  int* poff;          // [B][C + 1] each slice's first entry
+  PenEntry* pent;     // [B][kPenRowCap]
+  int lists;          // the preparation launch wrote rinfo / poff / pent (penalties, bias or a mask)
 };
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -214,6 +237,7 @@ struct Shared {
   SliceRec row;            // combined record of the row (heavy rows, finisher)
   unsigned long long bar;  // the slice copy's mbarrier
   unsigned bar_uses;       // its completed phases
+  uint32_t bulk;           // bytes of the slice copy in flight (issued at entry)
   float red_f[kWarps * 2];
   int red_i[kWarps * 2];
   unsigned long long red_u[kWarps];
@@ -434,6 +458,35 @@ __device__ void block_sort_desc(unsigned long long* k) {
   __syncthreads();
 }
 
+// Sorts 32 E keys held by one warp (lane l holds keys [l E, l E + E)) in descending order,
+// bitonic, with shuffles only.
+template <int E>
+__device__ void warp_sort_desc(unsigned long long (&v)[E]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll 1
+  for (int size = 2; size <= 32 * E; size <<= 1) {
+#pragma unroll 1
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      if (stride >= E) {
+        const int lm = stride / E;
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+          v[e] = bitonic_pick(v[e], __shfl_xor_sync(~0u, v[e], lm), lane * E + e, size, stride);
+      } else {
+        unsigned long long w[E];
+#pragma unroll
+        for (int st = 1; st < E; st <<= 1) {
+          if (st != stride) continue;
+#pragma unroll
+          for (int e = 0; e < E; ++e) w[e] = bitonic_pick(v[e], v[e ^ st], lane * E + e, size, st);
+#pragma unroll
+          for (int e = 0; e < E; ++e) v[e] = w[e];
+        }
+      }
+    }
+  }
+}
+
 // Sorts n <= 2048 keys (padded with zeros to 256 E) descending.
 __device__ void sort_desc(unsigned long long* k, int n) {
   int np = kThreads;
@@ -504,12 +557,201 @@ __device__ __forceinline__ int route_rank(int route) {
 
 // ---------------------------------------------------------------- ordering kernel
 
-constexpr int kOrderThreads = 1024;
+constexpr int kOrderThreads = 512;
+
+constexpr size_t kPrepSmem = (size_t)kHashSlots * 14;  // keys, counts, bias entries, slot list
+
+// Hash slot of id (an empty slot holds 0; a taken one id + 1), -1 if the table is full;
+// *created tells whether this call took the slot.
+__device__ __forceinline__ int hash_insert(uint32_t* key, int id, bool* created) {
+  uint32_t h = ((uint32_t)id * 2654435761u) >> 20;  // 12 bits: kHashSlots
+  *created = false;
+  for (int probe = 0; probe < kHashSlots; ++probe) {
+    const uint32_t k = atomicCAS(&key[h], 0u, (uint32_t)id + 1u);
+    if (k == 0u) *created = true;
+    if (k == 0u || k == (uint32_t)id + 1u) return (int)h;
+    h = (h + 1u) & (kHashSlots - 1u);
+  }
+  return -1;
+}
+
+// Appends the slots the warp's lanes created to the slot list, one counter update per warp.
+__device__ __forceinline__ void list_append(uint16_t* list, int* nlist, bool created, int h) {
+  const int lane = threadIdx.x & 31;
+  const unsigned b = __ballot_sync(~0u, created);
+  if (!b) return;
+  int base = 0;
+  if (lane == 0) base = atomicAdd(nlist, __popc(b));
+  base = __shfl_sync(~0u, base, 0);
+  if (created) list[base + __popc(b & ((1u << lane) - 1u))] = (uint16_t)h;
+}
+static_assert(kHashSlots == 1 << 12, "hash of 12 bits");
+
+// One CTA per row (preparation launch): the row's distinct history ids with their counts
+// and the last valid logit_bias entry of each id, listed by slice; validity flags; the
+// mask's allowed count.  A row whose entries do not fit is left to the slices (ready 0).
+__device__ void prep_row_lists(const LaunchParams& P, int row) {
+  uint32_t* key = reinterpret_cast<uint32_t*>(smem_dyn);
+  unsigned* cnt = key + kHashSlots;
+  int* bj = reinterpret_cast<int*>(cnt + kHashSlots);
+  uint16_t* list = reinterpret_cast<uint16_t*>(bj + kHashSlots);
+  __shared__ int scnt[kMaxSlices + 1], sfill[kMaxSlices];
+  __shared__ int sflags, sover, snal, nlist;
+  const int C = P.C, chunk = P.chunk, V = P.a.V;
+  for (int h = threadIdx.x; h < kHashSlots; h += kOrderThreads) {
+    key[h] = 0u;
+    cnt[h] = 0u;
+    bj[h] = -1;
+  }
+  if (threadIdx.x < kMaxSlices + 1) scnt[threadIdx.x] = 0;
+  if (threadIdx.x < kMaxSlices) sfill[threadIdx.x] = 0;
+  if (threadIdx.x == 0) {
+    sflags = 0;
+    sover = 0;
+    nlist = 0;
+  }
+  __syncthreads();
+  int bad = 0, over = 0;
+  const int lane = threadIdx.x & 31;
+  if (P.a.hist_offs) {
+    const int lo = P.a.hist_offs[row], hi = P.a.hist_offs[row + 1];
+    if (lo < 0 || hi < lo) bad = 1;
+    else
+      for (int j0 = lo; j0 < hi; j0 += 8 * kOrderThreads) {
+        int ids[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int j = j0 + u * kOrderThreads + threadIdx.x;
+          ids[u] = j < hi ? __ldg(P.a.hist_ids + j) : INT_MIN;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int id = ids[u];
+          const bool ok = id >= 0 && id < V;
+          if (id != INT_MIN && !ok) bad = 1;
+          const unsigned peers = __match_any_sync(~0u, ok ? id : -1);
+          bool created = false;
+          int h = -1;
+          if (ok && (__ffs(peers) - 1) == lane) {
+            h = hash_insert(key, id, &created);
+            if (h < 0) over = 1;
+            else atomicAdd(&cnt[h], (unsigned)__popc(peers));
+          }
+          list_append(list, &nlist, created, h);
+        }
+      }
+  }
+  if (P.a.bias_offs) {
+    const int lo = P.a.bias_offs[row], hi = P.a.bias_offs[row + 1];
+    if (lo < 0 || hi < lo) bad = 1;
+    else
+      for (int j0 = lo; j0 < hi; j0 += kOrderThreads) {
+        const int j = j0 + threadIdx.x;
+        bool created = false;
+        int h = -1;
+        if (j < hi) {
+          const int id = __ldg(P.a.bias_ids + j);
+          const float b = __ldg(P.a.bias_vals + j);
+          if (id < 0 || id >= V || b != b) {
+            bad = 1;
+          } else {
+            h = hash_insert(key, id, &created);
+            if (h < 0) over = 1;
+            else atomicMax(&bj[h], j);
+          }
+        }
+        list_append(list, &nlist, created, h);
+      }
+  }
+  if (bad) sflags = kFlagInvalid;
+  if (over) sover = 1;
+  __syncthreads();
+  const int nl = min(nlist, kHashSlots);
+  const int lane2 = threadIdx.x & 31;
+  for (int i0 = 0; i0 < nl; i0 += kOrderThreads) {
+    const int i = i0 + threadIdx.x;
+    const int sl = i < nl ? (int)(key[list[i]] - 1u) / chunk : -1;
+    const unsigned peers = __match_any_sync(~0u, sl);
+    if (sl >= 0 && (__ffs(peers) - 1) == lane2) atomicAdd(&scnt[sl], __popc(peers));
+  }
+  __syncthreads();
+  int* poff = P.poff + (size_t)row * (C + 1);
+  if (threadIdx.x == 0) {
+    int t = 0;
+    for (int s = 0; s < C; ++s) {
+      const int c = scnt[s];
+      scnt[s] = t;
+      poff[s] = t;
+      t += c;
+    }
+    poff[C] = t;
+    if (t > kPenRowCap) sover = 1;
+  }
+  __syncthreads();
+  if (!sover) {
+    PenEntry* out = P.pent + (size_t)row * kPenRowCap;
+    for (int i0 = 0; i0 < nl; i0 += kOrderThreads) {
+      const int i = i0 + threadIdx.x;
+      const int h = i < nl ? list[i] : 0;
+      const int id = i < nl ? (int)(key[h] - 1u) : -1;
+      const int sl = id >= 0 ? id / chunk : -1;
+      // one counter update per slice and warp; each thread takes its rank among its peers
+      const unsigned peers = __match_any_sync(~0u, sl);
+      const int leader = __ffs(peers) - 1;
+      int base = 0;
+      if (sl >= 0 && leader == lane2) base = atomicAdd(&sfill[sl], __popc(peers));
+      base = __shfl_sync(peers, base, leader);
+      if (sl < 0) continue;
+      const int pos = scnt[sl] + base + __popc(peers & ((1u << lane2) - 1u));
+      PenEntry e;
+      e.lid = id - sl * chunk;
+      e.cnt = cnt[h];
+      e.bj = bj[h];
+      e.pad = 0;
+      out[pos] = e;
+    }
+  }
+  int nal = V;
+  if (P.a.bitmask) {
+    const int W = (V + 31) >> 5;
+    const int32_t* mrow = P.a.bitmask + (long long)row * P.a.bitmask_row_stride;
+    int c = 0;
+    // eight words in flight per thread
+    for (int w0 = 0; w0 < W; w0 += 8 * kOrderThreads) {
+      uint32_t x[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int w = w0 + u * kOrderThreads + threadIdx.x;
+        x[u] = w < W ? (uint32_t)__ldg(mrow + w) : 0u;
+        if (w == W - 1 && (V & 31)) x[u] &= (1u << (V & 31)) - 1u;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) c += __popc(x[u]);
+    }
+    if (threadIdx.x == 0) snal = 0;
+    __syncthreads();
+    atomicAdd(&snal, c);
+    __syncthreads();
+    nal = snal;
+  }
+  if (threadIdx.x == 0) {
+    RowInfo ri;
+    ri.flags = sflags;
+    ri.nal = nal;
+    ri.ready = !sover;
+    ri.pad = 0;
+    P.rinfo[row] = ri;
+  }
+}
 
 // One CTA: classifies the rows, writes the list order (stable within a class) and resets
 // the call's counters.
 __global__ void __launch_bounds__(kOrderThreads) order_kernel(const __grid_constant__ LaunchParams P) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (blockIdx.x > 0) {
+    prep_row_lists(P, blockIdx.x - 1);
+    return;
+  }
   __shared__ int cnt[3][kOrderThreads / 32];
   const int B = P.a.B;
   if (threadIdx.x == 0) {
@@ -982,7 +1224,7 @@ __device__ void light_candidates(const LaunchParams& P, const Smem& S, const Row
     int nc = -1;
     // the need-th largest per-thread maximum of pass A has at least `need` tokens at or
     // above it, so the compaction keeps at least that many
-    const int need = (int)ceilf(1.2f * (float)q.k * share) + 16;
+    const int need = (int)ceilf(1.2f * (float)q.k * share) + 4;
     if (need < nal && need <= kThreads) {
       // each warp sorts its 32 per-thread maxima (shuffles only); the smallest over the
       // warps of their q-th largest, q = ceil(need / kWarps), has q tokens at or above it
@@ -1402,8 +1644,38 @@ constexpr int kSortCap = 2048;  // items the sorted finisher takes (its masses f
 
 // Sorts the n <= kSortCap smem items in place by (y descending, id ascending) as 64-bit
 // composites (order key << 32 | ~id), bitonic, padded to a power of two with zeros.
-__device__ void sort_items(const Smem& S, int n) {
+__device__ void sort_items(const Smem& S, int chunk, int n) {
   unsigned long long* k = reinterpret_cast<unsigned long long*>(fin_items(S));
+  if (n <= 2 * kThreads) {
+    // rank sort: the composites are distinct, so each one's position is the number of
+    // larger ones (every thread counts against all n, reading broadcast words)
+    unsigned long long mine[2];
+    int rank[2] = {0, 0};
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int i = threadIdx.x + u * kThreads;
+      mine[u] = 0ull;
+      if (i < n) {
+        const Item it = fin_items(S)[i];
+        mine[u] = ((unsigned long long)fkey(it.z) << 32) | (uint32_t)(~(uint32_t)it.id);
+      }
+    }
+    unsigned long long* tmp = reinterpret_cast<unsigned long long*>(fin_hc(S, chunk));
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+      if (threadIdx.x + u * kThreads < n) tmp[threadIdx.x + u * kThreads] = mine[u];
+    __syncthreads();
+    for (int j = 0; j < n; ++j) {
+      const unsigned long long o = tmp[j];
+      rank[0] += o > mine[0];
+      rank[1] += o > mine[1];
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+      if (threadIdx.x + u * kThreads < n) k[rank[u]] = mine[u];
+    __syncthreads();
+    return;
+  }
   static_assert(kSortCap <= 8 * kThreads, "eight items per thread");
   unsigned long long v[8];
 #pragma unroll
@@ -1435,7 +1707,7 @@ template <class Above>
 __device__ void finish_sorted(const LaunchParams& P, const Smem& S, const RowParams& q, int row, const Above& ab,
                               bool heavy, int status, const SliceRec& R, float lnS, bool sorted) {
   const int n = sh.fin_n;
-  if (!sorted) sort_items(S, n);
+  if (!sorted) sort_items(S, P.chunk, n);
   const unsigned long long* k = reinterpret_cast<const unsigned long long*>(fin_items(S));
   auto key_at = [&](int i) { return (uint32_t)(k[i] >> 32); };
   auto count_ge = [&](int lim, uint32_t key) {
@@ -1518,6 +1790,82 @@ __device__ void finish_sorted(const LaunchParams& P, const Smem& S, const RowPar
   }
 }
 
+// Narrows the finisher's items to those at or above the digit range that holds the
+// krem-th largest key, once that set has at most kSortCap items (histogram rounds as in
+// select_kth), and leaves them in fin_items as sorted composites (sh.fin_n, sh.fin_smem).
+// The kept set of a row with a top-k cut lies inside that set.  False if no round gets
+// the set small enough.
+__device__ bool prefilter_kth(const Smem& S, int chunk, float m, float invT, int krem) {
+  uint32_t* hc = fin_hc(S, chunk);
+  uint32_t prefix = 0, lo_key = 0;
+  int surv = -1, A = 0;  // A: items above the current digit range
+  for (int r = 0; r < 3 && surv < 0; ++r) {
+    const int sft = digit_shift(r);
+    const uint32_t dmask = (1u << digit_width(r)) - 1u;
+    for (int t = threadIdx.x; t < kDigitBins; t += kThreads) hc[t] = 0u;
+    if (threadIdx.x == 0) sh.digit = -1;
+    __syncthreads();
+    visit(S, m, invT, [&](float y, int) {
+      const uint32_t key = fkey(y);
+      if (digit_match(key, r, prefix)) atomicAdd(&hc[(key >> sft) & dmask], 1u);
+    });
+    __syncthreads();
+    int c = 0;
+    for (int d = 8 * (int)threadIdx.x; d < 8 * (int)threadIdx.x + 8; ++d) c += (int)hc[d];
+    int tot = 0;
+    const int pre = block_scan_i(c, &tot);
+    const int above = tot - pre - c;
+    if (above < krem && above + c >= krem) {
+      int run = above;
+      for (int d = 8 * (int)threadIdx.x + 7; d >= 8 * (int)threadIdx.x; --d) {
+        if (run + (int)hc[d] >= krem) {
+          sh.digit = d;
+          sh.cnt = run;
+          sh.flag = run + (int)hc[d];
+          break;
+        }
+        run += (int)hc[d];
+      }
+    }
+    __syncthreads();
+    if (sh.digit < 0) return false;
+    const int in_above = sh.cnt, in_incl = sh.flag;
+    prefix = (prefix << digit_width(r)) | (uint32_t)sh.digit;
+    if (A + in_incl <= kSortCap) {
+      lo_key = prefix << sft;  // every item at or above this digit's lower edge
+      surv = 1;
+    }
+    A += in_above;
+    krem -= in_above;
+    __syncthreads();
+  }
+  if (surv < 0) return false;
+  // compact the survivors as composites into the histogram area, then sort them into place
+  unsigned long long* tmp = reinterpret_cast<unsigned long long*>(hc);
+  if (threadIdx.x == 0) sh.cnt = 0;
+  __syncthreads();
+  visit(S, m, invT, [&](float y, int id) {
+    const uint32_t key = fkey(y);
+    if (key >= lo_key) {
+      const int pos = atomicAdd(&sh.cnt, 1);
+      if (pos < kSortCap) tmp[pos] = ((unsigned long long)key << 32) | (uint32_t)(~(uint32_t)id);
+    }
+  });
+  __syncthreads();
+  const int n = min(sh.cnt, kSortCap);
+  unsigned long long* k = reinterpret_cast<unsigned long long*>(fin_items(S));
+  for (int i = threadIdx.x; i < n; i += kThreads) k[i] = tmp[i];
+  __syncthreads();
+  sort_desc(k, n);
+  if (threadIdx.x == 0) {
+    sh.fin_n = n;
+    sh.fin_smem = 1;
+  }
+  __syncthreads();
+  return sh.cnt <= kSortCap;
+}
+static_assert(kSortCap * 8 <= kFinHistBytes, "survivors fit the histogram area");
+
 // ---------------------------------------------------------------- row end: finisher
 
 template <bool kBF16>
@@ -1583,8 +1931,11 @@ __device__ void finish_row(const LaunchParams& P, const Smem& S, const RowParams
       if (kc > 0 && kc <= sh.fin_n) {
         uint32_t key;
         if (sh.fin_smem && sh.fin_n <= kSortCap) {
-          sort_items(S, sh.fin_n);
+          sort_items(S, P.chunk, sh.fin_n);
           sorted = true;
+          key = (uint32_t)(reinterpret_cast<const unsigned long long*>(fin_items(S))[kc - 1] >> 32);
+        } else if (prefilter_kth(S, P.chunk, m, invT, kc)) {
+          sorted = true;  // the survivors (a superset of the top-k set) are sorted in place
           key = (uint32_t)(reinterpret_cast<const unsigned long long*>(fin_items(S))[kc - 1] >> 32);
         } else {
           key = select_kth(S, P.chunk, m, invT, kc);
@@ -1608,6 +1959,11 @@ __device__ void finish_row(const LaunchParams& P, const Smem& S, const RowParams
     sorted = false;
   }
   status = max(status, row_status_of(sh.row));  // a redone slice may have run out of spill room
+  // many items and a top-k cut (heavy rows with k > kKMax): narrow them to a sortable set
+  if (!sorted && !(sh.fin_smem && sh.fin_n <= kSortCap) && kc > 0) {
+    const int krem = kc - (int)ab.n;
+    if (krem >= 1 && krem <= sh.fin_n && prefilter_kth(S, P.chunk, m, invT, krem)) sorted = true;
+  }
   if (sh.fin_smem && sh.fin_n <= kSortCap) {
     finish_sorted(P, S, q, row, ab, heavy, status, R, lnS, sorted);
     return;
@@ -1738,7 +2094,7 @@ __device__ void heavy_slice(const LaunchParams& P, const Smem& S, const RowParam
       if (!(z > -INFINITY)) continue;
       const float y = y_of(z, m, invT);
       const int b = ybin(y);
-      const unsigned long long w = wm ? weight_fx(y) : 0ull;
+      const unsigned long long w = (wm && y > -28.0f) ? weight_fx(y) : 0ull;  // e^-28 < 2^-40
       if (b == kYBins - 1) {
         ++clast;
         wlast += w;
@@ -1890,26 +2246,69 @@ __device__ void heavy_above(Above& ab, int C) {
 // (sh.rec gets the slice statistics).
 template <bool kBF16>
 __device__ void slice_front(const LaunchParams& P, const Smem& S, const RowParams& q, int row, int slice, int c0,
-                            int n) {
-  const uint32_t bulk = slice_load<kBF16>(P, S, row, c0, n);
+                            int n, uint32_t bulk) {
+  RowInfo ri{0, P.a.V, 0, 0};
+  if (P.lists) ri = P.rinfo[row];
+  if (threadIdx.x == 0) {
+    sh.rec.flags |= ri.flags;
+    sh.nal_row = ri.nal;
+  }
+  if (ri.ready) {
+    // the row's entries of this slice, listed by the preparation launch: mark them (the
+    // checked walk of pass A must not sanitise them again) and keep up to two per thread
+    // in registers until the logits have landed
+    const int* po = P.poff + (size_t)row * (P.C + 1) + slice;
+    const int e0 = po[0], ne = po[1] - e0;
+    const PenEntry* seg = P.pent + (size_t)row * kPenRowCap + e0;
+    const int nw = (n + 31) >> 5;
+    for (int w = threadIdx.x; w < nw; w += kThreads) S.claim[w] = 0u;
+    PenEntry mine[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int i = threadIdx.x + u * kThreads;
+      mine[u].lid = -1;
+      if (i < ne) mine[u] = seg[i];
+    }
+    if (P.a.bitmask) {
+      const int32_t* mrow = P.a.bitmask + (long long)row * P.a.bitmask_row_stride + (c0 >> 5);
+      for (int w = threadIdx.x; w < nw; w += kThreads) S.mask[w] = (uint32_t)__ldg(mrow + w);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+      if (mine[u].lid >= 0) atomicOr(&S.claim[mine[u].lid >> 5], 1u << (mine[u].lid & 31));
+    if (!slice_wait(bulk) && threadIdx.x == 0) sh.rec.flags |= kFlagOverflow;
+    __syncthreads();
+    if (kBF16) widen_bf16(S, P.chunk, n);
+    for (int i0 = 0; i0 < ne; i0 += 2 * kThreads) {
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        PenEntry e = mine[u];
+        if (i0 > 0) {
+          const int i = i0 + threadIdx.x + u * kThreads;
+          e.lid = -1;
+          if (i < ne) {
+            e = seg[i];
+            atomicOr(&S.claim[e.lid >> 5], 1u << (e.lid & 31));
+          }
+        }
+        if (e.lid < 0) continue;
+        float z = sanitize(S.buf[e.lid]);
+        if (e.cnt) z = apply_penalties(z, e.cnt, q.freq, q.pres, q.rep);
+        if (e.bj >= 0) z = __fadd_rn(z, __ldg(P.a.bias_vals + e.bj));
+        S.buf[e.lid] = guard(z);
+      }
+    }
+    __syncthreads();
+    pass_a(P, S, q, row, c0, n);
+    return;
+  }
   claim_tokens(P, S, q, c0, n);
   const int ntouch = sh.ntouch;
   if (ntouch > 0) transforms_prep(P, S, q, c0, n, 0);
   if (P.a.bitmask) {
     const int32_t* mrow = P.a.bitmask + (long long)row * P.a.bitmask_row_stride + (c0 >> 5);
     for (int w = threadIdx.x; w < ((n + 31) >> 5); w += kThreads) S.mask[w] = (uint32_t)__ldg(mrow + w);
-  }
-  if (q.route == kRouteTopK && P.a.bitmask) {
-    const int V = P.a.V, W = (V + 31) >> 5;
-    const int32_t* mrow = P.a.bitmask + (long long)row * P.a.bitmask_row_stride;
-    int c = 0;
-    for (int w = threadIdx.x; w < W; w += kThreads) {
-      uint32_t x = (uint32_t)__ldg(mrow + w);
-      if (w == W - 1 && (V & 31)) x &= (1u << (V & 31)) - 1u;
-      c += __popc(x);
-    }
-    c = block_sum_i(c);
-    if (threadIdx.x == 0) sh.nal_row = c;
   }
   if (!slice_wait(bulk) && threadIdx.x == 0) sh.rec.flags |= kFlagOverflow;
   __syncthreads();
@@ -1927,7 +2326,7 @@ template <bool kBF16>
 __device__ void reprocess_slice(const LaunchParams& P, const Smem& S, const RowParams& q, int row, int s) {
   const int c0 = s * P.chunk;
   const int n = min(P.a.V - c0, P.chunk);
-  slice_front<kBF16>(P, S, q, row, s, c0, n);
+  slice_front<kBF16>(P, S, q, row, s, c0, n, slice_load<kBF16>(P, S, row, c0, n));
   const int nc = spill_slice(P, S, row, s, c0, n);
   if (threadIdx.x == 0) {
     if (nc < 0) {
@@ -1952,6 +2351,14 @@ __global__ void __launch_bounds__(kThreads, 3) sampler_kernel(const __grid_const
     sh.row_id = P.order[item / (unsigned)C];
     sh.slice = (int)(item % (unsigned)C);
     sh.bar_uses = 0;
+  }
+  __syncthreads();
+  {
+    // the slice copy starts before anything else is read
+    const int c0 = sh.slice * P.chunk;
+    sh.bulk = slice_load<kBF16>(P, S, sh.row_id, c0, min(P.a.V - c0, P.chunk));
+  }
+  if (threadIdx.x == 0) {
     load_params(P.a, sh.row_id, sh.rp);
     SliceRec z;
     memset(&z, 0, sizeof z);
@@ -1969,7 +2376,7 @@ __global__ void __launch_bounds__(kThreads, 3) sampler_kernel(const __grid_const
   const RowParams& q = sh.rp;
   const int c0 = slice * P.chunk;
   const int n = min(P.a.V - c0, P.chunk);
-  slice_front<kBF16>(P, S, q, row, slice, c0, n);
+  slice_front<kBF16>(P, S, q, row, slice, c0, n, sh.bulk);
   Above ab{0u, 0ull, 0ull, -INFINITY, 0.0f, INFINITY, INT_MAX, 0};
   const bool heavy = q.route == kRouteHeavy;
   if (heavy) heavy_slice(P, S, q, row, slice, c0, n, ab);
@@ -2022,7 +2429,7 @@ Geometry geometry_for(int vocab) {
 
 // Byte offsets of the scratch arrays for B rows of C slices of `chunk` tokens.
 struct ScratchLayout {
-  size_t ctl, order, rowctl, srec, bins, cand, spill, total;
+  size_t ctl, order, rowctl, srec, bins, cand, spill, rinfo, poff, pent, total;
 };
 
 constexpr size_t take(size_t& off, size_t bytes) {
@@ -2041,6 +2448,9 @@ constexpr ScratchLayout scratch_layout(size_t B, size_t C, size_t chunk, size_t 
   L.bins = take(off, B * C * sizeof(Bins));
   L.cand = take(off, B * C * kCandCap * sizeof(Item));
   L.spill = take(off, spill_rows * C * chunk * sizeof(Item));
+  L.rinfo = take(off, B * sizeof(RowInfo));
+  L.poff = take(off, B * (C + 1) * sizeof(int));
+  L.pent = take(off, B * kPenRowCap * sizeof(PenEntry));
   L.total = off;
   return L;
 }
@@ -2068,7 +2478,9 @@ int setup_device(int dev) {
   if (smem > optin) return CLSAMPLE_ERR_DEVICE;
   const void* k32 = reinterpret_cast<const void*>(&sampler_kernel<false>);
   const void* k16 = reinterpret_cast<const void*>(&sampler_kernel<true>);
-  if (cudaFuncSetAttribute(k32, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+  const void* ko = reinterpret_cast<const void*>(&order_kernel);
+  if (cudaFuncSetAttribute(ko, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem) != cudaSuccess ||
+      cudaFuncSetAttribute(k32, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
       cudaFuncSetAttribute(k16, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
       cudaFuncSetAttribute(k32, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared) !=
           cudaSuccess ||
@@ -2246,6 +2658,10 @@ int make_params(const Geometry& g, int vocab, int dev, const Scratch& sc, const 
   P->bins = reinterpret_cast<Bins*>(b + L.bins);
   P->cand = reinterpret_cast<Item*>(b + L.cand);
   P->spill = reinterpret_cast<Item*>(b + L.spill);
+  P->rinfo = reinterpret_cast<RowInfo*>(b + L.rinfo);
+  P->poff = reinterpret_cast<int*>(b + L.poff);
+  P->pent = reinterpret_cast<PenEntry*>(b + L.pent);
+  P->lists = (a->hist_offs || a->bias_offs || a->bitmask) ? 1 : 0;
   return CLSAMPLE_SUCCESS;
 }
 
@@ -2254,8 +2670,11 @@ int make_params(const clsample_t* h, const clsample_args_t* a, LaunchParams* P) 
   return make_params(h->g, h->vocab, h->device, h->sc, a, P);
 }
 
+// The preparation launch: CTA 0 orders the rows and resets the counters; with penalties,
+// bias or a mask, CTAs 1..B list each row's entries.
 int launch_order(const LaunchParams& P, cudaStream_t st) {
-  order_kernel<<<1, kOrderThreads, 0, st>>>(P);
+  const unsigned grid = P.lists ? 1u + (unsigned)P.a.B : 1u;
+  order_kernel<<<grid, kOrderThreads, P.lists ? kPrepSmem : 0, st>>>(P);
   return cudaGetLastError() == cudaSuccess ? CLSAMPLE_SUCCESS : CLSAMPLE_ERR_CUDA;
 }
 

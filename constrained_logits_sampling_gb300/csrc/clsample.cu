@@ -146,7 +146,8 @@ struct LaunchParams {
   int vec_ok;  // every row start is 16-byte aligned: slices arrive by TMA bulk copies
   int spill_rows;
   // scratch (device)
-  unsigned* ctl;      // [0] next item, [1] spill slots taken
+  unsigned* ctl;      // [0] next item, [1] spill slots taken, [2] order ready, [3] CTAs done
+  unsigned* rflag;    // [B] the row's entries are listed (preparation launch)
   int* order;         // [B] rows in list order
   RowCtl* rowctl;     // [B]
   SliceRec* srec;     // [B * C]
@@ -263,10 +264,25 @@ __shared__ Shared sh;
 
 // ---------------------------------------------------------------- block reductions
 
+__device__ __forceinline__ void st_release(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Bounded wait until *p == v (acquire); false on timeout.
+__device__ bool wait_flag(const unsigned* p, unsigned v);
+
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+
+__device__ bool wait_flag(const unsigned* p, unsigned v) {
+  for (uint32_t i = 0; i < kWaitPolls; ++i) {
+    if (ld_acquire(p) == v) return true;
+    __nanosleep(64);
+  }
+  return false;
 }
 
 
@@ -549,10 +565,14 @@ __device__ void load_params(const clsample_args_t& a, int row, RowParams& q) {
   else q.route = kRouteHeavy;
 }
 
-// List order of a row's route: heavy rows first (their CTAs wait for each other), then
-// rows that finish from candidates, greedy and invalid rows last (the cheapest).
-__device__ __forceinline__ int route_rank(int route) {
-  return route == kRouteHeavy ? 0 : (route == kRouteGreedy ? 2 : 1);
+// List order of a row: heavy rows first (their CTAs wait for each other and work longest),
+// then top-k rows with a large k (their row ends take longest), other rows that finish
+// from candidates, greedy and invalid rows last (the cheapest).
+constexpr int kClasses = 4;
+__device__ __forceinline__ int route_rank(const RowParams& q) {
+  if (q.route == kRouteHeavy) return 0;
+  if (q.route == kRouteTopK && q.k > 128) return 1;
+  return q.route == kRouteGreedy ? 3 : 2;
 }
 
 // ---------------------------------------------------------------- ordering kernel
@@ -734,6 +754,7 @@ __device__ void prep_row_lists(const LaunchParams& P, int row) {
     __syncthreads();
     nal = snal;
   }
+  __syncthreads();
   if (threadIdx.x == 0) {
     RowInfo ri;
     ri.flags = sflags;
@@ -741,6 +762,8 @@ __device__ void prep_row_lists(const LaunchParams& P, int row) {
     ri.ready = !sover;
     ri.pad = 0;
     P.rinfo[row] = ri;
+    __threadfence();
+    st_release(&P.rflag[row], 1u);
   }
 }
 
@@ -752,21 +775,22 @@ __global__ void __launch_bounds__(kOrderThreads) order_kernel(const __grid_const
     prep_row_lists(P, blockIdx.x - 1);
     return;
   }
-  __shared__ int cnt[3][kOrderThreads / 32];
+  __shared__ int cnt[kClasses][kOrderThreads / 32];
   const int B = P.a.B;
   if (threadIdx.x == 0) {
     P.ctl[0] = 0;
     P.ctl[1] = 0;
+    P.ctl[3] = 0;
   }
   // totals per class first, so each class knows where it starts
-  int tot[3] = {0, 0, 0};
+  int tot[kClasses] = {0, 0, 0, 0};
   for (int r0 = 0; r0 < B; r0 += kOrderThreads) {
     const int r = r0 + threadIdx.x;
     int c = -1;
     if (r < B) {
       RowParams q;
       load_params(P.a, r, q);
-      c = route_rank(q.route);
+      c = route_rank(q);
       RowCtl rc;
       rc.ticket = 0;
       rc.bar = 0;
@@ -774,19 +798,19 @@ __global__ void __launch_bounds__(kOrderThreads) order_kernel(const __grid_const
       rc.pad = 0;
       P.rowctl[r] = rc;
     }
-    for (int j = 0; j < 3; ++j) tot[j] += __syncthreads_count(c == j);
+    for (int j = 0; j < kClasses; ++j) tot[j] += __syncthreads_count(c == j);
   }
-  int start[3] = {0, tot[0], tot[0] + tot[1]};
+  int start[kClasses] = {0, tot[0], tot[0] + tot[1], tot[0] + tot[1] + tot[2]};
   for (int r0 = 0; r0 < B; r0 += kOrderThreads) {
     const int r = r0 + threadIdx.x;
     int c = -1;
     if (r < B) {
       RowParams q;
       load_params(P.a, r, q);
-      c = route_rank(q.route);
+      c = route_rank(q);
     }
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    for (int j = 0; j < 3; ++j) {
+    for (int j = 0; j < kClasses; ++j) {
       const unsigned bal = __ballot_sync(~0u, c == j);
       if (lane == 0) cnt[j][w] = __popc(bal);
       __syncthreads();
@@ -800,6 +824,10 @@ __global__ void __launch_bounds__(kOrderThreads) order_kernel(const __grid_const
       __syncthreads();
     }
   }
+  // the sampler's CTAs (already running under programmatic serialisation) wait for this
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) st_release(&P.ctl[2], 1u);
 }
 
 // ---------------------------------------------------------------- slice load and transforms
@@ -2248,7 +2276,15 @@ template <bool kBF16>
 __device__ void slice_front(const LaunchParams& P, const Smem& S, const RowParams& q, int row, int slice, int c0,
                             int n, uint32_t bulk) {
   RowInfo ri{0, P.a.V, 0, 0};
-  if (P.lists) ri = P.rinfo[row];
+  if (P.lists) {
+    if (threadIdx.x == 0) sh.flag = wait_flag(P.rflag + row, 1u);
+    __syncthreads();
+    if (sh.flag) {
+      const int4 v = __ldcg(reinterpret_cast<const int4*>(P.rinfo + row));
+      ri = RowInfo{v.x, v.y, v.z, v.w};
+    }
+    // (on a timeout the row's slices scan the CSRs themselves: ri.ready stays 0)
+  }
   if (threadIdx.x == 0) {
     sh.rec.flags |= ri.flags;
     sh.nal_row = ri.nal;
@@ -2258,7 +2294,7 @@ __device__ void slice_front(const LaunchParams& P, const Smem& S, const RowParam
     // checked walk of pass A must not sanitise them again) and keep up to two per thread
     // in registers until the logits have landed
     const int* po = P.poff + (size_t)row * (P.C + 1) + slice;
-    const int e0 = po[0], ne = po[1] - e0;
+    const int e0 = __ldcg(po), ne = __ldcg(po + 1) - e0;
     const PenEntry* seg = P.pent + (size_t)row * kPenRowCap + e0;
     const int nw = (n + 31) >> 5;
     for (int w = threadIdx.x; w < nw; w += kThreads) S.claim[w] = 0u;
@@ -2267,7 +2303,10 @@ __device__ void slice_front(const LaunchParams& P, const Smem& S, const RowParam
     for (int u = 0; u < 2; ++u) {
       const int i = threadIdx.x + u * kThreads;
       mine[u].lid = -1;
-      if (i < ne) mine[u] = seg[i];
+      if (i < ne) {
+        const int4 v = __ldcg(reinterpret_cast<const int4*>(seg + i));
+        mine[u] = PenEntry{v.x, (unsigned)v.y, v.z, v.w};
+      }
     }
     if (P.a.bitmask) {
       const int32_t* mrow = P.a.bitmask + (long long)row * P.a.bitmask_row_stride + (c0 >> 5);
@@ -2288,7 +2327,8 @@ __device__ void slice_front(const LaunchParams& P, const Smem& S, const RowParam
           const int i = i0 + threadIdx.x + u * kThreads;
           e.lid = -1;
           if (i < ne) {
-            e = seg[i];
+            const int4 v = __ldcg(reinterpret_cast<const int4*>(seg + i));
+            e = PenEntry{v.x, (unsigned)v.y, v.z, v.w};
             atomicOr(&S.claim[e.lid >> 5], 1u << (e.lid & 31));
           }
         }
@@ -2343,12 +2383,14 @@ __device__ void reprocess_slice(const LaunchParams& P, const Smem& S, const RowP
 
 template <bool kBF16>
 __global__ void __launch_bounds__(kThreads, 3) sampler_kernel(const __grid_constant__ LaunchParams P) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // No griddepcontrol.wait: this grid starts once every CTA of the preparation launch has
+  // started (they trigger at entry), and waits only for the flags that launch sets.
   const Smem S = carve(P.chunk);
   const int C = P.C;
   if (threadIdx.x == 0) {
+    sh.flag = wait_flag(&P.ctl[2], 1u);
     const unsigned item = atomicAdd(&P.ctl[0], 1u);
-    sh.row_id = P.order[item / (unsigned)C];
+    sh.row_id = __ldcg(P.order + item / (unsigned)C);
     sh.slice = (int)(item % (unsigned)C);
     sh.bar_uses = 0;
   }
@@ -2364,7 +2406,7 @@ __global__ void __launch_bounds__(kThreads, 3) sampler_kernel(const __grid_const
     memset(&z, 0, sizeof z);
     z.m = -INFINITY;
     z.arg = INT_MAX;
-    z.flags = sh.rp.invalid;
+    z.flags = sh.rp.invalid | (sh.flag ? 0 : kFlagOverflow);
     z.zc = -INFINITY;
     z.rs = -INFINITY;
     z.rtok = INT_MAX;
@@ -2384,11 +2426,21 @@ __global__ void __launch_bounds__(kThreads, 3) sampler_kernel(const __grid_const
   publish_rec(P, row, slice);
   if (threadIdx.x == 0) sh.last = atomicAdd(&P.rowctl[row].ticket, 1u) == (unsigned)(C - 1);
   __syncthreads();
-  if (!sh.last) return;
-  __threadfence();
-  combine_row(P, row, q);
-  if (heavy) heavy_above(ab, C);
-  finish_row<kBF16>(P, S, q, row, ab, heavy);
+  if (sh.last) {
+    __threadfence();
+    combine_row(P, row, q);
+    if (heavy) heavy_above(ab, C);
+    finish_row<kBF16>(P, S, q, row, ab, heavy);
+  }
+  // the grid's last CTA clears the preparation flags for the next call
+  __syncthreads();
+  if (threadIdx.x == 0) sh.last = atomicAdd(&P.ctl[3], 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (sh.last) {
+    if (P.lists)
+      for (int r = threadIdx.x; r < P.a.B; r += kThreads) P.rflag[r] = 0u;
+    if (threadIdx.x == 0) P.ctl[2] = 0u;
+  }
 }
 
 // ---------------------------------------------------------------- diagnostics
@@ -2429,7 +2481,7 @@ Geometry geometry_for(int vocab) {
 
 // Byte offsets of the scratch arrays for B rows of C slices of `chunk` tokens.
 struct ScratchLayout {
-  size_t ctl, order, rowctl, srec, bins, cand, spill, rinfo, poff, pent, total;
+  size_t ctl, order, rowctl, srec, bins, cand, spill, rinfo, poff, pent, rflag, total;
 };
 
 constexpr size_t take(size_t& off, size_t bytes) {
@@ -2451,6 +2503,7 @@ constexpr ScratchLayout scratch_layout(size_t B, size_t C, size_t chunk, size_t 
   L.rinfo = take(off, B * sizeof(RowInfo));
   L.poff = take(off, B * (C + 1) * sizeof(int));
   L.pent = take(off, B * kPenRowCap * sizeof(PenEntry));
+  L.rflag = take(off, B * sizeof(unsigned));
   L.total = off;
   return L;
 }
@@ -2661,6 +2714,7 @@ int make_params(const Geometry& g, int vocab, int dev, const Scratch& sc, const 
   P->rinfo = reinterpret_cast<RowInfo*>(b + L.rinfo);
   P->poff = reinterpret_cast<int*>(b + L.poff);
   P->pent = reinterpret_cast<PenEntry*>(b + L.pent);
+  P->rflag = reinterpret_cast<unsigned*>(b + L.rflag);
   P->lists = (a->hist_offs || a->bias_offs || a->bitmask) ? 1 : 0;
   return CLSAMPLE_SUCCESS;
 }

@@ -2117,18 +2117,23 @@ __device__ void heavy_slice(const LaunchParams& P, const Smem& S, const RowParam
     // the open-ended last bin (most tokens of a wide row) is summed in registers
     unsigned clast = 0;
     unsigned long long wlast = 0;
-    for (int l = threadIdx.x; l < n; l += kThreads) {
-      const float z = S.buf[l];
-      if (!(z > -INFINITY)) continue;
-      const float y = y_of(z, m, invT);
-      const int b = ybin(y);
-      const unsigned long long w = (wm && y > -28.0f) ? weight_fx(y) : 0ull;  // e^-28 < 2^-40
-      if (b == kYBins - 1) {
-        ++clast;
-        wlast += w;
-      } else {
-        atomicAdd(&B->cnt[b], 1u);
-        if (w) add_mass(&B->lo[b], &B->hi[b], w);
+    const float4* b4 = reinterpret_cast<const float4*>(S.buf);
+    for (int f = threadIdx.x; f < nv; f += kThreads) {
+      const float4 v = b4[f];
+      const float zz[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (!(zz[j] > -INFINITY)) continue;
+        const float y = y_of(zz[j], m, invT);
+        const int b = ybin(y);
+        const unsigned long long w = (wm && y > -28.0f) ? weight_fx(y) : 0ull;  // e^-28 < 2^-40
+        if (b == kYBins - 1) {
+          ++clast;
+          wlast += w;
+        } else {
+          atomicAdd(&B->cnt[b], 1u);
+          if (w) add_mass(&B->lo[b], &B->hi[b], w);
+        }
       }
     }
     clast = (unsigned)warp_sum_i((int)clast);
@@ -2208,33 +2213,90 @@ __device__ void heavy_slice(const LaunchParams& P, const Smem& S, const RowParam
     ab.w = sh.above_w;
     ab.wall = sh.W;
   }
-  // race over the surely-kept tokens (above the band, passing min-p), seeded with the
-  // exact score of the row's argmax token, which every kept set contains
+  // one walk: the surely-kept tokens (above the band, passing min-p) race in place, seeded
+  // with the exact score of the row's argmax token (every kept set contains it), and the
+  // band's tokens are compacted
   const float s0 = race_of(0.0f, R.arg, q.seed, q.pos);
   float bs = s0, by = 0.0f, ymin = INFINITY;
   int bid = R.arg, kept = 0;
   const float L = q.L;
-  race_slice(S, c0, n, m, invT, q, [&](float y) { return ybin(y) < blo && y >= L; }, bs, bid, by, kept, ymin);
+  const bool band = bhi >= blo;
+  Item* cdst = cand_area(P, row, slice);
+  if (threadIdx.x == 0) sh.cnt = 0;
+  __syncthreads();
+  {
+    const float4* b4 = reinterpret_cast<const float4*>(S.buf);
+    const int lane = threadIdx.x & 31;
+    for (int f0 = 0; f0 < nv; f0 += kThreads) {
+      const int f = f0 + threadIdx.x;
+      const float4 v = f < nv ? b4[f] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      const float zz[4] = {v.x, v.y, v.z, v.w};
+      float yy[4];
+      unsigned km = 0, bm = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        yy[j] = -INFINITY;
+        if (zz[j] > -INFINITY) {
+          yy[j] = y_of(zz[j], m, invT);
+          const int b = ybin(yy[j]);
+          if (b < blo) {
+            if (yy[j] >= L) km |= 1u << j;
+          } else if (b <= bhi) {
+            bm |= 1u << j;
+          }
+        }
+      }
+      const int id0 = c0 + 4 * f;
+      if (km) {
+        const uint4 w = race_words((uint32_t)id0 >> 2, q.seed, q.pos);
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (!((km >> j) & 1u)) continue;
+          ++kept;
+          ymin = fminf(ymin, yy[j]);
+          if (fast_race(yy[j], ww[j]) >= bs - kFastTol) {
+            const float sc = race_score(yy[j], ww[j]);
+            if (better(sc, id0 + j, bs, bid)) {
+              bs = sc;
+              bid = id0 + j;
+              by = yy[j];
+            }
+          }
+        }
+      }
+      if (band) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const bool pr = (bm >> j) & 1u;
+          const unsigned bal = __ballot_sync(~0u, pr);
+          if (!bal) continue;
+          int base = 0;
+          if (lane == 0) base = atomicAdd(&sh.cnt, __popc(bal));
+          base = __shfl_sync(~0u, base, 0);
+          const int pos = base + __popc(bal & ((1u << lane) - 1u));
+          if (pr && pos < kCandCap) cdst[pos] = Item{zz[j], id0 + j};
+        }
+      }
+    }
+  }
   block_race(bs, bid, by);
   kept = block_sum_i(kept);
   ymin = block_min_f(ymin);
-  int nc = 0, spilled = 0;
-  if (bhi >= blo) {
+  int nc = sh.cnt, spilled = 0;
+  if (band && nc > kCandCap) {
     auto in_band = [&](float z) {
       const int b = ybin(y_of(z, m, invT));
       return b >= blo && b <= bhi;
     };
-    nc = compact_if(S, c0, n, in_band, cand_area(P, row, slice), kCandCap);
-    if (nc > kCandCap) {
-      if (threadIdx.x == 0) sh.spill = row_spill_slot(P, row);
-      __syncthreads();
-      if (sh.spill >= 0) {
-        nc = compact_if(S, c0, n, in_band, spill_area(P, sh.spill, slice), P.chunk);
-        spilled = 1;
-      } else {
-        nc = 0;
-        if (threadIdx.x == 0) sh.rec.flags |= kFlagOverflow;
-      }
+    if (threadIdx.x == 0) sh.spill = row_spill_slot(P, row);
+    __syncthreads();
+    if (sh.spill >= 0) {
+      nc = compact_if(S, c0, n, in_band, spill_area(P, sh.spill, slice), P.chunk);
+      spilled = 1;
+    } else {
+      nc = 0;
+      if (threadIdx.x == 0) sh.rec.flags |= kFlagOverflow;
     }
   }
   if (threadIdx.x == 0) {

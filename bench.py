@@ -320,9 +320,11 @@ def main():
 
     peak, peak_kind = peaks()
     alg = b.algorithmic_bytes()
-    # the sampler kernel reads every input array (the ordering kernel ahead of it reads
-    # only the per-row parameters, which the sampler reads again)
-    alg_sampler = alg
+    # the sampler kernel reads the logits, the bitmask and the per-row parameters and
+    # writes the outputs; the history and logit_bias CSRs are read by the preparation
+    # launch ahead of it (which hands the sampler a short list per slice instead)
+    hb = b.host_bytes()
+    alg_sampler = alg - sum(hb.get(k, 0) for k in ("hist_offs", "hist_ids", "bias_offs", "bias_ids", "bias_vals"))
     achieved = alg_sampler / (mean_launch_ms / 1e3) / 1e9
     line = {
         "metric": METRIC,
@@ -355,8 +357,10 @@ def main():
             "traffic": traffic_from_profile(b.name),
             "algorithmic_bytes_per_launch": alg_sampler,
             "mean_launch_us": mean_launch_ms * 1e3,
-            "kernel": "sampler_kernel (persistent, one launch per step, after the ordering launch: order_kernel with the row preparation blocks)",
+            "kernel": "sampler_kernel (one CTA per (row, slice), launched with programmatic serialisation after "
+                      "order_kernel, the preparation launch: row order and per-row penalty/bias lists)",
             "order_kernel_us": order_ms * 1e3,
+            "step_algorithmic_gbs": alg / (ms_per_step / 1e3) / 1e9,
         },
         "gpu_launches": 2 * args.steps,
         "clocks": clk,

@@ -133,7 +133,7 @@ class Sampler:
         self.max_batch, self.vocab = int(max_batch), int(vocab)
 
     def resident_ctas(self, bf16: bool = False) -> int:
-        """CTAs of the persistent sampler kernel (``clsample_occupancy``)."""
+        """Resident CTAs of the sampler kernel on this device (``clsample_occupancy``)."""
         n = ctypes.c_int32()
         _check(self._L.clsample_occupancy(self._h, LOGITS_BF16 if bf16 else LOGITS_F32, ctypes.byref(n)))
         return n.value

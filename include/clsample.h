@@ -26,13 +26,14 @@
  *      log-softmax (SGLang page, section "Numerical consistency of logprobs").
  *
  * Threading and ownership.  A handle is bound to the CUDA device that was current at
- * clsample_create and owns device scratch sized for max_batch rows (the rows' order and
- * work list, per-slice records, penalised-token lists, tables of vector maxima and
- * compacted candidates; about 430 KB per row for V = 151936).  Every array in
- * clsample_args_t is a DEVICE pointer owned by the caller; it must stay valid until the
- * work enqueued on the stream has finished.  The logits are read-only (never written in
- * place).  Calls on one handle must be ordered (one stream, or streams joined by
- * events): they share the handle's scratch.  Separate handles are independent.
+ * clsample_create and owns device scratch sized for max_batch rows (row order and
+ * counters, per-slice records, per-row lists of penalised and biased tokens, compacted
+ * candidates, and a spill area of max(16, max_batch / 8) rows; about 456 KB per row for
+ * V = 151936).  Every array in clsample_args_t is a DEVICE pointer owned by the caller;
+ * it must stay valid until the work enqueued on the stream has finished.  The logits are
+ * read-only (never written in place).  Calls on one handle must be ordered (one stream,
+ * or streams joined by events): they share the handle's scratch.  Separate handles are
+ * independent.
  *
  * Errors.  Every entry point validates its arguments on the host, without any device
  * synchronisation, and returns a negative CLSAMPLE_ERR_* code on a bad argument;
@@ -106,10 +107,11 @@ enum {
  * dbg_kept_count    i32[B] output or NULL: size of the kept set K (1 for greedy rows).
  * dbg_cut           f32[B] output or NULL: min over K of y = (z' - max z') * (1/T).
  *
- * Limits: V <= 262144 (at most 8 slices of at most 32768 tokens per row).  Per row, at
- * most 512 distinct penalised or biased ids may fall inside one vocabulary slice of
- * ceil(V / slices) tokens (slices = 8 for V > 14336); a row that exceeds it gets status
- * OVERFLOW.
+ * Limits: V <= 262144 (at most 18 slices of at most 15360 tokens per row).  Any number
+ * of penalised, biased or allowed tokens is handled exactly.  A row whose candidate set
+ * must spill (a slice with more than 2048 candidates: flat or heavily tied rows) uses one
+ * of the handle's spill rows for the call; a row that finds none left gets status
+ * OVERFLOW, as does a row whose bounded waits for other CTAs gave up.
  */
 typedef struct {
   int32_t B, V;
@@ -152,33 +154,37 @@ int clsample_create(int32_t max_batch, int32_t vocab, clsample_t** out);
  * device, so no call on the handle may still be running. */
 void clsample_destroy(clsample_t* handle);
 
-/* Enqueues one sampler call on `stream`: the ordering launch (one CTA orders the rows,
- * heaviest first, and writes the work list; when the call has penalties or logit_bias,
- * one more CTA per row prepares the row's per-slice lists of penalised ids), then the
- * persistent sampler kernel (one CTA per resident slot; every CTA takes (row, slice)
- * items from the list); nothing when B == 0.  Returns after enqueueing; results are
- * valid once the stream reaches this point. */
+/* Enqueues one sampler call on `stream`: the preparation launch (one CTA orders the
+ * rows, heavy rows first, and resets the call's counters; when the call has penalties,
+ * logit_bias or a bitmask, one more CTA per row lists the row's distinct penalised and
+ * biased tokens by vocabulary slice and counts its allowed tokens), then the sampler
+ * kernel (one CTA per (row, slice), launched with programmatic stream serialisation; its
+ * CTAs wait, bounded, only for the flags the preparation launch sets); nothing when
+ * B == 0.  Returns after enqueueing; results are valid once the stream reaches this
+ * point. */
 int clsample_apply(clsample_t* handle, const clsample_args_t* args, clsample_stream_t stream);
 
 /* The two halves of clsample_apply, for callers that schedule or time them apart:
- * clsample_prepare enqueues the ordering launch, clsample_sample the sampler kernel,
- * which reads the work list the last clsample_prepare on this handle wrote (the list
- * may be sampled again with the same arguments).  The pair, with the same arguments on
- * one stream, equals clsample_apply.  Same validation and return codes. */
+ * clsample_prepare enqueues the preparation launch, clsample_sample the sampler kernel,
+ * which consumes what the last clsample_prepare on this handle wrote (each
+ * clsample_sample needs its own clsample_prepare before it: the sampler clears the
+ * preparation's flags when it ends; a sample without one waits about a second and
+ * reports every row OVERFLOW).  The pair, with the same arguments on one stream, equals
+ * clsample_apply.  Same validation and return codes. */
 int clsample_prepare(clsample_t* handle, const clsample_args_t* args, clsample_stream_t stream);
 int clsample_sample(clsample_t* handle, const clsample_args_t* args, clsample_stream_t stream);
 
 /* One sampler call without a handle that allocates nothing.  The pages have no
  * counterpart: this is a deployment convenience of this library, and it samples
  * exactly like clsample_apply.  Its scratch is one fixed device array compiled into
- * the library (about 28 MB, zero when the library loads); no cudaMalloc or cudaFree
+ * the library (about 37 MB, zero when the library loads); no cudaMalloc or cudaFree
  * ever happens.  The first call on a device looks up the array's address on that
  * device (cudaGetSymbolAddress) and sets the kernels' shared-memory limit, once per
  * device, under a host lock.  Limits: B <= 64 (else CLSAMPLE_ERR_BATCH) and
  * V <= 262144 (else CLSAMPLE_ERR_VOCAB); nothing is enqueued on an error.
  * Races: every call on a device, from any host thread or stream, uses the same array,
  * so calls of this entry point on one device must be ordered (one stream, or streams
- * joined by events); two overlapping calls corrupt each other's work lists and records.
+ * joined by events); two overlapping calls corrupt each other's row order and records.
  * Calls through handles are unaffected, and each process has its own array. */
 int clsample_apply_static(const clsample_args_t* args, clsample_stream_t stream);
 
@@ -190,9 +196,9 @@ const char* clsample_strerror(int code);
  * CLSAMPLE_ERR_VOCAB. */
 int clsample_geometry(int32_t vocab, int32_t* slices, int32_t* chunk, int32_t* smem_bytes);
 
-/* How many CTAs the persistent sampler kernel of this handle launches: as many as can be
- * resident on the device at once (cudaOccupancyMaxActiveBlocksPerMultiprocessor times
- * the SM count), computed at clsample_create. */
+/* How many sampler-kernel CTAs of this handle can be resident on the device at once
+ * (cudaOccupancyMaxActiveBlocksPerMultiprocessor times the SM count), computed at
+ * clsample_create; the kernel launches one CTA per (row, slice). */
 int clsample_occupancy(clsample_t* handle, int32_t logits_dtype, int32_t* resident_ctas);
 
 /* Diagnostics of the building blocks, on device arrays of length n (enqueued on

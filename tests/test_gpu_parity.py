@@ -270,3 +270,57 @@ def test_routes_and_fallbacks():
               min_ps=np.array([c[3] for c in params], F32), seeds=np.arange(B, dtype=np.uint64) + 5,
               positions=np.arange(B, dtype=np.int64) * 11)
     compare(b, run_gpu(b), run_oracle(b), name="routes")
+
+
+# ----------------------------------------------------------------------------- fallbacks of the candidate scheme
+
+def test_topk_concentrated_in_one_slice_is_redone():
+    """Light top-k rows take about 1.2 k times a slice's share of the row from each slice;
+    when the row's top tokens all sit in one slice that bound fails the row end's exact
+    check, the slice is redone in full and the result stays exact."""
+    V = 151936
+    rng = np.random.default_rng(31)
+    z = rng.standard_normal((4, V)).astype(F32)
+    z[:, 2000:3500] += 12.0  # the 1500 largest logits of every row lie in the first slice
+    b = small(z, temperatures=np.array([1.0, 0.7, 1.3, 0.9], F32), top_ks=np.array([1000, 700, 900, 1024], np.int32),
+              top_ps=np.array([1.0, 0.9, 0.95, 0.8], F32), min_ps=np.array([0.0, 0.0, 0.05, 0.0], F32),
+              positions=np.arange(4, dtype=np.int64))
+    compare(b, run_gpu(b), run_oracle(b), name="concentrated top-k")
+
+
+def test_history_beyond_the_preparation_hash():
+    """A history with more distinct ids than the preparation launch's per-row hash holds:
+    that row's slices scan the CSRs themselves, with the same result."""
+    V = 151936
+    rng = np.random.default_rng(32)
+    z = (rng.standard_normal((2, V)) * 3).astype(F32)
+    hist0 = rng.permutation(V)[:6000].astype(np.int32)  # 6000 distinct ids
+    hist1 = rng.integers(0, V, 50).astype(np.int32)
+    b = small(z, hist_offs=np.array([0, 6000, 6050], np.int32), hist_ids=np.concatenate([hist0, hist1]),
+              freq=np.full(2, 0.3, F32), pres=np.full(2, 0.1, F32), rep=np.full(2, 1.1, F32),
+              temperatures=np.array([0.9, 0.0], F32), top_ks=np.array([50, -1], np.int32),
+              top_ps=np.array([0.9, 1.0], F32), positions=np.arange(2, dtype=np.int64))
+    compare(b, run_gpu(b), run_oracle(b), name="long history")
+
+
+def test_spill_pool_exhaustion_reports_overflow():
+    """Flat rows under top-k put every token of every slice into the row's candidates,
+    which spill; once the handle's spill rows are used up the remaining such rows report
+    OVERFLOW (token -1 is not required: the status says the result is not to be used) and
+    every other row still matches the oracle."""
+    from constrained_logits_sampling_gb300.sampler import Sampler
+    V = 151936
+    B = 24
+    rng = np.random.default_rng(33)
+    z = (rng.standard_normal((B, V)) * 3).astype(F32)
+    z[:20] = 0.0  # 20 flat rows, more than the 16 spill rows of a small handle
+    b = small(z, temperatures=np.ones(B, F32), top_ks=np.full(B, 50, np.int32),
+              positions=np.arange(B, dtype=np.int64))
+    g = run_gpu(b, sampler=Sampler(B, V))
+    o = run_oracle(b)
+    st = g["status"]
+    assert set(np.unique(st[:20])) <= {0, 1} and (st[:20] == 1).sum() >= 1
+    assert np.all(st[20:] == 0)
+    ok = st == 0
+    assert np.array_equal(g["tokens"][ok], o["tokens"][ok])
+    assert np.array_equal(g["kept_count"][ok], o["kept_count"][ok])

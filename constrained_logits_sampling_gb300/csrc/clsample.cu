@@ -1617,6 +1617,9 @@ __device__ void block_race(float& s, int& id, float& y) {
 // Philox layout produces; a token pays for the exact score only if its fast score is
 // within kFastTol of the best exact score so far.
 constexpr float kFastTol = 1e-3f;
+// Largest race bonus -ln(-ln U) over the uniforms Philox words give: U <= 1 - 2^-24,
+// so -ln U >= 5.96e-8 and the bonus is at most 16.636.
+constexpr float kGumbelMax = 16.7f;
 __device__ __forceinline__ float fast_race(float y, uint32_t x) {
   const float u = word_to_uniform(x);
   const float d = 1.0f - u;
@@ -2240,7 +2243,12 @@ __device__ void heavy_slice(const LaunchParams& P, const Smem& S, const RowParam
           yy[j] = y_of(zz[j], m, invT);
           const int b = ybin(yy[j]);
           if (b < blo) {
-            if (yy[j] >= L) km |= 1u << j;
+            if (yy[j] >= L) {
+              ++kept;
+              ymin = fminf(ymin, yy[j]);
+              // -ln(-ln U) <= kGumbelMax on the U grid: a token below bs - kGumbelMax cannot win
+              if (yy[j] + kGumbelMax >= bs) km |= 1u << j;
+            }
           } else if (b <= bhi) {
             bm |= 1u << j;
           }
@@ -2253,8 +2261,6 @@ __device__ void heavy_slice(const LaunchParams& P, const Smem& S, const RowParam
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           if (!((km >> j) & 1u)) continue;
-          ++kept;
-          ymin = fminf(ymin, yy[j]);
           if (fast_race(yy[j], ww[j]) >= bs - kFastTol) {
             const float sc = race_score(yy[j], ww[j]);
             if (better(sc, id0 + j, bs, bid)) {

@@ -1123,11 +1123,49 @@ __device__ void pass_a(const LaunchParams& P, const Smem& S, const RowParams& q,
     const int j = v.x == tmax ? 0 : v.y == tmax ? 1 : v.z == tmax ? 2 : 3;
     arg = c0 + 4 * tf + j;
   }
+  // one combine: each warp reduces (max, lowest argmax, allowed count, sum rescaled to
+  // the warp max) with shuffles; thread 0 merges the warps in warp order
   float M = tmax;
-  block_argmax(M, arg);
-  nal = block_sum_i(nal);
-  // the block's sum against M, added in a fixed order
-  const float s = block_sum_f(M > -INFINITY && tmax > -INFINITY ? tsum * ex2_approx((tmax - M) * c) : 0.0f);
+  int am = arg;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const float v2 = __shfl_xor_sync(~0u, M, o);
+    const int i2 = __shfl_xor_sync(~0u, am, o);
+    if (better(v2, i2, M, am)) {
+      M = v2;
+      am = i2;
+    }
+    nal += __shfl_xor_sync(~0u, nal, o);
+  }
+  float ws = (M > -INFINITY && tmax > -INFINITY) ? tsum * ex2_approx((tmax - M) * c) : 0.0f;
+  ws = warp_sum_f(ws);
+  const int w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) {
+    sh.red_f[w] = M;
+    sh.red_i[w] = am;
+    sh.red_u[w] = ((unsigned long long)(unsigned)nal << 32) | __float_as_uint(ws);
+  }
+  __syncthreads();
+  float s = 0.0f;
+  if (threadIdx.x == 0) {
+    float Mb = sh.red_f[0];
+    int ab = sh.red_i[0];
+    for (int i = 1; i < kWarps; ++i)
+      if (better(sh.red_f[i], sh.red_i[i], Mb, ab)) {
+        Mb = sh.red_f[i];
+        ab = sh.red_i[i];
+      }
+    int nb = 0;
+    for (int i = 0; i < kWarps; ++i) {
+      const unsigned long long u = sh.red_u[i];
+      nb += (int)(u >> 32);
+      const float wsi = __uint_as_float((uint32_t)u);
+      if (Mb > -INFINITY && sh.red_f[i] > -INFINITY) s += wsi * ex2_approx((sh.red_f[i] - Mb) * c);
+    }
+    M = Mb;
+    arg = ab;
+    nal = nb;
+  }
   if (threadIdx.x == 0) {
     sh.rec.m = M;
     sh.rec.arg = M > -INFINITY ? arg : INT_MAX;
@@ -2491,20 +2529,28 @@ __global__ void __launch_bounds__(kThreads, 3) sampler_kernel(const __grid_const
   const bool heavy = q.route == kRouteHeavy;
   if (heavy) heavy_slice(P, S, q, row, slice, c0, n, ab);
   else if (q.route != kRouteGreedy) light_candidates(P, S, q, row, slice, c0, n);
-  publish_rec(P, row, slice);
-  if (threadIdx.x == 0) sh.last = atomicAdd(&P.rowctl[row].ticket, 1u) == (unsigned)(C - 1);
+  // publish the slice record (the barrier orders every thread's candidate writes before
+  // thread 0's cumulative fence) and take the row's ticket; a CTA that does not finish
+  // the row also counts itself done here
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    P.srec[(size_t)row * P.C + slice] = sh.rec;
+    __threadfence();
+    sh.last = atomicAdd(&P.rowctl[row].ticket, 1u) == (unsigned)(C - 1);
+    sh.flag = sh.last ? 0 : (atomicAdd(&P.ctl[3], 1u) == gridDim.x - 1);
+  }
   __syncthreads();
   if (sh.last) {
     __threadfence();
     combine_row(P, row, q);
     if (heavy) heavy_above(ab, C);
     finish_row<kBF16>(P, S, q, row, ab, heavy);
+    // the grid's last CTA clears the preparation flags for the next call
+    __syncthreads();
+    if (threadIdx.x == 0) sh.flag = atomicAdd(&P.ctl[3], 1u) == gridDim.x - 1;
+    __syncthreads();
   }
-  // the grid's last CTA clears the preparation flags for the next call
-  __syncthreads();
-  if (threadIdx.x == 0) sh.last = atomicAdd(&P.ctl[3], 1u) == gridDim.x - 1;
-  __syncthreads();
-  if (sh.last) {
+  if (sh.flag) {
     if (P.lists)
       for (int r = threadIdx.x; r < P.a.B; r += kThreads) P.rflag[r] = 0u;
     if (threadIdx.x == 0) P.ctl[2] = 0u;

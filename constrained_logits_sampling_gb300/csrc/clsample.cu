@@ -1,21 +1,33 @@
 // Batched constrained logits sampler for GB300 (sm_103a).
 //
-// A row's V logits are split into C slices of `chunk` tokens (a multiple of 128).  The
-// sampler kernel runs one CTA per (row, slice) item; a CTA takes its item from a global
-// counter (so items are taken in list order whatever order the hardware starts CTAs in),
-// copies the slice into shared memory with one TMA bulk copy and keeps it there:
+// A row's V logits are split into C slices of `chunk` tokens (a multiple of 128).  Two
+// launches per call:
 //
-//   transforms  the row's history and logit_bias ids that fall in the slice are marked in
-//               a bitmap, ranked, counted and applied in place (penalties, then bias);
+//   order_kernel    the preparation launch.  CTA 0 orders the rows (heavy rows first,
+//                   greedy last), resets the call's counters and sets "order ready";
+//                   CTAs 1..B each list one row's distinct penalised and biased tokens by
+//                   slice (a shared-memory hash of the history ids with their counts and
+//                   each id's last valid bias entry), count its allowed tokens, and set
+//                   the row's flag.
+//   sampler_kernel  one CTA per (row, slice), launched with programmatic serialisation
+//                   (its CTAs start once every preparation CTA has started and wait only
+//                   on those flags).  A CTA takes its item from a global counter (items
+//                   are taken in list order whatever order the hardware starts CTAs in),
+//                   copies the slice into shared memory with one TMA bulk copy and keeps
+//                   it there:
+//
+//   transforms  the slice's listed tokens get penalties, then bias, in place;
 //   pass A      the grammar mask (written back as -inf), the slice's max, lowest argmax
 //               and sum of 2^((z' - max) log2(e) / T);
 //   candidates  light rows (top-k with k <= kKMax, min-p with p = 1) compact a superset
-//               of the tokens their row can keep: the slice's local top-k (a histogram of
-//               distances to the slice max) or everything above the slice's min-p bound,
-//               with a rounding margin, to global scratch.  The CTA that finishes the
-//               row's last slice (a ticket counter) finishes the row alone from the
-//               candidates: exact radix selects for top-k (count) and top-p (exact
-//               fixed-point mass), min-p, and the exponential race.
+//               of the tokens their row can keep to global scratch: for top-k about
+//               1.2 k times the slice's share of the row's allowed tokens, bounded by the
+//               warps' sorted per-thread maxima; for min-p everything above the slice's
+//               bound, with a rounding margin.  The CTA that finishes the row's last slice
+//               (a ticket counter) finishes the row alone: it checks every slice's bound
+//               exactly against the row's k-th largest y (redoing a slice that fails),
+//               sorts the candidates, takes the top-k, top-p (exact fixed-point mass) and
+//               min-p cuts as prefixes, and runs the exponential race.
 //   heavy rows  rows whose kept set may span the whole vocabulary (top-p without a small
 //               top-k, or no truncation) keep their C CTAs together: they are first in the
 //               list, and each CTA waits (bounded) at two row barriers -- after pass A for
@@ -23,13 +35,12 @@
 //               slices race their surely-kept tokens in place and compact only the band
 //               that holds the cut; the last arriver resolves the cut exactly.
 //
-// A CTA only ever waits for CTAs that took earlier items of its own row, which are
-// running, so the list cannot deadlock.  A one-CTA kernel ahead of the sampler orders
-// the rows (heavy first, greedy last) and resets the counters.  The arithmetic that
-// decides integers (kept set, drawn id) is exact and identical on any IEEE machine
-// (sampler_math.cuh).  Page references: "SGLang source teardown (10): Sampling, Grammar
-// and structured output" (SGLang page) and "GLM-5.3 inference (7): output side" (GLM
-// page).
+// A CTA only ever waits for CTAs that took earlier items of its own row (running), or
+// for preparation CTAs (all started before this grid), so no wait can deadlock; every
+// wait is bounded.  The arithmetic that decides integers (kept set, drawn id) is exact
+// and identical on any IEEE machine (sampler_math.cuh).  Page references: "SGLang source
+// teardown (10): Sampling, Grammar and structured output" (SGLang page) and "GLM-5.3
+// inference (7): output side" (GLM page).
 
 #include <cuda_runtime.h>
 
@@ -334,15 +345,6 @@ __device__ void block_argmax(float& v, int& id) {
     }
 }
 
-__device__ float block_sum_f(float v) {
-  v = warp_sum_f(v);
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) sh.red_f[threadIdx.x >> 5] = v;
-  __syncthreads();
-  float r = 0.f;
-  for (int i = 0; i < kWarps; ++i) r += sh.red_f[i];  // fixed order
-  return r;
-}
 __device__ int block_sum_i(int v) {
   v = warp_sum_i(v);
   __syncthreads();
@@ -472,35 +474,6 @@ __device__ void block_sort_desc(unsigned long long* k) {
 #pragma unroll
   for (int e = 0; e < E; ++e) k[t * E + e] = v[e];
   __syncthreads();
-}
-
-// Sorts 32 E keys held by one warp (lane l holds keys [l E, l E + E)) in descending order,
-// bitonic, with shuffles only.
-template <int E>
-__device__ void warp_sort_desc(unsigned long long (&v)[E]) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll 1
-  for (int size = 2; size <= 32 * E; size <<= 1) {
-#pragma unroll 1
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      if (stride >= E) {
-        const int lm = stride / E;
-#pragma unroll
-        for (int e = 0; e < E; ++e)
-          v[e] = bitonic_pick(v[e], __shfl_xor_sync(~0u, v[e], lm), lane * E + e, size, stride);
-      } else {
-        unsigned long long w[E];
-#pragma unroll
-        for (int st = 1; st < E; st <<= 1) {
-          if (st != stride) continue;
-#pragma unroll
-          for (int e = 0; e < E; ++e) w[e] = bitonic_pick(v[e], v[e ^ st], lane * E + e, size, st);
-#pragma unroll
-          for (int e = 0; e < E; ++e) v[e] = w[e];
-        }
-      }
-    }
-  }
 }
 
 // Sorts n <= 2048 keys (padded with zeros to 256 E) descending.
@@ -1245,19 +1218,6 @@ __device__ int compact(const Smem& S, int c0, int n, float zc, Item* dst, int ca
   return compact_if(S, c0, n, [zc](float z) { return z >= zc; }, dst, cap, active);
 }
 
-// compact() that also counts the tokens at or above `hi_edge` (into *hi).
-__device__ int compact_count(const Smem& S, int c0, int n, float zc, float hi_edge, Item* dst, int cap, int* hi) {
-  int c = 0;
-  const int nv = (n + 3) >> 2;
-  const float4* b4 = reinterpret_cast<const float4*>(S.buf);
-  for (int f = threadIdx.x; f < nv; f += kThreads) {
-    const float4 v = b4[f];
-    c += (v.x >= hi_edge) + (v.y >= hi_edge) + (v.z >= hi_edge) + (v.w >= hi_edge);
-  }
-  *hi = block_sum_i(c);
-  return compact(S, c0, n, zc, dst, cap);
-}
-
 // Writes every allowed token of the slice to the row's spill area; returns the count, or
 // -1 (and flags OVERFLOW) if no spill slot is left.
 __device__ int spill_slice(const LaunchParams& P, const Smem& S, int row, int slice, int c0, int n) {
@@ -1273,23 +1233,20 @@ __device__ __forceinline__ float bound_margin(float M, float edge) {
   return (fabsf(M) + fabsf(edge) + 1.0f) * 0x1p-14f;
 }
 
-// Light rows: the slice's candidate superset.  Top-k: the tokens within the first
-// distance bin (1/8 logit below the slice max each) at which k tokens are reached, minus
-// a margin (every token of the row's top-k set, ties in y included, is in some slice's
-// set).  Min-p with p = 1: z' >= M + T ln(min_p) minus a margin (the row max is at least
-// M).  Candidates past kCandCap spill the whole slice.
+// Light rows: the slice's candidates.  Top-k: the tokens at or above a bound taken from
+// the warps' sorted per-thread maxima, aiming at 1.2 k times the slice's share of the
+// row's allowed tokens; whether that holds the row's whole top-k set is checked exactly
+// at the row end (a failing slice is redone in full).  Min-p with p = 1: z' >=
+// M + T ln(min_p) minus a rounding margin (the row max is at least M), a superset by
+// construction.  Candidates past kCandCap spill the whole slice.
 __device__ void light_candidates(const LaunchParams& P, const Smem& S, const RowParams& q, int row, int slice,
                                  int c0, int n) {
   const float M = sh.rec.m;
   float zc = -INFINITY, dz = 0.0f;
   if (M > -INFINITY && q.route == kRouteTopK) {
-    // about 1.5 k times the slice's share of the row's allowed tokens, from a sorted sample
-    // of the slice (the row end checks that every token left out is below the k-th)
     const int nal = sh.rec.nallowed;
     const float share = P.a.bitmask ? (float)nal / (float)max(1, sh.nal_row) : (float)n / (float)P.a.V;
     int nc = -1;
-    // the need-th largest per-thread maximum of pass A has at least `need` tokens at or
-    // above it, so the compaction keeps at least that many
     const int need = (int)ceilf(1.2f * (float)q.k * share) + 4;
     if (need < nal && need <= kThreads) {
       // each warp sorts its 32 per-thread maxima (shuffles only); the smallest over the
@@ -1663,48 +1620,6 @@ __device__ __forceinline__ float fast_race(float y, uint32_t x) {
   const float d = 1.0f - u;
   const float e = d < 0.125f ? d * (1.0f + d * (0.5f + d * (0.33333334f + d * (0.25f + d * 0.2f)))) : -__logf(u);
   return y - __logf(e);
-}
-
-// Race over a slice's tokens in place: tokens l (local ids, aligned groups of four share
-// one Philox call) for which keep(l, y) holds; seeds the race with (s0, arg0).  Also
-// counts the raced tokens and their smallest y.
-template <class Keep>
-__device__ void race_slice(const Smem& S, int c0, int n, float m, float invT, const RowParams& q, Keep&& keep,
-                           float& bs, int& bid, float& by, int& kept, float& ymin) {
-  const int nv = (n + 3) >> 2;
-  const float4* b4 = reinterpret_cast<const float4*>(S.buf);
-  for (int f = threadIdx.x; f < nv; f += kThreads) {
-    const float4 v = b4[f];
-    const float zz[4] = {v.x, v.y, v.z, v.w};
-    float yy[4];
-    unsigned km = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      yy[j] = -INFINITY;
-      if (zz[j] > -INFINITY) {
-        yy[j] = y_of(zz[j], m, invT);
-        if (keep(yy[j])) km |= 1u << j;
-      }
-    }
-    if (!km) continue;
-    const int id0 = c0 + 4 * f;
-    const uint4 w = race_words((uint32_t)id0 >> 2, q.seed, q.pos);
-    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if (!((km >> j) & 1u)) continue;
-      ++kept;
-      ymin = fminf(ymin, yy[j]);
-      if (fast_race(yy[j], ww[j]) >= bs - kFastTol) {
-        const float sc = race_score(yy[j], ww[j]);
-        if (better(sc, id0 + j, bs, bid)) {
-          bs = sc;
-          bid = id0 + j;
-          by = yy[j];
-        }
-      }
-    }
-  }
 }
 
 // ---------------------------------------------------------------- row end: sorted finisher

@@ -324,3 +324,32 @@ def test_spill_pool_exhaustion_reports_overflow():
     ok = st == 0
     assert np.array_equal(g["tokens"][ok], o["tokens"][ok])
     assert np.array_equal(g["kept_count"][ok], o["kept_count"][ok])
+
+
+def test_prepare_then_sample_equals_apply():
+    """clsample_prepare followed by clsample_sample (the split the benchmark times) gives
+    the same outputs as clsample_apply, twice in a row."""
+    from constrained_logits_sampling_gb300.sampler import Sampler, batch_to_device
+    b = make_workload(4, B=16, V=40000)
+    s = Sampler(b.B, b.V)
+    kw = batch_to_device(b, s.device)
+    logits = kw.pop("logits")
+    ref = s(logits, debug=True, **kw)
+    torch.cuda.synchronize()
+    ref = {k: v.cpu().numpy() for k, v in ref.items()}
+    dev = s.device
+    for _ in range(2):
+        out = {"tokens": torch.empty(b.B, dtype=torch.int32, device=dev),
+               "logprobs": torch.empty(b.B, dtype=torch.float32, device=dev),
+               "status": torch.empty(b.B, dtype=torch.int32, device=dev),
+               "kept_count": torch.empty(b.B, dtype=torch.int32, device=dev),
+               "cut": torch.empty(b.B, dtype=torch.float32, device=dev)}
+        args = s.make_args(logits, tokens=out["tokens"], logprobs=out["logprobs"], row_status=out["status"],
+                           dbg_kept_count=out["kept_count"], dbg_cut=out["cut"], **kw)
+        s.prepare(args)
+        s.sample(args)
+        torch.cuda.synchronize()
+        for k, v in out.items():
+            g = v.cpu().numpy()
+            assert np.array_equal(g.view(np.uint32) if g.dtype == np.float32 else g,
+                                  ref[k].view(np.uint32) if ref[k].dtype == np.float32 else ref[k]), k

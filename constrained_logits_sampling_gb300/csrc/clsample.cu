@@ -250,6 +250,9 @@ struct Shared {
   unsigned long long bar;  // the slice copy's mbarrier
   unsigned bar_uses;       // its completed phases
   uint32_t bulk;           // bytes of the slice copy in flight (issued at entry)
+  RowInfo ri;              // the row's preparation facts (valid when ri_ok)
+  int ri_ok, e0, ne;       // ... and this slice's entry range
+  int ri_slice;            // the slice they were loaded for
   float red_f[kWarps * 2];
   int red_i[kWarps * 2];
   unsigned long long red_u[kWarps];
@@ -2296,15 +2299,32 @@ __device__ void heavy_above(Above& ab, int C) {
 template <bool kBF16>
 __device__ void slice_front(const LaunchParams& P, const Smem& S, const RowParams& q, int row, int slice, int c0,
                             int n, uint32_t bulk) {
+  // the row's preparation facts, loaded at entry (a redone slice of a row end loads its
+  // own; on a timeout the slices scan the CSRs themselves: ready stays 0)
   RowInfo ri{0, P.a.V, 0, 0};
+  int e0 = 0, ne = 0;
   if (P.lists) {
-    if (threadIdx.x == 0) sh.flag = wait_flag(P.rflag + row, 1u);
-    __syncthreads();
-    if (sh.flag) {
-      const int4 v = __ldcg(reinterpret_cast<const int4*>(P.rinfo + row));
-      ri = RowInfo{v.x, v.y, v.z, v.w};
+    if (slice != sh.ri_slice) {
+      if (threadIdx.x == 0) {
+        sh.ri_ok = 0;
+        sh.ri_slice = slice;
+        if (wait_flag(P.rflag + row, 1u)) {
+          const int4 v = __ldcg(reinterpret_cast<const int4*>(P.rinfo + row));
+          const int* po = P.poff + (size_t)row * (P.C + 1) + slice;
+          const int a0 = __ldcg(po), a1 = __ldcg(po + 1);
+          sh.ri = RowInfo{v.x, v.y, v.z, v.w};
+          sh.e0 = a0;
+          sh.ne = a1 - a0;
+          sh.ri_ok = 1;
+        }
+      }
+      __syncthreads();
     }
-    // (on a timeout the row's slices scan the CSRs themselves: ri.ready stays 0)
+    if (sh.ri_ok) {
+      ri = sh.ri;
+      e0 = sh.e0;
+      ne = sh.ne;
+    }
   }
   if (threadIdx.x == 0) {
     sh.rec.flags |= ri.flags;
@@ -2314,8 +2334,6 @@ __device__ void slice_front(const LaunchParams& P, const Smem& S, const RowParam
     // the row's entries of this slice, listed by the preparation launch: mark them (the
     // checked walk of pass A must not sanitise them again) and keep up to two per thread
     // in registers until the logits have landed
-    const int* po = P.poff + (size_t)row * (P.C + 1) + slice;
-    const int e0 = __ldcg(po), ne = __ldcg(po + 1) - e0;
     const PenEntry* seg = P.pent + (size_t)row * kPenRowCap + e0;
     const int nw = (n + 31) >> 5;
     for (int w = threadIdx.x; w < nw; w += kThreads) S.claim[w] = 0u;
@@ -2420,6 +2438,21 @@ __global__ void __launch_bounds__(kThreads, 3) sampler_kernel(const __grid_const
     // the slice copy starts before anything else is read
     const int c0 = sh.slice * P.chunk;
     sh.bulk = slice_load<kBF16>(P, S, sh.row_id, c0, min(P.a.V - c0, P.chunk));
+  }
+  if (threadIdx.x == 32) {
+    // in parallel with the parameter loads: the row's preparation flag, then its facts
+    // and this slice's entry range
+    sh.ri_ok = 0;
+    sh.ri_slice = sh.slice;
+    if (P.lists && wait_flag(P.rflag + sh.row_id, 1u)) {
+      const int4 v = __ldcg(reinterpret_cast<const int4*>(P.rinfo + sh.row_id));
+      const int* po = P.poff + (size_t)sh.row_id * (P.C + 1) + sh.slice;
+      const int a0 = __ldcg(po), a1 = __ldcg(po + 1);
+      sh.ri = RowInfo{v.x, v.y, v.z, v.w};
+      sh.e0 = a0;
+      sh.ne = a1 - a0;
+      sh.ri_ok = 1;
+    }
   }
   if (threadIdx.x == 0) {
     load_params(P.a, sh.row_id, sh.rp);

@@ -33,7 +33,7 @@ N_SETS = 3
 FALLBACK_HBM_GBS = 6800.0
 
 
-def parse():
+def parse(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=1000)
@@ -42,7 +42,7 @@ def parse():
     p.add_argument("--workload", type=int, default=WORKLOAD)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
-    return p.parse_args()
+    return p.parse_args(argv)
 
 
 def dist_env():
@@ -188,6 +188,23 @@ def run_reference(args, rank, world):
     return 0
 
 
+def max_over_ranks(values, dist=None, device=None):
+    """Element-wise max of a list of floats over the ranks (the timing rule: the slowest
+    rank's time counts); the list unchanged on one process."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def rows_per_second(rows_per_rank, world, steps, total_ms):
+    """Whole-job throughput: every rank processes rows_per_rank rows per step (weak
+    scaling), over the slowest rank's time for `steps` steps."""
+    return rows_per_rank * world * steps / (total_ms / 1e3)
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
@@ -265,12 +282,9 @@ def main():
     barrier()
     order_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / n_split
     mean_launch_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / n_split  # the sampler kernel
-    if dist is not None:
-        t = torch.tensor([total_ms, mean_launch_ms, order_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, mean_launch_ms, order_ms = float(t[0]), float(t[1]), float(t[2])
+    total_ms, mean_launch_ms, order_ms = max_over_ranks([total_ms, mean_launch_ms, order_ms], dist, dev)
     ms_per_step = total_ms / args.steps
-    value = b.B * world * args.steps / (total_ms / 1e3)
+    value = rows_per_second(b.B, world, args.steps, total_ms)
 
     # ---- end to end through the public API: host inputs -> device -> sampler -> host
     e2e = None
@@ -305,12 +319,8 @@ def main():
             e2e_step()
         e1.record(stream)
         barrier()
-        e_ms = e0.elapsed_time(e1)
-        if dist is not None:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t[0])
-        e2e = {"value": b.B * world * e2e_steps / (e_ms / 1e3), "unit": "rows/s",
+        e_ms = max_over_ranks([e0.elapsed_time(e1)], dist, dev)[0]
+        e2e = {"value": rows_per_second(b.B, world, e2e_steps, e_ms), "unit": "rows/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e2e_steps}
 
     if rank != 0:

@@ -1496,7 +1496,8 @@ __device__ __forceinline__ int digit_width(int r) { return r == 2 ? 10 : 11; }
 __device__ __forceinline__ bool digit_match(uint32_t key, int r, uint32_t prefix) {
   return r == 0 || (key >> (digit_shift(r) + digit_width(r))) == prefix;
 }
-static_assert(kDigitBins == 8 * kThreads, "eight digit bins per thread");
+constexpr int kBPT = kDigitBins / kThreads;  // digit bins per thread
+static_assert(kDigitBins % kThreads == 0, "whole digit bins per thread");
 
 // Key of the krem-th largest y among the items (every item counted, ties by key).
 __device__ uint32_t select_kth(const Smem& S, int chunk, float m, float invT, int krem) {
@@ -1513,13 +1514,13 @@ __device__ uint32_t select_kth(const Smem& S, int chunk, float m, float invT, in
     });
     __syncthreads();
     int c = 0;
-    for (int d = 8 * (int)threadIdx.x; d < 8 * (int)threadIdx.x + 8; ++d) c += (int)hc[d];
+    for (int d = kBPT * (int)threadIdx.x; d < kBPT * (int)threadIdx.x + kBPT; ++d) c += (int)hc[d];
     int tot = 0;
     const int pre = block_scan_i(c, &tot);
     const int above = tot - pre - c;  // items in the digits above this thread's eight
     if (above < krem && above + c >= krem) {
       int run = above;
-      for (int d = 8 * (int)threadIdx.x + 7; d >= 8 * (int)threadIdx.x; --d) {
+      for (int d = kBPT * (int)threadIdx.x + kBPT - 1; d >= kBPT * (int)threadIdx.x; --d) {
         if (run + (int)hc[d] >= krem) {
           sh.digit = d;
           sh.cnt = run;
@@ -1565,13 +1566,13 @@ __device__ uint32_t select_mass(const Smem& S, int chunk, float m, float invT, u
     });
     __syncthreads();
     unsigned long long c = 0;
-    for (int d = 8 * (int)threadIdx.x; d < 8 * (int)threadIdx.x + 8; ++d) c += get_mass(&hlo[d], &hhi[d]);
+    for (int d = kBPT * (int)threadIdx.x; d < kBPT * (int)threadIdx.x + kBPT; ++d) c += get_mass(&hlo[d], &hhi[d]);
     unsigned long long tot = 0;
     const unsigned long long pre = block_scan_u64(c, &tot);
     const unsigned long long above = A + (tot - pre - c);
     unsigned long long run = above;
     int best = -1;
-    for (int d = 8 * (int)threadIdx.x + 7; d >= 8 * (int)threadIdx.x; --d) {
+    for (int d = kBPT * (int)threadIdx.x + kBPT - 1; d >= kBPT * (int)threadIdx.x; --d) {
       if (hc[d] > 0u && run < thr) best = d;
       run += get_mass(&hlo[d], &hhi[d]);
     }
@@ -1579,9 +1580,9 @@ __device__ uint32_t select_mass(const Smem& S, int chunk, float m, float invT, u
     __syncthreads();
     const int ds = sh.digit;
     if (ds == INT_MAX) return tk;  // no key qualifies (cannot happen while A < thr)
-    if (ds >= 8 * (int)threadIdx.x && ds < 8 * (int)threadIdx.x + 8) {
+    if (ds >= kBPT * (int)threadIdx.x && ds < kBPT * (int)threadIdx.x + kBPT) {
       unsigned long long cum = above;
-      for (int d = 8 * (int)threadIdx.x + 7; d > ds; --d) cum += get_mass(&hlo[d], &hhi[d]);
+      for (int d = kBPT * (int)threadIdx.x + kBPT - 1; d > ds; --d) cum += get_mass(&hlo[d], &hhi[d]);
       sh.digit_above = cum;
     }
     __syncthreads();
@@ -1798,13 +1799,13 @@ __device__ bool prefilter_kth(const Smem& S, int chunk, float m, float invT, int
     });
     __syncthreads();
     int c = 0;
-    for (int d = 8 * (int)threadIdx.x; d < 8 * (int)threadIdx.x + 8; ++d) c += (int)hc[d];
+    for (int d = kBPT * (int)threadIdx.x; d < kBPT * (int)threadIdx.x + kBPT; ++d) c += (int)hc[d];
     int tot = 0;
     const int pre = block_scan_i(c, &tot);
     const int above = tot - pre - c;
     if (above < krem && above + c >= krem) {
       int run = above;
-      for (int d = 8 * (int)threadIdx.x + 7; d >= 8 * (int)threadIdx.x; --d) {
+      for (int d = kBPT * (int)threadIdx.x + kBPT - 1; d >= kBPT * (int)threadIdx.x; --d) {
         if (run + (int)hc[d] >= krem) {
           sh.digit = d;
           sh.cnt = run;

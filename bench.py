@@ -302,21 +302,50 @@ def main():
         d2h = sum(v.numel() * v.element_size() for v in out_host.values())
         e2e_steps = max(10, min(args.steps, 50))
 
-        def e2e_step():
-            dkw = {k: (v.to(dev, non_blocking=True) if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
-            lg = dkw.pop("logits")
-            out = s(lg, **dkw)
+        # two buffer sets: the upload of step i + 1 (copy stream) overlaps the sampling of
+        # step i (compute stream); every step still uploads its inputs from pinned host
+        # memory and reads its tokens and logprobs back inside the timed region
+        copy_stream = torch.cuda.Stream(device=dev)
+        bufs = []
+        for _ in range(2):
+            dkw = {k: (torch.empty_like(v, device=dev) if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
+            bufs.append({"kw": dkw, "uploaded": torch.cuda.Event(), "consumed": torch.cuda.Event()})
+        for bset in bufs:
+            bset["consumed"].record(stream)
+
+        def upload(i):
+            bset = bufs[i % 2]
+            with torch.cuda.stream(copy_stream):
+                copy_stream.wait_event(bset["consumed"])
+                for k, v in host.items():
+                    if isinstance(v, torch.Tensor):
+                        bset["kw"][k].copy_(v, non_blocking=True)
+                bset["uploaded"].record(copy_stream)
+
+        def sample_step(i):
+            bset = bufs[i % 2]
+            stream.wait_event(bset["uploaded"])
+            kw_i = dict(bset["kw"])
+            lg = kw_i.pop("logits")
+            out = s(lg, **kw_i)
+            bset["consumed"].record(stream)
             out_host["tokens"].copy_(out["tokens"], non_blocking=True)
             out_host["logprobs"].copy_(out["logprobs"], non_blocking=True)
 
-        for _ in range(3):
-            e2e_step()
+        def e2e_run(nsteps):
+            upload(0)
+            for i in range(nsteps):
+                if i + 1 < nsteps:
+                    upload(i + 1)
+                sample_step(i)
+
+        e2e_run(3)
         barrier()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
+        copy_stream.wait_event(e0)
+        e2e_run(e2e_steps)
         e1.record(stream)
         barrier()
         e_ms = max_over_ranks([e0.elapsed_time(e1)], dist, dev)[0]

@@ -554,6 +554,7 @@ __device__ __forceinline__ int route_rank(const RowParams& q) {
 // ---------------------------------------------------------------- ordering kernel
 
 constexpr int kOrderThreads = 512;
+constexpr int kClassCache = 4096;  // rows whose class the ordering CTA keeps in shared memory
 
 constexpr size_t kPrepSmem = (size_t)kHashSlots * 14;  // keys, counts, bias entries, slot list
 
@@ -746,18 +747,25 @@ __device__ void prep_row_lists(const LaunchParams& P, int row) {
 // One CTA: classifies the rows, writes the list order (stable within a class) and resets
 // the call's counters.
 __global__ void __launch_bounds__(kOrderThreads) order_kernel(const __grid_constant__ LaunchParams P) {
+  // Each CTA first clears the flag it will set (a stale one could be left by a
+  // preparation that no sampler consumed), then lets the sampler grid launch: the sampler
+  // starts only after every CTA of this grid has passed this point.
+  if (threadIdx.x == 0) {
+    if (blockIdx.x == 0) P.ctl[2] = 0u;
+    else P.rflag[blockIdx.x - 1] = 0u;
+    __threadfence();
+  }
+  __syncthreads();
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (blockIdx.x > 0) {
     prep_row_lists(P, blockIdx.x - 1);
     return;
   }
   __shared__ int cnt[kClasses][kOrderThreads / 32];
+  __shared__ uint8_t cls_cache[kClassCache];  // classes of the first rows (read once)
   const int B = P.a.B;
-  if (threadIdx.x == 0) {
-    P.ctl[0] = 0;
-    P.ctl[1] = 0;
-    P.ctl[3] = 0;
-  }
+  // (the item counter, spill counter and done counter were reset by the previous sampler
+  // grid's last CTA, or are zero from the allocation)
   // totals per class first, so each class knows where it starts
   int tot[kClasses] = {0, 0, 0, 0};
   for (int r0 = 0; r0 < B; r0 += kOrderThreads) {
@@ -767,6 +775,7 @@ __global__ void __launch_bounds__(kOrderThreads) order_kernel(const __grid_const
       RowParams q;
       load_params(P.a, r, q);
       c = route_rank(q);
+      if (r < kClassCache) cls_cache[r] = (uint8_t)c;
       RowCtl rc;
       rc.ticket = 0;
       rc.bar = 0;
@@ -781,9 +790,13 @@ __global__ void __launch_bounds__(kOrderThreads) order_kernel(const __grid_const
     const int r = r0 + threadIdx.x;
     int c = -1;
     if (r < B) {
-      RowParams q;
-      load_params(P.a, r, q);
-      c = route_rank(q);
+      if (r < kClassCache) {
+        c = cls_cache[r];
+      } else {
+        RowParams q;
+        load_params(P.a, r, q);
+        c = route_rank(q);
+      }
     }
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     for (int j = 0; j < kClasses; ++j) {
@@ -2428,8 +2441,10 @@ __global__ void __launch_bounds__(kThreads, 3) sampler_kernel(const __grid_const
   const Smem S = carve(P.chunk);
   const int C = P.C;
   if (threadIdx.x == 0) {
-    sh.flag = wait_flag(&P.ctl[2], 1u);
+    // the counter is zero before the preparation launch runs, so the item is taken while
+    // the order may still be in the making
     const unsigned item = atomicAdd(&P.ctl[0], 1u);
+    sh.flag = wait_flag(&P.ctl[2], 1u);
     sh.row_id = __ldcg(P.order + item / (unsigned)C);
     sh.slice = (int)(item % (unsigned)C);
     sh.bar_uses = 0;
@@ -2502,7 +2517,12 @@ __global__ void __launch_bounds__(kThreads, 3) sampler_kernel(const __grid_const
   if (sh.flag) {
     if (P.lists)
       for (int r = threadIdx.x; r < P.a.B; r += kThreads) P.rflag[r] = 0u;
-    if (threadIdx.x == 0) P.ctl[2] = 0u;
+    if (threadIdx.x == 0) {
+      P.ctl[0] = 0u;
+      P.ctl[1] = 0u;
+      P.ctl[2] = 0u;
+      P.ctl[3] = 0u;
+    }
   }
 }
 

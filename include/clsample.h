@@ -169,8 +169,9 @@ int clsample_apply(clsample_t* handle, const clsample_args_t* args, clsample_str
  * which consumes what the last clsample_prepare on this handle wrote (each
  * clsample_sample needs its own clsample_prepare before it: the sampler clears the
  * preparation's flags when it ends; a sample without one waits about a second and
- * reports every row OVERFLOW).  The pair, with the same arguments on one stream, equals
- * clsample_apply.  Same validation and return codes. */
+ * reports every row OVERFLOW; a preparation that no sample consumes is harmless, the
+ * next one clears its flags first).  The pair, with the same arguments on one stream,
+ * equals clsample_apply.  Same validation and return codes. */
 int clsample_prepare(clsample_t* handle, const clsample_args_t* args, clsample_stream_t stream);
 int clsample_sample(clsample_t* handle, const clsample_args_t* args, clsample_stream_t stream);
 

@@ -256,14 +256,14 @@ struct Shared {
   float red_f[kWarps * 2];
   int red_i[kWarps * 2];
   unsigned long long red_u[kWarps];
-  int row_id, slice, c0, n, nv;
+  int row_id, slice;
   int ntouch, flag, cnt, last, spill;
   int nhist;    // history ids of the slice (cached in hlist while at most kHList)
   int nal_row;  // light top-k rows with a mask: allowed tokens of the whole row (by the mask)
   // heavy rows: the bin plan
   int blo, bhi;
   unsigned above_n;
-  unsigned long long above_w, W, thr;
+  unsigned long long above_w, W;
   float lnS;
   // finisher
   SliceRec recs[kMaxSlices];

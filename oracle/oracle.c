@@ -179,9 +179,11 @@ static float sanitize(float v) {
 }
 
 static void write_row(const cls_oracle_args* a, int r, int status, int token, double lp, int kept,
-                      float cut, float gap, float best) {
+                      float cut, float gap, float best, double lp_orig, double lp_kept) {
   a->tokens[r] = token;
   if (a->logprobs) a->logprobs[r] = lp;
+  if (a->logprobs_orig) a->logprobs_orig[r] = lp_orig;
+  if (a->logprobs_kept) a->logprobs_kept[r] = lp_kept;
   if (a->status) a->status[r] = status;
   if (a->kept_count) a->kept_count[r] = kept;
   if (a->cut) a->cut[r] = cut;
@@ -280,7 +282,7 @@ static void sample_row(const cls_oracle_args* a, int r, row_scratch* s) {
   if (a->transformed) memcpy(a->transformed + (int64_t)r * V, s->z, sizeof(float) * (size_t)V);
 
   if (status != ORACLE_OK) {
-    write_row(a, r, status, -1, -INFINITY, 0, -INFINITY, INFINITY, -INFINITY);
+    write_row(a, r, status, -1, -INFINITY, 0, -INFINITY, INFINITY, -INFINITY, -INFINITY, -INFINITY);
     return;
   }
 
@@ -298,7 +300,7 @@ static void sample_row(const cls_oracle_args* a, int r, row_scratch* s) {
     }
   }
   if (n_cand == 0) {
-    write_row(a, r, ORACLE_INVALID, -1, -INFINITY, 0, -INFINITY, INFINITY, -INFINITY);
+    write_row(a, r, ORACLE_INVALID, -1, -INFINITY, 0, -INFINITY, INFINITY, -INFINITY, -INFINITY, -INFINITY);
     return;
   }
 
@@ -316,8 +318,19 @@ static void sample_row(const cls_oracle_args* a, int r, row_scratch* s) {
     }
   }
   double logS = log(S);
+  /* the original (pre-temperature) distribution: log_softmax of z' at T = 1
+   * (SGLang page, "Numerical consistency of logprobs": logprobs before temperature) */
+  double S1 = 0.0;
+  for (int i = 0; i < V; ++i)
+    if (s->z[i] > -INFINITY) {
+      float d = s->z[i] - m;
+      S1 += exp((double)d);
+    }
+  float d_arg = s->z[arg] - m;
   if (greedy) {
-    write_row(a, r, ORACLE_OK, arg, (double)s->y[arg] - logS, 1, s->y[arg], INFINITY, -INFINITY);
+    /* the kept set of a greedy row is the token alone: its renormalised logprob is 0 */
+    write_row(a, r, ORACLE_OK, arg, (double)s->y[arg] - logS, 1, s->y[arg], INFINITY, -INFINITY,
+              (double)d_arg - log(S1), 0.0);
     return;
   }
 
@@ -380,9 +393,11 @@ static void sample_row(const cls_oracle_args* a, int r, row_scratch* s) {
    *    E_i = -ln U_i, i.e. argmax of y_i - ln E_i; ties go to the lowest id. */
   int kept = 0, tok = -1;
   float best = -INFINITY, second = -INFINITY, cut = INFINITY;
+  double SK = 0.0; /* mass of the kept set, for the renormalised logprob */
   for (int i = 0; i < V; ++i) {
     if (!s->keep[i]) continue;
     ++kept;
+    SK += exp((double)s->y[i]);
     if (s->y[i] < cut) cut = s->y[i];
     float u = cls_oracle_uniform(seed, pos, i);
     float e = -logf(u);
@@ -396,8 +411,11 @@ static void sample_row(const cls_oracle_args* a, int r, row_scratch* s) {
     }
   }
   /* 9. logprob of the drawn token under the full (pre-truncation) distribution at T */
+  /* the distribution the token was drawn from: softmax(y) renormalised over the kept
+   * set (GLM page, "Sampling": the top-k/top-p sampler's processed logprobs) */
+  float d_tok = s->z[tok] - m;
   write_row(a, r, ORACLE_OK, tok, (double)s->y[tok] - logS, kept, cut,
-            kept > 1 ? best - second : INFINITY, best);
+            kept > 1 ? best - second : INFINITY, best, (double)d_tok - log(S1), (double)s->y[tok] - log(SK));
 }
 
 /* ------------------------------------------------------------------ batch driver */

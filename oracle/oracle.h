@@ -50,6 +50,9 @@ typedef struct {
   float* race_gap;                 /* [B] or NULL: best - second race score (+inf if one) */
   float* race_best;                /* [B] or NULL: best race score (-inf if none) */
   int32_t nthreads;                /* 0 = all online cores */
+  double* logprobs_orig;           /* [B] or NULL: ln p(token) under softmax(z'), T = 1 */
+  double* logprobs_kept;           /* [B] or NULL: ln p(token) renormalised over the kept set
+                                      (0 for greedy rows: the kept set is the token alone) */
 } cls_oracle_args;
 
 /* Runs the whole batch.  Returns the number of threads used (>= 1). */

@@ -47,6 +47,7 @@ class _Args(ctypes.Structure):
         ("tokens", ctypes.c_void_p), ("logprobs", ctypes.c_void_p), ("status", ctypes.c_void_p),
         ("transformed", ctypes.c_void_p), ("kept_count", ctypes.c_void_p), ("cut", ctypes.c_void_p),
         ("race_gap", ctypes.c_void_p), ("race_best", ctypes.c_void_p), ("nthreads", ctypes.c_int32),
+        ("logprobs_orig", ctypes.c_void_p), ("logprobs_kept", ctypes.c_void_p),
     ]
 
 
@@ -81,7 +82,8 @@ def _ptr(a: Optional[np.ndarray], dtype) -> Optional[int]:
 
 def sample(batch, nthreads: int = 0, want_transformed: bool = False) -> Dict[str, np.ndarray]:
     """Run the oracle on a ``workloads.Batch`` (or any object with the same
-    fields).  Returns tokens, logprobs (float64), status, kept_count, cut,
+    fields).  Returns tokens, logprobs (float64), logprobs_orig (T = 1),
+    logprobs_kept (renormalised over the kept set), status, kept_count, cut,
     race_gap, race_best, threads and optionally the transformed logits z'."""
     L = lib()
     B, V = int(batch.B), int(batch.V)
@@ -105,6 +107,7 @@ def sample(batch, nthreads: int = 0, want_transformed: bool = False) -> Dict[str
         "status": np.zeros(B, np.int32), "kept_count": np.zeros(B, np.int32),
         "cut": np.zeros(B, np.float32), "race_gap": np.zeros(B, np.float32),
         "race_best": np.zeros(B, np.float32),
+        "logprobs_orig": np.zeros(B, np.float64), "logprobs_kept": np.zeros(B, np.float64),
     }
     if want_transformed:
         out["transformed"] = np.zeros((B, V), np.float32)
@@ -131,6 +134,8 @@ def sample(batch, nthreads: int = 0, want_transformed: bool = False) -> Dict[str
     a.race_best = out["race_best"].ctypes.data
     a.transformed = out["transformed"].ctypes.data if want_transformed else None
     a.nthreads = int(nthreads)
+    a.logprobs_orig = out["logprobs_orig"].ctypes.data
+    a.logprobs_kept = out["logprobs_kept"].ctypes.data
     out["threads"] = L.cls_oracle_sample(ctypes.byref(a))
     return out
 

@@ -367,6 +367,61 @@ def test_logprob_matches_library_log_softmax(oracle):
         assert abs(ref - o["logprobs"][r]) < 1e-5
 
 
+def test_original_logprob_is_log_softmax_at_t1(oracle):
+    """The original logprob (before temperature; SGLang teardown (10), 'Numerical
+    consistency of logprobs') is log_softmax of the transformed logits at T = 1, checked
+    against torch.log_softmax in float64; greedy rows with T < 1e-5 have it equal to the
+    ordinary logprob."""
+    import torch
+    b = make_workload(4, B=24, V=20000)
+    for r in range(24):
+        b.temperatures[r] = (0.0, 1.3, 0.5)[r % 3]
+    o = oracle.sample(b, want_transformed=True)
+    for r in range(24):
+        z = torch.tensor(o["transformed"][r], dtype=torch.float64)
+        ref = torch.log_softmax(z, dim=0)[int(o["tokens"][r])].item()
+        assert abs(ref - o["logprobs_orig"][r]) < 1e-5
+        if b.temperatures[r] == 0.0:
+            assert o["logprobs_orig"][r] == o["logprobs"][r]
+
+
+def test_kept_logprob_brute_force(oracle):
+    """The kept-set logprob (the distribution the token is drawn from; GLM page,
+    'Sampling': processed logprobs) at V=8 equals log(w_tok / sum over the enumerated
+    kept set of w); greedy rows give 0 (the kept set is the token alone)."""
+    rng = np.random.default_rng(6)
+    checked = 0
+    for trial in range(60):
+        V = 8
+        z = (rng.integers(-24, 24, size=V) / 8.0).astype(np.float32)
+        T = float(rng.choice([0.0, 0.5, 1.0, 2.0]))
+        k = int(rng.choice([-1, 1, 2, 3, 5]))
+        p = float(rng.choice([0.5, 0.8, 1.0]))
+        mp = float(rng.choice([0.0, 0.1]))
+        allowed = rng.random(V) < 0.8
+        allowed[int(rng.integers(V))] = True
+        b = batch(z[None].copy(), temperatures=full(1, T, F32), top_ks=full(1, k, np.int32),
+                  top_ps=full(1, p, F32), min_ps=full(1, mp, F32),
+                  bitmask=mask_from_allowed([np.nonzero(allowed)[0]], V), seeds=full(1, 77 + trial, np.uint64),
+                  positions=np.arange(1, dtype=np.int64))
+        o = oracle.sample(b)
+        tok = int(o["tokens"][0])
+        if T < 1e-5 or k in (0, 1):
+            assert o["logprobs_kept"][0] == 0.0
+            continue
+        zm = np.where(allowed, z, -np.inf)
+        m = float(zm.max())
+        y = [(float(zm[i]) - m) / T if allowed[i] else -math.inf for i in range(V)]
+        kept, margin = _brute_force_kept(y, allowed, k, p, mp)
+        if margin < 1e-5:
+            continue
+        assert kept[tok]
+        ref = y[tok] - math.log(sum(math.exp(y[i]) for i in range(V) if kept[i]))
+        assert abs(ref - o["logprobs_kept"][0]) < 1e-6
+        checked += 1
+    assert checked >= 20
+
+
 # ----------------------------------------------------------------------------- batching
 
 def test_batch_composition_independence(oracle):

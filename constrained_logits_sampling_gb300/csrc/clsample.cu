@@ -98,7 +98,10 @@ struct SliceRec {
   float ymin;    // their smallest y
   float ytok;    // y of rtok
   int spilled;   // the items are in the row's spill area (else in the slice's candidates)
-  int pad[2];
+  float s1;      // sum of 2^((z' - m) log2(e)) over allowed tokens (T = 1; when requested)
+  float skept;   // heavy rows: sum of e^y over the slice's surely-kept tokens
+  float ztok;    // heavy rows: z' of rtok
+  int pad[3];
 };
 
 // Per-row control words (reset by the ordering kernel every call).
@@ -254,6 +257,7 @@ struct Shared {
   int ri_ok, e0, ne;       // ... and this slice's entry range
   int ri_slice;            // the slice they were loaded for
   float red_f[kWarps * 2];
+  float red_f2[kWarps];
   int red_i[kWarps * 2];
   unsigned long long red_u[kWarps];
   int row_id, slice;
@@ -264,7 +268,8 @@ struct Shared {
   int blo, bhi;
   unsigned above_n;
   unsigned long long above_w, W;
-  float lnS;
+  float lnS, lnS1;  // ln of the row's normaliser at T, and at T = 1
+  float ztok;       // z' of the drawn token (original logprob)
   // finisher
   SliceRec recs[kMaxSlices];
   const Item* seg[2 * kMaxSlices];
@@ -1038,7 +1043,8 @@ __device__ __forceinline__ uint32_t mask_nibble(const uint32_t* mw, int f) {
 // mask (and the tail past the slice end) into buf as -inf.  Fast walk: finite input is
 // assumed and checked by a running sum; if any value was not finite the slice is redone
 // with per-token sanitising (claimed tokens already hold their final value).
-__device__ void pass_a(const LaunchParams& P, const Smem& S, const RowParams& q, int row, int c0, int n) {
+template <bool kT1>
+__device__ void pass_a_t(const LaunchParams& P, const Smem& S, const RowParams& q, int row, int c0, int n) {
   const int nv = (n + 3) >> 2;
   const uint32_t* mw = P.a.bitmask ? S.mask : nullptr;
   const uint32_t tail = (n & 3) ? ((1u << (n & 3)) - 1u) : 0xFu;
@@ -1050,7 +1056,9 @@ __device__ void pass_a(const LaunchParams& P, const Smem& S, const RowParams& q,
   // one walk: max, first vector reaching it, and the sum of 2^((z' - tmax) c) against a
   // running per-thread max (rescaled when it grows)
   const float c = __fmul_rn(1.4426950408889634f, q.invT);
-  float tmax = -INFINITY, tsum = 0.0f, chk = 0.0f;
+  const float c1 = 1.4426950408889634f;             // T = 1: the original distribution
+  constexpr bool want1 = kT1;  // the second (T = 1) sum only when its logprob is requested
+  float tmax = -INFINITY, tsum = 0.0f, tsum1 = 0.0f, chk = 0.0f;
   int tf = INT_MAX, nal = 0;
   for (int f = threadIdx.x; f < nv; f += kThreads) {
     float4 v = b4[f];
@@ -1068,12 +1076,17 @@ __device__ void pass_a(const LaunchParams& P, const Smem& S, const RowParams& q,
     const float a4 = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
     if (a4 > tmax) {
       tsum *= ex2_approx((tmax - a4) * c);
+      if (want1) tsum1 *= ex2_approx((tmax - a4) * c1);
       tmax = a4;
       tf = f;
     }
-    if (tmax > -INFINITY)
+    if (tmax > -INFINITY) {
       tsum += (ex2_approx((v.x - tmax) * c) + ex2_approx((v.y - tmax) * c)) +
               (ex2_approx((v.z - tmax) * c) + ex2_approx((v.w - tmax) * c));
+      if (want1)
+        tsum1 += (ex2_approx((v.x - tmax) * c1) + ex2_approx((v.y - tmax) * c1)) +
+                 (ex2_approx((v.z - tmax) * c1) + ex2_approx((v.w - tmax) * c1));
+    }
   }
   const int nonfinite = __syncthreads_or(!(fabsf(chk) < INFINITY));
   if (nonfinite) {
@@ -1091,18 +1104,24 @@ __device__ void pass_a(const LaunchParams& P, const Smem& S, const RowParams& q,
     }
     __syncthreads();
     tsum = 0.0f;
+    tsum1 = 0.0f;
     for (int f = threadIdx.x; f < nv; f += kThreads) {
       const float4 v = b4[f];
       nal += (v.x > -INFINITY) + (v.y > -INFINITY) + (v.z > -INFINITY) + (v.w > -INFINITY);
       const float a4 = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
       if (a4 > tmax) {
         tsum *= ex2_approx((tmax - a4) * c);
+        if (want1) tsum1 *= ex2_approx((tmax - a4) * c1);
         tmax = a4;
         tf = f;
       }
-      if (tmax > -INFINITY)
+      if (tmax > -INFINITY) {
         tsum += (ex2_approx((v.x - tmax) * c) + ex2_approx((v.y - tmax) * c)) +
                 (ex2_approx((v.z - tmax) * c) + ex2_approx((v.w - tmax) * c));
+        if (want1)
+          tsum1 += (ex2_approx((v.x - tmax) * c1) + ex2_approx((v.y - tmax) * c1)) +
+                   (ex2_approx((v.z - tmax) * c1) + ex2_approx((v.w - tmax) * c1));
+      }
     }
   }
   S.hist[threadIdx.x] = tmax > -INFINITY ? fkey(tmax) : 0u;  // per-thread maxima for the top-k bound
@@ -1128,14 +1147,17 @@ __device__ void pass_a(const LaunchParams& P, const Smem& S, const RowParams& q,
   }
   float ws = (M > -INFINITY && tmax > -INFINITY) ? tsum * ex2_approx((tmax - M) * c) : 0.0f;
   ws = warp_sum_f(ws);
+  float ws1 = (want1 && M > -INFINITY && tmax > -INFINITY) ? tsum1 * ex2_approx((tmax - M) * c1) : 0.0f;
+  if (want1) ws1 = warp_sum_f(ws1);
   const int w = threadIdx.x >> 5;
   if ((threadIdx.x & 31) == 0) {
     sh.red_f[w] = M;
     sh.red_i[w] = am;
     sh.red_u[w] = ((unsigned long long)(unsigned)nal << 32) | __float_as_uint(ws);
+    sh.red_f2[w] = ws1;
   }
   __syncthreads();
-  float s = 0.0f;
+  float s = 0.0f, s1 = 0.0f;
   if (threadIdx.x == 0) {
     float Mb = sh.red_f[0];
     int ab = sh.red_i[0];
@@ -1149,7 +1171,10 @@ __device__ void pass_a(const LaunchParams& P, const Smem& S, const RowParams& q,
       const unsigned long long u = sh.red_u[i];
       nb += (int)(u >> 32);
       const float wsi = __uint_as_float((uint32_t)u);
-      if (Mb > -INFINITY && sh.red_f[i] > -INFINITY) s += wsi * ex2_approx((sh.red_f[i] - Mb) * c);
+      if (Mb > -INFINITY && sh.red_f[i] > -INFINITY) {
+        s += wsi * ex2_approx((sh.red_f[i] - Mb) * c);
+        s1 += sh.red_f2[i] * ex2_approx((sh.red_f[i] - Mb) * c1);
+      }
     }
     M = Mb;
     arg = ab;
@@ -1159,6 +1184,7 @@ __device__ void pass_a(const LaunchParams& P, const Smem& S, const RowParams& q,
     sh.rec.m = M;
     sh.rec.arg = M > -INFINITY ? arg : INT_MAX;
     sh.rec.s = s;
+    sh.rec.s1 = s1;
     sh.rec.nallowed = nal;
   }
   if (P.a.dbg_transformed) {
@@ -1166,6 +1192,14 @@ __device__ void pass_a(const LaunchParams& P, const Smem& S, const RowParams& q,
     for (int l = threadIdx.x; l < n; l += kThreads) d[l] = S.buf[l];
   }
   __syncthreads();
+}
+
+// Pass A, compiled once without and once with the T = 1 sum, so the common case carries
+// no extra work in its walk.
+__device__ __forceinline__ void pass_a(const LaunchParams& P, const Smem& S, const RowParams& q, int row, int c0,
+                                       int n) {
+  if (P.a.logprobs_orig) pass_a_t<true>(P, S, q, row, c0, n);
+  else pass_a_t<false>(P, S, q, row, c0, n);
 }
 
 // ---------------------------------------------------------------- candidates of light rows
@@ -1374,11 +1408,14 @@ __device__ void combine_row(const LaunchParams& P, int row, const RowParams& q) 
       nal += x.nallowed;
       flags |= x.flags;
     }
-    float S = 0.0f;
+    float S = 0.0f, S1 = 0.0f;
     if (m > -INFINITY) {
       const float c = __fmul_rn(1.4426950408889634f, q.invT);
       for (int s = 0; s < C; ++s)
-        if (sh.recs[s].m > -INFINITY) S += sh.recs[s].s * ex2_approx((sh.recs[s].m - m) * c);
+        if (sh.recs[s].m > -INFINITY) {
+          S += sh.recs[s].s * ex2_approx((sh.recs[s].m - m) * c);
+          S1 += sh.recs[s].s1 * ex2_approx((sh.recs[s].m - m) * 1.4426950408889634f);
+        }
     }
     r.m = m;
     r.arg = arg;
@@ -1387,14 +1424,19 @@ __device__ void combine_row(const LaunchParams& P, int row, const RowParams& q) 
     r.s = S;
     sh.row = r;
     sh.lnS = logf(S);
+    sh.lnS1 = logf(S1);
   }
   __syncthreads();
 }
 
-// Writes a row's outputs.
-__device__ void write_row(const clsample_args_t& a, int row, int status, int tok, float lp, int kept, float cut) {
+// Writes a row's outputs.  lp_orig = z'_tok - m - ln S1 (T = 1); lp_kept = y_tok minus
+// the log of the kept set's mass.
+__device__ void write_row(const clsample_args_t& a, int row, int status, int tok, float lp, int kept, float cut,
+                          float lp_orig = -INFINITY, float lp_kept = -INFINITY) {
   a.tokens[row] = status == kRowInvalid ? -1 : tok;
   if (a.logprobs) a.logprobs[row] = status == kRowInvalid ? -INFINITY : lp;
+  if (a.logprobs_orig) a.logprobs_orig[row] = status == kRowInvalid ? -INFINITY : lp_orig;
+  if (a.logprobs_kept) a.logprobs_kept[row] = status == kRowInvalid ? -INFINITY : lp_kept;
   if (a.row_status) a.row_status[row] = status;
   if (a.dbg_kept_count) a.dbg_kept_count[row] = status == kRowInvalid ? 0 : kept;
   if (a.dbg_cut) a.dbg_cut[row] = status == kRowInvalid ? -INFINITY : cut;
@@ -1639,6 +1681,34 @@ __device__ __forceinline__ float fast_race(float y, uint32_t x) {
   return y - __logf(e);
 }
 
+// z' of token `tok` among the row's items (the global candidate / band segments, which
+// hold z'); the caller knows the token is one of them.  Block-wide.
+__device__ float find_item_z(int tok) {
+  if (threadIdx.x == 0) sh.ztok = NAN;
+  __syncthreads();
+  for (int s = 0; s < sh.nseg; ++s) {
+    const Item* g = sh.seg[s];
+    const int n = sh.segn[s];
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+      const Item x = ldcg_item(g + i);
+      if (x.id == tok) sh.ztok = x.z;
+    }
+  }
+  __syncthreads();
+  return sh.ztok;
+}
+
+// Sum over the block of per-thread floats (fixed order over the warps).
+__device__ float block_sum_f2(float v) {
+  v = warp_sum_f(v);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) sh.red_f2[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float r = 0.0f;
+  for (int i = 0; i < kWarps; ++i) r += sh.red_f2[i];
+  return r;
+}
+
 // ---------------------------------------------------------------- row end: sorted finisher
 
 constexpr int kSortCap = 2048;  // items the sorted finisher takes (its masses fit the histogram area)
@@ -1759,12 +1829,14 @@ __device__ void finish_sorted(const LaunchParams& P, const Smem& S, const RowPar
     for (int i = threadIdx.x; i < np; i += kThreads) c += key_to_float(key_at(i)) >= q.L;
     K = block_sum_i(c);
   }
-  // race over the kept prefix
-  float bs = -INFINITY, by = 0.0f;
+  // race over the kept prefix (and its mass, for the kept-set logprob)
+  float bs = -INFINITY, by = 0.0f, sk = 0.0f;
   int bid = INT_MAX;
+  const bool want_kept = P.a.logprobs_kept != nullptr;
   for (int i = threadIdx.x; i < K; i += kThreads) {
     const float y = key_to_float(key_at(i));
     const int id = sorted_id(k[i]);
+    if (want_kept) sk += ex2_approx(y * 1.4426950408889634f);
     const uint4 wv = race_words((uint32_t)id >> 2, q.seed, q.pos);
     const uint32_t x = pick_word(wv, id & 3);
     if (fast_race(y, x) >= bs - kFastTol) {
@@ -1777,9 +1849,13 @@ __device__ void finish_sorted(const LaunchParams& P, const Smem& S, const RowPar
     }
   }
   block_race(bs, bid, by);
+  if (want_kept) sk = block_sum_f2(sk) + ab.skept;
+  const bool from_above = ab.rtok != INT_MAX && better(ab.rs, ab.rtok, bs, bid);
+  float ztok = 0.0f;
+  if (P.a.logprobs_orig) ztok = from_above ? ab.ztok : (bid == INT_MAX ? R.m : find_item_z(bid));
   if (threadIdx.x == 0) {
     float ymin = K > 0 ? key_to_float(key_at(K - 1)) : INFINITY;
-    if (ab.rtok != INT_MAX && better(ab.rs, ab.rtok, bs, bid)) {
+    if (from_above) {
       bs = ab.rs;
       bid = ab.rtok;
       by = ab.ytok;
@@ -1787,7 +1863,8 @@ __device__ void finish_sorted(const LaunchParams& P, const Smem& S, const RowPar
     ymin = fminf(ymin, ab.ymin);
     int st = status;
     if (bid == INT_MAX) st = kRowOverflow;
-    write_row(P.a, row, st, bid == INT_MAX ? R.arg : bid, by - lnS, K + ab.kept, ymin);
+    write_row(P.a, row, st, bid == INT_MAX ? R.arg : bid, by - lnS, K + ab.kept, ymin,
+              __fsub_rn(ztok, R.m) - sh.lnS1, by - logf(sk));
   }
 }
 
@@ -1879,6 +1956,7 @@ struct Above {
   unsigned long long wall;  // mass of every allowed token (heavy rows without a top-k cut)
   float rs, ytok, ymin;   // best race among the surely-kept ones, its y, smallest kept y
   int rtok, kept;
+  float skept, ztok;      // sum of e^y over the surely-kept ones; z' of rtok
 };
 
 // Finishes a row from its combined record (sh.row, sh.recs) and its items (candidates or
@@ -1894,7 +1972,8 @@ __device__ void finish_row(const LaunchParams& P, const Smem& S, const RowParams
   }
   const float m = R.m, invT = q.invT, lnS = sh.lnS;
   if (q.route == kRouteGreedy) {
-    if (threadIdx.x == 0) write_row(P.a, row, status, R.arg, -lnS, 1, 0.0f);
+    // z' of the argmax is m; a greedy row's kept set is the token alone
+    if (threadIdx.x == 0) write_row(P.a, row, status, R.arg, -lnS, 1, 0.0f, -sh.lnS1, 0.0f);
     return;
   }
   const int C = P.C;
@@ -1989,13 +2068,15 @@ __device__ void finish_row(const LaunchParams& P, const Smem& S, const RowParams
     cut = select_mass(S, P.chunk, m, invT, tk, ab.w, thr);
   }
   // min-p and the race
-  float bs = -INFINITY, by = 0.0f, ymin = INFINITY;
+  float bs = -INFINITY, by = 0.0f, ymin = INFINITY, sk = 0.0f;
   int bid = INT_MAX, kept = 0;
   const float L = q.L;
+  const bool want_kept = P.a.logprobs_kept != nullptr;
   visit(S, m, invT, [&](float y, int id) {
     if (fkey(y) >= cut && y >= L) {
       ++kept;
       ymin = fminf(ymin, y);
+      if (want_kept) sk += ex2_approx(y * 1.4426950408889634f);
       const float sc = race_of(y, id, q.seed, q.pos);
       if (better(sc, id, bs, bid)) {
         bs = sc;
@@ -2007,8 +2088,12 @@ __device__ void finish_row(const LaunchParams& P, const Smem& S, const RowParams
   block_race(bs, bid, by);
   kept = block_sum_i(kept);
   ymin = block_min_f(ymin);
+  if (want_kept) sk = block_sum_f2(sk) + ab.skept;
+  const bool from_above = ab.rtok != INT_MAX && better(ab.rs, ab.rtok, bs, bid);
+  float ztok = 0.0f;
+  if (P.a.logprobs_orig) ztok = from_above ? ab.ztok : (bid == INT_MAX ? R.m : find_item_z(bid));
   if (threadIdx.x == 0) {
-    if (ab.rtok != INT_MAX && better(ab.rs, ab.rtok, bs, bid)) {
+    if (from_above) {
       bs = ab.rs;
       bid = ab.rtok;
       by = ab.ytok;
@@ -2017,7 +2102,8 @@ __device__ void finish_row(const LaunchParams& P, const Smem& S, const RowParams
     ymin = fminf(ymin, ab.ymin);
     int st = status;
     if (bid == INT_MAX) st = kRowOverflow;  // nothing kept: only if a limit was hit
-    write_row(P.a, row, st, bid == INT_MAX ? R.arg : bid, by - lnS, kept, ymin);
+    write_row(P.a, row, st, bid == INT_MAX ? R.arg : bid, by - lnS, kept, ymin,
+              __fsub_rn(ztok, R.m) - sh.lnS1, by - logf(sk));
   }
 }
 
@@ -2058,7 +2144,7 @@ __device__ void heavy_slice(const LaunchParams& P, const Smem& S, const RowParam
   publish_rec(P, row, slice);
   if (!row_barrier(P, row, (unsigned)C) && threadIdx.x == 0) sh.rec.flags |= kFlagOverflow;
   combine_row(P, row, q);
-  ab = Above{0u, 0ull, 0ull, -INFINITY, 0.0f, INFINITY, INT_MAX, 0};
+  ab = Above{0u, 0ull, 0ull, -INFINITY, 0.0f, INFINITY, INT_MAX, 0, 0.0f, 0.0f};
   if (threadIdx.x == 0) {
     sh.rec.ncand = 0;
     sh.rec.spilled = 0;
@@ -2190,10 +2276,11 @@ __device__ void heavy_slice(const LaunchParams& P, const Smem& S, const RowParam
   // with the exact score of the row's argmax token (every kept set contains it), and the
   // band's tokens are compacted
   const float s0 = race_of(0.0f, R.arg, q.seed, q.pos);
-  float bs = s0, by = 0.0f, ymin = INFINITY;
+  float bs = s0, by = 0.0f, ymin = INFINITY, bz = m, skept = 0.0f;
   int bid = R.arg, kept = 0;
   const float L = q.L;
   const bool band = bhi >= blo;
+  const bool want_kept = P.a.logprobs_kept != nullptr;
   Item* cdst = cand_area(P, row, slice);
   if (threadIdx.x == 0) sh.cnt = 0;
   __syncthreads();
@@ -2216,6 +2303,7 @@ __device__ void heavy_slice(const LaunchParams& P, const Smem& S, const RowParam
             if (yy[j] >= L) {
               ++kept;
               ymin = fminf(ymin, yy[j]);
+              if (want_kept) skept += ex2_approx(yy[j] * 1.4426950408889634f);
               // -ln(-ln U) <= kGumbelMax on the U grid: a token below bs - kGumbelMax cannot win
               if (yy[j] + kGumbelMax >= bs) km |= 1u << j;
             }
@@ -2237,6 +2325,7 @@ __device__ void heavy_slice(const LaunchParams& P, const Smem& S, const RowParam
               bs = sc;
               bid = id0 + j;
               by = yy[j];
+              bz = zz[j];
             }
           }
         }
@@ -2256,9 +2345,23 @@ __device__ void heavy_slice(const LaunchParams& P, const Smem& S, const RowParam
       }
     }
   }
-  block_race(bs, bid, by);
+  {
+    // the winner's z' travels with its y (same owner thread)
+    const int mine = bid;
+    const float my_z = bz;
+    block_race(bs, bid, by);
+    if (mine == bid && bid != INT_MAX) sh.ztok = my_z;
+  }
   kept = block_sum_i(kept);
   ymin = block_min_f(ymin);
+  if (want_kept) {
+    skept = warp_sum_f(skept);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) sh.red_f2[threadIdx.x >> 5] = skept;
+    __syncthreads();
+    skept = 0.0f;
+    for (int i = 0; i < kWarps; ++i) skept += sh.red_f2[i];
+  }
   int nc = sh.cnt, spilled = 0;
   if (band && nc > kCandCap) {
     auto in_band = [&](float z) {
@@ -2279,6 +2382,8 @@ __device__ void heavy_slice(const LaunchParams& P, const Smem& S, const RowParam
     sh.rec.rs = bs;
     sh.rec.rtok = bid;
     sh.rec.ytok = by;
+    sh.rec.ztok = bid == R.arg ? m : sh.ztok;
+    sh.rec.skept = skept;
     sh.rec.kept = kept;
     sh.rec.ymin = ymin;
     sh.rec.ncand = nc;
@@ -2294,15 +2399,19 @@ __device__ void heavy_above(Above& ab, int C) {
   ab.ytok = 0.0f;
   ab.kept = 0;
   ab.ymin = INFINITY;
+  ab.skept = 0.0f;
+  ab.ztok = 0.0f;
   for (int s = 0; s < C; ++s) {
     const SliceRec& x = sh.recs[s];
     if (x.rtok != INT_MAX && better(x.rs, x.rtok, ab.rs, ab.rtok)) {
       ab.rs = x.rs;
       ab.rtok = x.rtok;
       ab.ytok = x.ytok;
+      ab.ztok = x.ztok;
     }
     ab.kept += x.kept;
     ab.ymin = fminf(ab.ymin, x.ymin);
+    ab.skept += x.skept;
   }
 }
 
@@ -2489,7 +2598,7 @@ __global__ void __launch_bounds__(kThreads, 3) sampler_kernel(const __grid_const
   const int c0 = slice * P.chunk;
   const int n = min(P.a.V - c0, P.chunk);
   slice_front<kBF16>(P, S, q, row, slice, c0, n, sh.bulk);
-  Above ab{0u, 0ull, 0ull, -INFINITY, 0.0f, INFINITY, INT_MAX, 0};
+  Above ab{0u, 0ull, 0ull, -INFINITY, 0.0f, INFINITY, INT_MAX, 0, 0.0f, 0.0f};
   const bool heavy = q.route == kRouteHeavy;
   if (heavy) heavy_slice(P, S, q, row, slice, c0, n, ab);
   else if (q.route != kRouteGreedy) light_candidates(P, S, q, row, slice, c0, n);

@@ -37,7 +37,7 @@ class Args(ctypes.Structure):
         ("seeds", ctypes.c_void_p), ("positions", ctypes.c_void_p), ("step", ctypes.c_int64),
         ("tokens", ctypes.c_void_p), ("logprobs", ctypes.c_void_p), ("row_status", ctypes.c_void_p),
         ("dbg_transformed", ctypes.c_void_p), ("dbg_kept_count", ctypes.c_void_p),
-        ("dbg_cut", ctypes.c_void_p),
+        ("dbg_cut", ctypes.c_void_p), ("logprobs_orig", ctypes.c_void_p), ("logprobs_kept", ctypes.c_void_p),
     ]
 
 
@@ -153,7 +153,8 @@ class Sampler:
                   min_ps=None, rep=None, freq=None, pres=None, hist_offs=None, hist_ids=None,
                   bias_offs=None, bias_ids=None, bias_vals=None, bitmask=None, seeds=None,
                   positions=None, step: int = 0, tokens=None, logprobs=None, row_status=None,
-                  dbg_transformed=None, dbg_kept_count=None, dbg_cut=None) -> Args:
+                  dbg_transformed=None, dbg_kept_count=None, dbg_cut=None, logprobs_orig=None,
+                  logprobs_kept=None) -> Args:
         if logits.dim() != 2 or logits.stride(1) != 1:
             raise ValueError("logits must be [B, V] with unit column stride")
         if logits.dtype == torch.float32:
@@ -201,6 +202,8 @@ class Sampler:
         a.dbg_transformed = _dptr(dbg_transformed, f32, B * V, "dbg_transformed", dev)
         a.dbg_kept_count = _dptr(dbg_kept_count, i32, B, "dbg_kept_count", dev)
         a.dbg_cut = _dptr(dbg_cut, f32, B, "dbg_cut", dev)
+        a.logprobs_orig = _dptr(logprobs_orig, f32, B, "logprobs_orig", dev)
+        a.logprobs_kept = _dptr(logprobs_kept, f32, B, "logprobs_kept", dev)
         return a
 
     def apply(self, args: Args, stream: Optional[torch.cuda.Stream] = None):
@@ -216,11 +219,13 @@ class Sampler:
         last ``prepare`` on this handle wrote."""
         _check(self._L.clsample_sample(self._h, ctypes.byref(args), _stream_ptr(stream)))
 
-    def __call__(self, logits: torch.Tensor, *, debug: bool = False, stream=None,
+    def __call__(self, logits: torch.Tensor, *, debug: bool = False, variants: bool = False, stream=None,
                  **kw) -> Dict[str, torch.Tensor]:
         """Sample one token per row.  Returns a dict with ``tokens`` (int32),
         ``logprobs`` (float32) and ``status`` (int32); with ``debug`` also
-        ``transformed`` [B, V], ``kept_count`` and ``cut``."""
+        ``transformed`` [B, V], ``kept_count`` and ``cut``; with ``variants`` (or
+        ``debug``) also ``logprobs_orig`` (T = 1) and ``logprobs_kept`` (renormalised
+        over the kept set)."""
         B, V = logits.shape
         dev = self.device
         out = {
@@ -232,9 +237,14 @@ class Sampler:
             out["transformed"] = torch.empty(B, V, dtype=torch.float32, device=dev)
             out["kept_count"] = torch.empty(B, dtype=torch.int32, device=dev)
             out["cut"] = torch.empty(B, dtype=torch.float32, device=dev)
+        if variants or debug:
+            out["logprobs_orig"] = torch.empty(B, dtype=torch.float32, device=dev)
+            out["logprobs_kept"] = torch.empty(B, dtype=torch.float32, device=dev)
         args = self.make_args(logits, tokens=out["tokens"], logprobs=out["logprobs"],
                               row_status=out["status"], dbg_transformed=out.get("transformed"),
-                              dbg_kept_count=out.get("kept_count"), dbg_cut=out.get("cut"), **kw)
+                              dbg_kept_count=out.get("kept_count"), dbg_cut=out.get("cut"),
+                              logprobs_orig=out.get("logprobs_orig"), logprobs_kept=out.get("logprobs_kept"),
+                              **kw)
         self.apply(args, stream)
         return out
 

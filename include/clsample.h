@@ -106,6 +106,14 @@ enum {
  *                   bias and mask), row-major with row stride V.
  * dbg_kept_count    i32[B] output or NULL: size of the kept set K (1 for greedy rows).
  * dbg_cut           f32[B] output or NULL: min over K of y = (z' - max z') * (1/T).
+ * logprobs_orig     f32[B] output or NULL: ln p(token) under softmax(z') at T = 1, the
+ *                   distribution before temperature (SGLang page, "Numerical consistency
+ *                   of logprobs": the original logprobs).  Costs one more exponential
+ *                   per logit when requested.
+ * logprobs_kept     f32[B] output or NULL: ln of the token's probability renormalised
+ *                   over the kept set K, the distribution it was drawn from (GLM page,
+ *                   "Sampling": the top-k/top-p sampler's processed logprobs); 0 for
+ *                   greedy rows (K is the token alone).
  *
  * Limits: V <= 262144 (at most 18 slices of at most 15360 tokens per row).  Any number
  * of penalised, biased or allowed tokens is handled exactly.  A row whose candidate set
@@ -142,6 +150,8 @@ typedef struct {
   float* dbg_transformed;
   int32_t* dbg_kept_count;
   float* dbg_cut;
+  float* logprobs_orig;
+  float* logprobs_kept;
 } clsample_args_t;
 
 /* Creates a handle for batches of up to max_batch rows over a vocabulary of `vocab`

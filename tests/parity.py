@@ -8,7 +8,9 @@ Acceptance bar (element by element):
     within 1e-5 relative (max(1, |best|)) of each other -- "ambiguous" rows, where fp32
     logs on the two machines may order the pair differently; there the GPU token must
     still be a kept token, and such rows must stay under 0.1% of the batch;
-  * logprob of the drawn token: within 1e-5 absolute.
+  * logprob of the drawn token: within 1e-5 absolute; so are the drawn token's logprob
+    under the original (T = 1, untruncated) distribution and under the kept set, where
+    both sides report them.
 """
 import numpy as np
 import torch
@@ -62,5 +64,11 @@ def compare(batch, g, o, name="", max_ambiguous_frac=1e-3):
     assert np.all(np.isneginf(g["logprobs"][inval]))
     lp_err = np.abs(g["logprobs"][ok].astype(np.float64) - o["logprobs"][ok])
     assert (lp_err <= LOGPROB_TOL).all(), (name, "logprob", float(lp_err.max()), np.argmax(lp_err))
+    for key in ("logprobs_orig", "logprobs_kept"):
+        if key in g and key in o:
+            rows = ok & same
+            err = np.abs(g[key][rows].astype(np.float64) - o[key][rows])
+            assert (err <= LOGPROB_TOL).all(), (name, key, float(err.max()), np.nonzero(rows)[0][np.argmax(err)])
+            assert np.all(np.isneginf(g[key][inval])), (name, key, "invalid rows")
     return {"ambiguous": n_amb, "max_logprob_err": float(lp_err.max()) if lp_err.size else 0.0,
             "mismatch_ambiguous": int((amb & ~same).sum())}

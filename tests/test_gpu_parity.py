@@ -353,3 +353,27 @@ def test_prepare_then_sample_equals_apply():
             g = v.cpu().numpy()
             assert np.array_equal(g.view(np.uint32) if g.dtype == np.float32 else g,
                                   ref[k].view(np.uint32) if ref[k].dtype == np.float32 else ref[k]), k
+
+
+@pytest.mark.parametrize("w", [1, 3, 5])
+def test_logprob_variants_on_request(w):
+    """The two logprob variants, requested without the debug outputs, match the oracle;
+    requesting them leaves tokens, logprobs and status bit-identical."""
+    from constrained_logits_sampling_gb300.sampler import Sampler, batch_to_device
+    b = make_workload(w, B=24, V=30011)
+    s = Sampler(b.B, b.V)
+    kw = batch_to_device(b, s.device)
+    logits = kw.pop("logits")
+    plain = {k: v.cpu().numpy() for k, v in s(logits, **kw).items()}
+    var = {k: v.cpu().numpy() for k, v in s(logits, variants=True, **kw).items()}
+    assert "logprobs_orig" not in plain and "logprobs_orig" in var
+    for k in ("tokens", "logprobs", "status"):
+        a, c = plain[k], var[k]
+        assert np.array_equal(a.view(np.uint32) if a.dtype == np.float32 else a,
+                              c.view(np.uint32) if c.dtype == np.float32 else c), k
+    o = run_oracle(b, want_transformed=False)
+    ok = (o["status"] == 0) & (var["tokens"] == o["tokens"])
+    assert ok.sum() >= b.B - 1
+    for k in ("logprobs_orig", "logprobs_kept"):
+        err = np.abs(var[k][ok].astype(np.float64) - o[k][ok])
+        assert (err <= 1e-5).all(), (k, float(err.max()))

@@ -54,6 +54,9 @@ class Batch:
     positions: Optional[np.ndarray] = None  # i64[B]
     step: int = 0
     name: str = ""
+    mode: int = 0  # bit 0: joint top-k/top-p; bit 1: score only (no draw)
+    tid_offs: Optional[np.ndarray] = None  # i32[B+1]: requested token ids per row
+    tid_ids: Optional[np.ndarray] = None  # i32[nnz]
 
     def host_bytes(self) -> Dict[str, int]:
         out = {}
@@ -74,7 +77,7 @@ class Batch:
         """Sub-batch with the given row indices (CSR arrays re-based)."""
         idx = np.asarray(idx, dtype=np.int64)
         nb = Batch(B=len(idx), V=self.V, logits=np.ascontiguousarray(self.logits[idx]),
-                   logits_bf16=self.logits_bf16, step=self.step, name=self.name + "[sub]")
+                   logits_bf16=self.logits_bf16, step=self.step, name=self.name + "[sub]", mode=self.mode)
         for f in ("temperatures", "top_ks", "top_ps", "min_ps", "rep", "freq", "pres",
                   "seeds", "positions"):
             v = getattr(self, f)
@@ -83,7 +86,8 @@ class Batch:
         if self.bitmask is not None:
             nb.bitmask = np.ascontiguousarray(self.bitmask[idx])
         for offs_name, arrs in (("hist_offs", ("hist_ids",)),
-                                ("bias_offs", ("bias_ids", "bias_vals"))):
+                                ("bias_offs", ("bias_ids", "bias_vals")),
+                                ("tid_offs", ("tid_ids",))):
             offs = getattr(self, offs_name)
             if offs is None:
                 continue

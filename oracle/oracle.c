@@ -264,6 +264,23 @@ static void sample_row(const cls_oracle_args* a, int r, row_scratch* s) {
   for (int i = 0; i < V; ++i)
     if (s->has_bias[i]) s->z[i] = s->z[i] + s->bias[i];
 
+  /* requested token ids (logprobs of given tokens): an id outside the vocabulary makes
+   * the row INVALID, like the other id lists */
+  int32_t tlo = 0, thi = 0;
+  if (a->tid_offs) {
+    tlo = a->tid_offs[r];
+    thi = a->tid_offs[r + 1];
+    if (tlo < 0 || thi < tlo) {
+      status = ORACLE_INVALID;
+      thi = tlo = 0;
+    } else {
+      for (int32_t j = tlo; j < thi; ++j)
+        if (a->tid_ids[j] < 0 || a->tid_ids[j] >= V) status = ORACLE_INVALID;
+    }
+  }
+  if (a->tid_logprobs)
+    for (int32_t j = tlo; j < thi; ++j) a->tid_logprobs[j] = -INFINITY;
+
   /* An overflow in steps 2-3 is folded back the same way as step 1 treats its
    * input, except that -inf stays -inf (the token is out). */
   for (int i = 0; i < V; ++i) {
@@ -305,7 +322,7 @@ static void sample_row(const cls_oracle_args* a, int r, row_scratch* s) {
   }
 
   /* 5./6. greedy decision, temperature and the softmax normaliser */
-  int greedy = (T < 1e-5f) || k == 0 || k == 1;
+  int greedy = (T < 1e-5f) || k == 0 || k == 1 || (a->mode & CLS_ORACLE_SCORE_ONLY);
   float Teff = (T >= 1e-5f) ? T : 1.0f;
   float invT = 1.0f / Teff;
   double S = 0.0;
@@ -318,6 +335,13 @@ static void sample_row(const cls_oracle_args* a, int r, row_scratch* s) {
     }
   }
   double logS = log(S);
+  /* logprobs of the requested ids, under the same distribution as the drawn token's:
+   * y_id - ln S (-inf for a masked id) */
+  if (a->tid_logprobs)
+    for (int32_t j = tlo; j < thi; ++j) {
+      int id = a->tid_ids[j];
+      a->tid_logprobs[j] = s->z[id] > -INFINITY ? (double)s->y[id] - logS : -INFINITY;
+    }
   /* the original (pre-temperature) distribution: log_softmax of z' at T = 1
    * (SGLang page, "Numerical consistency of logprobs": logprobs before temperature) */
   double S1 = 0.0;
@@ -347,11 +371,44 @@ static void sample_row(const cls_oracle_args* a, int r, row_scratch* s) {
       if (s->keep[i] && s->y[i] < tk) s->keep[i] = 0;
   }
 
+  /* 7b'. joint mode: top-p over the whole candidate set, intersected with the top-k
+   *      set.  Token i passes iff the mass of the candidates strictly more probable than
+   *      i is below p times the mass of all candidates. */
+  int joint = (a->mode & CLS_ORACLE_JOINT) != 0;
+  if (joint && p < 1.0f) {
+    int n = 0;
+    uint64_t W = 0;
+    for (int i = 0; i < V; ++i) {
+      if (s->z[i] > -INFINITY) {
+        s->order[n].y = s->y[i];
+        s->order[n].id = i;
+        ++n;
+        W += cls_oracle_weight_fx(s->y[i]);
+      }
+    }
+    qsort(s->order, (size_t)n, sizeof(s->order[0]), cmp_yid_desc);
+    uint64_t C = cls_oracle_ceil_scaled(W, p);
+    uint64_t above = 0; /* mass of the candidates strictly above the current level */
+    int j = 0;
+    while (j < n) {
+      int j2 = j;
+      uint64_t level_mass = 0;
+      while (j2 < n && s->order[j2].y == s->order[j].y) {
+        level_mass += cls_oracle_weight_fx(s->order[j2].y);
+        ++j2;
+      }
+      if (!(above < C))
+        for (int t = j; t < j2; ++t) s->keep[s->order[t].id] = 0;
+      above += level_mass;
+      j = j2;
+    }
+  }
+
   /* 7b. top-p on the renormalised top-k set: token i stays iff the mass of the
    *     strictly more probable tokens is below p times the set's mass, so tokens of
    *     equal probability are all in or all out.  Weights are exp32(y) in 2^-40 fixed
    *     point, so the sums are exact and the comparison with ceil(p * W) is exact. */
-  if (p < 1.0f) {
+  if (!joint && p < 1.0f) {
     int n = 0;
     uint64_t W = 0;
     for (int i = 0; i < V; ++i) {

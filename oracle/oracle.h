@@ -53,7 +53,18 @@ typedef struct {
   double* logprobs_orig;           /* [B] or NULL: ln p(token) under softmax(z'), T = 1 */
   double* logprobs_kept;           /* [B] or NULL: ln p(token) renormalised over the kept set
                                       (0 for greedy rows: the kept set is the token alone) */
+  int32_t mode;                    /* bit flags: CLS_ORACLE_JOINT, CLS_ORACLE_SCORE_ONLY */
+  const int32_t* tid_offs;         /* [B+1] or NULL: per-row lists of requested token ids */
+  const int32_t* tid_ids;
+  double* tid_logprobs;            /* [tid_offs[B]] or NULL: ln p(id) at T, pre-truncation */
 } cls_oracle_args;
+
+/* mode bits.  JOINT: top-p is taken over the whole distribution and intersected with the
+ * top-k set (instead of top-p over the renormalised top-k set).  SCORE_ONLY: no draw;
+ * every row takes the greedy route (argmax, its logprob) and only the logprobs of the
+ * requested ids are of interest. */
+#define CLS_ORACLE_JOINT 1
+#define CLS_ORACLE_SCORE_ONLY 2
 
 /* Runs the whole batch.  Returns the number of threads used (>= 1). */
 int cls_oracle_sample(const cls_oracle_args* a);

@@ -48,7 +48,13 @@ class _Args(ctypes.Structure):
         ("transformed", ctypes.c_void_p), ("kept_count", ctypes.c_void_p), ("cut", ctypes.c_void_p),
         ("race_gap", ctypes.c_void_p), ("race_best", ctypes.c_void_p), ("nthreads", ctypes.c_int32),
         ("logprobs_orig", ctypes.c_void_p), ("logprobs_kept", ctypes.c_void_p),
+        ("mode", ctypes.c_int32), ("tid_offs", ctypes.c_void_p), ("tid_ids", ctypes.c_void_p),
+        ("tid_logprobs", ctypes.c_void_p),
     ]
+
+
+JOINT = 1       # top-p over the whole distribution, intersected with top-k
+SCORE_ONLY = 2  # no draw: greedy route for every row; logprobs of requested ids
 
 
 def lib():
@@ -84,7 +90,9 @@ def sample(batch, nthreads: int = 0, want_transformed: bool = False) -> Dict[str
     """Run the oracle on a ``workloads.Batch`` (or any object with the same
     fields).  Returns tokens, logprobs (float64), logprobs_orig (T = 1),
     logprobs_kept (renormalised over the kept set), status, kept_count, cut,
-    race_gap, race_best, threads and optionally the transformed logits z'."""
+    race_gap, race_best, threads, optionally the transformed logits z', and
+    ``tid_logprobs`` when the batch carries requested ids (``tid_offs``,
+    ``tid_ids``).  ``batch.mode`` holds the JOINT / SCORE_ONLY bits."""
     L = lib()
     B, V = int(batch.B), int(batch.V)
     logits = np.ascontiguousarray(batch.logits)
@@ -136,6 +144,12 @@ def sample(batch, nthreads: int = 0, want_transformed: bool = False) -> Dict[str
     a.nthreads = int(nthreads)
     a.logprobs_orig = out["logprobs_orig"].ctypes.data
     a.logprobs_kept = out["logprobs_kept"].ctypes.data
+    a.mode = int(getattr(batch, "mode", 0) or 0)
+    toffs, tids = arr("tid_offs", np.int32), arr("tid_ids", np.int32)
+    if toffs is not None:
+        a.tid_offs, a.tid_ids = toffs.ctypes.data, tids.ctypes.data
+        out["tid_logprobs"] = np.zeros(max(int(toffs[-1]), 0), np.float64)
+        a.tid_logprobs = out["tid_logprobs"].ctypes.data
     out["threads"] = L.cls_oracle_sample(ctypes.byref(a))
     return out
 

@@ -449,3 +449,170 @@ def test_invalid_rows(oracle):
     o = oracle.sample(b)
     assert np.all(o["status"][:7] == 2) and np.all(o["tokens"] == -1)
     assert np.all(np.isneginf(o["logprobs"]))
+
+
+# ----------------------------------------------------------------------------- joint top-k/top-p
+
+def _joint_brute_force(y, allowed, k, p):
+    """Joint order at tiny V by enumeration: the top-k set (strictly-larger counts)
+    intersected with the smallest subset of ALL candidates, closed under 'at least as
+    probable', whose mass reaches p of the whole candidate mass.  Returns (kept, margin)."""
+    V = len(y)
+    cand = [i for i in range(V) if allowed[i]]
+    w = {i: math.exp(y[i]) for i in cand}
+    W = sum(w.values())
+    Sk = {i for i in cand if k < 2 or sum(y[j] > y[i] for j in cand) < k}
+    margin = float("inf")
+    best = set(cand)
+    for n in range(1, len(cand) + 1):
+        for sub in itertools.combinations(cand, n):
+            s = set(sub)
+            if any(y[j] >= y[i] and j not in s for i in s for j in cand):
+                continue
+            mass = sum(w[i] for i in s) / W
+            margin = min(margin, abs(mass - p))
+            if mass >= p and len(s) < len(best):
+                best = s
+    kept = np.zeros(V, bool)
+    for i in best & Sk:
+        kept[i] = True
+    return kept, margin
+
+
+def test_joint_worked_example(oracle):
+    """Probabilities 0.4, 0.3, 0.2, 0.1 at T = 1.  Sequential (SGLang teardown (10), the
+    top-k -> top-p order): top-p runs over the renormalised top-k set; joint
+    (filter_apply_order 'joint'): top-p runs over the whole distribution and the result
+    is intersected with top-k.  Hand-derived: k=2, p=0.5 keeps 1 token sequentially
+    (0.4/0.7 >= 0.5) but 2 jointly (0.4 < 0.5); k=3, p=0.75 keeps 2 sequentially
+    (0.7/0.9 >= 0.75) but 3 jointly (0.7 < 0.75)."""
+    z = np.log(np.array([0.4, 0.3, 0.2, 0.1])).astype(np.float32)
+    for k, p, seq, joint in ((2, 0.5, 1, 2), (3, 0.75, 2, 3), (-1, 0.75, 3, 3), (2, 1.0, 2, 2)):
+        for mode, want in ((0, seq), (1, joint)):
+            b = batch(z[None].copy(), top_ks=full(1, k, np.int32), top_ps=full(1, p, F32), mode=mode,
+                      seeds=full(1, 5, np.uint64))
+            o = oracle.sample(b)
+            assert int(o["kept_count"][0]) == want, (k, p, mode)
+
+
+def test_joint_brute_force_and_nesting(oracle):
+    """Joint kept sets at V=8 match the enumeration above; on a larger workload the
+    sequential kept set is inside the joint one, which is inside the top-k set, and the
+    joint order equals the sequential one without a top-k cut."""
+    rng = np.random.default_rng(12)
+    checked = 0
+    for trial in range(60):
+        V = 8
+        z = (rng.integers(-24, 24, size=V) / 8.0).astype(np.float32)
+        T = float(rng.choice([0.5, 1.0, 2.0]))
+        k = int(rng.choice([-1, 2, 3, 5]))
+        p = float(rng.choice([0.3, 0.5, 0.8]))
+        allowed = rng.random(V) < 0.8
+        allowed[int(rng.integers(V))] = True
+        b = batch(z[None].copy(), temperatures=full(1, T, F32), top_ks=full(1, k, np.int32),
+                  top_ps=full(1, p, F32), bitmask=mask_from_allowed([np.nonzero(allowed)[0]], V),
+                  seeds=full(1, 9 + trial, np.uint64), mode=1)
+        o = oracle.sample(b)
+        zm = np.where(allowed, z, -np.inf)
+        m = float(zm.max())
+        y = [(float(zm[i]) - m) / T if allowed[i] else -math.inf for i in range(V)]
+        kept, margin = _joint_brute_force(y, allowed, k, p)
+        if margin < 1e-5:
+            continue
+        assert int(o["kept_count"][0]) == int(kept.sum()), trial
+        assert kept[int(o["tokens"][0])]
+        checked += 1
+    assert checked >= 30
+    w = make_workload(2, B=48, V=6000)
+    w.min_ps = np.zeros(48, np.float32)
+    seq = oracle.sample(w)
+    w.mode = 1
+    jnt = oracle.sample(w)
+    w.top_ps = np.ones(48, np.float32)
+    topk = oracle.sample(w)
+    ok = seq["status"] == 0
+    assert (seq["kept_count"][ok] <= jnt["kept_count"][ok]).all()
+    assert (jnt["kept_count"][ok] <= topk["kept_count"][ok]).all()
+    assert (seq["kept_count"] < jnt["kept_count"]).any()
+    nok = ok & ((w.top_ks <= 0) | (w.top_ks >= 6000))
+    assert np.array_equal(seq["kept_count"][nok], jnt["kept_count"][nok])
+    assert np.array_equal(seq["tokens"][nok], jnt["tokens"][nok])
+
+
+# ----------------------------------------------------------------------------- requested ids, scoring
+
+def _with_requests(b, per_row, rng):
+    offs, ids = [0], []
+    for r in range(b.B):
+        n = int(rng.integers(0, per_row + 1))
+        ids.extend(int(x) for x in rng.integers(0, b.V, size=n))
+        offs.append(len(ids))
+    b.tid_offs = np.asarray(offs, np.int32)
+    b.tid_ids = np.asarray(ids, np.int32)
+    return b
+
+
+def test_requested_id_logprobs_match_library_log_softmax(oracle):
+    """Logprobs of requested token ids (SGLang teardown (10), the output container's
+    token-ids logprobs) are log_softmax of z'/T at those ids, checked against
+    torch.log_softmax in float64; masked ids give -inf; a requested id equal to the drawn
+    token gives the drawn token's logprob."""
+    import torch
+    rng = np.random.default_rng(21)
+    b = _with_requests(make_workload(3, B=24, V=9000), 6, rng)
+    # every row also asks for its drawn token
+    o0 = oracle.sample(b)
+    offs, ids = [0], []
+    for r in range(b.B):
+        ids.extend(b.tid_ids[b.tid_offs[r]:b.tid_offs[r + 1]].tolist() + [int(o0["tokens"][r])])
+        offs.append(len(ids))
+    b.tid_offs, b.tid_ids = np.asarray(offs, np.int32), np.asarray(ids, np.int32)
+    o = oracle.sample(b, want_transformed=True)
+    assert np.array_equal(o["tokens"], o0["tokens"])
+    n_masked = 0
+    for r in range(b.B):
+        T = float(b.temperatures[r])
+        Teff = T if T >= 1e-5 else 1.0
+        z = torch.tensor(o["transformed"][r], dtype=torch.float64)
+        ref = torch.log_softmax(z / Teff, dim=0)
+        for j in range(b.tid_offs[r], b.tid_offs[r + 1]):
+            i = int(b.tid_ids[j])
+            if math.isinf(ref[i].item()):
+                assert o["tid_logprobs"][j] == -math.inf
+                n_masked += 1
+            else:
+                assert abs(ref[i].item() - o["tid_logprobs"][j]) < 1e-5
+        assert o["tid_logprobs"][b.tid_offs[r + 1] - 1] == o["logprobs"][r]
+    assert n_masked > 0
+
+
+def test_requested_id_out_of_range_invalidates_row(oracle):
+    """A requested id outside the vocabulary makes its row INVALID (like a bad history or
+    bias id); the other rows are untouched."""
+    b = make_workload(1, B=4, V=500)
+    b.tid_offs = np.array([0, 1, 3, 3, 4], np.int32)
+    b.tid_ids = np.array([3, 7, 500, 499], np.int32)
+    o = oracle.sample(b)
+    ref = oracle.sample(make_workload(1, B=4, V=500))
+    assert list(o["status"]) == [0, 2, 0, 0]
+    assert o["tokens"][1] == -1 and np.isneginf(o["tid_logprobs"][1:3]).all()
+    assert np.array_equal(o["tokens"][[0, 2, 3]], ref["tokens"][[0, 2, 3]])
+
+
+def test_score_only_mode(oracle):
+    """Score-only mode (SGLang teardown (10), logprobs-only scoring: same preprocessing, no
+    sampling): every row takes the greedy route whatever its parameters, so the seeds
+    change nothing, the token is the lowest-id argmax of z', and the requested ids get the
+    same logprobs as in sampling mode."""
+    rng = np.random.default_rng(4)
+    b = _with_requests(make_workload(4, B=16, V=7000), 5, rng)
+    samp = oracle.sample(b)
+    b.mode = 2
+    o = oracle.sample(b, want_transformed=True)
+    b.seeds = b.seeds[::-1].copy()
+    o2 = oracle.sample(b)
+    assert np.array_equal(o["tokens"], o2["tokens"])
+    ok = o["status"] == 0
+    assert np.array_equal(o["tokens"][ok], np.argmax(o["transformed"][ok], axis=1))
+    assert (o["kept_count"][ok] == 1).all()
+    assert np.array_equal(o["tid_logprobs"], samp["tid_logprobs"])

@@ -536,12 +536,14 @@ __device__ void load_params(const clsample_args_t& a, int row, RowParams& q) {
     }
   }
   q.invalid = inv ? kFlagInvalid : 0;
-  const bool greedy = (q.T < kGreedyEps) || q.k == 0 || q.k == 1;
+  const bool greedy = (q.T < kGreedyEps) || q.k == 0 || q.k == 1 || (a.mode & CLSAMPLE_MODE_SCORE_ONLY);
+  // joint top-k/top-p needs the whole row's exact mass: the co-resident row-group route
+  const bool joint = (a.mode & CLSAMPLE_MODE_JOINT_TOPK_TOPP) && q.p < 1.0f;
   q.Teff = (q.T >= kGreedyEps) ? q.T : 1.0f;
   q.invT = __fdiv_rn(1.0f, q.Teff);
   q.L = q.mp > 0.0f ? (float)log((double)q.mp) : -INFINITY;
   if (inv || greedy) q.route = kRouteGreedy;
-  else if (q.k >= 2 && q.k <= kKMax) q.route = kRouteTopK;
+  else if (q.k >= 2 && q.k <= kKMax && !joint) q.route = kRouteTopK;
   else if (q.p == 1.0f && q.mp > 0.0f) q.route = kRouteMinP;
   else q.route = kRouteHeavy;
 }
@@ -1808,7 +1810,8 @@ __device__ void finish_sorted(const LaunchParams& P, const Smem& S, const RowPar
     }
     unsigned long long tot = 0;
     unsigned long long run = ab.w + block_scan_u64(tsum, &tot);
-    const unsigned long long W = (heavy && kc == 0) ? ab.wall : ab.w + tot;
+    const bool whole = heavy && (kc == 0 || (P.a.mode & CLSAMPLE_MODE_JOINT_TOPK_TOPP));
+    const unsigned long long W = whole ? ab.wall : ab.w + tot;
     const unsigned long long thr = ceil_scaled(W, q.p);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -1959,6 +1962,36 @@ struct Above {
   float skept, ztok;      // sum of e^y over the surely-kept ones; z' of rtok
 };
 
+// Requested token ids: every slice CTA stores z' of the ids inside its slice in the
+// output slots (written before the slice's ticket, so the row end sees them) and flags
+// the row INVALID if an id or the row's offsets are out of range.
+__device__ __noinline__ void capture_tids(const LaunchParams& P, const Smem& S, int row, int c0, int n) {
+  const int lo = P.a.tid_offs[row], hi = P.a.tid_offs[row + 1];
+  int bad = lo < 0 || hi < lo;
+  if (!bad)
+    for (int j = lo + threadIdx.x; j < hi; j += kThreads) {
+      const int id = __ldg(P.a.tid_ids + j);
+      if (id < 0 || id >= P.a.V) bad = 1;
+      else if (id >= c0 && id < c0 + n) P.a.tid_logprobs[j] = S.buf[id - c0];
+    }
+  if (__syncthreads_or(bad) && threadIdx.x == 0) sh.rec.flags |= kFlagInvalid;
+}
+
+// Row end of the requested ids: z' -> y - ln S in place (-inf for masked ids and for
+// every id of an INVALID row).
+__device__ __noinline__ void finish_tids(const LaunchParams& P, int row, int status, float m, float invT, float lnS) {
+  const int lo = P.a.tid_offs[row], hi = P.a.tid_offs[row + 1];
+  if (lo < 0 || hi < lo) return;  // nothing addressable: the row is INVALID
+  for (int j = lo + threadIdx.x; j < hi; j += kThreads) {
+    float v = -INFINITY;
+    if (status != kRowInvalid) {
+      const float z = __ldcg(P.a.tid_logprobs + j);
+      if (z > -INFINITY) v = y_of(z, m, invT) - lnS;
+    }
+    P.a.tid_logprobs[j] = v;
+  }
+}
+
 // Finishes a row from its combined record (sh.row, sh.recs) and its items (candidates or
 // band), exactly: top-k count select, top-p mass select over the top-k set, min-p, race.
 template <bool kBF16>
@@ -1966,6 +1999,7 @@ __device__ void finish_row(const LaunchParams& P, const Smem& S, const RowParams
                            bool heavy) {
   const SliceRec R = sh.row;
   int status = row_status_of(R);
+  if (P.a.tid_offs) finish_tids(P, row, status, R.m, q.invT, sh.lnS);
   if (status == kRowInvalid) {
     if (threadIdx.x == 0) write_row(P.a, row, kRowInvalid, -1, -INFINITY, 0, -INFINITY);
     return;
@@ -2063,7 +2097,8 @@ __device__ void finish_row(const LaunchParams& P, const Smem& S, const RowParams
       if (fkey(y) >= tk) w += weight_fx(y);
     });
     unsigned long long W = ab.w + block_sum_u64(w);
-    if (heavy && kc == 0) W = ab.wall;  // the kept set's base is the whole row
+    // the base is the whole row without a top-k cut, and in the joint order
+    if (heavy && (kc == 0 || (P.a.mode & CLSAMPLE_MODE_JOINT_TOPK_TOPP))) W = ab.wall;
     const unsigned long long thr = ceil_scaled(W, q.p);
     cut = select_mass(S, P.chunk, m, invT, tk, ab.w, thr);
   }
@@ -2235,8 +2270,10 @@ __device__ void heavy_slice(const LaunchParams& P, const Smem& S, const RowParam
       }
       int lo = bk, hi = bk;
       if (q.p < 1.0f) {
+        // sequential: a lower bound on the top-k set's mass (the bins above its band);
+        // without a top-k cut, and in the joint order, the whole row's mass
         unsigned long long Wlo = 0;
-        const int lim = kc > 0 ? bk : kYBins;
+        const int lim = (kc > 0 && !(P.a.mode & CLSAMPLE_MODE_JOINT_TOPK_TOPP)) ? bk : kYBins;
         for (int b = 0; b < lim; ++b) Wlo += B->mass[b];
         const unsigned long long thr = ceil_scaled(Wlo, q.p);
         int bp = kYBins - 1;
@@ -2249,7 +2286,10 @@ __device__ void heavy_slice(const LaunchParams& P, const Smem& S, const RowParam
           }
         }
         lo = kc > 0 ? min(bp, bk) : bp;
-        hi = kc > 0 ? bk : bp;
+        // sequential: the top-p cut may lie anywhere up to the k-th token's bin.  Joint:
+        // the kept set is the prefix up to the tighter of the two cuts, and every token
+        // above either boundary bin passes both, so one bin decides
+        hi = kc > 0 ? ((P.a.mode & CLSAMPLE_MODE_JOINT_TOPK_TOPP) ? lo : bk) : bp;
       }
       unsigned an = 0;
       unsigned long long aw = 0;
@@ -2598,6 +2638,7 @@ __global__ void __launch_bounds__(kThreads, 3) sampler_kernel(const __grid_const
   const int c0 = slice * P.chunk;
   const int n = min(P.a.V - c0, P.chunk);
   slice_front<kBF16>(P, S, q, row, slice, c0, n, sh.bulk);
+  if (P.a.tid_offs) capture_tids(P, S, row, c0, n);
   Above ab{0u, 0ull, 0ull, -INFINITY, 0.0f, INFINITY, INT_MAX, 0, 0.0f, 0.0f};
   const bool heavy = q.route == kRouteHeavy;
   if (heavy) heavy_slice(P, S, q, row, slice, c0, n, ab);
@@ -2809,6 +2850,7 @@ const char* clsample_strerror(int code) {
     case CLSAMPLE_ERR_DTYPE: return "unknown logits dtype";
     case CLSAMPLE_ERR_CUDA: return "CUDA runtime error";
     case CLSAMPLE_ERR_DEVICE: return "wrong or unsupported CUDA device";
+    case CLSAMPLE_ERR_MODE: return "unknown mode bit";
     default: return "unknown error";
   }
 }
@@ -2878,10 +2920,12 @@ int make_params(const Geometry& g, int vocab, int dev, const Scratch& sc, const 
   if (a->B < 0 || a->B > sc.max_batch) return CLSAMPLE_ERR_BATCH;
   if (a->V != vocab) return CLSAMPLE_ERR_VOCAB;
   if (a->logits_dtype != CLSAMPLE_LOGITS_F32 && a->logits_dtype != CLSAMPLE_LOGITS_BF16) return CLSAMPLE_ERR_DTYPE;
+  if (a->mode & ~(CLSAMPLE_MODE_JOINT_TOPK_TOPP | CLSAMPLE_MODE_SCORE_ONLY)) return CLSAMPLE_ERR_MODE;
   if (a->B == 0) return CLSAMPLE_SUCCESS;
   if (!a->logits || !a->tokens) return CLSAMPLE_ERR_NULL;
   if (a->hist_offs && !a->hist_ids) return CLSAMPLE_ERR_NULL;
   if (a->bias_offs && (!a->bias_ids || !a->bias_vals)) return CLSAMPLE_ERR_NULL;
+  if (a->tid_offs && (!a->tid_ids || !a->tid_logprobs)) return CLSAMPLE_ERR_NULL;
   if (a->logits_row_stride < a->V) return CLSAMPLE_ERR_STRIDE;
   if (a->bitmask && a->bitmask_row_stride < (a->V + 31) / 32) return CLSAMPLE_ERR_STRIDE;
   int cur = -1;

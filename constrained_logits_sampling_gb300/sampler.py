@@ -20,6 +20,7 @@ _lock = threading.Lock()
 _lib = None
 
 LOGITS_F32, LOGITS_BF16 = 0, 1
+MODE_JOINT_TOPK_TOPP, MODE_SCORE_ONLY = 1, 2
 ROW_OK, ROW_OVERFLOW, ROW_INVALID = 0, 1, 2
 
 
@@ -27,7 +28,7 @@ class Args(ctypes.Structure):
     """Mirror of clsample_args_t (include/clsample.h)."""
     _fields_ = [
         ("B", ctypes.c_int32), ("V", ctypes.c_int32), ("logits_dtype", ctypes.c_int32),
-        ("reserved0", ctypes.c_int32),
+        ("mode", ctypes.c_int32),
         ("logits", ctypes.c_void_p), ("logits_row_stride", ctypes.c_int64),
         ("temperatures", ctypes.c_void_p), ("top_ks", ctypes.c_void_p), ("top_ps", ctypes.c_void_p),
         ("min_ps", ctypes.c_void_p), ("rep", ctypes.c_void_p), ("freq", ctypes.c_void_p),
@@ -38,6 +39,7 @@ class Args(ctypes.Structure):
         ("tokens", ctypes.c_void_p), ("logprobs", ctypes.c_void_p), ("row_status", ctypes.c_void_p),
         ("dbg_transformed", ctypes.c_void_p), ("dbg_kept_count", ctypes.c_void_p),
         ("dbg_cut", ctypes.c_void_p), ("logprobs_orig", ctypes.c_void_p), ("logprobs_kept", ctypes.c_void_p),
+        ("tid_offs", ctypes.c_void_p), ("tid_ids", ctypes.c_void_p), ("tid_logprobs", ctypes.c_void_p),
     ]
 
 
@@ -154,7 +156,7 @@ class Sampler:
                   bias_offs=None, bias_ids=None, bias_vals=None, bitmask=None, seeds=None,
                   positions=None, step: int = 0, tokens=None, logprobs=None, row_status=None,
                   dbg_transformed=None, dbg_kept_count=None, dbg_cut=None, logprobs_orig=None,
-                  logprobs_kept=None) -> Args:
+                  logprobs_kept=None, mode: int = 0, tid_offs=None, tid_ids=None, tid_logprobs=None) -> Args:
         if logits.dim() != 2 or logits.stride(1) != 1:
             raise ValueError("logits must be [B, V] with unit column stride")
         if logits.dtype == torch.float32:
@@ -168,7 +170,7 @@ class Sampler:
         if logits.device != dev:
             raise ValueError(f"logits on {logits.device}, handle on {dev}")
         a = Args()
-        a.B, a.V, a.logits_dtype = B, V, dt
+        a.B, a.V, a.logits_dtype, a.mode = B, V, dt, int(mode)
         a.logits = logits.data_ptr()
         a.logits_row_stride = logits.stride(0)
         f32, i32, i64 = torch.float32, torch.int32, torch.int64
@@ -204,6 +206,9 @@ class Sampler:
         a.dbg_cut = _dptr(dbg_cut, f32, B, "dbg_cut", dev)
         a.logprobs_orig = _dptr(logprobs_orig, f32, B, "logprobs_orig", dev)
         a.logprobs_kept = _dptr(logprobs_kept, f32, B, "logprobs_kept", dev)
+        a.tid_offs = _dptr(tid_offs, i32, B + 1, "tid_offs", dev)
+        a.tid_ids = _dptr(tid_ids, i32, None, "tid_ids", dev)
+        a.tid_logprobs = _dptr(tid_logprobs, f32, None, "tid_logprobs", dev)
         return a
 
     def apply(self, args: Args, stream: Optional[torch.cuda.Stream] = None):
@@ -225,7 +230,8 @@ class Sampler:
         ``logprobs`` (float32) and ``status`` (int32); with ``debug`` also
         ``transformed`` [B, V], ``kept_count`` and ``cut``; with ``variants`` (or
         ``debug``) also ``logprobs_orig`` (T = 1) and ``logprobs_kept`` (renormalised
-        over the kept set)."""
+        over the kept set); with ``tid_offs``/``tid_ids`` (requested token ids, CSR)
+        also ``tid_logprobs``.  ``mode`` takes the MODE_* bits."""
         B, V = logits.shape
         dev = self.device
         out = {
@@ -240,11 +246,14 @@ class Sampler:
         if variants or debug:
             out["logprobs_orig"] = torch.empty(B, dtype=torch.float32, device=dev)
             out["logprobs_kept"] = torch.empty(B, dtype=torch.float32, device=dev)
+        if kw.get("tid_offs") is not None:
+            n = kw["tid_ids"].numel() if kw.get("tid_ids") is not None else 0
+            out["tid_logprobs"] = torch.empty(max(n, 1), dtype=torch.float32, device=dev)[:n]
         args = self.make_args(logits, tokens=out["tokens"], logprobs=out["logprobs"],
                               row_status=out["status"], dbg_transformed=out.get("transformed"),
                               dbg_kept_count=out.get("kept_count"), dbg_cut=out.get("cut"),
                               logprobs_orig=out.get("logprobs_orig"), logprobs_kept=out.get("logprobs_kept"),
-                              **kw)
+                              tid_logprobs=out.get("tid_logprobs"), **kw)
         self.apply(args, stream)
         return out
 
@@ -295,4 +304,11 @@ def batch_to_device(batch, device) -> Dict[str, object]:
               hist_offs=t(batch.hist_offs), hist_ids=t(batch.hist_ids), bias_offs=t(batch.bias_offs),
               bias_ids=t(batch.bias_ids), bias_vals=t(batch.bias_vals), bitmask=t(batch.bitmask),
               seeds=t(batch.seeds), positions=t(batch.positions), step=int(batch.step))
+    if getattr(batch, "mode", 0):
+        kw["mode"] = int(batch.mode)
+    if getattr(batch, "tid_offs", None) is not None:
+        ids = np.asarray(batch.tid_ids, np.int32)
+        # a device copy of an empty array may have no address: keep one padding slot
+        kw["tid_offs"] = t(batch.tid_offs)
+        kw["tid_ids"] = t(np.concatenate([ids, np.zeros(1, np.int32)]))[:ids.size]
     return {"logits": logits, **kw}

@@ -73,11 +73,25 @@ enum {
   CLSAMPLE_ERR_STRIDE = -4,     /* logits_row_stride < V or bitmask_row_stride < ceil(V/32) */
   CLSAMPLE_ERR_DTYPE = -5,      /* logits_dtype is not a CLSAMPLE_LOGITS_* value */
   CLSAMPLE_ERR_CUDA = -6,       /* a CUDA runtime call failed (launch, attribute, device) */
-  CLSAMPLE_ERR_DEVICE = -7      /* the current device is not the handle's or not sm_103 */
+  CLSAMPLE_ERR_DEVICE = -7,     /* the current device is not the handle's or not sm_103 */
+  CLSAMPLE_ERR_MODE = -8        /* mode has a bit that is not a CLSAMPLE_MODE_* flag */
+};
+
+/* Bits of clsample_args_t.mode (0: sequential truncation, one draw per row). */
+enum {
+  /* Top-p over the whole distribution, intersected with the top-k set (SGLang page,
+   * the sampler's "joint" filter order), instead of top-p over the renormalised top-k
+   * set.  Rows with a top-k cut and top_p < 1 then take the co-resident row-group route. */
+  CLSAMPLE_MODE_JOINT_TOPK_TOPP = 1,
+  /* Scoring only (SGLang page, logprobs-only computation): the same transforms, no draw.
+   * Every row takes the greedy route whatever its parameters -- token = argmax of z',
+   * logprobs at T_eff -- and the requested ids (tid_*) get their logprobs. */
+  CLSAMPLE_MODE_SCORE_ONLY = 2
 };
 
 /* Arguments of one sampler call.  B rows, V vocabulary entries.
  *
+ * mode              CLSAMPLE_MODE_* bits, 0 for plain sampling; other bits: ERR_MODE.
  * logits            [B, logits_row_stride] elements of logits_dtype, row-major.
  * temperatures      f32[B]; NULL = 1.0.  T < 1e-5 (including 0 and negatives) is greedy;
  *                   NaN or +inf is INVALID.
@@ -114,6 +128,13 @@ enum {
  *                   over the kept set K, the distribution it was drawn from (GLM page,
  *                   "Sampling": the top-k/top-p sampler's processed logprobs); 0 for
  *                   greedy rows (K is the token alone).
+ * tid_offs/ids      CSR of requested token ids (SGLang page, the output container's
+ *                   token-ids logprobs): ids tid_ids[tid_offs[r] .. tid_offs[r+1]), in
+ *                   any order, repeats allowed.  NULL offs = none.  An id outside [0, V)
+ *                   or a decreasing offset makes the row INVALID.
+ * tid_logprobs      f32[tid_offs[B]] output (required with tid_offs): ln p(id) under the
+ *                   same distribution as `logprobs` (softmax(z'/T_eff), pre-truncation);
+ *                   -inf for a masked id and for every id of an INVALID row.
  *
  * Limits: V <= 262144 (at most 18 slices of at most 15360 tokens per row).  Any number
  * of penalised, biased or allowed tokens is handled exactly.  A row whose candidate set
@@ -124,7 +145,7 @@ enum {
 typedef struct {
   int32_t B, V;
   int32_t logits_dtype;
-  int32_t reserved0;
+  int32_t mode;
   const void* logits;
   int64_t logits_row_stride;
   const float* temperatures;
@@ -152,6 +173,9 @@ typedef struct {
   float* dbg_cut;
   float* logprobs_orig;
   float* logprobs_kept;
+  const int32_t* tid_offs;
+  const int32_t* tid_ids;
+  float* tid_logprobs;
 } clsample_args_t;
 
 /* Creates a handle for batches of up to max_batch rows over a vocabulary of `vocab`

@@ -10,7 +10,8 @@ Acceptance bar (element by element):
     still be a kept token, and such rows must stay under 0.1% of the batch;
   * logprob of the drawn token: within 1e-5 absolute; so are the drawn token's logprob
     under the original (T = 1, untruncated) distribution and under the kept set, where
-    both sides report them.
+    both sides report them; so are the logprobs of requested token ids (with the same
+    -inf pattern: masked ids and every id of an INVALID row).
 """
 import numpy as np
 import torch
@@ -70,5 +71,14 @@ def compare(batch, g, o, name="", max_ambiguous_frac=1e-3):
             err = np.abs(g[key][rows].astype(np.float64) - o[key][rows])
             assert (err <= LOGPROB_TOL).all(), (name, key, float(err.max()), np.nonzero(rows)[0][np.argmax(err)])
             assert np.all(np.isneginf(g[key][inval])), (name, key, "invalid rows")
+    if "tid_logprobs" in g and "tid_logprobs" in o:
+        offs = np.asarray(batch.tid_offs, np.int64)
+        owner = np.repeat(np.arange(B), np.diff(offs))
+        gv, ov = g["tid_logprobs"].astype(np.float64), o["tid_logprobs"]
+        assert np.array_equal(np.isneginf(gv), np.isneginf(ov)), (name, "tid -inf pattern")
+        fin = np.isfinite(ov) & ok[owner]
+        err = np.abs(gv[fin] - ov[fin])
+        assert (err <= LOGPROB_TOL).all(), (name, "tid_logprobs", float(err.max()) if err.size else 0.0)
+        assert np.all(np.isneginf(gv[~ok[owner]])), (name, "tid_logprobs of invalid rows")
     return {"ambiguous": n_amb, "max_logprob_err": float(lp_err.max()) if lp_err.size else 0.0,
             "mismatch_ambiguous": int((amb & ~same).sum())}

@@ -46,7 +46,7 @@ def test_nm_dynamic_symbols(lib):
 def test_strerror_and_geometry(lib):
     from constrained_logits_sampling_gb300 import sampler
     assert lib.clsample_strerror(0) == b"success"
-    for code in range(-7, 0):
+    for code in range(-8, 0):
         assert lib.clsample_strerror(code) != b"unknown error"
     g = sampler.geometry(151936)
     assert g == {"slices": 10, "chunk": 15232, "smem_bytes": g["smem_bytes"]}

@@ -377,3 +377,67 @@ def test_logprob_variants_on_request(w):
     for k in ("logprobs_orig", "logprobs_kept"):
         err = np.abs(var[k][ok].astype(np.float64) - o[k][ok])
         assert (err <= 1e-5).all(), (k, float(err.max()))
+
+
+def _requests(b, per_row, seed, bad_row=None):
+    rng = np.random.default_rng(seed)
+    offs, ids = [0], []
+    for r in range(b.B):
+        n = int(rng.integers(0, per_row + 1))
+        ids.extend(int(x) for x in rng.integers(0, b.V, size=n))
+        if r == bad_row:
+            ids.append(b.V)
+        offs.append(len(ids))
+    b.tid_offs, b.tid_ids = np.asarray(offs, np.int32), np.asarray(ids, np.int32)
+    return b
+
+
+@pytest.mark.parametrize("w,B,V", [(2, 48, 151936), (4, 32, 60000), (5, 64, 30011)])
+def test_joint_topk_topp_parity(w, B, V):
+    """Joint top-k/top-p order (top-p over the whole distribution, intersected with
+    top-k): bit-exact kept sets and tokens against the oracle; the joint order changes
+    some rows' kept sets relative to the sequential order."""
+    b = make_workload(w, B=B, V=V)
+    b.mode = 1
+    g, o = run_gpu(b), run_oracle(b)
+    compare(b, g, o, f"joint w{w}")
+    if w != 5:  # the verify-scale rows are peaked: one or two tokens either way
+        b.mode = 0
+        seq = run_oracle(b, want_transformed=False)
+        assert (seq["kept_count"] != o["kept_count"]).any()
+
+
+@pytest.mark.parametrize("w", [3, 4, 5])
+def test_requested_id_logprobs_parity(w):
+    """Logprobs of requested token ids (pre-truncation, at T) within 1e-5 of the oracle,
+    -inf exactly where the oracle has it; an id outside the vocabulary makes its row
+    INVALID."""
+    b = _requests(make_workload(w, B=40, V=50021), 8, 30 + w, bad_row=3)
+    g, o = run_gpu(b), run_oracle(b)
+    assert o["status"][3] == 2 and g["status"][3] == 2
+    compare(b, g, o, f"tids w{w}")
+
+
+def test_score_only_parity():
+    """Score-only mode: greedy route for every row (argmax token, logprobs at T), the
+    requested ids scored, the seeds irrelevant."""
+    b = _requests(make_workload(4, B=48, V=151936), 6, 7)
+    b.mode = 2
+    g, o = run_gpu(b), run_oracle(b)
+    compare(b, g, o, "score-only")
+    b.seeds = b.seeds[::-1].copy()
+    g2 = run_gpu(b)
+    assert np.array_equal(g["tokens"], g2["tokens"])
+    assert np.array_equal(g["tid_logprobs"].view(np.uint32), g2["tid_logprobs"].view(np.uint32))
+
+
+def test_unknown_mode_bit_is_rejected_on_the_host():
+    from constrained_logits_sampling_gb300.sampler import ClsampleError, Sampler, batch_to_device
+    b = make_workload(1, B=4, V=1000)
+    s = Sampler(4, 1000)
+    kw = batch_to_device(b, s.device)
+    logits = kw.pop("logits")
+    with pytest.raises(ClsampleError):
+        s(logits, mode=4, **kw)
+    s(logits, mode=3, **kw)
+    torch.cuda.synchronize()

@@ -2678,6 +2678,30 @@ __global__ void __launch_bounds__(kThreads, 3) sampler_kernel(const __grid_const
 
 // ---------------------------------------------------------------- diagnostics
 
+// Allowed-token lists -> grammar bitmask rows: one CTA per row clears the row's words,
+// then sets the bit of every listed id; a row with an id outside [0, V) or an empty list
+// ends all-zero (every token masked), which the sampler reports as INVALID.
+__global__ void allowed_to_bitmask_kernel(const int32_t* __restrict__ offs, const int32_t* __restrict__ ids, int V,
+                                          int32_t* bitmask, long long stride) {
+  __shared__ int bad;
+  const int row = blockIdx.x;
+  const int W = (V + 31) >> 5;
+  int32_t* words = bitmask + (long long)row * stride;
+  const int lo = offs[row], hi = offs[row + 1];
+  if (threadIdx.x == 0) bad = lo < 0 || hi < lo;
+  for (int w = threadIdx.x; w < W; w += blockDim.x) words[w] = 0;
+  __syncthreads();
+  if (!bad)
+    for (int j = lo + threadIdx.x; j < hi; j += blockDim.x) {
+      const int id = ids[j];
+      if (id < 0 || id >= V) bad = 1;
+      else atomicOr(reinterpret_cast<unsigned*>(words + (id >> 5)), 1u << (id & 31));
+    }
+  __syncthreads();
+  if (bad)
+    for (int w = threadIdx.x; w < W; w += blockDim.x) words[w] = 0;
+}
+
 __global__ void debug_weights_kernel(const float* y, unsigned long long* w, int n) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) w[i] = weight_fx(y[i]);
@@ -3040,6 +3064,18 @@ int clsample_occupancy(clsample_t* h, int32_t logits_dtype, int32_t* resident_ct
   if (logits_dtype != CLSAMPLE_LOGITS_F32 && logits_dtype != CLSAMPLE_LOGITS_BF16) return CLSAMPLE_ERR_DTYPE;
   *resident_ctas_out = h->grid[logits_dtype == CLSAMPLE_LOGITS_BF16 ? 1 : 0];
   return CLSAMPLE_SUCCESS;
+}
+
+int clsample_allowed_to_bitmask(const int32_t* offs, const int32_t* ids, int32_t B, int32_t V, int32_t* bitmask,
+                                int64_t bitmask_row_stride, clsample_stream_t stream) {
+  if (B < 0 || B > (1 << 24) - 1) return CLSAMPLE_ERR_BATCH;
+  if (V <= 0) return CLSAMPLE_ERR_VOCAB;
+  if (bitmask_row_stride < (V + 31) / 32) return CLSAMPLE_ERR_STRIDE;
+  if (B == 0) return CLSAMPLE_SUCCESS;
+  if (!offs || !ids || !bitmask) return CLSAMPLE_ERR_NULL;
+  allowed_to_bitmask_kernel<<<(unsigned)B, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      offs, ids, V, bitmask, (long long)bitmask_row_stride);
+  return cudaGetLastError() == cudaSuccess ? CLSAMPLE_SUCCESS : CLSAMPLE_ERR_CUDA;
 }
 
 int clsample_debug_weights(const float* y, uint64_t* w, int32_t n, clsample_stream_t stream) {

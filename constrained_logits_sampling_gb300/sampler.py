@@ -45,7 +45,7 @@ class Args(ctypes.Structure):
 
 EXPORTS = ("clsample_create", "clsample_destroy", "clsample_apply", "clsample_prepare", "clsample_sample",
            "clsample_apply_static", "clsample_strerror", "clsample_geometry", "clsample_occupancy",
-           "clsample_debug_weights", "clsample_debug_uniforms")
+           "clsample_debug_weights", "clsample_debug_uniforms", "clsample_allowed_to_bitmask")
 
 
 def load_library(path: str = LIB_PATH):
@@ -77,6 +77,10 @@ def load_library(path: str = LIB_PATH):
             L.clsample_debug_weights.restype = ctypes.c_int
             L.clsample_debug_uniforms.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int32, ctypes.c_void_p]
             L.clsample_debug_uniforms.restype = ctypes.c_int
+            L.clsample_allowed_to_bitmask.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                                      ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64,
+                                                      ctypes.c_void_p]
+            L.clsample_allowed_to_bitmask.restype = ctypes.c_int
             _lib = L
         return _lib
 
@@ -262,6 +266,24 @@ def apply_static(args: Args, stream: Optional[torch.cuda.Stream] = None):
     """One call through ``clsample_apply_static`` (no handle, no allocation; at most 64
     rows; calls on one device must be ordered)."""
     _check(load_library().clsample_apply_static(ctypes.byref(args), _stream_ptr(stream)))
+
+
+def allowed_to_bitmask(offs: torch.Tensor, ids: torch.Tensor, V: int, bitmask: Optional[torch.Tensor] = None,
+                       stream=None) -> torch.Tensor:
+    """Grammar-bitmask rows from allowed-token lists (CSR on the device), built by the
+    library's kernel.  Returns (or fills) int32 [B, ceil(V/32)]."""
+    L = load_library()
+    B = offs.numel() - 1
+    if bitmask is None:
+        bitmask = torch.empty(max(B, 0), (V + 31) // 32, dtype=torch.int32, device=offs.device)
+    if offs.dtype != torch.int32 or ids.dtype != torch.int32 or bitmask.dtype != torch.int32:
+        raise ValueError("offs, ids and bitmask must be int32")
+    if bitmask.dim() != 2 or bitmask.stride(1) != 1:
+        raise ValueError("bitmask must be [B, W] with unit column stride")
+    ids_ptr = ids.data_ptr() if ids.numel() else offs.data_ptr()  # an empty list is never read
+    _check(L.clsample_allowed_to_bitmask(offs.contiguous().data_ptr(), ids_ptr, B, V, bitmask.data_ptr(),
+                                         bitmask.stride(0), _stream_ptr(stream)))
+    return bitmask
 
 
 def debug_weights(y: torch.Tensor) -> torch.Tensor:

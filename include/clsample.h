@@ -236,6 +236,17 @@ int clsample_geometry(int32_t vocab, int32_t* slices, int32_t* chunk, int32_t* s
  * clsample_create; the kernel launches one CTA per (row, slice). */
 int clsample_occupancy(clsample_t* handle, int32_t logits_dtype, int32_t* resident_ctas);
 
+/* Builds grammar-bitmask rows from allowed-token lists (vLLM page, "allowed token ids",
+ * a hard-coded constraint of the sampler, expressed here as the bitmask the sampler
+ * takes).  offs i32[B+1] and ids (DEVICE) give row r's allowed ids ids[offs[r] ..
+ * offs[r+1]); bitmask i32[B, bitmask_row_stride] (DEVICE, written; words past
+ * ceil(V/32) untouched) gets bit id & 31 of word id >> 5 set for each listed id and every
+ * other bit cleared.  A row with an id outside [0, V), a decreasing offset or an empty
+ * list ends all-zero, which clsample_apply reports as INVALID.  Enqueue only on `stream`;
+ * returns a negative code for bad sizes or NULL pointers (nothing launched). */
+int clsample_allowed_to_bitmask(const int32_t* offs, const int32_t* ids, int32_t B, int32_t V, int32_t* bitmask,
+                                int64_t bitmask_row_stride, clsample_stream_t stream);
+
 /* Diagnostics of the building blocks, on device arrays of length n (enqueued on
  * `stream`): the fixed-point top-p weight floor(exp32(y) * 2^40) of each y (y <= 0),
  * and the race uniform U of (seed, position, token).  They run the same device code

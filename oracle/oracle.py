@@ -176,3 +176,24 @@ def weight_fx(y: float) -> int:
 
 def ceil_scaled(W: int, p: float) -> int:
     return int(lib().cls_oracle_ceil_scaled(W, float(np.float32(p))))
+
+
+def allowed_to_bitmask(offs, ids, V: int) -> np.ndarray:
+    """Grammar-bitmask rows from allowed-token lists (vLLM page, "allowed token ids",
+    expressed as the sampler's bitmask): bit i & 31 of word i >> 5 is set iff i is listed.
+    A row with an id outside [0, V), a decreasing offset or an empty list is all zero
+    (every token masked: the sampler reports the row INVALID)."""
+    offs = np.asarray(offs, np.int64)
+    ids = np.asarray(ids, np.int64)
+    B, W = len(offs) - 1, (V + 31) // 32
+    out = np.zeros((B, W), np.uint32)
+    for r in range(B):
+        lo, hi = int(offs[r]), int(offs[r + 1])
+        if lo < 0 or hi < lo:
+            continue
+        row = ids[lo:hi]
+        if ((row < 0) | (row >= V)).any():
+            continue
+        for i in row:
+            out[r, i >> 5] |= np.uint32(1) << np.uint32(i & 31)
+    return out.view(np.int32)

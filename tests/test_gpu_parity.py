@@ -441,3 +441,60 @@ def test_unknown_mode_bit_is_rejected_on_the_host():
         s(logits, mode=4, **kw)
     s(logits, mode=3, **kw)
     torch.cuda.synchronize()
+
+
+def test_allowed_ids_to_bitmask_bitexact():
+    """The library's allowed-ids kernel equals the oracle's bitmask bit for bit (strided
+    output, bad and empty rows, repeated ids), and sampling with it matches the oracle."""
+    from oracle import oracle as O
+    from constrained_logits_sampling_gb300.sampler import allowed_to_bitmask
+    rng = np.random.default_rng(17)
+    V, B = 40009, 24
+    offs, ids = [0], []
+    for r in range(B):
+        n = int(rng.choice([0, 1, 5, 300, 7000]))
+        row = rng.integers(0, V, size=n).tolist()
+        if r == 5:
+            row.append(V)
+        if r == 6:
+            row.append(-1)
+        ids.extend(row)
+        offs.append(len(ids))
+    offs, ids = np.asarray(offs, np.int32), np.asarray(ids, np.int32)
+    ref = O.allowed_to_bitmask(offs, ids, V)
+    W = (V + 31) // 32
+    dev = torch.device("cuda")
+    full = torch.full((B, W + 3), 0x5A5A5A5A, dtype=torch.int32, device=dev)
+    allowed_to_bitmask(torch.from_numpy(offs).to(dev), torch.from_numpy(ids).to(dev), V, bitmask=full[:, :W])
+    got = full.cpu().numpy()
+    assert np.array_equal(got[:, :W], ref)
+    assert (got[:, W:] == 0x5A5A5A5A).all()
+    b = make_workload(2, B=B, V=V)
+    b.bitmask = np.ascontiguousarray(ref)
+    g, o = run_gpu(b), run_oracle(b)
+    compare(b, g, o, "allowed ids")
+    empty_or_bad = np.diff(offs) == 0
+    empty_or_bad[[5, 6]] = True
+    assert (g["status"][empty_or_bad] == 2).all()
+
+
+def test_minus_inf_bias_parity():
+    """-inf logit_bias entries (the min-new-tokens reading: EOS ids banned) are never drawn
+    and the rows match the oracle bit for bit."""
+    b = make_workload(4, B=32, V=70001)
+    o0 = run_oracle(b, want_transformed=False)
+    n0 = np.diff(b.bias_offs)
+    ids, vals, offs = [], [], [0]
+    for r in range(b.B):
+        lo, hi = int(b.bias_offs[r]), int(b.bias_offs[r + 1])
+        ids.extend(b.bias_ids[lo:hi].tolist() + [int(o0["tokens"][r]), 7, 70000])
+        vals.extend(b.bias_vals[lo:hi].tolist() + [-np.inf] * 3)
+        offs.append(len(ids))
+    b.bias_offs, b.bias_ids = np.asarray(offs, np.int32), np.asarray(ids, np.int32)
+    b.bias_vals = np.asarray(vals, np.float32)
+    g, o = run_gpu(b), run_oracle(b)
+    compare(b, g, o, "-inf bias")
+    ok = o["status"] == 0
+    assert (g["tokens"][ok] != o0["tokens"][ok]).all()
+    assert not np.isin(g["tokens"][ok], [7, 70000]).any()
+    assert n0.sum() > 0

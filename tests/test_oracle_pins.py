@@ -616,3 +616,38 @@ def test_score_only_mode(oracle):
     assert np.array_equal(o["tokens"][ok], np.argmax(o["transformed"][ok], axis=1))
     assert (o["kept_count"][ok] == 1).all()
     assert np.array_equal(o["tid_logprobs"], samp["tid_logprobs"])
+
+
+# ----------------------------------------------------------------------------- allowed ids, min tokens
+
+def test_allowed_ids_bitmask_worked_example(oracle):
+    """Allowed-id lists as bitmask words, hand-computed from the bit layout (bit i & 31 of
+    word i >> 5): {0, 31, 32, 63, 64} over V = 70 -> 0x80000001, 0x80000001, 0x1; bad or
+    empty rows are all zero, and such a row samples INVALID."""
+    m = oracle.allowed_to_bitmask([0, 5, 5, 7, 8], [0, 31, 32, 63, 64, 3, 70, 69], 70).view(np.uint32)
+    assert m.shape == (4, 3)
+    assert [hex(int(x)) for x in m[0]] == ["0x80000001", "0x80000001", "0x1"]
+    assert (m[1] == 0).all() and (m[2] == 0).all()
+    assert [hex(int(x)) for x in m[3]] == ["0x0", "0x0", "0x20"]
+    b = batch(np.zeros((4, 70), F32), bitmask=m.view(np.int32))
+    o = oracle.sample(b)
+    assert list(o["status"]) == [0, 2, 2, 0]
+    assert int(o["tokens"][3]) == 69
+
+
+def test_min_new_tokens_as_minus_inf_bias(oracle):
+    """Min-new-tokens (SGLang teardown (10); vLLM logits processors, 'Min-tokens') read as
+    a -inf logit_bias on the EOS ids: those ids are never drawn, even as the argmax, and
+    the rest of the row is unchanged."""
+    b = make_workload(2, B=16, V=5000)
+    o = oracle.sample(b, want_transformed=True)
+    eos = [int(t) for t in o["tokens"][:4]] + [int(np.argmax(o["transformed"][0]))]
+    b.bias_offs = np.arange(0, 16 * len(eos) + 1, len(eos), dtype=np.int32)
+    b.bias_ids = np.tile(np.asarray(eos, np.int32), 16)
+    b.bias_vals = np.full(16 * len(eos), -np.inf, np.float32)
+    o2 = oracle.sample(b, want_transformed=True)
+    assert (o2["status"] == 0).all()
+    assert not np.isin(o2["tokens"], eos).any()
+    assert np.isneginf(o2["transformed"][:, eos]).all()
+    keep = np.setdiff1d(np.arange(5000), eos)
+    assert np.array_equal(o2["transformed"][:, keep], o["transformed"][:, keep])

@@ -57,6 +57,8 @@ class Batch:
     mode: int = 0  # bit 0: joint top-k/top-p; bit 1: score only (no draw)
     tid_offs: Optional[np.ndarray] = None  # i32[B+1]: requested token ids per row
     tid_ids: Optional[np.ndarray] = None  # i32[nnz]
+    top_ns: Optional[np.ndarray] = None  # i32[B]: top-N logprobs wanted per row (0..32)
+    top_n_stride: int = 0  # row stride of the top-N outputs (0: the largest N)
 
     def host_bytes(self) -> Dict[str, int]:
         out = {}
@@ -77,9 +79,10 @@ class Batch:
         """Sub-batch with the given row indices (CSR arrays re-based)."""
         idx = np.asarray(idx, dtype=np.int64)
         nb = Batch(B=len(idx), V=self.V, logits=np.ascontiguousarray(self.logits[idx]),
-                   logits_bf16=self.logits_bf16, step=self.step, name=self.name + "[sub]", mode=self.mode)
+                   logits_bf16=self.logits_bf16, step=self.step, name=self.name + "[sub]", mode=self.mode,
+                   top_n_stride=self.top_n_stride)
         for f in ("temperatures", "top_ks", "top_ps", "min_ps", "rep", "freq", "pres",
-                  "seeds", "positions"):
+                  "seeds", "positions", "top_ns"):
             v = getattr(self, f)
             if v is not None:
                 setattr(nb, f, np.ascontiguousarray(v[idx]))

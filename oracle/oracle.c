@@ -281,6 +281,21 @@ static void sample_row(const cls_oracle_args* a, int r, row_scratch* s) {
   if (a->tid_logprobs)
     for (int32_t j = tlo; j < thi; ++j) a->tid_logprobs[j] = -INFINITY;
 
+  /* top-N most probable tokens: N in [0, min(32, stride)], else INVALID */
+  int topn = 0;
+  if (a->top_ns) {
+    int32_t n = a->top_ns[r];
+    if (n < 0 || n > CLS_ORACLE_TOP_N_MAX || n > a->top_n_stride) {
+      status = ORACLE_INVALID;
+    } else {
+      topn = n;
+      for (int j = 0; j < n; ++j) {
+        a->top_ids[(int64_t)r * a->top_n_stride + j] = -1;
+        a->top_logprobs[(int64_t)r * a->top_n_stride + j] = -INFINITY;
+      }
+    }
+  }
+
   /* An overflow in steps 2-3 is folded back the same way as step 1 treats its
    * input, except that -inf stays -inf (the token is out). */
   for (int i = 0; i < V; ++i) {
@@ -335,6 +350,24 @@ static void sample_row(const cls_oracle_args* a, int r, row_scratch* s) {
     }
   }
   double logS = log(S);
+  /* the N most probable tokens (SGLang page, the output container's top logprobs):
+   * candidates ordered by z' descending -- the same order as y, which is monotone in z'
+   * -- with equal z' by id ascending; fewer than N candidates leave -1 / -inf */
+  if (topn > 0) {
+    int n = 0;
+    for (int i = 0; i < V; ++i)
+      if (s->z[i] > -INFINITY) {
+        s->order[n].y = s->z[i];
+        s->order[n].id = i;
+        ++n;
+      }
+    qsort(s->order, (size_t)n, sizeof(s->order[0]), cmp_yid_desc);
+    for (int j = 0; j < topn && j < n; ++j) {
+      int id = s->order[j].id;
+      a->top_ids[(int64_t)r * a->top_n_stride + j] = id;
+      a->top_logprobs[(int64_t)r * a->top_n_stride + j] = (double)s->y[id] - logS;
+    }
+  }
   /* logprobs of the requested ids, under the same distribution as the drawn token's:
    * y_id - ln S (-inf for a masked id) */
   if (a->tid_logprobs)

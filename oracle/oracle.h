@@ -57,7 +57,14 @@ typedef struct {
   const int32_t* tid_offs;         /* [B+1] or NULL: per-row lists of requested token ids */
   const int32_t* tid_ids;
   double* tid_logprobs;            /* [tid_offs[B]] or NULL: ln p(id) at T, pre-truncation */
+  const int32_t* top_ns;           /* [B] or NULL: how many most probable tokens to report */
+  int32_t top_n_stride;            /* row stride of top_ids / top_logprobs */
+  int32_t* top_ids;                /* [B, top_n_stride]: by z' descending, then id ascending */
+  double* top_logprobs;            /* [B, top_n_stride]: ln p at T, pre-truncation */
 } cls_oracle_args;
+
+/* Largest N the top-N outputs accept per row (more, or more than the stride: INVALID). */
+#define CLS_ORACLE_TOP_N_MAX 32
 
 /* mode bits.  JOINT: top-p is taken over the whole distribution and intersected with the
  * top-k set (instead of top-p over the renormalised top-k set).  SCORE_ONLY: no draw;

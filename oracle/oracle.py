@@ -49,7 +49,8 @@ class _Args(ctypes.Structure):
         ("race_gap", ctypes.c_void_p), ("race_best", ctypes.c_void_p), ("nthreads", ctypes.c_int32),
         ("logprobs_orig", ctypes.c_void_p), ("logprobs_kept", ctypes.c_void_p),
         ("mode", ctypes.c_int32), ("tid_offs", ctypes.c_void_p), ("tid_ids", ctypes.c_void_p),
-        ("tid_logprobs", ctypes.c_void_p),
+        ("tid_logprobs", ctypes.c_void_p), ("top_ns", ctypes.c_void_p), ("top_n_stride", ctypes.c_int32),
+        ("top_ids", ctypes.c_void_p), ("top_logprobs", ctypes.c_void_p),
     ]
 
 
@@ -150,6 +151,13 @@ def sample(batch, nthreads: int = 0, want_transformed: bool = False) -> Dict[str
         a.tid_offs, a.tid_ids = toffs.ctypes.data, tids.ctypes.data
         out["tid_logprobs"] = np.zeros(max(int(toffs[-1]), 0), np.float64)
         a.tid_logprobs = out["tid_logprobs"].ctypes.data
+    tns = arr("top_ns", np.int32)
+    if tns is not None:
+        stride = int(getattr(batch, "top_n_stride", 0) or max(int(tns.max()) if B else 1, 1))
+        a.top_ns, a.top_n_stride = tns.ctypes.data, stride
+        out["top_ids"] = np.full((B, stride), -7, np.int32)
+        out["top_logprobs"] = np.full((B, stride), 7.0, np.float64)
+        a.top_ids, a.top_logprobs = out["top_ids"].ctypes.data, out["top_logprobs"].ctypes.data
     out["threads"] = L.cls_oracle_sample(ctypes.byref(a))
     return out
 

@@ -651,3 +651,49 @@ def test_min_new_tokens_as_minus_inf_bias(oracle):
     assert np.isneginf(o2["transformed"][:, eos]).all()
     keep = np.setdiff1d(np.arange(5000), eos)
     assert np.array_equal(o2["transformed"][:, keep], o["transformed"][:, keep])
+
+
+# ----------------------------------------------------------------------------- top-N logprobs
+
+def test_top_n_against_library_topk(oracle):
+    """Top-N logprobs (SGLang teardown (10), the output container's top logprobs): the
+    reported values are the N largest of torch.log_softmax(z'/T) in float64 (the values
+    torch.topk returns), each reported id carries its own log_softmax value, and the
+    order is by descending probability."""
+    import torch
+    b = make_workload(4, B=20, V=9000)
+    b.top_ns = np.array([(0, 1, 5, 20, 32)[r % 5] for r in range(20)], np.int32)
+    o = oracle.sample(b, want_transformed=True)
+    assert o["top_ids"].shape == (20, 32)
+    for r in range(20):
+        n = int(b.top_ns[r])
+        T = float(b.temperatures[r])
+        Teff = T if T >= 1e-5 else 1.0
+        ref = torch.log_softmax(torch.tensor(o["transformed"][r], dtype=torch.float64) / Teff, dim=0)
+        vals = torch.topk(ref, n).values.numpy() if n else np.zeros(0)
+        got = o["top_logprobs"][r, :n]
+        assert np.allclose(got, vals, atol=1e-6, rtol=0)
+        ids = o["top_ids"][r, :n]
+        have = ids >= 0
+        assert np.array_equal(have, np.isfinite(vals))  # -1 exactly past the candidates
+        assert np.allclose(ref.numpy()[ids[have]], got[have], atol=1e-6, rtol=0)
+        assert (np.diff(got[have]) <= 0).all()
+        assert (o["top_ids"][r, n:] == -7).all()  # past N: untouched
+
+
+def test_top_n_ties_and_short_rows(oracle):
+    """Equal z' are reported lowest id first; a row with fewer candidates than N ends in
+    -1 / -inf; N above 32 or above the stride makes the row INVALID."""
+    V = 40
+    z = np.zeros((4, V), F32)
+    z[0, 17] = 1.0
+    allowed = [np.arange(V), np.arange(V), np.array([3, 9]), np.arange(V)]
+    b = batch(z, bitmask=mask_from_allowed(allowed, V), top_ns=np.array([4, 33, 4, 4], np.int32))
+    b.top_n_stride = 4
+    o = oracle.sample(b)
+    assert list(o["top_ids"][0]) == [17, 0, 1, 2]
+    assert list(o["status"]) == [0, 2, 0, 0]
+    assert list(o["top_ids"][2]) == [3, 9, -1, -1] and np.isneginf(o["top_logprobs"][2, 2:]).all()
+    assert abs(o["top_logprobs"][2, 0] - math.log(0.5)) < 1e-12
+    assert list(o["top_ids"][3]) == [0, 1, 2, 3]
+    assert abs(o["top_logprobs"][3, 0] - math.log(1 / 40)) < 1e-12

@@ -76,6 +76,8 @@ enum : int { kRowOk = 0, kRowOverflow = 1, kRowInvalid = 2 };
 enum : int { kRouteGreedy = 0, kRouteTopK = 1, kRouteMinP = 2, kRouteHeavy = 3 };
 enum : int { kFlagInvalid = 1, kFlagOverflow = 2 };
 
+constexpr int kTopNMax = 32;  // top-N logprobs: largest N per row
+
 struct Item {
   float z;  // transformed logit z'
   int id;   // token id
@@ -172,6 +174,7 @@ struct LaunchParams {
   int* poff;          // [B][C + 1] each slice's first entry
   PenEntry* pent;     // [B][kPenRowCap]
   int lists;          // the preparation launch wrote rinfo / poff / pent (penalties, bias or a mask)
+  Item* topn;         // [B * C][kTopNMax] each slice's most probable tokens (top-N logprobs)
 };
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -1992,6 +1995,104 @@ __device__ __noinline__ void finish_tids(const LaunchParams& P, int row, int sta
   }
 }
 
+// Top-N logprobs.  The order is "more probable first": y is monotone in z', so tokens are
+// ranked by z' descending and equal z' by id ascending -- a key no slice needs the row
+// max for.  Larger key = ranked earlier; 0 is never a token's key.
+__device__ __forceinline__ unsigned long long zid_key(float z, int id) {
+  uint32_t u = __float_as_uint(z == 0.0f ? 0.0f : z);  // -0 and +0 are one value
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((unsigned long long)u << 32) | (0xFFFFFFFFu - (uint32_t)id);
+}
+__device__ __forceinline__ Item key_item(unsigned long long k) {
+  uint32_t u = (uint32_t)(k >> 32);
+  u = (u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u;
+  return Item{__uint_as_float(u), (int)(0xFFFFFFFFu - (uint32_t)k)};
+}
+__device__ unsigned long long block_max_u64(unsigned long long v) {
+  __shared__ unsigned long long red[kWarps];
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const unsigned long long t = __shfl_xor_sync(~0u, v, o);
+    v = t > v ? t : v;
+  }
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  unsigned long long r = red[0];
+  for (int i = 1; i < kWarps; ++i) r = red[i] > r ? red[i] : r;
+  return r;
+}
+__device__ __forceinline__ bool top_n_ok(const LaunchParams& P, int N) {
+  return N >= 0 && N <= kTopNMax && N <= P.a.top_n_stride;
+}
+
+// Each slice CTA writes its N highest-ranked allowed tokens (N rounds of a block-wide
+// maximum below the previous one; z' = -inf marks an empty place) and flags the row
+// INVALID for an N out of range.
+__device__ __noinline__ void slice_top_n(const LaunchParams& P, const Smem& S, int row, int slice, int c0, int n) {
+  const int N = P.a.top_ns[row];
+  if (!top_n_ok(P, N)) {
+    if (threadIdx.x == 0) sh.rec.flags |= kFlagInvalid;
+    return;
+  }
+  Item* dst = P.topn + ((size_t)row * P.C + slice) * kTopNMax;
+  unsigned long long prev = ~0ull;
+  int r = 0;
+  for (; r < N; ++r) {
+    unsigned long long best = 0;
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+      const float z = S.buf[i];
+      if (z > -INFINITY) {
+        const unsigned long long k = zid_key(z, c0 + i);
+        if (k < prev && k > best) best = k;
+      }
+    }
+    best = block_max_u64(best);
+    if (!best) break;  // uniform: the slice has no more allowed tokens
+    if (threadIdx.x == 0) dst[r] = key_item(best);
+    prev = best;
+  }
+  for (int j = r + (int)threadIdx.x; j < N; j += kThreads) dst[j] = Item{-INFINITY, -1};
+}
+
+// Row end of the top-N outputs: the slices' lists are ranked together in shared memory
+// (each item's place = how many items rank above it) and the first N written with
+// logprob y - ln S; places past the row's allowed tokens get -1 / -inf, as does every
+// place of an INVALID row.
+__device__ __noinline__ void finish_top_n(const LaunchParams& P, const Smem& S, int row, int status, float m,
+                                          float invT, float lnS) {
+  const int N = P.a.top_ns[row];
+  if (!top_n_ok(P, N) || N == 0) return;  // nothing addressable (the row is INVALID) or wanted
+  int32_t* oid = P.a.top_ids + (size_t)row * P.a.top_n_stride;
+  float* olp = P.a.top_logprobs + (size_t)row * P.a.top_n_stride;
+  for (int j = threadIdx.x; j < N; j += kThreads) {
+    oid[j] = -1;
+    olp[j] = -INFINITY;
+  }
+  if (status == kRowInvalid) return;
+  const int C = P.C, tot = C * N;
+  Item* it = reinterpret_cast<Item*>(S.buf);  // free at a row end: the finisher's items come later
+  __syncthreads();
+  for (int t = threadIdx.x; t < tot; t += kThreads)
+    it[t] = ldcg_item(P.topn + ((size_t)row * C + t / N) * kTopNMax + t % N);
+  __syncthreads();
+  for (int t = threadIdx.x; t < tot; t += kThreads) {
+    const Item x = it[t];
+    if (!(x.z > -INFINITY)) continue;
+    const unsigned long long k = zid_key(x.z, x.id);
+    int rank = 0;
+    for (int u = 0; u < tot; ++u) {
+      const Item v = it[u];
+      rank += (v.z > -INFINITY && zid_key(v.z, v.id) > k) ? 1 : 0;
+    }
+    if (rank < N) {
+      oid[rank] = x.id;
+      olp[rank] = y_of(x.z, m, invT) - lnS;
+    }
+  }
+  __syncthreads();
+}
+
 // Finishes a row from its combined record (sh.row, sh.recs) and its items (candidates or
 // band), exactly: top-k count select, top-p mass select over the top-k set, min-p, race.
 template <bool kBF16>
@@ -2000,6 +2101,7 @@ __device__ void finish_row(const LaunchParams& P, const Smem& S, const RowParams
   const SliceRec R = sh.row;
   int status = row_status_of(R);
   if (P.a.tid_offs) finish_tids(P, row, status, R.m, q.invT, sh.lnS);
+  if (P.a.top_ns) finish_top_n(P, S, row, status, R.m, q.invT, sh.lnS);
   if (status == kRowInvalid) {
     if (threadIdx.x == 0) write_row(P.a, row, kRowInvalid, -1, -INFINITY, 0, -INFINITY);
     return;
@@ -2639,6 +2741,7 @@ __global__ void __launch_bounds__(kThreads, 3) sampler_kernel(const __grid_const
   const int n = min(P.a.V - c0, P.chunk);
   slice_front<kBF16>(P, S, q, row, slice, c0, n, sh.bulk);
   if (P.a.tid_offs) capture_tids(P, S, row, c0, n);
+  if (P.a.top_ns) slice_top_n(P, S, row, slice, c0, n);
   Above ab{0u, 0ull, 0ull, -INFINITY, 0.0f, INFINITY, INT_MAX, 0, 0.0f, 0.0f};
   const bool heavy = q.route == kRouteHeavy;
   if (heavy) heavy_slice(P, S, q, row, slice, c0, n, ab);
@@ -2738,7 +2841,7 @@ Geometry geometry_for(int vocab) {
 
 // Byte offsets of the scratch arrays for B rows of C slices of `chunk` tokens.
 struct ScratchLayout {
-  size_t ctl, order, rowctl, srec, bins, cand, spill, rinfo, poff, pent, rflag, total;
+  size_t ctl, order, rowctl, srec, bins, cand, spill, rinfo, poff, pent, rflag, topn, total;
 };
 
 constexpr size_t take(size_t& off, size_t bytes) {
@@ -2761,6 +2864,7 @@ constexpr ScratchLayout scratch_layout(size_t B, size_t C, size_t chunk, size_t 
   L.poff = take(off, B * (C + 1) * sizeof(int));
   L.pent = take(off, B * kPenRowCap * sizeof(PenEntry));
   L.rflag = take(off, B * sizeof(unsigned));
+  L.topn = take(off, B * C * kTopNMax * sizeof(Item));
   L.total = off;
   return L;
 }
@@ -2950,6 +3054,8 @@ int make_params(const Geometry& g, int vocab, int dev, const Scratch& sc, const 
   if (a->hist_offs && !a->hist_ids) return CLSAMPLE_ERR_NULL;
   if (a->bias_offs && (!a->bias_ids || !a->bias_vals)) return CLSAMPLE_ERR_NULL;
   if (a->tid_offs && (!a->tid_ids || !a->tid_logprobs)) return CLSAMPLE_ERR_NULL;
+  if (a->top_ns && (!a->top_ids || !a->top_logprobs)) return CLSAMPLE_ERR_NULL;
+  if (a->top_ns && a->top_n_stride < 1) return CLSAMPLE_ERR_STRIDE;
   if (a->logits_row_stride < a->V) return CLSAMPLE_ERR_STRIDE;
   if (a->bitmask && a->bitmask_row_stride < (a->V + 31) / 32) return CLSAMPLE_ERR_STRIDE;
   int cur = -1;
@@ -2975,6 +3081,7 @@ int make_params(const Geometry& g, int vocab, int dev, const Scratch& sc, const 
   P->poff = reinterpret_cast<int*>(b + L.poff);
   P->pent = reinterpret_cast<PenEntry*>(b + L.pent);
   P->rflag = reinterpret_cast<unsigned*>(b + L.rflag);
+  P->topn = reinterpret_cast<Item*>(b + L.topn);
   P->lists = (a->hist_offs || a->bias_offs || a->bitmask) ? 1 : 0;
   return CLSAMPLE_SUCCESS;
 }

@@ -40,6 +40,8 @@ class Args(ctypes.Structure):
         ("dbg_transformed", ctypes.c_void_p), ("dbg_kept_count", ctypes.c_void_p),
         ("dbg_cut", ctypes.c_void_p), ("logprobs_orig", ctypes.c_void_p), ("logprobs_kept", ctypes.c_void_p),
         ("tid_offs", ctypes.c_void_p), ("tid_ids", ctypes.c_void_p), ("tid_logprobs", ctypes.c_void_p),
+        ("top_ns", ctypes.c_void_p), ("top_n_stride", ctypes.c_int32), ("reserved1", ctypes.c_int32),
+        ("top_ids", ctypes.c_void_p), ("top_logprobs", ctypes.c_void_p),
     ]
 
 
@@ -160,7 +162,8 @@ class Sampler:
                   bias_offs=None, bias_ids=None, bias_vals=None, bitmask=None, seeds=None,
                   positions=None, step: int = 0, tokens=None, logprobs=None, row_status=None,
                   dbg_transformed=None, dbg_kept_count=None, dbg_cut=None, logprobs_orig=None,
-                  logprobs_kept=None, mode: int = 0, tid_offs=None, tid_ids=None, tid_logprobs=None) -> Args:
+                  logprobs_kept=None, mode: int = 0, tid_offs=None, tid_ids=None, tid_logprobs=None,
+                  top_ns=None, top_n_stride: int = 0, top_ids=None, top_logprobs=None) -> Args:
         if logits.dim() != 2 or logits.stride(1) != 1:
             raise ValueError("logits must be [B, V] with unit column stride")
         if logits.dtype == torch.float32:
@@ -213,6 +216,11 @@ class Sampler:
         a.tid_offs = _dptr(tid_offs, i32, B + 1, "tid_offs", dev)
         a.tid_ids = _dptr(tid_ids, i32, None, "tid_ids", dev)
         a.tid_logprobs = _dptr(tid_logprobs, f32, None, "tid_logprobs", dev)
+        a.top_ns = _dptr(top_ns, i32, B, "top_ns", dev)
+        a.top_n_stride = int(top_n_stride)
+        a.top_ids = _dptr(top_ids, i32, B * max(int(top_n_stride), 0), "top_ids", dev) if top_ids is not None else None
+        a.top_logprobs = (_dptr(top_logprobs, f32, B * max(int(top_n_stride), 0), "top_logprobs", dev)
+                          if top_logprobs is not None else None)
         return a
 
     def apply(self, args: Args, stream: Optional[torch.cuda.Stream] = None):
@@ -235,7 +243,8 @@ class Sampler:
         ``transformed`` [B, V], ``kept_count`` and ``cut``; with ``variants`` (or
         ``debug``) also ``logprobs_orig`` (T = 1) and ``logprobs_kept`` (renormalised
         over the kept set); with ``tid_offs``/``tid_ids`` (requested token ids, CSR)
-        also ``tid_logprobs``.  ``mode`` takes the MODE_* bits."""
+        also ``tid_logprobs``; with ``top_ns`` (and ``top_n_stride``, default 32) also
+        ``top_ids`` and ``top_logprobs`` [B, stride].  ``mode`` takes the MODE_* bits."""
         B, V = logits.shape
         dev = self.device
         out = {
@@ -250,6 +259,10 @@ class Sampler:
         if variants or debug:
             out["logprobs_orig"] = torch.empty(B, dtype=torch.float32, device=dev)
             out["logprobs_kept"] = torch.empty(B, dtype=torch.float32, device=dev)
+        if kw.get("top_ns") is not None:
+            stride = int(kw.setdefault("top_n_stride", 32))
+            out["top_ids"] = torch.empty(B, stride, dtype=torch.int32, device=dev)
+            out["top_logprobs"] = torch.empty(B, stride, dtype=torch.float32, device=dev)
         if kw.get("tid_offs") is not None:
             n = kw["tid_ids"].numel() if kw.get("tid_ids") is not None else 0
             out["tid_logprobs"] = torch.empty(max(n, 1), dtype=torch.float32, device=dev)[:n]
@@ -257,7 +270,8 @@ class Sampler:
                               row_status=out["status"], dbg_transformed=out.get("transformed"),
                               dbg_kept_count=out.get("kept_count"), dbg_cut=out.get("cut"),
                               logprobs_orig=out.get("logprobs_orig"), logprobs_kept=out.get("logprobs_kept"),
-                              tid_logprobs=out.get("tid_logprobs"), **kw)
+                              tid_logprobs=out.get("tid_logprobs"), top_ids=out.get("top_ids"),
+                              top_logprobs=out.get("top_logprobs"), **kw)
         self.apply(args, stream)
         return out
 
@@ -328,6 +342,9 @@ def batch_to_device(batch, device) -> Dict[str, object]:
               seeds=t(batch.seeds), positions=t(batch.positions), step=int(batch.step))
     if getattr(batch, "mode", 0):
         kw["mode"] = int(batch.mode)
+    if getattr(batch, "top_ns", None) is not None:
+        kw["top_ns"] = t(np.asarray(batch.top_ns, np.int32))
+        kw["top_n_stride"] = int(batch.top_n_stride or max(int(np.max(batch.top_ns)) if batch.B else 1, 1))
     if getattr(batch, "tid_offs", None) is not None:
         ids = np.asarray(batch.tid_ids, np.int32)
         # a device copy of an empty array may have no address: keep one padding slot

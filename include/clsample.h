@@ -135,6 +135,17 @@ enum {
  * tid_logprobs      f32[tid_offs[B]] output (required with tid_offs): ln p(id) under the
  *                   same distribution as `logprobs` (softmax(z'/T_eff), pre-truncation);
  *                   -inf for a masked id and for every id of an INVALID row.
+ * top_ns            i32[B] or NULL: N, the number of most probable tokens to report for
+ *                   row r (SGLang page, the output container's top logprobs); 0 <= N <=
+ *                   min(32, top_n_stride), else the row is INVALID.  Order: probability
+ *                   descending; y is monotone in z', so equal probabilities are ranked
+ *                   by z' descending, then by id ascending.
+ * top_n_stride      row stride (elements) of top_ids / top_logprobs, >= 1 with top_ns.
+ * top_ids           i32[B, top_n_stride] output (required with top_ns): places 0..N-1 of
+ *                   row r; -1 past the row's allowed tokens and for an INVALID row; places
+ *                   N.. untouched.
+ * top_logprobs      f32[B, top_n_stride] output (required with top_ns): ln p of those
+ *                   tokens under softmax(z'/T_eff) (pre-truncation); -inf where the id is -1.
  *
  * Limits: V <= 262144 (at most 18 slices of at most 15360 tokens per row).  Any number
  * of penalised, biased or allowed tokens is handled exactly.  A row whose candidate set
@@ -176,6 +187,11 @@ typedef struct {
   const int32_t* tid_offs;
   const int32_t* tid_ids;
   float* tid_logprobs;
+  const int32_t* top_ns;
+  int32_t top_n_stride;
+  int32_t reserved1;
+  int32_t* top_ids;
+  float* top_logprobs;
 } clsample_args_t;
 
 /* Creates a handle for batches of up to max_batch rows over a vocabulary of `vocab`

@@ -11,7 +11,8 @@ Acceptance bar (element by element):
   * logprob of the drawn token: within 1e-5 absolute; so are the drawn token's logprob
     under the original (T = 1, untruncated) distribution and under the kept set, where
     both sides report them; so are the logprobs of requested token ids (with the same
-    -inf pattern: masked ids and every id of an INVALID row).
+    -inf pattern: masked ids and every id of an INVALID row), and the top-N lists (ids
+    exact, logprobs within 1e-5).
 """
 import numpy as np
 import torch
@@ -80,5 +81,16 @@ def compare(batch, g, o, name="", max_ambiguous_frac=1e-3):
         err = np.abs(gv[fin] - ov[fin])
         assert (err <= LOGPROB_TOL).all(), (name, "tid_logprobs", float(err.max()) if err.size else 0.0)
         assert np.all(np.isneginf(gv[~ok[owner]])), (name, "tid_logprobs of invalid rows")
+    if "top_ids" in g and "top_ids" in o:
+        N = np.asarray(batch.top_ns)
+        for r in range(B):
+            n = int(N[r])
+            if not (0 <= n <= min(32, o["top_ids"].shape[1])):
+                continue
+            assert np.array_equal(g["top_ids"][r, :n], o["top_ids"][r, :n]), (name, "top_ids", r)
+            gv, ov = g["top_logprobs"][r, :n].astype(np.float64), o["top_logprobs"][r, :n]
+            assert np.array_equal(np.isneginf(gv), np.isneginf(ov)), (name, "top -inf pattern", r)
+            fin = np.isfinite(ov)
+            assert (np.abs(gv[fin] - ov[fin]) <= LOGPROB_TOL).all(), (name, "top_logprobs", r)
     return {"ambiguous": n_amb, "max_logprob_err": float(lp_err.max()) if lp_err.size else 0.0,
             "mismatch_ambiguous": int((amb & ~same).sum())}

@@ -498,3 +498,26 @@ def test_minus_inf_bias_parity():
     assert (g["tokens"][ok] != o0["tokens"][ok]).all()
     assert not np.isin(g["tokens"][ok], [7, 70000]).any()
     assert n0.sum() > 0
+
+
+@pytest.mark.parametrize("w,B,V", [(2, 40, 151936), (3, 32, 70001), (5, 48, 30011), (1, 4, 32000)])
+def test_top_n_logprobs_parity(w, B, V):
+    """Top-N logprobs: ids bit-exact (order: z' descending, then id), logprobs within 1e-5,
+    -1 / -inf past the allowed tokens; N = 33 makes its row INVALID; places past N stay
+    untouched."""
+    b = make_workload(w, B=B, V=V)
+    rng = np.random.default_rng(w)
+    b.top_ns = rng.choice([0, 1, 3, 8, 20, 32], size=B).astype(np.int32)
+    b.top_ns[min(2, B - 1)] = 33
+    b.top_n_stride = 33
+    g, o = run_gpu(b), run_oracle(b)
+    assert g["status"][min(2, B - 1)] == 2
+    compare(b, g, o, f"top-n w{w}")
+    # a bitmask that leaves one row two tokens: the rest of its list is -1 / -inf
+    if b.bitmask is not None:
+        r = int(np.argmax(b.top_ns * (b.top_ns <= 32)))
+        b.bitmask[r] = 0
+        b.bitmask[r, 0] = 0b101
+        g, o = run_gpu(b), run_oracle(b)
+        compare(b, g, o, f"top-n short w{w}")
+        assert list(g["top_ids"][r, :3]) in ([0, 2, -1], [2, 0, -1])

@@ -140,20 +140,23 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_baseline(batch, sample_rows, repeats):
-    """The oracle as it stands, on the host cores, on a bounded sample of the batch."""
+def cpu_baseline(batch, sample_rows, min_repeats=3, min_seconds=1.0, max_repeats=40):
+    """The oracle as it stands, on the host cores, on a bounded sample of the batch:
+    whole passes over the sample until about `min_seconds` of wall time (10-30 s of
+    CPU work on a many-core host), at least `min_repeats` of them."""
     from oracle import oracle as O
     sub = batch.rows(range(min(sample_rows, batch.B)))
     O.sample(sub, nthreads=0, want_transformed=False)  # warm-up (page-in, thread start)
     t0 = time.perf_counter()
-    threads = 1
-    for _ in range(repeats):
+    threads, repeats = 1, 0
+    while repeats < min_repeats or (time.perf_counter() - t0 < min_seconds and repeats < max_repeats):
         threads = O.sample(sub, nthreads=0, want_transformed=False)["threads"]
+        repeats += 1
     dt = time.perf_counter() - t0
     rows = sub.B * repeats
     return {"value": rows / dt, "unit": "rows/s", "cores": int(threads), "kind": "oracle",
             "sample": f"{sub.B} rows of workload {batch.name} (B={batch.B}, V={batch.V}) x {repeats} repeats, "
-                      f"{dt:.2f} s wall on {threads} threads"}
+                      f"{dt:.2f} s wall on {threads} threads (about {dt * threads:.0f} s of CPU work)"}
 
 
 def run_reference(args, rank, world):
@@ -406,7 +409,7 @@ def main():
         "e2e": e2e,
     }
     if not args.no_cpu:
-        line["cpu_baseline"] = cpu_baseline(b, sample_rows=b.B, repeats=3)
+        line["cpu_baseline"] = cpu_baseline(b, sample_rows=b.B)
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

@@ -52,8 +52,9 @@
 #include <mutex>
 
 #include "clsample.h"
-#include "cluster_sync.cuh"
+#include "bulk_copy.cuh"
 #include "sampler_math.cuh"
+#include "stream.h"
 
 namespace {
 
@@ -1671,20 +1672,6 @@ __device__ void block_race(float& s, int& id, float& y) {
   __syncthreads();
 }
 
-// Fast race score: y - ln(-ln U) with hardware logarithms, -ln U by its series where U is
-// close to 1 (1 - U is exact there).  Within about 1e-4 of race_score for every U the
-// Philox layout produces; a token pays for the exact score only if its fast score is
-// within kFastTol of the best exact score so far.
-constexpr float kFastTol = 1e-3f;
-// Largest race bonus -ln(-ln U) over the uniforms Philox words give: U <= 1 - 2^-24,
-// so -ln U >= 5.96e-8 and the bonus is at most 16.636.
-constexpr float kGumbelMax = 16.7f;
-__device__ __forceinline__ float fast_race(float y, uint32_t x) {
-  const float u = word_to_uniform(x);
-  const float d = 1.0f - u;
-  const float e = d < 0.125f ? d * (1.0f + d * (0.5f + d * (0.33333334f + d * (0.25f + d * 0.2f)))) : -__logf(u);
-  return y - __logf(e);
-}
 
 // z' of token `tok` among the row's items (the global candidate / band segments, which
 // hold z'); the caller knows the token is one of them.  Block-wide.
@@ -2696,7 +2683,8 @@ __global__ void __launch_bounds__(kThreads, 3) sampler_kernel(const __grid_const
     // the order may still be in the making
     const unsigned item = atomicAdd(&P.ctl[0], 1u);
     sh.flag = wait_flag(&P.ctl[2], 1u);
-    sh.row_id = __ldcg(P.order + item / (unsigned)C);
+    // without the order (the wait gave up) the item's own row, which is below B, stands in
+    sh.row_id = sh.flag ? __ldcg(P.order + item / (unsigned)C) : (int)(item / (unsigned)C);
     sh.slice = (int)(item % (unsigned)C);
     sh.bar_uses = 0;
   }
@@ -2924,22 +2912,28 @@ struct clsample_handle {
   int device;
   Geometry g;
   Scratch sc;
-  int grid[2];  // resident CTAs for f32 and bf16 logits
+  int grid[2];                // resident CTAs of the slice-resident kernel for f32 and bf16 logits
+  unsigned char* stream_base; // scratch of the streaming sampler
+  int stream_grid;            // its persistent grid
 };
 
 namespace {
 
 // Scratch of clsample_apply_static: a fixed device array compiled into the library
 // (every device that loads the library holds it until the process exits), sized for
-// kStaticRows rows of the longest slices and kStaticSpill spill rows.
+// kStaticRows rows of the longest slices and kStaticSpill spill rows of the
+// slice-resident kernel, followed by the streaming sampler's scratch for kStaticRows rows
+// of the largest vocabulary.
 constexpr int kStaticRows = 64;
 constexpr int kStaticSpill = 4;
 constexpr size_t kStaticBytes = scratch_layout(kStaticRows, kMaxSlices, kSliceMax, kStaticSpill).total;
-static __device__ __align__(256) unsigned char g_static_scratch[kStaticBytes];
+constexpr size_t kStaticStreamBytes = (size_t)28 << 20;  // checked against the layout at set-up
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticBytes + kStaticStreamBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_static_mutex;
 unsigned char* g_static_base[kMaxDevices];  // the array's device address on each device, once set up
+int g_static_grid[kMaxDevices];             // the streaming sampler's grid on each device
 
 // The static scratch of device `dev`: on the first call for a device (with that device
 // current) the kernels are set up and the array's device address is looked up with
@@ -2953,6 +2947,12 @@ unsigned char* static_scratch(int dev, int* rc) {
   if (!g_static_base[dev]) {
     *rc = setup_device(dev);
     if (*rc != CLSAMPLE_SUCCESS) return nullptr;
+    *rc = clsample_stream::setup(dev, &g_static_grid[dev]);
+    if (*rc != CLSAMPLE_SUCCESS) return nullptr;
+    if (clsample_stream::scratch_bytes(kStaticRows, kMaxVocab) > kStaticStreamBytes) {
+      *rc = CLSAMPLE_ERR_CUDA;
+      return nullptr;
+    }
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) {
       *rc = CLSAMPLE_ERR_CUDA;
@@ -3026,6 +3026,24 @@ int clsample_create(int32_t max_batch, int32_t vocab, clsample_t** out) {
   h->sc = Scratch{max_batch, g.C, g.chunk, spill_rows, base};
   h->grid[0] = grid[0];
   h->grid[1] = grid[1];
+  h->stream_base = nullptr;
+  h->stream_grid = 0;
+  if ((rc = clsample_stream::setup(dev, &h->stream_grid)) != CLSAMPLE_SUCCESS) {
+    cudaFree(base);
+    delete h;
+    return rc;
+  }
+  if (max_batch > 0) {
+    const size_t bytes = clsample_stream::scratch_bytes(max_batch, vocab);
+    void* p = nullptr;
+    if (cudaMalloc(&p, bytes) != cudaSuccess || cudaMemset(p, 0, bytes) != cudaSuccess) {
+      if (p) cudaFree(p);
+      cudaFree(base);
+      delete h;
+      return CLSAMPLE_ERR_CUDA;
+    }
+    h->stream_base = static_cast<unsigned char*>(p);
+  }
   *out = h;
   return CLSAMPLE_SUCCESS;
 }
@@ -3033,6 +3051,7 @@ int clsample_create(int32_t max_batch, int32_t vocab, clsample_t** out) {
 void clsample_destroy(clsample_t* h) {
   if (!h) return;
   if (h->sc.base) cudaFree(h->sc.base);
+  if (h->stream_base) cudaFree(h->stream_base);
   delete h;
 }
 
@@ -3128,6 +3147,8 @@ int clsample_apply(clsample_t* h, const clsample_args_t* a, clsample_stream_t st
   const int rc = make_params(h, a, &P);
   if (rc != CLSAMPLE_SUCCESS || a->B == 0) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (clsample_stream::serves(a))
+    return clsample_stream::launch(a, h->stream_base, h->max_batch, h->stream_grid, st);
   const int ro = launch_order(P, st);
   return ro != CLSAMPLE_SUCCESS ? ro : launch_sampler(h->g, P, st);
 }
@@ -3136,6 +3157,7 @@ int clsample_prepare(clsample_t* h, const clsample_args_t* a, clsample_stream_t 
   LaunchParams P;
   const int rc = make_params(h, a, &P);
   if (rc != CLSAMPLE_SUCCESS || a->B == 0) return rc;
+  if (clsample_stream::serves(a)) return CLSAMPLE_SUCCESS;  // the streaming sampler has no preparation launch
   return launch_order(P, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -3143,7 +3165,10 @@ int clsample_sample(clsample_t* h, const clsample_args_t* a, clsample_stream_t s
   LaunchParams P;
   const int rc = make_params(h, a, &P);
   if (rc != CLSAMPLE_SUCCESS || a->B == 0) return rc;
-  return launch_sampler(h->g, P, reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (clsample_stream::serves(a))
+    return clsample_stream::launch(a, h->stream_base, h->max_batch, h->stream_grid, st);
+  return launch_sampler(h->g, P, st);
 }
 
 int clsample_apply_static(const clsample_args_t* a, clsample_stream_t stream) {
@@ -3162,6 +3187,9 @@ int clsample_apply_static(const clsample_args_t* a, clsample_stream_t stream) {
   rc = make_params(g, a->V, dev, sc, a, &P);
   if (rc != CLSAMPLE_SUCCESS || a->B == 0) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (clsample_stream::serves(a)) {
+    return clsample_stream::launch(a, base + kStaticBytes, kStaticRows, g_static_grid[dev], st);
+  }
   rc = launch_order(P, st);
   return rc != CLSAMPLE_SUCCESS ? rc : launch_sampler(g, P, st);
 }

@@ -7,7 +7,7 @@ import pytest
 
 from constrained_logits_sampling_gb300.workloads import Batch, make_workload, round_to_bf16_bits
 
-from parity import compare, run_gpu, run_oracle
+from parity import LOGPROB_TOL, RACE_REL, compare, run_gpu, run_oracle
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -303,27 +303,23 @@ def test_history_beyond_the_preparation_hash():
     compare(b, run_gpu(b), run_oracle(b), name="long history")
 
 
-def test_spill_pool_exhaustion_reports_overflow():
-    """Flat rows under top-k put every token of every slice into the row's candidates,
-    which spill; once the handle's spill rows are used up the remaining such rows report
-    OVERFLOW (token -1 is not required: the status says the result is not to be used) and
-    every other row still matches the oracle."""
+def test_flat_topk_rows_are_exact():
+    """Flat rows under top-k keep every token (all tie with the k-th largest): more ties
+    than a slice's candidate area holds.  Such rows leave the candidate route for the
+    binned general route; every one of them, and every other row, matches the oracle
+    with status OK (more such rows than a small handle's batch, on a 24-row handle)."""
     from constrained_logits_sampling_gb300.sampler import Sampler
     V = 151936
     B = 24
     rng = np.random.default_rng(33)
     z = (rng.standard_normal((B, V)) * 3).astype(F32)
-    z[:20] = 0.0  # 20 flat rows, more than the 16 spill rows of a small handle
+    z[:20] = 0.0  # 20 flat rows
     b = small(z, temperatures=np.ones(B, F32), top_ks=np.full(B, 50, np.int32),
               positions=np.arange(B, dtype=np.int64))
     g = run_gpu(b, sampler=Sampler(B, V))
     o = run_oracle(b)
-    st = g["status"]
-    assert set(np.unique(st[:20])) <= {0, 1} and (st[:20] == 1).sum() >= 1
-    assert np.all(st[20:] == 0)
-    ok = st == 0
-    assert np.array_equal(g["tokens"][ok], o["tokens"][ok])
-    assert np.array_equal(g["kept_count"][ok], o["kept_count"][ok])
+    assert np.all(g["status"] == 0)
+    compare(b, g, o, name="flat top-k rows")
 
 
 def test_prepare_then_sample_equals_apply():
@@ -372,11 +368,18 @@ def test_logprob_variants_on_request(w):
         assert np.array_equal(a.view(np.uint32) if a.dtype == np.float32 else a,
                               c.view(np.uint32) if c.dtype == np.float32 else c), k
     o = run_oracle(b, want_transformed=False)
-    ok = (o["status"] == 0) & (var["tokens"] == o["tokens"])
-    assert ok.sum() >= b.B - 1
+    assert np.array_equal(var["status"], o["status"])
+    ok = o["status"] == 0
+    # the same bar as every parity test: tokens equal except ambiguous race rows
+    gap, best = o["race_gap"], o["race_best"]
+    amb = ok & np.isfinite(gap) & np.isfinite(best) & (gap <= RACE_REL * np.maximum(1.0, np.abs(best)))
+    same = var["tokens"] == o["tokens"]
+    assert not np.any(ok & ~same & ~amb), np.nonzero(ok & ~same & ~amb)
+    assert amb.sum() <= max(int(1e-3 * b.B), 0) or amb.sum() == 0
+    rows = ok & same
     for k in ("logprobs_orig", "logprobs_kept"):
-        err = np.abs(var[k][ok].astype(np.float64) - o[k][ok])
-        assert (err <= 1e-5).all(), (k, float(err.max()))
+        err = np.abs(var[k][rows].astype(np.float64) - o[k][rows])
+        assert (err <= LOGPROB_TOL).all(), (k, float(err.max()))
 
 
 def _requests(b, per_row, seed, bad_row=None):

@@ -77,15 +77,17 @@ constexpr int kEntStage = 128;          // of which the producer copies into sha
 constexpr int kBins = 64;
 constexpr int kNQ = 16;                 // consumer -> coordinator notices
 constexpr int kLightK = 1024;           // top-k rows with k <= this finish from candidates
-constexpr int kLead = 16;               // rows whose lists are prepared ahead of their slices
+constexpr int kLead = 32;               // rows whose lists are prepared ahead of their slices
 constexpr int kMaxRounds = 12;          // bin passes per row before it reports OVERFLOW
 constexpr int kPrepSlots = 4096;        // a preparation task's hash (8-byte slots in its buffer)
 constexpr int kPrepMax = 3072;          // distinct listed tokens of a row before the slow path
 constexpr uint32_t kPolls = 1u << 22;   // bounded polls (about a second with the naps)
+constexpr int kMaxGrid = 1024;          // persistent CTAs at most (the grid is capped to this)
 
 static_assert(kMaxC <= 32, "one slice per coordinator lane");
 static_assert(kPrepSlots * 8 <= kBuf, "the preparation hash fits a ring buffer");
 static_assert(kVPT * 4 * kCT == kSL, "whole vectors per thread");
+static_assert(kMW + kCT >= 512, "the row end's digit masses fit the slice scratch");
 
 enum : uint32_t { kP1 = 0, kP2 = 1, kP3 = 2, kFin = 3, kPrep = 4, kExit = 7 };
 __host__ __device__ constexpr uint32_t tcode(uint32_t ph, uint32_t slice) { return ph | (slice << 4); }
@@ -239,8 +241,13 @@ struct __align__(16) Sm {
   uint32_t nrow[kNQ], ncode[kNQ];
   alignas(16) unsigned mask[kNB][kMW];  // bulk-copy destinations: 16-byte aligned
   alignas(16) Ent ents[kNB][kEntStage];
-  unsigned claim[kMW];
-  unsigned tkey[kCT];
+  union {
+    struct {
+      unsigned claim[kMW];  // slice tasks: listed tokens
+      unsigned tkey[kCT];   // slice tasks: per-thread maxima
+    };
+    unsigned long long hmass[256];  // row end: masses per radix digit
+  };
   unsigned bcnt[kBins], bcm[kBins], bshift[kBins];
   unsigned hist[256];
   float rf[kCW * 2];
@@ -485,13 +492,14 @@ __device__ int row_rank(const clsample_args_t& a, int row) {
   return p < 1.0f ? kClsTopP : kClsGen;
 }
 
-// Candidates a light row's slice keeps at least (the rest of its top-k share is checked
-// at the row end when this is below k).
-__device__ __forceinline__ int light_q(int k, int masked, int n, int V) {
-  const int q = min(k, 256);
-  if (masked) return q;
+// Candidates a light row's slice keeps at least: 1.5 times its expected share of the
+// top-k set plus 10, at most 256 (the warps' sorted per-thread maxima give the bound).
+// Whether they hold the slice's whole part of the top-k set is checked at the row end;
+// rows whose top tokens crowd into few slices (a contiguous grammar range) fail the
+// check and take the general route.
+__device__ __forceinline__ int light_q(int k, int n, int V) {
   const float share = (float)n / (float)V;
-  return min(q, (int)ceilf(1.5f * (float)k * share) + 10);
+  return min(min(k, 256), (int)ceilf(1.5f * (float)k * share) + 10);
 }
 
 // ---------------------------------------------------------------- list order (all threads)
@@ -567,9 +575,11 @@ __device__ void static_task(const KP& P, unsigned i, uint32_t* row, uint32_t* co
 
 // ---------------------------------------------------------------- task queue
 
-// Entries per CTA queue: every CTA owns an equal segment of the queue area; entry t of
-// the launch goes to CTA t % grid, at position t / grid of its segment.
-__device__ __forceinline__ unsigned queue_seg(const KP& P) { return (P.dq_cap + gridDim.x - 1) / gridDim.x; }
+// Entries per CTA queue: every CTA owns an equal segment of the queue area (the area
+// holds at least kMaxGrid entries more than the launch can push, so the rounded-down
+// segment still fits every CTA's share); entry t of the launch goes to CTA t % grid, at
+// position t / grid of its segment.
+__device__ __forceinline__ unsigned queue_seg(const KP& P) { return P.dq_cap / gridDim.x; }
 
 // Appends C tasks (slices 0..C-1 of `ph`) or one task (slice 0) for `row`; single thread.
 // The caller's earlier writes (row state, zeroed accumulators) are published first.
@@ -788,7 +798,8 @@ __device__ int slice_front(const KP& P, const Desc& d, int st, float* buf, unsig
   cbar();
   int ninf = 0;
   if (P.lists) {
-    if (d.rflags & kFSlow) {
+    const unsigned rfl = d.rflags;
+    if (rfl & kFSlow) {
       ninf = slow_transforms(P, d, buf, mw, bad);
     } else {
       const Ent* g = P.ent + ((size_t)d.row * P.C + d.slice) * kEnt;
@@ -851,8 +862,7 @@ __device__ void task_p1(const KP& P, const Desc& d, int st, float* buf) {
   const clsample_args_t& a = P.a;
   const int row = d.row, n = d.n, c0 = d.c0;
   const Params& q = d.q;
-  const bool need_stats = q.cls != kClsInvalid;
-  if (!need_stats && !a.dbg_transformed) {
+  if (q.cls == kClsInvalid && !a.dbg_transformed) {
     if (threadIdx.x == 0) {
       Rec1 r{-INFINITY, INT_MAX, 0.0f, 0.0f, 0, -INFINITY, 0, kFInvalid};
       P.r1[(size_t)row * P.C + d.slice] = r;
@@ -860,77 +870,92 @@ __device__ void task_p1(const KP& P, const Desc& d, int st, float* buf) {
     return;
   }
   unsigned bad = 0;
-  int ninf = slice_front(P, d, st, buf, &bad);
+  const int ninf = slice_front(P, d, st, buf, &bad);
   const unsigned* mw = P.masked ? sm.mask[st] : nullptr;
   const int nv = (n + 3) >> 2;
   const uint32_t tail = (n & 3) ? ((1u << (n & 3)) - 1u) : 0xFu;
   const float c = __fmul_rn(1.4426950408889634f, q.invT);
-  const bool t1 = P.want_orig;
-  float tmax = -INFINITY, tsum = 0.0f, tsum1 = 0.0f, chk = 0.0f;
-  int tf = INT_MAX, nal = 0;
-#pragma unroll 4
+  constexpr float l2e = 1.4426950408889634f;
+  float4* b4 = reinterpret_cast<float4*>(buf);
+  // the thread's vectors in registers: masked tokens and the slice end become -inf (and
+  // are written back for the candidate and debug outputs); a running sum of the raw
+  // values detects non-finite input
+  float4 v[kVPT];
+  float chk0 = 0.0f, chk1 = 0.0f;
+  int nal = 0;
+#pragma unroll
   for (int u = 0; u < kVPT; ++u) {
     const int f = threadIdx.x + u * kCT;
-    if (f >= nv) break;
-    const float4 raw = reinterpret_cast<const float4*>(buf)[f];
-    chk += (raw.x + raw.y) + (raw.z + raw.w);
-    uint32_t bits = mask_nibble(mw, f);
-    if (f == nv - 1) bits &= tail;
-    nal += __popc(bits);
-    const float4 v = masked_vec(buf, mw, f, nv, tail);
-    const float a4 = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
-    if (a4 > tmax) {
-      if (tmax > -INFINITY) {
-        tsum *= ex2_approx((tmax - a4) * c);
-        if (t1) tsum1 *= ex2_approx((tmax - a4) * 1.4426950408889634f);
+    float4 x = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    if (f < nv) {
+      x = b4[f];
+      if (u & 1) chk1 += (x.x + x.y) + (x.z + x.w);
+      else chk0 += (x.x + x.y) + (x.z + x.w);
+      uint32_t bits = mask_nibble(mw, f);
+      if (f == nv - 1) bits &= tail;
+      nal += __popc(bits);
+      if (bits != 0xFu) {
+        if (!(bits & 1u)) x.x = -INFINITY;
+        if (!(bits & 2u)) x.y = -INFINITY;
+        if (!(bits & 4u)) x.z = -INFINITY;
+        if (!(bits & 8u)) x.w = -INFINITY;
+        b4[f] = x;
       }
-      tmax = a4;
-      tf = f;
     }
-    if (tmax > -INFINITY) {
-      tsum += (ex2_approx((v.x - tmax) * c) + ex2_approx((v.y - tmax) * c)) +
-              (ex2_approx((v.z - tmax) * c) + ex2_approx((v.w - tmax) * c));
-      if (t1)
-        tsum1 += (ex2_approx((v.x - tmax) * 1.4426950408889634f) + ex2_approx((v.y - tmax) * 1.4426950408889634f)) +
-                 (ex2_approx((v.z - tmax) * 1.4426950408889634f) + ex2_approx((v.w - tmax) * 1.4426950408889634f));
-    }
+    v[u] = x;
   }
   nal -= ninf;
-  const int nonfinite = cbar_or(!(fabsf(chk) < INFINITY));
+  const int nonfinite = cbar_or(!(fabsf(chk0 + chk1) < INFINITY));
   if (nonfinite) {
     checked_walk(P, d, st, buf);
-    tmax = -INFINITY;
-    tsum = tsum1 = 0.0f;
-    tf = INT_MAX;
     nal = 0;
+#pragma unroll
     for (int u = 0; u < kVPT; ++u) {
       const int f = threadIdx.x + u * kCT;
-      if (f >= nv) break;
-      const float4 v = reinterpret_cast<const float4*>(buf)[f];
-      nal += (v.x > -INFINITY) + (v.y > -INFINITY) + (v.z > -INFINITY) + (v.w > -INFINITY);
-      const float a4 = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
-      if (a4 > tmax) {
-        if (tmax > -INFINITY) {
-          tsum *= ex2_approx((tmax - a4) * c);
-          if (t1) tsum1 *= ex2_approx((tmax - a4) * 1.4426950408889634f);
-        }
-        tmax = a4;
-        tf = f;
+      v[u] = f < nv ? b4[f] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      nal += (v[u].x > -INFINITY) + (v[u].y > -INFINITY) + (v[u].z > -INFINITY) + (v[u].w > -INFINITY);
+    }
+  }
+  // the thread's max, its first vector reaching it, then the sums against it
+  float vm[kVPT];
+  float tmax = -INFINITY;
+#pragma unroll
+  for (int u = 0; u < kVPT; ++u) {
+    vm[u] = fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w));
+    tmax = fmaxf(tmax, vm[u]);
+  }
+  int tf = INT_MAX;
+#pragma unroll
+  for (int u = kVPT - 1; u >= 0; --u)
+    if (vm[u] == tmax) tf = threadIdx.x + u * kCT;
+  float tsum = 0.0f, tsum1 = 0.0f;
+  if (tmax > -INFINITY) {
+    float p0 = 0.0f, p1 = 0.0f, p2 = 0.0f, p3 = 0.0f;
+#pragma unroll
+    for (int u = 0; u < kVPT; ++u) {
+      p0 += ex2_approx((v[u].x - tmax) * c);
+      p1 += ex2_approx((v[u].y - tmax) * c);
+      p2 += ex2_approx((v[u].z - tmax) * c);
+      p3 += ex2_approx((v[u].w - tmax) * c);
+    }
+    tsum = (p0 + p1) + (p2 + p3);
+    if (P.want_orig) {
+      p0 = p1 = p2 = p3 = 0.0f;
+#pragma unroll
+      for (int u = 0; u < kVPT; ++u) {
+        p0 += ex2_approx((v[u].x - tmax) * l2e);
+        p1 += ex2_approx((v[u].y - tmax) * l2e);
+        p2 += ex2_approx((v[u].z - tmax) * l2e);
+        p3 += ex2_approx((v[u].w - tmax) * l2e);
       }
-      if (tmax > -INFINITY) {
-        tsum += (ex2_approx((v.x - tmax) * c) + ex2_approx((v.y - tmax) * c)) +
-                (ex2_approx((v.z - tmax) * c) + ex2_approx((v.w - tmax) * c));
-        if (t1)
-          tsum1 += (ex2_approx((v.x - tmax) * 1.4426950408889634f) + ex2_approx((v.y - tmax) * 1.4426950408889634f)) +
-                   (ex2_approx((v.z - tmax) * 1.4426950408889634f) + ex2_approx((v.w - tmax) * 1.4426950408889634f));
-      }
+      tsum1 = (p0 + p1) + (p2 + p3);
     }
   }
   sm.tkey[threadIdx.x] = tmax > -INFINITY ? fkey(tmax) : 0u;
   int arg = INT_MAX;
   if (tf != INT_MAX && tmax > -INFINITY) {
-    const float4 v = reinterpret_cast<const float4*>(buf)[tf];
-    const int j = v.x == tmax ? 0 : v.y == tmax ? 1 : v.z == tmax ? 2 : 3;
+    const float4 x = b4[tf];
+    const int j = x.x == tmax ? 0 : x.y == tmax ? 1 : x.z == tmax ? 2 : 3;
     arg = c0 + 4 * tf + j;
   }
   // combine: (max, lowest argmax) by 64-bit keys, then the sums rescaled to the max
@@ -946,7 +971,7 @@ __device__ void task_p1(const KP& P, const Desc& d, int st, float* buf) {
   for (int i = 1; i < kCW; ++i) bk = max(bk, sm.ru[i]);
   const float M = bk ? key_to_float((uint32_t)(bk >> 32)) : -INFINITY;
   float ws = (M > -INFINITY && tmax > -INFINITY) ? tsum * ex2_approx((tmax - M) * c) : 0.0f;
-  float ws1 = (t1 && M > -INFINITY && tmax > -INFINITY) ? tsum1 * ex2_approx((tmax - M) * 1.4426950408889634f) : 0.0f;
+  float ws1 = (P.want_orig && M > -INFINITY && tmax > -INFINITY) ? tsum1 * ex2_approx((tmax - M) * l2e) : 0.0f;
   ws = warp_sum(ws);
   ws1 = warp_sum(ws1);
   if (lane == 0) {
@@ -972,12 +997,25 @@ __device__ void task_p1(const KP& P, const Desc& d, int st, float* buf) {
   rec.bound = -INFINITY;
   rec.ncand = 0;
   if (a.dbg_transformed) {
-    float* dst = a.dbg_transformed + (long long)row * a.V + c0;
-    for (int l = threadIdx.x; l < n; l += kCT) dst[l] = buf[l];
+    float4* dst = reinterpret_cast<float4*>(a.dbg_transformed + (long long)row * a.V + c0);
+    const bool vec = ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0) && (n % 4 == 0);
+#pragma unroll
+    for (int u = 0; u < kVPT; ++u) {
+      const int f = threadIdx.x + u * kCT;
+      if (vec) {
+        if (f < nv) dst[f] = v[u];
+      } else {
+        float* d1 = a.dbg_transformed + (long long)row * a.V + c0;
+        const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (4 * f + j < n) d1[4 * f + j] = e[j];
+      }
+    }
   }
   if ((q.cls == kClsLight || q.cls == kClsBigK) && M > -INFINITY) {
     // candidate superset of the slice's part of the top-k set
-    const int qn = light_q(q.k, P.masked, n, a.V);
+    const int qn = light_q(q.k, n, a.V);
     uint32_t bkey = 0u;  // 0: take every candidate
     if (rec.nal > qn) {
       uint32_t kk = sm.tkey[threadIdx.x];
@@ -1001,17 +1039,13 @@ __device__ void task_p1(const KP& P, const Desc& d, int st, float* buf) {
     if (threadIdx.x == 0) sm.ci[0] = 0;
     cbar();
     Item* dst = P.cand + ((size_t)row * P.C + d.slice) * kCand;
-    const bool active = sm.tkey[threadIdx.x] >= bkey && sm.tkey[threadIdx.x] != 0u;
-    // per thread: count, warp-aggregated slot, then write
+    // per thread: count, warp-aggregated slot, then write (from the registers)
     int mine = 0;
-    if (active) {
-      for (int u = 0; u < kVPT; ++u) {
-        const int f = threadIdx.x + u * kCT;
-        if (f >= nv) break;
-        const float4 v = reinterpret_cast<const float4*>(buf)[f];
-        mine += (v.x >= bound && v.x > -INFINITY) + (v.y >= bound && v.y > -INFINITY) +
-                (v.z >= bound && v.z > -INFINITY) + (v.w >= bound && v.w > -INFINITY);
-      }
+    if (tmax > -INFINITY && tmax >= bound) {
+#pragma unroll
+      for (int u = 0; u < kVPT; ++u)
+        mine += (v[u].x >= bound && v[u].x > -INFINITY) + (v[u].y >= bound && v[u].y > -INFINITY) +
+                (v[u].z >= bound && v[u].z > -INFINITY) + (v[u].w >= bound && v[u].w > -INFINITY);
     }
     int incl = mine;
 #pragma unroll
@@ -1024,11 +1058,10 @@ __device__ void task_p1(const KP& P, const Desc& d, int st, float* buf) {
     base = __shfl_sync(~0u, base, 31) + incl - mine;
     if (mine) {
       int pos = base;
+#pragma unroll
       for (int u = 0; u < kVPT; ++u) {
         const int f = threadIdx.x + u * kCT;
-        if (f >= nv) break;
-        const float4 v = reinterpret_cast<const float4*>(buf)[f];
-        const float e[4] = {v.x, v.y, v.z, v.w};
+        const float e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           if (e[j] >= bound && e[j] > -INFINITY) {
@@ -1328,40 +1361,141 @@ __device__ void task_prep(const KP& P, const Desc& d, float* buf) {
 
 // ---------------------------------------------------------------- row end (consumers)
 
-// Bitonic sort, descending, of n 64-bit keys in `x` (padded with zeros to a power of two).
-__device__ int sort_desc(unsigned long long* x, int n) {
-  int N = 1;
-  while (N < n) N <<= 1;
-  for (int i = n + threadIdx.x; i < N; i += kCT) x[i] = 0ull;
-  cbar();
-  for (int k = 2; k <= N; k <<= 1)
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = threadIdx.x; i < N; i += kCT) {
-        const int ixj = i ^ j;
-        if (ixj > i) {
-          const unsigned long long a = x[i], b = x[ixj];
-          const bool desc = (i & k) == 0;
-          if (desc ? a < b : a > b) {
-            x[i] = b;
-            x[ixj] = a;
-          }
-        }
-      }
-      cbar();
-    }
-  return N;
-}
 __device__ __forceinline__ unsigned long long item_key(float z, int id) {
   return ((unsigned long long)fkey(z) << 32) | (unsigned)(~(unsigned)id);
 }
 __device__ __forceinline__ float key_z(unsigned long long k) { return key_to_float((uint32_t)(k >> 32)); }
 __device__ __forceinline__ int key_id(unsigned long long k) { return (int)~(uint32_t)k; }
 
+constexpr int kIPT = kItemCap / kCT;  // row-end items per consumer thread (item i: thread i % kCT)
+
+// The k-th largest (1-based) of the items' keys, counting repeats: four rounds of 8-bit
+// digits, most significant first, each a count histogram over the items whose higher
+// digits match.  Every consumer thread gets the key.
+__device__ uint32_t select_kth(const uint32_t (&key)[kIPT], unsigned have, int k) {
+  uint32_t prefix = 0;
+  int rem = k;
+  const int lane = threadIdx.x & 31;
+#pragma unroll 1
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    sm.hist[threadIdx.x] = 0u;
+    cbar();
+    const uint32_t hm = shift == 24 ? 0u : (0xFFFFFFFFu << (shift + 8));
+#pragma unroll
+    for (int u = 0; u < kIPT; ++u)
+      if (((have >> u) & 1u) && (key[u] & hm) == (prefix & hm)) atomicAdd(&sm.hist[(key[u] >> shift) & 255u], 1u);
+    cbar();
+    if (threadIdx.x < 32) {
+      // lane l owns digits 255 - 8l .. 248 - 8l; counts from the top
+      unsigned c8[8], tot = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c8[j] = sm.hist[255 - (lane * 8 + j)];
+        tot += c8[j];
+      }
+      unsigned incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned t = __shfl_up_sync(~0u, incl, o);
+        if (lane >= o) incl += t;
+      }
+      unsigned above = incl - tot;
+      if (above < (unsigned)rem && (unsigned)rem <= incl) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (above < (unsigned)rem && (unsigned)rem <= above + c8[j]) {
+            sm.ci[12] = 255 - (lane * 8 + j);
+            sm.ci[13] = rem - (int)above;
+          }
+          above += c8[j];
+        }
+      }
+    }
+    cbar();
+    prefix |= (uint32_t)sm.ci[12] << shift;
+    rem = sm.ci[13];
+  }
+  return prefix;
+}
+
+// The top-p threshold among the items in `in`: the smallest key g of an item such that
+// A (the mass of everything above the items) plus the mass of the items with a key above
+// g stays below T.  Items with a key of at least g are kept: a tie group (one key) stays
+// iff the mass strictly above it is below T.  Four rounds of 8-bit digits with exact
+// 64-bit digit masses.
+__device__ uint32_t select_mass(const uint32_t (&key)[kIPT], const float (&y)[kIPT], unsigned in,
+                                unsigned long long A, unsigned long long T) {
+  uint32_t prefix = 0;
+  const int lane = threadIdx.x & 31;
+#pragma unroll 1
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    sm.hist[threadIdx.x] = 0u;
+    sm.hmass[threadIdx.x] = 0ull;
+    cbar();
+    const uint32_t hm = shift == 24 ? 0u : (0xFFFFFFFFu << (shift + 8));
+#pragma unroll
+    for (int u = 0; u < kIPT; ++u)
+      if (((in >> u) & 1u) && (key[u] & hm) == (prefix & hm)) {
+        const unsigned dg = (key[u] >> shift) & 255u;
+        atomicAdd(&sm.hist[dg], 1u);
+        atomicAdd(&sm.hmass[dg], weight_fx(y[u]));
+      }
+    cbar();
+    if (threadIdx.x < 32) {
+      // the lowest non-empty digit whose mass above (A plus the higher digits) is below T
+      unsigned long long m8[8], tot = 0;
+      unsigned c8[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        m8[j] = sm.hmass[255 - (lane * 8 + j)];
+        c8[j] = sm.hist[255 - (lane * 8 + j)];
+        tot += m8[j];
+      }
+      unsigned long long incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long t = __shfl_up_sync(~0u, incl, o);
+        if (lane >= o) incl += t;
+      }
+      unsigned long long before = A + incl - tot;
+      int best = -1;
+      unsigned long long best_before = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (c8[j] && before < T) {
+          best = 255 - (lane * 8 + j);
+          best_before = before;
+        }
+        before += m8[j];
+      }
+      // lanes hold descending digit ranges: the highest lane with a candidate has the lowest digit
+      const unsigned has = __ballot_sync(~0u, best >= 0);
+      if (has) {
+        const int src = 31 - __clz(has);
+        const int d = __shfl_sync(~0u, best, src);
+        const unsigned long long bb = __shfl_sync(~0u, best_before, src);
+        if (lane == 0) {
+          sm.ci[12] = d;
+          sm.cu[2] = bb;
+        }
+      } else if (lane == 0) {
+        sm.ci[12] = -1;
+      }
+    }
+    cbar();
+    const int d = sm.ci[12];
+    if (d < 0) return 0xFFFFFFFFu;  // nothing stays (cannot happen while A < T)
+    prefix |= (uint32_t)d << shift;
+    A = sm.cu[2];
+  }
+  return prefix;
+}
+
 // The row end of light rows (items = the slices' candidates) and of general-route rows
 // with a compacted band (items = the band; the tokens above it were raced and summed by
-// P3).  Items sorted by z' (y follows), then the cuts as prefixes: top-k (all ties of the
-// k-th y), top-p (a tie group stays iff the mass strictly above it is below ceil(p W)),
-// min-p, and the race over the kept prefix.
+// P3).  The cuts are thresholds on the key of y found by radix selects, no sort: top-k
+// (every item with y at least the k-th largest), top-p (a tie group stays iff the mass
+// strictly above it is below ceil(p W)), min-p; then the race over the kept items.
 __device__ void task_fin(const KP& P, const Desc& d, float* buf) {
   const clsample_args_t& a = P.a;
   const int row = d.row, C = P.C;
@@ -1391,6 +1525,7 @@ __device__ void task_fin(const KP& P, const Desc& d, float* buf) {
   const float m = sm.cf[0], lnS = sm.cf[1], lnS1 = sm.cf[2];
   const int nal = sm.ci[0];
   const unsigned pf = (unsigned)sm.ci[1];
+  const unsigned nf = ((unsigned)sm.ci[6] & kFNonFinite) ? kPNonFinite : 0u;
   // a light row's first row end takes the slices' candidates; every other row end (a
   // general-route row, or a light row that fell back to it) takes its compacted band
   const bool fromband = (pf & kPBandCompact) != 0;
@@ -1416,7 +1551,7 @@ __device__ void task_fin(const KP& P, const Desc& d, float* buf) {
     }
   } else {
     // light row: the candidates of every slice; fall back to the general route when they
-    // do not fit, or when the top-k set may hold tokens no slice compacted
+    // do not fit, or when the kept set may hold tokens no slice compacted
     int total = 0, all_taken = 1;
     for (int s = 0; s < C; ++s) {
       const Rec1& r = sm.recs[s];
@@ -1426,7 +1561,7 @@ __device__ void task_fin(const KP& P, const Desc& d, float* buf) {
     }
     const int kcut = (q.k >= 2 && q.k < nal) ? q.k : 0;
     if (total > kItemCap || (!kcut && !all_taken)) {
-      if (threadIdx.x == 0) start_general(P, row, q, nal, (unsigned)sm.ci[6] & kFNonFinite ? kPNonFinite : 0u);
+      if (threadIdx.x == 0) start_general(P, row, q, nal, nf);
       return;
     }
     int off = 0;
@@ -1443,102 +1578,92 @@ __device__ void task_fin(const KP& P, const Desc& d, float* buf) {
     kk = kcut;
   }
   cbar();
-  sort_desc(x, n);
   const float invT = q.invT;
-  // top-k: every item with y >= the kk-th largest y
-  int nk = n;
+  // the thread's items: y and its key (items i = threadIdx.x + u * kCT)
+  uint32_t ky[kIPT];
+  float yv[kIPT];
+  unsigned have = 0u;
+#pragma unroll
+  for (int u = 0; u < kIPT; ++u) {
+    const int i = threadIdx.x + u * kCT;
+    yv[u] = -INFINITY;
+    ky[u] = 0u;
+    if (i < n) {
+      yv[u] = y_of(key_z(x[i]), m, invT);
+      ky[u] = fkey(yv[u]);
+      have |= 1u << u;
+    }
+  }
+  // top-k: every item with y at least the kk-th largest
+  uint32_t tk = 0u;
   if (kk > 0 && kk < n) {
-    const float Yk = y_of(key_z(x[kk - 1]), m, invT);
+    tk = select_kth(ky, have, kk);
     if (light) {
       // the candidates hold the row's whole top-k set iff every slice whose bound was
-      // below its top-k share left only tokens under Yk
+      // below its top-k share left only tokens under y_k
+      const float Yk = key_to_float(tk);
       int ok = 1;
       if (threadIdx.x < C) {
         const Rec1& r = sm.recs[threadIdx.x];
         const int nS = min(kSL, a.V - (int)threadIdx.x * kSL);
-        if (r.bound > -INFINITY && light_q(q.k, P.masked, nS, a.V) < q.k)
+        if (r.bound > -INFINITY && light_q(q.k, nS, a.V) < q.k)
           ok = y_of(nextafterf(r.bound, -INFINITY), m, invT) < Yk;
       }
       if (cbar_or(!ok)) {
-        if (threadIdx.x == 0) start_general(P, row, q, nal, (unsigned)sm.ci[6] & kFNonFinite ? kPNonFinite : 0u);
+        if (threadIdx.x == 0) start_general(P, row, q, nal, nf);
         return;
       }
     }
-    int last = -1;
-    for (int i = threadIdx.x; i < n; i += kCT)
-      if (y_of(key_z(x[i]), m, invT) >= Yk) last = max(last, i);
-    nk = cmax_i(last) + 1;
-  } else if (kk > 0 && kk >= n && light) {
+  } else if (kk > 0 && light) {
     // fewer candidates than k: only valid when every slice took all of its candidates
     int all_taken = 1;
     for (int s = 0; s < C; ++s) all_taken &= !(sm.recs[s].bound > -INFINITY);
     if (!all_taken) {
-      if (threadIdx.x == 0) start_general(P, row, q, nal, (unsigned)sm.ci[6] & kFNonFinite ? kPNonFinite : 0u);
+      if (threadIdx.x == 0) start_general(P, row, q, nal, nf);
       return;
     }
   }
-  // top-p over the top-k set (or the band, with the exact mass above it)
-  int np = nk;
-  if (q.p < 1.0f && nk > 0) {
-    constexpr int kPer = kItemCap / kCT;  // items per thread, contiguous
-    const int i0 = threadIdx.x * kPer;
-    unsigned long long wloc[kPer];
-    unsigned long long mine = 0ull;
+  unsigned insk = 0u;
 #pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-      const int i = i0 + u;
-      wloc[u] = i < nk ? weight_fx(y_of(key_z(x[i]), m, invT)) : 0ull;
-      mine += wloc[u];
+  for (int u = 0; u < kIPT; ++u)
+    if (((have >> u) & 1u) && ky[u] >= tk) insk |= 1u << u;
+  // top-p over the top-k set (or the band, with the exact mass above it)
+  uint32_t tp = 0u;
+  if (q.p < 1.0f) {
+    unsigned long long W = sm.cu[0];
+    if (!(pf & kPWKnown)) {
+      unsigned long long mine = 0ull;
+#pragma unroll
+      for (int u = 0; u < kIPT; ++u)
+        if ((insk >> u) & 1u) mine += weight_fx(yv[u]);
+      W = mass_above + csum(mine, sm.ru);
     }
-    unsigned long long tot = 0ull;
-    const unsigned long long excl = cscan_u64(mine, &tot);
-    const unsigned long long W = (pf & kPWKnown) ? sm.cu[0] : mass_above + tot;
-    const unsigned long long T = ceil_scaled(W, q.p);
-    // the first tie group whose mass strictly above reaches T is dropped, and everything
-    // after it: only the group's first item (a change of y) is tested
-    int cut = INT_MAX;
-    unsigned long long run = mass_above + excl;
-    float prev_y = (i0 > 0 && i0 - 1 < nk) ? y_of(key_z(x[i0 - 1]), m, invT) : INFINITY;
-    for (int u = 0; u < kPer; ++u) {
-      const int i = i0 + u;
-      if (i >= nk) break;
-      const float y = y_of(key_z(x[i]), m, invT);
-      if (y != prev_y && !(run < T)) {
-        cut = i;
-        break;
-      }
-      run += wloc[u];
-      prev_y = y;
-    }
-    np = min(nk, cmin_i(cut));
+    tp = select_mass(ky, yv, insk, mass_above, ceil_scaled(W, q.p));
   }
-  // min-p
-  int nm = np;
-  if (q.L > -INFINITY) {
-    int first = INT_MAX;
-    for (int i = threadIdx.x; i < np; i += kCT)
-      if (!(y_of(key_z(x[i]), m, invT) >= q.L)) first = min(first, i);
-    nm = min(np, cmin_i(first));
-  }
-  // race over the kept prefix
+  // min-p and the race over the kept items
+  const uint32_t cut_key = max(tk, tp);
   Race r{-INFINITY, INT_MAX, 0.0f, 0.0f};
   float sk = 0.0f, ymin = INFINITY;
-  for (int i = threadIdx.x; i < nm; i += kCT) {
-    const float z = key_z(x[i]);
-    const int id = key_id(x[i]);
-    const float y = y_of(z, m, invT);
+  int kept = 0;
+#pragma unroll
+  for (int u = 0; u < kIPT; ++u) {
+    if (!((insk >> u) & 1u) || ky[u] < cut_key || !(yv[u] >= q.L)) continue;
+    const unsigned long long it = x[threadIdx.x + u * kCT];
+    const int id = key_id(it);
     const uint4 w4 = race_words((uint32_t)id >> 2, q.seed, q.pos);
-    const float s = race_score(y, pick_word(w4, id & 3));
-    if (better(s, id, r.s, r.id)) r = Race{s, id, y, z};
-    sk += ex2_approx(y * 1.4426950408889634f);
-    ymin = fminf(ymin, y);
+    const float sc = race_score(yv[u], pick_word(w4, id & 3));
+    if (better(sc, id, r.s, r.id)) r = Race{sc, id, yv[u], key_z(it)};
+    sk += ex2_approx(yv[u] * 1.4426950408889634f);
+    ymin = fminf(ymin, yv[u]);
+    ++kept;
   }
   r = crace(r);
   sk = csum(sk, sm.rf);
   ymin = cmin_f(ymin);
+  kept = csum(kept, sm.ri);
   if (threadIdx.x == 0) {
     if (above.id != INT_MAX && better(above.s, above.id, r.s, r.id)) r = above;
-    const int kept = nm + kept_above;
+    kept += kept_above;
     if (r.id == INT_MAX || kept == 0) {
       row_fail(P, row, CLSAMPLE_ROW_OVERFLOW);
     } else {
@@ -1937,6 +2062,8 @@ __device__ void producer(const KP& P) {
         }
         d.rflags = 0u;
         if (P.lists) {
+          // the row's lists: the producer waits for them (never a consumer: a consumer
+          // waiting in front of a preparation task in its own ring could wait forever)
           unsigned long long pw = ld_acq64(P.prep + row);
           for (uint32_t polls = 0; (unsigned)pw != P.epoch && polls < kPolls; ++polls) {
             __nanosleep(64);
@@ -1984,7 +2111,10 @@ __device__ void consumer(const KP& P) {
       break;
     }
     const Desc& d = sm.desc[st];
-    const uint32_t ph = d.code & 15u;
+    // the task's identity, kept in registers: the descriptor belongs to the producer again
+    // once the stage is released
+    const uint32_t trow = d.row, tcode_ = d.code;
+    const uint32_t ph = tcode_ & 15u;
     float* buf = reinterpret_cast<float*>(dyn + (size_t)st * kBuf);
     if (ph == kExit) {
       if (threadIdx.x == 0) post_notice(nq, 0u, kExit);
@@ -1995,11 +2125,14 @@ __device__ void consumer(const KP& P) {
     else if (ph == kP3) task_p3(P, d, st, buf);
     else if (ph == kFin) task_fin(P, d, buf);
     else if (ph == kPrep) task_prep(P, d, buf);
+    // this task's ordinary writes into the ring buffer are ordered before the bulk copy
+    // that refills it (a different proxy)
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     cbar();
     int posted = 1;
     if (threadIdx.x == 0) {
       mbar_arrive(&sm.empty[st]);
-      if (ph <= kP3) posted = post_notice(nq++, d.row, d.code);
+      if (ph <= kP3) posted = post_notice(nq++, trow, tcode_);
       if (!posted) atomicOr(&P.ctl->err, 16u);
     }
     if (cbar_or(!posted)) break;
@@ -2065,7 +2198,12 @@ __global__ void __launch_bounds__(kBlock, 2) stream_kernel(const __grid_constant
   __syncthreads();
   // the last CTA out resets the call's counters; rows a failed poll left unfinished
   // report OVERFLOW
-  if (threadIdx.x == 0) sm.ci[0] = atomicInc(&P.ctl->exited, gridDim.x - 1u) == gridDim.x - 1u;
+  // every write of this CTA (outputs, finish markers) is published before it counts out,
+  // so the last CTA's sweep sees them
+  if (threadIdx.x == 0) {
+    __threadfence();
+    sm.ci[0] = atomicInc(&P.ctl->exited, gridDim.x - 1u) == gridDim.x - 1u;
+  }
   __syncthreads();
   if (sm.ci[0]) {
     __threadfence();
@@ -2089,6 +2227,7 @@ __global__ void __launch_bounds__(kBlock, 2) stream_kernel(const __grid_constant
       P.ctl->next = 0u;
       P.ctl->rr = 0u;
       P.ctl->rows_done = 0u;
+      P.ctl->err = 0u;
       P.ctl->epoch = P.epoch;
     }
   }
@@ -2112,7 +2251,7 @@ constexpr size_t take(size_t& off, size_t bytes) {
 Layout layout(size_t B, size_t C) {
   Layout L{};
   size_t off = 0;
-  L.dq_cap = (unsigned)(B * (2 + (kMaxRounds + 2) * C));
+  L.dq_cap = (unsigned)(B * (2 + (kMaxRounds + 2) * C) + kMaxGrid);
   L.ctl = take(off, sizeof(Ctl));
   L.dq = take(off, (size_t)L.dq_cap * sizeof(DSlot));
   L.rs = take(off, B * sizeof(RowState));
@@ -2217,7 +2356,8 @@ int launch(const clsample_args_t* a, unsigned char* scratch, int max_batch, int 
     P.ent = reinterpret_cast<Ent*>(scratch + L.ent);
     P.prep = reinterpret_cast<unsigned long long*>(scratch + L.prep);
     const int tasks = P.total;
-    const int g = grid < tasks ? grid : tasks;
+    int g = grid < tasks ? grid : tasks;
+    if (g > kMaxGrid) g = kMaxGrid;
     stream_kernel<<<g, kBlock, (size_t)kNB * kBuf, st>>>(P);
     if (cudaGetLastError() != cudaSuccess) return CLSAMPLE_ERR_CUDA;
   }

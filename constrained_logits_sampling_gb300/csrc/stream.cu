@@ -295,6 +295,9 @@ __device__ __forceinline__ void st_rel(unsigned* p, unsigned v) {
 __device__ __forceinline__ void st_rel64(unsigned long long* p, unsigned long long v) {
   asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
+__device__ __forceinline__ void st_relaxed64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
 __device__ __forceinline__ unsigned long long ld_acq64(const unsigned long long* p) {
   unsigned long long v;
   asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
@@ -595,7 +598,8 @@ __device__ bool push_tasks(const KP& P, uint32_t row, uint32_t ph, int n) {
       return false;
     }
     DSlot* d = P.dq + (size_t)(t % gridDim.x) * seg + pos;
-    st_rel64(d, make_slot(P.epoch, tcode(ph, (uint32_t)s), row));
+    // the fence above orders every earlier write before these entries: relaxed stores
+    st_relaxed64(d, make_slot(P.epoch, tcode(ph, (uint32_t)s), row));
   }
   return true;
 }
@@ -1188,8 +1192,7 @@ __device__ void task_p3(const KP& P, const Desc& d, int st, float* buf) {
         cls[j] = 0u;
       }
       if (cls[j] && yy[j] >= L) {
-        const Race& cur = cls[j] == 1u ? ra : rb;
-        if (yy[j] + kGumbelMax >= cur.s) any_race |= 1u << j;
+        if (yy[j] + kGumbelMax >= (cls[j] == 1u ? ra.s : rb.s)) any_race |= 1u << j;
         if (cls[j] == 1u) {
           ++kab;
           miny = fminf(miny, yy[j]);
@@ -1206,8 +1209,11 @@ __device__ void task_p3(const KP& P, const Desc& d, int st, float* buf) {
       const uint4 x = race_words((uint32_t)t0 >> 2, seed, pos);
       const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if ((any_race >> j) & 1u) race_in(cls[j] == 1u ? ra : rb, yy[j], e[j], t0 + j, xs[j]);
+      for (int j = 0; j < 4; ++j) {
+        if (!((any_race >> j) & 1u)) continue;
+        if (cls[j] == 1u) race_in(ra, yy[j], e[j], t0 + j, xs[j]);
+        else race_in(rb, yy[j], e[j], t0 + j, xs[j]);
+      }
     }
   }
   ra = crace(ra);
@@ -1369,21 +1375,34 @@ __device__ __forceinline__ int key_id(unsigned long long k) { return (int)~(uint
 
 constexpr int kIPT = kItemCap / kCT;  // row-end items per consumer thread (item i: thread i % kCT)
 
-// The k-th largest (1-based) of the items' keys, counting repeats: four rounds of 8-bit
-// digits, most significant first, each a count histogram over the items whose higher
-// digits match.  Every consumer thread gets the key.
-__device__ uint32_t select_kth(const uint32_t (&key)[kIPT], unsigned have, int k) {
-  uint32_t prefix = 0;
+// Row-end items in shared memory: (order key of y) << 32 | ~id, so a larger entry is a
+// larger y, then a lower id.
+__device__ __forceinline__ uint32_t ikey(unsigned long long e) { return (uint32_t)(e >> 32); }
+__device__ __forceinline__ int iid(unsigned long long e) { return (int)~(uint32_t)e; }
+
+// The k-th largest (1-based) of the keys of the items x[0..n) with key >= lo, counting
+// repeats: rounds of 8-bit digits from the highest bit in which kmin and kmax differ
+// down (the bits above it are common to every key, and skipping them spreads the first
+// round over its digits instead of piling the items onto one), each a count histogram
+// over the items whose higher bits match.  Every consumer thread gets the key.
+__device__ uint32_t select_kth(const unsigned long long* x, int n, uint32_t lo, uint32_t kmin, uint32_t kmax,
+                               int k) {
+  if (kmin == kmax) return kmin;
+  // bits at or above `fixed` are known; each round takes the 8 (or fewer) bits below them
+  int fixed = 32 - __clz(kmin ^ kmax);
+  uint32_t prefix = fixed >= 32 ? 0u : (kmin & ~((1u << fixed) - 1u));
   int rem = k;
   const int lane = threadIdx.x & 31;
-#pragma unroll 1
-  for (int shift = 24; shift >= 0; shift -= 8) {
+  while (fixed > 0) {
+    const int sh = fixed > 8 ? fixed - 8 : 0;
+    const uint32_t dm = (1u << (fixed - sh)) - 1u;
+    const uint32_t hm = fixed >= 32 ? 0u : ~((1u << fixed) - 1u);
     sm.hist[threadIdx.x] = 0u;
     cbar();
-    const uint32_t hm = shift == 24 ? 0u : (0xFFFFFFFFu << (shift + 8));
-#pragma unroll
-    for (int u = 0; u < kIPT; ++u)
-      if (((have >> u) & 1u) && (key[u] & hm) == (prefix & hm)) atomicAdd(&sm.hist[(key[u] >> shift) & 255u], 1u);
+    for (int i = threadIdx.x; i < n; i += kCT) {
+      const uint32_t key = ikey(x[i]);
+      if (key >= lo && (key & hm) == (prefix & hm)) atomicAdd(&sm.hist[(key >> sh) & dm], 1u);
+    }
     cbar();
     if (threadIdx.x < 32) {
       // lane l owns digits 255 - 8l .. 248 - 8l; counts from the top
@@ -1412,34 +1431,39 @@ __device__ uint32_t select_kth(const uint32_t (&key)[kIPT], unsigned have, int k
       }
     }
     cbar();
-    prefix |= (uint32_t)sm.ci[12] << shift;
+    prefix |= (uint32_t)sm.ci[12] << sh;
     rem = sm.ci[13];
+    fixed = sh;
   }
   return prefix;
 }
 
-// The top-p threshold among the items in `in`: the smallest key g of an item such that
-// A (the mass of everything above the items) plus the mass of the items with a key above
-// g stays below T.  Items with a key of at least g are kept: a tie group (one key) stays
-// iff the mass strictly above it is below T.  Four rounds of 8-bit digits with exact
-// 64-bit digit masses.
-__device__ uint32_t select_mass(const uint32_t (&key)[kIPT], const float (&y)[kIPT], unsigned in,
+// The top-p threshold among the items with key >= lo: the smallest key g of such an item
+// with A (the mass of everything above the items) plus the mass of the items with a key
+// above g below T.  Items with a key of at least g are kept: a tie group (one key) stays
+// iff the mass strictly above it is below T.  Rounds of 8-bit digits with exact 64-bit
+// digit masses, from the highest bit in which the keys differ.
+__device__ uint32_t select_mass(const unsigned long long* x, int n, uint32_t lo, uint32_t kmin, uint32_t kmax,
                                 unsigned long long A, unsigned long long T) {
-  uint32_t prefix = 0;
+  if (kmin == kmax) return A < T ? kmin : 0xFFFFFFFFu;
+  int fixed = 32 - __clz(kmin ^ kmax);
+  uint32_t prefix = fixed >= 32 ? 0u : (kmin & ~((1u << fixed) - 1u));
   const int lane = threadIdx.x & 31;
-#pragma unroll 1
-  for (int shift = 24; shift >= 0; shift -= 8) {
+  while (fixed > 0) {
+    const int sh = fixed > 8 ? fixed - 8 : 0;
+    const uint32_t dm = (1u << (fixed - sh)) - 1u;
+    const uint32_t hm = fixed >= 32 ? 0u : ~((1u << fixed) - 1u);
     sm.hist[threadIdx.x] = 0u;
     sm.hmass[threadIdx.x] = 0ull;
     cbar();
-    const uint32_t hm = shift == 24 ? 0u : (0xFFFFFFFFu << (shift + 8));
-#pragma unroll
-    for (int u = 0; u < kIPT; ++u)
-      if (((in >> u) & 1u) && (key[u] & hm) == (prefix & hm)) {
-        const unsigned dg = (key[u] >> shift) & 255u;
+    for (int i = threadIdx.x; i < n; i += kCT) {
+      const uint32_t key = ikey(x[i]);
+      if (key >= lo && (key & hm) == (prefix & hm)) {
+        const unsigned dg = (key >> sh) & dm;
         atomicAdd(&sm.hist[dg], 1u);
-        atomicAdd(&sm.hmass[dg], weight_fx(y[u]));
+        atomicAdd(&sm.hmass[dg], weight_fx(key_to_float(key)));
       }
+    }
     cbar();
     if (threadIdx.x < 32) {
       // the lowest non-empty digit whose mass above (A plus the higher digits) is below T
@@ -1472,10 +1496,10 @@ __device__ uint32_t select_mass(const uint32_t (&key)[kIPT], const float (&y)[kI
       const unsigned has = __ballot_sync(~0u, best >= 0);
       if (has) {
         const int src = 31 - __clz(has);
-        const int d = __shfl_sync(~0u, best, src);
+        const int dgt = __shfl_sync(~0u, best, src);
         const unsigned long long bb = __shfl_sync(~0u, best_before, src);
         if (lane == 0) {
-          sm.ci[12] = d;
+          sm.ci[12] = dgt;
           sm.cu[2] = bb;
         }
       } else if (lane == 0) {
@@ -1483,12 +1507,26 @@ __device__ uint32_t select_mass(const uint32_t (&key)[kIPT], const float (&y)[kI
       }
     }
     cbar();
-    const int d = sm.ci[12];
-    if (d < 0) return 0xFFFFFFFFu;  // nothing stays (cannot happen while A < T)
-    prefix |= (uint32_t)d << shift;
+    const int dgt = sm.ci[12];
+    if (dgt < 0) return 0xFFFFFFFFu;  // nothing stays (cannot happen while A < T)
+    prefix |= (uint32_t)dgt << sh;
     A = sm.cu[2];
+    fixed = sh;
   }
   return prefix;
+}
+
+// z' of the token `tok` among the row's items in global memory (the drawn token's
+// original logprob needs it); every consumer thread gets it.
+__device__ float find_z(const Item* g, int n, int tok) {
+  if (threadIdx.x == 0) sm.cf[11] = NAN;
+  cbar();
+  for (int i = threadIdx.x; i < n; i += kCT) {
+    const int2 v = __ldcg(reinterpret_cast<const int2*>(g + i));
+    if (v.y == tok) sm.cf[11] = __int_as_float(v.x);
+  }
+  cbar();
+  return sm.cf[11];
 }
 
 // The row end of light rows (items = the slices' candidates) and of general-route rows
@@ -1530,12 +1568,21 @@ __device__ void task_fin(const KP& P, const Desc& d, float* buf) {
   // general-route row, or a light row that fell back to it) takes its compacted band
   const bool fromband = (pf & kPBandCompact) != 0;
   const bool light = !fromband;
+  const float invT = q.invT;
   unsigned long long* x = reinterpret_cast<unsigned long long*>(buf);
   int n = 0, kk = 0;
   Race above{-INFINITY, INT_MAX, 0.0f, 0.0f};
   unsigned long long mass_above = 0ull;
   int kept_above = 0;
   float miny_above = INFINITY, sume_above = 0.0f;
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+  auto put = [&](int i, const Item* src) {
+    const int2 v = __ldcg(reinterpret_cast<const int2*>(src));
+    const uint32_t key = fkey(y_of(__int_as_float(v.x), m, invT));
+    x[i] = ((unsigned long long)key << 32) | (unsigned)(~(unsigned)v.y);
+    kmin = min(kmin, key);
+    kmax = max(kmax, key);
+  };
   if (fromband) {
     n = sm.ci[3];
     kk = sm.ci[2];
@@ -1545,10 +1592,7 @@ __device__ void task_fin(const KP& P, const Desc& d, float* buf) {
     sume_above = sm.cf[4];
     above = Race{sm.cf[5], sm.ci[5], sm.cf[6], sm.cf[7]};
     const Item* g = P.band + (size_t)row * kItemCap;
-    for (int i = threadIdx.x; i < n; i += kCT) {
-      const int2 v = __ldcg(reinterpret_cast<const int2*>(g + i));
-      x[i] = item_key(__int_as_float(v.x), v.y);
-    }
+    for (int i = threadIdx.x; i < n; i += kCT) put(i, g + i);
   } else {
     // light row: the candidates of every slice; fall back to the general route when they
     // do not fit, or when the kept set may hold tokens no slice compacted
@@ -1568,36 +1612,34 @@ __device__ void task_fin(const KP& P, const Desc& d, float* buf) {
     for (int s = 0; s < C; ++s) {
       const Item* g = P.cand + ((size_t)row * C + s) * kCand;
       const int c = sm.recs[s].ncand;
-      for (int i = threadIdx.x; i < c; i += kCT) {
-        const int2 v = __ldcg(reinterpret_cast<const int2*>(g + i));
-        x[off + i] = item_key(__int_as_float(v.x), v.y);
-      }
+      for (int i = threadIdx.x; i < c; i += kCT) put(off + i, g + i);
       off += c;
     }
     n = off;
     kk = kcut;
   }
-  cbar();
-  const float invT = q.invT;
-  // the thread's items: y and its key (items i = threadIdx.x + u * kCT)
-  uint32_t ky[kIPT];
-  float yv[kIPT];
-  unsigned have = 0u;
+  // key range of the items (the radix selects skip the bits they all share)
 #pragma unroll
-  for (int u = 0; u < kIPT; ++u) {
-    const int i = threadIdx.x + u * kCT;
-    yv[u] = -INFINITY;
-    ky[u] = 0u;
-    if (i < n) {
-      yv[u] = y_of(key_z(x[i]), m, invT);
-      ky[u] = fkey(yv[u]);
-      have |= 1u << u;
-    }
+  for (int o = 16; o; o >>= 1) {
+    kmin = min(kmin, __shfl_xor_sync(~0u, kmin, o));
+    kmax = max(kmax, __shfl_xor_sync(~0u, kmax, o));
+  }
+  cbar();
+  if ((threadIdx.x & 31) == 0) {
+    sm.ri[threadIdx.x >> 5] = (int)kmin;
+    sm.ri[kCW + (threadIdx.x >> 5)] = (int)kmax;
+  }
+  cbar();
+  kmin = 0xFFFFFFFFu;
+  kmax = 0u;
+  for (int i = 0; i < kCW; ++i) {
+    kmin = min(kmin, (uint32_t)sm.ri[i]);
+    kmax = max(kmax, (uint32_t)sm.ri[kCW + i]);
   }
   // top-k: every item with y at least the kk-th largest
   uint32_t tk = 0u;
   if (kk > 0 && kk < n) {
-    tk = select_kth(ky, have, kk);
+    tk = select_kth(x, n, 0u, kmin, kmax, kk);
     if (light) {
       // the candidates hold the row's whole top-k set iff every slice whose bound was
       // below its top-k share left only tokens under y_k
@@ -1623,46 +1665,57 @@ __device__ void task_fin(const KP& P, const Desc& d, float* buf) {
       return;
     }
   }
-  unsigned insk = 0u;
-#pragma unroll
-  for (int u = 0; u < kIPT; ++u)
-    if (((have >> u) & 1u) && ky[u] >= tk) insk |= 1u << u;
   // top-p over the top-k set (or the band, with the exact mass above it)
   uint32_t tp = 0u;
-  if (q.p < 1.0f) {
+  if (q.p < 1.0f && n > 0) {
     unsigned long long W = sm.cu[0];
     if (!(pf & kPWKnown)) {
       unsigned long long mine = 0ull;
-#pragma unroll
-      for (int u = 0; u < kIPT; ++u)
-        if ((insk >> u) & 1u) mine += weight_fx(yv[u]);
+      for (int i = threadIdx.x; i < n; i += kCT) {
+        const uint32_t key = ikey(x[i]);
+        if (key >= tk) mine += weight_fx(key_to_float(key));
+      }
       W = mass_above + csum(mine, sm.ru);
     }
-    tp = select_mass(ky, yv, insk, mass_above, ceil_scaled(W, q.p));
+    tp = select_mass(x, n, tk, max(kmin, tk), kmax, mass_above, ceil_scaled(W, q.p));
   }
   // min-p and the race over the kept items
   const uint32_t cut_key = max(tk, tp);
   Race r{-INFINITY, INT_MAX, 0.0f, 0.0f};
   float sk = 0.0f, ymin = INFINITY;
   int kept = 0;
-#pragma unroll
-  for (int u = 0; u < kIPT; ++u) {
-    if (!((insk >> u) & 1u) || ky[u] < cut_key || !(yv[u] >= q.L)) continue;
-    const unsigned long long it = x[threadIdx.x + u * kCT];
-    const int id = key_id(it);
+  for (int i = threadIdx.x; i < n; i += kCT) {
+    const unsigned long long it = x[i];
+    const uint32_t key = ikey(it);
+    const float y = key_to_float(key);
+    if (key < cut_key || !(y >= q.L)) continue;
+    const int id = iid(it);
     const uint4 w4 = race_words((uint32_t)id >> 2, q.seed, q.pos);
-    const float sc = race_score(yv[u], pick_word(w4, id & 3));
-    if (better(sc, id, r.s, r.id)) r = Race{sc, id, yv[u], key_z(it)};
-    sk += ex2_approx(yv[u] * 1.4426950408889634f);
-    ymin = fminf(ymin, yv[u]);
+    const float sc = race_score(y, pick_word(w4, id & 3));
+    if (better(sc, id, r.s, r.id)) r = Race{sc, id, y, 0.0f};
+    sk += ex2_approx(y * 1.4426950408889634f);
+    ymin = fminf(ymin, y);
     ++kept;
   }
   r = crace(r);
   sk = csum(sk, sm.rf);
   ymin = cmin_f(ymin);
   kept = csum(kept, sm.ri);
+  if (r.id != INT_MAX && above.id != INT_MAX && better(above.s, above.id, r.s, r.id)) r = above;
+  else if (r.id == INT_MAX) r = above;
+  if (r.id != INT_MAX && P.want_orig && !(r.id == above.id && above.id != INT_MAX)) {
+    // z' of a drawn item, from the items in global memory
+    r.z = fromband ? find_z(P.band + (size_t)row * kItemCap, n, r.id) : 0.0f;
+    if (!fromband) {
+      float z = NAN;
+      for (int s = 0; s < C && z != z; ++s) {
+        const float zs = find_z(P.cand + ((size_t)row * C + s) * kCand, sm.recs[s].ncand, r.id);
+        if (zs == zs) z = zs;
+      }
+      r.z = z;
+    }
+  }
   if (threadIdx.x == 0) {
-    if (above.id != INT_MAX && better(above.s, above.id, r.s, r.id)) r = above;
     kept += kept_above;
     if (r.id == INT_MAX || kept == 0) {
       row_fail(P, row, CLSAMPLE_ROW_OVERFLOW);

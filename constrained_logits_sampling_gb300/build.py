@@ -11,7 +11,7 @@ import sys
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
-SOURCES = [os.path.join(CSRC, "clsample.cu"), os.path.join(CSRC, "stream.cu")]
+SOURCES = [os.path.join(CSRC, "clsample.cu")]
 HEADERS = [os.path.join(ROOT, "include", "clsample.h")] + sorted(
     os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h")))
 LIB = os.path.join(PKG, "libclsample.so")

@@ -1,6 +1,6 @@
-// Inline-PTX wrappers for the mbarriers and the 1-D TMA bulk copies the sampler kernels
-// use on sm_103a: mbarrier set-up, arrival (with or without a transaction count), parity
-// polls, the bulk copy global -> shared with an L2 eviction policy, and the policies.
+// Inline-PTX wrappers for the mbarriers and the 1-D TMA bulk copies the sampler kernel
+// uses on sm_103a: mbarrier set-up, arrival with a transaction count, parity polls, and
+// the bulk copy global -> shared with an L2 eviction policy.
 // Every wait built on them is bounded by its caller.
 #pragma once
 
@@ -27,18 +27,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long* bar, u
                : "memory");
 }
 
-// Announces `bytes` of transactions for the current phase without arriving.
-__device__ __forceinline__ void mbar_expect_tx(unsigned long long* bar, uint32_t bytes) {
-  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
-               : "memory");
-}
-
-// Plain arrival (release at CTA scope: the caller's earlier shared-memory writes are
-// visible to a thread that sees the phase complete).
-__device__ __forceinline__ void mbar_arrive(unsigned long long* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
 // One poll of the phase with the given parity (acquire at CTA scope).
 __device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t parity) {
   uint32_t ok;
@@ -63,16 +51,6 @@ __device__ __forceinline__ bool mbar_wait(unsigned long long* bar, uint32_t pari
   return false;
 }
 
-// The same wait with a short sleep between polls, for threads that may wait long
-// (helper warps idling on their queue) so they take no issue slots from working warps.
-__device__ __forceinline__ bool mbar_wait_nap(unsigned long long* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (i > 64) __nanosleep(128);
-  }
-  return false;
-}
-
 // 1-D bulk copy (TMA) of `bytes` from global memory into this CTA's shared memory,
 // completing on `bar` (complete_tx), with an L2 eviction policy for the lines it brings
 // in.  Both addresses 16-byte aligned, bytes a multiple of 16.
@@ -85,16 +63,10 @@ __device__ __forceinline__ void bulk_copy_g2s_hint(void* dst, const void* src, u
       : "memory");
 }
 
-// L2 policies: lines a stream reads once go first when L2 needs room; lines read again
-// soon (a row that takes more than one pass) stay as long as possible.
+// L2 policy for lines a stream reads once: they go first when L2 needs room.
 __device__ __forceinline__ uint64_t make_policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-__device__ __forceinline__ uint64_t make_policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
 

@@ -54,7 +54,6 @@
 #include "clsample.h"
 #include "bulk_copy.cuh"
 #include "sampler_math.cuh"
-#include "stream.h"
 
 namespace {
 
@@ -2857,7 +2856,6 @@ constexpr ScratchLayout scratch_layout(size_t B, size_t C, size_t chunk, size_t 
   return L;
 }
 
-constexpr int kSpillRows = 16;  // at least this many spill rows per handle (max_batch / 8 for big batches)
 
 struct Scratch {
   int max_batch;
@@ -2912,28 +2910,22 @@ struct clsample_handle {
   int device;
   Geometry g;
   Scratch sc;
-  int grid[2];                // resident CTAs of the slice-resident kernel for f32 and bf16 logits
-  unsigned char* stream_base; // scratch of the streaming sampler
-  int stream_grid;            // its persistent grid
+  int grid[2];  // resident CTAs for f32 and bf16 logits
 };
 
 namespace {
 
 // Scratch of clsample_apply_static: a fixed device array compiled into the library
 // (every device that loads the library holds it until the process exits), sized for
-// kStaticRows rows of the longest slices and kStaticSpill spill rows of the
-// slice-resident kernel, followed by the streaming sampler's scratch for kStaticRows rows
-// of the largest vocabulary.
+// kStaticRows rows of the longest slices and kStaticSpill spill rows.
 constexpr int kStaticRows = 64;
 constexpr int kStaticSpill = 4;
 constexpr size_t kStaticBytes = scratch_layout(kStaticRows, kMaxSlices, kSliceMax, kStaticSpill).total;
-constexpr size_t kStaticStreamBytes = (size_t)28 << 20;  // checked against the layout at set-up
-static __device__ __align__(256) unsigned char g_static_scratch[kStaticBytes + kStaticStreamBytes];
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_static_mutex;
 unsigned char* g_static_base[kMaxDevices];  // the array's device address on each device, once set up
-int g_static_grid[kMaxDevices];             // the streaming sampler's grid on each device
 
 // The static scratch of device `dev`: on the first call for a device (with that device
 // current) the kernels are set up and the array's device address is looked up with
@@ -2947,12 +2939,6 @@ unsigned char* static_scratch(int dev, int* rc) {
   if (!g_static_base[dev]) {
     *rc = setup_device(dev);
     if (*rc != CLSAMPLE_SUCCESS) return nullptr;
-    *rc = clsample_stream::setup(dev, &g_static_grid[dev]);
-    if (*rc != CLSAMPLE_SUCCESS) return nullptr;
-    if (clsample_stream::scratch_bytes(kStaticRows, kMaxVocab) > kStaticStreamBytes) {
-      *rc = CLSAMPLE_ERR_CUDA;
-      return nullptr;
-    }
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) {
       *rc = CLSAMPLE_ERR_CUDA;
@@ -3005,8 +2991,8 @@ int clsample_create(int32_t max_batch, int32_t vocab, clsample_t** out) {
   int grid[2];
   if ((rc = resident_ctas(g, false, dev, &grid[0])) != CLSAMPLE_SUCCESS) return rc;
   if ((rc = resident_ctas(g, true, dev, &grid[1])) != CLSAMPLE_SUCCESS) return rc;
-  int spill_rows = max_batch / 8 > kSpillRows ? max_batch / 8 : kSpillRows;
-  if (spill_rows > max_batch) spill_rows = max_batch;
+  // one spill row per batch row: a row takes at most one, so no valid row runs out
+  const int spill_rows = max_batch;
   unsigned char* base = nullptr;
   if (max_batch > 0) {
     const size_t bytes = scratch_layout((size_t)max_batch, (size_t)g.C, (size_t)g.chunk, (size_t)spill_rows).total;
@@ -3026,24 +3012,6 @@ int clsample_create(int32_t max_batch, int32_t vocab, clsample_t** out) {
   h->sc = Scratch{max_batch, g.C, g.chunk, spill_rows, base};
   h->grid[0] = grid[0];
   h->grid[1] = grid[1];
-  h->stream_base = nullptr;
-  h->stream_grid = 0;
-  if ((rc = clsample_stream::setup(dev, &h->stream_grid)) != CLSAMPLE_SUCCESS) {
-    cudaFree(base);
-    delete h;
-    return rc;
-  }
-  if (max_batch > 0) {
-    const size_t bytes = clsample_stream::scratch_bytes(max_batch, vocab);
-    void* p = nullptr;
-    if (cudaMalloc(&p, bytes) != cudaSuccess || cudaMemset(p, 0, bytes) != cudaSuccess) {
-      if (p) cudaFree(p);
-      cudaFree(base);
-      delete h;
-      return CLSAMPLE_ERR_CUDA;
-    }
-    h->stream_base = static_cast<unsigned char*>(p);
-  }
   *out = h;
   return CLSAMPLE_SUCCESS;
 }
@@ -3051,7 +3019,6 @@ int clsample_create(int32_t max_batch, int32_t vocab, clsample_t** out) {
 void clsample_destroy(clsample_t* h) {
   if (!h) return;
   if (h->sc.base) cudaFree(h->sc.base);
-  if (h->stream_base) cudaFree(h->stream_base);
   delete h;
 }
 
@@ -3147,8 +3114,6 @@ int clsample_apply(clsample_t* h, const clsample_args_t* a, clsample_stream_t st
   const int rc = make_params(h, a, &P);
   if (rc != CLSAMPLE_SUCCESS || a->B == 0) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (clsample_stream::serves(a))
-    return clsample_stream::launch(a, h->stream_base, h->max_batch, h->stream_grid, st);
   const int ro = launch_order(P, st);
   return ro != CLSAMPLE_SUCCESS ? ro : launch_sampler(h->g, P, st);
 }
@@ -3157,7 +3122,6 @@ int clsample_prepare(clsample_t* h, const clsample_args_t* a, clsample_stream_t 
   LaunchParams P;
   const int rc = make_params(h, a, &P);
   if (rc != CLSAMPLE_SUCCESS || a->B == 0) return rc;
-  if (clsample_stream::serves(a)) return CLSAMPLE_SUCCESS;  // the streaming sampler has no preparation launch
   return launch_order(P, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -3165,10 +3129,7 @@ int clsample_sample(clsample_t* h, const clsample_args_t* a, clsample_stream_t s
   LaunchParams P;
   const int rc = make_params(h, a, &P);
   if (rc != CLSAMPLE_SUCCESS || a->B == 0) return rc;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (clsample_stream::serves(a))
-    return clsample_stream::launch(a, h->stream_base, h->max_batch, h->stream_grid, st);
-  return launch_sampler(h->g, P, st);
+  return launch_sampler(h->g, P, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int clsample_apply_static(const clsample_args_t* a, clsample_stream_t stream) {
@@ -3187,9 +3148,6 @@ int clsample_apply_static(const clsample_args_t* a, clsample_stream_t stream) {
   rc = make_params(g, a->V, dev, sc, a, &P);
   if (rc != CLSAMPLE_SUCCESS || a->B == 0) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (clsample_stream::serves(a)) {
-    return clsample_stream::launch(a, base + kStaticBytes, kStaticRows, g_static_grid[dev], st);
-  }
   rc = launch_order(P, st);
   return rc != CLSAMPLE_SUCCESS ? rc : launch_sampler(g, P, st);
 }

@@ -28,7 +28,7 @@
  * Threading and ownership.  A handle is bound to the CUDA device that was current at
  * clsample_create and owns device scratch sized for max_batch rows (row order and
  * counters, per-slice records, per-row lists of penalised and biased tokens, compacted
- * candidates, and a spill area of max(16, max_batch / 8) rows; about 456 KB per row for
+ * candidates, and a spill area of one row per batch row; about 1.5 MB per row for
  * V = 151936).  Every array in clsample_args_t is a DEVICE pointer owned by the caller;
  * it must stay valid until the work enqueued on the stream has finished.  The logits are
  * read-only (never written in place).  Calls on one handle must be ordered (one stream,
@@ -149,9 +149,11 @@ enum {
  *
  * Limits: V <= 262144 (at most 18 slices of at most 15360 tokens per row).  Any number
  * of penalised, biased or allowed tokens is handled exactly.  A row whose candidate set
- * must spill (a slice with more than 2048 candidates: flat or heavily tied rows) uses one
- * of the handle's spill rows for the call; a row that finds none left gets status
- * OVERFLOW, as does a row whose bounded waits for other CTAs gave up.
+ * must spill (a slice with more than 2048 candidates: flat or heavily tied rows) takes a
+ * spill row for the call.  A handle has one spill row per batch row, so no valid row of
+ * clsample_apply runs out; clsample_apply_static has 4, and a fifth row that must spill
+ * in one of its calls gets status OVERFLOW.  A row whose bounded waits for other CTAs
+ * gave up (a GPU that stopped scheduling them) is OVERFLOW too.
  */
 typedef struct {
   int32_t B, V;
@@ -232,7 +234,9 @@ int clsample_sample(clsample_t* handle, const clsample_args_t* args, clsample_st
  * ever happens.  The first call on a device looks up the array's address on that
  * device (cudaGetSymbolAddress) and sets the kernels' shared-memory limit, once per
  * device, under a host lock.  Limits: B <= 64 (else CLSAMPLE_ERR_BATCH) and
- * V <= 262144 (else CLSAMPLE_ERR_VOCAB); nothing is enqueued on an error.
+ * V <= 262144 (else CLSAMPLE_ERR_VOCAB); nothing is enqueued on an error.  The array
+ * holds 4 spill rows (see the limits of clsample_args_t): at most 4 rows of a call may
+ * spill; a further row that must spill reports OVERFLOW.
  * Races: every call on a device, from any host thread or stream, uses the same array,
  * so calls of this entry point on one device must be ordered (one stream, or streams
  * joined by events); two overlapping calls corrupt each other's row order and records.

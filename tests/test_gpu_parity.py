@@ -305,9 +305,9 @@ def test_history_beyond_the_preparation_hash():
 
 def test_flat_topk_rows_are_exact():
     """Flat rows under top-k keep every token (all tie with the k-th largest): more ties
-    than a slice's candidate area holds.  Such rows leave the candidate route for the
-    binned general route; every one of them, and every other row, matches the oracle
-    with status OK (more such rows than a small handle's batch, on a 24-row handle)."""
+    than a slice's candidate area holds, so each such row moves its slices to a spill
+    row.  A handle has one spill row per batch row, so every one of them, and every
+    other row, matches the oracle with status OK (20 such rows on a 24-row handle)."""
     from constrained_logits_sampling_gb300.sampler import Sampler
     V = 151936
     B = 24

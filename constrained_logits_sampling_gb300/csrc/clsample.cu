@@ -162,7 +162,7 @@ struct LaunchParams {
   int vec_ok;  // every row start is 16-byte aligned: slices arrive by TMA bulk copies
   int spill_rows;
   // scratch (device)
-  unsigned* ctl;      // [0] next item, [1] spill slots taken, [2] order ready, [3] CTAs done
+  unsigned* ctl;      // [0] next item, [1] spill slots taken, [2] order ready, [3] rows finished
   unsigned* rflag;    // [B] the row's entries are listed (preparation launch)
   int* order;         // [B] rows in list order
   RowCtl* rowctl;     // [B]
@@ -297,6 +297,24 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+
+__device__ __forceinline__ unsigned ld_relaxed(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Orders the loads that follow after a relaxed load that saw a released value.
+__device__ __forceinline__ void fence_acquire() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// Ticket increment that publishes this thread's earlier writes (and, through a preceding
+// block barrier, the CTA's) and, for the thread that sees the final count, acquires the
+// other CTAs' writes: one round trip instead of a fence and an atomic.
+__device__ __forceinline__ unsigned atomic_add_acq_rel(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
 }
 
 __device__ bool wait_flag(const unsigned* p, unsigned v) {
@@ -1269,8 +1287,38 @@ __device__ int compact_if(const Smem& S, int c0, int n, Pred&& keep, Item* dst, 
   return sh.cnt;
 }
 
+// The same for the threshold z' >= zc: a warp step whose vectors all lie below it (their
+// maxima) costs one vote and no per-token ballots.
 __device__ int compact(const Smem& S, int c0, int n, float zc, Item* dst, int cap, bool active = true) {
-  return compact_if(S, c0, n, [zc](float z) { return z >= zc; }, dst, cap, active);
+  const int nv = (n + 3) >> 2;
+  const float4* b4 = reinterpret_cast<const float4*>(S.buf);
+  if (threadIdx.x == 0) sh.cnt = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const unsigned lt = (1u << lane) - 1u;
+  const bool warp_active = __any_sync(~0u, active);
+  for (int f0 = 0; warp_active && f0 < nv; f0 += kThreads) {
+    const int f = f0 + threadIdx.x;
+    const float4 v = f < nv ? b4[f] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    const float vm = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+    const bool hit = active && vm > -INFINITY && vm >= zc;
+    if (!__any_sync(~0u, hit)) continue;
+    const float e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const bool pr = hit && e[j] > -INFINITY && e[j] >= zc;
+      const unsigned bal = __ballot_sync(~0u, pr);
+      if (bal) {
+        int base = 0;
+        if (lane == 0) base = atomicAdd(&sh.cnt, __popc(bal));
+        base = __shfl_sync(~0u, base, 0);
+        const int pos = base + __popc(bal & lt);
+        if (pr && pos < cap) dst[pos] = Item{e[j], c0 + 4 * f + j};
+      }
+    }
+  }
+  __syncthreads();
+  return sh.cnt;
 }
 
 // Writes every allowed token of the slice to the row's spill area; returns the count, or
@@ -2680,8 +2728,12 @@ __global__ void __launch_bounds__(kThreads, 3) sampler_kernel(const __grid_const
   if (threadIdx.x == 0) {
     // the counter is zero before the preparation launch runs, so the item is taken while
     // the order may still be in the making
+    // the item and a first look at the order flag go out together; the flag's acquire
+    // (a fence) follows once it reads set
     const unsigned item = atomicAdd(&P.ctl[0], 1u);
-    sh.flag = wait_flag(&P.ctl[2], 1u);
+    const unsigned seen = ld_relaxed(&P.ctl[2]);
+    if (seen == 1u) fence_acquire();
+    sh.flag = seen == 1u || wait_flag(&P.ctl[2], 1u);
     // without the order (the wait gave up) the item's own row, which is below B, stands in
     sh.row_id = sh.flag ? __ldcg(P.order + item / (unsigned)C) : (int)(item / (unsigned)C);
     sh.slice = (int)(item % (unsigned)C);
@@ -2734,24 +2786,22 @@ __global__ void __launch_bounds__(kThreads, 3) sampler_kernel(const __grid_const
   if (heavy) heavy_slice(P, S, q, row, slice, c0, n, ab);
   else if (q.route != kRouteGreedy) light_candidates(P, S, q, row, slice, c0, n);
   // publish the slice record (the barrier orders every thread's candidate writes before
-  // thread 0's cumulative fence) and take the row's ticket; a CTA that does not finish
-  // the row also counts itself done here
+  // thread 0's cumulative release) and take the row's ticket
   __syncthreads();
   if (threadIdx.x == 0) {
     P.srec[(size_t)row * P.C + slice] = sh.rec;
-    __threadfence();
-    sh.last = atomicAdd(&P.rowctl[row].ticket, 1u) == (unsigned)(C - 1);
-    sh.flag = sh.last ? 0 : (atomicAdd(&P.ctl[3], 1u) == gridDim.x - 1);
+    sh.last = atomic_add_acq_rel(&P.rowctl[row].ticket, 1u) == (unsigned)(C - 1);
+    sh.flag = 0;
   }
   __syncthreads();
   if (sh.last) {
-    __threadfence();
     combine_row(P, row, q);
     if (heavy) heavy_above(ab, C);
     finish_row<kBF16>(P, S, q, row, ab, heavy);
-    // the grid's last CTA clears the preparation flags for the next call
+    // the last row to finish clears the preparation flags for the next call: by then
+    // every CTA of the grid has taken its item and read the flags
     __syncthreads();
-    if (threadIdx.x == 0) sh.flag = atomicAdd(&P.ctl[3], 1u) == gridDim.x - 1;
+    if (threadIdx.x == 0) sh.flag = atomicAdd(&P.ctl[3], 1u) == (unsigned)(P.a.B - 1);
     __syncthreads();
   }
   if (sh.flag) {

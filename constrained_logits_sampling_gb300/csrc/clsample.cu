@@ -155,6 +155,8 @@ struct RowInfo {
   int pad;
 };
 
+struct SweepRec;
+
 struct LaunchParams {
   clsample_args_t a;
   int C;
@@ -175,6 +177,11 @@ struct LaunchParams {
   PenEntry* pent;     // [B][kPenRowCap]
   int lists;          // the preparation launch wrote rinfo / poff / pent (penalties, bias or a mask)
   Item* topn;         // [B * C][kTopNMax] each slice's most probable tokens (top-N logprobs)
+  // the single-sweep path's scratch
+  int sw_c;           // its slices per row
+  SweepRec* sw_rec;   // [B][kSwMaxC] slice records
+  Item* sw_cand;      // [B][kSwMaxC][kSwCand] race candidates (z', id)
+  unsigned* sw_tick;  // [B] row tickets, zero between calls
 };
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -2816,6 +2823,10 @@ __global__ void __launch_bounds__(kThreads, 3) sampler_kernel(const __grid_const
   }
 }
 
+// ---------------------------------------------------------------- single-sweep fast path
+
+#include "sweep.cuh"
+
 // ---------------------------------------------------------------- diagnostics
 
 // Allowed-token lists -> grammar bitmask rows: one CTA per row clears the row's words,
@@ -2878,7 +2889,7 @@ Geometry geometry_for(int vocab) {
 
 // Byte offsets of the scratch arrays for B rows of C slices of `chunk` tokens.
 struct ScratchLayout {
-  size_t ctl, order, rowctl, srec, bins, cand, spill, rinfo, poff, pent, rflag, topn, total;
+  size_t ctl, order, rowctl, srec, bins, cand, spill, rinfo, poff, pent, rflag, topn, sw_rec, sw_cand, sw_tick, total;
 };
 
 constexpr size_t take(size_t& off, size_t bytes) {
@@ -2902,6 +2913,9 @@ constexpr ScratchLayout scratch_layout(size_t B, size_t C, size_t chunk, size_t 
   L.pent = take(off, B * kPenRowCap * sizeof(PenEntry));
   L.rflag = take(off, B * sizeof(unsigned));
   L.topn = take(off, B * C * kTopNMax * sizeof(Item));
+  L.sw_rec = take(off, B * kSwMaxC * sizeof(SweepRec));
+  L.sw_cand = take(off, B * kSwMaxC * kSwCand * sizeof(Item));
+  L.sw_tick = take(off, B * sizeof(unsigned));
   L.total = off;
   return L;
 }
@@ -3084,7 +3098,10 @@ int make_params(const Geometry& g, int vocab, int dev, const Scratch& sc, const 
   if (a->B < 0 || a->B > sc.max_batch) return CLSAMPLE_ERR_BATCH;
   if (a->V != vocab) return CLSAMPLE_ERR_VOCAB;
   if (a->logits_dtype != CLSAMPLE_LOGITS_F32 && a->logits_dtype != CLSAMPLE_LOGITS_BF16) return CLSAMPLE_ERR_DTYPE;
-  if (a->mode & ~(CLSAMPLE_MODE_JOINT_TOPK_TOPP | CLSAMPLE_MODE_SCORE_ONLY)) return CLSAMPLE_ERR_MODE;
+  if (a->mode & ~(CLSAMPLE_MODE_JOINT_TOPK_TOPP | CLSAMPLE_MODE_SCORE_ONLY | CLSAMPLE_MODE_FAST_SWEEP))
+    return CLSAMPLE_ERR_MODE;
+  // the single sweep has neither requested-id nor top-N logprobs
+  if ((a->mode & CLSAMPLE_MODE_FAST_SWEEP) && (a->tid_offs || a->top_ns)) return CLSAMPLE_ERR_MODE;
   if (a->B == 0) return CLSAMPLE_SUCCESS;
   if (!a->logits || !a->tokens) return CLSAMPLE_ERR_NULL;
   if (a->hist_offs && !a->hist_ids) return CLSAMPLE_ERR_NULL;
@@ -3118,6 +3135,10 @@ int make_params(const Geometry& g, int vocab, int dev, const Scratch& sc, const 
   P->pent = reinterpret_cast<PenEntry*>(b + L.pent);
   P->rflag = reinterpret_cast<unsigned*>(b + L.rflag);
   P->topn = reinterpret_cast<Item*>(b + L.topn);
+  P->sw_c = (a->V + kSwSlice - 1) / kSwSlice;
+  P->sw_rec = reinterpret_cast<SweepRec*>(b + L.sw_rec);
+  P->sw_cand = reinterpret_cast<Item*>(b + L.sw_cand);
+  P->sw_tick = reinterpret_cast<unsigned*>(b + L.sw_tick);
   P->lists = (a->hist_offs || a->bias_offs || a->bitmask) ? 1 : 0;
   return CLSAMPLE_SUCCESS;
 }
@@ -3132,6 +3153,14 @@ int make_params(const clsample_t* h, const clsample_args_t* a, LaunchParams* P) 
 int launch_order(const LaunchParams& P, cudaStream_t st) {
   const unsigned grid = P.lists ? 1u + (unsigned)P.a.B : 1u;
   order_kernel<<<grid, kOrderThreads, P.lists ? kPrepSmem : 0, st>>>(P);
+  return cudaGetLastError() == cudaSuccess ? CLSAMPLE_SUCCESS : CLSAMPLE_ERR_CUDA;
+}
+
+// The single-sweep kernel: one CTA per (row, slice of kSwSlice tokens), no preparation.
+int launch_sweep(const LaunchParams& P, cudaStream_t st) {
+  const unsigned grid = (unsigned)(P.a.B * P.sw_c);
+  if (P.a.logits_dtype == CLSAMPLE_LOGITS_BF16) sweep_kernel<true><<<grid, kSwThreads, 0, st>>>(P);
+  else sweep_kernel<false><<<grid, kSwThreads, 0, st>>>(P);
   return cudaGetLastError() == cudaSuccess ? CLSAMPLE_SUCCESS : CLSAMPLE_ERR_CUDA;
 }
 
@@ -3164,6 +3193,7 @@ int clsample_apply(clsample_t* h, const clsample_args_t* a, clsample_stream_t st
   const int rc = make_params(h, a, &P);
   if (rc != CLSAMPLE_SUCCESS || a->B == 0) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (a->mode & CLSAMPLE_MODE_FAST_SWEEP) return launch_sweep(P, st);
   const int ro = launch_order(P, st);
   return ro != CLSAMPLE_SUCCESS ? ro : launch_sampler(h->g, P, st);
 }
@@ -3172,6 +3202,7 @@ int clsample_prepare(clsample_t* h, const clsample_args_t* a, clsample_stream_t 
   LaunchParams P;
   const int rc = make_params(h, a, &P);
   if (rc != CLSAMPLE_SUCCESS || a->B == 0) return rc;
+  if (a->mode & CLSAMPLE_MODE_FAST_SWEEP) return CLSAMPLE_SUCCESS;  // the sweep has no preparation
   return launch_order(P, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -3179,6 +3210,7 @@ int clsample_sample(clsample_t* h, const clsample_args_t* a, clsample_stream_t s
   LaunchParams P;
   const int rc = make_params(h, a, &P);
   if (rc != CLSAMPLE_SUCCESS || a->B == 0) return rc;
+  if (a->mode & CLSAMPLE_MODE_FAST_SWEEP) return launch_sweep(P, reinterpret_cast<cudaStream_t>(stream));
   return launch_sampler(h->g, P, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -3198,6 +3230,7 @@ int clsample_apply_static(const clsample_args_t* a, clsample_stream_t stream) {
   rc = make_params(g, a->V, dev, sc, a, &P);
   if (rc != CLSAMPLE_SUCCESS || a->B == 0) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (a->mode & CLSAMPLE_MODE_FAST_SWEEP) return launch_sweep(P, st);
   rc = launch_order(P, st);
   return rc != CLSAMPLE_SUCCESS ? rc : launch_sampler(g, P, st);
 }

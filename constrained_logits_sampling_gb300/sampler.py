@@ -20,7 +20,7 @@ _lock = threading.Lock()
 _lib = None
 
 LOGITS_F32, LOGITS_BF16 = 0, 1
-MODE_JOINT_TOPK_TOPP, MODE_SCORE_ONLY = 1, 2
+MODE_JOINT_TOPK_TOPP, MODE_SCORE_ONLY, MODE_FAST_SWEEP = 1, 2, 4
 ROW_OK, ROW_OVERFLOW, ROW_INVALID = 0, 1, 2
 
 

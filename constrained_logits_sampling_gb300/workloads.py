@@ -211,12 +211,31 @@ WORKLOADS = {
     3: "grammar-constrained: B=128 V=151936, 50% of rows bitmasked (0.1%/5%/60% density)",
     4: "penalties+bias: B=192 V=151936 fp32, Zipf histories, 16 logit_bias/row, 25% masked",
     5: "verify-scale: B=1024 (256 requests x 4 positions) V=151936 bf16 Student-t logits, all features",
+    6: "all-greedy fast path: workload 4 with T=0 on every row (single sweep)",
+    7: "all-untruncated fast path: workload 4 with T~U[0.5,1.2], no top-k/top-p/min-p (single sweep)",
 }
+
+MODE_FAST_SWEEP = 4  # clsample.h CLSAMPLE_MODE_FAST_SWEEP
 
 
 def make_workload(n: int, B: Optional[int] = None, V: Optional[int] = None) -> Batch:
-    """Build workload ``n`` (1..5).  ``B``/``V`` override the sizes for
-    reduced parity cases; the value distributions stay the same."""
+    """Build workload ``n`` (1..7).  ``B``/``V`` override the sizes for
+    reduced parity cases; the value distributions stay the same.  Workloads 6
+    and 7 are workload 4's logits, lists and masks with every row greedy, or
+    every row sampled without truncation, marked for the single-sweep path."""
+    if n in (6, 7):
+        b = make_workload(4, B=B, V=V)
+        rng = np.random.Generator(np.random.PCG64(1000 + n))
+        if n == 6:
+            b.temperatures = np.zeros(b.B, np.float32)
+        else:
+            b.temperatures = rng.uniform(0.5, 1.2, size=b.B).astype(np.float32)
+            b.top_ks = np.full(b.B, -1, np.int32)
+            b.top_ps = np.ones(b.B, np.float32)
+            b.min_ps = np.zeros(b.B, np.float32)
+        b.mode = MODE_FAST_SWEEP
+        b.name = "all_greedy" if n == 6 else "all_untruncated"
+        return b
     rng = np.random.Generator(np.random.PCG64(1000 + n))
     if n == 1:
         B = B or 4

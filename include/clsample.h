@@ -86,7 +86,19 @@ enum {
   /* Scoring only (SGLang page, logprobs-only computation): the same transforms, no draw.
    * Every row takes the greedy route whatever its parameters -- token = argmax of z',
    * logprobs at T_eff -- and the requested ids (tid_*) get their logprobs. */
-  CLSAMPLE_MODE_SCORE_ONLY = 2
+  CLSAMPLE_MODE_SCORE_ONLY = 2,
+  /* Batch fast path (SGLang page, "Field groups": the host-side batch booleans
+   * is_all_greedy and need_top_k/top_p/min_p_sampling, and the sampler's simple-sampling
+   * branch; GLM page, "Sampling").  The caller asserts that every row is greedy (T < 1e-5,
+   * top_k 0 or 1, or SCORE_ONLY) or untruncated (top_p 1, min_p 0, top_k -1 or at least
+   * the row's allowed tokens).  The call is then one sweep over the logits -- no
+   * preparation launch -- with the same results as without the flag.  A row that breaks
+   * the assertion, or has 2^20 or more history ids or 4095 or more bias entries, gets
+   * status INVALID.  Requested-id and top-N logprobs are not available (ERR_MODE).
+   * An untruncated row draws from candidates within 2e-3 of each slice's best fast race
+   * score; a slice with more than 64 of them (not seen in practice) makes the row
+   * OVERFLOW. */
+  CLSAMPLE_MODE_FAST_SWEEP = 4
 };
 
 /* Arguments of one sampler call.  B rows, V vocabulary entries.

@@ -441,7 +441,7 @@ def test_unknown_mode_bit_is_rejected_on_the_host():
     kw = batch_to_device(b, s.device)
     logits = kw.pop("logits")
     with pytest.raises(ClsampleError):
-        s(logits, mode=4, **kw)
+        s(logits, mode=8, **kw)
     s(logits, mode=3, **kw)
     torch.cuda.synchronize()
 

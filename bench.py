@@ -3,9 +3,16 @@
 One step = one sampler call (penalties, bias, grammar mask, temperature, top-k ->
 top-p -> min-p, exponential race, logprob) over one batch of the penalties+bias
 workload: B=192 rows, V=151936, fp32 logits, Zipf histories of 0-4096 ids, 16
-logit_bias entries per row, bitmasks on 25% of rows, mixed parameters.
+logit_bias entries per row, bitmasks on 25% of rows, mixed parameters.  --workload
+selects another batch (1-5: the tiny, decode-mix, grammar, penalties and
+verify-scale configurations; 6-7: all-greedy and all-untruncated batches on the
+single-sweep fast path).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload n]
+
+--gpus N > 1 runs N replicas, one process per GPU: under a launcher that sets
+WORLD_SIZE (torchrun) it must equal N; without one, bench.py starts
+torch.distributed.run itself.
 
 Prints one JSON line (rank 0).  Inputs are rotated over three resident copies of the
 batch (3 x 122 MB, more than twice the 129 MB L2), so no step reads a batch that the
@@ -29,8 +36,10 @@ sys.path.insert(0, ROOT)
 
 METRIC = "rows/s & HBM GB/s (% of peak), fused mask+top-k/p sample, B=192 V=151936"
 WORKLOAD = 4
+MODE_FAST_SWEEP = 4  # clsample.h CLSAMPLE_MODE_FAST_SWEEP
 N_SETS = 3
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal
 
 
 def parse(argv=None):
@@ -50,6 +59,25 @@ def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+def launch_plan(args, env, argv):
+    """How `--gpus N` runs: ("run", None) in this process; ("spawn", cmd) to start N
+    ranks with torch.distributed.run; ("error", message) when a launcher's world size
+    disagrees with --gpus."""
+    if args.gpus < 1:
+        return "error", f"--gpus {args.gpus}: at least one GPU"
+    world = env.get("WORLD_SIZE")
+    if world is not None:
+        if int(world) != args.gpus:
+            return "error", f"--gpus {args.gpus} but the launcher started WORLD_SIZE={world} ranks"
+        return "run", None
+    if args.gpus == 1:
+        return "run", None
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+           "--master-addr", "127.0.0.1", "--master-port", str(env.get("MASTER_PORT", "29531")),
+           os.path.abspath(__file__), *argv]
+    return "spawn", cmd
 
 
 def peaks():
@@ -140,23 +168,31 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_baseline(batch, sample_rows, min_repeats=3, min_seconds=1.0, max_repeats=40):
+def cpu_baseline(batch, sample_rows, min_repeats=3, min_seconds=1.0, max_repeats=40, single_rows=8):
     """The oracle as it stands, on the host cores, on a bounded sample of the batch:
     whole passes over the sample until about `min_seconds` of wall time (10-30 s of
-    CPU work on a many-core host), at least `min_repeats` of them."""
+    CPU work on a many-core host), at least `min_repeats` of them; then the same on one
+    thread over a smaller sample."""
     from oracle import oracle as O
+
+    def timed(sub, nthreads):
+        O.sample(sub, nthreads=nthreads, want_transformed=False)  # warm-up (page-in, thread start)
+        t0 = time.perf_counter()
+        threads, repeats = 1, 0
+        while repeats < min_repeats or (time.perf_counter() - t0 < min_seconds and repeats < max_repeats):
+            threads = O.sample(sub, nthreads=nthreads, want_transformed=False)["threads"]
+            repeats += 1
+        return time.perf_counter() - t0, int(threads), repeats
+
     sub = batch.rows(range(min(sample_rows, batch.B)))
-    O.sample(sub, nthreads=0, want_transformed=False)  # warm-up (page-in, thread start)
-    t0 = time.perf_counter()
-    threads, repeats = 1, 0
-    while repeats < min_repeats or (time.perf_counter() - t0 < min_seconds and repeats < max_repeats):
-        threads = O.sample(sub, nthreads=0, want_transformed=False)["threads"]
-        repeats += 1
-    dt = time.perf_counter() - t0
-    rows = sub.B * repeats
-    return {"value": rows / dt, "unit": "rows/s", "cores": int(threads), "kind": "oracle",
+    dt, threads, repeats = timed(sub, 0)
+    sub1 = batch.rows(range(min(single_rows, batch.B)))
+    dt1, _, repeats1 = timed(sub1, 1)
+    return {"value": sub.B * repeats / dt, "unit": "rows/s", "cores": threads, "kind": "oracle",
             "sample": f"{sub.B} rows of workload {batch.name} (B={batch.B}, V={batch.V}) x {repeats} repeats, "
-                      f"{dt:.2f} s wall on {threads} threads (about {dt * threads:.0f} s of CPU work)"}
+                      f"{dt:.2f} s wall on {threads} threads (about {dt * threads:.0f} s of CPU work)",
+            "single_thread": {"value": sub1.B * repeats1 / dt1, "unit": "rows/s", "cores": 1,
+                              "sample": f"{sub1.B} rows x {repeats1} repeats, {dt1:.2f} s on one thread"}}
 
 
 def run_reference(args, rank, world):
@@ -166,7 +202,7 @@ def run_reference(args, rank, world):
     from oracle import oracle as O
     O.build()
     b = make_workload(args.workload)
-    sample_rows = 32
+    sample_rows = min(32, b.B)
     sub = b.rows(range(sample_rows))
     for _ in range(max(args.warmup, 0)):
         O.sample(sub, nthreads=0)
@@ -181,8 +217,7 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32+f64",
         "data": "synthetic",
-        "config": {"workload": f"{b.name}: B={b.B} V={b.V} fp32 logits, penalties+bias, 25% bitmasked rows",
-                   "sample_rows_per_step": sample_rows},
+        "config": {"workload": workload_text(b, args.workload), "sample_rows_per_step": sample_rows},
         "cpu_baseline": {"value": value, "unit": "rows/s", "cores": int(threads), "kind": "oracle",
                          "sample": f"{sample_rows} rows of {b.name} per step, {args.steps} steps"},
         "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -208,8 +243,19 @@ def rows_per_second(rows_per_rank, world, steps, total_ms):
     return rows_per_rank * world * steps / (total_ms / 1e3)
 
 
+def workload_text(b, n):
+    from constrained_logits_sampling_gb300.workloads import WORKLOADS
+    return f"{b.name} (workload {n}): " + WORKLOADS.get(n, "").split(": ", 1)[-1]
+
+
 def main():
     args = parse()
+    how, what = launch_plan(args, os.environ, sys.argv[1:])
+    if how == "error":
+        print(json.dumps({"error": what}), flush=True)
+        return 2
+    if how == "spawn":
+        return subprocess.call(what)
     rank, world, local = dist_env()
     if args.impl == "reference":
         return run_reference(args, rank, world)
@@ -362,12 +408,22 @@ def main():
 
     peak, peak_kind = peaks()
     alg = b.algorithmic_bytes()
-    # the sampler kernel reads the logits, the bitmask and the per-row parameters and
-    # writes the outputs; the history and logit_bias CSRs are read by the preparation
-    # launch ahead of it (which hands the sampler a short list per slice instead)
+    sweep = bool(getattr(b, "mode", 0) & MODE_FAST_SWEEP)
     hb = b.host_bytes()
-    alg_sampler = alg - sum(hb.get(k, 0) for k in ("hist_offs", "hist_ids", "bias_offs", "bias_ids", "bias_vals"))
-    achieved = alg_sampler / (mean_launch_ms / 1e3) / 1e9
+    if sweep:
+        # the single-sweep kernel reads everything itself: logits, bitmask, parameters and
+        # the history and logit_bias CSRs (each CTA scans its rows' lists), writes outputs
+        alg_kernel = alg
+        kernel = ("sweep_kernel (single pass, one CTA per (row, 8192-token slice); no preparation launch; "
+                  "the row's last CTA draws)")
+    else:
+        # the sampler kernel reads the logits, the bitmask and the per-row parameters and
+        # writes the outputs; the history and logit_bias CSRs are read by the preparation
+        # launch ahead of it (which hands the sampler a short list per slice instead)
+        alg_kernel = alg - sum(hb.get(k, 0) for k in ("hist_offs", "hist_ids", "bias_offs", "bias_ids", "bias_vals"))
+        kernel = ("sampler_kernel (one CTA per (row, slice), launched with programmatic serialisation after "
+                  "order_kernel, the preparation launch: row order and per-row penalty/bias lists)")
+    achieved = alg_kernel / (mean_launch_ms / 1e3) / 1e9
     line = {
         "metric": METRIC,
         "value": value,
@@ -379,11 +435,10 @@ def main():
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32",
+        "dtype": "bf16" if b.logits_bf16 else "f32",
         "data": "synthetic",
         "config": {
-            "workload": f"{b.name}: B={b.B} V={b.V} fp32 logits, Zipf(1.1) histories 0-4096 ids, "
-                        "16 logit_bias/row, bitmasks on 25% of rows, mixed T/top-k/top-p/min-p, 25% greedy",
+            "workload": workload_text(b, args.workload),
             "rows_per_gpu": b.B,
             "l2": f"inputs rotated over {N_SETS} resident copies ({N_SETS * alg / 1e6:.0f} MB > 2 x L2)",
             "parallelism": f"replicas x{world} (rows are independent)",
@@ -395,16 +450,16 @@ def main():
             "peak": peak,
             "unit": "GB/s",
             "frac": achieved / peak,
+            "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
             "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
             "traffic": traffic_from_profile(b.name),
-            "algorithmic_bytes_per_launch": alg_sampler,
+            "algorithmic_bytes_per_launch": alg_kernel,
             "mean_launch_us": mean_launch_ms * 1e3,
-            "kernel": "sampler_kernel (one CTA per (row, slice), launched with programmatic serialisation after "
-                      "order_kernel, the preparation launch: row order and per-row penalty/bias lists)",
-            "order_kernel_us": order_ms * 1e3,
+            "kernel": kernel,
+            "order_kernel_us": None if sweep else order_ms * 1e3,
             "step_algorithmic_gbs": alg / (ms_per_step / 1e3) / 1e9,
         },
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": (1 if sweep else 2) * args.steps,
         "clocks": clk,
         "e2e": e2e,
     }

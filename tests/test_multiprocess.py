@@ -52,3 +52,32 @@ def test_two_gloo_ranks_take_the_slowest_time():
         assert got == [11.0, 3.0]  # the max over both ranks, on every rank
         assert value == pytest.approx(192 * 2 * 5 / 0.011)
         assert rc == 0
+
+
+def test_gpus_flag_plans_one_process_per_gpu():
+    sys.path.insert(0, ROOT)
+    import bench
+    a = bench.parse(["--gpus", "2"])
+    how, cmd = bench.launch_plan(a, {}, ["--gpus", "2"])
+    assert how == "spawn" and "--nproc-per-node=2" in cmd and "127.0.0.1" in cmd
+    assert bench.launch_plan(a, {"WORLD_SIZE": "2"}, [])[0] == "run"
+    assert bench.launch_plan(a, {"WORLD_SIZE": "4"}, [])[0] == "error"
+    assert bench.launch_plan(bench.parse([]), {}, [])[0] == "run"
+
+
+def test_gpus_2_starts_two_replicas_of_the_reference_arm():
+    """bench.py --gpus 2 without a launcher starts two ranks itself; in the reference arm
+    rank 0 prints the one JSON line and rank 1 exits 0 without work (CPU only)."""
+    import json
+    import subprocess
+    env = dict(os.environ, MASTER_PORT=str(_free_port()))
+    env.pop("WORLD_SIZE", None)
+    env.pop("RANK", None)
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--impl", "reference",
+                        "--workload", "1", "--steps", "1", "--warmup", "0"],
+                       capture_output=True, text=True, env=env, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2

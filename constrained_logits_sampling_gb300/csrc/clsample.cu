@@ -526,17 +526,43 @@ __device__ void sort_desc(unsigned long long* k, int n) {
 
 // ---------------------------------------------------------------- row parameters
 
-// Parameters, greedy rule and route of a row (every CTA of the row computes the same).
-__device__ void load_params(const clsample_args_t& a, int row, RowParams& q) {
-  q.T = a.temperatures ? a.temperatures[row] : 1.0f;
-  q.k = a.top_ks ? a.top_ks[row] : -1;
-  q.p = a.top_ps ? a.top_ps[row] : 1.0f;
-  q.mp = a.min_ps ? a.min_ps[row] : 0.0f;
-  q.rep = a.rep ? a.rep[row] : 1.0f;
-  q.freq = a.freq ? a.freq[row] : 0.0f;
-  q.pres = a.pres ? a.pres[row] : 0.0f;
-  q.seed = a.seeds ? a.seeds[row] : 0ull;
-  q.pos = (unsigned long long)(a.positions ? a.positions[row] : a.step);
+// A row's parameters as read from memory (loads only: a kernel may issue them early and
+// decode them when it needs them).
+struct RawRow {
+  float T, p, mp, rep, freq, pres;
+  int k, h0, h1, b0, b1;
+  unsigned long long seed, pos;
+};
+__device__ __forceinline__ RawRow load_raw(const clsample_args_t& a, int row) {
+  RawRow w;
+  w.T = a.temperatures ? a.temperatures[row] : 1.0f;
+  w.k = a.top_ks ? a.top_ks[row] : -1;
+  w.p = a.top_ps ? a.top_ps[row] : 1.0f;
+  w.mp = a.min_ps ? a.min_ps[row] : 0.0f;
+  w.rep = a.rep ? a.rep[row] : 1.0f;
+  w.freq = a.freq ? a.freq[row] : 0.0f;
+  w.pres = a.pres ? a.pres[row] : 0.0f;
+  w.seed = a.seeds ? a.seeds[row] : 0ull;
+  w.pos = (unsigned long long)(a.positions ? a.positions[row] : a.step);
+  w.h0 = a.hist_offs ? a.hist_offs[row] : 0;
+  w.h1 = a.hist_offs ? a.hist_offs[row + 1] : 0;
+  w.b0 = a.bias_offs ? a.bias_offs[row] : 0;
+  w.b1 = a.bias_offs ? a.bias_offs[row + 1] : 0;
+  return w;
+}
+
+// Parameters, greedy rule and route of a row from its loaded values (every CTA of the
+// row computes the same).
+__device__ void decode_params(const clsample_args_t& a, const RawRow& w, RowParams& q) {
+  q.T = w.T;
+  q.k = w.k;
+  q.p = w.p;
+  q.mp = w.mp;
+  q.rep = w.rep;
+  q.freq = w.freq;
+  q.pres = w.pres;
+  q.seed = w.seed;
+  q.pos = w.pos;
   int inv = 0;
   if (q.T != q.T || q.T == INFINITY) inv = 1;
   if (q.k < -1) inv = 1;
@@ -546,21 +572,19 @@ __device__ void load_params(const clsample_args_t& a, int row, RowParams& q) {
   q.hlo = 0;
   q.hhi = 0;
   if (a.hist_offs) {
-    const int lo = a.hist_offs[row], hi = a.hist_offs[row + 1];
-    if (lo < 0 || hi < lo) inv = 1;
+    if (w.h0 < 0 || w.h1 < w.h0) inv = 1;
     else {
-      q.hlo = lo;
-      q.hhi = hi;
+      q.hlo = w.h0;
+      q.hhi = w.h1;
     }
   }
   q.blo = 0;
   q.bhi = 0;
   if (a.bias_offs) {
-    const int lo = a.bias_offs[row], hi = a.bias_offs[row + 1];
-    if (lo < 0 || hi < lo) inv = 1;
+    if (w.b0 < 0 || w.b1 < w.b0) inv = 1;
     else {
-      q.blo = lo;
-      q.bhi = hi;
+      q.blo = w.b0;
+      q.bhi = w.b1;
     }
   }
   q.invalid = inv ? kFlagInvalid : 0;
@@ -575,6 +599,8 @@ __device__ void load_params(const clsample_args_t& a, int row, RowParams& q) {
   else if (q.p == 1.0f && q.mp > 0.0f) q.route = kRouteMinP;
   else q.route = kRouteHeavy;
 }
+
+__device__ void load_params(const clsample_args_t& a, int row, RowParams& q) { decode_params(a, load_raw(a, row), q); }
 
 // List order of a row: heavy rows first (their CTAs wait for each other and work longest),
 // then top-k rows with a large k (their row ends take longest), other rows that finish

@@ -8,7 +8,8 @@
 //   one CTA per (row, slice of kSwSlice tokens), each warp on a region of kSwRegion
 //   tokens held in registers (coalesced vector loads, issued first);
 //   while the loads fly, the row's history and bias lists are scanned for this slice's
-//   tokens into a shared-memory table (count | bias entry), so no preparation launch;
+//   tokens into a shared-memory table (count | bias entry), so no preparation launch; each
+//   listed token's transformed value is then computed once, into its table entry;
 //   the slice's transforms, mask, max / lowest argmax, allowed count and sums of
 //   2^((z' - m_s) log2(e) / T) come from the registers; untruncated rows also race their
 //   tokens with fast scores relative to the slice max and keep every token within
@@ -101,9 +102,8 @@ __device__ __forceinline__ float4 sweep_load(const clsample_args_t& a, long long
 }
 
 // The transforms of one listed token (sanitise, penalties, bias, overflow guard), in the
-// order and arithmetic of the per-slice sampler.  Out of line: listed tokens are rare and
-// the division of the repetition penalty is long code.
-__device__ __noinline__ float sweep_transform(const clsample_args_t& a, const RowParams& q, float z, unsigned e) {
+// order and arithmetic of the per-slice sampler.
+__device__ __forceinline__ float sweep_transform(const clsample_args_t& a, const RowParams& q, float z, unsigned e) {
   z = sanitize(z);
   const unsigned c = e & ((1u << kSwCountBits) - 1u), bj = e >> kSwCountBits;
   if (c) z = apply_penalties(z, c, q.freq, q.pres, q.rep);
@@ -120,7 +120,7 @@ __device__ __forceinline__ void vset(float4& v, int j, float z) {
 }
 
 template <bool kBF16>
-__global__ void __launch_bounds__(kSwThreads, 3) sweep_kernel(const __grid_constant__ LaunchParams P) {
+__global__ void __launch_bounds__(kSwThreads, 4) sweep_kernel(const __grid_constant__ LaunchParams P) {
   __shared__ SweepShared X;
   __shared__ RowParams q;
   const clsample_args_t& a = P.a;
@@ -150,55 +150,97 @@ __global__ void __launch_bounds__(kSwThreads, 3) sweep_kernel(const __grid_const
     X.ncand = 0;
   }
   const bool lists = a.hist_offs || a.bias_offs;
+  // the row's first history ids and bias entries are loaded now, while the logits are in
+  // flight (every thread reads the offsets itself, so nothing waits for thread 0)
+  int h0 = 0, h1 = 0, b0 = 0, b1 = 0;
+  if (a.hist_offs) {
+    h0 = __ldg(a.hist_offs + row);
+    h1 = __ldg(a.hist_offs + row + 1);
+  }
+  if (a.bias_offs) {
+    b0 = __ldg(a.bias_offs + row);
+    b1 = __ldg(a.bias_offs + row + 1);
+  }
+  // offsets that are bad or past the table's limits make the row INVALID or ineligible
+  // (its parameters say so): no list is read then
+  if (!(h0 >= 0 && h1 >= h0 && h1 - h0 < (1 << kSwCountBits))) h1 = h0;
+  if (!(b0 >= 0 && b1 >= b0 && b1 - b0 < (1 << (32 - kSwCountBits)) - 1)) b1 = b0;
+  int ids[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int j = h0 + u * kSwThreads + (int)threadIdx.x;
+    ids[u] = j < h1 ? __ldg(a.hist_ids + j) : c0 - 1;
+  }
+  int bid = c0 - 1;
+  float bval = 0.0f;
+  if (b0 + (int)threadIdx.x < b1) {
+    bid = __ldg(a.bias_ids + b0 + threadIdx.x);
+    bval = __ldg(a.bias_vals + b0 + threadIdx.x);
+  }
   if (lists) {
     uint4* t4 = reinterpret_cast<uint4*>(X.tab);
     for (int i = threadIdx.x; i < kSwSlice / 4; i += kSwThreads) t4[i] = make_uint4(0u, 0u, 0u, 0u);
     if (threadIdx.x < kSwSlice / 32) X.listed[threadIdx.x] = 0u;
   }
   __syncthreads();
-  // 2. this slice's part of the row's lists
+  // 2. this slice's part of the row's lists: history counts, and the last valid bias entry
+  //    of each id (the largest entry index, kept in the high bits by a compare-and-swap
+  //    whatever the order; the count in the low bits may change underneath: it retries)
   if (lists && !(X.flags & kSwIneligible)) {
     unsigned bad = 0;
-    // eight ids in flight per thread: one memory round trip per 2048 ids
-    for (int j0 = q.hlo; j0 < q.hhi; j0 += 8 * kSwThreads) {
-      int ids[8];
+    auto hist = [&](int id, int j) {
+      if (j < h1 && (id < 0 || id >= a.V)) bad = 1;
+      const int l = id - c0;
+      if ((unsigned)l < (unsigned)n) {
+        atomicAdd(&X.tab[l], 1u);
+        atomicOr(&X.listed[l >> 5], 1u << (l & 31));
+      }
+    };
+#pragma unroll
+    for (int u = 0; u < 8; ++u) hist(ids[u], h0 + u * kSwThreads + (int)threadIdx.x);
+    // longer histories: eight more ids in flight per thread each round
+    for (int j0 = h0 + 8 * kSwThreads; j0 < h1; j0 += 8 * kSwThreads) {
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int j = j0 + u * kSwThreads + (int)threadIdx.x;
-        ids[u] = j < q.hhi ? __ldg(a.hist_ids + j) : c0 - 1;
+        ids[u] = j < h1 ? __ldg(a.hist_ids + j) : c0 - 1;
       }
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int id = ids[u];
-        const int j = j0 + u * kSwThreads + (int)threadIdx.x;
-        if (j < q.hhi && (id < 0 || id >= a.V)) bad = 1;
-        const int l = id - c0;
-        if ((unsigned)l < (unsigned)n) {
-          atomicAdd(&X.tab[l], 1u);
-          atomicOr(&X.listed[l >> 5], 1u << (l & 31));
-        }
-      }
+      for (int u = 0; u < 8; ++u) hist(ids[u], j0 + u * kSwThreads + (int)threadIdx.x);
     }
-    if (bad) X.flags = kFlagInvalid;  // benign race: every writer stores the same value
+    for (int j = b0 + (int)threadIdx.x; j < b1; j += kSwThreads) {
+      if (j != b0 + (int)threadIdx.x) {
+        bid = __ldg(a.bias_ids + j);
+        bval = __ldg(a.bias_vals + j);
+      }
+      if (bid < 0 || bid >= a.V || bval != bval) {
+        bad = 1;
+        continue;
+      }
+      const int l = bid - c0;
+      if ((unsigned)l >= (unsigned)n) continue;
+      const unsigned e = (unsigned)(j - b0 + 1);
+      unsigned old = X.tab[l];
+      while ((old >> kSwCountBits) < e) {
+        const unsigned seen = atomicCAS(&X.tab[l], old, (old & ((1u << kSwCountBits) - 1u)) | (e << kSwCountBits));
+        if (seen == old) break;
+        old = seen;
+      }
+      atomicOr(&X.listed[l >> 5], 1u << (l & 31));
+    }
+    if (bad) atomicOr(&X.flags, kFlagInvalid);
     __syncthreads();
-    // bias entries by one warp in entry order: the last valid entry of an id wins (within
-    // a group of 32, the highest lane of the id)
-    if (wp == 0) {
-      for (int j0 = q.blo; j0 < q.bhi; j0 += 32) {
-        const int j = j0 + lane;
-        int l = -1 - lane;
-        if (j < q.bhi) {
-          const int id = __ldg(a.bias_ids + j);
-          const float bv = __ldg(a.bias_vals + j);
-          if (id < 0 || id >= a.V || bv != bv) X.flags = kFlagInvalid;
-          else if ((unsigned)(id - c0) < (unsigned)n) l = id - c0;
-        }
-        const unsigned same = __match_any_sync(~0u, l);
-        if (l >= 0 && (31 - __clz(same)) == lane) {
-          X.tab[l] = (X.tab[l] & ((1u << kSwCountBits) - 1u)) | ((unsigned)(j - q.blo + 1) << kSwCountBits);
-          atomicOr(&X.listed[l >> 5], 1u << (l & 31));  // lanes of one word at once
-        }
-        __syncwarp();
+    // each listed token's transformed value, computed once from its raw logit (an L2 hit:
+    // the slice was just loaded) and left in its table entry as float bits
+    for (int wi = threadIdx.x; wi < kSwSlice / 32; wi += kSwThreads) {
+      uint32_t bits = X.listed[wi];
+      while (bits) {
+        const int l = wi * 32 + __ffs(bits) - 1;
+        bits &= bits - 1u;
+        float z;
+        if (kBF16) z = __uint_as_float((uint32_t)__ldg(static_cast<const uint16_t*>(a.logits) + off + l) << 16);
+        else z = __ldg(static_cast<const float*>(a.logits) + off + l);
+        X.tab[l] = __float_as_uint(sweep_transform(a, q, z, X.tab[l]));
       }
     }
     __syncthreads();
@@ -229,7 +271,7 @@ __global__ void __launch_bounds__(kSwThreads, 3) sweep_kernel(const __grid_const
     if (lst) {
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        if ((lst >> j) & 1u) vset(v[u], j, sweep_transform(a, q, vget(v[u], j), X.tab[t + j]));
+        if ((lst >> j) & 1u) vset(v[u], j, __uint_as_float(X.tab[t + j]));
     }
     if (allow != 0xFu) {
       if (!(allow & 1u)) v[u].x = -INFINITY;

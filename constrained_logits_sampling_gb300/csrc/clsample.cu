@@ -110,7 +110,7 @@ struct SliceRec {
 struct RowCtl {
   unsigned ticket;  // slices that finished their last phase
   unsigned bar;     // heavy rows: arrivals at the row barriers
-  int spill;        // spill slot of the row (-1: none)
+  int spill;        // spill slot of the row + 1 (0: none; see row_spill_slot)
   unsigned pad;
 };
 
@@ -840,7 +840,7 @@ __global__ void __launch_bounds__(kOrderThreads) order_kernel(const __grid_const
       RowCtl rc;
       rc.ticket = 0;
       rc.bar = 0;
-      rc.spill = -1;
+      rc.spill = 0;
       rc.pad = 0;
       P.rowctl[r] = rc;
     }
@@ -1260,23 +1260,24 @@ __device__ __forceinline__ void pass_a(const LaunchParams& P, const Smem& S, con
 
 // ---------------------------------------------------------------- candidates of light rows
 
-// The row's spill slot, taken once per row by the first slice that needs one (the cell
-// goes -1 -> -2 while that slice draws a slot, then to the slot or -3 if none was left);
-// -1 if the row has none.
+// The row's spill slot, taken once per row by the first slice that needs one.  The cell
+// holds 0 (none yet: its state after a finished row and after allocation), -1 while that
+// slice draws a slot, then slot + 1, or -2 if none was left.  Returns the slot, or -1 if
+// the row has none.
 __device__ int row_spill_slot(const LaunchParams& P, int row) {
   int* cell = &P.rowctl[row].spill;
-  int cur = atomicCAS(cell, -1, -2);
-  if (cur == -1) {
+  int cur = atomicCAS(cell, 0, -1);
+  if (cur == 0) {
     const unsigned slot = atomicAdd(&P.ctl[1], 1u);
-    const int v = slot < (unsigned)P.spill_rows ? (int)slot : -3;
+    const int v = slot < (unsigned)P.spill_rows ? (int)slot + 1 : -2;
     atomicExch(cell, v);
-    return v >= 0 ? v : -1;
+    return v > 0 ? v - 1 : -1;
   }
-  for (uint32_t i = 0; i < kWaitPolls && cur == -2; ++i) {
+  for (uint32_t i = 0; i < kWaitPolls && cur == -1; ++i) {
     __nanosleep(64);
     cur = (int)ld_acquire(reinterpret_cast<const unsigned*>(cell));
   }
-  return cur >= 0 ? cur : -1;
+  return cur > 0 ? cur - 1 : -1;
 }
 
 __device__ __forceinline__ Item* spill_area(const LaunchParams& P, int slot, int slice) {
@@ -2184,7 +2185,8 @@ __device__ void finish_row(const LaunchParams& P, const Smem& S, const RowParams
   bool sorted = false;
   for (int attempt = 0;; ++attempt) {
     if (threadIdx.x == 0) {
-      const int spill = atomicAdd(&P.rowctl[row].spill, 0);
+      const int sc = atomicAdd(&P.rowctl[row].spill, 0);
+      const int spill = sc > 0 ? sc - 1 : -1;
       int ns = 0;
       for (int s = 0; s < C; ++s) {
         const SliceRec& x = sh.recs[s];
@@ -2831,10 +2833,15 @@ __global__ void __launch_bounds__(kThreads, 3) sampler_kernel(const __grid_const
     combine_row(P, row, q);
     if (heavy) heavy_above(ab, C);
     finish_row<kBF16>(P, S, q, row, ab, heavy);
-    // the last row to finish clears the preparation flags for the next call: by then
-    // every CTA of the grid has taken its item and read the flags
+    // the row's control words go back to their initial state (every CTA of the row is past
+    // its ticket), so a sampler grid that runs without its preparation launch still finds
+    // them clean; the last row to finish clears the preparation flags for the next call:
+    // by then every CTA of the grid has taken its item and read the flags
     __syncthreads();
-    if (threadIdx.x == 0) sh.flag = atomicAdd(&P.ctl[3], 1u) == (unsigned)(P.a.B - 1);
+    if (threadIdx.x == 0) {
+      P.rowctl[row] = RowCtl{0u, 0u, 0, 0u};
+      sh.flag = atomicAdd(&P.ctl[3], 1u) == (unsigned)(P.a.B - 1);
+    }
     __syncthreads();
   }
   if (sh.flag) {

@@ -232,8 +232,8 @@ int clsample_apply(clsample_t* handle, const clsample_args_t* args, clsample_str
  * clsample_prepare enqueues the preparation launch, clsample_sample the sampler kernel,
  * which consumes what the last clsample_prepare on this handle wrote (each
  * clsample_sample needs its own clsample_prepare before it: the sampler clears the
- * preparation's flags when it ends; a sample without one waits about a second and
- * reports every row OVERFLOW; a preparation that no sample consumes is harmless, the
+ * preparation's flags when it ends; a sample without one waits a few seconds at most
+ * and reports every row OVERFLOW, touching no row past B; a preparation that no sample consumes is harmless, the
  * next one clears its flags first).  The pair, with the same arguments on one stream,
  * equals clsample_apply.  Same validation and return codes. */
 int clsample_prepare(clsample_t* handle, const clsample_args_t* args, clsample_stream_t stream);

@@ -524,3 +524,30 @@ def test_top_n_logprobs_parity(w, B, V):
         g, o = run_gpu(b), run_oracle(b)
         compare(b, g, o, f"top-n short w{w}")
         assert list(g["top_ids"][r, :3]) in ([0, 2, -1], [2, 0, -1])
+
+
+def test_sample_without_its_preparation_reports_overflow():
+    """clsample_sample without its clsample_prepare, after a larger call on the handle:
+    the sampler's bounded wait for the row order gives up (about a second), every row of
+    the call reports OVERFLOW, nothing past row B is touched, and the next full call is
+    exact again."""
+    from constrained_logits_sampling_gb300.sampler import Sampler, batch_to_device
+    s = Sampler(64, 32000)
+    big = make_workload(1, B=64)
+    kw = batch_to_device(big, s.device)
+    s(kw.pop("logits"), **kw)
+    torch.cuda.synchronize()
+    b = make_workload(1, B=4)
+    kw = batch_to_device(b, s.device)
+    logits = kw.pop("logits")
+    dev = s.device
+    out = {"tokens": torch.full((8,), 12345, dtype=torch.int32, device=dev),
+           "logprobs": torch.empty(8, dtype=torch.float32, device=dev),
+           "status": torch.full((8,), 7, dtype=torch.int32, device=dev)}
+    args = s.make_args(logits, tokens=out["tokens"][:4], logprobs=out["logprobs"][:4], row_status=out["status"][:4],
+                       **kw)
+    s.sample(args)
+    torch.cuda.synchronize()
+    assert out["status"][:4].tolist() == [1, 1, 1, 1]
+    assert out["status"][4:].tolist() == [7, 7, 7, 7] and out["tokens"][4:].tolist() == [12345] * 4
+    compare(b, run_gpu(b, sampler=s), run_oracle(b), name="after a sample without preparation")

@@ -64,3 +64,51 @@ def test_static_rejects_oversize(lib):
     with pytest.raises(lib.ClsampleError) as e:
         lib.apply_static(args)
     assert e.value.code == -3  # CLSAMPLE_ERR_VOCAB
+
+
+def _static_vs_handle(lib, b):
+    s = lib.Sampler(b.B, b.V)
+    kw = lib.batch_to_device(b, "cuda")
+    logits = kw.pop("logits")
+    ref = s(logits, **kw)
+    out = _outputs(b.B)
+    args = s.make_args(logits, tokens=out["tokens"], logprobs=out["logprobs"], row_status=out["status"], **kw)
+    lib.apply_static(args)
+    torch.cuda.synchronize()
+    return out, ref
+
+
+def test_static_calls_of_different_sizes_in_a_row(lib):
+    """Calls of different V (slice count and length) and B one after another on the one
+    array: each uses a prefix of it laid out for the longest slices, and whatever a call
+    leaves there is read back by the next.  Each call equals its own handle bit for bit."""
+    for n, B, V in ((4, 48, None), (4, 8, 5003), (2, 64, None), (5, 16, 40001), (4, 48, None)):
+        b = make_workload(n, B=B, V=V)
+        out, ref = _static_vs_handle(lib, b)
+        for key in ("tokens", "status"):
+            assert torch.equal(out[key], ref[key]), (n, B, V, key)
+        assert np.array_equal(out["logprobs"].cpu().numpy().view(np.uint32),
+                              ref["logprobs"].cpu().numpy().view(np.uint32)), (n, B, V)
+
+
+def test_static_spill_rows_are_four(lib):
+    """Flat rows under top-k spill every slice; the static array holds 4 spill rows (the
+    header states it), a handle one per batch row.  With 8 such rows the static call
+    samples 4 of them exactly like the handle and reports the other 4 OVERFLOW; every
+    other row matches."""
+    V = 151936
+    B = 12
+    rng = np.random.default_rng(41)
+    z = (rng.standard_normal((B, V)) * 3).astype(np.float32)
+    z[:8] = 0.0
+    from constrained_logits_sampling_gb300.workloads import Batch
+    b = Batch(B=B, V=V, logits=z, logits_bf16=False)
+    b.temperatures = np.ones(B, np.float32)
+    b.top_ks = np.full(B, 50, np.int32)
+    b.positions = np.arange(B, dtype=np.int64)
+    out, ref = _static_vs_handle(lib, b)
+    st, rs = out["status"].cpu().numpy(), ref["status"].cpu().numpy()
+    assert np.all(rs == 0)
+    assert np.all(st[8:] == 0) and (st[:8] == 1).sum() == 4 and (st[:8] == 0).sum() == 4
+    ok = st == 0
+    assert np.array_equal(out["tokens"].cpu().numpy()[ok], ref["tokens"].cpu().numpy()[ok])

@@ -111,9 +111,10 @@ def traffic_from_profile(workload_name):
             d = json.load(f)
     except Exception:
         return None
-    if d.get("kernel_source_sha") != kernel_source_hash() or d.get("workload") != workload_name:
-        return None
-    return d.get("dram_bytes_per_launch")
+    for c in d.get("captures", [d]):
+        if c.get("kernel_source_sha") == kernel_source_hash() and c.get("workload") == workload_name:
+            return c.get("dram_bytes_per_launch")
+    return None
 
 
 class ClockSampler:

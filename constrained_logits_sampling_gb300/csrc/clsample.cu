@@ -1841,7 +1841,6 @@ __device__ void sort_items(const Smem& S, int chunk, int n) {
   sort_desc(k, n);
 }
 
-__device__ __forceinline__ float sorted_y(unsigned long long v) { return key_to_float((uint32_t)(v >> 32)); }
 __device__ __forceinline__ int sorted_id(unsigned long long v) { return (int)~(uint32_t)v; }
 
 // Finishes a row whose n <= kSortCap items are in shared memory: sort, then the top-k,

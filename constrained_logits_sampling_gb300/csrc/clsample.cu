@@ -1338,17 +1338,24 @@ __device__ int compact(const Smem& S, int c0, int n, float zc, Item* dst, int ca
     const bool hit = active && vm > -INFINITY && vm >= zc;
     if (!__any_sync(~0u, hit)) continue;
     const float e[4] = {v.x, v.y, v.z, v.w};
+    // the four ballots first, then one shared-memory atomic for the warp's whole step
+    unsigned bal[4];
+    int tot = 0;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const bool pr = hit && e[j] > -INFINITY && e[j] >= zc;
-      const unsigned bal = __ballot_sync(~0u, pr);
-      if (bal) {
-        int base = 0;
-        if (lane == 0) base = atomicAdd(&sh.cnt, __popc(bal));
-        base = __shfl_sync(~0u, base, 0);
-        const int pos = base + __popc(bal & lt);
-        if (pr && pos < cap) dst[pos] = Item{e[j], c0 + 4 * f + j};
+      bal[j] = __ballot_sync(~0u, hit && e[j] > -INFINITY && e[j] >= zc);
+      tot += __popc(bal[j]);
+    }
+    int base = 0;
+    if (lane == 0) base = atomicAdd(&sh.cnt, tot);
+    base = __shfl_sync(~0u, base, 0);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if ((bal[j] >> lane) & 1u) {
+        const int pos = base + __popc(bal[j] & lt);
+        if (pos < cap) dst[pos] = Item{e[j], c0 + 4 * f + j};
       }
+      base += __popc(bal[j]);
     }
   }
   __syncthreads();

@@ -1304,17 +1304,24 @@ __device__ int compact_if(const Smem& S, int c0, int n, Pred&& keep, Item* dst, 
     const int f = f0 + threadIdx.x;
     const float4 v = f < nv ? b4[f] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
     const float e[4] = {v.x, v.y, v.z, v.w};
+    unsigned bal[4];
+    int tot = 0;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const bool pr = active && e[j] > -INFINITY && keep(e[j]);
-      const unsigned bal = __ballot_sync(~0u, pr);
-      if (bal) {
-        int base = 0;
-        if (lane == 0) base = atomicAdd(&sh.cnt, __popc(bal));
-        base = __shfl_sync(~0u, base, 0);
-        const int pos = base + __popc(bal & lt);
-        if (pr && pos < cap) dst[pos] = Item{e[j], c0 + 4 * f + j};
+      bal[j] = __ballot_sync(~0u, active && e[j] > -INFINITY && keep(e[j]));
+      tot += __popc(bal[j]);
+    }
+    if (!tot) continue;
+    int base = 0;
+    if (lane == 0) base = atomicAdd(&sh.cnt, tot);
+    base = __shfl_sync(~0u, base, 0);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if ((bal[j] >> lane) & 1u) {
+        const int pos = base + __popc(bal[j] & lt);
+        if (pos < cap) dst[pos] = Item{e[j], c0 + 4 * f + j};
       }
+      base += __popc(bal[j]);
     }
   }
   __syncthreads();
@@ -1619,16 +1626,25 @@ __device__ void gather_items(const Smem& S, int chunk, float m, float invT) {
         x[j] = ldcg_item(sh.seg[s] + i);
       }
     }
+    // the eight ballots first, then one shared-memory atomic for the warp's step
+    unsigned bal[8];
+    int tot = 0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const bool pr = x[j].z > -INFINITY && x[j].z >= zmin;
-      const unsigned bal = __ballot_sync(~0u, pr);
-      if (!bal) continue;
-      int base = 0;
-      if (lane == 0) base = atomicAdd(&sh.cnt, __popc(bal));
-      base = __shfl_sync(~0u, base, 0);
-      const int pos = base + __popc(bal & ((1u << lane) - 1u));
-      if (pr && pos < cap) it[pos] = Item{y_of(x[j].z, m, invT), x[j].id};
+      bal[j] = __ballot_sync(~0u, x[j].z > -INFINITY && x[j].z >= zmin);
+      tot += __popc(bal[j]);
+    }
+    if (!tot) continue;
+    int base = 0;
+    if (lane == 0) base = atomicAdd(&sh.cnt, tot);
+    base = __shfl_sync(~0u, base, 0);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if ((bal[j] >> lane) & 1u) {
+        const int pos = base + __popc(bal[j] & ((1u << lane) - 1u));
+        if (pos < cap) it[pos] = Item{y_of(x[j].z, m, invT), x[j].id};
+      }
+      base += __popc(bal[j]);
     }
   }
   __syncthreads();
@@ -2547,17 +2563,25 @@ __device__ void heavy_slice(const LaunchParams& P, const Smem& S, const RowParam
           }
         }
       }
-      if (band) {
+      if (band && __any_sync(~0u, bm != 0u)) {
+        // the four ballots first, then one shared-memory atomic for the warp's step
+        unsigned bal[4];
+        int tot = 0;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const bool pr = (bm >> j) & 1u;
-          const unsigned bal = __ballot_sync(~0u, pr);
-          if (!bal) continue;
-          int base = 0;
-          if (lane == 0) base = atomicAdd(&sh.cnt, __popc(bal));
-          base = __shfl_sync(~0u, base, 0);
-          const int pos = base + __popc(bal & ((1u << lane) - 1u));
-          if (pr && pos < kCandCap) cdst[pos] = Item{zz[j], id0 + j};
+          bal[j] = __ballot_sync(~0u, (bm >> j) & 1u);
+          tot += __popc(bal[j]);
+        }
+        int base = 0;
+        if (lane == 0) base = atomicAdd(&sh.cnt, tot);
+        base = __shfl_sync(~0u, base, 0);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if ((bal[j] >> lane) & 1u) {
+            const int pos = base + __popc(bal[j] & ((1u << lane) - 1u));
+            if (pos < kCandCap) cdst[pos] = Item{zz[j], id0 + j};
+          }
+          base += __popc(bal[j]);
         }
       }
     }

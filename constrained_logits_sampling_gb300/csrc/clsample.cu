@@ -1406,17 +1406,30 @@ __device__ void light_candidates(const LaunchParams& P, const Smem& S, const Row
       const uint32_t mine = S.hist[threadIdx.x];  // this thread's maximum (order key)
       uint32_t key = mine;
       const int lane = threadIdx.x & 31;
-#pragma unroll
-      for (int size = 2; size <= 32; size <<= 1)
-#pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-          const uint32_t o = __shfl_xor_sync(~0u, key, stride);
-          const bool keep_max = ((lane & stride) == 0) == ((lane & size) == 0);
-          key = keep_max ? max(key, o) : min(key, o);
-        }
       int qj = min(31, (need + kWarps - 1) / kWarps - 1);
+      // qj <= 1 (small k): the warp's two largest by a pair reduction; else a full sort
+      uint32_t t1 = mine, t2 = 0u;
+      const bool small = qj <= 1;
+      if (small) {
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+          const uint32_t a1 = __shfl_xor_sync(~0u, t1, o), a2 = __shfl_xor_sync(~0u, t2, o);
+          const uint32_t hi = max(t1, a1);
+          t2 = max(min(t1, a1), max(t2, a2));
+          t1 = hi;
+        }
+      } else {
+#pragma unroll
+        for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+          for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const uint32_t o = __shfl_xor_sync(~0u, key, stride);
+            const bool keep_max = ((lane & stride) == 0) == ((lane & size) == 0);
+            key = keep_max ? max(key, o) : min(key, o);
+          }
+      }
       for (int tries = 0; tries < 3; ++tries) {
-        const uint32_t thr = block_min_u32(__shfl_sync(~0u, key, qj));
+        const uint32_t thr = block_min_u32(small ? (qj == 0 ? t1 : t2) : __shfl_sync(~0u, key, qj));
         if (thr == 0u) break;  // a warp has fewer live threads: take every allowed token
         const float edge = key_to_float(thr);
         const int c = compact(S, c0, n, edge, cand_area(P, row, slice), kCandCap, mine >= thr);
@@ -1813,6 +1826,22 @@ constexpr int kSortCap = 2048;  // items the sorted finisher takes (its masses f
 // composites (order key << 32 | ~id), bitonic, padded to a power of two with zeros.
 __device__ void sort_items(const Smem& S, int chunk, int n) {
   unsigned long long* k = reinterpret_cast<unsigned long long*>(fin_items(S));
+  if (n <= kThreads) {
+    // rank sort with one item per thread
+    unsigned long long mine = 0ull;
+    if ((int)threadIdx.x < n) {
+      const Item it = fin_items(S)[threadIdx.x];
+      mine = ((unsigned long long)fkey(it.z) << 32) | (uint32_t)(~(uint32_t)it.id);
+    }
+    unsigned long long* tmp = reinterpret_cast<unsigned long long*>(fin_hc(S, chunk));
+    if ((int)threadIdx.x < n) tmp[threadIdx.x] = mine;
+    __syncthreads();
+    int rank = 0;
+    for (int j = 0; j < n; ++j) rank += tmp[j] > mine;
+    if ((int)threadIdx.x < n) k[rank] = mine;
+    __syncthreads();
+    return;
+  }
   if (n <= 2 * kThreads) {
     // rank sort: the composites are distinct, so each one's position is the number of
     // larger ones (every thread counts against all n, reading broadcast words)

@@ -1105,10 +1105,11 @@ __device__ void pass_a_t(const LaunchParams& P, const Smem& S, const RowParams& 
   const uint32_t* mw = P.a.bitmask ? S.mask : nullptr;
   const uint32_t tail = (n & 3) ? ((1u << (n & 3)) - 1u) : 0xFu;
   float4* b4 = reinterpret_cast<float4*>(S.buf);
-  if (threadIdx.x == 0 && (n & 3)) {
-    for (int j = n; j < 4 * nv; ++j) S.buf[j] = 0.0f;  // pads: finite, masked below
+  if (n & 3) {
+    if (threadIdx.x == 0)
+      for (int j = n; j < 4 * nv; ++j) S.buf[j] = 0.0f;  // pads: finite, masked below
+    __syncthreads();
   }
-  __syncthreads();
   // one walk: max, first vector reaching it, and the sum of 2^((z' - tmax) c) against a
   // running per-thread max (rescaled when it grows)
   const float c = __fmul_rn(1.4426950408889634f, q.invT);
@@ -1394,6 +1395,7 @@ __device__ void light_candidates(const LaunchParams& P, const Smem& S, const Row
                                  int c0, int n) {
   const float M = sh.rec.m;
   float zc = -INFINITY, dz = 0.0f;
+  int tnc = -1;  // top-k: candidates compacted while the bound was chosen (-1: none yet)
   if (M > -INFINITY && q.route == kRouteTopK) {
     const int nal = sh.rec.nallowed;
     const float share = P.a.bitmask ? (float)nal / (float)max(1, sh.nal_row) : (float)n / (float)P.a.V;
@@ -1445,8 +1447,7 @@ __device__ void light_candidates(const LaunchParams& P, const Smem& S, const Row
         qj >>= 1;
       }
     }
-    if (threadIdx.x == 0) sh.flag = nc;
-    __syncthreads();
+    tnc = nc;  // uniform: every thread saw the same counts
   } else if (M > -INFINITY && q.route == kRouteMinP) {
     const float edge = M + q.L * q.Teff;
     dz = bound_margin(M, edge);
@@ -1454,7 +1455,7 @@ __device__ void light_candidates(const LaunchParams& P, const Smem& S, const Row
   }
   int nc = 0;
   if (M > -INFINITY) {
-    if (q.route == kRouteTopK && sh.flag >= 0) nc = sh.flag;  // compacted while the bound was chosen
+    if (tnc >= 0) nc = tnc;  // compacted while the bound was chosen
     else nc = compact(S, c0, n, zc, cand_area(P, row, slice), kCandCap, !(zc > -INFINITY) || S.hist[threadIdx.x] >= fkey(zc));
     if (nc > kCandCap) {
       nc = spill_slice(P, S, row, slice, c0, n);
@@ -1465,12 +1466,11 @@ __device__ void light_candidates(const LaunchParams& P, const Smem& S, const Row
       }
     }
   }
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0) {  // the caller's barrier publishes the record
     sh.rec.ncand = nc;
     sh.rec.zc = zc;
     sh.rec.dz = dz;
   }
-  __syncthreads();
 }
 
 // ---------------------------------------------------------------- row end: records
@@ -2749,7 +2749,7 @@ __device__ void slice_front(const LaunchParams& P, const Smem& S, const RowParam
     for (int u = 0; u < 2; ++u)
       if (mine[u].lid >= 0) atomicOr(&S.claim[mine[u].lid >> 5], 1u << (mine[u].lid & 31));
     if (!slice_wait(bulk) && threadIdx.x == 0) sh.rec.flags |= kFlagOverflow;
-    __syncthreads();
+    if (!bulk) __syncthreads();  // a slice of plain loads only (slice_wait did not sync)
     if (kBF16) widen_bf16(S, P.chunk, n);
     for (int i0 = 0; i0 < ne; i0 += 2 * kThreads) {
 #pragma unroll
@@ -2783,7 +2783,7 @@ __device__ void slice_front(const LaunchParams& P, const Smem& S, const RowParam
     for (int w = threadIdx.x; w < ((n + 31) >> 5); w += kThreads) S.mask[w] = (uint32_t)__ldg(mrow + w);
   }
   if (!slice_wait(bulk) && threadIdx.x == 0) sh.rec.flags |= kFlagOverflow;
-  __syncthreads();
+  if (!bulk) __syncthreads();  // a slice of plain loads only (slice_wait did not sync)
   if (kBF16) widen_bf16(S, P.chunk, n);
   for (int r0 = 0; r0 < ntouch; r0 += kPen) {
     if (r0 > 0) transforms_prep(P, S, q, c0, n, r0);

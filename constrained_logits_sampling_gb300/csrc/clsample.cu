@@ -1821,6 +1821,7 @@ __device__ float block_sum_f2(float v) {
 // ---------------------------------------------------------------- row end: sorted finisher
 
 constexpr int kSortCap = 2048;  // items the sorted finisher takes (its masses fit the histogram area)
+constexpr int kHeavySortMax = 1024;  // heavy rows without a top-k cut sort at most this many band items
 
 // Sorts the n <= kSortCap smem items in place by (y descending, id ascending) as 64-bit
 // composites (order key << 32 | ~id), bitonic, padded to a power of two with zeros.
@@ -2300,7 +2301,10 @@ __device__ void finish_row(const LaunchParams& P, const Smem& S, const RowParams
     const int krem = kc - (int)ab.n;
     if (krem >= 1 && krem <= sh.fin_n && prefilter_kth(S, P.chunk, m, invT, krem)) sorted = true;
   }
-  if (sh.fin_smem && sh.fin_n <= kSortCap) {
+  // a heavy row without a top-k cut and many band items: its cut by radix mass selects
+  // costs less than sorting them
+  const bool by_digits = heavy && kc == 0 && !sorted && sh.fin_n > kHeavySortMax;
+  if (sh.fin_smem && sh.fin_n <= kSortCap && !by_digits) {
     finish_sorted(P, S, q, row, ab, heavy, status, R, lnS, sorted);
     return;
   }

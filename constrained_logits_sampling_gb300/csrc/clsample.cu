@@ -603,13 +603,15 @@ __device__ void decode_params(const clsample_args_t& a, const RawRow& w, RowPara
 __device__ void load_params(const clsample_args_t& a, int row, RowParams& q) { decode_params(a, load_raw(a, row), q); }
 
 // List order of a row: heavy rows first (their CTAs wait for each other and work longest),
-// then top-k rows with a large k (their row ends take longest), other rows that finish
-// from candidates, greedy and invalid rows last (the cheapest).
-constexpr int kClasses = 4;
+// then top-k rows with a large k (their row ends take longest), top-k rows with a top-p
+// cut, other rows that finish from candidates, greedy and invalid rows last (the
+// cheapest).
+constexpr int kClasses = 5;
 __device__ __forceinline__ int route_rank(const RowParams& q) {
   if (q.route == kRouteHeavy) return 0;
   if (q.route == kRouteTopK && q.k > 128) return 1;
-  return q.route == kRouteGreedy ? 3 : 2;
+  if (q.route == kRouteTopK && q.p < 1.0f) return 2;  // a top-p cut lengthens the row end
+  return q.route == kRouteGreedy ? 4 : 3;
 }
 
 // ---------------------------------------------------------------- ordering kernel
@@ -828,7 +830,7 @@ __global__ void __launch_bounds__(kOrderThreads) order_kernel(const __grid_const
   // (the item counter, spill counter and done counter were reset by the previous sampler
   // grid's last CTA, or are zero from the allocation)
   // totals per class first, so each class knows where it starts
-  int tot[kClasses] = {0, 0, 0, 0};
+  int tot[kClasses] = {0, 0, 0, 0, 0};
   for (int r0 = 0; r0 < B; r0 += kOrderThreads) {
     const int r = r0 + threadIdx.x;
     int c = -1;
@@ -846,7 +848,9 @@ __global__ void __launch_bounds__(kOrderThreads) order_kernel(const __grid_const
     }
     for (int j = 0; j < kClasses; ++j) tot[j] += __syncthreads_count(c == j);
   }
-  int start[kClasses] = {0, tot[0], tot[0] + tot[1], tot[0] + tot[1] + tot[2]};
+  int start[kClasses];
+  start[0] = 0;
+  for (int j = 1; j < kClasses; ++j) start[j] = start[j - 1] + tot[j - 1];
   for (int r0 = 0; r0 < B; r0 += kOrderThreads) {
     const int r = r0 + threadIdx.x;
     int c = -1;
